@@ -1,0 +1,196 @@
+"""ctypes binding of libattn.so: argument marshalling only.
+
+Every computation happens inside the CUDA library.  PyTorch is used here to
+hand over device pointers and streams, and to allocate outputs when the caller
+does not pass them.  A missing library raises; there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+from . import build as _build
+
+ATTN_F16 = 0
+ATTN_BF16 = 1
+
+STATUS_NAMES = {
+    0: "ATTN_OK", 1: "ATTN_ERR_NULL", 2: "ATTN_ERR_ALIGN", 3: "ATTN_ERR_SHAPE",
+    4: "ATTN_ERR_HEADS", 5: "ATTN_ERR_HEADDIM", 6: "ATTN_ERR_DTYPE", 7: "ATTN_ERR_SCALE",
+    8: "ATTN_ERR_ARCH", 9: "ATTN_ERR_CUDA", 10: "ATTN_ERR_TIMEOUT", 11: "ATTN_ERR_VALID_LEN",
+    12: "ATTN_ERR_ARG",
+}
+ATTN_OK = 0
+
+
+class AttnError(RuntimeError):
+    """A non-zero attn_status_t returned by the library."""
+
+    def __init__(self, status: int, where: str):
+        self.status = int(status)
+        name = STATUS_NAMES.get(self.status, "status %d" % self.status)
+        msg = "%s: %s (%s)" % (where, name, strerror(self.status))
+        if self.status == 9:
+            msg += " [cudaError %d]" % last_cuda_error()
+        super().__init__(msg)
+
+
+class Caps(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in (
+        "supported", "block_m", "q_tiles_per_cta", "block_n", "kv_stages", "threads",
+        "smem_bytes", "tmem_cols", "num_sms", "lse_natural_log")]
+
+    def as_dict(self):
+        return {n: getattr(self, n) for n, _ in self._fields_}
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib_path() -> str:
+    return _build.LIB_PATH
+
+
+def load():
+    """Load libattn.so (built in-tree by ``build.build_library``).  Raises when absent."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.LIB_PATH
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    "libattn.so is not built (%s); build it with "
+                    "attention_forward_attn_gb300.build.build_library()" % path)
+            lib = ctypes.CDLL(path)
+            p = ctypes.c_void_p
+            i = ctypes.c_int
+            fwd_args = [p, p, p, p, p, i, i, i, i, i, ctypes.c_float, i, p, i, p]
+            for name in ("attn_fwd", "attn_fwd_simt"):
+                fn = getattr(lib, name)
+                fn.argtypes = fwd_args
+                fn.restype = i
+            lib.attn_status.argtypes = [p, ctypes.POINTER(ctypes.c_int)]
+            lib.attn_status.restype = i
+            lib.attn_query.argtypes = [i, i, ctypes.POINTER(Caps)]
+            lib.attn_query.restype = i
+            lib.attn_strerror.argtypes = [i]
+            lib.attn_strerror.restype = ctypes.c_char_p
+            lib.attn_last_cuda_error.argtypes = []
+            lib.attn_last_cuda_error.restype = i
+            lib.attn_shutdown.argtypes = []
+            lib.attn_shutdown.restype = None
+            _lib = lib
+    return _lib
+
+
+def declared_symbols():
+    """Function names declared in include/attn.h."""
+    hdr = os.path.join(_build.INCLUDE, "attn.h")
+    text = open(hdr).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(attn_[a-z0-9_]+)\s*\(", text)))
+
+
+def strerror(status: int) -> str:
+    return load().attn_strerror(int(status)).decode()
+
+
+def last_cuda_error() -> int:
+    return int(load().attn_last_cuda_error())
+
+
+# ------------------------------------------------------------------ raw C calls
+
+def fwd_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, Hq, Hkv, L, D, sm_scale, causal,
+            valid_len_ptr, dtype, stream, simt=False) -> int:
+    """Call attn_fwd (or attn_fwd_simt) with raw integer pointers; returns the status."""
+    fn = load().attn_fwd_simt if simt else load().attn_fwd
+    return int(fn(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, int(B), int(Hq), int(Hkv), int(L), int(D),
+                  float(sm_scale), int(causal), valid_len_ptr, int(dtype), stream))
+
+
+def status(stream=None):
+    """attn_status: synchronise the stream, read and clear the device word -> (status, code)."""
+    code = ctypes.c_int(0)
+    st = int(load().attn_status(_stream_handle(stream), ctypes.byref(code)))
+    return st, int(code.value)
+
+
+def query(D: int, dtype: int = ATTN_BF16) -> dict:
+    caps = Caps()
+    st = int(load().attn_query(int(D), int(dtype), ctypes.byref(caps)))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_query")
+    return caps.as_dict()
+
+
+def shutdown():
+    load().attn_shutdown()
+
+
+# ------------------------------------------------------------------ torch-facing call
+
+def _stream_handle(stream):
+    if stream is None:
+        import torch
+        if not torch.cuda.is_available():
+            return None
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, int):
+        return stream or None
+    return stream.cuda_stream or None
+
+
+def _dtype_code(t):
+    import torch
+    if t.dtype == torch.float16:
+        return ATTN_F16
+    if t.dtype == torch.bfloat16:
+        return ATTN_BF16
+    raise TypeError("q/k/v must be float16 or bfloat16, got %s" % t.dtype)
+
+
+def attn_fwd(q, k, v, *, causal=False, sm_scale=None, valid_len=None, out=None, lse=None,
+             return_lse=True, stream=None, simt=False):
+    """Fused attention forward on CUDA tensors.
+
+    q: [B, Hq, L, D]; k, v: [B, Hkv, L, D] (or [B, L, D] for MQA); fp16/bf16,
+    contiguous, on the current CUDA device.  valid_len: int32 CUDA tensor [B]
+    or None.  Returns (o, lse) with o like q and lse float32 [B*Hq, L]
+    (lse is None when return_lse is False).
+    """
+    import torch
+    if k.dim() == 3:
+        k = k.unsqueeze(1)
+    if v.dim() == 3:
+        v = v.unsqueeze(1)
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("%s must be a contiguous CUDA tensor" % name)
+    B, Hq, L, D = q.shape
+    Hkv = k.shape[1]
+    if k.shape != v.shape or k.shape[0] != B or k.shape[2] != L or k.shape[3] != D:
+        raise ValueError("k and v must be [B, Hkv, L, D] matching q")
+    if q.dtype != k.dtype or q.dtype != v.dtype:
+        raise TypeError("q, k and v must share one dtype")
+    if sm_scale is None:
+        sm_scale = 1.0 / float(D) ** 0.5
+    if out is None:
+        out = torch.empty_like(q)
+    if return_lse and lse is None:
+        lse = torch.empty((B * Hq, L), dtype=torch.float32, device=q.device)
+    vl_ptr = None
+    if valid_len is not None:
+        if valid_len.dtype != torch.int32 or not valid_len.is_cuda or valid_len.numel() != B:
+            raise ValueError("valid_len must be an int32 CUDA tensor of B elements")
+        vl_ptr = valid_len.data_ptr()
+    st = fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                 lse.data_ptr() if (return_lse and lse is not None) else None,
+                 B, Hq, Hkv, L, D, sm_scale, int(bool(causal)), vl_ptr, _dtype_code(q),
+                 _stream_handle(stream), simt=simt)
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fwd_simt" if simt else "attn_fwd")
+    return out, (lse if return_lse else None)

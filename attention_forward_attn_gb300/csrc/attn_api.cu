@@ -1,0 +1,284 @@
+// Host side of libattn.so: the C ABI declared in include/attn.h.
+//
+// Validates arguments (no device synchronisation), keeps one device status
+// word per GPU, encodes the TMA tensor maps of Q, K and V, and launches the
+// kernels on the caller's stream.  Nothing here allocates per call.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "../../include/attn.h"
+#include "attn_internal.h"
+
+namespace {
+
+using attn::Problem;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  bool probed = false;
+  bool arch_ok = false;
+  int num_sms = 0;
+  int* status = nullptr;  // one int of device memory
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+thread_local int g_last_cuda_error = 0;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+attn_status_t cuda_fail(cudaError_t e) {
+  g_last_cuda_error = static_cast<int>(e);
+  return ATTN_ERR_CUDA;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Argument checks that need no device.
+attn_status_t validate(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                       int Hq, int Hkv, int L, int D, float sm_scale, int causal,
+                       const int32_t* valid_len, attn_dtype_t dtype) {
+  if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_DTYPE;
+  if (q == nullptr || k == nullptr || v == nullptr || o == nullptr) return ATTN_ERR_NULL;
+  if (B < 1 || Hq < 1 || Hkv < 1 || L < 1) return ATTN_ERR_SHAPE;
+  if (D != 64 && D != 128) return ATTN_ERR_HEADDIM;
+  if (Hq % Hkv != 0) return ATTN_ERR_HEADS;
+  if (causal != 0 && causal != 1) return ATTN_ERR_ARG;
+  if (!(sm_scale >= 0.f) || isinf(sm_scale)) return ATTN_ERR_SCALE;
+  // every flat row index (b*Hq + h)*L + i fits in int32, and so does the unit count
+  if (static_cast<int64_t>(B) * Hq * L > INT32_MAX) return ATTN_ERR_SHAPE;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16))
+    return ATTN_ERR_ALIGN;
+  if ((lse != nullptr && !aligned(lse, 4)) || (valid_len != nullptr && !aligned(valid_len, 4)))
+    return ATTN_ERR_ALIGN;
+  return ATTN_OK;
+}
+
+// Per-device probe and status-word allocation (first call on a device only).
+attn_status_t device_state(int* dev_out, DeviceState** st_out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_ARCH;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState& st = g_dev[dev];
+  if (!st.probed) {
+    cudaDeviceProp prop;
+    e = cudaGetDeviceProperties(&prop, dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    st.arch_ok = (prop.major == 10 && prop.minor == 3);
+    st.num_sms = prop.multiProcessorCount;
+    st.probed = true;
+  }
+  if (!st.arch_ok) return ATTN_ERR_ARCH;
+  if (st.status == nullptr) {
+    int* s = nullptr;
+    e = cudaMalloc(&s, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = cudaMemset(s, 0, sizeof(int));
+    if (e != cudaSuccess) {
+      cudaFree(s);
+      return cuda_fail(e);
+    }
+    st.status = s;
+  }
+  if (g_encode == nullptr) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &qr);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (qr != cudaDriverEntryPointSuccess || fn == nullptr) return cuda_fail(cudaErrorNotSupported);
+    g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  }
+  *dev_out = dev;
+  *st_out = &st;
+  return ATTN_OK;
+}
+
+// Tensor map over a contiguous [heads, L, D] 16-bit tensor viewed as 3-D
+// (D innermost), boxes of 64 columns x `rows` rows x 1 head, 128-byte swizzle.
+attn_status_t encode_map(CUtensorMap* map, const void* base, int heads, int L, int D, int rows,
+                         bool bf16) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(L),
+                        static_cast<cuuint64_t>(heads)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
+                           static_cast<cuuint64_t>(L) * static_cast<cuuint64_t>(D) * 2};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(rows), 1};
+  cuuint32_t estride[3] = {1, 1, 1};
+  CUresult r = g_encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                        3, const_cast<void*>(base), dims, strides, box, estride,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
+  return ATTN_OK;
+}
+
+Problem make_problem(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                     int Hq, int Hkv, int L, int D, float sm_scale, int causal,
+                     const int32_t* valid_len, attn_dtype_t dtype, attn_stream_t stream,
+                     int* status) {
+  Problem p;
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.o = o;
+  p.lse = lse;
+  p.valid_len = valid_len;
+  p.status = status;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.L = L;
+  p.D = D;
+  p.sm_scale = sm_scale;
+  p.causal = causal;
+  p.bf16 = dtype == ATTN_BF16 ? 1 : 0;
+  p.stream = reinterpret_cast<cudaStream_t>(stream);
+  return p;
+}
+
+}  // namespace
+
+extern "C" {
+
+attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                       int Hq, int Hkv, int L, int D, float sm_scale, int causal,
+                       const int32_t* valid_len, attn_dtype_t dtype, attn_stream_t stream) {
+  attn_status_t s = validate(q, k, v, o, lse, B, Hq, Hkv, L, D, sm_scale, causal, valid_len, dtype);
+  if (s != ATTN_OK) return s;
+  int dev = 0;
+  DeviceState* st = nullptr;
+  s = device_state(&dev, &st);
+  if (s != ATTN_OK) return s;
+  attn::TcConfig cfg;
+  if (!attn::tc_config(D, &cfg)) return ATTN_ERR_HEADDIM;
+  const bool bf16 = dtype == ATTN_BF16;
+  CUtensorMap maps[3];
+  if ((s = encode_map(&maps[0], q, B * Hq, L, D, cfg.block_m, bf16)) != ATTN_OK) return s;
+  if ((s = encode_map(&maps[1], k, B * Hkv, L, D, cfg.block_n, bf16)) != ATTN_OK) return s;
+  if ((s = encode_map(&maps[2], v, B * Hkv, L, D, cfg.block_n, bf16)) != ATTN_OK) return s;
+  Problem p = make_problem(q, k, v, o, lse, B, Hq, Hkv, L, D, sm_scale, causal, valid_len, dtype,
+                           stream, st->status);
+  cudaError_t e = attn::launch_tc(p, maps, st->num_sms);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return ATTN_OK;
+}
+
+attn_status_t attn_fwd_simt(const void* q, const void* k, const void* v, void* o, float* lse,
+                            int B, int Hq, int Hkv, int L, int D, float sm_scale, int causal,
+                            const int32_t* valid_len, attn_dtype_t dtype, attn_stream_t stream) {
+  attn_status_t s = validate(q, k, v, o, lse, B, Hq, Hkv, L, D, sm_scale, causal, valid_len, dtype);
+  if (s != ATTN_OK) return s;
+  if (static_cast<int64_t>(B) * Hq > 65535) return ATTN_ERR_SHAPE;
+  int dev = 0;
+  DeviceState* st = nullptr;
+  s = device_state(&dev, &st);
+  if (s != ATTN_OK) return s;
+  Problem p = make_problem(q, k, v, o, lse, B, Hq, Hkv, L, D, sm_scale, causal, valid_len, dtype,
+                           stream, st->status);
+  cudaError_t e = attn::launch_simt(p);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return ATTN_OK;
+}
+
+attn_status_t attn_status(attn_stream_t stream, int* device_code) {
+  if (device_code != nullptr) *device_code = 0;
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  int dev = 0;
+  e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= kMaxDevices) return ATTN_OK;
+  int* word = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    word = g_dev[dev].status;
+  }
+  if (word == nullptr) return ATTN_OK;  // nothing ever launched on this device
+  int code = 0;
+  e = cudaMemcpy(&code, word, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (code != 0) {
+    e = cudaMemset(word, 0, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  if (device_code != nullptr) *device_code = code;
+  if (code & attn::kStatusTimeout) return ATTN_ERR_TIMEOUT;
+  if (code & attn::kStatusValidLenClamped) return ATTN_ERR_VALID_LEN;
+  return ATTN_OK;
+}
+
+attn_status_t attn_query(int D, attn_dtype_t dtype, attn_caps_t* out) {
+  if (out == nullptr) return ATTN_ERR_ARG;
+  *out = attn_caps_t{};
+  if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_DTYPE;
+  attn::TcConfig cfg;
+  if (!attn::tc_config(D, &cfg)) return ATTN_ERR_HEADDIM;
+  out->block_m = cfg.block_m;
+  out->q_tiles_per_cta = cfg.q_tiles;
+  out->block_n = cfg.block_n;
+  out->kv_stages = cfg.stages;
+  out->threads = cfg.threads;
+  out->smem_bytes = cfg.smem_bytes;
+  out->tmem_cols = cfg.tmem_cols;
+  out->lse_natural_log = 1;
+  int n = 0;
+  if (cudaGetDeviceCount(&n) == cudaSuccess && n > 0) {
+    int dev = 0;
+    cudaDeviceProp prop;
+    if (cudaGetDevice(&dev) == cudaSuccess && cudaGetDeviceProperties(&prop, dev) == cudaSuccess) {
+      out->num_sms = prop.multiProcessorCount;
+      out->supported = (prop.major == 10 && prop.minor == 3) ? 1 : 0;
+    }
+  } else {
+    cudaGetLastError();  // clear the "no device" error
+  }
+  return ATTN_OK;
+}
+
+const char* attn_strerror(attn_status_t status) {
+  switch (status) {
+    case ATTN_OK: return "success";
+    case ATTN_ERR_NULL: return "a required pointer is NULL";
+    case ATTN_ERR_ALIGN: return "q/k/v/o must be 16-byte aligned, lse/valid_len 4-byte aligned";
+    case ATTN_ERR_SHAPE: return "B, Hq, Hkv and L must be >= 1 and B*Hq*L must fit in int32";
+    case ATTN_ERR_HEADS: return "Hq must be a multiple of Hkv";
+    case ATTN_ERR_HEADDIM: return "unsupported head dimension (64 or 128)";
+    case ATTN_ERR_DTYPE: return "dtype must be ATTN_F16 or ATTN_BF16";
+    case ATTN_ERR_SCALE: return "sm_scale must be finite and >= 0";
+    case ATTN_ERR_ARCH: return "no sm_103 (GB300) device is current";
+    case ATTN_ERR_CUDA: return "a CUDA call failed (see attn_last_cuda_error)";
+    case ATTN_ERR_TIMEOUT: return "a bounded wait inside the kernel timed out";
+    case ATTN_ERR_VALID_LEN: return "a valid_len value was outside [0, L] and was clamped";
+    case ATTN_ERR_ARG: return "invalid argument";
+  }
+  return "unknown status";
+}
+
+int attn_last_cuda_error(void) { return g_last_cuda_error; }
+
+void attn_shutdown(void) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  int cur = 0;
+  const bool have_cur = cudaGetDevice(&cur) == cudaSuccess;
+  for (int d = 0; d < kMaxDevices; ++d) {
+    if (g_dev[d].status != nullptr) {
+      if (cudaSetDevice(d) == cudaSuccess) cudaFree(g_dev[d].status);
+      g_dev[d].status = nullptr;
+    }
+  }
+  if (have_cur) cudaSetDevice(cur);
+  cudaGetLastError();
+}
+
+}  // extern "C"

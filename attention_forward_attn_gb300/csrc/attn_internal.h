@@ -1,0 +1,55 @@
+// Internal interface between the host API (attn_api.cu) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace attn {
+
+// Device status word bits (see attn_status in include/attn.h).
+enum : int {
+  kStatusTimeout = 1 << 0,
+  kStatusValidLenClamped = 1 << 1,
+  kRoleProducer = 1 << 8,
+  kRoleMma = 2 << 8,
+  kRoleSoftmax = 4 << 8,
+  kRoleEpilogue = 8 << 8,
+};
+
+// Problem description handed to a kernel launcher (already validated).
+struct Problem {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* o;
+  float* lse;              // may be null
+  const int32_t* valid_len;  // may be null
+  int* status;             // device status word
+  int B, Hq, Hkv, L, D;
+  float sm_scale;
+  int causal;
+  int bf16;                // 0 fp16, 1 bf16
+  cudaStream_t stream;
+};
+
+// Static configuration of the tensor-core kernel for one head dimension.
+struct TcConfig {
+  int block_m;          // rows per query tile (= TMEM lanes)
+  int q_tiles;          // query tiles per CTA
+  int block_n;          // keys per K/V tile
+  int stages;           // K/V ring stages
+  int threads;
+  int smem_bytes;
+  int tmem_cols;
+};
+
+bool tc_config(int D, TcConfig* out);
+
+// Tensor-core (tcgen05/TMA) forward.  maps: Q, K, V tensor maps.
+cudaError_t launch_tc(const Problem& p, const CUtensorMap* maps, int num_sms);
+
+// SIMT cross-check forward.
+cudaError_t launch_simt(const Problem& p);
+
+}  // namespace attn

@@ -1,0 +1,652 @@
+// Tensor-core attention forward for sm_103a (tcgen05 + TMA + TMEM).
+//
+// What it computes: O = softmax(Q K^T * sm_scale + Mask) V and the per-row
+// natural-log LSE, tile by tile with the online softmax of the Triton-CUDA
+// Attention page ("Online Softmax core algorithm": running max m_i, exp-sum
+// l_i, an fp32 accumulator rescaled by alpha = exp2(m_old - m_new), scores
+// pre-multiplied by sm_scale*log2(e)); masks and head map as in include/attn.h.
+//
+// How (one CTA per SM, persistent over work units):
+//   * work unit = (b, h_q, 256 query rows) = two 128-row query tiles that share
+//     one stream of K/V tiles (128 keys each);
+//   * warp 8 (producer): TMA loads of the two Q tiles and of the K/V ring,
+//     128-byte swizzled, into a 4-stage (D=128) / 8-stage (D=64) ring;
+//   * warp 9 (MMA issuer, one thread): S_t = Q_t K^T into TMEM (fp32), then
+//     O_t += P_t V with P_t read from TMEM, interleaved PV_0, S_0(next),
+//     PV_1, S_1(next) so the tensor core works on one tile while the other
+//     tile's softmax runs;
+//   * warps 0-3 / 4-7 (softmax, one thread per query row = TMEM lane): load
+//     the S row, mask (only on boundary tiles), row max, ex2.approx, row sum,
+//     write P as 16-bit pairs over the S columns, rescale the O row in TMEM
+//     when the max grew by more than 2^8 (exact after the final division),
+//     and finally O / l -> global memory and the LSE.
+// Causal units skip every key tile above the diagonal; padded units skip every
+// key tile at or beyond valid_len[b]; a unit with no visible key writes O = 0
+// and LSE = -inf without touching the tensor core.
+//
+// Every mbarrier wait is bounded: after ATTN_WAIT_LIMIT_NS the waiting role
+// records a timeout in the device status word, raises a CTA-wide abort flag
+// and leaves its loop; the others see the flag and leave too; the CTA then
+// waits (bounded) for its own copies and MMAs in flight and frees its TMEM.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "attn_internal.h"
+#include "ptx.cuh"
+
+#ifndef ATTN_WAIT_LIMIT_NS
+#define ATTN_WAIT_LIMIT_NS 2000000000ull
+#endif
+
+namespace attn {
+namespace {
+
+constexpr int BM = 128;       // query rows per tile (TMEM lanes)
+constexpr int QT = 2;         // query tiles per work unit
+constexpr int BN = 128;       // keys per K/V tile
+constexpr int kUnitRows = QT * BM;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = 384;  // warpgroups: softmax tile 0, softmax tile 1, producer/MMA
+// Register split between warpgroups (setmaxnreg).  The CTA is launched with
+// kLaunchRegs per thread (the __launch_bounds__(384, 1) ceiling: 3 warps per
+// SM sub-partition); the split must add up to exactly that pool:
+// 2 * 128 * 216 + 128 * 72 = 384 * 168.
+constexpr int kLaunchRegs = 168;
+constexpr int kSoftmaxRegs = 216;
+constexpr int kControlRegs = 72;
+static_assert(2 * 128 * kSoftmaxRegs + 128 * kControlRegs == kThreads * kLaunchRegs,
+              "register split must equal the launch pool");
+constexpr float kRescaleLog2 = 8.0f;  // rescale O only when the max grows by > 2^8
+constexpr float kLn2 = 0.69314718055994531f;
+
+template <int D>
+struct Cfg {
+  static constexpr int kStages = (D == 128) ? 4 : 8;
+  static constexpr int kHalves = D / 64;           // 64-column (128-byte) slabs per row
+  static constexpr int kQBytes = BM * D * 2;
+  static constexpr int kKVBytes = BN * D * 2;
+  static constexpr int kSlabQ = BM * 128;          // bytes of one 64-column slab of a Q tile
+  static constexpr int kSlabKV = BN * 128;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffKV = QT * kQBytes;
+  static constexpr int kOffBar = kOffKV + kStages * kKVBytes;
+  static constexpr int kNumBars = 2 * QT + 2 * kStages + 3 * QT + 1;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + slack to align the base to 1 KB
+  // TMEM columns: S_0, S_1 (fp32, BN each; P_t overwrites the first BN/2
+  // columns of S_t as 16-bit pairs), then O_0, O_1 (fp32, D each).
+  static __device__ __forceinline__ uint32_t col_s(int t) { return static_cast<uint32_t>(t * BN); }
+  static __device__ __forceinline__ uint32_t col_o(int t) {
+    return static_cast<uint32_t>(2 * BN + t * D);
+  }
+  static constexpr uint32_t kTmemCols = 512;
+  static_assert(2 * BN + 2 * D <= 512, "TMEM budget");
+  static_assert(kSmemBytes <= 232448, "shared-memory budget");
+};
+
+struct KParams {
+  void* o;
+  float* lse;
+  const int32_t* valid_len;
+  int* status;
+  int B, Hq, Hkv, L, G;
+  int n_mb;     // 256-row blocks per (b, h_q)
+  int n_units;  // B * Hq * n_mb
+  float scale_log2;
+  int causal;
+};
+
+struct Unit {
+  int bh, b, hkv, m0, kv_len;
+  int n[QT];  // key tiles each query tile visits (0: tile absent or no visible key)
+};
+
+// Units are ordered so that causal work runs heaviest-first (last row blocks
+// first) with heads innermost (query heads of one KV group are adjacent, so
+// their K/V stay in L2), and non-causal work runs head by head.
+__device__ __forceinline__ Unit decode_unit(const KParams& p, int u) {
+  Unit w;
+  const int BH = p.B * p.Hq;
+  int mb;
+  if (p.causal) {
+    mb = p.n_mb - 1 - u / BH;
+    w.bh = u % BH;
+  } else {
+    w.bh = u / p.n_mb;
+    mb = u % p.n_mb;
+  }
+  w.b = w.bh / p.Hq;
+  w.hkv = (w.bh % p.Hq) / p.G;
+  w.m0 = mb * kUnitRows;
+  int kv = p.L;
+  if (p.valid_len != nullptr) {
+    kv = p.valid_len[w.b];
+    kv = kv < 0 ? 0 : (kv > p.L ? p.L : kv);
+  }
+  w.kv_len = kv;
+#pragma unroll
+  for (int t = 0; t < QT; ++t) {
+    const int r0 = w.m0 + t * BM;
+    if (r0 >= p.L) {
+      w.n[t] = 0;
+    } else {
+      const int hi = p.causal ? min(kv, r0 + BM) : kv;
+      w.n[t] = (hi + BN - 1) / BN;
+    }
+  }
+  return w;
+}
+
+struct Sync {
+  uint64_t* q_full;    // [QT]  TMA -> MMA
+  uint64_t* q_empty;   // [QT]  softmax (all S MMAs of the tile done) -> producer
+  uint64_t* kv_full;   // [S]   TMA -> MMA
+  uint64_t* kv_empty;  // [S]   MMA commit -> producer
+  uint64_t* s_full;    // [QT]  MMA commit -> softmax
+  uint64_t* p_full;    // [QT]  softmax (P written, O rescaled) -> MMA
+  uint64_t* o_full;    // [QT]  MMA commit after the tile's last PV -> softmax
+  uint64_t* drain;     // [1]
+  volatile uint32_t* abort_flag;
+  int* status;
+};
+
+// Bounded mbarrier wait.  False: timed out (recorded) or another role aborted.
+// (Everything is inlined: out-of-line calls do not mix with setmaxnreg.)
+__device__ __forceinline__ bool wait_bar_slow(const Sync& sy, uint64_t* bar, uint32_t parity,
+                                           int role) {
+  const uint64_t t0 = ptx::globaltimer_ns();
+  for (;;) {
+#pragma unroll 1
+    for (int i = 0; i < 16; ++i)
+      if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (*sy.abort_flag) return false;
+    if (ptx::globaltimer_ns() - t0 > ATTN_WAIT_LIMIT_NS) {
+      *sy.abort_flag = 1u;
+      atomicOr(sy.status, kStatusTimeout | role);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ bool wait_bar(const Sync& sy, uint64_t* bar, uint32_t parity, int role) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  return wait_bar_slow(sy, bar, parity, role);
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if constexpr (BF16) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  } else {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+}
+
+// ------------------------------------------------------------------ producer
+
+template <int D>
+__device__ void producer_role(const KParams& p, const Sync& sy, uint8_t* smem,
+                              const CUtensorMap* tm_q, const CUtensorMap* tm_k,
+                              const CUtensorMap* tm_v) {
+  using C = Cfg<D>;
+  uint32_t q_phase[QT] = {0, 0};
+  uint32_t it = 0;
+  int last_stage_parity[C::kStages];
+#pragma unroll
+  for (int s = 0; s < C::kStages; ++s) last_stage_parity[s] = -1;
+  bool q_used[QT] = {false, false};
+  const uint64_t pol_keep = ptx::policy_evict_last();
+  const uint64_t pol_stream = ptx::policy_evict_first();
+  bool ok = true;
+
+  for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+    const Unit w = decode_unit(p, u);
+    const int n = max(w.n[0], w.n[1]);
+    if (n == 0) continue;
+    const int z_kv = w.b * p.Hkv + w.hkv;
+#pragma unroll
+    for (int t = 0; t < QT; ++t) {
+      if (w.n[t] == 0) continue;
+      if (!wait_bar(sy, &sy.q_empty[t], q_phase[t] ^ 1u, kRoleProducer)) { ok = false; break; }
+      q_phase[t] ^= 1u;
+      q_used[t] = true;
+      uint8_t* dst = smem + C::kOffQ + t * C::kQBytes;
+      ptx::mbar_arrive_expect_tx(&sy.q_full[t], C::kQBytes);
+#pragma unroll
+      for (int h = 0; h < C::kHalves; ++h)
+        ptx::tma_load_3d_hint(dst + h * C::kSlabQ, tm_q, &sy.q_full[t], h * 64, w.m0 + t * BM,
+                              w.bh, pol_stream);
+    }
+    for (int j = 0; ok && j < n; ++j) {
+#pragma unroll
+      for (int kind = 0; kind < 2; ++kind) {
+        const uint32_t s = it % C::kStages;
+        const uint32_t par = (it / C::kStages) & 1u;
+        if (!wait_bar(sy, &sy.kv_empty[s], par ^ 1u, kRoleProducer)) { ok = false; break; }
+        ++it;
+        uint8_t* dst = smem + C::kOffKV + s * C::kKVBytes;
+        ptx::mbar_arrive_expect_tx(&sy.kv_full[s], C::kKVBytes);
+        const CUtensorMap* tm = kind == 0 ? tm_k : tm_v;
+#pragma unroll
+        for (int h = 0; h < C::kHalves; ++h)
+          ptx::tma_load_3d_hint(dst + h * C::kSlabKV, tm, &sy.kv_full[s], h * 64, j * BN, z_kv,
+                                pol_keep);
+        last_stage_parity[s] = static_cast<int>(par);
+      }
+    }
+  }
+  // Never leave with a copy in flight: wait (bounded) for the last load of
+  // every buffer.  In a normal run these phases completed long ago.
+  for (int s = 0; s < C::kStages; ++s)
+    if (last_stage_parity[s] >= 0) {
+      const uint64_t t0 = ptx::globaltimer_ns();
+      while (!ptx::mbar_try_wait(&sy.kv_full[s], static_cast<uint32_t>(last_stage_parity[s])) &&
+             ptx::globaltimer_ns() - t0 < ATTN_WAIT_LIMIT_NS) {
+      }
+    }
+  for (int t = 0; t < QT; ++t)
+    if (q_used[t]) {
+      const uint64_t t0 = ptx::globaltimer_ns();
+      while (!ptx::mbar_try_wait(&sy.q_full[t], q_phase[t] ^ 1u) &&
+             ptx::globaltimer_ns() - t0 < ATTN_WAIT_LIMIT_NS) {
+      }
+    }
+}
+
+// ------------------------------------------------------------------ MMA issuer
+
+// A descriptor's start address is its low 14 bits (address >> 4); a byte
+// offset inside the same shared-memory window is added there directly.
+__device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t bytes) {
+  return desc + (bytes >> 4);
+}
+
+// S = Q K^T over D: A = Q tile, B = K tile, both K-major 128-byte swizzled
+// (64-column slabs); each MMA consumes 16 columns (32 bytes of a slab row).
+template <int D, bool BF16>
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t q_desc, uint64_t k_desc) {
+  using C = Cfg<D>;
+  constexpr uint32_t idesc = ptx::idesc_f16(BM, BN, BF16, false);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = (kk & 3) * 32u;
+    ptx::mma_ss(d_tmem, desc_add(q_desc, (kk / 4) * C::kSlabQ + off),
+                desc_add(k_desc, (kk / 4) * C::kSlabKV + off), idesc, kk > 0 ? 1u : 0u);
+  }
+}
+
+// O += P V: A = P from TMEM (16-bit pairs, 8 columns per 16 keys), B = V tile
+// as an MN-major 128-byte-swizzled operand (16 keys = two 8-row groups).
+template <int D, bool BF16>
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint64_t v_desc,
+                                         bool accumulate) {
+  constexpr uint32_t idesc = ptx::idesc_f16(BM, D, BF16, true);
+#pragma unroll
+  for (int kk = 0; kk < BN / 16; ++kk)
+    ptx::mma_ts(d_tmem, p_tmem + kk * 8u, desc_add(v_desc, kk * 2048u), idesc,
+                (accumulate || kk > 0) ? 1u : 0u);
+}
+
+template <int D, bool BF16>
+__device__ void mma_role(const KParams& p, const Sync& sy, uint8_t* smem, uint32_t tmem) {
+  using C = Cfg<D>;
+  uint32_t q_phase[QT] = {0, 0};
+  uint32_t p_phase[QT] = {0, 0};
+  uint32_t it = 0;
+  // K-major operands (Q, K): leading byte offset unused with 128-byte swizzle,
+  // 1024 bytes between 8-row groups.  MN-major V: 64-column slabs kSlabKV
+  // apart (leading), 1024 bytes between 8-key groups (stride).
+  const uint64_t q_desc0 = ptx::sdesc_sw128(ptx::smem_u32(smem + C::kOffQ), 16, 1024);
+  const uint64_t k_desc0 = ptx::sdesc_sw128(ptx::smem_u32(smem + C::kOffKV), 16, 1024);
+  const uint64_t v_desc0 = ptx::sdesc_sw128(ptx::smem_u32(smem + C::kOffKV), C::kSlabKV, 1024);
+  bool ok = true;
+
+  for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+    const Unit w = decode_unit(p, u);
+    const int n = max(w.n[0], w.n[1]);
+    if (n == 0) continue;
+#pragma unroll
+    for (int t = 0; t < QT; ++t) {
+      if (w.n[t] == 0) continue;
+      if (!wait_bar(sy, &sy.q_full[t], q_phase[t], kRoleMma)) { ok = false; break; }
+      q_phase[t] ^= 1u;
+    }
+    if (!ok) break;
+    // K_0
+    uint32_t sk = it % C::kStages;
+    if (!wait_bar(sy, &sy.kv_full[sk], (it / C::kStages) & 1u, kRoleMma)) break;
+    ++it;
+    ptx::tc_fence_after();
+#pragma unroll
+    for (int t = 0; t < QT; ++t)
+      if (w.n[t] > 0) {
+        issue_qk<D, BF16>(tmem + C::col_s(t), desc_add(q_desc0, t * C::kQBytes),
+                          desc_add(k_desc0, sk * C::kKVBytes));
+        ptx::mma_commit(&sy.s_full[t]);
+      }
+    ptx::mma_commit(&sy.kv_empty[sk]);
+
+    for (int j = 0; j < n; ++j) {
+      const uint32_t sv = it % C::kStages;
+      if (!wait_bar(sy, &sy.kv_full[sv], (it / C::kStages) & 1u, kRoleMma)) { ok = false; break; }
+      ++it;
+      const bool has_next = j + 1 < n;
+      uint32_t sk2 = 0;
+      bool next_loaded = false;
+#pragma unroll
+      for (int t = 0; t < QT; ++t) {
+        if (j < w.n[t]) {
+          if (!wait_bar(sy, &sy.p_full[t], p_phase[t], kRoleMma)) { ok = false; break; }
+          p_phase[t] ^= 1u;
+          ptx::tc_fence_after();
+          issue_pv<D, BF16>(tmem + C::col_o(t), tmem + C::col_s(t),
+                            desc_add(v_desc0, sv * C::kKVBytes), j > 0);
+          if (j == w.n[t] - 1) ptx::mma_commit(&sy.o_full[t]);
+        }
+        if (t == QT - 1) ptx::mma_commit(&sy.kv_empty[sv]);  // V_j read by every PV above
+        if (has_next && !next_loaded) {
+          sk2 = it % C::kStages;
+          if (!wait_bar(sy, &sy.kv_full[sk2], (it / C::kStages) & 1u, kRoleMma)) {
+            ok = false;
+            break;
+          }
+          ++it;
+          next_loaded = true;
+          ptx::tc_fence_after();
+        }
+        if (j + 1 < w.n[t]) {
+          issue_qk<D, BF16>(tmem + C::col_s(t), desc_add(q_desc0, t * C::kQBytes),
+                            desc_add(k_desc0, sk2 * C::kKVBytes));
+          ptx::mma_commit(&sy.s_full[t]);
+        }
+      }
+      if (!ok) break;
+      if (has_next) ptx::mma_commit(&sy.kv_empty[sk2]);
+    }
+  }
+  // Every MMA issued by this thread completes before TMEM is released.
+  ptx::mma_commit(sy.drain);
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (!ptx::mbar_try_wait(sy.drain, 0) && ptx::globaltimer_ns() - t0 < ATTN_WAIT_LIMIT_NS) {
+  }
+}
+
+// ------------------------------------------------------------------ softmax + epilogue
+
+template <int D, bool BF16>
+__device__ void softmax_role(const KParams& p, const Sync& sy, uint32_t tmem, int t) {
+  using C = Cfg<D>;
+  const int lane_row = threadIdx.x & 127;           // row within the tile = TMEM lane
+  const uint32_t quad = (threadIdx.x >> 5) & 3u;    // this warp's 32-lane TMEM quadrant
+  const uint32_t t_s = tmem + ((quad * 32u) << 16) + C::col_s(t);
+  const uint32_t t_o = tmem + ((quad * 32u) << 16) + C::col_o(t);
+  const float scale_log2 = p.scale_log2;
+  uint32_t s_phase = 0, o_phase = 0;
+
+  for (int u = blockIdx.x; u < p.n_units; u += gridDim.x) {
+    const Unit w = decode_unit(p, u);
+    const int r0 = w.m0 + t * BM;
+    if (r0 >= p.L) continue;
+    const int row = r0 + lane_row;
+    const bool row_ok = row < p.L;
+    const int64_t grow = static_cast<int64_t>(w.bh) * p.L + row;
+    if (t == 0 && threadIdx.x == 0 && p.valid_len != nullptr) {
+      const int vl = p.valid_len[w.b];
+      if (vl < 0 || vl > p.L) atomicOr(p.status, kStatusValidLenClamped);
+    }
+    const int nt = w.n[t];
+    if (nt == 0) {  // no visible key: O = 0, LSE = -inf
+      if (row_ok) {
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.o) + grow * D * 2);
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
+        if (p.lse != nullptr) p.lse[grow] = -INFINITY;
+      }
+      continue;
+    }
+    // keys < key_lim are visible to this row
+    const int key_lim = p.causal ? min(w.kv_len, row + 1) : w.kv_len;
+    float m = -INFINITY;  // running max, log2 units (scaled)
+    float l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nt; ++j) {
+      ok = wait_bar(sy, &sy.s_full[t], s_phase, kRoleSoftmax);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      s_phase ^= 1u;
+      ptx::tc_fence_after();
+      uint32_t s[BN];
+      ptx::tmem_ld64(t_s, *reinterpret_cast<uint32_t(*)[64]>(&s[0]));
+      ptx::tmem_ld64(t_s + 64, *reinterpret_cast<uint32_t(*)[64]>(&s[64]));
+      const int n0 = j * BN;
+      const bool masked = (n0 + BN > w.kv_len) || (p.causal && n0 + BN - 1 > r0);
+      const int c_lim = key_lim - n0;  // columns c < c_lim are visible
+      float mx = -INFINITY;
+      if (masked) {
+#pragma unroll
+        for (int c = 0; c < BN; ++c) {
+          const float x = (c < c_lim) ? __uint_as_float(s[c]) : -INFINITY;
+          mx = fmaxf(mx, x);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < BN; ++c) mx = fmaxf(mx, __uint_as_float(s[c]));
+      }
+      const float m_tile = (mx == -INFINITY) ? -INFINITY : mx * scale_log2;
+      const float m_new = fmaxf(m, m_tile);
+      float alpha = 1.f;
+      bool rescale = false;
+      if (m_new > m + kRescaleLog2) {  // also taken on the first tile (m = -inf)
+        alpha = ptx::ex2_approx(m - m_new);
+        m = m_new;
+        rescale = true;
+      }
+      const float neg_m = (m == -INFINITY) ? 0.f : -m;
+      float rowsum = 0.f;
+      // P as 16-bit pairs over the first BN/2 columns of S, written one half
+      // at a time (S columns still to be read lie beyond what is written)
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t pk[BN / 4];
+#pragma unroll
+        for (int i = 0; i < BN / 4; ++i) {
+          const int c = half * (BN / 2) + 2 * i;
+          float p0 = ptx::ex2_approx(fmaf(__uint_as_float(s[c]), scale_log2, neg_m));
+          float p1 = ptx::ex2_approx(fmaf(__uint_as_float(s[c + 1]), scale_log2, neg_m));
+          if (masked) {
+            p0 = (c < c_lim) ? p0 : 0.f;
+            p1 = (c + 1 < c_lim) ? p1 : 0.f;
+          }
+          rowsum += p0 + p1;
+          pk[i] = pack2<BF16>(p0, p1);
+        }
+        ptx::tmem_st32(t_s + half * 32, pk);
+      }
+      l = l * alpha + rowsum;
+      // O was accumulated against the old max: rescale it before PV_j runs.
+      // PV_{j-1} is complete: the commit that signalled S_j came after it.
+      if (j > 0 && __any_sync(0xffffffffu, rescale)) {
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t o[32];
+          ptx::tmem_ld32(t_o + c0, o);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+          ptx::tmem_st32(t_o + c0, o);
+        }
+      }
+      ptx::tmem_st_wait();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&sy.p_full[t]);
+    }
+    if (!ok) return;
+    // epilogue
+    ok = wait_bar(sy, &sy.o_full[t], o_phase, kRoleEpilogue);
+    if (!__all_sync(0xffffffffu, ok)) return;
+    o_phase ^= 1u;
+    ptx::tc_fence_after();
+    ptx::mbar_arrive(&sy.q_empty[t]);  // every S MMA of this tile is done: Q_t is free
+    const float inv_l = 1.f / l;
+#pragma unroll 1
+    for (int c0 = 0; c0 < D; c0 += 32) {
+      uint32_t o[32];
+      ptx::tmem_ld32(t_o + c0, o);
+      uint32_t h[16];
+#pragma unroll
+      for (int c = 0; c < 16; ++c)
+        h[c] = pack2<BF16>(__uint_as_float(o[2 * c]) * inv_l, __uint_as_float(o[2 * c + 1]) * inv_l);
+      if (row_ok) {
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.o) + (grow * D + c0) * 2);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) dst[c] = make_uint4(h[4 * c], h[4 * c + 1], h[4 * c + 2], h[4 * c + 3]);
+      }
+    }
+    if (row_ok && p.lse != nullptr) p.lse[grow] = (m + ptx::lg2_approx(l)) * kLn2;
+  }
+}
+
+// ------------------------------------------------------------------ kernel
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
+                       const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, const KParams p) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  Sync sy;
+  sy.q_full = bars;
+  sy.q_empty = sy.q_full + QT;
+  sy.kv_full = sy.q_empty + QT;
+  sy.kv_empty = sy.kv_full + C::kStages;
+  sy.s_full = sy.kv_empty + C::kStages;
+  sy.p_full = sy.s_full + QT;
+  sy.o_full = sy.p_full + QT;
+  sy.drain = sy.o_full + QT;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
+  sy.abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::kOffMisc + 4);
+  sy.status = p.status;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int t = 0; t < QT; ++t) {
+      ptx::mbar_init(&sy.q_full[t], 1);
+      ptx::mbar_init(&sy.q_empty[t], BM);
+      ptx::mbar_init(&sy.s_full[t], 1);
+      ptx::mbar_init(&sy.p_full[t], BM);
+      ptx::mbar_init(&sy.o_full[t], 1);
+    }
+    for (int s = 0; s < C::kStages; ++s) {
+      ptx::mbar_init(&sy.kv_full[s], 1);
+      ptx::mbar_init(&sy.kv_empty[s], 1);
+    }
+    ptx::mbar_init(sy.drain, 1);
+    *sy.abort_flag = 0u;
+    ptx::fence_barrier_init();
+  }
+  if (warp == kProducerWarp && lane == 0) {
+    ptx::prefetch_tensormap(&tm_q);
+    ptx::prefetch_tensormap(&tm_k);
+    ptx::prefetch_tensormap(&tm_v);
+  }
+  if (warp == kMmaWarp) {
+    ptx::tmem_alloc(tmem_holder, C::kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  if (warp >= 8) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kControlRegs));
+    if (warp == kProducerWarp) {
+      if (lane == 0) producer_role<D>(p, sy, smem, &tm_q, &tm_k, &tm_v);
+    } else if (warp == kMmaWarp) {
+      if (lane == 0) mma_role<D, BF16>(p, sy, smem, tmem);
+    }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
+    softmax_role<D, BF16>(p, sy, tmem, warp >> 2);
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+template <int D, bool BF16>
+cudaError_t launch_instance(const Problem& pr, const CUtensorMap* maps, int num_sms) {
+  using C = Cfg<D>;
+  static bool configured = false;  // per (D, dtype) instance
+  auto kern = attn_fwd_tc_kernel<D, BF16>;
+  if (!configured) {
+    // The setmaxnreg split is only safe when the CTA is launched with exactly
+    // kLaunchRegs registers per thread; anything else could stall the
+    // increasing warpgroups forever, so refuse to launch.
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidKernelImage;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  KParams kp;
+  kp.o = pr.o;
+  kp.lse = pr.lse;
+  kp.valid_len = pr.valid_len;
+  kp.status = pr.status;
+  kp.B = pr.B;
+  kp.Hq = pr.Hq;
+  kp.Hkv = pr.Hkv;
+  kp.L = pr.L;
+  kp.G = pr.Hq / pr.Hkv;
+  kp.n_mb = (pr.L + kUnitRows - 1) / kUnitRows;
+  kp.n_units = pr.B * pr.Hq * kp.n_mb;
+  kp.scale_log2 = pr.sm_scale * 1.4426950408889634f;
+  kp.causal = pr.causal;
+  const int grid = kp.n_units < num_sms ? kp.n_units : num_sms;
+  kern<<<grid, kThreads, C::kSmemBytes, pr.stream>>>(maps[0], maps[1], maps[2], kp);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool tc_config(int D, TcConfig* out) {
+  if (D == 64) {
+    *out = {BM, QT, BN, Cfg<64>::kStages, kThreads, Cfg<64>::kSmemBytes,
+            static_cast<int>(Cfg<64>::kTmemCols)};
+    return true;
+  }
+  if (D == 128) {
+    *out = {BM, QT, BN, Cfg<128>::kStages, kThreads, Cfg<128>::kSmemBytes,
+            static_cast<int>(Cfg<128>::kTmemCols)};
+    return true;
+  }
+  return false;
+}
+
+cudaError_t launch_tc(const Problem& p, const CUtensorMap* maps, int num_sms) {
+  if (p.D == 64) {
+    return p.bf16 ? launch_instance<64, true>(p, maps, num_sms)
+                  : launch_instance<64, false>(p, maps, num_sms);
+  }
+  if (p.D == 128) {
+    return p.bf16 ? launch_instance<128, true>(p, maps, num_sms)
+                  : launch_instance<128, false>(p, maps, num_sms);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace attn

@@ -1,0 +1,486 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused attention forward on GB300.
+
+One step = one attn_fwd call over the whole workload (every query row of every
+head).  Default workload C4: causal GQA, bf16, Q [4,32,4096,128], K/V
+[4,8,4096,128] -- the configuration the throughput target is quoted on.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload C1..C5]
+    python bench.py --impl reference ...   # the float64 CPU oracle, bounded samples
+
+Prints ONE JSON line (rank 0).  Multi-GPU (torchrun): every rank runs an
+independent replica of the workload (the forward has no exchange step);
+value = all ranks' FLOPs / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from attention_forward_attn_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "attention fwd TFLOP/s and % of GB300 dense fp16/bf16 tensor peak; ms/call"
+UNIT = "TFLOP/s"
+L2_FLUSH_BYTES = 256 << 20          # > 129 MB L2
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "attn_fwd_tc_dram_traffic.txt")
+KERNEL_SOURCES = [os.path.join(ROOT, "attention_forward_attn_gb300", "csrc", f)
+                  for f in ("attn_tc.cu", "ptx.cuh")]
+
+
+# ------------------------------------------------------------------ work accounting
+
+def nominal_flops(w) -> float:
+    """The metric's formula: 4*B*Hq*L^2*D, halved for causal."""
+    f = 4.0 * w.B * w.Hq * w.L * w.L * w.D
+    return f / 2 if w.causal else f
+
+
+def visible_keys_per_row(w, valid_len):
+    """|J_i| for every row i of one (b, h) head, per batch: array [B, L]."""
+    i = np.arange(w.L, dtype=np.int64)
+    out = np.empty((w.B, w.L), dtype=np.int64)
+    for b in range(w.B):
+        kv = w.L if valid_len is None else int(min(max(int(valid_len[b]), 0), w.L))
+        out[b] = np.minimum(kv, i + 1) if w.causal else kv
+    return out
+
+
+def algorithmic_flops(w, valid_len) -> float:
+    """Only unmasked work: 4*D per visible (query, key) pair (QK^T and PV)."""
+    return 4.0 * w.D * w.Hq * float(visible_keys_per_row(w, valid_len).sum())
+
+
+def io_bytes(w) -> dict:
+    e = 2
+    q = w.B * w.Hq * w.L * w.D * e
+    kv = 2 * w.B * w.Hkv * w.L * w.D * e
+    o = q
+    lse = w.B * w.Hq * w.L * 4
+    vl = w.B * 4 if w.padded else 0
+    return {"q": q, "kv": kv, "o": o, "lse": lse, "valid_len": vl}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source for this workload; else None."""
+    try:
+        text = open(PROFILE_TRAFFIC).read()
+    except OSError:
+        return None
+    fields = {}
+    for line in text.splitlines():
+        if ":" in line:
+            k, v = line.split(":", 1)
+            fields[k.strip()] = v.strip()
+    if fields.get("source_sha256_16") != kernel_source_hash():
+        return None
+    key = "dram_bytes_per_launch_%s" % workload
+    try:
+        return float(fields[key])
+    except (KeyError, ValueError):
+        return None
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle sampling while the timed region runs."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+            self.path = os.path.join(ROOT, "gpurun_out", "clocks_bench_%d.csv" % os.getpid())
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.QUERY,
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.fh,
+                stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ distributed
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reduce_max(value: float, world: int) -> float:
+    """Max over ranks (identity for one process)."""
+    if world == 1:
+        return value
+    import torch.distributed as dist
+    dev = torch.device("cuda") if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def aggregate(per_rank_flops: float, max_seconds: float, world: int) -> float:
+    """Whole-job TFLOP/s: the work of every replica over the slowest rank's time."""
+    return per_rank_flops * world / max_seconds / 1e12
+
+
+# ------------------------------------------------------------------ CPU oracle baseline
+
+def oracle_sample(w, q, k, v, vl, budget_s: float, rng, threads: int = 0):
+    """Time the float64 oracle on a bounded random sample of query rows of the
+    workload.  Returns (TFLOP/s in the metric's convention, details)."""
+    import oracle
+    code = wl.dtype_code(w.dtype)
+    qd = oracle.decode(wl.bits(q), code)
+    kd = oracle.decode(wl.bits(k), code)
+    vd = oracle.decode(wl.bits(v), code)
+    vln = None if vl is None else vl.numpy()
+    keys = visible_keys_per_row(w, vln)                      # [B, L]
+    total_rows = w.B * w.Hq * w.L
+    ratio = nominal_flops(w) / max(algorithmic_flops(w, vln), 1.0)
+
+    def run(n_rows):
+        rows = np.sort(rng.choice(total_rows, size=n_rows, replace=False))
+        b = (rows // w.L) // w.Hq
+        i = rows % w.L
+        flops = 4.0 * w.D * float(keys[b, i].sum())
+        t0 = time.perf_counter()
+        oracle.attn_fwd_f64(qd, kd, vd, w.sm_scale, causal=w.causal, valid_len=vln, rows=rows,
+                            threads=threads)
+        return time.perf_counter() - t0, flops, n_rows
+
+    # calibrate on a small sample, then size the measured sample to the budget
+    n = min(total_rows, 64 * max(1, oracle.max_threads()))
+    dt, fl, _ = run(n)
+    per_row = dt / n
+    n_rows = int(min(total_rows, max(n, budget_s / max(per_row, 1e-9))))
+    dt, fl, n_rows = run(n_rows)
+    tflops = fl * ratio / dt / 1e12
+    return tflops, {"rows": n_rows, "seconds": dt, "algorithmic_flops": fl,
+                    "nominal_per_algorithmic": ratio}
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def run_gpu(args, w, world, rank, local):
+    import attention_forward_attn_gb300 as attn
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    attn.load()
+    q, k, v, vl = wl.workload_inputs(w)
+    q_d, k_d, v_d = q.to(dev), k.to(dev), v.to(dev)
+    vl_d = None if vl is None else vl.to(dev)
+    o_d = torch.empty_like(q_d)
+    lse_d = torch.empty((w.B * w.Hq, w.L), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        attn.attn_fwd(q_d, k_d, v_d, causal=w.causal, sm_scale=w.sm_scale, valid_len=vl_d,
+                      out=o_d, lse=lse_d, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    st, code = attn.status(stream)
+    if st != 0:
+        raise RuntimeError("device status after warm-up: %d (code %#x)" % (st, code))
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    wall0 = time.perf_counter()
+    for s in range(args.steps):
+        flush.zero_()                     # L2 flushed between timed steps
+        starts[s].record(stream)
+        step()
+        ends[s].record(stream)
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop()
+    barrier(world)
+    st, code = attn.status(stream)
+    if st != 0:
+        raise RuntimeError("device status after timing: %d (code %#x)" % (st, code))
+    ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    ms_mean = sum(ms) / len(ms)
+    ms_max_rank = reduce_max(ms_mean, world)
+
+    # end to end through the public API: pinned host inputs -> device -> attn_fwd -> host
+    q_h, k_h, v_h = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    vl_h = None if vl is None else vl.pin_memory()
+    o_h = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+    lse_h = torch.empty((w.B * w.Hq, w.L), dtype=torch.float32).pin_memory()
+    e2e_steps = max(3, min(args.steps, args.e2e_steps))
+
+    def e2e_step():
+        qq = q_h.to(dev, non_blocking=True)
+        kk = k_h.to(dev, non_blocking=True)
+        vv = v_h.to(dev, non_blocking=True)
+        vvl = None if vl_h is None else vl_h.to(dev, non_blocking=True)
+        oo, ll = attn.attn_fwd(qq, kk, vv, causal=w.causal, sm_scale=w.sm_scale, valid_len=vvl,
+                               stream=stream)
+        o_h.copy_(oo, non_blocking=True)
+        lse_h.copy_(ll, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = reduce_max(e0.elapsed_time(e1) / e2e_steps, world)
+    st, code = attn.status(stream)
+    if st != 0:
+        raise RuntimeError("device status after e2e: %d (code %#x)" % (st, code))
+
+    # results
+    vln = None if vl is None else vl.numpy()
+    nom = nominal_flops(w)
+    alg = algorithmic_flops(w, vln)
+    peaks, peak_src = load_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    ms_med = statistics.median(ms)
+    achieved = alg / (ms_mean * 1e-3) / 1e12
+    b = io_bytes(w)
+    line = {
+        "metric": METRIC,
+        "value": round(aggregate(nom, ms_max_rank * 1e-3, world), 3),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_max_rank, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": w.dtype,
+        "data": "synthetic: seeded N(0,1) fp32 rounded to %s%s" % (
+            w.dtype, ", Q x%g" % w.q_scale if w.q_scale != 1.0 else ""),
+        "config": {
+            "workload": "%s: %s" % (w.name, w.description),
+            "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "L": w.L, "D": w.D, "causal": w.causal,
+            "valid_len": None if vl is None else vl.tolist(), "sm_scale": w.sm_scale,
+            "parallelism": "replicas x%d (no exchange step)" % world,
+            "l2": "flushed between timed steps (256 MB write, outside the events)",
+            "timing": "CUDA events around each attn_fwd call on its stream",
+            "ms_median": round(ms_med, 5),
+            "ms_p10": round(float(np.percentile(ms, 10)), 5),
+            "ms_p90": round(float(np.percentile(ms, 90)), 5),
+            "wall_s_timed_region": round(wall, 4),
+            "nominal_flops": nom,
+            "algorithmic_flops": alg,
+        },
+        "roofline": {
+            "bound": "tensor",
+            "achieved": round(achieved, 3),
+            "peak": peak,
+            "unit": "TFLOP/s",
+            "frac": round(achieved / peak, 4),
+            "peak_source": "%s bf16_tflops (burst; kernel timed alone)" % peak_src,
+            "traffic": committed_traffic(w.name),
+            "traffic_unit": "bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum)",
+            "hbm_min_bytes": sum(b.values()),
+            "hbm_gbs_at_min_bytes": round(sum(b.values()) / (ms_mean * 1e-3) / 1e9, 1),
+            "hbm_peak_gbs": float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])),
+        },
+        "e2e": {
+            "value": round(aggregate(nom, e2e_ms * 1e-3, world), 3),
+            "unit": UNIT,
+            "h2d_bytes_per_step": b["q"] + b["kv"] + b["valid_len"],
+            "d2h_bytes_per_step": b["o"] + b["lse"],
+            "ms_per_step": round(e2e_ms, 4),
+            "steps": e2e_steps,
+            "path": "pinned host Q/K/V -> device, attn_fwd (C ABI via the binding), O/LSE -> host",
+        },
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        rng = np.random.default_rng(1234)
+        tfl, det = oracle_sample(w, q, k, v, vl, args.cpu_budget_s, rng)
+        line["cpu_baseline"] = {
+            "value": round(tfl, 6), "unit": UNIT, "cores": _oracle_threads(),
+            "kind": "oracle",
+            "sample": "%d random query rows of %s (%.1f s of float64 oracle work, scaled by "
+                      "nominal/algorithmic FLOPs %.4f)" % (det["rows"], w.name, det["seconds"],
+                                                          det["nominal_per_algorithmic"]),
+        }
+    return line
+
+
+def _oracle_threads() -> int:
+    import oracle
+    return oracle.max_threads()
+
+
+# ------------------------------------------------------------------ reference arm
+
+def run_reference(args, w):
+    """The float64 CPU oracle as the reference arm: each step a bounded sample."""
+    q, k, v, vl = wl.workload_inputs(w)
+    rng = np.random.default_rng(99)
+    per_step = max(0.2, args.reference_budget_s / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        oracle_sample(w, q, k, v, vl, per_step, rng)
+    vals, secs, rows = [], [], 0
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        tfl, det = oracle_sample(w, q, k, v, vl, per_step, rng)
+        vals.append(tfl)
+        secs.append(det["seconds"])
+        rows += det["rows"]
+    wall = time.perf_counter() - t0
+    value = sum(vals) / len(vals)
+    nom = nominal_flops(w)
+    cores = _oracle_threads()
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 6),
+        "unit": UNIT,
+        "n_gpus": 1,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(nom / (value * 1e12) * 1e3, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic: seeded N(0,1) rounded to %s, decoded to float64" % w.dtype,
+        "config": {"workload": "%s: %s" % (w.name, w.description), "B": w.B, "Hq": w.Hq,
+                   "Hkv": w.Hkv, "L": w.L, "D": w.D, "causal": w.causal,
+                   "ms_per_step_note": "extrapolated: the whole workload at the sampled rate",
+                   "wall_s": round(wall, 2)},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": cores,
+                         "kind": "oracle",
+                         "sample": "%d random query rows per step on average (%.2f s each)" % (
+                             rows // max(1, args.steps), sum(secs) / len(secs))},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    return line
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="C4", choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-budget-s", type=float, default=12.0)
+    ap.add_argument("--reference-budget-s", type=float, default=120.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = wl.WORKLOADS[args.workload]
+    world, rank, local = dist_env()
+    if world != args.gpus and world > 1:
+        ap.error("--gpus %d does not match WORLD_SIZE %d" % (args.gpus, world))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, w)), flush=True)
+        return 0
+
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    line = run_gpu(args, w, world, rank, local)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,157 @@
+/*
+ * attn.h -- C ABI of libattn.so, a fused multi-head attention forward for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The operation (one call = one forward over a whole batch):
+ *
+ *   O = softmax(Q K^T * sm_scale + Mask) V,   LSE = log sum exp(Q K^T * sm_scale + Mask)
+ *
+ * as defined in "masked multi head attention in CUDA" (wzjinhao.cn), section
+ * 2.1, over [B, H, L, D] tensors, evaluated tile by tile with the online
+ * softmax of the Triton-CUDA Attention page ("Online Softmax core algorithm":
+ * running row max m_i, exp-sum l_i, fp32 accumulator rescaled by
+ * alpha = exp2(m_old - m_new), scores pre-multiplied by sm_scale * log2(e)),
+ * so the [B, H, L, L] score matrix never reaches device memory.
+ *
+ * All entry points are plain C: no C++ exceptions cross this boundary, every
+ * call returns an attn_status_t, and no argument is a framework type.
+ */
+#ifndef ATTN_GB300_ATTN_H
+#define ATTN_GB300_ATTN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream (the same object as cudaStream_t / CUstream); NULL is the
+ * legacy default stream. */
+typedef struct CUstream_st* attn_stream_t;
+
+/* Element type of Q, K, V and O.  The accumulation is always fp32. */
+typedef enum {
+  ATTN_F16 = 0,  /* IEEE binary16 */
+  ATTN_BF16 = 1  /* bfloat16 */
+} attn_dtype_t;
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_NULL = 1,       /* a required pointer is NULL */
+  ATTN_ERR_ALIGN = 2,      /* q, k, v or o is not 16-byte aligned, or lse / valid_len not 4-byte aligned */
+  ATTN_ERR_SHAPE = 3,      /* B, Hq, Hkv or L < 1, or a size overflows the supported range */
+  ATTN_ERR_HEADS = 4,      /* Hq is not a multiple of Hkv */
+  ATTN_ERR_HEADDIM = 5,    /* D is not supported by this entry point */
+  ATTN_ERR_DTYPE = 6,      /* dtype is not ATTN_F16 / ATTN_BF16 */
+  ATTN_ERR_SCALE = 7,      /* sm_scale is negative, NaN or infinite */
+  ATTN_ERR_ARCH = 8,       /* the current device is not an sm_103 GPU, or no device */
+  ATTN_ERR_CUDA = 9,       /* a CUDA runtime/driver call failed (see attn_last_cuda_error) */
+  ATTN_ERR_TIMEOUT = 10,   /* device side: a bounded wait inside a kernel gave up */
+  ATTN_ERR_VALID_LEN = 11, /* device side: a valid_len value was outside [0, L] and was clamped */
+  ATTN_ERR_ARG = 12        /* another invalid argument (causal not 0/1, NULL out-pointer, ...) */
+} attn_status_t;
+
+/*
+ * attn_fwd -- the fused attention forward.
+ *
+ * Defined by: the attention formula of wzjinhao.cn section 2.1; the implicit
+ * causal mask (Triton-CUDA Attention page, "Causal Attention": key j is
+ * visible to query i iff j <= i, square and top-left aligned); the padding
+ * mask by per-batch valid length (wzjinhao.cn section 2.2: key j is masked
+ * when j >= valid_len[b]); the GQA/MQA head map h_kv = h_q / (Hq / Hkv) with
+ * integer division (Triton-CUDA Attention page, "GQA" and "MQA"); and the
+ * per-row log-sum-exp that tiny_flash_attn_triton.py stores for the backward
+ * pass, here in natural-log units.
+ *
+ * Arguments (all pointers are DEVICE pointers, owned by the caller):
+ *   q         [B, Hq, L, D] contiguous, dtype elements, 16-byte aligned.
+ *   k, v      [B, Hkv, L, D] contiguous, 16-byte aligned.  Hkv = 1 is
+ *             multi-query attention; its bytes equal a squeezed [B, L, D].
+ *   o         [B, Hq, L, D] contiguous output, dtype, 16-byte aligned.
+ *   lse       [B*Hq, L] row-major fp32 output, natural log:
+ *             lse[(b*Hq + h)*L + i] = log(sum_{j visible} exp(sm_scale * q_i . k_j)).
+ *             NULL skips the store.
+ *   B, Hq, Hkv, L   batch, query heads, key/value heads, sequence length (>= 1).
+ *   D         head dimension: 64 or 128.
+ *   sm_scale  score scale, finite and >= 0 (normally 1/sqrt(D)).
+ *   causal    0 or 1.
+ *   valid_len NULL (no padding mask) or a device array of B int32 values.
+ *             Values outside [0, L] are clamped on the device and reported
+ *             by attn_status as ATTN_ERR_VALID_LEN.
+ *   dtype     ATTN_F16 or ATTN_BF16 (q, k, v and o share it).
+ *   stream    the stream the work is queued on.
+ *
+ * A query row with no visible key (valid_len[b] == 0) gets O = 0 and
+ * LSE = -inf (wzjinhao.cn section 3.2: such a row outputs 0, never NaN).
+ *
+ * Errors: argument errors are detected on the host before anything is
+ * queued and returned immediately (nothing is written).  The call never
+ * synchronises; device-side conditions (ATTN_ERR_TIMEOUT, ATTN_ERR_VALID_LEN)
+ * are recorded in a per-device status word and reported by attn_status.
+ * The library allocates no per-call device memory: the only device memory it
+ * owns is that status word (one int per device, allocated on first use).
+ */
+attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                       int B, int Hq, int Hkv, int L, int D, float sm_scale, int causal,
+                       const int32_t* valid_len, attn_dtype_t dtype, attn_stream_t stream);
+
+/*
+ * attn_fwd_simt -- the same operation, same arguments and same contract as
+ * attn_fwd, computed by a plain SIMT kernel (one warp per query row, fp32
+ * FMA dot products, online softmax over 32-key blocks; no tensor cores).
+ * It is a slow cross-check of attn_fwd, not the fast path.  D must be 64 or
+ * 128.
+ */
+attn_status_t attn_fwd_simt(const void* q, const void* k, const void* v, void* o, float* lse,
+                            int B, int Hq, int Hkv, int L, int D, float sm_scale, int causal,
+                            const int32_t* valid_len, attn_dtype_t dtype, attn_stream_t stream);
+
+/*
+ * attn_status -- synchronise `stream`, then read and clear the device status
+ * word of the current device.  *device_code (may be NULL) receives the raw
+ * word: bit 0 a bounded wait timed out, bit 1 a valid_len value was clamped;
+ * bits 8..15 name the waiting role of the first timeout (1 producer, 2 MMA
+ * issuer, 3 softmax, 4 epilogue).  Returns ATTN_OK, ATTN_ERR_TIMEOUT,
+ * ATTN_ERR_VALID_LEN (timeout wins when both are set) or ATTN_ERR_CUDA when
+ * the synchronisation itself reported an error.
+ */
+attn_status_t attn_status(attn_stream_t stream, int* device_code);
+
+/* Capabilities and launch configuration of attn_fwd for a head dimension. */
+typedef struct {
+  int supported;        /* 1 if attn_fwd accepts this (D, dtype) on the current device */
+  int block_m;          /* query rows per tensor-core tile (TMEM lanes) */
+  int q_tiles_per_cta;  /* query tiles a CTA keeps in flight (ping-pong) */
+  int block_n;          /* keys per K/V tile */
+  int kv_stages;        /* shared-memory ring stages (one K or one V tile each) */
+  int threads;          /* threads per CTA */
+  int smem_bytes;       /* dynamic shared memory per CTA */
+  int tmem_cols;        /* tensor-memory columns allocated per CTA */
+  int num_sms;          /* SMs on the current device (0 without a device) */
+  int lse_natural_log;  /* 1: lse is in natural-log units */
+} attn_caps_t;
+
+/*
+ * attn_query -- fill *out for head dimension D and dtype.  Does not need a
+ * device for the static fields; num_sms is 0 and supported is 0 without an
+ * sm_103 device.  Returns ATTN_ERR_ARG for a NULL out, ATTN_ERR_HEADDIM /
+ * ATTN_ERR_DTYPE for unsupported values (out still describes nothing).
+ */
+attn_status_t attn_query(int D, attn_dtype_t dtype, attn_caps_t* out);
+
+/* A static, human-readable description of a status code. */
+const char* attn_strerror(attn_status_t status);
+
+/* The CUDA error code (cudaError_t as int) of the most recent ATTN_ERR_CUDA
+ * returned on this thread, or 0. */
+int attn_last_cuda_error(void);
+
+/* Free the per-device status words.  Optional, at process exit; attn_fwd
+ * may be called again afterwards (they are re-allocated). */
+void attn_shutdown(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_GB300_ATTN_H */

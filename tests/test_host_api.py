@@ -1,0 +1,105 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports
+every function include/attn.h declares, and rejects bad arguments before
+touching a device."""
+import ctypes
+
+import pytest
+
+import attention_forward_attn_gb300 as attn
+from attention_forward_attn_gb300 import binding
+
+A16 = 0x10000  # a 16-byte aligned fake device address (never dereferenced)
+
+
+@pytest.fixture(scope="module")
+def lib(cuda_lib_path):
+    return attn.load()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = attn.declared_symbols()
+    assert {"attn_fwd", "attn_fwd_simt", "attn_status", "attn_query", "attn_strerror",
+            "attn_shutdown", "attn_last_cuda_error"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), "libattn.so does not export %s" % n
+
+
+def _call(**kw):
+    args = dict(q_ptr=A16, k_ptr=A16, v_ptr=A16, o_ptr=A16, lse_ptr=None, B=1, Hq=2, Hkv=1, L=16,
+                D=64, sm_scale=0.125, causal=0, valid_len_ptr=None, dtype=attn.ATTN_BF16,
+                stream=None)
+    args.update(kw)
+    return attn.fwd_raw(**args)
+
+
+@pytest.mark.parametrize("simt", [False, True])
+@pytest.mark.parametrize("kw, expected", [
+    (dict(dtype=7), "ATTN_ERR_DTYPE"),
+    (dict(q_ptr=None), "ATTN_ERR_NULL"),
+    (dict(k_ptr=None), "ATTN_ERR_NULL"),
+    (dict(v_ptr=None), "ATTN_ERR_NULL"),
+    (dict(o_ptr=None), "ATTN_ERR_NULL"),
+    (dict(B=0), "ATTN_ERR_SHAPE"),
+    (dict(Hq=0), "ATTN_ERR_SHAPE"),
+    (dict(Hkv=0), "ATTN_ERR_SHAPE"),
+    (dict(L=0), "ATTN_ERR_SHAPE"),
+    (dict(L=-5), "ATTN_ERR_SHAPE"),
+    (dict(B=1 << 12, Hq=1 << 10, Hkv=1, L=1 << 10), "ATTN_ERR_SHAPE"),
+    (dict(D=96), "ATTN_ERR_HEADDIM"),
+    (dict(D=0), "ATTN_ERR_HEADDIM"),
+    (dict(Hq=3, Hkv=2), "ATTN_ERR_HEADS"),
+    (dict(causal=2), "ATTN_ERR_ARG"),
+    (dict(sm_scale=-1.0), "ATTN_ERR_SCALE"),
+    (dict(sm_scale=float("nan")), "ATTN_ERR_SCALE"),
+    (dict(sm_scale=float("inf")), "ATTN_ERR_SCALE"),
+    (dict(q_ptr=A16 + 8), "ATTN_ERR_ALIGN"),
+    (dict(k_ptr=A16 + 2), "ATTN_ERR_ALIGN"),
+    (dict(v_ptr=A16 + 4), "ATTN_ERR_ALIGN"),
+    (dict(o_ptr=A16 + 1), "ATTN_ERR_ALIGN"),
+    (dict(lse_ptr=A16 + 2), "ATTN_ERR_ALIGN"),
+    (dict(valid_len_ptr=A16 + 1), "ATTN_ERR_ALIGN"),
+])
+def test_invalid_arguments_rejected_on_host(lib, kw, expected, simt):
+    st = _call(simt=simt, **kw)
+    assert binding.STATUS_NAMES[st] == expected
+
+
+def test_valid_arguments_need_a_device(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present; covered by the gpu tests")
+    st = _call()
+    assert binding.STATUS_NAMES[st] in ("ATTN_ERR_CUDA", "ATTN_ERR_ARCH")
+
+
+def test_query_static_fields(lib):
+    for D, stages in ((64, 8), (128, 4)):
+        caps = attn.query(D, attn.ATTN_BF16)
+        assert caps["block_m"] == 128 and caps["block_n"] == 128
+        assert caps["q_tiles_per_cta"] == 2 and caps["kv_stages"] == stages
+        assert caps["threads"] == 384 and caps["tmem_cols"] == 512
+        assert 0 < caps["smem_bytes"] <= 232448
+        assert caps["lse_natural_log"] == 1
+    with pytest.raises(attn.AttnError):
+        attn.query(80)
+    with pytest.raises(attn.AttnError):
+        attn.query(64, 5)
+    assert lib.attn_query(64, 0, None) == 12  # NULL out-pointer: ATTN_ERR_ARG
+
+
+def test_strerror_covers_every_status(lib):
+    for code, name in binding.STATUS_NAMES.items():
+        msg = attn.strerror(code)
+        assert msg and msg != "unknown status", name
+    assert attn.strerror(999) == "unknown status"
+
+
+def test_status_and_shutdown_without_device(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    code = ctypes.c_int(-1)
+    st = lib.attn_status(None, ctypes.byref(code))
+    assert binding.STATUS_NAMES[st] == "ATTN_ERR_CUDA"
+    assert code.value == 0
+    attn.shutdown()  # harmless with nothing allocated
