@@ -17,9 +17,9 @@
 //     tile's softmax runs;
 //   * warps 0-3 / 4-7 (softmax, one thread per query row = TMEM lane): load
 //     the S row, mask (only on boundary tiles), row max, ex2.approx, row sum,
-//     write P as 16-bit pairs over the S columns, rescale the O row in TMEM
-//     when the max grew by more than 2^8 (exact after the final division),
-//     and finally O / l -> global memory and the LSE.
+//     write P into TMEM over the S columns, rescale the O row in TMEM when the
+//     max grew by more than 2^8 (exact after the final division), and finally
+//     O / l -> global memory and the LSE.
 // Causal units skip every key tile above the diagonal; padded units skip every
 // key tile at or beyond valid_len[b]; a unit with no visible key writes O = 0
 // and LSE = -inf without touching the tensor core.
@@ -71,11 +71,13 @@ struct Cfg {
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = QT * kQBytes;
   static constexpr int kOffBar = kOffKV + kStages * kKVBytes;
-  static constexpr int kNumBars = 2 * QT + 2 * kStages + 3 * QT + 1;
+  // barrier block: q_full[QT] q_empty[QT] kv_full[S] kv_empty[S] s_full[QT]
+  // p_full[QT] o_full[QT] drain, then the TMEM base word and the abort flag
+  static constexpr int kNumBars = 5 * QT + 2 * kStages + 1;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + slack to align the base to 1 KB
-  // TMEM columns: S_0, S_1 (fp32, BN each; P_t overwrites the first BN/2
-  // columns of S_t as 16-bit pairs), then O_0, O_1 (fp32, D each).
+  // TMEM columns: S_0, S_1 (fp32, BN each; P_t is written over S_t), then
+  // O_0, O_1 (fp32, D each).
   static __device__ __forceinline__ uint32_t col_s(int t) { return static_cast<uint32_t>(t * BN); }
   static __device__ __forceinline__ uint32_t col_o(int t) {
     return static_cast<uint32_t>(2 * BN + t * D);
@@ -83,6 +85,24 @@ struct Cfg {
   static constexpr uint32_t kTmemCols = 512;
   static_assert(2 * BN + 2 * D <= 512, "TMEM budget");
   static_assert(kSmemBytes <= 232448, "shared-memory budget");
+};
+
+// Shared-memory addresses of the barriers (32-bit, one base + constants).
+template <int S>
+struct Bars {
+  uint32_t base;
+  __device__ __forceinline__ uint32_t q_full(int t) const { return base + 8u * t; }
+  __device__ __forceinline__ uint32_t q_empty(int t) const { return base + 8u * (QT + t); }
+  __device__ __forceinline__ uint32_t kv_full(uint32_t s) const { return base + 8u * (2 * QT + s); }
+  __device__ __forceinline__ uint32_t kv_empty(uint32_t s) const {
+    return base + 8u * (2 * QT + S + s);
+  }
+  __device__ __forceinline__ uint32_t s_full(int t) const { return base + 8u * (2 * QT + 2 * S + t); }
+  __device__ __forceinline__ uint32_t p_full(int t) const { return base + 8u * (3 * QT + 2 * S + t); }
+  __device__ __forceinline__ uint32_t o_full(int t) const { return base + 8u * (4 * QT + 2 * S + t); }
+  __device__ __forceinline__ uint32_t drain() const { return base + 8u * (5 * QT + 2 * S); }
+  __device__ __forceinline__ uint32_t tmem_word() const { return base + 8u * (5 * QT + 2 * S + 1); }
+  __device__ __forceinline__ uint32_t abort_word() const { return tmem_word() + 4u; }
 };
 
 struct KParams {
@@ -104,7 +124,15 @@ struct Unit {
 
 // Units are ordered so that causal work runs heaviest-first (last row blocks
 // first) with heads innermost (query heads of one KV group are adjacent, so
-// their K/V stay in L2), and non-causal work runs head by head.
+// their K/V stay in L2), and non-causal work runs head by head.  CTA c takes
+// the unit of round r at position c (r even) or gridDim.x-1-c (r odd): this
+// "snake" keeps per-CTA totals within a few percent on heaviest-first lists.
+__device__ __forceinline__ int unit_of(int round) {
+  const int g = static_cast<int>(gridDim.x);
+  const int c = static_cast<int>(blockIdx.x);
+  return round * g + ((round & 1) ? (g - 1 - c) : c);
+}
+
 __device__ __forceinline__ Unit decode_unit(const KParams& p, int u) {
   Unit w;
   const int BH = p.B * p.Hq;
@@ -138,40 +166,31 @@ __device__ __forceinline__ Unit decode_unit(const KParams& p, int u) {
   return w;
 }
 
-struct Sync {
-  uint64_t* q_full;    // [QT]  TMA -> MMA
-  uint64_t* q_empty;   // [QT]  softmax (all S MMAs of the tile done) -> producer
-  uint64_t* kv_full;   // [S]   TMA -> MMA
-  uint64_t* kv_empty;  // [S]   MMA commit -> producer
-  uint64_t* s_full;    // [QT]  MMA commit -> softmax
-  uint64_t* p_full;    // [QT]  softmax (P written, O rescaled) -> MMA
-  uint64_t* o_full;    // [QT]  MMA commit after the tile's last PV -> softmax
-  uint64_t* drain;     // [1]
-  volatile uint32_t* abort_flag;
-  int* status;
-};
-
 // Bounded mbarrier wait.  False: timed out (recorded) or another role aborted.
 // (Everything is inlined: out-of-line calls do not mix with setmaxnreg.)
-__device__ __forceinline__ bool wait_bar_slow(const Sync& sy, uint64_t* bar, uint32_t parity,
-                                           int role) {
+template <int S>
+__device__ __forceinline__ bool wait_bar(const Bars<S>& br, int* status, uint32_t bar,
+                                         uint32_t parity, int role) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer_ns();
   for (;;) {
 #pragma unroll 1
     for (int i = 0; i < 16; ++i)
       if (ptx::mbar_try_wait(bar, parity)) return true;
-    if (*sy.abort_flag) return false;
+    if (ptx::ld_shared_volatile(br.abort_word()) != 0u) return false;
     if (ptx::globaltimer_ns() - t0 > ATTN_WAIT_LIMIT_NS) {
-      *sy.abort_flag = 1u;
-      atomicOr(sy.status, kStatusTimeout | role);
+      ptx::st_shared_volatile(br.abort_word(), 1u);
+      atomicOr(status, kStatusTimeout | role);
       return false;
     }
   }
 }
 
-__device__ __forceinline__ bool wait_bar(const Sync& sy, uint64_t* bar, uint32_t parity, int role) {
-  if (ptx::mbar_try_wait(bar, parity)) return true;
-  return wait_bar_slow(sy, bar, parity, role);
+// Wait with a time limit and no abort check (used only to drain in-flight work).
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (!ptx::mbar_try_wait(bar, parity) && ptx::globaltimer_ns() - t0 < ATTN_WAIT_LIMIT_NS) {
+  }
 }
 
 template <bool BF16>
@@ -188,21 +207,23 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 // ------------------------------------------------------------------ producer
 
 template <int D>
-__device__ void producer_role(const KParams& p, const Sync& sy, uint8_t* smem,
+__device__ void producer_role(const KParams& p, const Bars<Cfg<D>::kStages>& br, uint32_t smem,
                               const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                               const CUtensorMap* tm_v) {
   using C = Cfg<D>;
-  uint32_t q_phase[QT] = {0, 0};
+  uint32_t q_phase = 0;     // bit t: parity of tile t's next q_empty wait ^ 1
+  uint32_t q_used = 0;      // bit t: a Q_t load was issued
+  uint32_t stage_used = 0;  // bit s: stage s received a load
+  uint32_t stage_par = 0;   // bit s: phase parity of the last load into stage s
   uint32_t it = 0;
-  int last_stage_parity[C::kStages];
-#pragma unroll
-  for (int s = 0; s < C::kStages; ++s) last_stage_parity[s] = -1;
-  bool q_used[QT] = {false, false};
   const uint64_t pol_keep = ptx::policy_evict_last();
   const uint64_t pol_stream = ptx::policy_evict_first();
   bool ok = true;
 
-  for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+  const int rounds = (p.n_units + gridDim.x - 1) / gridDim.x;
+  for (int r = 0; ok && r < rounds; ++r) {
+    const int u = unit_of(r);
+    if (u >= p.n_units) continue;
     const Unit w = decode_unit(p, u);
     const int n = max(w.n[0], w.n[1]);
     if (n == 0) continue;
@@ -210,14 +231,17 @@ __device__ void producer_role(const KParams& p, const Sync& sy, uint8_t* smem,
 #pragma unroll
     for (int t = 0; t < QT; ++t) {
       if (w.n[t] == 0) continue;
-      if (!wait_bar(sy, &sy.q_empty[t], q_phase[t] ^ 1u, kRoleProducer)) { ok = false; break; }
-      q_phase[t] ^= 1u;
-      q_used[t] = true;
-      uint8_t* dst = smem + C::kOffQ + t * C::kQBytes;
-      ptx::mbar_arrive_expect_tx(&sy.q_full[t], C::kQBytes);
+      if (!wait_bar(br, p.status, br.q_empty(t), ((q_phase >> t) & 1u) ^ 1u, kRoleProducer)) {
+        ok = false;
+        break;
+      }
+      q_phase ^= 1u << t;
+      q_used |= 1u << t;
+      const uint32_t dst = smem + C::kOffQ + t * C::kQBytes;
+      ptx::mbar_arrive_expect_tx(br.q_full(t), C::kQBytes);
 #pragma unroll
       for (int h = 0; h < C::kHalves; ++h)
-        ptx::tma_load_3d_hint(dst + h * C::kSlabQ, tm_q, &sy.q_full[t], h * 64, w.m0 + t * BM,
+        ptx::tma_load_3d_hint(dst + h * C::kSlabQ, tm_q, br.q_full(t), h * 64, w.m0 + t * BM,
                               w.bh, pol_stream);
     }
     for (int j = 0; ok && j < n; ++j) {
@@ -225,35 +249,29 @@ __device__ void producer_role(const KParams& p, const Sync& sy, uint8_t* smem,
       for (int kind = 0; kind < 2; ++kind) {
         const uint32_t s = it % C::kStages;
         const uint32_t par = (it / C::kStages) & 1u;
-        if (!wait_bar(sy, &sy.kv_empty[s], par ^ 1u, kRoleProducer)) { ok = false; break; }
+        if (!wait_bar(br, p.status, br.kv_empty(s), par ^ 1u, kRoleProducer)) {
+          ok = false;
+          break;
+        }
         ++it;
-        uint8_t* dst = smem + C::kOffKV + s * C::kKVBytes;
-        ptx::mbar_arrive_expect_tx(&sy.kv_full[s], C::kKVBytes);
+        const uint32_t dst = smem + C::kOffKV + s * C::kKVBytes;
+        ptx::mbar_arrive_expect_tx(br.kv_full(s), C::kKVBytes);
         const CUtensorMap* tm = kind == 0 ? tm_k : tm_v;
 #pragma unroll
         for (int h = 0; h < C::kHalves; ++h)
-          ptx::tma_load_3d_hint(dst + h * C::kSlabKV, tm, &sy.kv_full[s], h * 64, j * BN, z_kv,
+          ptx::tma_load_3d_hint(dst + h * C::kSlabKV, tm, br.kv_full(s), h * 64, j * BN, z_kv,
                                 pol_keep);
-        last_stage_parity[s] = static_cast<int>(par);
+        stage_used |= 1u << s;
+        stage_par = (stage_par & ~(1u << s)) | (par << s);
       }
     }
   }
   // Never leave with a copy in flight: wait (bounded) for the last load of
   // every buffer.  In a normal run these phases completed long ago.
   for (int s = 0; s < C::kStages; ++s)
-    if (last_stage_parity[s] >= 0) {
-      const uint64_t t0 = ptx::globaltimer_ns();
-      while (!ptx::mbar_try_wait(&sy.kv_full[s], static_cast<uint32_t>(last_stage_parity[s])) &&
-             ptx::globaltimer_ns() - t0 < ATTN_WAIT_LIMIT_NS) {
-      }
-    }
+    if ((stage_used >> s) & 1u) drain_wait(br.kv_full(s), (stage_par >> s) & 1u);
   for (int t = 0; t < QT; ++t)
-    if (q_used[t]) {
-      const uint64_t t0 = ptx::globaltimer_ns();
-      while (!ptx::mbar_try_wait(&sy.q_full[t], q_phase[t] ^ 1u) &&
-             ptx::globaltimer_ns() - t0 < ATTN_WAIT_LIMIT_NS) {
-      }
-    }
+    if ((q_used >> t) & 1u) drain_wait(br.q_full(t), ((q_phase >> t) & 1u) ^ 1u);
 }
 
 // ------------------------------------------------------------------ MMA issuer
@@ -270,7 +288,7 @@ template <int D, bool BF16>
 __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t q_desc, uint64_t k_desc) {
   using C = Cfg<D>;
   constexpr uint32_t idesc = ptx::idesc_f16(BM, BN, BF16, false);
-#pragma unroll
+#pragma unroll 1
   for (int kk = 0; kk < D / 16; ++kk) {
     const uint32_t off = (kk & 3) * 32u;
     ptx::mma_ss(d_tmem, desc_add(q_desc, (kk / 4) * C::kSlabQ + off),
@@ -280,44 +298,57 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t q_desc, uint6
 
 // O += P V: A = P from TMEM (16-bit pairs, 8 columns per 16 keys), B = V tile
 // as an MN-major 128-byte-swizzled operand (16 keys = two 8-row groups).
+// bf16: O += [P_hi | P_lo] [V; V], the same V tile read twice.
 template <int D, bool BF16>
 __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint64_t v_desc,
                                          bool accumulate) {
   constexpr uint32_t idesc = ptx::idesc_f16(BM, D, BF16, true);
-#pragma unroll
+#pragma unroll 1
   for (int kk = 0; kk < BN / 16; ++kk)
     ptx::mma_ts(d_tmem, p_tmem + kk * 8u, desc_add(v_desc, kk * 2048u), idesc,
                 (accumulate || kk > 0) ? 1u : 0u);
+  if constexpr (BF16) {
+#pragma unroll 1
+    for (int kk = 0; kk < BN / 16; ++kk)
+      ptx::mma_ts(d_tmem, p_tmem + BN / 2 + kk * 8u, desc_add(v_desc, kk * 2048u), idesc, 1u);
+  }
 }
 
 template <int D, bool BF16>
-__device__ void mma_role(const KParams& p, const Sync& sy, uint8_t* smem, uint32_t tmem) {
+__device__ void mma_role(const KParams& p, const Bars<Cfg<D>::kStages>& br, uint32_t smem,
+                         uint32_t tmem) {
   using C = Cfg<D>;
-  uint32_t q_phase[QT] = {0, 0};
-  uint32_t p_phase[QT] = {0, 0};
+  uint32_t q_phase = 0;  // bit t: parity of tile t's next q_full wait
+  uint32_t p_phase = 0;  // bit t: parity of tile t's next p_full wait
   uint32_t it = 0;
   // K-major operands (Q, K): leading byte offset unused with 128-byte swizzle,
   // 1024 bytes between 8-row groups.  MN-major V: 64-column slabs kSlabKV
   // apart (leading), 1024 bytes between 8-key groups (stride).
-  const uint64_t q_desc0 = ptx::sdesc_sw128(ptx::smem_u32(smem + C::kOffQ), 16, 1024);
-  const uint64_t k_desc0 = ptx::sdesc_sw128(ptx::smem_u32(smem + C::kOffKV), 16, 1024);
-  const uint64_t v_desc0 = ptx::sdesc_sw128(ptx::smem_u32(smem + C::kOffKV), C::kSlabKV, 1024);
+  const uint64_t q_desc0 = ptx::sdesc_sw128(smem + C::kOffQ, 16, 1024);
+  const uint64_t k_desc0 = ptx::sdesc_sw128(smem + C::kOffKV, 16, 1024);
+  const uint64_t v_desc0 = ptx::sdesc_sw128(smem + C::kOffKV, C::kSlabKV, 1024);
   bool ok = true;
 
-  for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+  const int rounds = (p.n_units + gridDim.x - 1) / gridDim.x;
+  for (int r = 0; ok && r < rounds; ++r) {
+    const int u = unit_of(r);
+    if (u >= p.n_units) continue;
     const Unit w = decode_unit(p, u);
     const int n = max(w.n[0], w.n[1]);
     if (n == 0) continue;
 #pragma unroll
     for (int t = 0; t < QT; ++t) {
       if (w.n[t] == 0) continue;
-      if (!wait_bar(sy, &sy.q_full[t], q_phase[t], kRoleMma)) { ok = false; break; }
-      q_phase[t] ^= 1u;
+      if (!wait_bar(br, p.status, br.q_full(t), (q_phase >> t) & 1u, kRoleMma)) {
+        ok = false;
+        break;
+      }
+      q_phase ^= 1u << t;
     }
     if (!ok) break;
     // K_0
-    uint32_t sk = it % C::kStages;
-    if (!wait_bar(sy, &sy.kv_full[sk], (it / C::kStages) & 1u, kRoleMma)) break;
+    const uint32_t sk = it % C::kStages;
+    if (!wait_bar(br, p.status, br.kv_full(sk), (it / C::kStages) & 1u, kRoleMma)) break;
     ++it;
     ptx::tc_fence_after();
 #pragma unroll
@@ -325,13 +356,16 @@ __device__ void mma_role(const KParams& p, const Sync& sy, uint8_t* smem, uint32
       if (w.n[t] > 0) {
         issue_qk<D, BF16>(tmem + C::col_s(t), desc_add(q_desc0, t * C::kQBytes),
                           desc_add(k_desc0, sk * C::kKVBytes));
-        ptx::mma_commit(&sy.s_full[t]);
+        ptx::mma_commit(br.s_full(t));
       }
-    ptx::mma_commit(&sy.kv_empty[sk]);
+    ptx::mma_commit(br.kv_empty(sk));
 
     for (int j = 0; j < n; ++j) {
       const uint32_t sv = it % C::kStages;
-      if (!wait_bar(sy, &sy.kv_full[sv], (it / C::kStages) & 1u, kRoleMma)) { ok = false; break; }
+      if (!wait_bar(br, p.status, br.kv_full(sv), (it / C::kStages) & 1u, kRoleMma)) {
+        ok = false;
+        break;
+      }
       ++it;
       const bool has_next = j + 1 < n;
       uint32_t sk2 = 0;
@@ -339,17 +373,20 @@ __device__ void mma_role(const KParams& p, const Sync& sy, uint8_t* smem, uint32
 #pragma unroll
       for (int t = 0; t < QT; ++t) {
         if (j < w.n[t]) {
-          if (!wait_bar(sy, &sy.p_full[t], p_phase[t], kRoleMma)) { ok = false; break; }
-          p_phase[t] ^= 1u;
+          if (!wait_bar(br, p.status, br.p_full(t), (p_phase >> t) & 1u, kRoleMma)) {
+            ok = false;
+            break;
+          }
+          p_phase ^= 1u << t;
           ptx::tc_fence_after();
           issue_pv<D, BF16>(tmem + C::col_o(t), tmem + C::col_s(t),
                             desc_add(v_desc0, sv * C::kKVBytes), j > 0);
-          if (j == w.n[t] - 1) ptx::mma_commit(&sy.o_full[t]);
+          if (j == w.n[t] - 1) ptx::mma_commit(br.o_full(t));
         }
-        if (t == QT - 1) ptx::mma_commit(&sy.kv_empty[sv]);  // V_j read by every PV above
+        if (t == QT - 1) ptx::mma_commit(br.kv_empty(sv));  // V_j read by every PV above
         if (has_next && !next_loaded) {
           sk2 = it % C::kStages;
-          if (!wait_bar(sy, &sy.kv_full[sk2], (it / C::kStages) & 1u, kRoleMma)) {
+          if (!wait_bar(br, p.status, br.kv_full(sk2), (it / C::kStages) & 1u, kRoleMma)) {
             ok = false;
             break;
           }
@@ -360,24 +397,23 @@ __device__ void mma_role(const KParams& p, const Sync& sy, uint8_t* smem, uint32
         if (j + 1 < w.n[t]) {
           issue_qk<D, BF16>(tmem + C::col_s(t), desc_add(q_desc0, t * C::kQBytes),
                             desc_add(k_desc0, sk2 * C::kKVBytes));
-          ptx::mma_commit(&sy.s_full[t]);
+          ptx::mma_commit(br.s_full(t));
         }
       }
       if (!ok) break;
-      if (has_next) ptx::mma_commit(&sy.kv_empty[sk2]);
+      if (has_next) ptx::mma_commit(br.kv_empty(sk2));
     }
   }
   // Every MMA issued by this thread completes before TMEM is released.
-  ptx::mma_commit(sy.drain);
-  const uint64_t t0 = ptx::globaltimer_ns();
-  while (!ptx::mbar_try_wait(sy.drain, 0) && ptx::globaltimer_ns() - t0 < ATTN_WAIT_LIMIT_NS) {
-  }
+  ptx::mma_commit(br.drain());
+  drain_wait(br.drain(), 0);
 }
 
 // ------------------------------------------------------------------ softmax + epilogue
 
 template <int D, bool BF16>
-__device__ void softmax_role(const KParams& p, const Sync& sy, uint32_t tmem, int t) {
+__device__ void softmax_role(const KParams& p, const Bars<Cfg<D>::kStages>& br, uint32_t tmem,
+                             int t) {
   using C = Cfg<D>;
   const int lane_row = threadIdx.x & 127;           // row within the tile = TMEM lane
   const uint32_t quad = (threadIdx.x >> 5) & 3u;    // this warp's 32-lane TMEM quadrant
@@ -386,7 +422,10 @@ __device__ void softmax_role(const KParams& p, const Sync& sy, uint32_t tmem, in
   const float scale_log2 = p.scale_log2;
   uint32_t s_phase = 0, o_phase = 0;
 
-  for (int u = blockIdx.x; u < p.n_units; u += gridDim.x) {
+  const int rounds = (p.n_units + gridDim.x - 1) / gridDim.x;
+  for (int r = 0; r < rounds; ++r) {
+    const int u = unit_of(r);
+    if (u >= p.n_units) continue;
     const Unit w = decode_unit(p, u);
     const int r0 = w.m0 + t * BM;
     if (r0 >= p.L) continue;
@@ -413,8 +452,11 @@ __device__ void softmax_role(const KParams& p, const Sync& sy, uint32_t tmem, in
     float l = 0.f;
     bool ok = true;
     for (int j = 0; j < nt; ++j) {
-      ok = wait_bar(sy, &sy.s_full[t], s_phase, kRoleSoftmax);
-      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      ok = wait_bar(br, p.status, br.s_full(t), s_phase, kRoleSoftmax);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
       s_phase ^= 1u;
       ptx::tc_fence_after();
       uint32_t s[BN];
@@ -426,10 +468,8 @@ __device__ void softmax_role(const KParams& p, const Sync& sy, uint32_t tmem, in
       float mx = -INFINITY;
       if (masked) {
 #pragma unroll
-        for (int c = 0; c < BN; ++c) {
-          const float x = (c < c_lim) ? __uint_as_float(s[c]) : -INFINITY;
-          mx = fmaxf(mx, x);
-        }
+        for (int c = 0; c < BN; ++c)
+          mx = fmaxf(mx, (c < c_lim) ? __uint_as_float(s[c]) : -INFINITY);
       } else {
 #pragma unroll
         for (int c = 0; c < BN; ++c) mx = fmaxf(mx, __uint_as_float(s[c]));
@@ -445,14 +485,19 @@ __device__ void softmax_role(const KParams& p, const Sync& sy, uint32_t tmem, in
       }
       const float neg_m = (m == -INFINITY) ? 0.f : -m;
       float rowsum = 0.f;
-      // P as 16-bit pairs over the first BN/2 columns of S, written one half
-      // at a time (S columns still to be read lie beyond what is written)
+      // P over the S columns, 32 keys at a time (every S value is already in
+      // registers).  fp16: P rounded to fp16 in columns [0, 64).  bf16:
+      // P = P_hi + P_lo with P_hi = p truncated to bf16 (columns [0, 64)) and
+      // P_lo = bf16(p - P_hi) (columns [64, 128)); a single bf16 P (unit
+      // roundoff 2^-8) is too coarse for rows dominated by a few keys, the
+      // pair leaves a relative error below 2^-15.
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t pk[BN / 4];
+      for (int qtr = 0; qtr < 4; ++qtr) {
+        uint32_t hi[16];
+        uint32_t lo[BF16 ? 16 : 1];
 #pragma unroll
-        for (int i = 0; i < BN / 4; ++i) {
-          const int c = half * (BN / 2) + 2 * i;
+        for (int i = 0; i < 16; ++i) {
+          const int c = qtr * 32 + 2 * i;
           float p0 = ptx::ex2_approx(fmaf(__uint_as_float(s[c]), scale_log2, neg_m));
           float p1 = ptx::ex2_approx(fmaf(__uint_as_float(s[c + 1]), scale_log2, neg_m));
           if (masked) {
@@ -460,9 +505,17 @@ __device__ void softmax_role(const KParams& p, const Sync& sy, uint32_t tmem, in
             p1 = (c + 1 < c_lim) ? p1 : 0.f;
           }
           rowsum += p0 + p1;
-          pk[i] = pack2<BF16>(p0, p1);
+          if constexpr (BF16) {
+            const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
+            hi[i] = __byte_perm(b0, b1, 0x7632);  // upper halves: truncated bf16 pair
+            lo[i] = pack2<true>(p0 - __uint_as_float(b0 & 0xFFFF0000u),
+                                p1 - __uint_as_float(b1 & 0xFFFF0000u));
+          } else {
+            hi[i] = pack2<false>(p0, p1);
+          }
         }
-        ptx::tmem_st32(t_s + half * 32, pk);
+        ptx::tmem_st16(t_s + qtr * 16, hi);
+        if constexpr (BF16) ptx::tmem_st16(t_s + BN / 2 + qtr * 16, lo);
       }
       l = l * alpha + rowsum;
       // O was accumulated against the old max: rescale it before PV_j runs.
@@ -479,15 +532,15 @@ __device__ void softmax_role(const KParams& p, const Sync& sy, uint32_t tmem, in
       }
       ptx::tmem_st_wait();
       ptx::tc_fence_before();
-      ptx::mbar_arrive(&sy.p_full[t]);
+      ptx::mbar_arrive(br.p_full(t));
     }
     if (!ok) return;
     // epilogue
-    ok = wait_bar(sy, &sy.o_full[t], o_phase, kRoleEpilogue);
+    ok = wait_bar(br, p.status, br.o_full(t), o_phase, kRoleEpilogue);
     if (!__all_sync(0xffffffffu, ok)) return;
     o_phase ^= 1u;
     ptx::tc_fence_after();
-    ptx::mbar_arrive(&sy.q_empty[t]);  // every S MMA of this tile is done: Q_t is free
+    ptx::mbar_arrive(br.q_empty(t));  // every S MMA of this tile is done: Q_t is free
     const float inv_l = 1.f / l;
 #pragma unroll 1
     for (int c0 = 0; c0 < D; c0 += 32) {
@@ -516,39 +569,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const __grid_constant__ CUtensorMap tm_v, const KParams p) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
-  Sync sy;
-  sy.q_full = bars;
-  sy.q_empty = sy.q_full + QT;
-  sy.kv_full = sy.q_empty + QT;
-  sy.kv_empty = sy.kv_full + C::kStages;
-  sy.s_full = sy.kv_empty + C::kStages;
-  sy.p_full = sy.s_full + QT;
-  sy.o_full = sy.p_full + QT;
-  sy.drain = sy.o_full + QT;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
-  sy.abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::kOffMisc + 4);
-  sy.status = p.status;
+  const uint32_t smem = (ptx::smem_u32(smem_raw) + 1023u) & ~1023u;
+  const Bars<C::kStages> br{smem + C::kOffBar};
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
     for (int t = 0; t < QT; ++t) {
-      ptx::mbar_init(&sy.q_full[t], 1);
-      ptx::mbar_init(&sy.q_empty[t], BM);
-      ptx::mbar_init(&sy.s_full[t], 1);
-      ptx::mbar_init(&sy.p_full[t], BM);
-      ptx::mbar_init(&sy.o_full[t], 1);
+      ptx::mbar_init(br.q_full(t), 1);
+      ptx::mbar_init(br.q_empty(t), BM);
+      ptx::mbar_init(br.s_full(t), 1);
+      ptx::mbar_init(br.p_full(t), BM);
+      ptx::mbar_init(br.o_full(t), 1);
     }
     for (int s = 0; s < C::kStages; ++s) {
-      ptx::mbar_init(&sy.kv_full[s], 1);
-      ptx::mbar_init(&sy.kv_empty[s], 1);
+      ptx::mbar_init(br.kv_full(s), 1);
+      ptx::mbar_init(br.kv_empty(s), 1);
     }
-    ptx::mbar_init(sy.drain, 1);
-    *sy.abort_flag = 0u;
+    ptx::mbar_init(br.drain(), 1);
+    ptx::st_shared_volatile(br.abort_word(), 0u);
     ptx::fence_barrier_init();
   }
   if (warp == kProducerWarp && lane == 0) {
@@ -557,24 +597,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::prefetch_tensormap(&tm_v);
   }
   if (warp == kMmaWarp) {
-    ptx::tmem_alloc(tmem_holder, C::kTmemCols);
+    ptx::tmem_alloc(br.tmem_word(), C::kTmemCols);
     ptx::tmem_relinquish();
   }
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
-  const uint32_t tmem = *tmem_holder;
+  const uint32_t tmem = ptx::ld_shared_volatile(br.tmem_word());
 
   if (warp >= 8) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kControlRegs));
     if (warp == kProducerWarp) {
-      if (lane == 0) producer_role<D>(p, sy, smem, &tm_q, &tm_k, &tm_v);
+      if (lane == 0) producer_role<D>(p, br, smem, &tm_q, &tm_k, &tm_v);
     } else if (warp == kMmaWarp) {
-      if (lane == 0) mma_role<D, BF16>(p, sy, smem, tmem);
+      if (lane == 0) mma_role<D, BF16>(p, br, smem, tmem);
     }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
-    softmax_role<D, BF16>(p, sy, tmem, warp >> 2);
+    softmax_role<D, BF16>(p, br, tmem, warp >> 2);
   }
 
   ptx::tc_fence_before();
