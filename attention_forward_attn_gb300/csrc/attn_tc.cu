@@ -357,6 +357,9 @@ __device__ void mma_role(const KParams& p, const Bars<Cfg<D>::kStages>& br, uint
         issue_qk<D, BF16>(tmem + C::col_s(t), desc_add(q_desc0, t * C::kQBytes),
                           desc_add(k_desc0, sk * C::kKVBytes));
         ptx::mma_commit(br.s_full(t));
+        // Q_t is free once the unit's last S_t MMA completes: the producer can
+        // load the next unit's Q_t while this unit finishes
+        if (w.n[t] == 1) ptx::mma_commit(br.q_empty(t));
       }
     ptx::mma_commit(br.kv_empty(sk));
 
@@ -398,6 +401,7 @@ __device__ void mma_role(const KParams& p, const Bars<Cfg<D>::kStages>& br, uint
           issue_qk<D, BF16>(tmem + C::col_s(t), desc_add(q_desc0, t * C::kQBytes),
                             desc_add(k_desc0, sk2 * C::kKVBytes));
           ptx::mma_commit(br.s_full(t));
+          if (j + 2 == w.n[t]) ptx::mma_commit(br.q_empty(t));  // last S_t of the unit
         }
       }
       if (!ok) break;
@@ -460,20 +464,24 @@ __device__ void softmax_role(const KParams& p, const Bars<Cfg<D>::kStages>& br, 
       s_phase ^= 1u;
       ptx::tc_fence_after();
       uint32_t s[BN];
-      ptx::tmem_ld64(t_s, *reinterpret_cast<uint32_t(*)[64]>(&s[0]));
-      ptx::tmem_ld64(t_s + 64, *reinterpret_cast<uint32_t(*)[64]>(&s[64]));
+      ptx::tmem_ld128(t_s, s);
       const int n0 = j * BN;
       const bool masked = (n0 + BN > w.kv_len) || (p.causal && n0 + BN - 1 > r0);
       const int c_lim = key_lim - n0;  // columns c < c_lim are visible
-      float mx = -INFINITY;
+      // row max with 8 independent chains (a single chain is 128 dependent ops)
+      float mxk[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mxk[k] = -INFINITY;
       if (masked) {
 #pragma unroll
         for (int c = 0; c < BN; ++c)
-          mx = fmaxf(mx, (c < c_lim) ? __uint_as_float(s[c]) : -INFINITY);
+          mxk[c & 7] = fmaxf(mxk[c & 7], (c < c_lim) ? __uint_as_float(s[c]) : -INFINITY);
       } else {
 #pragma unroll
-        for (int c = 0; c < BN; ++c) mx = fmaxf(mx, __uint_as_float(s[c]));
+        for (int c = 0; c < BN; ++c) mxk[c & 7] = fmaxf(mxk[c & 7], __uint_as_float(s[c]));
       }
+      const float mx = fmaxf(fmaxf(fmaxf(mxk[0], mxk[1]), fmaxf(mxk[2], mxk[3])),
+                             fmaxf(fmaxf(mxk[4], mxk[5]), fmaxf(mxk[6], mxk[7])));
       const float m_tile = (mx == -INFINITY) ? -INFINITY : mx * scale_log2;
       const float m_new = fmaxf(m, m_tile);
       float alpha = 1.f;
@@ -484,7 +492,7 @@ __device__ void softmax_role(const KParams& p, const Bars<Cfg<D>::kStages>& br, 
         rescale = true;
       }
       const float neg_m = (m == -INFINITY) ? 0.f : -m;
-      float rowsum = 0.f;
+      float rsum[4] = {0.f, 0.f, 0.f, 0.f};  // independent partial row sums
       // P over the S columns, 32 keys at a time (every S value is already in
       // registers).  fp16: P rounded to fp16 in columns [0, 64).  bf16:
       // P = P_hi + P_lo with P_hi = p truncated to bf16 (columns [0, 64)) and
@@ -504,7 +512,7 @@ __device__ void softmax_role(const KParams& p, const Bars<Cfg<D>::kStages>& br, 
             p0 = (c < c_lim) ? p0 : 0.f;
             p1 = (c + 1 < c_lim) ? p1 : 0.f;
           }
-          rowsum += p0 + p1;
+          rsum[i & 3] += p0 + p1;
           if constexpr (BF16) {
             const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
             hi[i] = __byte_perm(b0, b1, 0x7632);  // upper halves: truncated bf16 pair
@@ -517,7 +525,7 @@ __device__ void softmax_role(const KParams& p, const Bars<Cfg<D>::kStages>& br, 
         ptx::tmem_st16(t_s + qtr * 16, hi);
         if constexpr (BF16) ptx::tmem_st16(t_s + BN / 2 + qtr * 16, lo);
       }
-      l = l * alpha + rowsum;
+      l = l * alpha + ((rsum[0] + rsum[1]) + (rsum[2] + rsum[3]));
       // O was accumulated against the old max: rescale it before PV_j runs.
       // PV_{j-1} is complete: the commit that signalled S_j came after it.
       if (j > 0 && __any_sync(0xffffffffu, rescale)) {
@@ -540,7 +548,6 @@ __device__ void softmax_role(const KParams& p, const Bars<Cfg<D>::kStages>& br, 
     if (!__all_sync(0xffffffffu, ok)) return;
     o_phase ^= 1u;
     ptx::tc_fence_after();
-    ptx::mbar_arrive(br.q_empty(t));  // every S MMA of this tile is done: Q_t is free
     const float inv_l = 1.f / l;
 #pragma unroll 1
     for (int c0 = 0; c0 < D; c0 += 32) {
@@ -578,7 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int t = 0; t < QT; ++t) {
       ptx::mbar_init(br.q_full(t), 1);
-      ptx::mbar_init(br.q_empty(t), BM);
+      ptx::mbar_init(br.q_empty(t), 1);
       ptx::mbar_init(br.s_full(t), 1);
       ptx::mbar_init(br.p_full(t), BM);
       ptx::mbar_init(br.o_full(t), 1);
