@@ -20,7 +20,7 @@ STATUS_NAMES = {
     0: "ATTN_OK", 1: "ATTN_ERR_NULL", 2: "ATTN_ERR_ALIGN", 3: "ATTN_ERR_SHAPE",
     4: "ATTN_ERR_HEADS", 5: "ATTN_ERR_HEADDIM", 6: "ATTN_ERR_DTYPE", 7: "ATTN_ERR_SCALE",
     8: "ATTN_ERR_ARCH", 9: "ATTN_ERR_CUDA", 10: "ATTN_ERR_TIMEOUT", 11: "ATTN_ERR_VALID_LEN",
-    12: "ATTN_ERR_ARG",
+    12: "ATTN_ERR_ARG", 13: "ATTN_ERR_SCRATCH",
 }
 ATTN_OK = 0
 
@@ -68,7 +68,7 @@ def load():
             p = ctypes.c_void_p
             i = ctypes.c_int
             fwd_args = [p, p, p, p, p, i, i, i, i, i, ctypes.c_float, i, p, i, p]
-            for name in ("attn_fwd", "attn_fwd_simt"):
+            for name in ("attn_fwd", "attn_fwd_simt", "attn_fwd_noalloc"):
                 fn = getattr(lib, name)
                 fn.argtypes = fwd_args
                 fn.restype = i
@@ -105,9 +105,13 @@ def last_cuda_error() -> int:
 # ------------------------------------------------------------------ raw C calls
 
 def fwd_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, Hq, Hkv, L, D, sm_scale, causal,
-            valid_len_ptr, dtype, stream, simt=False) -> int:
-    """Call attn_fwd (or attn_fwd_simt) with raw integer pointers; returns the status."""
-    fn = load().attn_fwd_simt if simt else load().attn_fwd
+            valid_len_ptr, dtype, stream, simt=False, entry=None) -> int:
+    """Call attn_fwd (or attn_fwd_simt, or the entry point named by ``entry``)
+    with raw integer pointers; returns the status."""
+    if entry is not None:
+        fn = getattr(load(), entry)
+    else:
+        fn = load().attn_fwd_simt if simt else load().attn_fwd
     return int(fn(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, int(B), int(Hq), int(Hkv), int(L), int(D),
                   float(sm_scale), int(causal), valid_len_ptr, int(dtype), stream))
 

@@ -36,12 +36,16 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn g_encode = nullptr;
 
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+
+namespace attn {
+
 attn_status_t cuda_fail(cudaError_t e) {
   g_last_cuda_error = static_cast<int>(e);
   return ATTN_ERR_CUDA;
 }
-
-bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 // Argument checks that need no device.
 attn_status_t validate(const void* q, const void* k, const void* v, void* o, float* lse, int B,
@@ -62,6 +66,28 @@ attn_status_t validate(const void* q, const void* k, const void* v, void* o, flo
     return ATTN_ERR_ALIGN;
   return ATTN_OK;
 }
+
+// The driver's cuTensorMapEncodeTiled, looked up once (no allocation).
+attn_status_t tensor_map_encoder_ready() {
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_encode == nullptr) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                     cudaEnableDefault, &qr);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (qr != cudaDriverEntryPointSuccess || fn == nullptr) return cuda_fail(cudaErrorNotSupported);
+    g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  }
+  return ATTN_OK;
+}
+
+}  // namespace attn
+
+namespace {
+
+using attn::cuda_fail;
+using attn::validate;
 
 // Per-device probe and status-word allocation (first call on a device only).
 attn_status_t device_state(int* dev_out, DeviceState** st_out) {
@@ -105,6 +131,10 @@ attn_status_t device_state(int* dev_out, DeviceState** st_out) {
   return ATTN_OK;
 }
 
+}  // namespace
+
+namespace attn {
+
 // Tensor map over a contiguous [heads, L, D] 16-bit tensor viewed as 3-D
 // (D innermost), boxes of 64 columns x `rows` rows x 1 head, 128-byte swizzle.
 attn_status_t encode_map(CUtensorMap* map, const void* base, int heads, int L, int D, int rows,
@@ -147,7 +177,10 @@ Problem make_problem(const void* q, const void* k, const void* v, void* o, float
   return p;
 }
 
-}  // namespace
+}  // namespace attn
+
+using attn::encode_map;
+using attn::make_problem;
 
 extern "C" {
 
@@ -204,14 +237,17 @@ attn_status_t attn_status(attn_stream_t stream, int* device_code) {
     std::lock_guard<std::mutex> lock(g_mu);
     word = g_dev[dev].status;
   }
-  if (word == nullptr) return ATTN_OK;  // nothing ever launched on this device
   int code = 0;
-  e = cudaMemcpy(&code, word, sizeof(int), cudaMemcpyDeviceToHost);
-  if (e != cudaSuccess) return cuda_fail(e);
-  if (code != 0) {
-    e = cudaMemset(word, 0, sizeof(int));
+  if (word != nullptr) {
+    e = cudaMemcpy(&code, word, sizeof(int), cudaMemcpyDeviceToHost);
     if (e != cudaSuccess) return cuda_fail(e);
+    if (code != 0) {
+      e = cudaMemset(word, 0, sizeof(int));
+      if (e != cudaSuccess) return cuda_fail(e);
+    }
   }
+  attn_status_t s = attn::noalloc_take_status(dev, &code);
+  if (s != ATTN_OK) return s;
   if (device_code != nullptr) *device_code = code;
   if (code & attn::kStatusTimeout) return ATTN_ERR_TIMEOUT;
   if (code & attn::kStatusValidLenClamped) return ATTN_ERR_VALID_LEN;
@@ -261,6 +297,8 @@ const char* attn_strerror(attn_status_t status) {
     case ATTN_ERR_TIMEOUT: return "a bounded wait inside the kernel timed out";
     case ATTN_ERR_VALID_LEN: return "a valid_len value was outside [0, L] and was clamped";
     case ATTN_ERR_ARG: return "invalid argument";
+    case ATTN_ERR_SCRATCH:
+      return "the call needs more scratch than attn_fwd_noalloc's static array holds";
   }
   return "unknown status";
 }

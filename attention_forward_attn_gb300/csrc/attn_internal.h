@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "../../include/attn.h"
+
 namespace attn {
 
 // Device status word bits (see attn_status in include/attn.h).
@@ -51,5 +53,22 @@ cudaError_t launch_tc(const Problem& p, const CUtensorMap* maps, int num_sms);
 
 // SIMT cross-check forward.
 cudaError_t launch_simt(const Problem& p);
+
+// Host helpers shared by the entry points (attn_api.cu).
+attn_status_t cuda_fail(cudaError_t e);  // records e for attn_last_cuda_error
+attn_status_t validate(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                       int Hq, int Hkv, int L, int D, float sm_scale, int causal,
+                       const int32_t* valid_len, attn_dtype_t dtype);
+attn_status_t tensor_map_encoder_ready();
+attn_status_t encode_map(CUtensorMap* map, const void* base, int heads, int L, int D, int rows,
+                         bool bf16);
+Problem make_problem(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                     int Hq, int Hkv, int L, int D, float sm_scale, int causal,
+                     const int32_t* valid_len, attn_dtype_t dtype, attn_stream_t stream,
+                     int* status);
+
+// attn_noalloc.cu: OR the no-alloc path's status word on `dev` into *code
+// and clear it (a no-op unless attn_fwd_noalloc ran on that device).
+attn_status_t noalloc_take_status(int dev, int* code);
 
 }  // namespace attn

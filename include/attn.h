@@ -48,7 +48,8 @@ typedef enum {
   ATTN_ERR_CUDA = 9,       /* a CUDA runtime/driver call failed (see attn_last_cuda_error) */
   ATTN_ERR_TIMEOUT = 10,   /* device side: a bounded wait inside a kernel gave up */
   ATTN_ERR_VALID_LEN = 11, /* device side: a valid_len value was outside [0, L] and was clamped */
-  ATTN_ERR_ARG = 12        /* another invalid argument (causal not 0/1, NULL out-pointer, ...) */
+  ATTN_ERR_ARG = 12,       /* another invalid argument (causal not 0/1, NULL out-pointer, ...) */
+  ATTN_ERR_SCRATCH = 13    /* attn_fwd_noalloc: the call needs more scratch than its static array holds */
 } attn_status_t;
 
 /*
@@ -105,6 +106,44 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
 attn_status_t attn_fwd_simt(const void* q, const void* k, const void* v, void* o, float* lse,
                             int B, int Hq, int Hkv, int L, int D, float sm_scale, int causal,
                             const int32_t* valid_len, attn_dtype_t dtype, attn_stream_t stream);
+
+/*
+ * attn_fwd_noalloc -- attn_fwd for callers that must not allocate device
+ * memory.  The pages have no counterpart: this is a deployment variant.
+ *
+ * attn_fwd allocates one int of device memory (its device status word) with
+ * cudaMalloc on its first call on a device.  Callers that cannot allow that
+ * -- servers that reserve all device memory at start-up and forbid
+ * allocations on the request path (cudaMalloc can synchronise the device and
+ * stall every other stream); latency-bound loops that cannot afford an
+ * allocation's unpredictable cost; runtimes whose memory accounting covers
+ * only their own allocator -- use this entry point instead.  Same arguments, same layouts, same kernel and
+ * the same results as attn_fwd; it calls no cudaMalloc, cudaFree or any other
+ * allocating routine.
+ *
+ * Scratch: the kernel's status word lives in a fixed 256-byte array
+ * (64 int32 words) of the library's static device memory, which every GPU
+ * that loads libattn.so holds until the process exits.  One call uses one
+ * word; a call that needed more than the array holds would be rejected with
+ * ATTN_ERR_SCRATCH before anything is queued.
+ *
+ * Set-up: the first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current); if the CUDA driver has
+ * not yet loaded the library's static device data on that device, this is
+ * when it does (the array itself, a one-time cost).  Make that first call
+ * before any stream capture begins on the device.
+ *
+ * Sharing: every call on a device uses the same array.  Each call clears the
+ * status word on its stream (cudaMemsetAsync) before its kernel, so the word
+ * holds only the latest call's conditions; attn_status reads and clears it
+ * together with attn_fwd's word.  Calls whose executions overlap on the GPU
+ * (different streams without ordering) race on the word: order them, or read
+ * attn_status between them, if their device-side status matters.
+ */
+attn_status_t attn_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
+                               int B, int Hq, int Hkv, int L, int D, float sm_scale, int causal,
+                               const int32_t* valid_len, attn_dtype_t dtype,
+                               attn_stream_t stream);
 
 /*
  * attn_status -- synchronise `stream`, then read and clear the device status
