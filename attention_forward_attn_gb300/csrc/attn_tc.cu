@@ -51,10 +51,10 @@ constexpr int kThreads = 384;  // warpgroups: softmax tile 0, softmax tile 1, pr
 // Register split between warpgroups (setmaxnreg).  The CTA is launched with
 // kLaunchRegs per thread (the __launch_bounds__(384, 1) ceiling: 3 warps per
 // SM sub-partition); the split must add up to exactly that pool:
-// 2 * 128 * 216 + 128 * 72 = 384 * 168.
+// 2 * 128 * 224 + 128 * 56 = 384 * 168.
 constexpr int kLaunchRegs = 168;
-constexpr int kSoftmaxRegs = 216;
-constexpr int kControlRegs = 72;
+constexpr int kSoftmaxRegs = 224;
+constexpr int kControlRegs = 56;
 static_assert(2 * 128 * kSoftmaxRegs + 128 * kControlRegs == kThreads * kLaunchRegs,
               "register split must equal the launch pool");
 constexpr float kRescaleLog2 = 8.0f;  // rescale O only when the max grows by > 2^8
@@ -468,20 +468,24 @@ __device__ void softmax_role(const KParams& p, const Bars<Cfg<D>::kStages>& br, 
       const int n0 = j * BN;
       const bool masked = (n0 + BN > w.kv_len) || (p.causal && n0 + BN - 1 > r0);
       const int c_lim = key_lim - n0;  // columns c < c_lim are visible
-      // row max with 8 independent chains (a single chain is 128 dependent ops)
+      // row max: 8 independent chains of 3-input maxima
       float mxk[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) mxk[k] = -INFINITY;
       if (masked) {
 #pragma unroll
-        for (int c = 0; c < BN; ++c)
-          mxk[c & 7] = fmaxf(mxk[c & 7], (c < c_lim) ? __uint_as_float(s[c]) : -INFINITY);
+        for (int i = 0; i < BN / 2; ++i) {
+          const int c = 2 * i;
+          mxk[i & 7] = ptx::max3(mxk[i & 7], (c < c_lim) ? __uint_as_float(s[c]) : -INFINITY,
+                                 (c + 1 < c_lim) ? __uint_as_float(s[c + 1]) : -INFINITY);
+        }
       } else {
 #pragma unroll
-        for (int c = 0; c < BN; ++c) mxk[c & 7] = fmaxf(mxk[c & 7], __uint_as_float(s[c]));
+        for (int i = 0; i < BN / 2; ++i)
+          mxk[i & 7] = ptx::max3(mxk[i & 7], __uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1]));
       }
-      const float mx = fmaxf(fmaxf(fmaxf(mxk[0], mxk[1]), fmaxf(mxk[2], mxk[3])),
-                             fmaxf(fmaxf(mxk[4], mxk[5]), fmaxf(mxk[6], mxk[7])));
+      const float mx = ptx::max3(ptx::max3(mxk[0], mxk[1], mxk[2]), ptx::max3(mxk[3], mxk[4], mxk[5]),
+                                 fmaxf(mxk[6], mxk[7]));
       const float m_tile = (mx == -INFINITY) ? -INFINITY : mx * scale_log2;
       const float m_new = fmaxf(m, m_tile);
       float alpha = 1.f;
@@ -492,7 +496,11 @@ __device__ void softmax_role(const KParams& p, const Bars<Cfg<D>::kStages>& br, 
         rescale = true;
       }
       const float neg_m = (m == -INFINITY) ? 0.f : -m;
-      float rsum[4] = {0.f, 0.f, 0.f, 0.f};  // independent partial row sums
+      const uint64_t sc2 = ptx::f2_pack(scale_log2, scale_log2);
+      const uint64_t nm2 = ptx::f2_pack(neg_m, neg_m);
+      uint64_t rsum2[4];  // independent partial row sums, two lanes each
+#pragma unroll
+      for (int k = 0; k < 4; ++k) rsum2[k] = 0ull;
       // P over the S columns, 32 keys at a time (every S value is already in
       // registers).  fp16: P rounded to fp16 in columns [0, 64).  bf16:
       // P = P_hi + P_lo with P_hi = p truncated to bf16 (columns [0, 64)) and
@@ -506,18 +514,27 @@ __device__ void softmax_role(const KParams& p, const Bars<Cfg<D>::kStages>& br, 
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int c = qtr * 32 + 2 * i;
-          float p0 = ptx::ex2_approx(fmaf(__uint_as_float(s[c]), scale_log2, neg_m));
-          float p1 = ptx::ex2_approx(fmaf(__uint_as_float(s[c + 1]), scale_log2, neg_m));
+          // exponent argument s*scale - m for two keys in one instruction
+          const uint64_t x2 = ptx::f2_fma(ptx::f2_pack(__uint_as_float(s[c]), __uint_as_float(s[c + 1])),
+                                          sc2, nm2);
+          float x0, x1;
+          ptx::f2_unpack(x2, x0, x1);
+          float p0 = ptx::ex2_approx(x0);
+          float p1 = ptx::ex2_approx(x1);
           if (masked) {
             p0 = (c < c_lim) ? p0 : 0.f;
             p1 = (c + 1 < c_lim) ? p1 : 0.f;
           }
-          rsum[i & 3] += p0 + p1;
+          const uint64_t p2 = ptx::f2_pack(p0, p1);
+          rsum2[i & 3] = ptx::f2_add(rsum2[i & 3], p2);
           if constexpr (BF16) {
             const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
             hi[i] = __byte_perm(b0, b1, 0x7632);  // upper halves: truncated bf16 pair
-            lo[i] = pack2<true>(p0 - __uint_as_float(b0 & 0xFFFF0000u),
-                                p1 - __uint_as_float(b1 & 0xFFFF0000u));
+            const uint64_t r2 = ptx::f2_sub(
+                p2, ptx::f2_pack(__uint_as_float(b0 & 0xFFFF0000u), __uint_as_float(b1 & 0xFFFF0000u)));
+            float r0, r1;
+            ptx::f2_unpack(r2, r0, r1);
+            lo[i] = pack2<true>(r0, r1);
           } else {
             hi[i] = pack2<false>(p0, p1);
           }
@@ -525,7 +542,9 @@ __device__ void softmax_role(const KParams& p, const Bars<Cfg<D>::kStages>& br, 
         ptx::tmem_st16(t_s + qtr * 16, hi);
         if constexpr (BF16) ptx::tmem_st16(t_s + BN / 2 + qtr * 16, lo);
       }
-      l = l * alpha + ((rsum[0] + rsum[1]) + (rsum[2] + rsum[3]));
+      float ra, rb;
+      ptx::f2_unpack(ptx::f2_add(ptx::f2_add(rsum2[0], rsum2[1]), ptx::f2_add(rsum2[2], rsum2[3])), ra, rb);
+      l = l * alpha + (ra + rb);
       // O was accumulated against the old max: rescale it before PV_j runs.
       // PV_{j-1} is complete: the commit that signalled S_j came after it.
       if (j > 0 && __any_sync(0xffffffffu, rescale)) {
