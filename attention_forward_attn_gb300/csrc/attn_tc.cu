@@ -276,6 +276,25 @@ __device__ void producer_role(const KParams& p, const Bars<Cfg<D>::kStages>& br,
 
 // ------------------------------------------------------------------ MMA issuer
 
+// One lane of a converged warp, chosen by the hardware (elect.sync).  The MMA
+// issuer runs on the whole warp so that descriptors and TMEM addresses stay
+// warp-uniform values; only the tcgen05.mma / tcgen05.commit instructions
+// themselves are executed by the elected lane.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "elect.sync _|P, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, P;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
+__device__ __forceinline__ void commit_one(uint32_t bar) {
+  if (elect_one()) ptx::mma_commit(bar);
+  __syncwarp();
+}
+
 // A descriptor's start address is its low 14 bits (address >> 4); a byte
 // offset inside the same shared-memory window is added there directly.
 __device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t bytes) {
@@ -339,7 +358,7 @@ __device__ void mma_role(const KParams& p, const Bars<Cfg<D>::kStages>& br, uint
 #pragma unroll
     for (int t = 0; t < QT; ++t) {
       if (w.n[t] == 0) continue;
-      if (!wait_bar(br, p.status, br.q_full(t), (q_phase >> t) & 1u, kRoleMma)) {
+      if (!__all_sync(0xffffffffu, wait_bar(br, p.status, br.q_full(t), (q_phase >> t) & 1u, kRoleMma))) {
         ok = false;
         break;
       }
@@ -348,24 +367,27 @@ __device__ void mma_role(const KParams& p, const Bars<Cfg<D>::kStages>& br, uint
     if (!ok) break;
     // K_0
     const uint32_t sk = it % C::kStages;
-    if (!wait_bar(br, p.status, br.kv_full(sk), (it / C::kStages) & 1u, kRoleMma)) break;
+    if (!__all_sync(0xffffffffu, wait_bar(br, p.status, br.kv_full(sk), (it / C::kStages) & 1u, kRoleMma))) break;
     ++it;
     ptx::tc_fence_after();
 #pragma unroll
     for (int t = 0; t < QT; ++t)
       if (w.n[t] > 0) {
-        issue_qk<D, BF16>(tmem + C::col_s(t), desc_add(q_desc0, t * C::kQBytes),
+        if (elect_one()) {
+          issue_qk<D, BF16>(tmem + C::col_s(t), desc_add(q_desc0, t * C::kQBytes),
                           desc_add(k_desc0, sk * C::kKVBytes));
-        ptx::mma_commit(br.s_full(t));
+        }
+        __syncwarp();
+        commit_one(br.s_full(t));
         // Q_t is free once the unit's last S_t MMA completes: the producer can
         // load the next unit's Q_t while this unit finishes
-        if (w.n[t] == 1) ptx::mma_commit(br.q_empty(t));
+        if (w.n[t] == 1) commit_one(br.q_empty(t));
       }
-    ptx::mma_commit(br.kv_empty(sk));
+    commit_one(br.kv_empty(sk));
 
     for (int j = 0; j < n; ++j) {
       const uint32_t sv = it % C::kStages;
-      if (!wait_bar(br, p.status, br.kv_full(sv), (it / C::kStages) & 1u, kRoleMma)) {
+      if (!__all_sync(0xffffffffu, wait_bar(br, p.status, br.kv_full(sv), (it / C::kStages) & 1u, kRoleMma))) {
         ok = false;
         break;
       }
@@ -376,20 +398,23 @@ __device__ void mma_role(const KParams& p, const Bars<Cfg<D>::kStages>& br, uint
 #pragma unroll
       for (int t = 0; t < QT; ++t) {
         if (j < w.n[t]) {
-          if (!wait_bar(br, p.status, br.p_full(t), (p_phase >> t) & 1u, kRoleMma)) {
+          if (!__all_sync(0xffffffffu, wait_bar(br, p.status, br.p_full(t), (p_phase >> t) & 1u, kRoleMma))) {
             ok = false;
             break;
           }
           p_phase ^= 1u << t;
           ptx::tc_fence_after();
-          issue_pv<D, BF16>(tmem + C::col_o(t), tmem + C::col_s(t),
+          if (elect_one()) {
+            issue_pv<D, BF16>(tmem + C::col_o(t), tmem + C::col_s(t),
                             desc_add(v_desc0, sv * C::kKVBytes), j > 0);
-          if (j == w.n[t] - 1) ptx::mma_commit(br.o_full(t));
+          }
+          __syncwarp();
+          if (j == w.n[t] - 1) commit_one(br.o_full(t));
         }
-        if (t == QT - 1) ptx::mma_commit(br.kv_empty(sv));  // V_j read by every PV above
+        if (t == QT - 1) commit_one(br.kv_empty(sv));  // V_j read by every PV above
         if (has_next && !next_loaded) {
           sk2 = it % C::kStages;
-          if (!wait_bar(br, p.status, br.kv_full(sk2), (it / C::kStages) & 1u, kRoleMma)) {
+          if (!__all_sync(0xffffffffu, wait_bar(br, p.status, br.kv_full(sk2), (it / C::kStages) & 1u, kRoleMma))) {
             ok = false;
             break;
           }
@@ -398,18 +423,21 @@ __device__ void mma_role(const KParams& p, const Bars<Cfg<D>::kStages>& br, uint
           ptx::tc_fence_after();
         }
         if (j + 1 < w.n[t]) {
-          issue_qk<D, BF16>(tmem + C::col_s(t), desc_add(q_desc0, t * C::kQBytes),
+          if (elect_one()) {
+            issue_qk<D, BF16>(tmem + C::col_s(t), desc_add(q_desc0, t * C::kQBytes),
                             desc_add(k_desc0, sk2 * C::kKVBytes));
-          ptx::mma_commit(br.s_full(t));
-          if (j + 2 == w.n[t]) ptx::mma_commit(br.q_empty(t));  // last S_t of the unit
+          }
+          __syncwarp();
+          commit_one(br.s_full(t));
+          if (j + 2 == w.n[t]) commit_one(br.q_empty(t));  // last S_t of the unit
         }
       }
       if (!ok) break;
-      if (has_next) ptx::mma_commit(br.kv_empty(sk2));
+      if (has_next) commit_one(br.kv_empty(sk2));
     }
   }
   // Every MMA issued by this thread completes before TMEM is released.
-  ptx::mma_commit(br.drain());
+  commit_one(br.drain());
   drain_wait(br.drain(), 0);
 }
 
@@ -636,7 +664,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kProducerWarp) {
       if (lane == 0) producer_role<D>(p, br, smem, &tm_q, &tm_k, &tm_v);
     } else if (warp == kMmaWarp) {
-      if (lane == 0) mma_role<D, BF16>(p, br, smem, tmem);
+      mma_role<D, BF16>(p, br, smem, tmem);  // whole warp
     }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
