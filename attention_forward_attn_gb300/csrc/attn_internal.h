@@ -17,6 +17,7 @@ enum : int {
   kRoleMma = 2 << 8,
   kRoleSoftmax = 4 << 8,
   kRoleEpilogue = 8 << 8,
+  kRoleConvert = 16 << 8,
 };
 
 // Problem description handed to a kernel launcher (already validated).

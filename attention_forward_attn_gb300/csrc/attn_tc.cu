@@ -72,10 +72,12 @@ struct Cfg {
   static constexpr int kOffKV = QT * kQBytes;
   static constexpr int kOffBar = kOffKV + kStages * kKVBytes;
   // barrier block: q_full[QT] q_empty[QT] kv_full[S] kv_empty[S] s_full[QT]
-  // p_full[QT] o_full[QT] drain, then the TMEM base word and the abort flag
-  static constexpr int kNumBars = 5 * QT + 2 * kStages + 1;
+  // p_full[QT] o_full[QT] drain v_conv[S], then 32-bit words: TMEM base,
+  // abort flag, two converter votes, and one precision flag per stage
+  static constexpr int kNumBars = 5 * QT + 3 * kStages + 1;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + slack to align the base to 1 KB
+  static constexpr int kMiscBytes = 16 + 4 * kStages;
+  static constexpr int kSmemBytes = kOffMisc + kMiscBytes + 1024;  // + slack to align the base
   // TMEM columns: S_0, S_1 (fp32, BN each; P_t is written over S_t), then
   // O_0, O_1 (fp32, D each).
   static __device__ __forceinline__ uint32_t col_s(int t) { return static_cast<uint32_t>(t * BN); }
@@ -101,8 +103,15 @@ struct Bars {
   __device__ __forceinline__ uint32_t p_full(int t) const { return base + 8u * (3 * QT + 2 * S + t); }
   __device__ __forceinline__ uint32_t o_full(int t) const { return base + 8u * (4 * QT + 2 * S + t); }
   __device__ __forceinline__ uint32_t drain() const { return base + 8u * (5 * QT + 2 * S); }
-  __device__ __forceinline__ uint32_t tmem_word() const { return base + 8u * (5 * QT + 2 * S + 1); }
+  // V tile in stage s converted (or checked and left in bf16): converters -> MMA, softmax
+  __device__ __forceinline__ uint32_t v_conv(uint32_t s) const {
+    return base + 8u * (5 * QT + 2 * S + 1 + s);
+  }
+  __device__ __forceinline__ uint32_t tmem_word() const { return base + 8u * (5 * QT + 3 * S + 1); }
   __device__ __forceinline__ uint32_t abort_word() const { return tmem_word() + 4u; }
+  __device__ __forceinline__ uint32_t vote_word(int w) const { return tmem_word() + 8u + 4u * w; }
+  // 1: the V tile in stage s is fp16 (P·V in fp16); 0: it stayed bf16 (split P)
+  __device__ __forceinline__ uint32_t vflag(uint32_t s) const { return tmem_word() + 16u + 4u * s; }
 };
 
 struct KParams {
@@ -317,16 +326,18 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t q_desc, uint6
 
 // O += P V: A = P from TMEM (16-bit pairs, 8 columns per 16 keys), B = V tile
 // as an MN-major 128-byte-swizzled operand (16 keys = two 8-row groups).
-// bf16: O += [P_hi | P_lo] [V; V], the same V tile read twice.
-template <int D, bool BF16>
+// fp16 V tile (fp16 inputs, or a bf16 tile the converters turned into fp16):
+// O += P V with fp16 P.  bf16 V tile (split): O += [P_hi | P_lo] [V; V], the
+// same V tile read twice.
+template <int D>
 __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint64_t v_desc,
-                                         bool accumulate) {
-  constexpr uint32_t idesc = ptx::idesc_f16(BM, D, BF16, true);
+                                         bool accumulate, bool split) {
+  const uint32_t idesc = split ? ptx::idesc_f16(BM, D, true, true) : ptx::idesc_f16(BM, D, false, true);
 #pragma unroll 1
   for (int kk = 0; kk < BN / 16; ++kk)
     ptx::mma_ts(d_tmem, p_tmem + kk * 8u, desc_add(v_desc, kk * 2048u), idesc,
                 (accumulate || kk > 0) ? 1u : 0u);
-  if constexpr (BF16) {
+  if (split) {
 #pragma unroll 1
     for (int kk = 0; kk < BN / 16; ++kk)
       ptx::mma_ts(d_tmem, p_tmem + BN / 2 + kk * 8u, desc_add(v_desc, kk * 2048u), idesc, 1u);
@@ -387,11 +398,14 @@ __device__ void mma_role(const KParams& p, const Bars<Cfg<D>::kStages>& br, uint
 
     for (int j = 0; j < n; ++j) {
       const uint32_t sv = it % C::kStages;
-      if (!__all_sync(0xffffffffu, wait_bar(br, p.status, br.kv_full(sv), (it / C::kStages) & 1u, kRoleMma))) {
+      // bf16: wait until the converters have checked (and converted) V_j
+      const uint32_t vbar = BF16 ? br.v_conv(sv) : br.kv_full(sv);
+      if (!__all_sync(0xffffffffu, wait_bar(br, p.status, vbar, (it / C::kStages) & 1u, kRoleMma))) {
         ok = false;
         break;
       }
       ++it;
+      const bool split = BF16 && ptx::ld_shared_volatile(br.vflag(sv)) == 0u;
       const bool has_next = j + 1 < n;
       uint32_t sk2 = 0;
       bool next_loaded = false;
@@ -405,8 +419,8 @@ __device__ void mma_role(const KParams& p, const Bars<Cfg<D>::kStages>& br, uint
           p_phase ^= 1u << t;
           ptx::tc_fence_after();
           if (elect_one()) {
-            issue_pv<D, BF16>(tmem + C::col_o(t), tmem + C::col_s(t),
-                            desc_add(v_desc0, sv * C::kKVBytes), j > 0);
+            issue_pv<D>(tmem + C::col_o(t), tmem + C::col_s(t),
+                        desc_add(v_desc0, sv * C::kKVBytes), j > 0, split);
           }
           __syncwarp();
           if (j == w.n[t] - 1) commit_one(br.o_full(t));
@@ -441,6 +455,72 @@ __device__ void mma_role(const KParams& p, const Bars<Cfg<D>::kStages>& br, uint
   drain_wait(br.drain(), 0);
 }
 
+// ------------------------------------------------------------------ V converters (bf16 only)
+
+// Warps 10-11.  For every V tile (in ring order) they check whether all its
+// bf16 values are finite with |v| < 65536; if so they rewrite the tile in
+// place as fp16 (exact for |v| >= 2^-14, within 2^-25 absolutely below), so
+// that P.V can use fp16 P.  Otherwise the tile stays bf16 and P is split.
+// The verdict goes to vflag[s]; v_conv[s] signals the MMA issuer and softmax.
+template <int D>
+__device__ void convert_role(const KParams& p, const Bars<Cfg<D>::kStages>& br, uint32_t smem) {
+  using C = Cfg<D>;
+  const int ct = static_cast<int>(threadIdx.x) - 10 * 32;  // 0..63
+  const int cw = ct >> 5;
+  constexpr int kVec = C::kKVBytes / 16;  // 16-byte vectors per tile
+  uint32_t it = 0;
+  const int rounds = (p.n_units + gridDim.x - 1) / gridDim.x;
+  for (int r = 0; r < rounds; ++r) {
+    const int u = unit_of(r);
+    if (u >= p.n_units) continue;
+    const Unit w = decode_unit(p, u);
+    const int n = max(w.n[0], w.n[1]);
+    for (int j = 0; j < n; ++j) {
+      ++it;  // K_j
+      const uint32_t s = it % C::kStages;
+      const uint32_t par = (it / C::kStages) & 1u;
+      ++it;  // V_j
+      if (!__all_sync(0xffffffffu, wait_bar(br, p.status, br.kv_full(s), par, kRoleConvert)))
+        return;
+      const uint32_t tile = smem + C::kOffKV + s * C::kKVBytes;
+      // pass 1: largest exponent field of every bf16 half (>= 143: |v| >= 2^16, inf, NaN)
+      uint32_t ex = 0;
+#pragma unroll 4
+      for (int k = ct; k < kVec; k += 64) {
+        const uint4 v = ptx::ld_shared_v4(tile + 16u * k);
+        ex = __vmaxu2(ex, v.x & 0x7F807F80u);
+        ex = __vmaxu2(ex, v.y & 0x7F807F80u);
+        ex = __vmaxu2(ex, v.z & 0x7F807F80u);
+        ex = __vmaxu2(ex, v.w & 0x7F807F80u);
+      }
+      const bool bad_mine = (ex & 0xFFFFu) >= 0x4780u || (ex >> 16) >= 0x4780u;
+      const uint32_t bad_warp = __any_sync(0xffffffffu, bad_mine) ? 1u : 0u;
+      if ((ct & 31) == 0) ptx::st_shared_volatile(br.vote_word(cw), bad_warp);
+      ptx::named_barrier_sync(1, 64);
+      const bool bad = (ptx::ld_shared_volatile(br.vote_word(0)) |
+                        ptx::ld_shared_volatile(br.vote_word(1))) != 0u;
+      ptx::named_barrier_sync(1, 64);  // both votes read before the next tile's
+      if (!bad) {
+        // pass 2: bf16 pairs -> fp16 pairs, in place
+#pragma unroll 4
+        for (int k = ct; k < kVec; k += 64) {
+          const uint32_t a = tile + 16u * k;
+          const uint4 v = ptx::ld_shared_v4(a);
+          uint4 o;
+          o.x = pack2<false>(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xFFFF0000u));
+          o.y = pack2<false>(__uint_as_float(v.y << 16), __uint_as_float(v.y & 0xFFFF0000u));
+          o.z = pack2<false>(__uint_as_float(v.z << 16), __uint_as_float(v.z & 0xFFFF0000u));
+          o.w = pack2<false>(__uint_as_float(v.w << 16), __uint_as_float(v.w & 0xFFFF0000u));
+          ptx::st_shared_v4(a, o);
+        }
+      }
+      if (ct == 0) ptx::st_shared_volatile(br.vflag(s), bad ? 0u : 1u);
+      ptx::fence_proxy_async_shared();  // our writes before the tensor core's reads
+      ptx::mbar_arrive(br.v_conv(s));
+    }
+  }
+}
+
 // ------------------------------------------------------------------ softmax + epilogue
 
 template <int D, bool BF16>
@@ -453,12 +533,15 @@ __device__ void softmax_role(const KParams& p, const Bars<Cfg<D>::kStages>& br, 
   const uint32_t t_o = tmem + ((quad * 32u) << 16) + C::col_o(t);
   const float scale_log2 = p.scale_log2;
   uint32_t s_phase = 0, o_phase = 0;
+  uint32_t items = 0;  // K/V ring items of the units before this one (K_0 V_0 K_1 V_1 ...)
 
   const int rounds = (p.n_units + gridDim.x - 1) / gridDim.x;
   for (int r = 0; r < rounds; ++r) {
     const int u = unit_of(r);
     if (u >= p.n_units) continue;
     const Unit w = decode_unit(p, u);
+    const uint32_t item_base = items;
+    items += 2u * static_cast<uint32_t>(max(w.n[0], w.n[1]));
     const int r0 = w.m0 + t * BM;
     if (r0 >= p.L) continue;
     const int row = r0 + lane_row;
@@ -524,38 +607,72 @@ __device__ void softmax_role(const KParams& p, const Bars<Cfg<D>::kStages>& br, 
         rescale = true;
       }
       const float neg_m = (m == -INFINITY) ? 0.f : -m;
+      // bf16 inputs: is V_j in fp16 now (converted) or still bf16?
+      bool split = false;
+      if constexpr (BF16) {
+        const uint32_t vi = item_base + 2u * static_cast<uint32_t>(j) + 1u;
+        const uint32_t vs = vi % C::kStages;
+        ok = wait_bar(br, p.status, br.v_conv(vs), (vi / C::kStages) & 1u, kRoleSoftmax);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        split = ptx::ld_shared_volatile(br.vflag(vs)) == 0u;
+      }
       const uint64_t sc2 = ptx::f2_pack(scale_log2, scale_log2);
       const uint64_t nm2 = ptx::f2_pack(neg_m, neg_m);
       uint64_t rsum2[4];  // independent partial row sums, two lanes each
 #pragma unroll
       for (int k = 0; k < 4; ++k) rsum2[k] = 0ull;
       // P over the S columns, 32 keys at a time (every S value is already in
-      // registers).  fp16: P rounded to fp16 in columns [0, 64).  bf16:
-      // P = P_hi + P_lo with P_hi = p truncated to bf16 (columns [0, 64)) and
-      // P_lo = bf16(p - P_hi) (columns [64, 128)); a single bf16 P (unit
-      // roundoff 2^-8) is too coarse for rows dominated by a few keys, the
-      // pair leaves a relative error below 2^-15.
+      // registers).  fp16 V tile: P rounded to fp16 in columns [0, 64).
+      // bf16 V tile: P = P_hi + P_lo with P_hi = p truncated to bf16 (columns
+      // [0, 64)) and P_lo = bf16(p - P_hi) (columns [64, 128)); a single bf16
+      // P (unit roundoff 2^-8) is too coarse for rows dominated by a few keys,
+      // the pair leaves a relative error below 2^-15.
+      if (!split) {
 #pragma unroll
-      for (int qtr = 0; qtr < 4; ++qtr) {
-        uint32_t hi[16];
-        uint32_t lo[BF16 ? 16 : 1];
+        for (int qtr = 0; qtr < 4; ++qtr) {
+          uint32_t hi[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int c = qtr * 32 + 2 * i;
-          // exponent argument s*scale - m for two keys in one instruction
-          const uint64_t x2 = ptx::f2_fma(ptx::f2_pack(__uint_as_float(s[c]), __uint_as_float(s[c + 1])),
-                                          sc2, nm2);
-          float x0, x1;
-          ptx::f2_unpack(x2, x0, x1);
-          float p0 = ptx::ex2_approx(x0);
-          float p1 = ptx::ex2_approx(x1);
-          if (masked) {
-            p0 = (c < c_lim) ? p0 : 0.f;
-            p1 = (c + 1 < c_lim) ? p1 : 0.f;
+          for (int i = 0; i < 16; ++i) {
+            const int c = qtr * 32 + 2 * i;
+            // exponent argument s*scale - m for two keys in one instruction
+            const uint64_t x2 = ptx::f2_fma(
+                ptx::f2_pack(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), sc2, nm2);
+            float x0, x1;
+            ptx::f2_unpack(x2, x0, x1);
+            float p0 = ptx::ex2_approx(x0);
+            float p1 = ptx::ex2_approx(x1);
+            if (masked) {
+              p0 = (c < c_lim) ? p0 : 0.f;
+              p1 = (c + 1 < c_lim) ? p1 : 0.f;
+            }
+            rsum2[i & 3] = ptx::f2_add(rsum2[i & 3], ptx::f2_pack(p0, p1));
+            hi[i] = pack2<false>(p0, p1);
           }
-          const uint64_t p2 = ptx::f2_pack(p0, p1);
-          rsum2[i & 3] = ptx::f2_add(rsum2[i & 3], p2);
-          if constexpr (BF16) {
+          ptx::tmem_st16(t_s + qtr * 16, hi);
+        }
+      } else if constexpr (BF16) {
+#pragma unroll
+        for (int qtr = 0; qtr < 4; ++qtr) {
+          uint32_t hi[16];
+          uint32_t lo[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int c = qtr * 32 + 2 * i;
+            const uint64_t x2 = ptx::f2_fma(
+                ptx::f2_pack(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), sc2, nm2);
+            float x0, x1;
+            ptx::f2_unpack(x2, x0, x1);
+            float p0 = ptx::ex2_approx(x0);
+            float p1 = ptx::ex2_approx(x1);
+            if (masked) {
+              p0 = (c < c_lim) ? p0 : 0.f;
+              p1 = (c + 1 < c_lim) ? p1 : 0.f;
+            }
+            const uint64_t p2 = ptx::f2_pack(p0, p1);
+            rsum2[i & 3] = ptx::f2_add(rsum2[i & 3], p2);
             const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
             hi[i] = __byte_perm(b0, b1, 0x7632);  // upper halves: truncated bf16 pair
             const uint64_t r2 = ptx::f2_sub(
@@ -563,12 +680,10 @@ __device__ void softmax_role(const KParams& p, const Bars<Cfg<D>::kStages>& br, 
             float r0, r1;
             ptx::f2_unpack(r2, r0, r1);
             lo[i] = pack2<true>(r0, r1);
-          } else {
-            hi[i] = pack2<false>(p0, p1);
           }
+          ptx::tmem_st16(t_s + qtr * 16, hi);
+          ptx::tmem_st16(t_s + BN / 2 + qtr * 16, lo);
         }
-        ptx::tmem_st16(t_s + qtr * 16, hi);
-        if constexpr (BF16) ptx::tmem_st16(t_s + BN / 2 + qtr * 16, lo);
       }
       float ra, rb;
       ptx::f2_unpack(ptx::f2_add(ptx::f2_add(rsum2[0], rsum2[1]), ptx::f2_add(rsum2[2], rsum2[3])), ra, rb);
@@ -640,6 +755,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < C::kStages; ++s) {
       ptx::mbar_init(br.kv_full(s), 1);
       ptx::mbar_init(br.kv_empty(s), 1);
+      ptx::mbar_init(br.v_conv(s), 64);  // every converter thread arrives
     }
     ptx::mbar_init(br.drain(), 1);
     ptx::st_shared_volatile(br.abort_word(), 0u);
@@ -665,6 +781,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) producer_role<D>(p, br, smem, &tm_q, &tm_k, &tm_v);
     } else if (warp == kMmaWarp) {
       mma_role<D, BF16>(p, br, smem, tmem);  // whole warp
+    } else if constexpr (BF16) {
+      convert_role<D>(p, br, smem);  // warps 10, 11
     }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));

@@ -213,3 +213,20 @@ def test_workload_tc_matches_simt_everywhere(name):
     neg = np.isneginf(l2)
     assert np.array_equal(np.isneginf(l1), neg)
     assert np.abs(l1[~neg] - l2[~neg]).max() <= 2 * LSE_ATOL
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_bf16_v_tiles_beyond_fp16_range(D, causal):
+    """bf16 V tiles holding |v| >= 65536 keep bf16 (split P) while the other
+    tiles of the same launch run P.V in fp16; both must match the oracle."""
+    B, Hq, Hkv, L = 2, 4, 2, 640
+    q, k, v, _ = wl.make_inputs(B, Hq, Hkv, L, D, wl.BF16, seed=31 + D)
+    v = v.clone()
+    v[0, 0, 130, 5] = 70000.0       # key tile 1 of kv head 0, batch 0
+    v[1, 1, 600, :3] = -3.0e6       # key tile 4 of kv head 1, batch 1
+    v[1, 0, 0, 7] = 65504.0         # still in fp16 range: this tile converts
+    sm = 1.0 / math.sqrt(D)
+    o, lse = run_gpu(q, k, v, causal, None, sm)
+    o_ref, lse_ref = oracle.attn_fwd_bits(wl.bits(q), wl.bits(k), wl.bits(v), 1, sm, causal=causal)
+    check(o, lse, o_ref, lse_ref, "bf16 V beyond fp16 range D%d causal=%s" % (D, causal))
