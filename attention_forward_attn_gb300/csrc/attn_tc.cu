@@ -62,21 +62,26 @@ constexpr float kLn2 = 0.69314718055994531f;
 
 template <int D>
 struct Cfg {
-  static constexpr int kStages = (D == 128) ? 4 : 8;
+  // separate rings for K and V tiles; V gets the extra stage so that bf16 V
+  // tiles reach shared memory (and the converters) well before their P.V
+  static constexpr int kKStages = (D == 128) ? 2 : 4;
+  static constexpr int kVStages = (D == 128) ? 3 : 4;
   static constexpr int kHalves = D / 64;           // 64-column (128-byte) slabs per row
   static constexpr int kQBytes = BM * D * 2;
   static constexpr int kKVBytes = BN * D * 2;
   static constexpr int kSlabQ = BM * 128;          // bytes of one 64-column slab of a Q tile
   static constexpr int kSlabKV = BN * 128;
   static constexpr int kOffQ = 0;
-  static constexpr int kOffKV = QT * kQBytes;
-  static constexpr int kOffBar = kOffKV + kStages * kKVBytes;
-  // barrier block: q_full[QT] q_empty[QT] kv_full[S] kv_empty[S] s_full[QT]
-  // p_full[QT] o_full[QT] drain v_conv[S], then 32-bit words: TMEM base,
-  // abort flag, two converter votes, and one precision flag per stage
-  static constexpr int kNumBars = 5 * QT + 3 * kStages + 1;
+  static constexpr int kOffK = QT * kQBytes;
+  static constexpr int kOffV = kOffK + kKStages * kKVBytes;
+  static constexpr int kOffBar = kOffV + kVStages * kKVBytes;
+  // barrier block: q_full[QT] q_empty[QT] k_full[KS] k_empty[KS] v_full[VS]
+  // v_empty[VS] v_conv[VS] s_full[QT] p_full[QT] o_full[QT] drain, then
+  // 32-bit words: TMEM base, abort flag, two converter votes, one precision
+  // flag per V stage
+  static constexpr int kNumBars = 5 * QT + 2 * kKStages + 3 * kVStages + 1;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-  static constexpr int kMiscBytes = 16 + 4 * kStages;
+  static constexpr int kMiscBytes = 16 + 4 * kVStages;
   static constexpr int kSmemBytes = kOffMisc + kMiscBytes + 1024;  // + slack to align the base
   // TMEM columns: S_0, S_1 (fp32, BN each; P_t is written over S_t), then
   // O_0, O_1 (fp32, D each).
@@ -90,27 +95,43 @@ struct Cfg {
 };
 
 // Shared-memory addresses of the barriers (32-bit, one base + constants).
-template <int S>
+template <int D>
 struct Bars {
+  static constexpr uint32_t KS = Cfg<D>::kKStages;
+  static constexpr uint32_t VS = Cfg<D>::kVStages;
   uint32_t base;
   __device__ __forceinline__ uint32_t q_full(int t) const { return base + 8u * t; }
   __device__ __forceinline__ uint32_t q_empty(int t) const { return base + 8u * (QT + t); }
-  __device__ __forceinline__ uint32_t kv_full(uint32_t s) const { return base + 8u * (2 * QT + s); }
-  __device__ __forceinline__ uint32_t kv_empty(uint32_t s) const {
-    return base + 8u * (2 * QT + S + s);
+  __device__ __forceinline__ uint32_t k_full(uint32_t s) const { return base + 8u * (2 * QT + s); }
+  __device__ __forceinline__ uint32_t k_empty(uint32_t s) const {
+    return base + 8u * (2 * QT + KS + s);
   }
-  __device__ __forceinline__ uint32_t s_full(int t) const { return base + 8u * (2 * QT + 2 * S + t); }
-  __device__ __forceinline__ uint32_t p_full(int t) const { return base + 8u * (3 * QT + 2 * S + t); }
-  __device__ __forceinline__ uint32_t o_full(int t) const { return base + 8u * (4 * QT + 2 * S + t); }
-  __device__ __forceinline__ uint32_t drain() const { return base + 8u * (5 * QT + 2 * S); }
-  // V tile in stage s converted (or checked and left in bf16): converters -> MMA, softmax
+  __device__ __forceinline__ uint32_t v_full(uint32_t s) const {
+    return base + 8u * (2 * QT + 2 * KS + s);
+  }
+  __device__ __forceinline__ uint32_t v_empty(uint32_t s) const {
+    return base + 8u * (2 * QT + 2 * KS + VS + s);
+  }
+  // V tile in stage s checked (and converted to fp16 when in range): converters -> MMA, softmax
   __device__ __forceinline__ uint32_t v_conv(uint32_t s) const {
-    return base + 8u * (5 * QT + 2 * S + 1 + s);
+    return base + 8u * (2 * QT + 2 * KS + 2 * VS + s);
   }
-  __device__ __forceinline__ uint32_t tmem_word() const { return base + 8u * (5 * QT + 3 * S + 1); }
+  __device__ __forceinline__ uint32_t s_full(int t) const {
+    return base + 8u * (2 * QT + 2 * KS + 3 * VS + t);
+  }
+  __device__ __forceinline__ uint32_t p_full(int t) const {
+    return base + 8u * (3 * QT + 2 * KS + 3 * VS + t);
+  }
+  __device__ __forceinline__ uint32_t o_full(int t) const {
+    return base + 8u * (4 * QT + 2 * KS + 3 * VS + t);
+  }
+  __device__ __forceinline__ uint32_t drain() const { return base + 8u * (5 * QT + 2 * KS + 3 * VS); }
+  __device__ __forceinline__ uint32_t tmem_word() const {
+    return base + 8u * (5 * QT + 2 * KS + 3 * VS + 1);
+  }
   __device__ __forceinline__ uint32_t abort_word() const { return tmem_word() + 4u; }
   __device__ __forceinline__ uint32_t vote_word(int w) const { return tmem_word() + 8u + 4u * w; }
-  // 1: the V tile in stage s is fp16 (P·V in fp16); 0: it stayed bf16 (split P)
+  // 1: the V tile in stage s is fp16 (P.V in fp16); 0: it stayed bf16 (split P)
   __device__ __forceinline__ uint32_t vflag(uint32_t s) const { return tmem_word() + 16u + 4u * s; }
 };
 
@@ -177,8 +198,8 @@ __device__ __forceinline__ Unit decode_unit(const KParams& p, int u) {
 
 // Bounded mbarrier wait.  False: timed out (recorded) or another role aborted.
 // (Everything is inlined: out-of-line calls do not mix with setmaxnreg.)
-template <int S>
-__device__ __forceinline__ bool wait_bar(const Bars<S>& br, int* status, uint32_t bar,
+template <class BarsT>
+__device__ __forceinline__ bool wait_bar(const BarsT& br, int* status, uint32_t bar,
                                          uint32_t parity, int role) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer_ns();
@@ -216,18 +237,44 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 // ------------------------------------------------------------------ producer
 
 template <int D>
-__device__ void producer_role(const KParams& p, const Bars<Cfg<D>::kStages>& br, uint32_t smem,
+__device__ void producer_role(const KParams& p, const Bars<D>& br, uint32_t smem,
                               const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                               const CUtensorMap* tm_v) {
   using C = Cfg<D>;
-  uint32_t q_phase = 0;     // bit t: parity of tile t's next q_empty wait ^ 1
-  uint32_t q_used = 0;      // bit t: a Q_t load was issued
-  uint32_t stage_used = 0;  // bit s: stage s received a load
-  uint32_t stage_par = 0;   // bit s: phase parity of the last load into stage s
-  uint32_t it = 0;
+  uint32_t q_phase = 0;   // bit t: parity of tile t's next q_empty wait ^ 1
+  uint32_t q_used = 0;    // bit t: a Q_t load was issued
+  uint32_t k_used = 0, k_par = 0;  // per K stage: loaded at least once / parity of the last load
+  uint32_t v_used = 0, v_par = 0;  // per V stage: the same
+  uint32_t kit = 0, vit = 0;       // K and V ring items issued
   const uint64_t pol_keep = ptx::policy_evict_last();
   const uint64_t pol_stream = ptx::policy_evict_first();
   bool ok = true;
+
+  // One K or V tile into the next slot of its ring.
+  auto load_kv = [&](bool is_v, int j, int z_kv) -> bool {
+    uint32_t& it = is_v ? vit : kit;
+    const uint32_t ns = is_v ? C::kVStages : C::kKStages;
+    const uint32_t s = it % ns;
+    const uint32_t par = (it / ns) & 1u;
+    if (!wait_bar(br, p.status, is_v ? br.v_empty(s) : br.k_empty(s), par ^ 1u, kRoleProducer))
+      return false;
+    ++it;
+    const uint32_t full = is_v ? br.v_full(s) : br.k_full(s);
+    const uint32_t dst = smem + (is_v ? C::kOffV : C::kOffK) + s * C::kKVBytes;
+    ptx::mbar_arrive_expect_tx(full, C::kKVBytes);
+#pragma unroll
+    for (int h = 0; h < C::kHalves; ++h)
+      ptx::tma_load_3d_hint(dst + h * C::kSlabKV, is_v ? tm_v : tm_k, full, h * 64, j * BN, z_kv,
+                            pol_keep);
+    if (is_v) {
+      v_used |= 1u << s;
+      v_par = (v_par & ~(1u << s)) | (par << s);
+    } else {
+      k_used |= 1u << s;
+      k_par = (k_par & ~(1u << s)) | (par << s);
+    }
+    return true;
+  };
 
   const int rounds = (p.n_units + gridDim.x - 1) / gridDim.x;
   for (int r = 0; ok && r < rounds; ++r) {
@@ -253,32 +300,17 @@ __device__ void producer_role(const KParams& p, const Bars<Cfg<D>::kStages>& br,
         ptx::tma_load_3d_hint(dst + h * C::kSlabQ, tm_q, br.q_full(t), h * 64, w.m0 + t * BM,
                               w.bh, pol_stream);
     }
-    for (int j = 0; ok && j < n; ++j) {
-#pragma unroll
-      for (int kind = 0; kind < 2; ++kind) {
-        const uint32_t s = it % C::kStages;
-        const uint32_t par = (it / C::kStages) & 1u;
-        if (!wait_bar(br, p.status, br.kv_empty(s), par ^ 1u, kRoleProducer)) {
-          ok = false;
-          break;
-        }
-        ++it;
-        const uint32_t dst = smem + C::kOffKV + s * C::kKVBytes;
-        ptx::mbar_arrive_expect_tx(br.kv_full(s), C::kKVBytes);
-        const CUtensorMap* tm = kind == 0 ? tm_k : tm_v;
-#pragma unroll
-        for (int h = 0; h < C::kHalves; ++h)
-          ptx::tma_load_3d_hint(dst + h * C::kSlabKV, tm, br.kv_full(s), h * 64, j * BN, z_kv,
-                                pol_keep);
-        stage_used |= 1u << s;
-        stage_par = (stage_par & ~(1u << s)) | (par << s);
-      }
-    }
+    // issue order K_0 V_0 | V_1 K_1 | V_2 K_2 ...: each V tile is requested as
+    // soon as its (deeper) ring has room
+    ok = ok && load_kv(false, 0, z_kv) && load_kv(true, 0, z_kv);
+    for (int j = 1; ok && j < n; ++j) ok = load_kv(true, j, z_kv) && load_kv(false, j, z_kv);
   }
   // Never leave with a copy in flight: wait (bounded) for the last load of
   // every buffer.  In a normal run these phases completed long ago.
-  for (int s = 0; s < C::kStages; ++s)
-    if ((stage_used >> s) & 1u) drain_wait(br.kv_full(s), (stage_par >> s) & 1u);
+  for (uint32_t s = 0; s < C::kKStages; ++s)
+    if ((k_used >> s) & 1u) drain_wait(br.k_full(s), (k_par >> s) & 1u);
+  for (uint32_t s = 0; s < C::kVStages; ++s)
+    if ((v_used >> s) & 1u) drain_wait(br.v_full(s), (v_par >> s) & 1u);
   for (int t = 0; t < QT; ++t)
     if ((q_used >> t) & 1u) drain_wait(br.q_full(t), ((q_phase >> t) & 1u) ^ 1u);
 }
@@ -345,18 +377,17 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint6
 }
 
 template <int D, bool BF16>
-__device__ void mma_role(const KParams& p, const Bars<Cfg<D>::kStages>& br, uint32_t smem,
-                         uint32_t tmem) {
+__device__ void mma_role(const KParams& p, const Bars<D>& br, uint32_t smem, uint32_t tmem) {
   using C = Cfg<D>;
   uint32_t q_phase = 0;  // bit t: parity of tile t's next q_full wait
   uint32_t p_phase = 0;  // bit t: parity of tile t's next p_full wait
-  uint32_t it = 0;
+  uint32_t kit = 0, vit = 0;
   // K-major operands (Q, K): leading byte offset unused with 128-byte swizzle,
   // 1024 bytes between 8-row groups.  MN-major V: 64-column slabs kSlabKV
   // apart (leading), 1024 bytes between 8-key groups (stride).
   const uint64_t q_desc0 = ptx::sdesc_sw128(smem + C::kOffQ, 16, 1024);
-  const uint64_t k_desc0 = ptx::sdesc_sw128(smem + C::kOffKV, 16, 1024);
-  const uint64_t v_desc0 = ptx::sdesc_sw128(smem + C::kOffKV, C::kSlabKV, 1024);
+  const uint64_t k_desc0 = ptx::sdesc_sw128(smem + C::kOffK, 16, 1024);
+  const uint64_t v_desc0 = ptx::sdesc_sw128(smem + C::kOffV, C::kSlabKV, 1024);
   bool ok = true;
 
   const int rounds = (p.n_units + gridDim.x - 1) / gridDim.x;
@@ -369,7 +400,8 @@ __device__ void mma_role(const KParams& p, const Bars<Cfg<D>::kStages>& br, uint
 #pragma unroll
     for (int t = 0; t < QT; ++t) {
       if (w.n[t] == 0) continue;
-      if (!__all_sync(0xffffffffu, wait_bar(br, p.status, br.q_full(t), (q_phase >> t) & 1u, kRoleMma))) {
+      if (!__all_sync(0xffffffffu,
+                      wait_bar(br, p.status, br.q_full(t), (q_phase >> t) & 1u, kRoleMma))) {
         ok = false;
         break;
       }
@@ -377,16 +409,18 @@ __device__ void mma_role(const KParams& p, const Bars<Cfg<D>::kStages>& br, uint
     }
     if (!ok) break;
     // K_0
-    const uint32_t sk = it % C::kStages;
-    if (!__all_sync(0xffffffffu, wait_bar(br, p.status, br.kv_full(sk), (it / C::kStages) & 1u, kRoleMma))) break;
-    ++it;
+    const uint32_t sk = kit % C::kKStages;
+    if (!__all_sync(0xffffffffu, wait_bar(br, p.status, br.k_full(sk),
+                                          (kit / C::kKStages) & 1u, kRoleMma)))
+      break;
+    ++kit;
     ptx::tc_fence_after();
 #pragma unroll
     for (int t = 0; t < QT; ++t)
       if (w.n[t] > 0) {
         if (elect_one()) {
           issue_qk<D, BF16>(tmem + C::col_s(t), desc_add(q_desc0, t * C::kQBytes),
-                          desc_add(k_desc0, sk * C::kKVBytes));
+                            desc_add(k_desc0, sk * C::kKVBytes));
         }
         __syncwarp();
         commit_one(br.s_full(t));
@@ -394,17 +428,18 @@ __device__ void mma_role(const KParams& p, const Bars<Cfg<D>::kStages>& br, uint
         // load the next unit's Q_t while this unit finishes
         if (w.n[t] == 1) commit_one(br.q_empty(t));
       }
-    commit_one(br.kv_empty(sk));
+    commit_one(br.k_empty(sk));
 
     for (int j = 0; j < n; ++j) {
-      const uint32_t sv = it % C::kStages;
+      const uint32_t sv = vit % C::kVStages;
       // bf16: wait until the converters have checked (and converted) V_j
-      const uint32_t vbar = BF16 ? br.v_conv(sv) : br.kv_full(sv);
-      if (!__all_sync(0xffffffffu, wait_bar(br, p.status, vbar, (it / C::kStages) & 1u, kRoleMma))) {
+      const uint32_t vbar = BF16 ? br.v_conv(sv) : br.v_full(sv);
+      if (!__all_sync(0xffffffffu,
+                      wait_bar(br, p.status, vbar, (vit / C::kVStages) & 1u, kRoleMma))) {
         ok = false;
         break;
       }
-      ++it;
+      ++vit;
       const bool split = BF16 && ptx::ld_shared_volatile(br.vflag(sv)) == 0u;
       const bool has_next = j + 1 < n;
       uint32_t sk2 = 0;
@@ -412,7 +447,8 @@ __device__ void mma_role(const KParams& p, const Bars<Cfg<D>::kStages>& br, uint
 #pragma unroll
       for (int t = 0; t < QT; ++t) {
         if (j < w.n[t]) {
-          if (!__all_sync(0xffffffffu, wait_bar(br, p.status, br.p_full(t), (p_phase >> t) & 1u, kRoleMma))) {
+          if (!__all_sync(0xffffffffu, wait_bar(br, p.status, br.p_full(t),
+                                                (p_phase >> t) & 1u, kRoleMma))) {
             ok = false;
             break;
           }
@@ -425,21 +461,22 @@ __device__ void mma_role(const KParams& p, const Bars<Cfg<D>::kStages>& br, uint
           __syncwarp();
           if (j == w.n[t] - 1) commit_one(br.o_full(t));
         }
-        if (t == QT - 1) commit_one(br.kv_empty(sv));  // V_j read by every PV above
+        if (t == QT - 1) commit_one(br.v_empty(sv));  // V_j read by every PV above
         if (has_next && !next_loaded) {
-          sk2 = it % C::kStages;
-          if (!__all_sync(0xffffffffu, wait_bar(br, p.status, br.kv_full(sk2), (it / C::kStages) & 1u, kRoleMma))) {
+          sk2 = kit % C::kKStages;
+          if (!__all_sync(0xffffffffu, wait_bar(br, p.status, br.k_full(sk2),
+                                                (kit / C::kKStages) & 1u, kRoleMma))) {
             ok = false;
             break;
           }
-          ++it;
+          ++kit;
           next_loaded = true;
           ptx::tc_fence_after();
         }
         if (j + 1 < w.n[t]) {
           if (elect_one()) {
             issue_qk<D, BF16>(tmem + C::col_s(t), desc_add(q_desc0, t * C::kQBytes),
-                            desc_add(k_desc0, sk2 * C::kKVBytes));
+                              desc_add(k_desc0, sk2 * C::kKVBytes));
           }
           __syncwarp();
           commit_one(br.s_full(t));
@@ -447,7 +484,7 @@ __device__ void mma_role(const KParams& p, const Bars<Cfg<D>::kStages>& br, uint
         }
       }
       if (!ok) break;
-      if (has_next) commit_one(br.kv_empty(sk2));
+      if (has_next) commit_one(br.k_empty(sk2));
     }
   }
   // Every MMA issued by this thread completes before TMEM is released.
@@ -463,12 +500,15 @@ __device__ void mma_role(const KParams& p, const Bars<Cfg<D>::kStages>& br, uint
 // that P.V can use fp16 P.  Otherwise the tile stays bf16 and P is split.
 // The verdict goes to vflag[s]; v_conv[s] signals the MMA issuer and softmax.
 template <int D>
-__device__ void convert_role(const KParams& p, const Bars<Cfg<D>::kStages>& br, uint32_t smem) {
+__device__ void convert_role(const KParams& p, const Bars<D>& br, uint32_t smem) {
   using C = Cfg<D>;
   const int ct = static_cast<int>(threadIdx.x) - 10 * 32;  // 0..63
   const int cw = ct >> 5;
   constexpr int kVec = C::kKVBytes / 16;  // 16-byte vectors per tile
-  uint32_t it = 0;
+  constexpr int kPerThread = kVec / 64;
+  constexpr int kBatch = 8;
+  static_assert(kPerThread % kBatch == 0, "converter batching");
+  uint32_t vit = 0;
   const int rounds = (p.n_units + gridDim.x - 1) / gridDim.x;
   for (int r = 0; r < rounds; ++r) {
     const int u = unit_of(r);
@@ -476,22 +516,27 @@ __device__ void convert_role(const KParams& p, const Bars<Cfg<D>::kStages>& br, 
     const Unit w = decode_unit(p, u);
     const int n = max(w.n[0], w.n[1]);
     for (int j = 0; j < n; ++j) {
-      ++it;  // K_j
-      const uint32_t s = it % C::kStages;
-      const uint32_t par = (it / C::kStages) & 1u;
-      ++it;  // V_j
-      if (!__all_sync(0xffffffffu, wait_bar(br, p.status, br.kv_full(s), par, kRoleConvert)))
+      const uint32_t s = vit % C::kVStages;
+      const uint32_t par = (vit / C::kVStages) & 1u;
+      ++vit;
+      if (!__all_sync(0xffffffffu, wait_bar(br, p.status, br.v_full(s), par, kRoleConvert)))
         return;
-      const uint32_t tile = smem + C::kOffKV + s * C::kKVBytes;
-      // pass 1: largest exponent field of every bf16 half (>= 143: |v| >= 2^16, inf, NaN)
+      const uint32_t tile = smem + C::kOffV + s * C::kKVBytes;
+      // pass 1: largest exponent field of every bf16 half (>= 143: |v| >= 2^16, inf, NaN);
+      // kBatch 16-byte loads in flight per thread
       uint32_t ex = 0;
-#pragma unroll 4
-      for (int k = ct; k < kVec; k += 64) {
-        const uint4 v = ptx::ld_shared_v4(tile + 16u * k);
-        ex = __vmaxu2(ex, v.x & 0x7F807F80u);
-        ex = __vmaxu2(ex, v.y & 0x7F807F80u);
-        ex = __vmaxu2(ex, v.z & 0x7F807F80u);
-        ex = __vmaxu2(ex, v.w & 0x7F807F80u);
+#pragma unroll
+      for (int b0 = 0; b0 < kPerThread; b0 += kBatch) {
+        uint4 v[kBatch];
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) v[i] = ptx::ld_shared_v4(tile + 16u * (ct + 64 * (b0 + i)));
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+          ex = __vmaxu2(ex, v[i].x & 0x7F807F80u);
+          ex = __vmaxu2(ex, v[i].y & 0x7F807F80u);
+          ex = __vmaxu2(ex, v[i].z & 0x7F807F80u);
+          ex = __vmaxu2(ex, v[i].w & 0x7F807F80u);
+        }
       }
       const bool bad_mine = (ex & 0xFFFFu) >= 0x4780u || (ex >> 16) >= 0x4780u;
       const uint32_t bad_warp = __any_sync(0xffffffffu, bad_mine) ? 1u : 0u;
@@ -502,16 +547,20 @@ __device__ void convert_role(const KParams& p, const Bars<Cfg<D>::kStages>& br, 
       ptx::named_barrier_sync(1, 64);  // both votes read before the next tile's
       if (!bad) {
         // pass 2: bf16 pairs -> fp16 pairs, in place
-#pragma unroll 4
-        for (int k = ct; k < kVec; k += 64) {
-          const uint32_t a = tile + 16u * k;
-          const uint4 v = ptx::ld_shared_v4(a);
-          uint4 o;
-          o.x = pack2<false>(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xFFFF0000u));
-          o.y = pack2<false>(__uint_as_float(v.y << 16), __uint_as_float(v.y & 0xFFFF0000u));
-          o.z = pack2<false>(__uint_as_float(v.z << 16), __uint_as_float(v.z & 0xFFFF0000u));
-          o.w = pack2<false>(__uint_as_float(v.w << 16), __uint_as_float(v.w & 0xFFFF0000u));
-          ptx::st_shared_v4(a, o);
+#pragma unroll
+        for (int b0 = 0; b0 < kPerThread; b0 += kBatch) {
+          uint4 v[kBatch];
+#pragma unroll
+          for (int i = 0; i < kBatch; ++i) v[i] = ptx::ld_shared_v4(tile + 16u * (ct + 64 * (b0 + i)));
+#pragma unroll
+          for (int i = 0; i < kBatch; ++i) {
+            uint4 o;
+            o.x = pack2<false>(__uint_as_float(v[i].x << 16), __uint_as_float(v[i].x & 0xFFFF0000u));
+            o.y = pack2<false>(__uint_as_float(v[i].y << 16), __uint_as_float(v[i].y & 0xFFFF0000u));
+            o.z = pack2<false>(__uint_as_float(v[i].z << 16), __uint_as_float(v[i].z & 0xFFFF0000u));
+            o.w = pack2<false>(__uint_as_float(v[i].w << 16), __uint_as_float(v[i].w & 0xFFFF0000u));
+            ptx::st_shared_v4(tile + 16u * (ct + 64 * (b0 + i)), o);
+          }
         }
       }
       if (ct == 0) ptx::st_shared_volatile(br.vflag(s), bad ? 0u : 1u);
@@ -524,8 +573,7 @@ __device__ void convert_role(const KParams& p, const Bars<Cfg<D>::kStages>& br, 
 // ------------------------------------------------------------------ softmax + epilogue
 
 template <int D, bool BF16>
-__device__ void softmax_role(const KParams& p, const Bars<Cfg<D>::kStages>& br, uint32_t tmem,
-                             int t) {
+__device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t tmem, int t) {
   using C = Cfg<D>;
   const int lane_row = threadIdx.x & 127;           // row within the tile = TMEM lane
   const uint32_t quad = (threadIdx.x >> 5) & 3u;    // this warp's 32-lane TMEM quadrant
@@ -533,15 +581,15 @@ __device__ void softmax_role(const KParams& p, const Bars<Cfg<D>::kStages>& br, 
   const uint32_t t_o = tmem + ((quad * 32u) << 16) + C::col_o(t);
   const float scale_log2 = p.scale_log2;
   uint32_t s_phase = 0, o_phase = 0;
-  uint32_t items = 0;  // K/V ring items of the units before this one (K_0 V_0 K_1 V_1 ...)
+  uint32_t v_items = 0;  // V ring items of the units before this one
 
   const int rounds = (p.n_units + gridDim.x - 1) / gridDim.x;
   for (int r = 0; r < rounds; ++r) {
     const int u = unit_of(r);
     if (u >= p.n_units) continue;
     const Unit w = decode_unit(p, u);
-    const uint32_t item_base = items;
-    items += 2u * static_cast<uint32_t>(max(w.n[0], w.n[1]));
+    const uint32_t v_base = v_items;
+    v_items += static_cast<uint32_t>(max(w.n[0], w.n[1]));
     const int r0 = w.m0 + t * BM;
     if (r0 >= p.L) continue;
     const int row = r0 + lane_row;
@@ -610,9 +658,9 @@ __device__ void softmax_role(const KParams& p, const Bars<Cfg<D>::kStages>& br, 
       // bf16 inputs: is V_j in fp16 now (converted) or still bf16?
       bool split = false;
       if constexpr (BF16) {
-        const uint32_t vi = item_base + 2u * static_cast<uint32_t>(j) + 1u;
-        const uint32_t vs = vi % C::kStages;
-        ok = wait_bar(br, p.status, br.v_conv(vs), (vi / C::kStages) & 1u, kRoleSoftmax);
+        const uint32_t vi = v_base + static_cast<uint32_t>(j);
+        const uint32_t vs = vi % C::kVStages;
+        ok = wait_bar(br, p.status, br.v_conv(vs), (vi / C::kVStages) & 1u, kRoleSoftmax);
         if (!__all_sync(0xffffffffu, ok)) {
           ok = false;
           break;
@@ -739,7 +787,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t smem = (ptx::smem_u32(smem_raw) + 1023u) & ~1023u;
-  const Bars<C::kStages> br{smem + C::kOffBar};
+  const Bars<D> br{smem + C::kOffBar};
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -752,9 +800,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(br.p_full(t), BM);
       ptx::mbar_init(br.o_full(t), 1);
     }
-    for (int s = 0; s < C::kStages; ++s) {
-      ptx::mbar_init(br.kv_full(s), 1);
-      ptx::mbar_init(br.kv_empty(s), 1);
+    for (int s = 0; s < C::kKStages; ++s) {
+      ptx::mbar_init(br.k_full(s), 1);
+      ptx::mbar_init(br.k_empty(s), 1);
+    }
+    for (int s = 0; s < C::kVStages; ++s) {
+      ptx::mbar_init(br.v_full(s), 1);
+      ptx::mbar_init(br.v_empty(s), 1);
       ptx::mbar_init(br.v_conv(s), 64);  // every converter thread arrives
     }
     ptx::mbar_init(br.drain(), 1);
@@ -837,12 +889,12 @@ cudaError_t launch_instance(const Problem& pr, const CUtensorMap* maps, int num_
 
 bool tc_config(int D, TcConfig* out) {
   if (D == 64) {
-    *out = {BM, QT, BN, Cfg<64>::kStages, kThreads, Cfg<64>::kSmemBytes,
+    *out = {BM, QT, BN, Cfg<64>::kKStages + Cfg<64>::kVStages, kThreads, Cfg<64>::kSmemBytes,
             static_cast<int>(Cfg<64>::kTmemCols)};
     return true;
   }
   if (D == 128) {
-    *out = {BM, QT, BN, Cfg<128>::kStages, kThreads, Cfg<128>::kSmemBytes,
+    *out = {BM, QT, BN, Cfg<128>::kKStages + Cfg<128>::kVStages, kThreads, Cfg<128>::kSmemBytes,
             static_cast<int>(Cfg<128>::kTmemCols)};
     return true;
   }
