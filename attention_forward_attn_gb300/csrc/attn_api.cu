@@ -2,7 +2,8 @@
 //
 // Validates arguments (no device synchronisation), keeps one device status
 // word per GPU, encodes the TMA tensor maps of Q, K and V, and launches the
-// kernels on the caller's stream.  Nothing here allocates per call.
+// kernels on the caller's stream.  bf16 calls take a stream-ordered workspace
+// (the fp16 copy of V and its tile flags) from a per-device pool owned here.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -24,6 +25,7 @@ struct DeviceState {
   bool arch_ok = false;
   int num_sms = 0;
   int* status = nullptr;  // one int of device memory
+  cudaMemPool_t pool = nullptr;  // bf16 workspaces (created on first bf16 call)
 };
 
 std::mutex g_mu;
@@ -131,6 +133,32 @@ attn_status_t device_state(int* dev_out, DeviceState** st_out) {
   return ATTN_OK;
 }
 
+// The device's workspace pool: memory stays reserved between calls (release
+// threshold: never), so after the first bf16 call of a given size the
+// stream-ordered allocation is a pool lookup.
+attn_status_t workspace_pool(int dev, DeviceState* st, cudaMemPool_t* out) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (st->pool == nullptr) {
+    cudaMemPoolProps props = {};
+    props.allocType = cudaMemAllocationTypePinned;
+    props.handleTypes = cudaMemHandleTypeNone;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    cudaMemPool_t pool = nullptr;
+    cudaError_t e = cudaMemPoolCreate(&pool, &props);
+    if (e != cudaSuccess) return cuda_fail(e);
+    uint64_t keep = UINT64_MAX;
+    e = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+    if (e != cudaSuccess) {
+      cudaMemPoolDestroy(pool);
+      return cuda_fail(e);
+    }
+    st->pool = pool;
+  }
+  *out = st->pool;
+  return ATTN_OK;
+}
+
 }  // namespace
 
 namespace attn {
@@ -165,6 +193,7 @@ Problem make_problem(const void* q, const void* k, const void* v, void* o, float
   p.lse = lse;
   p.valid_len = valid_len;
   p.status = status;
+  p.vflags = nullptr;
   p.B = B;
   p.Hq = Hq;
   p.Hkv = Hkv;
@@ -196,13 +225,39 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
   attn::TcConfig cfg;
   if (!attn::tc_config(D, &cfg)) return ATTN_ERR_HEADDIM;
   const bool bf16 = dtype == ATTN_BF16;
-  CUtensorMap maps[3];
+  CUtensorMap maps[4];
   if ((s = encode_map(&maps[0], q, B * Hq, L, D, cfg.block_m, bf16)) != ATTN_OK) return s;
   if ((s = encode_map(&maps[1], k, B * Hkv, L, D, cfg.block_n, bf16)) != ATTN_OK) return s;
   if ((s = encode_map(&maps[2], v, B * Hkv, L, D, cfg.block_n, bf16)) != ATTN_OK) return s;
+  maps[3] = maps[2];
   Problem p = make_problem(q, k, v, o, lse, B, Hq, Hkv, L, D, sm_scale, causal, valid_len, dtype,
                            stream, st->status);
+  void* ws = nullptr;
+  if (bf16) {
+    // workspace: fp16 copy of V, then the per-tile flags
+    cudaMemPool_t pool = nullptr;
+    if ((s = workspace_pool(dev, st, &pool)) != ATTN_OK) return s;
+    cudaError_t e = cudaMallocFromPoolAsync(&ws, static_cast<size_t>(attn::vconv_workspace_bytes(p)),
+                                            pool, p.stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    const size_t v_bytes = static_cast<size_t>(B) * Hkv * L * D * 2;
+    int* flags = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + v_bytes);
+    s = encode_map(&maps[3], ws, B * Hkv, L, D, cfg.block_n, false);
+    if (s == ATTN_OK) {
+      e = attn::launch_vconv(p, ws, flags);
+      if (e != cudaSuccess) s = cuda_fail(e);
+    }
+    if (s != ATTN_OK) {
+      cudaFreeAsync(ws, p.stream);
+      return s;
+    }
+    p.vflags = flags;
+  }
   cudaError_t e = attn::launch_tc(p, maps, st->num_sms);
+  if (ws != nullptr) {
+    const cudaError_t ef = cudaFreeAsync(ws, p.stream);
+    if (e == cudaSuccess) e = ef;
+  }
   if (e != cudaSuccess) return cuda_fail(e);
   return ATTN_OK;
 }
@@ -313,6 +368,11 @@ void attn_shutdown(void) {
     if (g_dev[d].status != nullptr) {
       if (cudaSetDevice(d) == cudaSuccess) cudaFree(g_dev[d].status);
       g_dev[d].status = nullptr;
+    }
+    if (g_dev[d].pool != nullptr) {
+      // released once the workspaces still queued have been freed
+      cudaMemPoolDestroy(g_dev[d].pool);
+      g_dev[d].pool = nullptr;
     }
   }
   if (have_cur) cudaSetDevice(cur);

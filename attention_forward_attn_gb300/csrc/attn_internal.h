@@ -17,7 +17,6 @@ enum : int {
   kRoleMma = 2 << 8,
   kRoleSoftmax = 4 << 8,
   kRoleEpilogue = 8 << 8,
-  kRoleConvert = 16 << 8,
 };
 
 // Problem description handed to a kernel launcher (already validated).
@@ -29,6 +28,9 @@ struct Problem {
   float* lse;              // may be null
   const int32_t* valid_len;  // may be null
   int* status;             // device status word
+  // bf16: per (b*Hkv + h, 128-key tile) flag from the V pre-pass (1 = exact
+  // fp16 copy of the tile exists); null = no copy (every tile split)
+  const int* vflags;
   int B, Hq, Hkv, L, D;
   float sm_scale;
   int causal;
@@ -49,8 +51,14 @@ struct TcConfig {
 
 bool tc_config(int D, TcConfig* out);
 
-// Tensor-core (tcgen05/TMA) forward.  maps: Q, K, V tensor maps.
+// Tensor-core (tcgen05/TMA) forward.  maps: Q, K, V and the fp16 copy of V
+// (bf16 inputs with p.vflags set; any valid map otherwise, it is not read).
 cudaError_t launch_tc(const Problem& p, const CUtensorMap* maps, int num_sms);
+
+// bf16 V pre-pass (attn_vconv.cu): bytes of its workspace (the fp16 copy of
+// V, then one int flag per (b*Hkv + h, 128-key tile)), and its launch.
+int64_t vconv_workspace_bytes(const Problem& p);
+cudaError_t launch_vconv(const Problem& p, void* v16, int* flags);
 
 // SIMT cross-check forward.
 cudaError_t launch_simt(const Problem& p);

@@ -9,12 +9,12 @@
 // How (one CTA per SM, persistent over work units):
 //   * work unit = (b, h_q, 256 query rows) = two 128-row query tiles that share
 //     one stream of K/V tiles (128 keys each);
-//   * warp 8 (producer): TMA loads of the two Q tiles and of the K/V ring,
-//     128-byte swizzled, into a 4-stage (D=128) / 8-stage (D=64) ring;
-//   * warp 9 (MMA issuer, one thread): S_t = Q_t K^T into TMEM (fp32), then
-//     O_t += P_t V with P_t read from TMEM, interleaved PV_0, S_0(next),
-//     PV_1, S_1(next) so the tensor core works on one tile while the other
-//     tile's softmax runs;
+//   * warp 8 (producer): TMA loads of the two Q tiles and of the K and V rings
+//     (2 + 3 stages at D=128, 4 + 4 at D=64), 128-byte swizzled;
+//   * warps 9 and 10 (MMA issuers, one per query tile t): S_t = Q_t K^T into
+//     TMEM (fp32), then O_t += P_t V with P_t read from TMEM.  Each warp
+//     issues PV_t(j) and then S_t(j+1); with two issuers the tensor core keeps
+//     working on one tile's MMAs while the other issuer waits on its barriers;
 //   * warps 0-3 / 4-7 (softmax, one thread per query row = TMEM lane): load
 //     the S row, mask (only on boundary tiles), row max, ex2.approx, row sum,
 //     write P into TMEM over the S columns, rescale the O row in TMEM when the
@@ -23,6 +23,13 @@
 // Causal units skip every key tile above the diagonal; padded units skip every
 // key tile at or beyond valid_len[b]; a unit with no visible key writes O = 0
 // and LSE = -inf without touching the tensor core.
+//
+// bf16 inputs: P.V runs with fp16 P (unit roundoff 2^-11) whenever the V tile
+// has an exact fp16 copy -- made once per call by the pre-pass in
+// attn_vconv.cu, which flags every 128-key tile whose values are all finite
+// with |v| < 2^16 -- and the producer then loads that copy.  A tile without
+// one stays bf16 and P is split into two bf16 terms (see the softmax).
+// Without flags (no workspace) every bf16 tile takes the split form.
 //
 // Every mbarrier wait is bounded: after ATTN_WAIT_LIMIT_NS the waiting role
 // records a timeout in the device status word, raises a CTA-wide abort flag
@@ -46,7 +53,7 @@ constexpr int QT = 2;         // query tiles per work unit
 constexpr int BN = 128;       // keys per K/V tile
 constexpr int kUnitRows = QT * BM;
 constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kMmaWarp0 = 9;   // MMA issuer of query tile 0; tile 1 has warp 10
 constexpr int kThreads = 384;  // warpgroups: softmax tile 0, softmax tile 1, producer/MMA
 // Register split between warpgroups (setmaxnreg).  The CTA is launched with
 // kLaunchRegs per thread (the __launch_bounds__(384, 1) ceiling: 3 warps per
@@ -62,8 +69,8 @@ constexpr float kLn2 = 0.69314718055994531f;
 
 template <int D>
 struct Cfg {
-  // separate rings for K and V tiles; V gets the extra stage so that bf16 V
-  // tiles reach shared memory (and the converters) well before their P.V
+  // separate rings for K and V tiles; V gets the extra stage (its tiles are
+  // consumed later in each step than the K tiles)
   static constexpr int kKStages = (D == 128) ? 2 : 4;
   static constexpr int kVStages = (D == 128) ? 3 : 4;
   static constexpr int kHalves = D / 64;           // 64-column (128-byte) slabs per row
@@ -76,12 +83,11 @@ struct Cfg {
   static constexpr int kOffV = kOffK + kKStages * kKVBytes;
   static constexpr int kOffBar = kOffV + kVStages * kKVBytes;
   // barrier block: q_full[QT] q_empty[QT] k_full[KS] k_empty[KS] v_full[VS]
-  // v_empty[VS] v_conv[VS] s_full[QT] p_full[QT] o_full[QT] drain, then
-  // 32-bit words: TMEM base, abort flag, two converter votes, one precision
-  // flag per V stage
-  static constexpr int kNumBars = 5 * QT + 2 * kKStages + 3 * kVStages + 1;
+  // v_empty[VS] s_full[QT] p_full[QT] o_full[QT] drain, then 32-bit words:
+  // TMEM base, abort flag
+  static constexpr int kNumBars = 5 * QT + 2 * kKStages + 2 * kVStages + 1;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-  static constexpr int kMiscBytes = 16 + 4 * kVStages;
+  static constexpr int kMiscBytes = 8;
   static constexpr int kSmemBytes = kOffMisc + kMiscBytes + 1024;  // + slack to align the base
   // TMEM columns: S_0, S_1 (fp32, BN each; P_t is written over S_t), then
   // O_0, O_1 (fp32, D each).
@@ -112,27 +118,20 @@ struct Bars {
   __device__ __forceinline__ uint32_t v_empty(uint32_t s) const {
     return base + 8u * (2 * QT + 2 * KS + VS + s);
   }
-  // V tile in stage s checked (and converted to fp16 when in range): converters -> MMA, softmax
-  __device__ __forceinline__ uint32_t v_conv(uint32_t s) const {
-    return base + 8u * (2 * QT + 2 * KS + 2 * VS + s);
-  }
   __device__ __forceinline__ uint32_t s_full(int t) const {
-    return base + 8u * (2 * QT + 2 * KS + 3 * VS + t);
+    return base + 8u * (2 * QT + 2 * KS + 2 * VS + t);
   }
   __device__ __forceinline__ uint32_t p_full(int t) const {
-    return base + 8u * (3 * QT + 2 * KS + 3 * VS + t);
+    return base + 8u * (3 * QT + 2 * KS + 2 * VS + t);
   }
   __device__ __forceinline__ uint32_t o_full(int t) const {
-    return base + 8u * (4 * QT + 2 * KS + 3 * VS + t);
+    return base + 8u * (4 * QT + 2 * KS + 2 * VS + t);
   }
-  __device__ __forceinline__ uint32_t drain() const { return base + 8u * (5 * QT + 2 * KS + 3 * VS); }
+  __device__ __forceinline__ uint32_t drain() const { return base + 8u * (5 * QT + 2 * KS + 2 * VS); }
   __device__ __forceinline__ uint32_t tmem_word() const {
-    return base + 8u * (5 * QT + 2 * KS + 3 * VS + 1);
+    return base + 8u * (5 * QT + 2 * KS + 2 * VS + 1);
   }
   __device__ __forceinline__ uint32_t abort_word() const { return tmem_word() + 4u; }
-  __device__ __forceinline__ uint32_t vote_word(int w) const { return tmem_word() + 8u + 4u * w; }
-  // 1: the V tile in stage s is fp16 (P.V in fp16); 0: it stayed bf16 (split P)
-  __device__ __forceinline__ uint32_t vflag(uint32_t s) const { return tmem_word() + 16u + 4u * s; }
 };
 
 struct KParams {
@@ -140,6 +139,10 @@ struct KParams {
   float* lse;
   const int32_t* valid_len;
   int* status;
+  // bf16 only: per (b, h_kv, 128-key tile) 1 = the fp16 copy of the V tile is
+  // exact, 0 = use the bf16 tile; null = no fp16 copy exists
+  const int* vflags;
+  int n_kt;     // 128-key tiles per (b, h_kv)
   int B, Hq, Hkv, L, G;
   int n_mb;     // 256-row blocks per (b, h_q)
   int n_units;  // B * Hq * n_mb
@@ -223,6 +226,17 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
+// bf16 inputs: true when P.V for key tile j of KV head z takes the split form
+// (no exact fp16 copy of the V tile).  fp16 inputs: never.
+template <bool BF16>
+__device__ __forceinline__ bool v_split(const KParams& p, int z_kv, int j) {
+  if constexpr (!BF16) {
+    return false;
+  } else {
+    return p.vflags == nullptr || __ldg(p.vflags + static_cast<int64_t>(z_kv) * p.n_kt + j) == 0;
+  }
+}
+
 template <bool BF16>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   if constexpr (BF16) {
@@ -236,10 +250,10 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 
 // ------------------------------------------------------------------ producer
 
-template <int D>
+template <int D, bool BF16>
 __device__ void producer_role(const KParams& p, const Bars<D>& br, uint32_t smem,
                               const CUtensorMap* tm_q, const CUtensorMap* tm_k,
-                              const CUtensorMap* tm_v) {
+                              const CUtensorMap* tm_v, const CUtensorMap* tm_v16) {
   using C = Cfg<D>;
   uint32_t q_phase = 0;   // bit t: parity of tile t's next q_empty wait ^ 1
   uint32_t q_used = 0;    // bit t: a Q_t load was issued
@@ -261,11 +275,12 @@ __device__ void producer_role(const KParams& p, const Bars<D>& br, uint32_t smem
     ++it;
     const uint32_t full = is_v ? br.v_full(s) : br.k_full(s);
     const uint32_t dst = smem + (is_v ? C::kOffV : C::kOffK) + s * C::kKVBytes;
+    // bf16 V: the exact fp16 copy of the tile when there is one
+    const CUtensorMap* map = !is_v ? tm_k : ((!BF16 || v_split<BF16>(p, z_kv, j)) ? tm_v : tm_v16);
     ptx::mbar_arrive_expect_tx(full, C::kKVBytes);
 #pragma unroll
     for (int h = 0; h < C::kHalves; ++h)
-      ptx::tma_load_3d_hint(dst + h * C::kSlabKV, is_v ? tm_v : tm_k, full, h * 64, j * BN, z_kv,
-                            pol_keep);
+      ptx::tma_load_3d_hint(dst + h * C::kSlabKV, map, full, h * 64, j * BN, z_kv, pol_keep);
     if (is_v) {
       v_used |= 1u << s;
       v_par = (v_par & ~(1u << s)) | (par << s);
@@ -358,7 +373,7 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t q_desc, uint6
 
 // O += P V: A = P from TMEM (16-bit pairs, 8 columns per 16 keys), B = V tile
 // as an MN-major 128-byte-swizzled operand (16 keys = two 8-row groups).
-// fp16 V tile (fp16 inputs, or a bf16 tile the converters turned into fp16):
+// fp16 V tile (fp16 inputs, or the exact fp16 copy of a bf16 tile):
 // O += P V with fp16 P.  bf16 V tile (split): O += [P_hi | P_lo] [V; V], the
 // same V tile read twice.
 template <int D>
@@ -376,18 +391,62 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint6
   }
 }
 
+// Release of a K or V ring slot by an issuer warp: after the warp's MMAs that
+// read it (commit), or at once when its tile does not use the slot.  Each
+// slot's empty barrier expects one release from each of the two issuers.
+__device__ __forceinline__ void release_slot(uint32_t bar, bool used) {
+  if (used) {
+    commit_one(bar);
+  } else {
+    if (elect_one()) ptx::mbar_arrive(bar);
+    __syncwarp();
+  }
+}
+
+// Next K tile of the ring for the issuer of query tile t: wait for it, issue
+// S_t = Q_t K^T when it is key tile jn of this query tile (nt key tiles),
+// release the slot.  False: the wait gave up.
 template <int D, bool BF16>
-__device__ void mma_role(const KParams& p, const Bars<D>& br, uint32_t smem, uint32_t tmem) {
+__device__ __forceinline__ bool mma_next_k(const KParams& p, const Bars<D>& br, int t, uint32_t& kit,
+                                           int jn, int nt, uint32_t t_s, uint64_t q_desc,
+                                           uint64_t k_desc0) {
   using C = Cfg<D>;
-  uint32_t q_phase = 0;  // bit t: parity of tile t's next q_full wait
-  uint32_t p_phase = 0;  // bit t: parity of tile t's next p_full wait
+  const uint32_t sk = kit % C::kKStages;
+  if (!__all_sync(0xffffffffu, wait_bar(br, p.status, br.k_full(sk),
+                                        (kit / C::kKStages) & 1u, kRoleMma)))
+    return false;
+  ++kit;
+  const bool use = jn < nt;
+  if (use) {
+    ptx::tc_fence_after();
+    if (elect_one()) issue_qk<D, BF16>(t_s, q_desc, desc_add(k_desc0, sk * C::kKVBytes));
+    __syncwarp();
+    commit_one(br.s_full(t));
+    // Q_t is free once the unit's last S_t MMA completes: the producer can
+    // load the next unit's Q_t while this unit finishes
+    if (jn == nt - 1) commit_one(br.q_empty(t));
+  }
+  release_slot(br.k_empty(sk), use);
+  return true;
+}
+
+// Issuer of query tile t (whole warp; one elected lane issues).  It walks
+// every K and V ring item of every unit in the producer's order, so both
+// issuers stay in phase with the rings even when one tile has fewer key tiles
+// (causal diagonal) or none.
+template <int D, bool BF16>
+__device__ void mma_role(const KParams& p, const Bars<D>& br, uint32_t smem, uint32_t tmem, int t) {
+  using C = Cfg<D>;
+  uint32_t q_phase = 0, p_phase = 0;
   uint32_t kit = 0, vit = 0;
   // K-major operands (Q, K): leading byte offset unused with 128-byte swizzle,
   // 1024 bytes between 8-row groups.  MN-major V: 64-column slabs kSlabKV
   // apart (leading), 1024 bytes between 8-key groups (stride).
-  const uint64_t q_desc0 = ptx::sdesc_sw128(smem + C::kOffQ, 16, 1024);
+  const uint64_t q_desc = ptx::sdesc_sw128(smem + C::kOffQ + t * C::kQBytes, 16, 1024);
   const uint64_t k_desc0 = ptx::sdesc_sw128(smem + C::kOffK, 16, 1024);
   const uint64_t v_desc0 = ptx::sdesc_sw128(smem + C::kOffV, C::kSlabKV, 1024);
+  const uint32_t t_s = tmem + C::col_s(t);
+  const uint32_t t_o = tmem + C::col_o(t);
   bool ok = true;
 
   const int rounds = (p.n_units + gridDim.x - 1) / gridDim.x;
@@ -396,178 +455,45 @@ __device__ void mma_role(const KParams& p, const Bars<D>& br, uint32_t smem, uin
     if (u >= p.n_units) continue;
     const Unit w = decode_unit(p, u);
     const int n = max(w.n[0], w.n[1]);
+    const int nt = t == 0 ? w.n[0] : w.n[1];  // (a select keeps Unit in registers)
     if (n == 0) continue;
-#pragma unroll
-    for (int t = 0; t < QT; ++t) {
-      if (w.n[t] == 0) continue;
-      if (!__all_sync(0xffffffffu,
-                      wait_bar(br, p.status, br.q_full(t), (q_phase >> t) & 1u, kRoleMma))) {
-        ok = false;
-        break;
-      }
-      q_phase ^= 1u << t;
+    const int z_kv = w.b * p.Hkv + w.hkv;
+    if (nt > 0) {
+      if (!__all_sync(0xffffffffu, wait_bar(br, p.status, br.q_full(t), q_phase, kRoleMma))) break;
+      q_phase ^= 1u;
     }
-    if (!ok) break;
-    // K_0
-    const uint32_t sk = kit % C::kKStages;
-    if (!__all_sync(0xffffffffu, wait_bar(br, p.status, br.k_full(sk),
-                                          (kit / C::kKStages) & 1u, kRoleMma)))
-      break;
-    ++kit;
-    ptx::tc_fence_after();
-#pragma unroll
-    for (int t = 0; t < QT; ++t)
-      if (w.n[t] > 0) {
-        if (elect_one()) {
-          issue_qk<D, BF16>(tmem + C::col_s(t), desc_add(q_desc0, t * C::kQBytes),
-                            desc_add(k_desc0, sk * C::kKVBytes));
-        }
-        __syncwarp();
-        commit_one(br.s_full(t));
-        // Q_t is free once the unit's last S_t MMA completes: the producer can
-        // load the next unit's Q_t while this unit finishes
-        if (w.n[t] == 1) commit_one(br.q_empty(t));
-      }
-    commit_one(br.k_empty(sk));
-
+    if (!mma_next_k<D, BF16>(p, br, t, kit, 0, nt, t_s, q_desc, k_desc0)) break;
     for (int j = 0; j < n; ++j) {
       const uint32_t sv = vit % C::kVStages;
-      // bf16: wait until the converters have checked (and converted) V_j
-      const uint32_t vbar = BF16 ? br.v_conv(sv) : br.v_full(sv);
       if (!__all_sync(0xffffffffu,
-                      wait_bar(br, p.status, vbar, (vit / C::kVStages) & 1u, kRoleMma))) {
+                      wait_bar(br, p.status, br.v_full(sv), (vit / C::kVStages) & 1u, kRoleMma))) {
         ok = false;
         break;
       }
       ++vit;
-      const bool split = BF16 && ptx::ld_shared_volatile(br.vflag(sv)) == 0u;
-      const bool has_next = j + 1 < n;
-      uint32_t sk2 = 0;
-      bool next_loaded = false;
-#pragma unroll
-      for (int t = 0; t < QT; ++t) {
-        if (j < w.n[t]) {
-          if (!__all_sync(0xffffffffu, wait_bar(br, p.status, br.p_full(t),
-                                                (p_phase >> t) & 1u, kRoleMma))) {
-            ok = false;
-            break;
-          }
-          p_phase ^= 1u << t;
-          ptx::tc_fence_after();
-          if (elect_one()) {
-            issue_pv<D>(tmem + C::col_o(t), tmem + C::col_s(t),
-                        desc_add(v_desc0, sv * C::kKVBytes), j > 0, split);
-          }
-          __syncwarp();
-          if (j == w.n[t] - 1) commit_one(br.o_full(t));
+      const bool use = j < nt;
+      if (use) {
+        const bool split = v_split<BF16>(p, z_kv, j);
+        if (!__all_sync(0xffffffffu, wait_bar(br, p.status, br.p_full(t), p_phase, kRoleMma))) {
+          ok = false;
+          break;
         }
-        if (t == QT - 1) commit_one(br.v_empty(sv));  // V_j read by every PV above
-        if (has_next && !next_loaded) {
-          sk2 = kit % C::kKStages;
-          if (!__all_sync(0xffffffffu, wait_bar(br, p.status, br.k_full(sk2),
-                                                (kit / C::kKStages) & 1u, kRoleMma))) {
-            ok = false;
-            break;
-          }
-          ++kit;
-          next_loaded = true;
-          ptx::tc_fence_after();
-        }
-        if (j + 1 < w.n[t]) {
-          if (elect_one()) {
-            issue_qk<D, BF16>(tmem + C::col_s(t), desc_add(q_desc0, t * C::kQBytes),
-                              desc_add(k_desc0, sk2 * C::kKVBytes));
-          }
-          __syncwarp();
-          commit_one(br.s_full(t));
-          if (j + 2 == w.n[t]) commit_one(br.q_empty(t));  // last S_t of the unit
-        }
+        p_phase ^= 1u;
+        ptx::tc_fence_after();
+        if (elect_one()) issue_pv<D>(t_o, t_s, desc_add(v_desc0, sv * C::kKVBytes), j > 0, split);
+        __syncwarp();
+        if (j == nt - 1) commit_one(br.o_full(t));
       }
-      if (!ok) break;
-      if (has_next) commit_one(br.k_empty(sk2));
+      release_slot(br.v_empty(sv), use);
+      if (j + 1 < n && !mma_next_k<D, BF16>(p, br, t, kit, j + 1, nt, t_s, q_desc, k_desc0)) {
+        ok = false;
+        break;
+      }
     }
   }
-  // Every MMA issued by this thread completes before TMEM is released.
+  // Every MMA issued by this warp completes before TMEM is released.
   commit_one(br.drain());
   drain_wait(br.drain(), 0);
-}
-
-// ------------------------------------------------------------------ V converters (bf16 only)
-
-// Warps 10-11.  For every V tile (in ring order) they check whether all its
-// bf16 values are finite with |v| < 65536; if so they rewrite the tile in
-// place as fp16 (exact for |v| >= 2^-14, within 2^-25 absolutely below), so
-// that P.V can use fp16 P.  Otherwise the tile stays bf16 and P is split.
-// The verdict goes to vflag[s]; v_conv[s] signals the MMA issuer and softmax.
-template <int D>
-__device__ void convert_role(const KParams& p, const Bars<D>& br, uint32_t smem) {
-  using C = Cfg<D>;
-  const int ct = static_cast<int>(threadIdx.x) - 10 * 32;  // 0..63
-  const int cw = ct >> 5;
-  constexpr int kVec = C::kKVBytes / 16;  // 16-byte vectors per tile
-  constexpr int kPerThread = kVec / 64;
-  constexpr int kBatch = 8;
-  static_assert(kPerThread % kBatch == 0, "converter batching");
-  uint32_t vit = 0;
-  const int rounds = (p.n_units + gridDim.x - 1) / gridDim.x;
-  for (int r = 0; r < rounds; ++r) {
-    const int u = unit_of(r);
-    if (u >= p.n_units) continue;
-    const Unit w = decode_unit(p, u);
-    const int n = max(w.n[0], w.n[1]);
-    for (int j = 0; j < n; ++j) {
-      const uint32_t s = vit % C::kVStages;
-      const uint32_t par = (vit / C::kVStages) & 1u;
-      ++vit;
-      if (!__all_sync(0xffffffffu, wait_bar(br, p.status, br.v_full(s), par, kRoleConvert)))
-        return;
-      const uint32_t tile = smem + C::kOffV + s * C::kKVBytes;
-      // pass 1: largest exponent field of every bf16 half (>= 143: |v| >= 2^16, inf, NaN);
-      // kBatch 16-byte loads in flight per thread
-      uint32_t ex = 0;
-#pragma unroll
-      for (int b0 = 0; b0 < kPerThread; b0 += kBatch) {
-        uint4 v[kBatch];
-#pragma unroll
-        for (int i = 0; i < kBatch; ++i) v[i] = ptx::ld_shared_v4(tile + 16u * (ct + 64 * (b0 + i)));
-#pragma unroll
-        for (int i = 0; i < kBatch; ++i) {
-          ex = __vmaxu2(ex, v[i].x & 0x7F807F80u);
-          ex = __vmaxu2(ex, v[i].y & 0x7F807F80u);
-          ex = __vmaxu2(ex, v[i].z & 0x7F807F80u);
-          ex = __vmaxu2(ex, v[i].w & 0x7F807F80u);
-        }
-      }
-      const bool bad_mine = (ex & 0xFFFFu) >= 0x4780u || (ex >> 16) >= 0x4780u;
-      const uint32_t bad_warp = __any_sync(0xffffffffu, bad_mine) ? 1u : 0u;
-      if ((ct & 31) == 0) ptx::st_shared_volatile(br.vote_word(cw), bad_warp);
-      ptx::named_barrier_sync(1, 64);
-      const bool bad = (ptx::ld_shared_volatile(br.vote_word(0)) |
-                        ptx::ld_shared_volatile(br.vote_word(1))) != 0u;
-      ptx::named_barrier_sync(1, 64);  // both votes read before the next tile's
-      if (!bad) {
-        // pass 2: bf16 pairs -> fp16 pairs, in place
-#pragma unroll
-        for (int b0 = 0; b0 < kPerThread; b0 += kBatch) {
-          uint4 v[kBatch];
-#pragma unroll
-          for (int i = 0; i < kBatch; ++i) v[i] = ptx::ld_shared_v4(tile + 16u * (ct + 64 * (b0 + i)));
-#pragma unroll
-          for (int i = 0; i < kBatch; ++i) {
-            uint4 o;
-            o.x = pack2<false>(__uint_as_float(v[i].x << 16), __uint_as_float(v[i].x & 0xFFFF0000u));
-            o.y = pack2<false>(__uint_as_float(v[i].y << 16), __uint_as_float(v[i].y & 0xFFFF0000u));
-            o.z = pack2<false>(__uint_as_float(v[i].z << 16), __uint_as_float(v[i].z & 0xFFFF0000u));
-            o.w = pack2<false>(__uint_as_float(v[i].w << 16), __uint_as_float(v[i].w & 0xFFFF0000u));
-            ptx::st_shared_v4(tile + 16u * (ct + 64 * (b0 + i)), o);
-          }
-        }
-      }
-      if (ct == 0) ptx::st_shared_volatile(br.vflag(s), bad ? 0u : 1u);
-      ptx::fence_proxy_async_shared();  // our writes before the tensor core's reads
-      ptx::mbar_arrive(br.v_conv(s));
-    }
-  }
 }
 
 // ------------------------------------------------------------------ softmax + epilogue
@@ -581,15 +507,13 @@ __device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t tmem,
   const uint32_t t_o = tmem + ((quad * 32u) << 16) + C::col_o(t);
   const float scale_log2 = p.scale_log2;
   uint32_t s_phase = 0, o_phase = 0;
-  uint32_t v_items = 0;  // V ring items of the units before this one
 
   const int rounds = (p.n_units + gridDim.x - 1) / gridDim.x;
   for (int r = 0; r < rounds; ++r) {
     const int u = unit_of(r);
     if (u >= p.n_units) continue;
     const Unit w = decode_unit(p, u);
-    const uint32_t v_base = v_items;
-    v_items += static_cast<uint32_t>(max(w.n[0], w.n[1]));
+    const int z_kv = w.b * p.Hkv + w.hkv;
     const int r0 = w.m0 + t * BM;
     if (r0 >= p.L) continue;
     const int row = r0 + lane_row;
@@ -615,6 +539,8 @@ __device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t tmem,
     float l = 0.f;
     bool ok = true;
     for (int j = 0; j < nt; ++j) {
+      // P format of this key tile: fp16 P, or the bf16 pair (split)
+      const bool split = v_split<BF16>(p, z_kv, j);
       ok = wait_bar(br, p.status, br.s_full(t), s_phase, kRoleSoftmax);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
@@ -655,18 +581,6 @@ __device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t tmem,
         rescale = true;
       }
       const float neg_m = (m == -INFINITY) ? 0.f : -m;
-      // bf16 inputs: is V_j in fp16 now (converted) or still bf16?
-      bool split = false;
-      if constexpr (BF16) {
-        const uint32_t vi = v_base + static_cast<uint32_t>(j);
-        const uint32_t vs = vi % C::kVStages;
-        ok = wait_bar(br, p.status, br.v_conv(vs), (vi / C::kVStages) & 1u, kRoleSoftmax);
-        if (!__all_sync(0xffffffffu, ok)) {
-          ok = false;
-          break;
-        }
-        split = ptx::ld_shared_volatile(br.vflag(vs)) == 0u;
-      }
       const uint64_t sc2 = ptx::f2_pack(scale_log2, scale_log2);
       const uint64_t nm2 = ptx::f2_pack(neg_m, neg_m);
       uint64_t rsum2[4];  // independent partial row sums, two lanes each
@@ -783,7 +697,8 @@ template <int D, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
-                       const __grid_constant__ CUtensorMap tm_v, const KParams p) {
+                       const __grid_constant__ CUtensorMap tm_v,
+                       const __grid_constant__ CUtensorMap tm_v16, const KParams p) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t smem = (ptx::smem_u32(smem_raw) + 1023u) & ~1023u;
@@ -800,16 +715,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(br.p_full(t), BM);
       ptx::mbar_init(br.o_full(t), 1);
     }
+    // ring slots and the final drain: one release from each MMA issuer
     for (int s = 0; s < C::kKStages; ++s) {
       ptx::mbar_init(br.k_full(s), 1);
-      ptx::mbar_init(br.k_empty(s), 1);
+      ptx::mbar_init(br.k_empty(s), QT);
     }
     for (int s = 0; s < C::kVStages; ++s) {
       ptx::mbar_init(br.v_full(s), 1);
-      ptx::mbar_init(br.v_empty(s), 1);
-      ptx::mbar_init(br.v_conv(s), 64);  // every converter thread arrives
+      ptx::mbar_init(br.v_empty(s), QT);
     }
-    ptx::mbar_init(br.drain(), 1);
+    ptx::mbar_init(br.drain(), QT);
     ptx::st_shared_volatile(br.abort_word(), 0u);
     ptx::fence_barrier_init();
   }
@@ -817,8 +732,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::prefetch_tensormap(&tm_q);
     ptx::prefetch_tensormap(&tm_k);
     ptx::prefetch_tensormap(&tm_v);
+    if constexpr (BF16) ptx::prefetch_tensormap(&tm_v16);
   }
-  if (warp == kMmaWarp) {
+  if (warp == kMmaWarp0) {
     ptx::tmem_alloc(br.tmem_word(), C::kTmemCols);
     ptx::tmem_relinquish();
   }
@@ -830,12 +746,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp >= 8) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kControlRegs));
     if (warp == kProducerWarp) {
-      if (lane == 0) producer_role<D>(p, br, smem, &tm_q, &tm_k, &tm_v);
-    } else if (warp == kMmaWarp) {
-      mma_role<D, BF16>(p, br, smem, tmem);  // whole warp
-    } else if constexpr (BF16) {
-      convert_role<D>(p, br, smem);  // warps 10, 11
+      if (lane == 0) producer_role<D, BF16>(p, br, smem, &tm_q, &tm_k, &tm_v, &tm_v16);
+    } else if (warp < kMmaWarp0 + QT) {
+      mma_role<D, BF16>(p, br, smem, tmem, warp - kMmaWarp0);  // whole warp
     }
+    // warp 11 has no role
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
     softmax_role<D, BF16>(p, br, tmem, warp >> 2);
@@ -843,7 +758,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   ptx::tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == kMmaWarp0) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, C::kTmemCols);
   }
@@ -871,6 +786,8 @@ cudaError_t launch_instance(const Problem& pr, const CUtensorMap* maps, int num_
   kp.lse = pr.lse;
   kp.valid_len = pr.valid_len;
   kp.status = pr.status;
+  kp.vflags = pr.vflags;
+  kp.n_kt = (pr.L + BN - 1) / BN;
   kp.B = pr.B;
   kp.Hq = pr.Hq;
   kp.Hkv = pr.Hkv;
@@ -881,7 +798,7 @@ cudaError_t launch_instance(const Problem& pr, const CUtensorMap* maps, int num_
   kp.scale_log2 = pr.sm_scale * 1.4426950408889634f;
   kp.causal = pr.causal;
   const int grid = kp.n_units < num_sms ? kp.n_units : num_sms;
-  kern<<<grid, kThreads, C::kSmemBytes, pr.stream>>>(maps[0], maps[1], maps[2], kp);
+  kern<<<grid, kThreads, C::kSmemBytes, pr.stream>>>(maps[0], maps[1], maps[2], maps[3], kp);
   return cudaGetLastError();
 }
 

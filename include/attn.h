@@ -89,8 +89,17 @@ typedef enum {
  * queued and returned immediately (nothing is written).  The call never
  * synchronises; device-side conditions (ATTN_ERR_TIMEOUT, ATTN_ERR_VALID_LEN)
  * are recorded in a per-device status word and reported by attn_status.
- * The library allocates no per-call device memory: the only device memory it
- * owns is that status word (one int per device, allocated on first use).
+ *
+ * Device memory owned by the library: the status word (one int per device,
+ * cudaMalloc on first use) and, for ATTN_BF16, a per-call workspace of
+ * B*Hkv*L*D*2 bytes plus 4 bytes per (b, h_kv, 128-key tile).  The workspace
+ * holds an fp16 copy of V (exact where every value of a 128-key tile is
+ * finite with |v| < 65536; flagged tiles keep bf16) so that P.V runs with fp16
+ * probabilities.  It is taken with cudaMallocFromPoolAsync from a pool the
+ * library creates per device (release threshold: never) and returned with
+ * cudaFreeAsync on the same stream after the kernel, so calls on different
+ * streams never share it and repeated calls reuse the pool's memory.
+ * attn_shutdown destroys the pools.  ATTN_F16 calls take no workspace.
  */
 attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                        int B, int Hq, int Hkv, int L, int D, float sm_scale, int causal,
@@ -117,9 +126,13 @@ attn_status_t attn_fwd_simt(const void* q, const void* k, const void* v, void* o
  * allocations on the request path (cudaMalloc can synchronise the device and
  * stall every other stream); latency-bound loops that cannot afford an
  * allocation's unpredictable cost; runtimes whose memory accounting covers
- * only their own allocator -- use this entry point instead.  Same arguments, same layouts, same kernel and
- * the same results as attn_fwd; it calls no cudaMalloc, cudaFree or any other
- * allocating routine.
+ * only their own allocator -- use this entry point instead.  Same arguments,
+ * same layouts and the same kernel as attn_fwd; it calls no cudaMalloc,
+ * cudaFree or any other allocating routine.  Results: ATTN_F16 calls equal
+ * attn_fwd's.  ATTN_BF16 calls cannot take attn_fwd's workspace (the fp16 copy
+ * of V), so every key tile runs P.V with P split into two bf16 terms
+ * (P_hi + P_lo), the form attn_fwd uses only for tiles outside fp16's range:
+ * the same accuracy bound, about twice the P.V tensor-core work.
  *
  * Scratch: the kernel's status word lives in a fixed 256-byte array
  * (64 int32 words) of the library's static device memory, which every GPU
@@ -185,8 +198,10 @@ const char* attn_strerror(attn_status_t status);
  * returned on this thread, or 0. */
 int attn_last_cuda_error(void);
 
-/* Free the per-device status words.  Optional, at process exit; attn_fwd
- * may be called again afterwards (they are re-allocated). */
+/* Free the per-device status words and destroy the per-device workspace
+ * pools (their memory is released once every queued call that took a
+ * workspace has completed).  Optional, at process exit; attn_fwd may be called
+ * again afterwards (they are re-created). */
 void attn_shutdown(void);
 
 #ifdef __cplusplus
