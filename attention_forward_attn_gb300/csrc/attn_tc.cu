@@ -12,9 +12,10 @@
 //   * warp 8 (producer): TMA loads of the two Q tiles and of the K and V rings
 //     (2 + 3 stages at D=128, 4 + 4 at D=64), 128-byte swizzled;
 //   * warps 9 and 10 (MMA issuers, one per query tile t): S_t = Q_t K^T into
-//     TMEM (fp32), then O_t += P_t V with P_t read from TMEM.  Each warp
-//     issues PV_t(j) and then S_t(j+1); with two issuers the tensor core keeps
-//     working on one tile's MMAs while the other issuer waits on its barriers;
+//     TMEM (fp32), then O_t += P_t V with P_t read from TMEM.  For every key
+//     tile j the issuers take turns -- PV_0(j) S_0(j+1), then PV_1(j)
+//     S_1(j+1) -- so the tensor core runs one tile's group while that tile's
+//     issuer does its barrier work and the other tile's softmax runs;
 //   * warps 0-3 / 4-7 (softmax, one thread per query row = TMEM lane): load
 //     the S row, mask (only on boundary tiles), row max, ex2.approx, row sum,
 //     write P into TMEM over the S columns, rescale the O row in TMEM when the
@@ -83,9 +84,9 @@ struct Cfg {
   static constexpr int kOffV = kOffK + kKStages * kKVBytes;
   static constexpr int kOffBar = kOffV + kVStages * kKVBytes;
   // barrier block: q_full[QT] q_empty[QT] k_full[KS] k_empty[KS] v_full[VS]
-  // v_empty[VS] s_full[QT] p_full[QT] o_full[QT] drain, then 32-bit words:
-  // TMEM base, abort flag
-  static constexpr int kNumBars = 5 * QT + 2 * kKStages + 2 * kVStages + 1;
+  // v_empty[VS] s_full[QT] p_full[QT] o_full[QT] drain turn[QT], then 32-bit
+  // words: TMEM base, abort flag
+  static constexpr int kNumBars = 6 * QT + 2 * kKStages + 2 * kVStages + 1;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kMiscBytes = 8;
   static constexpr int kSmemBytes = kOffMisc + kMiscBytes + 1024;  // + slack to align the base
@@ -128,8 +129,12 @@ struct Bars {
     return base + 8u * (4 * QT + 2 * KS + 2 * VS + t);
   }
   __device__ __forceinline__ uint32_t drain() const { return base + 8u * (5 * QT + 2 * KS + 2 * VS); }
+  // issuer t may issue its MMA group of the current key tile
+  __device__ __forceinline__ uint32_t turn(int t) const {
+    return base + 8u * (5 * QT + 2 * KS + 2 * VS + 1 + t);
+  }
   __device__ __forceinline__ uint32_t tmem_word() const {
-    return base + 8u * (5 * QT + 2 * KS + 2 * VS + 1);
+    return base + 8u * (6 * QT + 2 * KS + 2 * VS + 1);
   }
   __device__ __forceinline__ uint32_t abort_word() const { return tmem_word() + 4u; }
 };
@@ -403,42 +408,22 @@ __device__ __forceinline__ void release_slot(uint32_t bar, bool used) {
   }
 }
 
-// Next K tile of the ring for the issuer of query tile t: wait for it, issue
-// S_t = Q_t K^T when it is key tile jn of this query tile (nt key tiles),
-// release the slot.  False: the wait gave up.
-template <int D, bool BF16>
-__device__ __forceinline__ bool mma_next_k(const KParams& p, const Bars<D>& br, int t, uint32_t& kit,
-                                           int jn, int nt, uint32_t t_s, uint64_t q_desc,
-                                           uint64_t k_desc0) {
-  using C = Cfg<D>;
-  const uint32_t sk = kit % C::kKStages;
-  if (!__all_sync(0xffffffffu, wait_bar(br, p.status, br.k_full(sk),
-                                        (kit / C::kKStages) & 1u, kRoleMma)))
-    return false;
-  ++kit;
-  const bool use = jn < nt;
-  if (use) {
-    ptx::tc_fence_after();
-    if (elect_one()) issue_qk<D, BF16>(t_s, q_desc, desc_add(k_desc0, sk * C::kKVBytes));
-    __syncwarp();
-    commit_one(br.s_full(t));
-    // Q_t is free once the unit's last S_t MMA completes: the producer can
-    // load the next unit's Q_t while this unit finishes
-    if (jn == nt - 1) commit_one(br.q_empty(t));
-  }
-  release_slot(br.k_empty(sk), use);
-  return true;
-}
-
 // Issuer of query tile t (whole warp; one elected lane issues).  It walks
 // every K and V ring item of every unit in the producer's order, so both
 // issuers stay in phase with the rings even when one tile has fewer key tiles
 // (causal diagonal) or none.
+//
+// Turns: for every key tile (counted over all units) issuer 0 issues its
+// group (PV_0(j), S_0(j+1)) and hands the turn to issuer 1, which issues its
+// group and hands it back.  The tensor core then works through whole groups
+// in that order, so the two tiles' scores complete half a step apart and the
+// two softmax warpgroups alternate instead of running at the same time.
 template <int D, bool BF16>
 __device__ void mma_role(const KParams& p, const Bars<D>& br, uint32_t smem, uint32_t tmem, int t) {
   using C = Cfg<D>;
   uint32_t q_phase = 0, p_phase = 0;
   uint32_t kit = 0, vit = 0;
+  uint32_t step = 0;  // key tiles of all units so far (turn phase)
   // K-major operands (Q, K): leading byte offset unused with 128-byte swizzle,
   // 1024 bytes between 8-row groups.  MN-major V: 64-column slabs kSlabKV
   // apart (leading), 1024 bytes between 8-key groups (stride).
@@ -462,8 +447,23 @@ __device__ void mma_role(const KParams& p, const Bars<D>& br, uint32_t smem, uin
       if (!__all_sync(0xffffffffu, wait_bar(br, p.status, br.q_full(t), q_phase, kRoleMma))) break;
       q_phase ^= 1u;
     }
-    if (!mma_next_k<D, BF16>(p, br, t, kit, 0, nt, t_s, q_desc, k_desc0)) break;
-    for (int j = 0; j < n; ++j) {
+    // S_t(0)
+    {
+      const uint32_t sk = kit % C::kKStages;
+      if (!__all_sync(0xffffffffu, wait_bar(br, p.status, br.k_full(sk),
+                                            (kit / C::kKStages) & 1u, kRoleMma)))
+        break;
+      ++kit;
+      if (nt > 0) {
+        ptx::tc_fence_after();
+        if (elect_one()) issue_qk<D, BF16>(t_s, q_desc, desc_add(k_desc0, sk * C::kKVBytes));
+        __syncwarp();
+        commit_one(br.s_full(t));
+        if (nt == 1) commit_one(br.q_empty(t));
+      }
+      release_slot(br.k_empty(sk), nt > 0);
+    }
+    for (int j = 0; j < n; ++j, ++step) {
       const uint32_t sv = vit % C::kVStages;
       if (!__all_sync(0xffffffffu,
                       wait_bar(br, p.status, br.v_full(sv), (vit / C::kVStages) & 1u, kRoleMma))) {
@@ -471,24 +471,52 @@ __device__ void mma_role(const KParams& p, const Bars<D>& br, uint32_t smem, uin
         break;
       }
       ++vit;
-      const bool use = j < nt;
-      if (use) {
-        const bool split = v_split<BF16>(p, z_kv, j);
+      const bool use_v = j < nt;
+      bool split = false;
+      if (use_v) {
+        split = v_split<BF16>(p, z_kv, j);
         if (!__all_sync(0xffffffffu, wait_bar(br, p.status, br.p_full(t), p_phase, kRoleMma))) {
           ok = false;
           break;
         }
         p_phase ^= 1u;
-        ptx::tc_fence_after();
-        if (elect_one()) issue_pv<D>(t_o, t_s, desc_add(v_desc0, sv * C::kKVBytes), j > 0, split);
-        __syncwarp();
-        if (j == nt - 1) commit_one(br.o_full(t));
       }
-      release_slot(br.v_empty(sv), use);
-      if (j + 1 < n && !mma_next_k<D, BF16>(p, br, t, kit, j + 1, nt, t_s, q_desc, k_desc0)) {
+      const bool has_next = j + 1 < n;
+      uint32_t sk = 0;
+      if (has_next) {
+        sk = kit % C::kKStages;
+        if (!__all_sync(0xffffffffu, wait_bar(br, p.status, br.k_full(sk),
+                                              (kit / C::kKStages) & 1u, kRoleMma))) {
+          ok = false;
+          break;
+        }
+        ++kit;
+      }
+      const bool use_k = j + 1 < nt;
+      // my turn: issuer 0 waits for issuer 1's previous group (none at the
+      // first key tile: the fresh barrier's preceding phase counts as done),
+      // issuer 1 for issuer 0's group of this key tile
+      const uint32_t turn_par = (t == 0) ? ((step & 1u) ^ 1u) : (step & 1u);
+      if (!__all_sync(0xffffffffu, wait_bar(br, p.status, br.turn(t), turn_par, kRoleMma))) {
         ok = false;
         break;
       }
+      ptx::tc_fence_after();
+      if (elect_one()) {
+        if (use_v) issue_pv<D>(t_o, t_s, desc_add(v_desc0, sv * C::kKVBytes), j > 0, split);
+        if (use_k) issue_qk<D, BF16>(t_s, q_desc, desc_add(k_desc0, sk * C::kKVBytes));
+        ptx::mbar_arrive(br.turn(t ^ 1));  // the other issuer's group may follow
+      }
+      __syncwarp();
+      if (use_v && j == nt - 1) commit_one(br.o_full(t));
+      release_slot(br.v_empty(sv), use_v);
+      if (use_k) {
+        commit_one(br.s_full(t));
+        // Q_t is free once the unit's last S_t MMA completes: the producer
+        // can load the next unit's Q_t while this unit finishes
+        if (j + 2 == nt) commit_one(br.q_empty(t));
+      }
+      if (has_next) release_slot(br.k_empty(sk), use_k);
     }
   }
   // Every MMA issued by this warp completes before TMEM is released.
@@ -725,6 +753,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(br.v_empty(s), QT);
     }
     ptx::mbar_init(br.drain(), QT);
+    ptx::mbar_init(br.turn(0), 1);
+    ptx::mbar_init(br.turn(1), 1);
     ptx::st_shared_volatile(br.abort_word(), 0u);
     ptx::fence_barrier_init();
   }
