@@ -472,15 +472,7 @@ __device__ void mma_role(const KParams& p, const Bars<D>& br, uint32_t smem, uin
       }
       ++vit;
       const bool use_v = j < nt;
-      bool split = false;
-      if (use_v) {
-        split = v_split<BF16>(p, z_kv, j);
-        if (!__all_sync(0xffffffffu, wait_bar(br, p.status, br.p_full(t), p_phase, kRoleMma))) {
-          ok = false;
-          break;
-        }
-        p_phase ^= 1u;
-      }
+      const bool split = use_v && v_split<BF16>(p, z_kv, j);
       const bool has_next = j + 1 < n;
       uint32_t sk = 0;
       if (has_next) {
@@ -500,6 +492,15 @@ __device__ void mma_role(const KParams& p, const Bars<D>& br, uint32_t smem, uin
       if (!__all_sync(0xffffffffu, wait_bar(br, p.status, br.turn(t), turn_par, kRoleMma))) {
         ok = false;
         break;
+      }
+      // P last: V, K and the turn are normally ready long before the softmax
+      // finishes, so only this wait stands between P_t(j) and its MMAs
+      if (use_v) {
+        if (!__all_sync(0xffffffffu, wait_bar(br, p.status, br.p_full(t), p_phase, kRoleMma))) {
+          ok = false;
+          break;
+        }
+        p_phase ^= 1u;
       }
       ptx::tc_fence_after();
       if (elect_one()) {
