@@ -58,13 +58,18 @@ constexpr int kMmaWarp0 = 9;   // MMA issuer of query tile 0; tile 1 has warp 10
 constexpr int kThreads = 384;  // warpgroups: softmax tile 0, softmax tile 1, producer/MMA
 // Register split between warpgroups (setmaxnreg).  The CTA is launched with
 // kLaunchRegs per thread (the __launch_bounds__(384, 1) ceiling: 3 warps per
-// SM sub-partition); the split must add up to exactly that pool:
-// 2 * 128 * 224 + 128 * 56 = 384 * 168.
+// SM sub-partition); the split must add up to exactly that pool.  D = 128
+// issues its MMAs from fully unrolled loops (fewer instructions between MMAs
+// on the issuer warps), which needs more control registers; D = 64 keeps
+// every register it can for the softmax.
 constexpr int kLaunchRegs = 168;
-constexpr int kSoftmaxRegs = 224;
-constexpr int kControlRegs = 56;
-static_assert(2 * 128 * kSoftmaxRegs + 128 * kControlRegs == kThreads * kLaunchRegs,
-              "register split must equal the launch pool");
+template <int D>
+struct RegSplit {
+  static constexpr int kSoftmax = (D == 128) ? 208 : 224;
+  static constexpr int kControl = (D == 128) ? 88 : 56;
+  static_assert(2 * 128 * kSoftmax + 128 * kControl == kThreads * kLaunchRegs,
+                "register split must equal the launch pool");
+};
 constexpr float kRescaleLog2 = 8.0f;  // rescale O only when the max grows by > 2^8
 constexpr float kLn2 = 0.69314718055994531f;
 
@@ -368,7 +373,7 @@ template <int D, bool BF16>
 __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t q_desc, uint64_t k_desc) {
   using C = Cfg<D>;
   constexpr uint32_t idesc = ptx::idesc_f16(BM, BN, BF16, false);
-#pragma unroll 1
+#pragma unroll (D == 128 ? D / 16 : 1)
   for (int kk = 0; kk < D / 16; ++kk) {
     const uint32_t off = (kk & 3) * 32u;
     ptx::mma_ss(d_tmem, desc_add(q_desc, (kk / 4) * C::kSlabQ + off),
@@ -385,7 +390,7 @@ template <int D>
 __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint64_t v_desc,
                                          bool accumulate, bool split) {
   const uint32_t idesc = split ? ptx::idesc_f16(BM, D, true, true) : ptx::idesc_f16(BM, D, false, true);
-#pragma unroll 1
+#pragma unroll (D == 128 ? BN / 16 : 1)
   for (int kk = 0; kk < BN / 16; ++kk)
     ptx::mma_ts(d_tmem, p_tmem + kk * 8u, desc_add(v_desc, kk * 2048u), idesc,
                 (accumulate || kk > 0) ? 1u : 0u);
@@ -775,7 +780,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = ptx::ld_shared_volatile(br.tmem_word());
 
   if (warp >= 8) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kControlRegs));
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(RegSplit<D>::kControl));
     if (warp == kProducerWarp) {
       if (lane == 0) producer_role<D, BF16>(p, br, smem, &tm_q, &tm_k, &tm_v, &tm_v16);
     } else if (warp < kMmaWarp0 + QT) {
@@ -783,7 +788,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // warp 11 has no role
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(RegSplit<D>::kSoftmax));
     softmax_role<D, BF16>(p, br, tmem, warp >> 2);
   }
 
