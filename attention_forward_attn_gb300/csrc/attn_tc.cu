@@ -65,8 +65,8 @@ constexpr int kThreads = 384;  // warpgroups: softmax tile 0, softmax tile 1, pr
 constexpr int kLaunchRegs = 168;
 template <int D>
 struct RegSplit {
-  static constexpr int kSoftmax = (D == 128) ? 208 : 224;
-  static constexpr int kControl = (D == 128) ? 88 : 56;
+  static constexpr int kSoftmax = (D == 128) ? 216 : 224;
+  static constexpr int kControl = (D == 128) ? 72 : 56;
   static_assert(2 * 128 * kSoftmax + 128 * kControl == kThreads * kLaunchRegs,
                 "register split must equal the launch pool");
 };
@@ -532,6 +532,59 @@ __device__ void mma_role(const KParams& p, const Bars<D>& br, uint32_t smem, uin
 
 // ------------------------------------------------------------------ softmax + epilogue
 
+// P for one score row (128 keys in registers), 32 keys at a time, written
+// over the row's S columns in TMEM; returns the row sum of P.  fp16 V tile:
+// P rounded to fp16 in columns [0, 64).  bf16 V tile (SPLIT): P = P_hi + P_lo
+// with P_hi = p truncated to bf16 (columns [0, 64)) and P_lo = bf16(p - P_hi)
+// (columns [64, 128)); a single bf16 P (unit roundoff 2^-8) is too coarse for
+// rows dominated by a few keys, the pair leaves a relative error below 2^-15.
+// MASKED: columns c >= c_lim get P = 0.
+template <bool MASKED, bool SPLIT>
+__device__ __forceinline__ float exp_row(const uint32_t (&s)[BN], uint64_t sc2, uint64_t nm2, int c_lim,
+                                         uint32_t t_s) {
+  uint64_t rsum2[4];  // independent partial row sums, two lanes each
+#pragma unroll
+  for (int k = 0; k < 4; ++k) rsum2[k] = 0ull;
+#pragma unroll
+  for (int qtr = 0; qtr < 4; ++qtr) {
+    uint32_t hi[16];
+    uint32_t lo[SPLIT ? 16 : 1];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int c = qtr * 32 + 2 * i;
+      // exponent argument s*scale - m for two keys in one instruction
+      const uint64_t x2 =
+          ptx::f2_fma(ptx::f2_pack(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), sc2, nm2);
+      float x0, x1;
+      ptx::f2_unpack(x2, x0, x1);
+      float p0 = ptx::ex2_approx(x0);
+      float p1 = ptx::ex2_approx(x1);
+      if constexpr (MASKED) {
+        p0 = (c < c_lim) ? p0 : 0.f;
+        p1 = (c + 1 < c_lim) ? p1 : 0.f;
+      }
+      const uint64_t p2 = ptx::f2_pack(p0, p1);
+      rsum2[i & 3] = ptx::f2_add(rsum2[i & 3], p2);
+      if constexpr (SPLIT) {
+        const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
+        hi[i] = __byte_perm(b0, b1, 0x7632);  // upper halves: truncated bf16 pair
+        const uint64_t r2 = ptx::f2_sub(
+            p2, ptx::f2_pack(__uint_as_float(b0 & 0xFFFF0000u), __uint_as_float(b1 & 0xFFFF0000u)));
+        float r0, r1;
+        ptx::f2_unpack(r2, r0, r1);
+        lo[i] = pack2<true>(r0, r1);
+      } else {
+        hi[i] = pack2<false>(p0, p1);
+      }
+    }
+    ptx::tmem_st16(t_s + qtr * 16, hi);
+    if constexpr (SPLIT) ptx::tmem_st16(t_s + BN / 2 + qtr * 16, lo);
+  }
+  float ra, rb;
+  ptx::f2_unpack(ptx::f2_add(ptx::f2_add(rsum2[0], rsum2[1]), ptx::f2_add(rsum2[2], rsum2[3])), ra, rb);
+  return ra + rb;
+}
+
 template <int D, bool BF16>
 __device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t tmem, int t) {
   using C = Cfg<D>;
@@ -617,73 +670,20 @@ __device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t tmem,
       const float neg_m = (m == -INFINITY) ? 0.f : -m;
       const uint64_t sc2 = ptx::f2_pack(scale_log2, scale_log2);
       const uint64_t nm2 = ptx::f2_pack(neg_m, neg_m);
-      uint64_t rsum2[4];  // independent partial row sums, two lanes each
-#pragma unroll
-      for (int k = 0; k < 4; ++k) rsum2[k] = 0ull;
-      // P over the S columns, 32 keys at a time (every S value is already in
-      // registers).  fp16 V tile: P rounded to fp16 in columns [0, 64).
-      // bf16 V tile: P = P_hi + P_lo with P_hi = p truncated to bf16 (columns
-      // [0, 64)) and P_lo = bf16(p - P_hi) (columns [64, 128)); a single bf16
-      // P (unit roundoff 2^-8) is too coarse for rows dominated by a few keys,
-      // the pair leaves a relative error below 2^-15.
+      // P over the S columns (every S value is already in registers); the
+      // masked form only on key tiles that need it, so full tiles carry no
+      // per-key selects
+      float rowsum;
       if (!split) {
-#pragma unroll
-        for (int qtr = 0; qtr < 4; ++qtr) {
-          uint32_t hi[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int c = qtr * 32 + 2 * i;
-            // exponent argument s*scale - m for two keys in one instruction
-            const uint64_t x2 = ptx::f2_fma(
-                ptx::f2_pack(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), sc2, nm2);
-            float x0, x1;
-            ptx::f2_unpack(x2, x0, x1);
-            float p0 = ptx::ex2_approx(x0);
-            float p1 = ptx::ex2_approx(x1);
-            if (masked) {
-              p0 = (c < c_lim) ? p0 : 0.f;
-              p1 = (c + 1 < c_lim) ? p1 : 0.f;
-            }
-            rsum2[i & 3] = ptx::f2_add(rsum2[i & 3], ptx::f2_pack(p0, p1));
-            hi[i] = pack2<false>(p0, p1);
-          }
-          ptx::tmem_st16(t_s + qtr * 16, hi);
-        }
+        rowsum = masked ? exp_row<true, false>(s, sc2, nm2, c_lim, t_s)
+                        : exp_row<false, false>(s, sc2, nm2, c_lim, t_s);
       } else if constexpr (BF16) {
-#pragma unroll
-        for (int qtr = 0; qtr < 4; ++qtr) {
-          uint32_t hi[16];
-          uint32_t lo[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int c = qtr * 32 + 2 * i;
-            const uint64_t x2 = ptx::f2_fma(
-                ptx::f2_pack(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), sc2, nm2);
-            float x0, x1;
-            ptx::f2_unpack(x2, x0, x1);
-            float p0 = ptx::ex2_approx(x0);
-            float p1 = ptx::ex2_approx(x1);
-            if (masked) {
-              p0 = (c < c_lim) ? p0 : 0.f;
-              p1 = (c + 1 < c_lim) ? p1 : 0.f;
-            }
-            const uint64_t p2 = ptx::f2_pack(p0, p1);
-            rsum2[i & 3] = ptx::f2_add(rsum2[i & 3], p2);
-            const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
-            hi[i] = __byte_perm(b0, b1, 0x7632);  // upper halves: truncated bf16 pair
-            const uint64_t r2 = ptx::f2_sub(
-                p2, ptx::f2_pack(__uint_as_float(b0 & 0xFFFF0000u), __uint_as_float(b1 & 0xFFFF0000u)));
-            float r0, r1;
-            ptx::f2_unpack(r2, r0, r1);
-            lo[i] = pack2<true>(r0, r1);
-          }
-          ptx::tmem_st16(t_s + qtr * 16, hi);
-          ptx::tmem_st16(t_s + BN / 2 + qtr * 16, lo);
-        }
+        rowsum = masked ? exp_row<true, true>(s, sc2, nm2, c_lim, t_s)
+                        : exp_row<false, true>(s, sc2, nm2, c_lim, t_s);
+      } else {
+        rowsum = 0.f;
       }
-      float ra, rb;
-      ptx::f2_unpack(ptx::f2_add(ptx::f2_add(rsum2[0], rsum2[1]), ptx::f2_add(rsum2[2], rsum2[3])), ra, rb);
-      l = l * alpha + (ra + rb);
+      l = l * alpha + rowsum;
       // O was accumulated against the old max: rescale it before PV_j runs.
       // PV_{j-1} is complete: the commit that signalled S_j came after it.
       if (j > 0 && __any_sync(0xffffffffu, rescale)) {
