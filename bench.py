@@ -38,7 +38,7 @@ L2_FLUSH_BYTES = 256 << 20          # > 129 MB L2
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "attn_fwd_tc_dram_traffic.txt")
 KERNEL_SOURCES = [os.path.join(ROOT, "attention_forward_attn_gb300", "csrc", f)
-                  for f in ("attn_tc.cu", "ptx.cuh")]
+                  for f in ("attn_tc.cu", "attn_vconv.cu", "ptx.cuh")]
 
 
 # ------------------------------------------------------------------ work accounting
@@ -345,7 +345,8 @@ def run_gpu(args, w, world, rank, local):
             "valid_len": None if vl is None else vl.tolist(), "sm_scale": w.sm_scale,
             "parallelism": "replicas x%d (no exchange step)" % world,
             "l2": "flushed between timed steps (256 MB write, outside the events)",
-            "timing": "CUDA events around each attn_fwd call on its stream",
+            "timing": "CUDA events around each attn_fwd call on its stream (%s)" % (
+                "bf16: V pre-pass + attention kernel" if w.dtype == "bf16" else "attention kernel"),
             "ms_median": round(ms_med, 5),
             "ms_p10": round(float(np.percentile(ms, 10)), 5),
             "ms_p90": round(float(np.percentile(ms, 90)), 5),
@@ -375,7 +376,9 @@ def run_gpu(args, w, world, rank, local):
             "steps": e2e_steps,
             "path": "pinned host Q/K/V -> device, attn_fwd (C ABI via the binding), O/LSE -> host",
         },
-        "gpu_launches": args.steps,
+        # attn_fwd launches the attention kernel, preceded for bf16 by the
+        # kernel that makes the fp16 copy of V
+        "gpu_launches": args.steps * (2 if w.dtype == "bf16" else 1),
         "clocks": clocks,
     }
     if rank == 0 and not args.no_cpu_baseline:
