@@ -225,11 +225,12 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
   attn::TcConfig cfg;
   if (!attn::tc_config(D, &cfg)) return ATTN_ERR_HEADDIM;
   const bool bf16 = dtype == ATTN_BF16;
-  CUtensorMap maps[4];
+  CUtensorMap maps[5];
   if ((s = encode_map(&maps[0], q, B * Hq, L, D, cfg.block_m, bf16)) != ATTN_OK) return s;
   if ((s = encode_map(&maps[1], k, B * Hkv, L, D, cfg.block_n, bf16)) != ATTN_OK) return s;
   if ((s = encode_map(&maps[2], v, B * Hkv, L, D, cfg.block_n, bf16)) != ATTN_OK) return s;
   maps[3] = maps[2];
+  if ((s = encode_map(&maps[4], o, B * Hq, L, D, cfg.block_m, bf16)) != ATTN_OK) return s;
   Problem p = make_problem(q, k, v, o, lse, B, Hq, Hkv, L, D, sm_scale, causal, valid_len, dtype,
                            stream, st->status);
   void* ws = nullptr;

@@ -51,8 +51,9 @@ struct TcConfig {
 
 bool tc_config(int D, TcConfig* out);
 
-// Tensor-core (tcgen05/TMA) forward.  maps: Q, K, V and the fp16 copy of V
-// (bf16 inputs with p.vflags set; any valid map otherwise, it is not read).
+// Tensor-core (tcgen05/TMA) forward.  maps: Q, K, V, the fp16 copy of V
+// (bf16 inputs with p.vflags set; any valid map otherwise, it is not read)
+// and O (boxes of 128 rows, the kernel's store map).
 cudaError_t launch_tc(const Problem& p, const CUtensorMap* maps, int num_sms);
 
 // bf16 V pre-pass (attn_vconv.cu): bytes of its workspace (the fp16 copy of

@@ -115,11 +115,12 @@ extern "C" attn_status_t attn_fwd_noalloc(const void* q, const void* k, const vo
   const bool bf16 = dtype == ATTN_BF16;
   // no fp16 copy of V without a workspace: bf16 tiles all take the split
   // P.V (Problem::vflags stays null); the fourth map is never read
-  CUtensorMap maps[4];
+  CUtensorMap maps[5];
   if ((s = attn::encode_map(&maps[0], q, B * Hq, L, D, cfg.block_m, bf16)) != ATTN_OK) return s;
   if ((s = attn::encode_map(&maps[1], k, B * Hkv, L, D, cfg.block_n, bf16)) != ATTN_OK) return s;
   if ((s = attn::encode_map(&maps[2], v, B * Hkv, L, D, cfg.block_n, bf16)) != ATTN_OK) return s;
   maps[3] = maps[2];
+  if ((s = attn::encode_map(&maps[4], o, B * Hq, L, D, cfg.block_m, bf16)) != ATTN_OK) return s;
   // The status word must start at zero for this call: the array keeps
   // whatever the previous call (on any stream) left in it.
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

@@ -7,20 +7,27 @@
 // pre-multiplied by sm_scale*log2(e)); masks and head map as in include/attn.h.
 //
 // How (one CTA per SM, persistent over work units):
-//   * work unit = (b, h_q, 256 query rows) = two 128-row query tiles that share
-//     one stream of K/V tiles (128 keys each);
-//   * warp 8 (producer): TMA loads of the two Q tiles and of the K and V rings
-//     (2 + 3 stages at D=128, 4 + 4 at D=64), 128-byte swizzled;
-//   * warps 9 and 10 (MMA issuers, one per query tile t): S_t = Q_t K^T into
-//     TMEM (fp32), then O_t += P_t V with P_t read from TMEM.  For every key
-//     tile j the issuers take turns -- PV_0(j) S_0(j+1), then PV_1(j)
-//     S_1(j+1) -- so the tensor core runs one tile's group while that tile's
-//     issuer does its barrier work and the other tile's softmax runs;
-//   * warps 0-3 / 4-7 (softmax, one thread per query row = TMEM lane): load
-//     the S row, mask (only on boundary tiles), row max, ex2.approx, row sum,
-//     write P into TMEM over the S columns, rescale the O row in TMEM when the
-//     max grew by more than 2^8 (exact after the final division), and finally
-//     O / l -> global memory and the LSE.
+//   * work unit = (b, h_q, 128 query rows), one query tile; K/V streamed in
+//     tiles of 128 keys;
+//   * warp 4 (producer): TMA loads of the Q tile and of the K and V rings
+//     (3 + 3 stages at D=128, 6 + 6 at D=64), 128-byte swizzled;
+//   * warps 5 and 6 (MMA issuers; one elected lane each issues): warp 6
+//     issues S(j) = Q K_j^T into one of three TMEM score buffers, warp 5
+//     issues O += P(j) V_j with P read from TMEM.  The scores run up to three
+//     key tiles ahead of the softmax (S(j+3) goes into the buffer P(j) came
+//     from, once PV(j) has completed), so the softmax never waits for scores
+//     and the tensor core has work queued while P(j) is being computed;
+//   * warps 0-3 (softmax, one thread per query row = TMEM lane): load the S
+//     row, mask (only on boundary tiles), row max, ex2.approx, row sum, write
+//     P into TMEM over the S columns, rescale the O row in TMEM when the max
+//     grew by more than 2^8 (exact after the final division), and finally
+//     O / l, staged in shared memory in the TMA layout and written by one
+//     TMA store per 64-column slab (a thread's own row would be 16 strided
+//     16-byte stores, one cache line each), and the LSE.  The staging tile is
+//     the V ring stage of the unit's last key tile: idle from its PV's
+//     completion until the producer refills it three V loads later, so the
+//     epilogue, not the PV issuer, releases that stage once the store has
+//     read it.
 // Causal units skip every key tile above the diagonal; padded units skip every
 // key tile at or beyond valid_len[b]; a unit with no visible key writes O = 0
 // and LSE = -inf without touching the tensor core.
@@ -50,59 +57,43 @@ namespace attn {
 namespace {
 
 constexpr int BM = 128;       // query rows per tile (TMEM lanes)
-constexpr int QT = 2;         // query tiles per work unit
 constexpr int BN = 128;       // keys per K/V tile
-constexpr int kUnitRows = QT * BM;
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp0 = 9;   // MMA issuer of query tile 0; tile 1 has warp 10
-constexpr int kThreads = 384;  // warpgroups: softmax tile 0, softmax tile 1, producer/MMA
-// Register split between warpgroups (setmaxnreg).  The CTA is launched with
-// kLaunchRegs per thread (the __launch_bounds__(384, 1) ceiling: 3 warps per
-// SM sub-partition); the split must add up to exactly that pool.  D = 128
-// issues its MMAs from fully unrolled loops (fewer instructions between MMAs
-// on the issuer warps), which needs more control registers; D = 64 keeps
-// every register it can for the softmax.
-constexpr int kLaunchRegs = 168;
-template <int D>
-struct RegSplit {
-  static constexpr int kSoftmax = (D == 128) ? 216 : 224;
-  static constexpr int kControl = (D == 128) ? 72 : 56;
-  static_assert(2 * 128 * kSoftmax + 128 * kControl == kThreads * kLaunchRegs,
-                "register split must equal the launch pool");
-};
+constexpr int kProducerWarp = 4;
+constexpr int kPvWarp = 5;     // P.V issuer; also allocates TMEM
+constexpr int kSWarp = 6;      // score issuer
+constexpr int kThreads = 224;  // softmax warpgroup, producer, two MMA issuers
+constexpr int kSoftmaxThreads = 128;
 constexpr float kRescaleLog2 = 8.0f;  // rescale O only when the max grows by > 2^8
 constexpr float kLn2 = 0.69314718055994531f;
 
 template <int D>
 struct Cfg {
-  // separate rings for K and V tiles; V gets the extra stage (its tiles are
-  // consumed later in each step than the K tiles)
-  static constexpr int kKStages = (D == 128) ? 2 : 4;
-  static constexpr int kVStages = (D == 128) ? 3 : 4;
+  static constexpr int kKStages = (D == 128) ? 3 : 6;
+  static constexpr int kVStages = (D == 128) ? 3 : 6;
   static constexpr int kHalves = D / 64;           // 64-column (128-byte) slabs per row
   static constexpr int kQBytes = BM * D * 2;
   static constexpr int kKVBytes = BN * D * 2;
   static constexpr int kSlabQ = BM * 128;          // bytes of one 64-column slab of a Q tile
   static constexpr int kSlabKV = BN * 128;
   static constexpr int kOffQ = 0;
-  static constexpr int kOffK = QT * kQBytes;
+  static constexpr int kOffK = kQBytes;
   static constexpr int kOffV = kOffK + kKStages * kKVBytes;
   static constexpr int kOffBar = kOffV + kVStages * kKVBytes;
-  // barrier block: q_full[QT] q_empty[QT] k_full[KS] k_empty[KS] v_full[VS]
-  // v_empty[VS] s_full[QT] p_full[QT] o_full[QT] drain turn[QT], then 32-bit
-  // words: TMEM base, abort flag
-  static constexpr int kNumBars = 6 * QT + 2 * kKStages + 2 * kVStages + 1;
+  static_assert(kQBytes == kKVBytes, "an O tile is staged in a V stage");
+  // barrier block: q_full q_empty k_full[KS] k_empty[KS] v_full[VS] v_empty[VS]
+  // s_full[3] p_full[3] pv_done[3] o_full drain o_staged, then 32-bit words:
+  // TMEM base, abort flag
+  static constexpr int kScoreBufs = 3;
+  static constexpr int kNumBars = 2 + 2 * kKStages + 2 * kVStages + 3 * kScoreBufs + 3;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kMiscBytes = 8;
   static constexpr int kSmemBytes = kOffMisc + kMiscBytes + 1024;  // + slack to align the base
-  // TMEM columns: S_0, S_1 (fp32, BN each; P_t is written over S_t), then
-  // O_0, O_1 (fp32, D each).
-  static __device__ __forceinline__ uint32_t col_s(int t) { return static_cast<uint32_t>(t * BN); }
-  static __device__ __forceinline__ uint32_t col_o(int t) {
-    return static_cast<uint32_t>(2 * BN + t * D);
-  }
+  // TMEM columns: score buffers S_0, S_1, S_2 (fp32, BN each; P is written
+  // over the first columns of its score buffer), then O (fp32, D).
+  static __device__ __forceinline__ uint32_t col_s(uint32_t b) { return b * BN; }
+  static constexpr uint32_t kColO = kScoreBufs * BN;
   static constexpr uint32_t kTmemCols = 512;
-  static_assert(2 * BN + 2 * D <= 512, "TMEM budget");
+  static_assert(kScoreBufs * BN + D <= 512, "TMEM budget");
   static_assert(kSmemBytes <= 232448, "shared-memory budget");
 };
 
@@ -111,35 +102,32 @@ template <int D>
 struct Bars {
   static constexpr uint32_t KS = Cfg<D>::kKStages;
   static constexpr uint32_t VS = Cfg<D>::kVStages;
+  static constexpr uint32_t SB = Cfg<D>::kScoreBufs;
   uint32_t base;
-  __device__ __forceinline__ uint32_t q_full(int t) const { return base + 8u * t; }
-  __device__ __forceinline__ uint32_t q_empty(int t) const { return base + 8u * (QT + t); }
-  __device__ __forceinline__ uint32_t k_full(uint32_t s) const { return base + 8u * (2 * QT + s); }
-  __device__ __forceinline__ uint32_t k_empty(uint32_t s) const {
-    return base + 8u * (2 * QT + KS + s);
-  }
-  __device__ __forceinline__ uint32_t v_full(uint32_t s) const {
-    return base + 8u * (2 * QT + 2 * KS + s);
-  }
+  __device__ __forceinline__ uint32_t q_full() const { return base; }
+  __device__ __forceinline__ uint32_t q_empty() const { return base + 8u; }
+  __device__ __forceinline__ uint32_t k_full(uint32_t s) const { return base + 8u * (2 + s); }
+  __device__ __forceinline__ uint32_t k_empty(uint32_t s) const { return base + 8u * (2 + KS + s); }
+  __device__ __forceinline__ uint32_t v_full(uint32_t s) const { return base + 8u * (2 + 2 * KS + s); }
   __device__ __forceinline__ uint32_t v_empty(uint32_t s) const {
-    return base + 8u * (2 * QT + 2 * KS + VS + s);
+    return base + 8u * (2 + 2 * KS + VS + s);
   }
-  __device__ __forceinline__ uint32_t s_full(int t) const {
-    return base + 8u * (2 * QT + 2 * KS + 2 * VS + t);
+  __device__ __forceinline__ uint32_t s_full(uint32_t b) const {
+    return base + 8u * (2 + 2 * KS + 2 * VS + b);
   }
-  __device__ __forceinline__ uint32_t p_full(int t) const {
-    return base + 8u * (3 * QT + 2 * KS + 2 * VS + t);
+  __device__ __forceinline__ uint32_t p_full(uint32_t b) const {
+    return base + 8u * (2 + 2 * KS + 2 * VS + SB + b);
   }
-  __device__ __forceinline__ uint32_t o_full(int t) const {
-    return base + 8u * (4 * QT + 2 * KS + 2 * VS + t);
+  // PV of the key tile whose P was in buffer b has completed
+  __device__ __forceinline__ uint32_t pv_done(uint32_t b) const {
+    return base + 8u * (2 + 2 * KS + 2 * VS + 2 * SB + b);
   }
-  __device__ __forceinline__ uint32_t drain() const { return base + 8u * (5 * QT + 2 * KS + 2 * VS); }
-  // issuer t may issue its MMA group of the current key tile
-  __device__ __forceinline__ uint32_t turn(int t) const {
-    return base + 8u * (5 * QT + 2 * KS + 2 * VS + 1 + t);
-  }
+  __device__ __forceinline__ uint32_t o_full() const { return base + 8u * (2 + 2 * KS + 2 * VS + 3 * SB); }
+  __device__ __forceinline__ uint32_t drain() const { return base + 8u * (3 + 2 * KS + 2 * VS + 3 * SB); }
+  // every softmax thread has written its O row into the staging tile
+  __device__ __forceinline__ uint32_t o_staged() const { return base + 8u * (4 + 2 * KS + 2 * VS + 3 * SB); }
   __device__ __forceinline__ uint32_t tmem_word() const {
-    return base + 8u * (6 * QT + 2 * KS + 2 * VS + 1);
+    return base + 8u * (5 + 2 * KS + 2 * VS + 3 * SB);
   }
   __device__ __forceinline__ uint32_t abort_word() const { return tmem_word() + 4u; }
 };
@@ -154,7 +142,7 @@ struct KParams {
   const int* vflags;
   int n_kt;     // 128-key tiles per (b, h_kv)
   int B, Hq, Hkv, L, G;
-  int n_mb;     // 256-row blocks per (b, h_q)
+  int n_mb;     // 128-row query tiles per (b, h_q)
   int n_units;  // B * Hq * n_mb
   float scale_log2;
   int causal;
@@ -162,7 +150,7 @@ struct KParams {
 
 struct Unit {
   int bh, b, hkv, m0, kv_len;
-  int n[QT];  // key tiles each query tile visits (0: tile absent or no visible key)
+  int n;  // key tiles the query tile visits (0: no visible key)
 };
 
 // Units are ordered so that causal work runs heaviest-first (last row blocks
@@ -189,23 +177,15 @@ __device__ __forceinline__ Unit decode_unit(const KParams& p, int u) {
   }
   w.b = w.bh / p.Hq;
   w.hkv = (w.bh % p.Hq) / p.G;
-  w.m0 = mb * kUnitRows;
+  w.m0 = mb * BM;
   int kv = p.L;
   if (p.valid_len != nullptr) {
     kv = p.valid_len[w.b];
     kv = kv < 0 ? 0 : (kv > p.L ? p.L : kv);
   }
   w.kv_len = kv;
-#pragma unroll
-  for (int t = 0; t < QT; ++t) {
-    const int r0 = w.m0 + t * BM;
-    if (r0 >= p.L) {
-      w.n[t] = 0;
-    } else {
-      const int hi = p.causal ? min(kv, r0 + BM) : kv;
-      w.n[t] = (hi + BN - 1) / BN;
-    }
-  }
+  const int hi = p.causal ? min(kv, w.m0 + BM) : kv;
+  w.n = (hi + BN - 1) / BN;
   return w;
 }
 
@@ -247,6 +227,22 @@ __device__ __forceinline__ bool v_split(const KParams& p, int z_kv, int j) {
   }
 }
 
+// The same for key tiles [j0, j0 + 32) at once, as a bit mask (bit i: tile
+// j0 + i has an exact fp16 copy): lane i reads one flag, a ballot combines
+// them, so a warp touches global memory once per 32 key tiles.  Every lane
+// of the warp must take part.  fp16 inputs and bf16 without flags: 0.
+template <bool BF16>
+__device__ __forceinline__ uint32_t v_fp16_mask(const KParams& p, int z_kv, int j0, int n) {
+  if constexpr (!BF16) {
+    return 0u;
+  } else {
+    const int j = j0 + static_cast<int>(threadIdx.x & 31);
+    int f = 0;
+    if (p.vflags != nullptr && j < n) f = __ldg(p.vflags + static_cast<int64_t>(z_kv) * p.n_kt + j);
+    return __ballot_sync(0xffffffffu, f != 0);
+  }
+}
+
 template <bool BF16>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   if constexpr (BF16) {
@@ -265,8 +261,7 @@ __device__ void producer_role(const KParams& p, const Bars<D>& br, uint32_t smem
                               const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                               const CUtensorMap* tm_v, const CUtensorMap* tm_v16) {
   using C = Cfg<D>;
-  uint32_t q_phase = 0;   // bit t: parity of tile t's next q_empty wait ^ 1
-  uint32_t q_used = 0;    // bit t: a Q_t load was issued
+  uint32_t q_loads = 0;            // Q tiles loaded so far (one buffer)
   uint32_t k_used = 0, k_par = 0;  // per K stage: loaded at least once / parity of the last load
   uint32_t v_used = 0, v_par = 0;  // per V stage: the same
   uint32_t kit = 0, vit = 0;       // K and V ring items issued
@@ -306,29 +301,24 @@ __device__ void producer_role(const KParams& p, const Bars<D>& br, uint32_t smem
     const int u = unit_of(r);
     if (u >= p.n_units) continue;
     const Unit w = decode_unit(p, u);
-    const int n = max(w.n[0], w.n[1]);
+    const int n = w.n;
     if (n == 0) continue;
     const int z_kv = w.b * p.Hkv + w.hkv;
+    // Q: the buffer is free once the previous unit's last score MMA completed
+    if (!wait_bar(br, p.status, br.q_empty(), (q_loads & 1u) ^ 1u, kRoleProducer)) break;
+    ++q_loads;
+    ptx::mbar_arrive_expect_tx(br.q_full(), C::kQBytes);
 #pragma unroll
-    for (int t = 0; t < QT; ++t) {
-      if (w.n[t] == 0) continue;
-      if (!wait_bar(br, p.status, br.q_empty(t), ((q_phase >> t) & 1u) ^ 1u, kRoleProducer)) {
-        ok = false;
-        break;
-      }
-      q_phase ^= 1u << t;
-      q_used |= 1u << t;
-      const uint32_t dst = smem + C::kOffQ + t * C::kQBytes;
-      ptx::mbar_arrive_expect_tx(br.q_full(t), C::kQBytes);
-#pragma unroll
-      for (int h = 0; h < C::kHalves; ++h)
-        ptx::tma_load_3d_hint(dst + h * C::kSlabQ, tm_q, br.q_full(t), h * 64, w.m0 + t * BM,
-                              w.bh, pol_stream);
+    for (int h = 0; h < C::kHalves; ++h)
+      ptx::tma_load_3d_hint(smem + C::kOffQ + h * C::kSlabQ, tm_q, br.q_full(), h * 64, w.m0, w.bh,
+                            pol_stream);
+    // issue order = consumption order: K_0 K_1 K_2 | V_0 K_3 | V_1 K_4 | ...
+    const int lead = n < C::kScoreBufs ? n : C::kScoreBufs;
+    for (int i = 0; ok && i < lead; ++i) ok = load_kv(false, i, z_kv);
+    for (int j = 0; ok && j < n; ++j) {
+      ok = load_kv(true, j, z_kv);
+      if (ok && j + C::kScoreBufs < n) ok = load_kv(false, j + C::kScoreBufs, z_kv);
     }
-    // issue order K_0 V_0 | V_1 K_1 | V_2 K_2 ...: each V tile is requested as
-    // soon as its (deeper) ring has room
-    ok = ok && load_kv(false, 0, z_kv) && load_kv(true, 0, z_kv);
-    for (int j = 1; ok && j < n; ++j) ok = load_kv(true, j, z_kv) && load_kv(false, j, z_kv);
   }
   // Never leave with a copy in flight: wait (bounded) for the last load of
   // every buffer.  In a normal run these phases completed long ago.
@@ -336,8 +326,7 @@ __device__ void producer_role(const KParams& p, const Bars<D>& br, uint32_t smem
     if ((k_used >> s) & 1u) drain_wait(br.k_full(s), (k_par >> s) & 1u);
   for (uint32_t s = 0; s < C::kVStages; ++s)
     if ((v_used >> s) & 1u) drain_wait(br.v_full(s), (v_par >> s) & 1u);
-  for (int t = 0; t < QT; ++t)
-    if ((q_used >> t) & 1u) drain_wait(br.q_full(t), ((q_phase >> t) & 1u) ^ 1u);
+  if (q_loads > 0) drain_wait(br.q_full(), (q_loads - 1u) & 1u);
 }
 
 // ------------------------------------------------------------------ MMA issuer
@@ -401,42 +390,28 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint6
   }
 }
 
-// Release of a K or V ring slot by an issuer warp: after the warp's MMAs that
-// read it (commit), or at once when its tile does not use the slot.  Each
-// slot's empty barrier expects one release from each of the two issuers.
-__device__ __forceinline__ void release_slot(uint32_t bar, bool used) {
-  if (used) {
-    commit_one(bar);
-  } else {
-    if (elect_one()) ptx::mbar_arrive(bar);
-    __syncwarp();
-  }
-}
 
-// Issuer of query tile t (whole warp; one elected lane issues).  It walks
-// every K and V ring item of every unit in the producer's order, so both
-// issuers stay in phase with the rings even when one tile has fewer key tiles
-// (causal diagonal) or none.
-//
-// Turns: for every key tile (counted over all units) issuer 0 issues its
-// group (PV_0(j), S_0(j+1)) and hands the turn to issuer 1, which issues its
-// group and hands it back.  The tensor core then works through whole groups
-// in that order, so the two tiles' scores complete half a step apart and the
-// two softmax warpgroups alternate instead of running at the same time.
+// Two issuer warps (one elected lane each issues), so that one warp's
+// barrier waits and commits overlap the other's MMAs on the tensor core:
+//   * the S issuer (warp 6) issues every score tile in order, S(g) into
+//     buffer g % 3; before overwriting a buffer it waits until PV(g-3), which
+//     read P from it, has completed -- the scores run up to three key tiles
+//     ahead of the softmax;
+//   * the PV issuer (warp 5) issues PV(j) as soon as P(j) is in TMEM.
+// Per-buffer completion barriers (pv_done[b]) cannot run two phases ahead of
+// a waiter: PV(g+3) needs S(g+3), which the S issuer issues only after its
+// wait for PV(g).
 template <int D, bool BF16>
-__device__ void mma_role(const KParams& p, const Bars<D>& br, uint32_t smem, uint32_t tmem, int t) {
+__device__ void s_issuer_role(const KParams& p, const Bars<D>& br, uint32_t smem, uint32_t tmem) {
   using C = Cfg<D>;
-  uint32_t q_phase = 0, p_phase = 0;
-  uint32_t kit = 0, vit = 0;
-  uint32_t step = 0;  // key tiles of all units so far (turn phase)
+  constexpr uint32_t SB = C::kScoreBufs;
+  uint32_t q_phase = 0;
+  uint32_t kit = 0;
+  uint32_t g = 0;  // score tiles of all units so far: tile g uses buffer g % 3
   // K-major operands (Q, K): leading byte offset unused with 128-byte swizzle,
-  // 1024 bytes between 8-row groups.  MN-major V: 64-column slabs kSlabKV
-  // apart (leading), 1024 bytes between 8-key groups (stride).
-  const uint64_t q_desc = ptx::sdesc_sw128(smem + C::kOffQ + t * C::kQBytes, 16, 1024);
+  // 1024 bytes between 8-row groups
+  const uint64_t q_desc = ptx::sdesc_sw128(smem + C::kOffQ, 16, 1024);
   const uint64_t k_desc0 = ptx::sdesc_sw128(smem + C::kOffK, 16, 1024);
-  const uint64_t v_desc0 = ptx::sdesc_sw128(smem + C::kOffV, C::kSlabKV, 1024);
-  const uint32_t t_s = tmem + C::col_s(t);
-  const uint32_t t_o = tmem + C::col_o(t);
   bool ok = true;
 
   const int rounds = (p.n_units + gridDim.x - 1) / gridDim.x;
@@ -444,31 +419,62 @@ __device__ void mma_role(const KParams& p, const Bars<D>& br, uint32_t smem, uin
     const int u = unit_of(r);
     if (u >= p.n_units) continue;
     const Unit w = decode_unit(p, u);
-    const int n = max(w.n[0], w.n[1]);
-    const int nt = t == 0 ? w.n[0] : w.n[1];  // (a select keeps Unit in registers)
+    const int n = w.n;
     if (n == 0) continue;
-    const int z_kv = w.b * p.Hkv + w.hkv;
-    if (nt > 0) {
-      if (!__all_sync(0xffffffffu, wait_bar(br, p.status, br.q_full(t), q_phase, kRoleMma))) break;
-      q_phase ^= 1u;
-    }
-    // S_t(0)
-    {
+    if (!__all_sync(0xffffffffu, wait_bar(br, p.status, br.q_full(), q_phase, kRoleMma))) break;
+    q_phase ^= 1u;
+    for (int j = 0; j < n; ++j, ++g) {
+      const uint32_t b = g % SB;
+      // buffer b held P(g-3): wait until PV(g-3) has read it
+      if (g >= SB && !__all_sync(0xffffffffu, wait_bar(br, p.status, br.pv_done(b),
+                                                       ((g - SB) / SB) & 1u, kRoleMma))) {
+        ok = false;
+        break;
+      }
       const uint32_t sk = kit % C::kKStages;
       if (!__all_sync(0xffffffffu, wait_bar(br, p.status, br.k_full(sk),
-                                            (kit / C::kKStages) & 1u, kRoleMma)))
+                                            (kit / C::kKStages) & 1u, kRoleMma))) {
+        ok = false;
         break;
-      ++kit;
-      if (nt > 0) {
-        ptx::tc_fence_after();
-        if (elect_one()) issue_qk<D, BF16>(t_s, q_desc, desc_add(k_desc0, sk * C::kKVBytes));
-        __syncwarp();
-        commit_one(br.s_full(t));
-        if (nt == 1) commit_one(br.q_empty(t));
       }
-      release_slot(br.k_empty(sk), nt > 0);
+      ++kit;
+      ptx::tc_fence_after();
+      if (elect_one()) issue_qk<D, BF16>(tmem + C::col_s(b), q_desc, desc_add(k_desc0, sk * C::kKVBytes));
+      __syncwarp();
+      commit_one(br.s_full(b));
+      commit_one(br.k_empty(sk));
+      if (j == n - 1) commit_one(br.q_empty());  // Q is free once its last S completes
     }
-    for (int j = 0; j < n; ++j, ++step) {
+  }
+  // Every MMA issued by this warp completes before TMEM is released.
+  commit_one(br.drain());
+  drain_wait(br.drain(), 0);
+}
+
+template <int D, bool BF16>
+__device__ void pv_issuer_role(const KParams& p, const Bars<D>& br, uint32_t smem, uint32_t tmem) {
+  using C = Cfg<D>;
+  constexpr uint32_t SB = C::kScoreBufs;
+  uint32_t vit = 0;
+  uint32_t g = 0;
+  // MN-major V: 64-column slabs kSlabKV apart (leading), 1024 bytes between
+  // 8-key groups (stride)
+  const uint64_t v_desc0 = ptx::sdesc_sw128(smem + C::kOffV, C::kSlabKV, 1024);
+  const uint32_t t_o = tmem + C::kColO;
+  bool ok = true;
+
+  const int rounds = (p.n_units + gridDim.x - 1) / gridDim.x;
+  for (int r = 0; ok && r < rounds; ++r) {
+    const int u = unit_of(r);
+    if (u >= p.n_units) continue;
+    const Unit w = decode_unit(p, u);
+    const int n = w.n;
+    if (n == 0) continue;
+    const int z_kv = w.b * p.Hkv + w.hkv;
+    uint32_t fmask = 0;
+    for (int j = 0; j < n; ++j, ++g) {
+      if ((j & 31) == 0) fmask = v_fp16_mask<BF16>(p, z_kv, j, n);
+      const uint32_t b = g % SB;
       const uint32_t sv = vit % C::kVStages;
       if (!__all_sync(0xffffffffu,
                       wait_bar(br, p.status, br.v_full(sv), (vit / C::kVStages) & 1u, kRoleMma))) {
@@ -476,56 +482,26 @@ __device__ void mma_role(const KParams& p, const Bars<D>& br, uint32_t smem, uin
         break;
       }
       ++vit;
-      const bool use_v = j < nt;
-      const bool split = use_v && v_split<BF16>(p, z_kv, j);
-      const bool has_next = j + 1 < n;
-      uint32_t sk = 0;
-      if (has_next) {
-        sk = kit % C::kKStages;
-        if (!__all_sync(0xffffffffu, wait_bar(br, p.status, br.k_full(sk),
-                                              (kit / C::kKStages) & 1u, kRoleMma))) {
-          ok = false;
-          break;
-        }
-        ++kit;
-      }
-      const bool use_k = j + 1 < nt;
-      // my turn: issuer 0 waits for issuer 1's previous group (none at the
-      // first key tile: the fresh barrier's preceding phase counts as done),
-      // issuer 1 for issuer 0's group of this key tile
-      const uint32_t turn_par = (t == 0) ? ((step & 1u) ^ 1u) : (step & 1u);
-      if (!__all_sync(0xffffffffu, wait_bar(br, p.status, br.turn(t), turn_par, kRoleMma))) {
+      const bool split = BF16 && ((fmask >> (j & 31)) & 1u) == 0u;
+      // P last: V is normally in shared memory long before the softmax
+      // delivers P(j)
+      if (!__all_sync(0xffffffffu, wait_bar(br, p.status, br.p_full(b), (g / SB) & 1u, kRoleMma))) {
         ok = false;
         break;
       }
-      // P last: V, K and the turn are normally ready long before the softmax
-      // finishes, so only this wait stands between P_t(j) and its MMAs
-      if (use_v) {
-        if (!__all_sync(0xffffffffu, wait_bar(br, p.status, br.p_full(t), p_phase, kRoleMma))) {
-          ok = false;
-          break;
-        }
-        p_phase ^= 1u;
-      }
       ptx::tc_fence_after();
-      if (elect_one()) {
-        if (use_v) issue_pv<D>(t_o, t_s, desc_add(v_desc0, sv * C::kKVBytes), j > 0, split);
-        if (use_k) issue_qk<D, BF16>(t_s, q_desc, desc_add(k_desc0, sk * C::kKVBytes));
-        ptx::mbar_arrive(br.turn(t ^ 1));  // the other issuer's group may follow
-      }
+      if (elect_one())
+        issue_pv<D>(t_o, tmem + C::col_s(b), desc_add(v_desc0, sv * C::kKVBytes), j > 0, split);
       __syncwarp();
-      if (use_v && j == nt - 1) commit_one(br.o_full(t));
-      release_slot(br.v_empty(sv), use_v);
-      if (use_k) {
-        commit_one(br.s_full(t));
-        // Q_t is free once the unit's last S_t MMA completes: the producer
-        // can load the next unit's Q_t while this unit finishes
-        if (j + 2 == nt) commit_one(br.q_empty(t));
+      commit_one(br.pv_done(b));
+      // the unit's last V stage is released by the epilogue (it stages O)
+      if (j == n - 1) {
+        commit_one(br.o_full());
+      } else {
+        commit_one(br.v_empty(sv));
       }
-      if (has_next) release_slot(br.k_empty(sk), use_k);
     }
   }
-  // Every MMA issued by this warp completes before TMEM is released.
   commit_one(br.drain());
   drain_wait(br.drain(), 0);
 }
@@ -538,10 +514,9 @@ __device__ void mma_role(const KParams& p, const Bars<D>& br, uint32_t smem, uin
 // with P_hi = p truncated to bf16 (columns [0, 64)) and P_lo = bf16(p - P_hi)
 // (columns [64, 128)); a single bf16 P (unit roundoff 2^-8) is too coarse for
 // rows dominated by a few keys, the pair leaves a relative error below 2^-15.
-// MASKED: columns c >= c_lim get P = 0.
-template <bool MASKED, bool SPLIT>
-__device__ __forceinline__ float exp_row(const uint32_t (&s)[BN], uint64_t sc2, uint64_t nm2, int c_lim,
-                                         uint32_t t_s) {
+// Masked keys arrive as -inf scores and give P = 0.
+template <bool SPLIT>
+__device__ __forceinline__ float exp_row(const uint32_t (&s)[BN], uint64_t sc2, uint64_t nm2, uint32_t t_s) {
   uint64_t rsum2[4];  // independent partial row sums, two lanes each
 #pragma unroll
   for (int k = 0; k < 4; ++k) rsum2[k] = 0ull;
@@ -557,12 +532,8 @@ __device__ __forceinline__ float exp_row(const uint32_t (&s)[BN], uint64_t sc2, 
           ptx::f2_fma(ptx::f2_pack(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), sc2, nm2);
       float x0, x1;
       ptx::f2_unpack(x2, x0, x1);
-      float p0 = ptx::ex2_approx(x0);
-      float p1 = ptx::ex2_approx(x1);
-      if constexpr (MASKED) {
-        p0 = (c < c_lim) ? p0 : 0.f;
-        p1 = (c + 1 < c_lim) ? p1 : 0.f;
-      }
+      const float p0 = ptx::ex2_approx(x0);
+      const float p1 = ptx::ex2_approx(x1);
       const uint64_t p2 = ptx::f2_pack(p0, p1);
       rsum2[i & 3] = ptx::f2_add(rsum2[i & 3], p2);
       if constexpr (SPLIT) {
@@ -586,76 +557,101 @@ __device__ __forceinline__ float exp_row(const uint32_t (&s)[BN], uint64_t sc2, 
 }
 
 template <int D, bool BF16>
-__device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t tmem, int t) {
+__device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t smem, uint32_t tmem,
+                             const CUtensorMap* tm_o) {
   using C = Cfg<D>;
+  constexpr int SB = C::kScoreBufs;
   const int lane_row = threadIdx.x & 127;           // row within the tile = TMEM lane
   const uint32_t quad = (threadIdx.x >> 5) & 3u;    // this warp's 32-lane TMEM quadrant
-  const uint32_t t_s = tmem + ((quad * 32u) << 16) + C::col_s(t);
-  const uint32_t t_o = tmem + ((quad * 32u) << 16) + C::col_o(t);
+  const uint32_t lane_addr = (quad * 32u) << 16;
+  const uint32_t t_o = tmem + lane_addr + C::kColO;
   const float scale_log2 = p.scale_log2;
-  uint32_t s_phase = 0, o_phase = 0;
+  uint32_t o_phase = 0;
+  uint32_t epi = 0;  // epilogues (staged O tiles) so far
+  uint32_t g = 0;    // score (and V) tiles of all units so far (buffer g % 3)
+  // thread 0: V stage still being read by the last O store (kNoStage: none)
+  constexpr uint32_t kNoStage = 0xFFFFFFFFu;
+  uint32_t pending_stage = kNoStage;
 
+  // Each unit is decoded one unit ahead, with the fp16 flags of its first
+  // 32 key tiles: during the previous unit's wait for its last P.V, where the
+  // integer divisions and the flag load cost nothing.  Unit indices grow
+  // with the round, so the first one past the end ends the loop.
   const int rounds = (p.n_units + gridDim.x - 1) / gridDim.x;
-  for (int r = 0; r < rounds; ++r) {
-    const int u = unit_of(r);
-    if (u >= p.n_units) continue;
-    const Unit w = decode_unit(p, u);
-    const int z_kv = w.b * p.Hkv + w.hkv;
-    const int r0 = w.m0 + t * BM;
-    if (r0 >= p.L) continue;
-    const int row = r0 + lane_row;
+  int u_next = unit_of(0);
+  Unit w_next;
+  uint32_t fmask_next = 0;
+  if (u_next < p.n_units) {
+    w_next = decode_unit(p, u_next);
+    fmask_next = v_fp16_mask<BF16>(p, w_next.b * p.Hkv + w_next.hkv, 0, w_next.n);
+  }
+  for (int r = 0; r < rounds && u_next < p.n_units; ++r) {
+    const Unit w = w_next;
+    uint32_t fmask = fmask_next;
+    auto decode_ahead = [&]() {
+      u_next = unit_of(r + 1);
+      if (u_next < p.n_units) {
+        w_next = decode_unit(p, u_next);
+        fmask_next = v_fp16_mask<BF16>(p, w_next.b * p.Hkv + w_next.hkv, 0, w_next.n);
+      }
+    };
+    const int row = w.m0 + lane_row;
     const bool row_ok = row < p.L;
     const int64_t grow = static_cast<int64_t>(w.bh) * p.L + row;
-    if (t == 0 && threadIdx.x == 0 && p.valid_len != nullptr) {
+    if (threadIdx.x == 0 && p.valid_len != nullptr) {
       const int vl = p.valid_len[w.b];
       if (vl < 0 || vl > p.L) atomicOr(p.status, kStatusValidLenClamped);
     }
-    const int nt = w.n[t];
-    if (nt == 0) {  // no visible key: O = 0, LSE = -inf
+    const int n = w.n;
+    if (n == 0) {  // no visible key: O = 0, LSE = -inf
       if (row_ok) {
         uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.o) + grow * D * 2);
 #pragma unroll
         for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
         if (p.lse != nullptr) p.lse[grow] = -INFINITY;
       }
+      decode_ahead();
       continue;
     }
+    const int z_kv = w.b * p.Hkv + w.hkv;
     // keys < key_lim are visible to this row
     const int key_lim = p.causal ? min(w.kv_len, row + 1) : w.kv_len;
     float m = -INFINITY;  // running max, log2 units (scaled)
     float l = 0.f;
     bool ok = true;
-    for (int j = 0; j < nt; ++j) {
+    for (int j = 0; j < n; ++j) {
+      const uint32_t gg = g + static_cast<uint32_t>(j);
+      const uint32_t b = gg % SB;
+      const uint32_t t_s = tmem + lane_addr + C::col_s(b);
       // P format of this key tile: fp16 P, or the bf16 pair (split)
-      const bool split = v_split<BF16>(p, z_kv, j);
-      ok = wait_bar(br, p.status, br.s_full(t), s_phase, kRoleSoftmax);
+      if (j > 0 && (j & 31) == 0) fmask = v_fp16_mask<BF16>(p, z_kv, j, n);
+      const bool split = BF16 && ((fmask >> (j & 31)) & 1u) == 0u;
+      ok = wait_bar(br, p.status, br.s_full(b), (gg / SB) & 1u, kRoleSoftmax);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
       }
-      s_phase ^= 1u;
       ptx::tc_fence_after();
       uint32_t s[BN];
       ptx::tmem_ld128(t_s, s);
       const int n0 = j * BN;
-      const bool masked = (n0 + BN > w.kv_len) || (p.causal && n0 + BN - 1 > r0);
+      const bool masked = (n0 + BN > w.kv_len) || (p.causal && n0 + BN - 1 > w.m0);
       const int c_lim = key_lim - n0;  // columns c < c_lim are visible
+      // Boundary tiles only: invisible scores become -inf, so the max and the
+      // exponentials below are the same code for every tile (one copy of the
+      // unrolled loops keeps the hot code small); exp2(-inf * scale - m) = 0
+      // because the scale is > 0 (a zero sm_scale arrives as FLT_MIN).
+      if (masked) {
+#pragma unroll
+        for (int c = 0; c < BN; ++c) s[c] = (c < c_lim) ? s[c] : 0xFF800000u;
+      }
       // row max: 8 independent chains of 3-input maxima
       float mxk[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) mxk[k] = -INFINITY;
-      if (masked) {
 #pragma unroll
-        for (int i = 0; i < BN / 2; ++i) {
-          const int c = 2 * i;
-          mxk[i & 7] = ptx::max3(mxk[i & 7], (c < c_lim) ? __uint_as_float(s[c]) : -INFINITY,
-                                 (c + 1 < c_lim) ? __uint_as_float(s[c + 1]) : -INFINITY);
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < BN / 2; ++i)
-          mxk[i & 7] = ptx::max3(mxk[i & 7], __uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1]));
-      }
+      for (int i = 0; i < BN / 2; ++i)
+        mxk[i & 7] = ptx::max3(mxk[i & 7], __uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1]));
       const float mx = ptx::max3(ptx::max3(mxk[0], mxk[1], mxk[2]), ptx::max3(mxk[3], mxk[4], mxk[5]),
                                  fmaxf(mxk[6], mxk[7]));
       const float m_tile = (mx == -INFINITY) ? -INFINITY : mx * scale_log2;
@@ -670,23 +666,27 @@ __device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t tmem,
       const float neg_m = (m == -INFINITY) ? 0.f : -m;
       const uint64_t sc2 = ptx::f2_pack(scale_log2, scale_log2);
       const uint64_t nm2 = ptx::f2_pack(neg_m, neg_m);
-      // P over the S columns (every S value is already in registers); the
-      // masked form only on key tiles that need it, so full tiles carry no
-      // per-key selects
+      // P over the S columns (every S value is already in registers)
       float rowsum;
       if (!split) {
-        rowsum = masked ? exp_row<true, false>(s, sc2, nm2, c_lim, t_s)
-                        : exp_row<false, false>(s, sc2, nm2, c_lim, t_s);
+        rowsum = exp_row<false>(s, sc2, nm2, t_s);
       } else if constexpr (BF16) {
-        rowsum = masked ? exp_row<true, true>(s, sc2, nm2, c_lim, t_s)
-                        : exp_row<false, true>(s, sc2, nm2, c_lim, t_s);
+        rowsum = exp_row<true>(s, sc2, nm2, t_s);
       } else {
         rowsum = 0.f;
       }
       l = l * alpha + rowsum;
-      // O was accumulated against the old max: rescale it before PV_j runs.
-      // PV_{j-1} is complete: the commit that signalled S_j came after it.
+      // O was accumulated against the old max: rescale it before PV(j) runs.
+      // PV(j-3) and earlier are complete (S(j) was issued after PV(j-3)
+      // completed); PV(j-2) and PV(j-1) may still be running: wait for
+      // PV(j-1) (the tensor core completes them in order).
       if (j > 0 && __any_sync(0xffffffffu, rescale)) {
+        ok = wait_bar(br, p.status, br.pv_done((gg - 1u) % SB), ((gg - 1u) / SB) & 1u, kRoleSoftmax);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
 #pragma unroll 1
         for (int c0 = 0; c0 < D; c0 += 32) {
           uint32_t o[32];
@@ -698,15 +698,33 @@ __device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t tmem,
       }
       ptx::tmem_st_wait();
       ptx::tc_fence_before();
-      ptx::mbar_arrive(br.p_full(t));
+      ptx::mbar_arrive(br.p_full(b));
+      // one step after an O store was issued its source has long been read:
+      // hand that V stage back to the producer
+      if (threadIdx.x == 0 && pending_stage != kNoStage) {
+        ptx::bulk_wait_read_all();
+        ptx::mbar_arrive(br.v_empty(pending_stage));
+        pending_stage = kNoStage;
+      }
     }
+    g += static_cast<uint32_t>(n);
     if (!ok) return;
+    decode_ahead();  // while the last P.V runs
     // epilogue
-    ok = wait_bar(br, p.status, br.o_full(t), o_phase, kRoleEpilogue);
+    ok = wait_bar(br, p.status, br.o_full(), o_phase, kRoleEpilogue);
     if (!__all_sync(0xffffffffu, ok)) return;
     o_phase ^= 1u;
     ptx::tc_fence_after();
+    // staging tile: the V stage of this unit's last key tile (g counts V
+    // tiles too); its PV has completed (o_full)
+    const uint32_t vstage = (g - 1u) % C::kVStages;
+    const uint32_t stage = smem + C::kOffV + vstage * C::kKVBytes;
+    // O / l as 16-bit pairs into the staging tile: 64-column slabs of 128-byte
+    // rows, the 16-byte chunk k of row r at chunk position k ^ (r % 8) (the
+    // 128-byte swizzle of the O tensor map)
     const float inv_l = 1.f / l;
+    const uint32_t stage_row = stage + static_cast<uint32_t>(lane_row) * 128u;
+    const uint32_t rsw = static_cast<uint32_t>(lane_row) & 7u;
 #pragma unroll 1
     for (int c0 = 0; c0 < D; c0 += 32) {
       uint32_t o[32];
@@ -715,12 +733,26 @@ __device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t tmem,
 #pragma unroll
       for (int c = 0; c < 16; ++c)
         h[c] = pack2<BF16>(__uint_as_float(o[2 * c]) * inv_l, __uint_as_float(o[2 * c + 1]) * inv_l);
-      if (row_ok) {
-        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.o) + (grow * D + c0) * 2);
+      const uint32_t slab = stage_row + static_cast<uint32_t>(c0 / 64) * C::kSlabQ;
+      const uint32_t k0 = static_cast<uint32_t>(c0 % 64) / 8u;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) dst[c] = make_uint4(h[4 * c], h[4 * c + 1], h[4 * c + 2], h[4 * c + 3]);
+      for (int i = 0; i < 4; ++i)
+        ptx::st_shared_v4(slab + (((k0 + i) ^ rsw) << 4),
+                          make_uint4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]));
+    }
+    ptx::fence_proxy_async_shared();  // the generic-proxy writes, before the TMA reads them
+    ptx::mbar_arrive(br.o_staged());
+    if (threadIdx.x == 0) {
+      // rows past L are outside the tensor map and are not written
+      if (wait_bar(br, p.status, br.o_staged(), epi & 1u, kRoleEpilogue)) {
+#pragma unroll
+        for (int hs = 0; hs < C::kHalves; ++hs)
+          ptx::tma_store_3d(tm_o, stage + hs * C::kSlabQ, hs * 64, w.m0, w.bh);
+        ptx::bulk_commit_group();
+        pending_stage = vstage;  // released after the next softmax step
       }
     }
+    ++epi;
     if (row_ok && p.lse != nullptr) p.lse[grow] = (m + ptx::lg2_approx(l)) * kLn2;
   }
 }
@@ -732,7 +764,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v,
-                       const __grid_constant__ CUtensorMap tm_v16, const KParams p) {
+                       const __grid_constant__ CUtensorMap tm_v16,
+                       const __grid_constant__ CUtensorMap tm_o, const KParams p) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t smem = (ptx::smem_u32(smem_raw) + 1023u) & ~1023u;
@@ -742,25 +775,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int t = 0; t < QT; ++t) {
-      ptx::mbar_init(br.q_full(t), 1);
-      ptx::mbar_init(br.q_empty(t), 1);
-      ptx::mbar_init(br.s_full(t), 1);
-      ptx::mbar_init(br.p_full(t), BM);
-      ptx::mbar_init(br.o_full(t), 1);
-    }
-    // ring slots and the final drain: one release from each MMA issuer
+    ptx::mbar_init(br.q_full(), 1);
+    ptx::mbar_init(br.q_empty(), 1);
     for (int s = 0; s < C::kKStages; ++s) {
       ptx::mbar_init(br.k_full(s), 1);
-      ptx::mbar_init(br.k_empty(s), QT);
+      ptx::mbar_init(br.k_empty(s), 1);
     }
     for (int s = 0; s < C::kVStages; ++s) {
       ptx::mbar_init(br.v_full(s), 1);
-      ptx::mbar_init(br.v_empty(s), QT);
+      ptx::mbar_init(br.v_empty(s), 1);
     }
-    ptx::mbar_init(br.drain(), QT);
-    ptx::mbar_init(br.turn(0), 1);
-    ptx::mbar_init(br.turn(1), 1);
+    for (int b = 0; b < C::kScoreBufs; ++b) {
+      ptx::mbar_init(br.s_full(b), 1);
+      ptx::mbar_init(br.p_full(b), kSoftmaxThreads);
+    }
+    for (int b = 0; b < C::kScoreBufs; ++b) ptx::mbar_init(br.pv_done(b), 1);
+    ptx::mbar_init(br.o_full(), 1);
+    ptx::mbar_init(br.drain(), 2);  // one commit from each issuer
+    ptx::mbar_init(br.o_staged(), kSoftmaxThreads);
     ptx::st_shared_volatile(br.abort_word(), 0u);
     ptx::fence_barrier_init();
   }
@@ -770,7 +802,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::prefetch_tensormap(&tm_v);
     if constexpr (BF16) ptx::prefetch_tensormap(&tm_v16);
   }
-  if (warp == kMmaWarp0) {
+  if (threadIdx.x == 0) ptx::prefetch_tensormap(&tm_o);
+  if (warp == kPvWarp) {
     ptx::tmem_alloc(br.tmem_word(), C::kTmemCols);
     ptx::tmem_relinquish();
   }
@@ -779,22 +812,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = ptx::ld_shared_volatile(br.tmem_word());
 
-  if (warp >= 8) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(RegSplit<D>::kControl));
-    if (warp == kProducerWarp) {
-      if (lane == 0) producer_role<D, BF16>(p, br, smem, &tm_q, &tm_k, &tm_v, &tm_v16);
-    } else if (warp < kMmaWarp0 + QT) {
-      mma_role<D, BF16>(p, br, smem, tmem, warp - kMmaWarp0);  // whole warp
-    }
-    // warp 11 has no role
+  if (warp == kProducerWarp) {
+    if (lane == 0) producer_role<D, BF16>(p, br, smem, &tm_q, &tm_k, &tm_v, &tm_v16);
+  } else if (warp == kPvWarp) {
+    pv_issuer_role<D, BF16>(p, br, smem, tmem);  // whole warp
+  } else if (warp == kSWarp) {
+    s_issuer_role<D, BF16>(p, br, smem, tmem);  // whole warp
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(RegSplit<D>::kSoftmax));
-    softmax_role<D, BF16>(p, br, tmem, warp >> 2);
+    softmax_role<D, BF16>(p, br, smem, tmem, &tm_o);  // warps 0-3
+    // the last O stores read their staging tiles: finish before shared memory
+    // goes (no stage needs releasing: the producer has no loads left)
+    if (threadIdx.x == 0) ptx::bulk_wait_all();
   }
 
   ptx::tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp0) {
+  if (warp == kPvWarp) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, C::kTmemCols);
   }
@@ -806,14 +839,7 @@ cudaError_t launch_instance(const Problem& pr, const CUtensorMap* maps, int num_
   static bool configured = false;  // per (D, dtype) instance
   auto kern = attn_fwd_tc_kernel<D, BF16>;
   if (!configured) {
-    // The setmaxnreg split is only safe when the CTA is launched with exactly
-    // kLaunchRegs registers per thread; anything else could stall the
-    // increasing warpgroups forever, so refuse to launch.
-    cudaFuncAttributes fa;
-    cudaError_t e = cudaFuncGetAttributes(&fa, kern);
-    if (e != cudaSuccess) return e;
-    if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidKernelImage;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     configured = true;
   }
@@ -829,12 +855,15 @@ cudaError_t launch_instance(const Problem& pr, const CUtensorMap* maps, int num_
   kp.Hkv = pr.Hkv;
   kp.L = pr.L;
   kp.G = pr.Hq / pr.Hkv;
-  kp.n_mb = (pr.L + kUnitRows - 1) / kUnitRows;
+  kp.n_mb = (pr.L + BM - 1) / BM;
   kp.n_units = pr.B * pr.Hq * kp.n_mb;
-  kp.scale_log2 = pr.sm_scale * 1.4426950408889634f;
+  // A zero scale is passed as the smallest normal float: every product
+  // s * scale then rounds to zero exactly as with 0 (all visible keys get
+  // P = 1), while -inf (a masked score) times it stays -inf and gives P = 0.
+  kp.scale_log2 = pr.sm_scale > 0.f ? pr.sm_scale * 1.4426950408889634f : 1.17549435e-38f;
   kp.causal = pr.causal;
   const int grid = kp.n_units < num_sms ? kp.n_units : num_sms;
-  kern<<<grid, kThreads, C::kSmemBytes, pr.stream>>>(maps[0], maps[1], maps[2], maps[3], kp);
+  kern<<<grid, kThreads, C::kSmemBytes, pr.stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4], kp);
   return cudaGetLastError();
 }
 
@@ -842,12 +871,12 @@ cudaError_t launch_instance(const Problem& pr, const CUtensorMap* maps, int num_
 
 bool tc_config(int D, TcConfig* out) {
   if (D == 64) {
-    *out = {BM, QT, BN, Cfg<64>::kKStages + Cfg<64>::kVStages, kThreads, Cfg<64>::kSmemBytes,
+    *out = {BM, 1, BN, Cfg<64>::kKStages + Cfg<64>::kVStages, kThreads, Cfg<64>::kSmemBytes,
             static_cast<int>(Cfg<64>::kTmemCols)};
     return true;
   }
   if (D == 128) {
-    *out = {BM, QT, BN, Cfg<128>::kKStages + Cfg<128>::kVStages, kThreads, Cfg<128>::kSmemBytes,
+    *out = {BM, 1, BN, Cfg<128>::kKStages + Cfg<128>::kVStages, kThreads, Cfg<128>::kSmemBytes,
             static_cast<int>(Cfg<128>::kTmemCols)};
     return true;
   }
