@@ -230,3 +230,26 @@ def test_bf16_v_tiles_beyond_fp16_range(D, causal):
     o, lse = run_gpu(q, k, v, causal, None, sm)
     o_ref, lse_ref = oracle.attn_fwd_bits(wl.bits(q), wl.bits(k), wl.bits(v), 1, sm, causal=causal)
     check(o, lse, o_ref, lse_ref, "bf16 V beyond fp16 range D%d causal=%s" % (D, causal))
+
+
+@pytest.mark.parametrize("L, D, dtype, causal, valid_len", [
+    (128, 128, wl.BF16, True, None),
+    (200, 64, wl.F16, False, [200, 0, 77, 129, 200, 1, 150, 199]),
+    (300, 128, wl.BF16, True, [300, 257, 0, 128, 300, 5, 299, 255]),
+    (260, 64, wl.BF16, True, None),
+])
+def test_many_short_units_per_cta(L, D, dtype, causal, valid_len):
+    """Several units per CTA with one to three key tiles each: the unit
+    boundary (O staged in the last V stage, its deferred release, the next
+    unit decoded ahead, fewer score tiles than score buffers) many times per
+    CTA, with empty and ragged units mixed in."""
+    B, Hq, Hkv = 8, 40, 8
+    q, k, v, vl = wl.make_inputs(B, Hq, Hkv, L, D, dtype, seed=L + D + 7, valid_len=valid_len)
+    sm = 1.0 / math.sqrt(D)
+    o, lse = run_gpu(q, k, v, causal, vl, sm)
+    o_ref, lse_ref = oracle.attn_fwd_bits(wl.bits(q), wl.bits(k), wl.bits(v), wl.dtype_code(dtype), sm,
+                                          causal=causal, valid_len=None if vl is None else vl.numpy())
+    check(o, lse, o_ref, lse_ref, "many short units L%d D%d causal=%s" % (L, D, causal))
+    # the same call again gives the same bits (the staging stages rotate)
+    o2, lse2 = run_gpu(q, k, v, causal, vl, sm)
+    assert np.array_equal(o, o2) and np.array_equal(lse, lse2)
