@@ -5,8 +5,10 @@ see ``csrc/`` and ``include/attn.h``).  This package is its thin ctypes
 binding: argument marshalling only.  The library is loaded on first use and a
 missing or unbuilt library is an error, never a fallback.
 """
-from .binding import (ATTN_BF16, ATTN_F16, ATTN_OK, AttnError, attn_fwd, declared_symbols,
-                      fwd_raw, lib_path, load, query, shutdown, status, strerror)
+from .binding import (ATTN_BF16, ATTN_F16, ATTN_OK, AttnError, attn_fwd, attn_fwd_host,
+                      declared_symbols, fwd_raw, host_plan, lib_path, load, query, shutdown,
+                      status, strerror)
 
-__all__ = ["ATTN_BF16", "ATTN_F16", "ATTN_OK", "AttnError", "attn_fwd", "declared_symbols",
-           "fwd_raw", "lib_path", "load", "query", "shutdown", "status", "strerror"]
+__all__ = ["ATTN_BF16", "ATTN_F16", "ATTN_OK", "AttnError", "attn_fwd", "attn_fwd_host",
+           "declared_symbols", "fwd_raw", "host_plan", "lib_path", "load", "query", "shutdown",
+           "status", "strerror"]

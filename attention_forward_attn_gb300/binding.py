@@ -46,6 +46,16 @@ class Caps(ctypes.Structure):
         return {n: getattr(self, n) for n, _ in self._fields_}
 
 
+class Chunk(ctypes.Structure):
+    """attn_chunk_t: flattened query heads [q_head0, q_head0 + q_heads), the K/V
+    heads [kv_head0, kv_head0 + kv_heads) it copies in, its attention calls."""
+    _fields_ = [(n, ctypes.c_int) for n in ("q_head0", "q_heads", "kv_head0", "kv_heads",
+                                            "calls")]
+
+    def as_tuple(self):
+        return (self.q_head0, self.q_heads, self.kv_head0, self.kv_heads, self.calls)
+
+
 _lock = threading.Lock()
 _lib = None
 
@@ -68,10 +78,13 @@ def load():
             p = ctypes.c_void_p
             i = ctypes.c_int
             fwd_args = [p, p, p, p, p, i, i, i, i, i, ctypes.c_float, i, p, i, p]
-            for name in ("attn_fwd", "attn_fwd_simt", "attn_fwd_noalloc"):
+            for name in ("attn_fwd", "attn_fwd_simt", "attn_fwd_noalloc", "attn_fwd_host"):
                 fn = getattr(lib, name)
                 fn.argtypes = fwd_args
                 fn.restype = i
+            lib.attn_host_plan.argtypes = [i, i, i, i, i, i, ctypes.POINTER(Chunk), i,
+                                           ctypes.POINTER(ctypes.c_int)]
+            lib.attn_host_plan.restype = i
             lib.attn_status.argtypes = [p, ctypes.POINTER(ctypes.c_int)]
             lib.attn_status.restype = i
             lib.attn_query.argtypes = [i, i, ctypes.POINTER(Caps)]
@@ -133,6 +146,23 @@ def query(D: int, dtype: int = ATTN_BF16) -> dict:
 
 def shutdown():
     load().attn_shutdown()
+
+
+def host_plan(B: int, Hq: int, Hkv: int, L: int, D: int, dtype: int = ATTN_BF16):
+    """attn_host_plan: the chunks attn_fwd_host queues, as
+    (q_head0, q_heads, kv_head0, kv_heads, calls) tuples."""
+    lib = load()
+    n = ctypes.c_int(0)
+    st = int(lib.attn_host_plan(int(B), int(Hq), int(Hkv), int(L), int(D), int(dtype), None, 0,
+                                ctypes.byref(n)))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_host_plan")
+    arr = (Chunk * max(1, n.value))()
+    st = int(lib.attn_host_plan(int(B), int(Hq), int(Hkv), int(L), int(D), int(dtype), arr,
+                                n.value, ctypes.byref(n)))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_host_plan")
+    return [c.as_tuple() for c in arr[:n.value]]
 
 
 # ------------------------------------------------------------------ torch-facing call
@@ -197,4 +227,59 @@ def attn_fwd(q, k, v, *, causal=False, sm_scale=None, valid_len=None, out=None, 
                  _stream_handle(stream), simt=simt)
     if st != ATTN_OK:
         raise AttnError(st, "attn_fwd_simt" if simt else "attn_fwd")
+    return out, (lse if return_lse else None)
+
+
+def attn_fwd_host(q, k, v, *, causal=False, sm_scale=None, valid_len=None, out=None, lse=None,
+                  return_lse=True, stream=None, synchronize=True):
+    """Fused attention forward on host (CPU) tensors through attn_fwd_host.
+
+    Same shapes as attn_fwd, but q, k, v, valid_len and the outputs live in
+    host memory; page-locked tensors (``pin_memory()``) let the library
+    overlap the copies with the kernels.  Outputs that are not passed are
+    allocated page-locked.  With ``synchronize`` the call waits for the
+    stream before returning; otherwise o and lse are valid once the stream
+    has synchronised.  Returns (o, lse).
+    """
+    import torch
+    if k.dim() == 3:
+        k = k.unsqueeze(1)
+    if v.dim() == 3:
+        v = v.unsqueeze(1)
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("%s must be a contiguous host tensor" % name)
+    B, Hq, L, D = q.shape
+    Hkv = k.shape[1]
+    if k.shape != v.shape or k.shape[0] != B or k.shape[2] != L or k.shape[3] != D:
+        raise ValueError("k and v must be [B, Hkv, L, D] matching q")
+    if q.dtype != k.dtype or q.dtype != v.dtype:
+        raise TypeError("q, k and v must share one dtype")
+    if sm_scale is None:
+        sm_scale = 1.0 / float(D) ** 0.5
+    if out is None:
+        out = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+    elif out.is_cuda or not out.is_contiguous() or out.shape != q.shape or out.dtype != q.dtype:
+        raise ValueError("out must be a contiguous host tensor like q")
+    if return_lse and lse is None:
+        lse = torch.empty((B * Hq, L), dtype=torch.float32, pin_memory=True)
+    elif return_lse and (lse.is_cuda or not lse.is_contiguous() or lse.dtype != torch.float32
+                         or lse.numel() != B * Hq * L):
+        raise ValueError("lse must be a contiguous float32 host tensor of B*Hq*L elements")
+    vl_ptr = None
+    if valid_len is not None:
+        if valid_len.dtype != torch.int32 or valid_len.is_cuda or valid_len.numel() != B:
+            raise ValueError("valid_len must be an int32 host tensor of B elements")
+        valid_len = valid_len.contiguous()
+        vl_ptr = valid_len.data_ptr()
+    handle = _stream_handle(stream)
+    st = fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                 lse.data_ptr() if return_lse else None, B, Hq, Hkv, L, D, sm_scale,
+                 int(bool(causal)), vl_ptr, _dtype_code(q), handle, entry="attn_fwd_host")
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fwd_host")
+    if synchronize:
+        st, code = status(stream)
+        if st != ATTN_OK:
+            raise AttnError(st, "attn_fwd_host (device status %#x)" % code)
     return out, (lse if return_lse else None)

@@ -66,6 +66,8 @@ attn_status_t validate(const void* q, const void* k, const void* v, void* o, flo
     return ATTN_ERR_ALIGN;
   if ((lse != nullptr && !aligned(lse, 4)) || (valid_len != nullptr && !aligned(valid_len, 4)))
     return ATTN_ERR_ALIGN;
+  // (alignment is checked last: attn_fwd_host, whose host buffers need none,
+  // treats ATTN_ERR_ALIGN as success)
   return ATTN_OK;
 }
 
@@ -162,6 +164,20 @@ attn_status_t workspace_pool(int dev, DeviceState* st, cudaMemPool_t* out) {
 }  // namespace
 
 namespace attn {
+
+attn_status_t current_device(int* dev, int* num_sms, int** status) {
+  DeviceState* st = nullptr;
+  attn_status_t s = device_state(dev, &st);
+  if (s != ATTN_OK) return s;
+  *num_sms = st->num_sms;
+  *status = st->status;
+  return ATTN_OK;
+}
+
+attn_status_t device_pool(int dev, cudaMemPool_t* out) {
+  if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_ARCH;
+  return workspace_pool(dev, &g_dev[dev], out);
+}
 
 // Tensor map over a contiguous [heads, L, D] 16-bit tensor viewed as 3-D
 // (D innermost), boxes of 64 columns x `rows` rows x 1 head, 128-byte swizzle.
@@ -362,6 +378,7 @@ const char* attn_strerror(attn_status_t status) {
 int attn_last_cuda_error(void) { return g_last_cuda_error; }
 
 void attn_shutdown(void) {
+  attn::host_path_shutdown();  // before g_mu: attn_fwd_host takes its own lock, then g_mu
   std::lock_guard<std::mutex> lock(g_mu);
   int cur = 0;
   const bool have_cur = cudaGetDevice(&cur) == cudaSuccess;

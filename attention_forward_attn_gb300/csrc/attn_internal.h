@@ -81,4 +81,13 @@ Problem make_problem(const void* q, const void* k, const void* v, void* o, float
 // and clear it (a no-op unless attn_fwd_noalloc ran on that device).
 attn_status_t noalloc_take_status(int dev, int* code);
 
+// attn_api.cu: the current device (probed, status word allocated, sm_103
+// checked) with its SM count and status word, and its workspace pool
+// (created on first use).
+attn_status_t current_device(int* dev, int* num_sms, int** status);
+attn_status_t device_pool(int dev, cudaMemPool_t* out);
+
+// attn_host.cu: destroy the host path's per-device copy streams and events.
+void host_path_shutdown();
+
 }  // namespace attn

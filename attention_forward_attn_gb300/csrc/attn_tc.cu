@@ -46,6 +46,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <atomic>
+
 #include "attn_internal.h"
 #include "ptx.cuh"
 
@@ -836,12 +838,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D, bool BF16>
 cudaError_t launch_instance(const Problem& pr, const CUtensorMap* maps, int num_sms) {
   using C = Cfg<D>;
-  static bool configured = false;  // per (D, dtype) instance
+  // the shared-memory opt-in is per device; set once per (D, dtype) instance and device
+  static std::atomic<uint64_t> configured{0};
   auto kern = attn_fwd_tc_kernel<D, BF16>;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev < 64 ? (1ull << dev) : 0ull;
+  if (bit == 0 || (configured.load(std::memory_order_relaxed) & bit) == 0) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    configured = true;
+    configured.fetch_or(bit, std::memory_order_relaxed);
   }
   KParams kp;
   kp.o = pr.o;

@@ -159,6 +159,81 @@ attn_status_t attn_fwd_noalloc(const void* q, const void* k, const void* v, void
                                attn_stream_t stream);
 
 /*
+ * attn_fwd_host -- attn_fwd with every buffer in HOST memory: the call a
+ * program makes when its tensors are not yet on the GPU.  The pages define
+ * only the device-side operation; this entry point adds the host<->device
+ * transfers around it.
+ *
+ * Arguments: as attn_fwd, except that q, k, v, o, lse and valid_len are host
+ * pointers (any alignment).  Page-locked memory (cudaHostAlloc,
+ * cudaHostRegister, torch pin_memory) lets the copies overlap the kernels;
+ * pageable memory gives the same results, but the CUDA driver then stages
+ * each copy and this call blocks until it is done.  Pointers to device or
+ * managed memory are accepted too (the copies use cudaMemcpyDefault).
+ *
+ * Work: the problem is cut into chunks of consecutive query heads -- see
+ * attn_host_plan; each chunk is one contiguous slice of every tensor -- and
+ * three queues run side by side: the host->device copies of Q, K and V
+ * chunk by chunk on a copy stream the library owns, the attention of each
+ * chunk (exactly attn_fwd's kernels, on `stream`) once its inputs have
+ * landed, and the device->host copies of O and LSE of each finished chunk
+ * on a second library-owned copy stream.  The host link is the bound: the
+ * call moves 2*(B*Hq + 2*B*Hkv)*L*D bytes in and 2*B*Hq*L*D (+ 4*B*Hq*L
+ * for lse) out.  Results are identical to attn_fwd's on the same inputs.
+ *
+ * Ordering: everything the call queues starts after the work already on
+ * `stream`, and `stream` waits for all of it (both copy streams join it at
+ * the end), so o and lse may be read once `stream` has synchronised
+ * (attn_status(stream, ...) or cudaStreamSynchronize).  The call itself
+ * returns after queueing (unless the memory is pageable).
+ *
+ * Device memory: one stream-ordered allocation from the library's
+ * per-device pool holding the device copies of the whole problem
+ * (2*(2*B*Hq + 2*B*Hkv)*L*D bytes, + lse, + valid_len), returned with
+ * cudaFreeAsync on `stream` after the last copy; ATTN_BF16 chunks also take
+ * attn_fwd's workspace.  The copy streams and their events are created on
+ * the first call on a device and destroyed by attn_shutdown.  Calls on one
+ * device are serialised while they are queued (a per-device lock); their
+ * copies share the two copy streams.
+ *
+ * Errors: argument errors as attn_fwd (nothing is queued).  A CUDA error
+ * while queueing stops the remaining chunks, still joins and frees what
+ * was queued, and returns ATTN_ERR_CUDA.
+ */
+attn_status_t attn_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse,
+                            int B, int Hq, int Hkv, int L, int D, float sm_scale, int causal,
+                            const int32_t* valid_len, attn_dtype_t dtype, attn_stream_t stream);
+
+/* One chunk of attn_fwd_host.  Heads are flattened: query head h of batch b
+ * is b*Hq + h, key/value head h_kv of batch b is b*Hkv + h_kv. */
+typedef struct {
+  int q_head0;   /* first query head of the chunk */
+  int q_heads;   /* consecutive query heads in the chunk (>= 1) */
+  int kv_head0;  /* first key/value head whose K and V this chunk copies in */
+  int kv_heads;  /* K/V heads it copies in (0 when earlier chunks copied all it needs) */
+  int calls;     /* attention calls it is computed in: the query heads are cut at
+                    key/value-group and batch boundaries into calls of whole batches,
+                    whole groups of one batch, or part of one group */
+} attn_chunk_t;
+
+/*
+ * attn_host_plan -- the chunks attn_fwd_host cuts a problem into, in the
+ * order it queues them.  Together the chunks copy every query head and
+ * every key/value head in exactly once, in order, and each chunk's K/V heads
+ * have landed no later than its own inputs.  A full chunk holds about
+ * 8 MiB of input (more when that would make over 48 of them); the first
+ * chunks ramp up from 1/8 of that and the last ones ramp down, so that the
+ * first kernel starts early and little is left once the last input lands.
+ * A problem under 12 MiB of input is one chunk.  Writes min(*n_chunks, cap)
+ * entries to chunks (chunks may be NULL when cap is 0) and the full count
+ * to *n_chunks.  Host-only: needs no device.  Returns attn_fwd's argument
+ * errors for invalid sizes, ATTN_ERR_ARG for a NULL n_chunks or a negative
+ * cap.
+ */
+attn_status_t attn_host_plan(int B, int Hq, int Hkv, int L, int D, attn_dtype_t dtype,
+                             attn_chunk_t* chunks, int cap, int* n_chunks);
+
+/*
  * attn_status -- synchronise `stream`, then read and clear the device status
  * word of the current device.  *device_code (may be NULL) receives the raw
  * word: bit 0 a bounded wait timed out, bit 1 a valid_len value was clamped;
@@ -198,9 +273,9 @@ const char* attn_strerror(attn_status_t status);
  * returned on this thread, or 0. */
 int attn_last_cuda_error(void);
 
-/* Free the per-device status words and destroy the per-device workspace
- * pools (their memory is released once every queued call that took a
- * workspace has completed).  Optional, at process exit; attn_fwd may be called
+/* Free the per-device status words, destroy the per-device workspace pools
+ * (their memory is released once every queued call that took a workspace
+ * has completed) and attn_fwd_host's copy streams and events.  Optional, at process exit; attn_fwd may be called
  * again afterwards (they are re-created). */
 void attn_shutdown(void);
 
