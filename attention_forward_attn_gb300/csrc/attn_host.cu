@@ -168,18 +168,25 @@ int plan(int B, int Hq, int Hkv, int L, int D, attn_chunk_t* out, int cap) {
   for (int c = 0; u < units; ++c) {
     const int64_t ramp = c < 3 ? first << c : full;
     const int64_t target = std::min(std::min(full, ramp), std::max(first, left / 2));
-    const int64_t u0 = u, kv0 = kv_done;
-    int64_t bytes = 0;
-    while (u < units) {
-      const int64_t kv = u / group;  // flattened K/V head of query head u
-      const int64_t add = head + (kv >= kv_done ? 2 * head : 0);
-      if (u > u0 && bytes + add > target) break;
+    int64_t end = u, bytes = 0, kv_seen = kv_done;
+    while (end < units) {
+      const int64_t kv = end / group;  // flattened K/V head of query head `end`
+      const int64_t add = head + (kv >= kv_seen ? 2 * head : 0);
+      if (end > u && bytes + add > target) break;
       bytes += add;
-      if (kv >= kv_done) kv_done = kv + 1;
-      ++u;
+      if (kv >= kv_seen) kv_seen = kv + 1;
+      ++end;
     }
-    left -= bytes;
-    emit(u0, u, kv0, kv_done);
+    // a chunk of a whole group or more ends on a group boundary when that
+    // drops at most a quarter of it: its calls are then whole groups (or
+    // whole batches), not parts of a group
+    if (end < units && end - u >= group && end % group != 0 && 4 * (end % group) <= end - u)
+      end -= end % group;
+    const int64_t kv0 = kv_done;
+    kv_done = std::max(kv_done, (end - 1) / group + 1);
+    left -= (end - u) * head + 2 * (kv_done - kv0) * head;
+    emit(u, end, kv0, kv_done);
+    u = end;
   }
   return n;
 }

@@ -220,11 +220,12 @@ typedef struct {
  * attn_host_plan -- the chunks attn_fwd_host cuts a problem into, in the
  * order it queues them.  Together the chunks copy every query head and
  * every key/value head in exactly once, in order, and each chunk's K/V heads
- * have landed no later than its own inputs.  A full chunk holds about
- * 8 MiB of input (more when that would make over 48 of them); the first
- * chunks ramp up from 1/8 of that and the last ones ramp down, so that the
- * first kernel starts early and little is left once the last input lands.
- * A problem under 12 MiB of input is one chunk.  Writes min(*n_chunks, cap)
+ * have landed no later than its own inputs.  A full chunk holds about an
+ * eighth of the problem's input, kept within [8, 32] MiB (and larger only
+ * when that would make over 48 chunks); the first chunks ramp up from 1/8
+ * of a full chunk and the last ones ramp down, so that the first kernel
+ * starts early and little is left once the last input lands.  A problem
+ * under 12 MiB of input is one chunk.  Writes min(*n_chunks, cap)
  * entries to chunks (chunks may be NULL when cap is 0) and the full count
  * to *n_chunks.  Host-only: needs no device.  Returns attn_fwd's argument
  * errors for invalid sizes, ATTN_ERR_ARG for a NULL n_chunks or a negative

@@ -77,9 +77,9 @@ def _check_plan(B, Hq, Hkv, L, D, chunks):
     G = Hq // Hkv
     head = L * D * 2
     total = B * (Hq + 2 * Hkv) * head
-    full = max(8 << 20, -(-total // 48))
+    full = max(min(max(total // 8, 8 << 20), 32 << 20), -(-total // 48))
     q_next = kv_next = 0
-    for q0, nq, kv0, nkv, calls in chunks:
+    for i, (q0, nq, kv0, nkv, calls) in enumerate(chunks):
         assert q0 == q_next and nq >= 1
         assert kv0 == kv_next and nkv >= 0
         q_next += nq
@@ -87,6 +87,9 @@ def _check_plan(B, Hq, Hkv, L, D, chunks):
         assert (q_next - 1) // G < kv_next, "chunk computes before its K/V heads are copied"
         assert calls == _pieces(q0, q0 + nq, Hq, Hkv)
         assert len(chunks) == 1 or nq == 1 or (nq + 2 * nkv) * head <= full
+        if nq >= G and i + 1 < len(chunks) and q_next % G:
+            # not ending on a group boundary: rounding down would drop over a quarter
+            assert 4 * (q_next % G) > nq
     assert q_next == B * Hq and kv_next == B * Hkv
 
 
@@ -98,7 +101,9 @@ SHAPES = list(itertools.product((1, 2, 3, 4, 7, 64), (1, 8, 32), (1, 2, 3, 8), (
 def test_plan_covers_every_head_once(lib, B, Hq, Hkv, L, D):
     chunks = attn.host_plan(B, Hq, Hkv, L, D)
     _check_plan(B, Hq, Hkv, L, D, chunks)
-    assert 1 <= len(chunks) <= 64
+    # at most 48 full chunks, each cut by at most a quarter at a group
+    # boundary, plus the ramps at both ends
+    assert 1 <= len(chunks) <= 48 * 4 // 3 + 8
     if B * (Hq + 2 * Hkv) * L * D * 2 < 12 << 20:
         assert len(chunks) == 1
 
@@ -112,7 +117,8 @@ def test_plan_of_large_problems(lib, B, Hq, Hkv, L, D):
     chunks = attn.host_plan(B, Hq, Hkv, L, D)
     _check_plan(B, Hq, Hkv, L, D, chunks)
     head = L * D * 2
-    full = max(8 << 20, -(-B * (Hq + 2 * Hkv) * head // 48))
+    total = B * (Hq + 2 * Hkv) * head
+    full = max(min(max(total // 8, 8 << 20), 32 << 20), -(-total // 48))
     small = max(full // 8, 3 * head)
     size = [(nq + 2 * nkv) * head for _, nq, _, nkv, _ in chunks]
     if B * Hq > 8:
@@ -122,21 +128,22 @@ def test_plan_of_large_problems(lib, B, Hq, Hkv, L, D):
 
 def test_plan_of_the_causal_gqa_workload(lib):
     """Q 4x32x4096x128, K/V 4x8x4096x128 (201 MB of input): 1 MiB per query
-    head, 2 MiB per K/V head pair; full chunks of 8 MiB."""
+    head, 2 MiB per K/V head pair (a group of four query heads shares one);
+    full chunks of 24 MiB (an eighth of the input), 3 MiB first."""
     chunks = attn.host_plan(4, 32, 8, 4096, 128)
-    assert chunks[:3] == [(0, 1, 0, 1, 1), (1, 2, 1, 0, 1), (3, 2, 1, 1, 2)]
-    assert max((nq + 2 * nkv) for _, nq, _, nkv, _ in chunks) == 8
-    assert len(chunks) == 36
+    assert chunks[:3] == [(0, 1, 0, 1, 1), (1, 3, 1, 0, 1), (4, 8, 1, 2, 1)]
+    assert max((nq + 2 * nkv) for _, nq, _, nkv, _ in chunks) <= 24
+    assert len(chunks) == 14 and sum(c[4] for c in chunks) == 17
 
 
 def test_plan_cap_and_errors(lib):
     n = ctypes.c_int(-1)
     arr = (binding.Chunk * 3)()
     assert lib.attn_host_plan(4, 32, 8, 4096, 128, 1, arr, 3, ctypes.byref(n)) == 0
-    assert n.value == 36  # full count, first three written
-    assert [c.as_tuple() for c in arr] == [(0, 1, 0, 1, 1), (1, 2, 1, 0, 1), (3, 2, 1, 1, 2)]
+    assert n.value == 14  # full count, first three written
+    assert [c.as_tuple() for c in arr] == [(0, 1, 0, 1, 1), (1, 3, 1, 0, 1), (4, 8, 1, 2, 1)]
     assert lib.attn_host_plan(4, 32, 8, 4096, 128, 1, None, 0, ctypes.byref(n)) == 0
-    assert n.value == 36
+    assert n.value == 14
     assert lib.attn_host_plan(4, 32, 8, 4096, 128, 1, None, 0, None) == 12   # NULL n_chunks
     assert lib.attn_host_plan(4, 32, 8, 4096, 128, 1, None, 2, ctypes.byref(n)) == 12
     assert lib.attn_host_plan(4, 32, 8, 4096, 128, 1, arr, -1, ctypes.byref(n)) == 12
