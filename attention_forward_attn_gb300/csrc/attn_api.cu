@@ -56,7 +56,7 @@ attn_status_t validate(const void* q, const void* k, const void* v, void* o, flo
   if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_DTYPE;
   if (q == nullptr || k == nullptr || v == nullptr || o == nullptr) return ATTN_ERR_NULL;
   if (B < 1 || Hq < 1 || Hkv < 1 || L < 1) return ATTN_ERR_SHAPE;
-  if (D != 64 && D != 128) return ATTN_ERR_HEADDIM;
+  if (D != 16 && D != 32 && D != 64 && D != 128) return ATTN_ERR_HEADDIM;
   if (Hq % Hkv != 0) return ATTN_ERR_HEADS;
   if (causal != 0 && causal != 1) return ATTN_ERR_ARG;
   if (!(sm_scale >= 0.f) || isinf(sm_scale)) return ATTN_ERR_SCALE;
@@ -361,7 +361,7 @@ const char* attn_strerror(attn_status_t status) {
     case ATTN_ERR_ALIGN: return "q/k/v/o must be 16-byte aligned, lse/valid_len 4-byte aligned";
     case ATTN_ERR_SHAPE: return "B, Hq, Hkv and L must be >= 1 and B*Hq*L must fit in int32";
     case ATTN_ERR_HEADS: return "Hq must be a multiple of Hkv";
-    case ATTN_ERR_HEADDIM: return "unsupported head dimension (64 or 128)";
+    case ATTN_ERR_HEADDIM: return "unsupported head dimension (16, 32, 64 or 128)";
     case ATTN_ERR_DTYPE: return "dtype must be ATTN_F16 or ATTN_BF16";
     case ATTN_ERR_SCALE: return "sm_scale must be finite and >= 0";
     case ATTN_ERR_ARCH: return "no sm_103 (GB300) device is current";

@@ -53,7 +53,7 @@ __device__ __forceinline__ float warp_sum(float x) {
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     attn_fwd_simt_kernel(Problem p, float scale_log2) {
-  constexpr int kPerLane = D / 32;
+  constexpr int kPerLane = (D + 31) / 32;  // accumulator columns lane + 32c (c < kPerLane, < D)
   __shared__ float q_sh[kWarpsPerBlock][D];
 
   const int warp = threadIdx.x >> 5;
@@ -108,15 +108,19 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
       const float wj = __shfl_sync(0xffffffffu, w, j);
       const int64_t v_row = (kv_head * p.L + kb + j) * D;
 #pragma unroll
-      for (int c = 0; c < kPerLane; ++c)
-        acc[c] = fmaf(wj, load_elem<BF16>(p.v, v_row + lane + 32 * c), acc[c]);
+      for (int c = 0; c < kPerLane; ++c) {
+        if (D % 32 == 0 || lane + 32 * c < D)
+          acc[c] = fmaf(wj, load_elem<BF16>(p.v, v_row + lane + 32 * c), acc[c]);
+      }
     }
     m = m_new;
   }
 
   const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
 #pragma unroll
-  for (int c = 0; c < kPerLane; ++c) store_elem<BF16>(p.o, q_row * D + lane + 32 * c, acc[c] * inv_l);
+  for (int c = 0; c < kPerLane; ++c) {
+    if (D % 32 == 0 || lane + 32 * c < D) store_elem<BF16>(p.o, q_row * D + lane + 32 * c, acc[c] * inv_l);
+  }
   if (p.lse != nullptr && lane == 0) {
     // natural log: ln(sum exp(s)) = ln2 * (m + log2 l) with m in log2 units
     p.lse[q_row] = (l > 0.f) ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
@@ -130,7 +134,13 @@ cudaError_t launch_simt(const Problem& p) {
   if (static_cast<int64_t>(p.B) * p.Hq > 65535) return cudaErrorInvalidConfiguration;
   dim3 grid((p.L + kWarpsPerBlock - 1) / kWarpsPerBlock, p.B * p.Hq);
   dim3 block(kWarpsPerBlock * 32);
-  if (p.D == 64) {
+  if (p.D == 16) {
+    if (p.bf16) attn_fwd_simt_kernel<16, true><<<grid, block, 0, p.stream>>>(p, scale_log2);
+    else attn_fwd_simt_kernel<16, false><<<grid, block, 0, p.stream>>>(p, scale_log2);
+  } else if (p.D == 32) {
+    if (p.bf16) attn_fwd_simt_kernel<32, true><<<grid, block, 0, p.stream>>>(p, scale_log2);
+    else attn_fwd_simt_kernel<32, false><<<grid, block, 0, p.stream>>>(p, scale_log2);
+  } else if (p.D == 64) {
     if (p.bf16) attn_fwd_simt_kernel<64, true><<<grid, block, 0, p.stream>>>(p, scale_log2);
     else attn_fwd_simt_kernel<64, false><<<grid, block, 0, p.stream>>>(p, scale_log2);
   } else if (p.D == 128) {

@@ -144,6 +144,7 @@ struct KParams {
   const int* vflags;
   int n_kt;     // 128-key tiles per (b, h_kv)
   int B, Hq, Hkv, L, G;
+  int d_o;      // elements per row of O in memory: the problem's D (<= the instance's D)
   int n_mb;     // 128-row query tiles per (b, h_q)
   int n_units;  // B * Hq * n_mb
   float scale_log2;
@@ -607,9 +608,12 @@ __device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t smem,
     const int n = w.n;
     if (n == 0) {  // no visible key: O = 0, LSE = -inf
       if (row_ok) {
-        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.o) + grow * D * 2);
+        // rows of O are d_o elements long (D = 16 and 32 run the D = 64 instance)
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.o) + grow * p.d_o * 2);
 #pragma unroll
-        for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
+        for (int c = 0; c < D / 8; ++c) {
+          if (c < p.d_o / 8) dst[c] = make_uint4(0u, 0u, 0u, 0u);
+        }
         if (p.lse != nullptr) p.lse[grow] = -INFINITY;
       }
       decode_ahead();
@@ -862,6 +866,7 @@ cudaError_t launch_instance(const Problem& pr, const CUtensorMap* maps, int num_
   kp.Hkv = pr.Hkv;
   kp.L = pr.L;
   kp.G = pr.Hq / pr.Hkv;
+  kp.d_o = pr.D;
   kp.n_mb = (pr.L + BM - 1) / BM;
   kp.n_units = pr.B * pr.Hq * kp.n_mb;
   // A zero scale is passed as the smallest normal float: every product
@@ -877,7 +882,7 @@ cudaError_t launch_instance(const Problem& pr, const CUtensorMap* maps, int num_
 }  // namespace
 
 bool tc_config(int D, TcConfig* out) {
-  if (D == 64) {
+  if (D == 16 || D == 32 || D == 64) {  // D < 64: the D = 64 kernel on zero-filled columns
     *out = {BM, 1, BN, Cfg<64>::kKStages + Cfg<64>::kVStages, kThreads, Cfg<64>::kSmemBytes,
             static_cast<int>(Cfg<64>::kTmemCols)};
     return true;
@@ -890,8 +895,12 @@ bool tc_config(int D, TcConfig* out) {
   return false;
 }
 
+// D = 16 and 32 run the D = 64 instance: their tensor maps have an inner
+// extent of D with 64-column boxes, so TMA fills columns D..63 of every Q, K
+// and V tile with zeros (Q.K^T and P.V unchanged; O's extra columns are 0)
+// and the O store writes only the D columns inside the tensor.
 cudaError_t launch_tc(const Problem& p, const CUtensorMap* maps, int num_sms) {
-  if (p.D == 64) {
+  if (p.D == 16 || p.D == 32 || p.D == 64) {
     return p.bf16 ? launch_instance<64, true>(p, maps, num_sms)
                   : launch_instance<64, false>(p, maps, num_sms);
   }

@@ -55,6 +55,7 @@ __global__ void __launch_bounds__(kThreadsV) v_to_f16_kernel(const uint16_t* __r
                                                              int n_kt) {
   constexpr int kVecPerRow = D / 8;                 // 16-byte vectors per row
   constexpr int kPer = kTileKeys * kVecPerRow / kThreadsV;
+  static_assert(kPer >= 1 && kPer * kThreadsV == kTileKeys * kVecPerRow, "tile / thread split");
   const int z = static_cast<int>(blockIdx.x) / n_kt;  // b*Hkv + h
   const int tile = static_cast<int>(blockIdx.x) % n_kt;
   const int r0 = tile * kTileKeys;
@@ -101,7 +102,13 @@ cudaError_t launch_vconv(const Problem& p, void* v16, int* flags) {
   if (blocks > INT32_MAX) return cudaErrorInvalidValue;
   const auto* v = static_cast<const uint16_t*>(p.v);
   auto* out = static_cast<uint16_t*>(v16);
-  if (p.D == 64) {
+  if (p.D == 16) {
+    v_to_f16_kernel<16><<<static_cast<unsigned>(blocks), kThreadsV, 0, p.stream>>>(
+        v, out, flags, p.L, static_cast<int>(n_kt));
+  } else if (p.D == 32) {
+    v_to_f16_kernel<32><<<static_cast<unsigned>(blocks), kThreadsV, 0, p.stream>>>(
+        v, out, flags, p.L, static_cast<int>(n_kt));
+  } else if (p.D == 64) {
     v_to_f16_kernel<64><<<static_cast<unsigned>(blocks), kThreadsV, 0, p.stream>>>(
         v, out, flags, p.L, static_cast<int>(n_kt));
   } else if (p.D == 128) {

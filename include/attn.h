@@ -73,7 +73,10 @@ typedef enum {
  *             lse[(b*Hq + h)*L + i] = log(sum_{j visible} exp(sm_scale * q_i . k_j)).
  *             NULL skips the store.
  *   B, Hq, Hkv, L   batch, query heads, key/value heads, sequence length (>= 1).
- *   D         head dimension: 64 or 128.
+ *   D         head dimension: 16, 32, 64 or 128 (the Triton-CUDA Attention
+ *             page's set).  D = 16 and 32 run the D = 64 kernel: its loads
+ *             fill columns D..63 with zeros (scores and O unchanged) and its
+ *             stores write only the D columns, so they cost as much as D = 64.
  *   sm_scale  score scale, finite and >= 0 (normally 1/sqrt(D)).
  *   causal    0 or 1.
  *   valid_len NULL (no padding mask) or a device array of B int32 values.
@@ -109,8 +112,8 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
  * attn_fwd_simt -- the same operation, same arguments and same contract as
  * attn_fwd, computed by a plain SIMT kernel (one warp per query row, fp32
  * FMA dot products, online softmax over 32-key blocks; no tensor cores).
- * It is a slow cross-check of attn_fwd, not the fast path.  D must be 64 or
- * 128.
+ * It is a slow cross-check of attn_fwd, not the fast path.  D is 16, 32, 64
+ * or 128.
  */
 attn_status_t attn_fwd_simt(const void* q, const void* k, const void* v, void* o, float* lse,
                             int B, int Hq, int Hkv, int L, int D, float sm_scale, int causal,

@@ -47,6 +47,9 @@ def _call(**kw):
     (dict(B=1 << 12, Hq=1 << 10, Hkv=1, L=1 << 10), "ATTN_ERR_SHAPE"),
     (dict(D=96), "ATTN_ERR_HEADDIM"),
     (dict(D=0), "ATTN_ERR_HEADDIM"),
+    (dict(D=8), "ATTN_ERR_HEADDIM"),
+    (dict(D=48), "ATTN_ERR_HEADDIM"),
+    (dict(D=256), "ATTN_ERR_HEADDIM"),
     (dict(Hq=3, Hkv=2), "ATTN_ERR_HEADS"),
     (dict(causal=2), "ATTN_ERR_ARG"),
     (dict(sm_scale=-1.0), "ATTN_ERR_SCALE"),
@@ -73,7 +76,8 @@ def test_valid_arguments_need_a_device(lib):
 
 
 def test_query_static_fields(lib):
-    for D, stages in ((64, 12), (128, 6)):
+    # D = 16 and 32 run the D = 64 kernel (zero-filled columns)
+    for D, stages in ((16, 12), (32, 12), (64, 12), (128, 6)):
         caps = attn.query(D, attn.ATTN_BF16)
         assert caps["block_m"] == 128 and caps["block_n"] == 128
         assert caps["q_tiles_per_cta"] == 1 and caps["kv_stages"] == stages

@@ -38,6 +38,8 @@ def _device_result(q, k, v, causal, vl):
     (3, 8, 8, 1000, 64, wl.F16, False, False),      # ragged key tile, whole-batch chunks
     (5, 4, 1, 1536, 128, wl.BF16, False, True),     # MQA
     (1, 2, 2, 130, 64, wl.F16, True, False),        # one small chunk
+    (4, 16, 4, 4096, 32, wl.BF16, True, True),      # D = 32 (runs the D = 64 kernel), 9 chunks
+    (2, 8, 2, 1000, 16, wl.F16, False, False),      # D = 16, one chunk
 ])
 def test_host_path_equals_device_path(B, Hq, Hkv, L, D, dtype, causal, padded):
     q, k, v, _ = wl.make_inputs(B, Hq, Hkv, L, D, dtype, seed=200 + L)

@@ -73,7 +73,7 @@ KERNELS = [pytest.param(False, id="tc"), pytest.param(True, id="simt")]
 
 
 @pytest.mark.parametrize("simt", KERNELS)
-@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("D", [16, 32, 64, 128])
 @pytest.mark.parametrize("dtype", [wl.F16, wl.BF16])
 @pytest.mark.parametrize("causal", [False, True])
 def test_small_shapes_full_compare(simt, D, dtype, causal):
@@ -90,7 +90,7 @@ def test_sequence_lengths(simt, L):
 
 @pytest.mark.parametrize("simt", KERNELS)
 @pytest.mark.parametrize("causal", [False, True])
-@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("D", [16, 32, 64, 128])
 def test_padding_masks(simt, causal, D):
     # 0 (fully masked rows), 1, tile edges, L
     full_case(6, 2, 2, 300, D, wl.BF16, causal, seed=7, valid_len=[0, 1, 127, 128, 129, 300],
@@ -215,7 +215,7 @@ def test_workload_tc_matches_simt_everywhere(name):
     assert np.abs(l1[~neg] - l2[~neg]).max() <= 2 * LSE_ATOL
 
 
-@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("D", [32, 64, 128])
 @pytest.mark.parametrize("causal", [False, True])
 def test_bf16_v_tiles_beyond_fp16_range(D, causal):
     """bf16 V tiles holding |v| >= 65536 keep bf16 (split P) while the other

@@ -51,6 +51,8 @@ def _close(o, lse, o_ref, lse_ref):
 @pytest.mark.parametrize("B, Hq, Hkv, L, D, dtype, causal, valid_len", [
     (2, 4, 2, 700, 128, wl.BF16, True, [700, 333]),
     (2, 2, 2, 300, 64, wl.F16, False, [0, 300]),
+    (1, 4, 1, 333, 32, wl.BF16, True, [333]),
+    (2, 2, 1, 140, 16, wl.F16, False, [140, 3]),
 ])
 def test_noalloc_matches_attn_fwd_twice(B, Hq, Hkv, L, D, dtype, causal, valid_len):
     dev = torch.device("cuda")
