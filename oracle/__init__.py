@@ -53,10 +53,10 @@ def _bind(path: str):
     p = ctypes.c_void_p
     i = ctypes.c_int
     i64 = ctypes.c_int64
-    lib.oracle_attn_fwd_f64.argtypes = [p, p, p, p, p, i, i, i, i, i, ctypes.c_double,
+    lib.oracle_attn_fwd_f64.argtypes = [p, p, p, p, p, i, i, i, i, i, i, ctypes.c_double,
                                         i, p, p, i64, i]
     lib.oracle_attn_fwd_f64.restype = i
-    lib.oracle_attn_fwd_u16.argtypes = [p, p, p, p, p, i, i, i, i, i, ctypes.c_double,
+    lib.oracle_attn_fwd_u16.argtypes = [p, p, p, p, p, i, i, i, i, i, i, ctypes.c_double,
                                         i, p, i, p, i64, i]
     lib.oracle_attn_fwd_u16.restype = i
     lib.oracle_decode.argtypes = [p, p, i64, i]
@@ -97,10 +97,10 @@ def decode(bits: np.ndarray, dtype: int) -> np.ndarray:
 def _shapes(q, k, v):
     if q.ndim != 4 or k.ndim != 4 or v.ndim != 4:
         raise ValueError("q, k, v must be [B, H, L, D]")
-    B, Hq, L, D = q.shape
-    if k.shape != v.shape or k.shape[0] != B or k.shape[2] != L or k.shape[3] != D:
-        raise ValueError("k, v must be [B, Hkv, L, D] matching q")
-    return B, Hq, k.shape[1], L, D
+    B, Hq, Lq, D = q.shape
+    if k.shape != v.shape or k.shape[0] != B or k.shape[3] != D:
+        raise ValueError("k, v must be [B, Hkv, Lk, D] matching q's B and D")
+    return B, Hq, k.shape[1], Lq, k.shape[2], D
 
 
 def _valid(valid_len, B):
@@ -123,28 +123,29 @@ def attn_fwd_f64(q, k, v, sm_scale, causal=False, valid_len=None, rows=None, thr
                  _lib_override=None):
     """Oracle on float64 inputs.
 
-    q: [B, Hq, L, D]; k, v: [B, Hkv, L, D].  Returns (o, lse): o is
-    [B, Hq, L, D] and lse [B*Hq, L] when ``rows`` is None, else o is
-    [len(rows), D] and lse [len(rows)] for the flat row indices
-    r = (b*Hq + h_q)*L + i.
+    q: [B, Hq, Lq, D]; k, v: [B, Hkv, Lk, D] (Lq = Lk is the pages' case; the
+    causal mask compares absolute positions, key j visible to query i iff
+    j <= i).  Returns (o, lse): o is [B, Hq, Lq, D] and lse [B*Hq, Lq] when
+    ``rows`` is None, else o is [len(rows), D] and lse [len(rows)] for the
+    flat row indices r = (b*Hq + h_q)*Lq + i.
     """
     q = np.ascontiguousarray(q, dtype=np.float64)
     k = np.ascontiguousarray(k, dtype=np.float64)
     v = np.ascontiguousarray(v, dtype=np.float64)
-    B, Hq, Hkv, L, D = _shapes(q, k, v)
+    B, Hq, Hkv, Lq, Lk, D = _shapes(q, k, v)
     vl = _valid(valid_len, B)
     r, nr = _rows(rows)
-    n_out = nr if r is not None else B * Hq * L
+    n_out = nr if r is not None else B * Hq * Lq
     o = np.empty((n_out, D), dtype=np.float64)
     lse = np.empty((n_out,), dtype=np.float64)
     lib = _lib_override if _lib_override is not None else _load()
     rc = lib.oracle_attn_fwd_f64(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv,
-                                 L, D, float(sm_scale), int(bool(causal)), _ptr(vl), _ptr(r),
-                                 nr, int(threads))
+                                 Lq, Lk, D, float(sm_scale), int(bool(causal)), _ptr(vl),
+                                 _ptr(r), nr, int(threads))
     if rc != 0:
         raise ValueError("oracle_attn_fwd_f64 failed with code %d" % rc)
     if r is None:
-        return o.reshape(B, Hq, L, D), lse.reshape(B * Hq, L)
+        return o.reshape(B, Hq, Lq, D), lse.reshape(B * Hq, Lq)
     return o, lse
 
 
@@ -157,19 +158,19 @@ def attn_fwd_bits(q_bits, k_bits, v_bits, dtype, sm_scale, causal=False, valid_l
     q = np.ascontiguousarray(q_bits, dtype=np.uint16)
     k = np.ascontiguousarray(k_bits, dtype=np.uint16)
     v = np.ascontiguousarray(v_bits, dtype=np.uint16)
-    B, Hq, Hkv, L, D = _shapes(q, k, v)
+    B, Hq, Hkv, Lq, Lk, D = _shapes(q, k, v)
     vl = _valid(valid_len, B)
     r, nr = _rows(rows)
-    n_out = nr if r is not None else B * Hq * L
+    n_out = nr if r is not None else B * Hq * Lq
     o = np.empty((n_out, D), dtype=np.float64)
     lse = np.empty((n_out,), dtype=np.float64)
     rc = _load().oracle_attn_fwd_u16(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv,
-                                     L, D, float(sm_scale), int(bool(causal)), _ptr(vl),
+                                     Lq, Lk, D, float(sm_scale), int(bool(causal)), _ptr(vl),
                                      int(dtype), _ptr(r), nr, int(threads))
     if rc != 0:
         raise ValueError("oracle_attn_fwd_u16 failed with code %d" % rc)
     if r is None:
-        return o.reshape(B, Hq, L, D), lse.reshape(B * Hq, L)
+        return o.reshape(B, Hq, Lq, D), lse.reshape(B * Hq, Lq)
     return o, lse
 
 

@@ -28,6 +28,12 @@
  * Head grouping (Triton-CUDA Attention page, "GQA"): h_kv = h_q // (Hq/Hkv),
  * integer division, never modulo.
  *
+ * Query and key lengths: the pages use one sequence length for Q, K and V.
+ * Here Q has Lq rows and K/V have Lk rows (Lq = Lk is the pages' case); the
+ * masks keep the pages' comparisons on absolute positions, so the causal
+ * mask stays top-left aligned (key j visible to query i iff j <= i) and the
+ * padding mask still removes key j >= valid_len[b].
+ *
  * Log-sum-exp: the natural-log LSE of the scaled scores,
  *   LSE[i] = log sum_{j in J} exp(sm_scale * q_i . k_j),
  * which is tiny_flash_attn_triton.py's stored m + log2(l) (base 2, in the
@@ -82,16 +88,16 @@ static int key_visible(int64_t i, int64_t j, int b, int causal, const int32_t* v
 }
 
 /*
- * One query row, three passes.  q_row: D values; k_head, v_head: L x D rows
- * of the mapped key/value head; s: scratch of L doubles.
+ * One query row, three passes.  q_row: D values; k_head, v_head: Lk x D rows
+ * of the mapped key/value head; s: scratch of Lk doubles.
  */
 static void one_row(const double* q_row, const double* k_head, const double* v_head,
-                    int64_t i, int b, int L, int D, double sm_scale, int causal,
+                    int64_t i, int b, int Lk, int D, double sm_scale, int causal,
                     const int32_t* valid_len, double* s, double* o_row, double* lse_out) {
   /* pass 1: scores of the visible keys and their maximum */
   double m = -INFINITY;
   int64_t n_visible = 0;
-  for (int64_t j = 0; j < L; ++j) {
+  for (int64_t j = 0; j < Lk; ++j) {
     if (!key_visible(i, j, b, causal, valid_len)) continue;
     const double* k_row = k_head + j * (int64_t)D;
     double dot = 0.0;
@@ -107,14 +113,14 @@ static void one_row(const double* q_row, const double* k_head, const double* v_h
   }
   /* pass 2: the normaliser l = sum_j exp(s_j - m); s_j is replaced by its weight */
   double l = 0.0;
-  for (int64_t j = 0; j < L; ++j) {
+  for (int64_t j = 0; j < Lk; ++j) {
     if (!key_visible(i, j, b, causal, valid_len)) continue;
     s[j] = exp(s[j] - m);
     l += s[j];
   }
   /* pass 3: O = sum_j w_j v_j / l */
   for (int d = 0; d < D; ++d) o_row[d] = 0.0;
-  for (int64_t j = 0; j < L; ++j) {
+  for (int64_t j = 0; j < Lk; ++j) {
     if (!key_visible(i, j, b, causal, valid_len)) continue;
     const double* v_row = v_head + j * (int64_t)D;
     for (int d = 0; d < D; ++d) o_row[d] += s[j] * v_row[d];
@@ -124,20 +130,20 @@ static void one_row(const double* q_row, const double* k_head, const double* v_h
 }
 
 /*
- * q: [B, Hq, L, D]; k, v: [B, Hkv, L, D] (contiguous, float64).
- * rows == NULL: every row r = (b*Hq + h_q)*L + i, written to o[r*D..], lse[r].
+ * q: [B, Hq, Lq, D]; k, v: [B, Hkv, Lk, D] (contiguous, float64).
+ * rows == NULL: every row r = (b*Hq + h_q)*Lq + i, written to o[r*D..], lse[r].
  * rows != NULL: row rows[n] written to o[n*D..], lse[n], for n < nrows.
  * valid_len: NULL (no padding mask) or B int32 values.
  * threads <= 0: OpenMP default.
  * Returns 0, or 1 on invalid arguments.
  */
 int oracle_attn_fwd_f64(const double* q, const double* k, const double* v, double* o,
-                        double* lse, int B, int Hq, int Hkv, int L, int D, double sm_scale,
-                        int causal, const int32_t* valid_len, const int64_t* rows,
-                        int64_t nrows, int threads) {
-  if (B < 1 || Hq < 1 || Hkv < 1 || L < 1 || D < 1 || Hq % Hkv != 0) return 1;
+                        double* lse, int B, int Hq, int Hkv, int Lq, int Lk, int D,
+                        double sm_scale, int causal, const int32_t* valid_len,
+                        const int64_t* rows, int64_t nrows, int threads) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Lq < 1 || Lk < 1 || D < 1 || Hq % Hkv != 0) return 1;
   const int G = Hq / Hkv;
-  const int64_t total = (int64_t)B * Hq * L;
+  const int64_t total = (int64_t)B * Hq * Lq;
   const int64_t n_out = rows ? nrows : total;
   if (rows)
     for (int64_t n = 0; n < nrows; ++n)
@@ -150,7 +156,7 @@ int oracle_attn_fwd_f64(const double* q, const double* k, const double* v, doubl
   int bad = 0;
 #pragma omp parallel
   {
-    double* s = (double*)malloc(sizeof(double) * (size_t)L);
+    double* s = (double*)malloc(sizeof(double) * (size_t)Lk);
     if (!s) {
 #pragma omp atomic write
       bad = 1;
@@ -159,15 +165,15 @@ int oracle_attn_fwd_f64(const double* q, const double* k, const double* v, doubl
     for (int64_t n = 0; n < n_out; ++n) {
       if (!s) continue;
       const int64_t r = rows ? rows[n] : n;
-      const int64_t bh = r / L;
-      const int64_t i = r % L;
+      const int64_t bh = r / Lq;
+      const int64_t i = r % Lq;
       const int b = (int)(bh / Hq);
       const int h_q = (int)(bh % Hq);
       const int h_kv = h_q / G; /* integer division, never modulo */
       const double* q_row = q + r * (int64_t)D;
-      const double* k_head = k + ((int64_t)b * Hkv + h_kv) * L * (int64_t)D;
-      const double* v_head = v + ((int64_t)b * Hkv + h_kv) * L * (int64_t)D;
-      one_row(q_row, k_head, v_head, i, b, L, D, sm_scale, causal, valid_len, s,
+      const double* k_head = k + ((int64_t)b * Hkv + h_kv) * Lk * (int64_t)D;
+      const double* v_head = v + ((int64_t)b * Hkv + h_kv) * Lk * (int64_t)D;
+      one_row(q_row, k_head, v_head, i, b, Lk, D, sm_scale, causal, valid_len, s,
               o + n * (int64_t)D, lse + n);
     }
     free(s);
@@ -177,13 +183,13 @@ int oracle_attn_fwd_f64(const double* q, const double* k, const double* v, doubl
 
 /* Same as oracle_attn_fwd_f64, on raw fp16 (dtype 0) or bf16 (dtype 1) bits. */
 int oracle_attn_fwd_u16(const uint16_t* q, const uint16_t* k, const uint16_t* v, double* o,
-                        double* lse, int B, int Hq, int Hkv, int L, int D, double sm_scale,
-                        int causal, const int32_t* valid_len, int dtype, const int64_t* rows,
-                        int64_t nrows, int threads) {
-  if (B < 1 || Hq < 1 || Hkv < 1 || L < 1 || D < 1 || Hq % Hkv != 0) return 1;
+                        double* lse, int B, int Hq, int Hkv, int Lq, int Lk, int D,
+                        double sm_scale, int causal, const int32_t* valid_len, int dtype,
+                        const int64_t* rows, int64_t nrows, int threads) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Lq < 1 || Lk < 1 || D < 1 || Hq % Hkv != 0) return 1;
   if (dtype != 0 && dtype != 1) return 1;
-  const int64_t nq = (int64_t)B * Hq * L * D;
-  const int64_t nkv = (int64_t)B * Hkv * L * D;
+  const int64_t nq = (int64_t)B * Hq * Lq * D;
+  const int64_t nkv = (int64_t)B * Hkv * Lk * D;
   double* qd = (double*)malloc(sizeof(double) * (size_t)nq);
   double* kd = (double*)malloc(sizeof(double) * (size_t)nkv);
   double* vd = (double*)malloc(sizeof(double) * (size_t)nkv);
@@ -192,8 +198,8 @@ int oracle_attn_fwd_u16(const uint16_t* q, const uint16_t* k, const uint16_t* v,
     oracle_decode(q, qd, nq, dtype);
     oracle_decode(k, kd, nkv, dtype);
     oracle_decode(v, vd, nkv, dtype);
-    rc = oracle_attn_fwd_f64(qd, kd, vd, o, lse, B, Hq, Hkv, L, D, sm_scale, causal, valid_len,
-                             rows, nrows, threads);
+    rc = oracle_attn_fwd_f64(qd, kd, vd, o, lse, B, Hq, Hkv, Lq, Lk, D, sm_scale, causal,
+                             valid_len, rows, nrows, threads);
   }
   free(qd);
   free(kd);

@@ -42,23 +42,23 @@ def brute_force(q, k, v, sm_scale, causal, valid_len):
     mpmath = pytest.importorskip("mpmath")
     mp = mpmath.mp
     mp.dps = 50
-    B, Hq, L, D = q.shape
-    Hkv = k.shape[1]
+    B, Hq, Lq, D = q.shape
+    Hkv, Lk = k.shape[1], k.shape[2]
     G = Hq // Hkv
     head_of = [g for g in range(Hkv) for _ in range(G)]  # repetition, as repeat_interleave
-    O = np.zeros((B, Hq, L, D))
-    LSE = np.zeros((B * Hq, L))
+    O = np.zeros((B, Hq, Lq, D))
+    LSE = np.zeros((B * Hq, Lq))
     for b in range(B):
         for h in range(Hq):
             g = head_of[h]
-            for i in range(L):
+            for i in range(Lq):
                 keep = [(not causal or i >= j) and (valid_len is None or j < valid_len[b])
-                        for j in range(L)]
+                        for j in range(Lk)]
                 if not any(keep):
                     LSE[b * Hq + h, i] = -math.inf
                     continue
                 w = {}
-                for j in range(L):
+                for j in range(Lk):
                     if keep[j]:
                         s = mp.mpf(sm_scale) * mp.fsum(mp.mpf(q[b, h, i, d]) * mp.mpf(k[b, g, j, d])
                                                        for d in range(D))
@@ -70,12 +70,13 @@ def brute_force(q, k, v, sm_scale, causal, valid_len):
     return O, LSE
 
 
-def explicit_mask(B, L, causal, valid_len):
-    m = torch.ones(B, 1, L, L, dtype=torch.bool)
+def explicit_mask(B, Lq, Lk, causal, valid_len):
+    m = torch.ones(B, 1, Lq, Lk, dtype=torch.bool)
     if causal:
-        m &= torch.tril(torch.ones(L, L, dtype=torch.bool))
+        # torch.tril keeps column j <= row i of the [Lq, Lk] matrix: top-left
+        m &= torch.tril(torch.ones(Lq, Lk, dtype=torch.bool))
     if valid_len is not None:
-        keys = torch.arange(L)
+        keys = torch.arange(Lk)
         for b in range(B):
             m[b, :, :, :] &= (keys < int(valid_len[b]))[None, :]
     return m
@@ -83,17 +84,18 @@ def explicit_mask(B, L, causal, valid_len):
 
 def torch_reference(q, k, v, sm_scale, causal, valid_len):
     qt, kt, vt = (torch.from_numpy(np.ascontiguousarray(x)) for x in (q, k, v))
-    B, Hq, L, D = qt.shape
+    B, Hq, Lq, D = qt.shape
+    Lk = kt.shape[2]
     G = Hq // kt.shape[1]
     kt = kt.repeat_interleave(G, dim=1)
     vt = vt.repeat_interleave(G, dim=1)
-    mask = explicit_mask(B, L, causal, valid_len)
+    mask = explicit_mask(B, Lq, Lk, causal, valid_len)
     o = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=mask,
                                                          scale=sm_scale)
     scores = (qt @ kt.transpose(-1, -2)) * sm_scale
     lse = torch.logsumexp(scores.masked_fill(~mask, -math.inf), dim=-1)
-    empty = ~mask.any(dim=-1).expand(B, Hq, L)
-    return o.numpy(), lse.reshape(B * Hq, L).numpy(), empty.numpy()
+    empty = ~mask.any(dim=-1).expand(B, Hq, Lq)
+    return o.numpy(), lse.reshape(B * Hq, Lq).numpy(), empty.numpy()
 
 
 def rand(shape, rng, scale=1.0):
@@ -115,10 +117,18 @@ def pin_brute_force(fwd):
         (1, 4, 1, 6, 7, False, [5]),
         (2, 2, 1, 8, 8, True, [7, 2]),
     ]
+    # query length != key length (Lq, Lk)
+    cases += [
+        (1, 2, 1, (3, 7), 4, True, None),
+        (2, 2, 2, (7, 3), 3, True, [3, 2]),
+        (2, 4, 2, (5, 8), 5, False, [6, 0]),
+        (1, 3, 3, (8, 2), 2, False, None),
+    ]
     for (B, Hq, Hkv, L, D, causal, vl) in cases:
-        q = rand((B, Hq, L, D), rng, 1.5)
-        k = rand((B, Hkv, L, D), rng)
-        v = rand((B, Hkv, L, D), rng)
+        Lq, Lk = L if isinstance(L, tuple) else (L, L)
+        q = rand((B, Hq, Lq, D), rng, 1.5)
+        k = rand((B, Hkv, Lk, D), rng)
+        v = rand((B, Hkv, Lk, D), rng)
         sm = 1.0 / math.sqrt(D) * 1.7
         o, lse = fwd(q, k, v, sm, causal=causal, valid_len=vl)
         o_ref, lse_ref = brute_force(q, k, v, sm, causal, vl)
@@ -134,20 +144,24 @@ def pin_torch_sdpa(fwd):
         (3, 4, 4, 41, 16, False, [41, 0, 17]),
         (2, 8, 1, 50, 32, True, [50, 23]),
         (1, 4, 2, 64, 64, True, [60]),
+        (2, 4, 2, (29, 53), 16, True, [53, 11]),
+        (2, 4, 4, (61, 22), 32, True, None),
+        (1, 8, 2, (40, 70), 24, False, [66]),
     ]
     for (B, Hq, Hkv, L, D, causal, vl) in cases:
-        q = rand((B, Hq, L, D), rng, 2.0)
-        k = rand((B, Hkv, L, D), rng)
-        v = rand((B, Hkv, L, D), rng)
+        Lq, Lk = L if isinstance(L, tuple) else (L, L)
+        q = rand((B, Hq, Lq, D), rng, 2.0)
+        k = rand((B, Hkv, Lk, D), rng)
+        v = rand((B, Hkv, Lk, D), rng)
         sm = 1.0 / math.sqrt(D)
         o, lse = fwd(q, k, v, sm, causal=causal, valid_len=vl)
         o_ref, lse_ref, empty = torch_reference(q, k, v, sm, causal, vl)
         keep = ~empty
         np.testing.assert_allclose(o[keep], o_ref[keep], rtol=1e-11, atol=1e-12)
-        np.testing.assert_allclose(lse.reshape(B, Hq, L)[keep], lse_ref.reshape(B, Hq, L)[keep],
-                                   rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(lse.reshape(B, Hq, Lq)[keep],
+                                   lse_ref.reshape(B, Hq, Lq)[keep], rtol=1e-12, atol=1e-12)
         assert np.all(o[empty] == 0.0)
-        assert np.all(np.isneginf(lse.reshape(B, Hq, L)[empty]))
+        assert np.all(np.isneginf(lse.reshape(B, Hq, Lq)[empty]))
 
 
 def pin_golden(fwd):
@@ -256,7 +270,55 @@ def pin_closed_forms(fwd):
     np.testing.assert_array_equal(o_q, o_r)
 
 
-PINS = [pin_brute_force, pin_torch_sdpa, pin_golden, pin_invariants, pin_closed_forms]
+def pin_lengths(fwd):
+    """Query length Lq != key length Lk: relations to square problems."""
+    rng = np.random.default_rng(7)
+    B, Hq, Hkv, D = 2, 4, 2, 6
+    # one key: every query row gets V[0]; LSE is that key's scaled score
+    q, k, v = rand((B, Hq, 5, D), rng), rand((B, Hkv, 1, D), rng), rand((B, Hkv, 1, D), rng)
+    for causal in (False, True):
+        o, lse = fwd(q, k, v, 0.3, causal=causal)
+        np.testing.assert_allclose(o, np.broadcast_to(np.repeat(v, 2, axis=1), o.shape),
+                                   rtol=1e-14, atol=0)
+        s = 0.3 * np.einsum("bhid,bhd->bhi", q, np.repeat(k[:, :, 0], 2, axis=1))
+        np.testing.assert_allclose(lse, s.reshape(B * Hq, 5), rtol=1e-13, atol=1e-15)
+    # causal, Lk > Lq: keys at positions >= Lq are never visible (top-left
+    # alignment), so the result equals the square problem on the first Lq keys
+    q = rand((B, Hq, 6, D), rng)
+    k, v = rand((B, Hkv, 11, D), rng), rand((B, Hkv, 11, D), rng)
+    for vl in (None, [11, 4]):
+        o, lse = fwd(q, k, v, 0.45, causal=True, valid_len=vl)
+        vl_sq = None if vl is None else [min(x, 6) for x in vl]
+        o_sq, lse_sq = fwd(q, k[:, :, :6], v[:, :, :6], 0.45, causal=True, valid_len=vl_sq)
+        np.testing.assert_array_equal(o, o_sq)
+        np.testing.assert_array_equal(lse, lse_sq)
+    # causal, Lq > Lk: rows i < Lk are the square problem; rows i >= Lk - 1
+    # see every key, as without the causal mask
+    q = rand((B, Hq, 10, D), rng)
+    k, v = rand((B, Hkv, 4, D), rng), rand((B, Hkv, 4, D), rng)
+    o, lse = fwd(q, k, v, 0.45, causal=True)
+    o_sq, lse_sq = fwd(q[:, :, :4], k, v, 0.45, causal=True)
+    np.testing.assert_array_equal(o[:, :, :4], o_sq)
+    np.testing.assert_array_equal(lse.reshape(B, Hq, 10)[:, :, :4], lse_sq.reshape(B, Hq, 4))
+    o_nc, lse_nc = fwd(q, k, v, 0.45, causal=False)
+    np.testing.assert_array_equal(o[:, :, 3:], o_nc[:, :, 3:])
+    np.testing.assert_array_equal(lse.reshape(B, Hq, 10)[:, :, 3:],
+                                  lse_nc.reshape(B, Hq, 10)[:, :, 3:])
+    # without the causal mask query rows are independent: the rows of a split
+    # query block equal the whole block's rows
+    q = rand((B, Hq, 9, D), rng)
+    k, v = rand((B, Hkv, 13, D), rng), rand((B, Hkv, 13, D), rng)
+    o, lse = fwd(q, k, v, 0.5, valid_len=[13, 6])
+    o_a, lse_a = fwd(q[:, :, :4], k, v, 0.5, valid_len=[13, 6])
+    o_b, lse_b = fwd(q[:, :, 4:], k, v, 0.5, valid_len=[13, 6])
+    np.testing.assert_array_equal(o, np.concatenate([o_a, o_b], axis=2))
+    np.testing.assert_array_equal(lse.reshape(B, Hq, 9),
+                                  np.concatenate([lse_a.reshape(B, Hq, 4),
+                                                  lse_b.reshape(B, Hq, 5)], axis=2))
+
+
+PINS = [pin_brute_force, pin_torch_sdpa, pin_golden, pin_invariants, pin_closed_forms,
+        pin_lengths]
 
 
 # ---------------------------------------------------------------- the tests
@@ -326,7 +388,10 @@ MUTANTS = {
     "causal_inverted": ("if (causal && j > i) return 0;", "if (causal && j < i) return 0;"),
     "padding_off_by_one": ("j >= (int64_t)valid_len[b]", "j > (int64_t)valid_len[b]"),
     "modulo_head_map": ("const int h_kv = h_q / G;", "const int h_kv = h_q % Hkv;"),
-    "transposed_k": ("dot += q_row[d] * k_row[d];", "dot += q_row[d] * k_head[d * (int64_t)L + j];"),
+    "transposed_k": ("dot += q_row[d] * k_row[d];", "dot += q_row[d] * k_head[d * (int64_t)Lk + j];"),
+    "key_head_stride_from_query_length": ("* Lk * (int64_t)D;", "* Lq * (int64_t)D;"),
+    "row_split_by_key_length": ("const int64_t i = r % Lq;", "const int64_t i = r % Lk;"),
+    "padding_on_query_index": ("j >= (int64_t)valid_len[b]", "i >= (int64_t)valid_len[b]"),
     "log2_lse": ("*lse_out = m + log(l);", "*lse_out = m + log2(l);"),
     "lse_without_max": ("*lse_out = m + log(l);", "*lse_out = log(l);"),
     "no_normalisation": ("for (int d = 0; d < D; ++d) o_row[d] /= l;", ""),
