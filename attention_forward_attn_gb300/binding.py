@@ -20,7 +20,7 @@ STATUS_NAMES = {
     0: "ATTN_OK", 1: "ATTN_ERR_NULL", 2: "ATTN_ERR_ALIGN", 3: "ATTN_ERR_SHAPE",
     4: "ATTN_ERR_HEADS", 5: "ATTN_ERR_HEADDIM", 6: "ATTN_ERR_DTYPE", 7: "ATTN_ERR_SCALE",
     8: "ATTN_ERR_ARCH", 9: "ATTN_ERR_CUDA", 10: "ATTN_ERR_TIMEOUT", 11: "ATTN_ERR_VALID_LEN",
-    12: "ATTN_ERR_ARG", 13: "ATTN_ERR_SCRATCH",
+    12: "ATTN_ERR_ARG", 13: "ATTN_ERR_SCRATCH", 14: "ATTN_ERR_STRIDE",
 }
 ATTN_OK = 0
 
@@ -44,6 +44,11 @@ class Caps(ctypes.Structure):
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}
+
+
+class Strides(ctypes.Structure):
+    """attn_strides_t: element strides of batch, head and sequence position."""
+    _fields_ = [("batch", ctypes.c_int64), ("head", ctypes.c_int64), ("seq", ctypes.c_int64)]
 
 
 class Chunk(ctypes.Structure):
@@ -82,6 +87,10 @@ def load():
                 fn = getattr(lib, name)
                 fn.argtypes = fwd_args
                 fn.restype = i
+            sp = ctypes.POINTER(Strides)
+            lib.attn_fwd_strided.argtypes = [p, sp, p, sp, p, sp, p, sp, p, i, i, i, i, i, i,
+                                             ctypes.c_float, i, p, i, p]
+            lib.attn_fwd_strided.restype = i
             lib.attn_host_plan.argtypes = [i, i, i, i, i, i, ctypes.POINTER(Chunk), i,
                                            ctypes.POINTER(ctypes.c_int)]
             lib.attn_host_plan.restype = i
@@ -127,6 +136,25 @@ def fwd_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, Hq, Hkv, L, D, sm_scale, cau
         fn = load().attn_fwd_simt if simt else load().attn_fwd
     return int(fn(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, int(B), int(Hq), int(Hkv), int(L), int(D),
                   float(sm_scale), int(causal), valid_len_ptr, int(dtype), stream))
+
+
+def _strides_arg(st):
+    if st is None:
+        return None
+    return ctypes.byref(Strides(int(st[0]), int(st[1]), int(st[2])))
+
+
+def fwd_strided_raw(q_ptr, q_strides, k_ptr, k_strides, v_ptr, v_strides, o_ptr, o_strides,
+                    lse_ptr, B, Hq, Hkv, Lq, Lk, D, sm_scale, causal, valid_len_ptr, dtype,
+                    stream) -> int:
+    """Call attn_fwd_strided with raw integer pointers; each *_strides is a
+    (batch, head, seq) element-stride triple or None (contiguous).  Returns
+    the status."""
+    return int(load().attn_fwd_strided(
+        q_ptr, _strides_arg(q_strides), k_ptr, _strides_arg(k_strides), v_ptr,
+        _strides_arg(v_strides), o_ptr, _strides_arg(o_strides), lse_ptr, int(B), int(Hq),
+        int(Hkv), int(Lq), int(Lk), int(D), float(sm_scale), int(causal), valid_len_ptr,
+        int(dtype), stream))
 
 
 def status(stream=None):
@@ -282,4 +310,50 @@ def attn_fwd_host(q, k, v, *, causal=False, sm_scale=None, valid_len=None, out=N
         st, code = status(stream)
         if st != ATTN_OK:
             raise AttnError(st, "attn_fwd_host (device status %#x)" % code)
+    return out, (lse if return_lse else None)
+
+
+def attn_fwd_strided(q, k, v, *, causal=False, sm_scale=None, valid_len=None, out=None, lse=None,
+                     return_lse=True, stream=None):
+    """Fused attention forward on strided CUDA tensors through attn_fwd_strided.
+
+    q: [B, Hq, Lq, D]; k, v: [B, Hkv, Lk, D] -- any views whose last
+    dimension is contiguous and whose other strides are multiples of 8
+    elements, e.g. ``x.transpose(1, 2)`` of a [B, L, H, D] tensor or slices of
+    a packed QKV tensor; no copy is made.  Lq may differ from Lk (the causal
+    mask keeps key j <= query i).  out: optional [B, Hq, Lq, D] view to write
+    (default: ``torch.empty_like(q)``).  Returns (o, lse) with lse float32
+    [B*Hq, Lq].
+    """
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not t.is_cuda or t.dim() != 4 or (t.shape[3] > 1 and t.stride(3) != 1):
+            raise ValueError("%s must be a 4-D CUDA tensor with a contiguous last dimension"
+                             % name)
+    B, Hq, Lq, D = q.shape
+    Hkv, Lk = k.shape[1], k.shape[2]
+    if k.shape != v.shape or k.shape[0] != B or k.shape[3] != D:
+        raise ValueError("k and v must be [B, Hkv, Lk, D] matching q's B and D")
+    if q.dtype != k.dtype or q.dtype != v.dtype:
+        raise TypeError("q, k and v must share one dtype")
+    if sm_scale is None:
+        sm_scale = 1.0 / float(D) ** 0.5
+    if out is None:
+        out = torch.empty_like(q)
+    elif (not out.is_cuda or out.shape != q.shape or out.dtype != q.dtype
+          or (D > 1 and out.stride(3) != 1)):
+        raise ValueError("out must be a CUDA tensor like q with a contiguous last dimension")
+    if return_lse and lse is None:
+        lse = torch.empty((B * Hq, Lq), dtype=torch.float32, device=q.device)
+    vl_ptr = None
+    if valid_len is not None:
+        if valid_len.dtype != torch.int32 or not valid_len.is_cuda or valid_len.numel() != B:
+            raise ValueError("valid_len must be an int32 CUDA tensor of B elements")
+        vl_ptr = valid_len.data_ptr()
+    st = fwd_strided_raw(q.data_ptr(), q.stride()[:3], k.data_ptr(), k.stride()[:3], v.data_ptr(),
+                         v.stride()[:3], out.data_ptr(), out.stride()[:3],
+                         lse.data_ptr() if return_lse else None, B, Hq, Hkv, Lq, Lk, D, sm_scale,
+                         int(bool(causal)), vl_ptr, _dtype_code(q), _stream_handle(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fwd_strided")
     return out, (lse if return_lse else None)

@@ -179,22 +179,43 @@ attn_status_t device_pool(int dev, cudaMemPool_t* out) {
   return workspace_pool(dev, &g_dev[dev], out);
 }
 
-// Tensor map over a contiguous [heads, L, D] 16-bit tensor viewed as 3-D
-// (D innermost), boxes of 64 columns x `rows` rows x 1 head, 128-byte swizzle.
-attn_status_t encode_map(CUtensorMap* map, const void* base, int heads, int L, int D, int rows,
-                         bool bf16) {
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(L),
-                        static_cast<cuuint64_t>(heads)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
-                           static_cast<cuuint64_t>(L) * static_cast<cuuint64_t>(D) * 2};
-  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(rows), 1};
-  cuuint32_t estride[3] = {1, 1, 1};
+// Tensor map over a [B, H, L, D] 16-bit operand with element strides st,
+// viewed as 4-D (D innermost, then L, H, B), boxes of 64 columns x `rows`
+// rows x 1 head x 1 batch, 128-byte swizzle.  Strides are validated by the
+// entry points (positive multiples of 8 elements where the extent is > 1);
+// the stride of an extent-1 dimension is never used and is replaced by a
+// valid one.
+attn_status_t encode_map(CUtensorMap* map, const void* base, int B, int H, int L, int D,
+                         const Strides& st, int rows, bool bf16) {
+  const Strides c = contiguous_strides(H, L, D);
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(L),
+                        static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(L > 1 ? st.l : c.l) * 2,
+                           static_cast<cuuint64_t>(H > 1 ? st.h : c.h) * 2,
+                           static_cast<cuuint64_t>(B > 1 ? st.b : c.b) * 2};
+  cuuint32_t box[4] = {64, static_cast<cuuint32_t>(rows), 1, 1};
+  cuuint32_t estride[4] = {1, 1, 1, 1};
   CUresult r = g_encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                        3, const_cast<void*>(base), dims, strides, box, estride,
+                        4, const_cast<void*>(base), dims, strides, box, estride,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
   return ATTN_OK;
+}
+
+attn_status_t encode_problem_maps(const Problem& p, CUtensorMap (&maps)[5]) {
+  TcConfig cfg;
+  if (!tc_config(p.D, &cfg)) return ATTN_ERR_HEADDIM;
+  const bool bf16 = p.bf16 != 0;
+  attn_status_t s;
+  if ((s = encode_map(&maps[0], p.q, p.B, p.Hq, p.Lq, p.D, p.sq, cfg.block_m, bf16)) != ATTN_OK)
+    return s;
+  if ((s = encode_map(&maps[1], p.k, p.B, p.Hkv, p.Lk, p.D, p.sk, cfg.block_n, bf16)) != ATTN_OK)
+    return s;
+  if ((s = encode_map(&maps[2], p.v, p.B, p.Hkv, p.Lk, p.D, p.sv, cfg.block_n, bf16)) != ATTN_OK)
+    return s;
+  maps[3] = maps[2];
+  return encode_map(&maps[4], p.o, p.B, p.Hq, p.Lq, p.D, p.so, cfg.block_m, bf16);
 }
 
 Problem make_problem(const void* q, const void* k, const void* v, void* o, float* lse, int B,
@@ -213,8 +234,11 @@ Problem make_problem(const void* q, const void* k, const void* v, void* o, float
   p.B = B;
   p.Hq = Hq;
   p.Hkv = Hkv;
-  p.L = L;
+  p.Lq = L;
+  p.Lk = L;
   p.D = D;
+  p.sq = p.so = contiguous_strides(Hq, L, D);
+  p.sk = p.sv = contiguous_strides(Hkv, L, D);
   p.sm_scale = sm_scale;
   p.causal = causal;
   p.bf16 = dtype == ATTN_BF16 ? 1 : 0;
@@ -227,39 +251,29 @@ Problem make_problem(const void* q, const void* k, const void* v, void* o, float
 using attn::encode_map;
 using attn::make_problem;
 
-extern "C" {
+namespace {
 
-attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
-                       int Hq, int Hkv, int L, int D, float sm_scale, int causal,
-                       const int32_t* valid_len, attn_dtype_t dtype, attn_stream_t stream) {
-  attn_status_t s = validate(q, k, v, o, lse, B, Hq, Hkv, L, D, sm_scale, causal, valid_len, dtype);
-  if (s != ATTN_OK) return s;
-  int dev = 0;
-  DeviceState* st = nullptr;
-  s = device_state(&dev, &st);
-  if (s != ATTN_OK) return s;
+// The tensor-core path for a validated problem on the current device: for
+// bf16, the stream-ordered workspace and the V pre-pass, then the attention
+// kernel, then the workspace returned to the pool.
+attn_status_t run_tc(Problem& p, int dev, DeviceState* st) {
   attn::TcConfig cfg;
-  if (!attn::tc_config(D, &cfg)) return ATTN_ERR_HEADDIM;
-  const bool bf16 = dtype == ATTN_BF16;
+  if (!attn::tc_config(p.D, &cfg)) return ATTN_ERR_HEADDIM;
   CUtensorMap maps[5];
-  if ((s = encode_map(&maps[0], q, B * Hq, L, D, cfg.block_m, bf16)) != ATTN_OK) return s;
-  if ((s = encode_map(&maps[1], k, B * Hkv, L, D, cfg.block_n, bf16)) != ATTN_OK) return s;
-  if ((s = encode_map(&maps[2], v, B * Hkv, L, D, cfg.block_n, bf16)) != ATTN_OK) return s;
-  maps[3] = maps[2];
-  if ((s = encode_map(&maps[4], o, B * Hq, L, D, cfg.block_m, bf16)) != ATTN_OK) return s;
-  Problem p = make_problem(q, k, v, o, lse, B, Hq, Hkv, L, D, sm_scale, causal, valid_len, dtype,
-                           stream, st->status);
+  attn_status_t s = attn::encode_problem_maps(p, maps);
+  if (s != ATTN_OK) return s;
   void* ws = nullptr;
-  if (bf16) {
-    // workspace: fp16 copy of V, then the per-tile flags
+  if (p.bf16) {
+    // workspace: contiguous fp16 copy of V, then the per-tile flags
     cudaMemPool_t pool = nullptr;
     if ((s = workspace_pool(dev, st, &pool)) != ATTN_OK) return s;
     cudaError_t e = cudaMallocFromPoolAsync(&ws, static_cast<size_t>(attn::vconv_workspace_bytes(p)),
                                             pool, p.stream);
     if (e != cudaSuccess) return cuda_fail(e);
-    const size_t v_bytes = static_cast<size_t>(B) * Hkv * L * D * 2;
+    const size_t v_bytes = static_cast<size_t>(p.B) * p.Hkv * p.Lk * p.D * 2;
     int* flags = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + v_bytes);
-    s = encode_map(&maps[3], ws, B * Hkv, L, D, cfg.block_n, false);
+    s = encode_map(&maps[3], ws, p.B, p.Hkv, p.Lk, p.D, attn::contiguous_strides(p.Hkv, p.Lk, p.D),
+                   cfg.block_n, false);
     if (s == ATTN_OK) {
       e = attn::launch_vconv(p, ws, flags);
       if (e != cudaSuccess) s = cuda_fail(e);
@@ -277,6 +291,100 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
   }
   if (e != cudaSuccess) return cuda_fail(e);
   return ATTN_OK;
+}
+
+// Strides of one operand: NULL means contiguous.  Every stride of a
+// dimension with extent > 1 must be a positive multiple of 8 elements (16
+// bytes: TMA strides and 16-byte row loads) below 2^39 elements (the tensor
+// map's 2^40-byte limit); an extent-1 dimension's stride is not used.
+attn_status_t strides_of(const attn_strides_t* in, int B, int H, int L, int D,
+                         attn::Strides* out) {
+  if (in == nullptr) {
+    *out = attn::contiguous_strides(H, L, D);
+    return ATTN_OK;
+  }
+  const int64_t v[3] = {in->batch, in->head, in->seq};
+  const bool used[3] = {B > 1, H > 1, L > 1};
+  for (int i = 0; i < 3; ++i) {
+    if (!used[i]) continue;
+    if (v[i] < 1 || v[i] % 8 != 0 || v[i] >= (int64_t(1) << 39)) return ATTN_ERR_STRIDE;
+  }
+  *out = attn::Strides{in->batch, in->head, in->seq};
+  return ATTN_OK;
+}
+
+// O is written: no two of its elements may share an address.  With the
+// dimensions of extent > 1 ordered by stride, each stride must step over the
+// whole extent of the next smaller one (the row of D elements innermost).
+bool no_self_overlap(const attn::Strides& s, int B, int H, int L, int D) {
+  int64_t st[3] = {s.l, s.h, s.b};
+  int64_t ext[3] = {L, H, B};
+  // sort the three dimensions by stride (insertion sort)
+  for (int i = 1; i < 3; ++i)
+    for (int j = i; j > 0 && st[j] < st[j - 1]; --j) {
+      const int64_t a = st[j], e = ext[j];
+      st[j] = st[j - 1];
+      ext[j] = ext[j - 1];
+      st[j - 1] = a;
+      ext[j - 1] = e;
+    }
+  int64_t span = D;  // elements covered by the dimensions below
+  for (int i = 0; i < 3; ++i) {
+    if (ext[i] == 1) continue;
+    if (st[i] < span) return false;
+    span = st[i] * ext[i];
+  }
+  return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                       int Hq, int Hkv, int L, int D, float sm_scale, int causal,
+                       const int32_t* valid_len, attn_dtype_t dtype, attn_stream_t stream) {
+  attn_status_t s = validate(q, k, v, o, lse, B, Hq, Hkv, L, D, sm_scale, causal, valid_len, dtype);
+  if (s != ATTN_OK) return s;
+  int dev = 0;
+  DeviceState* st = nullptr;
+  s = device_state(&dev, &st);
+  if (s != ATTN_OK) return s;
+  Problem p = make_problem(q, k, v, o, lse, B, Hq, Hkv, L, D, sm_scale, causal, valid_len, dtype,
+                           stream, st->status);
+  return run_tc(p, dev, st);
+}
+
+attn_status_t attn_fwd_strided(const void* q, const attn_strides_t* q_strides, const void* k,
+                               const attn_strides_t* k_strides, const void* v,
+                               const attn_strides_t* v_strides, void* o,
+                               const attn_strides_t* o_strides, float* lse, int B, int Hq,
+                               int Hkv, int Lq, int Lk, int D, float sm_scale, int causal,
+                               const int32_t* valid_len, attn_dtype_t dtype,
+                               attn_stream_t stream) {
+  // attn_fwd's checks with L = Lq, then the key length
+  attn_status_t s =
+      validate(q, k, v, o, lse, B, Hq, Hkv, Lq, D, sm_scale, causal, valid_len, dtype);
+  if (s != ATTN_OK) return s;
+  if (Lk < 1 || static_cast<int64_t>(B) * Hkv * Lk > INT32_MAX) return ATTN_ERR_SHAPE;
+  attn::Strides sq, sk, sv, so;
+  if ((s = strides_of(q_strides, B, Hq, Lq, D, &sq)) != ATTN_OK) return s;
+  if ((s = strides_of(k_strides, B, Hkv, Lk, D, &sk)) != ATTN_OK) return s;
+  if ((s = strides_of(v_strides, B, Hkv, Lk, D, &sv)) != ATTN_OK) return s;
+  if ((s = strides_of(o_strides, B, Hq, Lq, D, &so)) != ATTN_OK) return s;
+  if (!no_self_overlap(so, B, Hq, Lq, D)) return ATTN_ERR_STRIDE;
+  int dev = 0;
+  DeviceState* st = nullptr;
+  s = device_state(&dev, &st);
+  if (s != ATTN_OK) return s;
+  Problem p = make_problem(q, k, v, o, lse, B, Hq, Hkv, Lq, D, sm_scale, causal, valid_len, dtype,
+                           stream, st->status);
+  p.Lk = Lk;
+  p.sq = sq;
+  p.sk = sk;
+  p.sv = sv;
+  p.so = so;
+  return run_tc(p, dev, st);
 }
 
 attn_status_t attn_fwd_simt(const void* q, const void* k, const void* v, void* o, float* lse,
@@ -371,6 +479,8 @@ const char* attn_strerror(attn_status_t status) {
     case ATTN_ERR_ARG: return "invalid argument";
     case ATTN_ERR_SCRATCH:
       return "the call needs more scratch than attn_fwd_noalloc's static array holds";
+    case ATTN_ERR_STRIDE:
+      return "a stride is not a positive multiple of 8 elements below 2^39, or O's elements overlap";
   }
   return "unknown status";
 }

@@ -336,25 +336,20 @@ attn_status_t attn_fwd_host(const void* q, const void* k, const void* v, void* o
     for_each_piece(static_cast<int64_t>(q0), static_cast<int64_t>(q0 + nq), Hq, Hkv,
                    [&](const Piece& pc) {
       if (result != ATTN_OK) return;
-      const int heads_q = pc.nb * pc.hq, heads_kv = pc.nb * pc.hkv;
       const uint8_t* pq = d_q + pc.q0 * head;
       const uint8_t* pk = d_k + pc.kv0 * head;
       const uint8_t* pv = d_v + pc.kv0 * head;
       uint8_t* po = d_o + pc.q0 * head;
-      CUtensorMap maps[5];
-      if (!status_step(attn::encode_map(&maps[0], pq, heads_q, L, D, cfg.block_m, bf16)) ||
-          !status_step(attn::encode_map(&maps[1], pk, heads_kv, L, D, cfg.block_n, bf16)) ||
-          !status_step(attn::encode_map(&maps[2], pv, heads_kv, L, D, cfg.block_n, bf16)) ||
-          !status_step(attn::encode_map(&maps[4], po, heads_q, L, D, cfg.block_m, bf16)))
-        return;
-      maps[3] = maps[2];
-      if (bf16 && !status_step(attn::encode_map(&maps[3], d_v16 + pc.kv0 * head, heads_kv, L, D,
-                                                cfg.block_n, false)))
-        return;
       attn::Problem p = attn::make_problem(
           pq, pk, pv, po, d_lse != nullptr ? d_lse + pc.q0 * L : nullptr, pc.nb, pc.hq, pc.hkv, L,
           D, sm_scale, causal, d_vl != nullptr ? d_vl + pc.b : nullptr, dtype,
           reinterpret_cast<attn_stream_t>(comp), status_word);
+      CUtensorMap maps[5];
+      if (!status_step(attn::encode_problem_maps(p, maps))) return;
+      if (bf16 && !status_step(attn::encode_map(&maps[3], d_v16 + pc.kv0 * head, pc.nb, pc.hkv, L,
+                                                D, attn::contiguous_strides(pc.hkv, L, D),
+                                                cfg.block_n, false)))
+        return;
       p.vflags = bf16 ? d_flags + pc.kv0 * n_kt : nullptr;
       step(attn::launch_tc(p, maps, num_sms));
     });

@@ -19,6 +19,17 @@ enum : int {
   kRoleEpilogue = 8 << 8,
 };
 
+// Element strides of one [B, H, L, D] operand (batch, head, sequence
+// position); the D elements of a row are contiguous.
+struct Strides {
+  int64_t b, h, l;
+};
+
+// Strides of a contiguous [B, H, L, D] tensor.
+inline Strides contiguous_strides(int H, int L, int D) {
+  return {static_cast<int64_t>(H) * L * D, static_cast<int64_t>(L) * D, static_cast<int64_t>(D)};
+}
+
 // Problem description handed to a kernel launcher (already validated).
 struct Problem {
   const void* q;
@@ -31,7 +42,10 @@ struct Problem {
   // bf16: per (b*Hkv + h, 128-key tile) flag from the V pre-pass (1 = exact
   // fp16 copy of the tile exists); null = no copy (every tile split)
   const int* vflags;
-  int B, Hq, Hkv, L, D;
+  int B, Hq, Hkv;
+  int Lq, Lk;              // query rows, key/value rows per head
+  int D;
+  Strides sq, sk, sv, so;  // element strides of q, k, v and o
   float sm_scale;
   int causal;
   int bf16;                // 0 fp16, 1 bf16
@@ -70,12 +84,22 @@ attn_status_t validate(const void* q, const void* k, const void* v, void* o, flo
                        int Hq, int Hkv, int L, int D, float sm_scale, int causal,
                        const int32_t* valid_len, attn_dtype_t dtype);
 attn_status_t tensor_map_encoder_ready();
-attn_status_t encode_map(CUtensorMap* map, const void* base, int heads, int L, int D, int rows,
-                         bool bf16);
+// Tensor map over a [B, H, L, D] 16-bit operand with element strides st,
+// viewed as 4-D (D innermost, then L, H, B); boxes of 64 columns x `rows`
+// rows of one head, 128-byte swizzle.  Columns D..63 of a box (D < 64) and
+// rows past L read as zeros and are not written by stores.
+attn_status_t encode_map(CUtensorMap* map, const void* base, int B, int H, int L, int D,
+                         const Strides& st, int rows, bool bf16);
+// A problem over contiguous tensors with Lq = Lk = L.
 Problem make_problem(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                      int Hq, int Hkv, int L, int D, float sm_scale, int causal,
                      const int32_t* valid_len, attn_dtype_t dtype, attn_stream_t stream,
                      int* status);
+
+// The five tensor maps of the tensor-core kernel for p (Q, K, V, V again in
+// place of the fp16 copy, O); launch_tc's caller replaces maps[3] when it
+// makes the fp16 copy.
+attn_status_t encode_problem_maps(const Problem& p, CUtensorMap (&maps)[5]);
 
 // attn_noalloc.cu: OR the no-alloc path's status word on `dev` into *code
 // and clear it (a no-op unless attn_fwd_noalloc ran on that device).

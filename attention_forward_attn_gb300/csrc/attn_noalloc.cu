@@ -110,24 +110,17 @@ extern "C" attn_status_t attn_fwd_noalloc(const void* q, const void* k, const vo
   NoallocDevice* d = nullptr;
   if ((s = setup_device(dev, &d)) != ATTN_OK) return s;
   if ((s = attn::tensor_map_encoder_ready()) != ATTN_OK) return s;
-  attn::TcConfig cfg;
-  if (!attn::tc_config(D, &cfg)) return ATTN_ERR_HEADDIM;
-  const bool bf16 = dtype == ATTN_BF16;
+  attn::Problem p = attn::make_problem(q, k, v, o, lse, B, Hq, Hkv, L, D, sm_scale, causal,
+                                       valid_len, dtype, stream, d->scratch);
   // no fp16 copy of V without a workspace: bf16 tiles all take the split
   // P.V (Problem::vflags stays null); the fourth map is never read
   CUtensorMap maps[5];
-  if ((s = attn::encode_map(&maps[0], q, B * Hq, L, D, cfg.block_m, bf16)) != ATTN_OK) return s;
-  if ((s = attn::encode_map(&maps[1], k, B * Hkv, L, D, cfg.block_n, bf16)) != ATTN_OK) return s;
-  if ((s = attn::encode_map(&maps[2], v, B * Hkv, L, D, cfg.block_n, bf16)) != ATTN_OK) return s;
-  maps[3] = maps[2];
-  if ((s = attn::encode_map(&maps[4], o, B * Hq, L, D, cfg.block_m, bf16)) != ATTN_OK) return s;
+  if ((s = attn::encode_problem_maps(p, maps)) != ATTN_OK) return s;
   // The status word must start at zero for this call: the array keeps
   // whatever the previous call (on any stream) left in it.
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   e = cudaMemsetAsync(d->scratch, 0, sizeof(int) * kStatusWordsPerCall, st);
   if (e != cudaSuccess) return attn::cuda_fail(e);
-  attn::Problem p = attn::make_problem(q, k, v, o, lse, B, Hq, Hkv, L, D, sm_scale, causal,
-                                       valid_len, dtype, stream, d->scratch);
   e = attn::launch_tc(p, maps, d->num_sms);
   if (e != cudaSuccess) return attn::cuda_fail(e);
   {

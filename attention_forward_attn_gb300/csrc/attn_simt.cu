@@ -60,25 +60,30 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
   const int lane = threadIdx.x & 31;
   const int i = blockIdx.x * kWarpsPerBlock + warp;  // query row
   const int bh = blockIdx.y;                         // b * Hq + h_q
-  if (i >= p.L) return;                              // whole warp leaves together
+  if (i >= p.Lq) return;                             // whole warp leaves together
   const int b = bh / p.Hq;
   const int h_q = bh % p.Hq;
   const int h_kv = h_q / (p.Hq / p.Hkv);
 
-  int kv_len = p.L;
+  int kv_len = p.Lk;
   if (p.valid_len != nullptr) {
     int vl = p.valid_len[b];
-    if (vl < 0 || vl > p.L) {
+    if (vl < 0 || vl > p.Lk) {
       if (lane == 0) atomicOr(p.status, kStatusValidLenClamped);
-      vl = vl < 0 ? 0 : p.L;
+      vl = vl < 0 ? 0 : p.Lk;
     }
     kv_len = vl;
   }
   const int key_end = p.causal ? min(kv_len, i + 1) : kv_len;
 
-  const int64_t q_row = static_cast<int64_t>(bh) * p.L + i;
-  const int64_t kv_head = static_cast<int64_t>(b) * p.Hkv + h_kv;
-  for (int d = lane; d < D; d += 32) q_sh[warp][d] = load_elem<BF16>(p.q, q_row * D + d);
+  // element offsets of this row of Q and O, of key 0 of the K and V head, and
+  // of this row of LSE ([B*Hq, Lq] contiguous)
+  const int64_t q_row = b * p.sq.b + h_q * p.sq.h + i * p.sq.l;
+  const int64_t o_row = b * p.so.b + h_q * p.so.h + i * p.so.l;
+  const int64_t k_head = b * p.sk.b + h_kv * p.sk.h;
+  const int64_t v_head = b * p.sv.b + h_kv * p.sv.h;
+  const int64_t lse_row = static_cast<int64_t>(bh) * p.Lq + i;
+  for (int d = lane; d < D; d += 32) q_sh[warp][d] = load_elem<BF16>(p.q, q_row + d);
   __syncwarp();
 
   float m = -INFINITY;  // running max of the scaled (log2-domain) scores
@@ -91,7 +96,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     const int key = kb + lane;
     float t = -INFINITY;
     if (key < key_end) {
-      const int64_t k_row = (kv_head * p.L + key) * D;
+      const int64_t k_row = k_head + key * p.sk.l;
       float dot = 0.f;
 #pragma unroll 8
       for (int d = 0; d < D; ++d) dot = fmaf(q_sh[warp][d], load_elem<BF16>(p.k, k_row + d), dot);
@@ -106,7 +111,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     const int n_keys = min(32, key_end - kb);
     for (int j = 0; j < n_keys; ++j) {
       const float wj = __shfl_sync(0xffffffffu, w, j);
-      const int64_t v_row = (kv_head * p.L + kb + j) * D;
+      const int64_t v_row = v_head + (kb + j) * p.sv.l;
 #pragma unroll
       for (int c = 0; c < kPerLane; ++c) {
         if (D % 32 == 0 || lane + 32 * c < D)
@@ -119,11 +124,11 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
   const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
 #pragma unroll
   for (int c = 0; c < kPerLane; ++c) {
-    if (D % 32 == 0 || lane + 32 * c < D) store_elem<BF16>(p.o, q_row * D + lane + 32 * c, acc[c] * inv_l);
+    if (D % 32 == 0 || lane + 32 * c < D) store_elem<BF16>(p.o, o_row + lane + 32 * c, acc[c] * inv_l);
   }
   if (p.lse != nullptr && lane == 0) {
     // natural log: ln(sum exp(s)) = ln2 * (m + log2 l) with m in log2 units
-    p.lse[q_row] = (l > 0.f) ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
+    p.lse[lse_row] = (l > 0.f) ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
   }
 }
 
@@ -132,7 +137,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 cudaError_t launch_simt(const Problem& p) {
   const float scale_log2 = p.sm_scale * 1.4426950408889634f;
   if (static_cast<int64_t>(p.B) * p.Hq > 65535) return cudaErrorInvalidConfiguration;
-  dim3 grid((p.L + kWarpsPerBlock - 1) / kWarpsPerBlock, p.B * p.Hq);
+  dim3 grid((p.Lq + kWarpsPerBlock - 1) / kWarpsPerBlock, p.B * p.Hq);
   dim3 block(kWarpsPerBlock * 32);
   if (p.D == 16) {
     if (p.bf16) attn_fwd_simt_kernel<16, true><<<grid, block, 0, p.stream>>>(p, scale_log2);

@@ -143,8 +143,10 @@ struct KParams {
   // exact, 0 = use the bf16 tile; null = no fp16 copy exists
   const int* vflags;
   int n_kt;     // 128-key tiles per (b, h_kv)
-  int B, Hq, Hkv, L, G;
+  int B, Hq, Hkv, G;
+  int Lq, Lk;   // query rows, key/value rows per head
   int d_o;      // elements per row of O in memory: the problem's D (<= the instance's D)
+  int64_t o_sb, o_sh, o_sl;  // element strides of O (batch, head, row)
   int n_mb;     // 128-row query tiles per (b, h_q)
   int n_units;  // B * Hq * n_mb
   float scale_log2;
@@ -152,7 +154,7 @@ struct KParams {
 };
 
 struct Unit {
-  int bh, b, hkv, m0, kv_len;
+  int bh, b, hq, hkv, m0, kv_len;
   int n;  // key tiles the query tile visits (0: no visible key)
 };
 
@@ -179,12 +181,13 @@ __device__ __forceinline__ Unit decode_unit(const KParams& p, int u) {
     mb = u % p.n_mb;
   }
   w.b = w.bh / p.Hq;
-  w.hkv = (w.bh % p.Hq) / p.G;
+  w.hq = w.bh % p.Hq;
+  w.hkv = w.hq / p.G;
   w.m0 = mb * BM;
-  int kv = p.L;
+  int kv = p.Lk;
   if (p.valid_len != nullptr) {
     kv = p.valid_len[w.b];
-    kv = kv < 0 ? 0 : (kv > p.L ? p.L : kv);
+    kv = kv < 0 ? 0 : (kv > p.Lk ? p.Lk : kv);
   }
   w.kv_len = kv;
   const int hi = p.causal ? min(kv, w.m0 + BM) : kv;
@@ -273,7 +276,7 @@ __device__ void producer_role(const KParams& p, const Bars<D>& br, uint32_t smem
   bool ok = true;
 
   // One K or V tile into the next slot of its ring.
-  auto load_kv = [&](bool is_v, int j, int z_kv) -> bool {
+  auto load_kv = [&](bool is_v, int j, const Unit& w, int z_kv) -> bool {
     uint32_t& it = is_v ? vit : kit;
     const uint32_t ns = is_v ? C::kVStages : C::kKStages;
     const uint32_t s = it % ns;
@@ -288,7 +291,7 @@ __device__ void producer_role(const KParams& p, const Bars<D>& br, uint32_t smem
     ptx::mbar_arrive_expect_tx(full, C::kKVBytes);
 #pragma unroll
     for (int h = 0; h < C::kHalves; ++h)
-      ptx::tma_load_3d_hint(dst + h * C::kSlabKV, map, full, h * 64, j * BN, z_kv, pol_keep);
+      ptx::tma_load_4d_hint(dst + h * C::kSlabKV, map, full, h * 64, j * BN, w.hkv, w.b, pol_keep);
     if (is_v) {
       v_used |= 1u << s;
       v_par = (v_par & ~(1u << s)) | (par << s);
@@ -313,14 +316,14 @@ __device__ void producer_role(const KParams& p, const Bars<D>& br, uint32_t smem
     ptx::mbar_arrive_expect_tx(br.q_full(), C::kQBytes);
 #pragma unroll
     for (int h = 0; h < C::kHalves; ++h)
-      ptx::tma_load_3d_hint(smem + C::kOffQ + h * C::kSlabQ, tm_q, br.q_full(), h * 64, w.m0, w.bh,
-                            pol_stream);
+      ptx::tma_load_4d_hint(smem + C::kOffQ + h * C::kSlabQ, tm_q, br.q_full(), h * 64, w.m0, w.hq,
+                            w.b, pol_stream);
     // issue order = consumption order: K_0 K_1 K_2 | V_0 K_3 | V_1 K_4 | ...
     const int lead = n < C::kScoreBufs ? n : C::kScoreBufs;
-    for (int i = 0; ok && i < lead; ++i) ok = load_kv(false, i, z_kv);
+    for (int i = 0; ok && i < lead; ++i) ok = load_kv(false, i, w, z_kv);
     for (int j = 0; ok && j < n; ++j) {
-      ok = load_kv(true, j, z_kv);
-      if (ok && j + C::kScoreBufs < n) ok = load_kv(false, j + C::kScoreBufs, z_kv);
+      ok = load_kv(true, j, w, z_kv);
+      if (ok && j + C::kScoreBufs < n) ok = load_kv(false, j + C::kScoreBufs, w, z_kv);
     }
   }
   // Never leave with a copy in flight: wait (bounded) for the last load of
@@ -599,17 +602,18 @@ __device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t smem,
       }
     };
     const int row = w.m0 + lane_row;
-    const bool row_ok = row < p.L;
-    const int64_t grow = static_cast<int64_t>(w.bh) * p.L + row;
+    const bool row_ok = row < p.Lq;
+    const int64_t grow = static_cast<int64_t>(w.bh) * p.Lq + row;  // LSE row
     if (threadIdx.x == 0 && p.valid_len != nullptr) {
       const int vl = p.valid_len[w.b];
-      if (vl < 0 || vl > p.L) atomicOr(p.status, kStatusValidLenClamped);
+      if (vl < 0 || vl > p.Lk) atomicOr(p.status, kStatusValidLenClamped);
     }
     const int n = w.n;
     if (n == 0) {  // no visible key: O = 0, LSE = -inf
       if (row_ok) {
         // rows of O are d_o elements long (D = 16 and 32 run the D = 64 instance)
-        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.o) + grow * p.d_o * 2);
+        const int64_t orow = w.b * p.o_sb + w.hq * p.o_sh + row * p.o_sl;
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.o) + orow * 2);
 #pragma unroll
         for (int c = 0; c < D / 8; ++c) {
           if (c < p.d_o / 8) dst[c] = make_uint4(0u, 0u, 0u, 0u);
@@ -749,11 +753,11 @@ __device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t smem,
     ptx::fence_proxy_async_shared();  // the generic-proxy writes, before the TMA reads them
     ptx::mbar_arrive(br.o_staged());
     if (threadIdx.x == 0) {
-      // rows past L are outside the tensor map and are not written
+      // rows past Lq are outside the tensor map and are not written
       if (wait_bar(br, p.status, br.o_staged(), epi & 1u, kRoleEpilogue)) {
 #pragma unroll
         for (int hs = 0; hs < C::kHalves; ++hs)
-          ptx::tma_store_3d(tm_o, stage + hs * C::kSlabQ, hs * 64, w.m0, w.bh);
+          ptx::tma_store_4d(tm_o, stage + hs * C::kSlabQ, hs * 64, w.m0, w.hq, w.b);
         ptx::bulk_commit_group();
         pending_stage = vstage;  // released after the next softmax step
       }
@@ -860,14 +864,18 @@ cudaError_t launch_instance(const Problem& pr, const CUtensorMap* maps, int num_
   kp.valid_len = pr.valid_len;
   kp.status = pr.status;
   kp.vflags = pr.vflags;
-  kp.n_kt = (pr.L + BN - 1) / BN;
+  kp.n_kt = (pr.Lk + BN - 1) / BN;
   kp.B = pr.B;
   kp.Hq = pr.Hq;
   kp.Hkv = pr.Hkv;
-  kp.L = pr.L;
+  kp.Lq = pr.Lq;
+  kp.Lk = pr.Lk;
   kp.G = pr.Hq / pr.Hkv;
   kp.d_o = pr.D;
-  kp.n_mb = (pr.L + BM - 1) / BM;
+  kp.o_sb = pr.so.b;
+  kp.o_sh = pr.so.h;
+  kp.o_sl = pr.so.l;
+  kp.n_mb = (pr.Lq + BM - 1) / BM;
   kp.n_units = pr.B * pr.Hq * kp.n_mb;
   // A zero scale is passed as the smallest normal float: every product
   // s * scale then rounds to zero exactly as with 0 (all visible keys get

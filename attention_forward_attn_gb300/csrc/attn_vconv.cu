@@ -14,7 +14,9 @@
 //
 // One CTA per (b*Hkv + h, 128-key tile): 256 threads hold the tile in
 // registers (16-byte loads), vote on the range check, and write the fp16
-// tile and its flag.  HBM-bound: reads 2 bytes and writes 2 bytes per
+// tile and its flag.  V may be strided (any batch, head and row strides that
+// are multiples of 8 elements); the copy is always a contiguous
+// [B, Hkv, Lk, D] tensor.  HBM-bound: reads 2 bytes and writes 2 bytes per
 // element.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -52,7 +54,7 @@ template <int D>
 __global__ void __launch_bounds__(kThreadsV) v_to_f16_kernel(const uint16_t* __restrict__ v,
                                                              uint16_t* __restrict__ v16,
                                                              int* __restrict__ flags, int L,
-                                                             int n_kt) {
+                                                             int n_kt, int Hkv, Strides sv) {
   constexpr int kVecPerRow = D / 8;                 // 16-byte vectors per row
   constexpr int kPer = kTileKeys * kVecPerRow / kThreadsV;
   static_assert(kPer >= 1 && kPer * kThreadsV == kTileKeys * kVecPerRow, "tile / thread split");
@@ -61,16 +63,18 @@ __global__ void __launch_bounds__(kThreadsV) v_to_f16_kernel(const uint16_t* __r
   const int r0 = tile * kTileKeys;
   const int rows = min(kTileKeys, L - r0);
   const int nvec = rows * kVecPerRow;
-  const int64_t base = (static_cast<int64_t>(z) * L + r0) * D / 8;  // in 16-byte vectors
-  const uint4* src = reinterpret_cast<const uint4*>(v) + base;
-  uint4* dst = reinterpret_cast<uint4*>(v16) + base;
+  // source: row r0 of head (b, h) of V, rows sv.l elements apart
+  const uint16_t* src = v + (z / Hkv) * sv.b + (z % Hkv) * sv.h + static_cast<int64_t>(r0) * sv.l;
+  // destination: the contiguous copy, in 16-byte vectors
+  uint4* dst = reinterpret_cast<uint4*>(v16) + (static_cast<int64_t>(z) * L + r0) * D / 8;
 
   uint4 x[kPer];
   uint32_t ex = 0;
 #pragma unroll
   for (int i = 0; i < kPer; ++i) {
     const int idx = static_cast<int>(threadIdx.x) + kThreadsV * i;
-    x[i] = idx < nvec ? ld_stream(src + idx) : make_uint4(0u, 0u, 0u, 0u);
+    const uint4* a = reinterpret_cast<const uint4*>(src + (idx / kVecPerRow) * sv.l) + idx % kVecPerRow;
+    x[i] = idx < nvec ? ld_stream(a) : make_uint4(0u, 0u, 0u, 0u);
     ex = max(ex, max(max(exp_max(x[i].x), exp_max(x[i].y)), max(exp_max(x[i].z), exp_max(x[i].w))));
   }
   // exponent field 143 (0x4780) and above: |v| >= 2^16, inf or NaN
@@ -91,29 +95,29 @@ __global__ void __launch_bounds__(kThreadsV) v_to_f16_kernel(const uint16_t* __r
 }  // namespace
 
 int64_t vconv_workspace_bytes(const Problem& p) {
-  const int64_t n_kt = (p.L + kTileKeys - 1) / kTileKeys;
-  const int64_t v_bytes = static_cast<int64_t>(p.B) * p.Hkv * p.L * p.D * 2;
+  const int64_t n_kt = (p.Lk + kTileKeys - 1) / kTileKeys;
+  const int64_t v_bytes = static_cast<int64_t>(p.B) * p.Hkv * p.Lk * p.D * 2;
   return v_bytes + static_cast<int64_t>(p.B) * p.Hkv * n_kt * 4;
 }
 
 cudaError_t launch_vconv(const Problem& p, void* v16, int* flags) {
-  const int64_t n_kt = (p.L + kTileKeys - 1) / kTileKeys;
+  const int64_t n_kt = (p.Lk + kTileKeys - 1) / kTileKeys;
   const int64_t blocks = static_cast<int64_t>(p.B) * p.Hkv * n_kt;
   if (blocks > INT32_MAX) return cudaErrorInvalidValue;
   const auto* v = static_cast<const uint16_t*>(p.v);
   auto* out = static_cast<uint16_t*>(v16);
   if (p.D == 16) {
     v_to_f16_kernel<16><<<static_cast<unsigned>(blocks), kThreadsV, 0, p.stream>>>(
-        v, out, flags, p.L, static_cast<int>(n_kt));
+        v, out, flags, p.Lk, static_cast<int>(n_kt), p.Hkv, p.sv);
   } else if (p.D == 32) {
     v_to_f16_kernel<32><<<static_cast<unsigned>(blocks), kThreadsV, 0, p.stream>>>(
-        v, out, flags, p.L, static_cast<int>(n_kt));
+        v, out, flags, p.Lk, static_cast<int>(n_kt), p.Hkv, p.sv);
   } else if (p.D == 64) {
     v_to_f16_kernel<64><<<static_cast<unsigned>(blocks), kThreadsV, 0, p.stream>>>(
-        v, out, flags, p.L, static_cast<int>(n_kt));
+        v, out, flags, p.Lk, static_cast<int>(n_kt), p.Hkv, p.sv);
   } else if (p.D == 128) {
     v_to_f16_kernel<128><<<static_cast<unsigned>(blocks), kThreadsV, 0, p.stream>>>(
-        v, out, flags, p.L, static_cast<int>(n_kt));
+        v, out, flags, p.Lk, static_cast<int>(n_kt), p.Hkv, p.sv);
   } else {
     return cudaErrorInvalidValue;
   }

@@ -132,6 +132,31 @@ __device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
+// Tile load global -> shared through a 4-D tensor map (coordinates innermost
+// first) with an L2 cache-policy hint; completion is counted on `bar`.
+__device__ __forceinline__ void tma_load_4d_hint(uint32_t dst, const CUtensorMap* map,
+                                                 uint32_t bar, int x, int y, int z, int w,
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w),
+      "l"(policy)
+      : "memory");
+}
+
+// Tile store shared -> global through a 4-D tensor map, tracked by the
+// issuing thread's bulk-async group.  Elements outside the tensor are not
+// written.
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, uint32_t src, int x, int y,
+                                             int z, int w) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::
+          "l"(reinterpret_cast<uint64_t>(map)),
+      "r"(src), "r"(x), "r"(y), "r"(z), "r"(w)
+      : "memory");
+}
+
 // Tile store shared -> global (3-D tensor map, coordinates innermost first),
 // tracked by the issuing thread's bulk-async group.  Rows outside the tensor
 // are not written.

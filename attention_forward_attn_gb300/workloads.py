@@ -70,23 +70,26 @@ def _normal(gen: torch.Generator, shape, dtype: str, scale: float = 1.0) -> torc
 
 
 def make_inputs(B: int, Hq: int, Hkv: int, L: int, D: int, dtype: str, seed: int,
-                q_scale: float = 1.0, valid_len=None, padded: bool = False):
+                q_scale: float = 1.0, valid_len=None, padded: bool = False,
+                Lk: Optional[int] = None):
     """Seeded CPU tensors (q, k, v, valid_len).
 
-    q: [B, Hq, L, D], k/v: [B, Hkv, L, D] in ``dtype``.  ``valid_len`` is
-    returned as an int32 CPU tensor [B]: the given values, or, when ``padded``
-    and none are given, B draws uniform in [0, L] with valid_len[0] = 0 (one
-    fully masked batch).  None when there is no padding mask.
+    q: [B, Hq, L, D], k/v: [B, Hkv, Lk, D] in ``dtype`` (Lk = L unless
+    given).  ``valid_len`` is returned as an int32 CPU tensor [B]: the given
+    values, or, when ``padded`` and none are given, B draws uniform in
+    [0, Lk] with valid_len[0] = 0 (one fully masked batch).  None when there
+    is no padding mask.
     """
+    Lk = L if Lk is None else Lk
     gen = torch.Generator().manual_seed(int(seed))
     q = _normal(gen, (B, Hq, L, D), dtype, q_scale)
-    k = _normal(gen, (B, Hkv, L, D), dtype)
-    v = _normal(gen, (B, Hkv, L, D), dtype)
+    k = _normal(gen, (B, Hkv, Lk, D), dtype)
+    v = _normal(gen, (B, Hkv, Lk, D), dtype)
     vl = None
     if valid_len is not None:
         vl = torch.tensor(list(valid_len), dtype=torch.int32)
     elif padded:
-        vl = torch.randint(0, L + 1, (B,), generator=gen, dtype=torch.int32)
+        vl = torch.randint(0, Lk + 1, (B,), generator=gen, dtype=torch.int32)
         vl[0] = 0
     return q, k, v, vl
 

@@ -49,7 +49,8 @@ typedef enum {
   ATTN_ERR_TIMEOUT = 10,   /* device side: a bounded wait inside a kernel gave up */
   ATTN_ERR_VALID_LEN = 11, /* device side: a valid_len value was outside [0, L] and was clamped */
   ATTN_ERR_ARG = 12,       /* another invalid argument (causal not 0/1, NULL out-pointer, ...) */
-  ATTN_ERR_SCRATCH = 13    /* attn_fwd_noalloc: the call needs more scratch than its static array holds */
+  ATTN_ERR_SCRATCH = 13,   /* attn_fwd_noalloc: the call needs more scratch than its static array holds */
+  ATTN_ERR_STRIDE = 14     /* attn_fwd_strided: a stride is invalid, or O's elements overlap */
 } attn_status_t;
 
 /*
@@ -107,6 +108,66 @@ typedef enum {
 attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                        int B, int Hq, int Hkv, int L, int D, float sm_scale, int causal,
                        const int32_t* valid_len, attn_dtype_t dtype, attn_stream_t stream);
+
+/* Element strides of one [B, H, L, D] operand of attn_fwd_strided: how many
+ * elements apart (b, h, i, d) and (b + 1, h, i, d), (b, h + 1, i, d) and
+ * (b, h, i + 1, d) are.  The D elements of a row are always contiguous. */
+typedef struct {
+  int64_t batch;
+  int64_t head;
+  int64_t seq;
+} attn_strides_t;
+
+/*
+ * attn_fwd_strided -- attn_fwd on strided operands, with a query length Lq and
+ * a key/value length Lk.
+ *
+ * Defined by: the same operation as attn_fwd.  tiny_flash_attn_triton.py's
+ * flash_attn_triton and the Triton-CUDA Attention page's standard Flash
+ * Attention pass every operand to the kernel with its own batch, head,
+ * sequence and dim strides; "masked multi head attention in CUDA"
+ * (wzjinhao.cn) section 2.1 notes that frameworks hold Q, K and V either as
+ * [B, N, H, D] or as [B, H, N, D].  Here both, and any other layout whose rows
+ * of D elements are contiguous (a slice of a packed QKV tensor, for example),
+ * are read and written in place, without a copy.  The pages use one sequence
+ * length; with Lq != Lk the masks keep their comparisons on absolute
+ * positions: key j is visible to query i iff (!causal || j <= i) and
+ * (valid_len == NULL || j < valid_len[b]) -- the causal mask stays top-left
+ * aligned.
+ *
+ * Arguments (device pointers, owned by the caller):
+ *   q, o      base of query and output element (0, 0, 0, 0); Q and O are
+ *             [B, Hq, Lq, D] in the index space, placed by q_strides and
+ *             o_strides.
+ *   k, v      base of K and V, [B, Hkv, Lk, D] in the index space.
+ *   *_strides NULL for a contiguous [B, H, L, D] tensor, else its element
+ *             strides.  Every stride of a dimension whose extent is > 1 must
+ *             be a positive multiple of 8 elements (16 bytes) below 2^39;
+ *             the stride of an extent-1 dimension is ignored.  O's elements
+ *             must not overlap one another (ATTN_ERR_STRIDE); Q, K and V may
+ *             overlap one another and themselves.  O must not overlap Q, K or
+ *             V (not checked: the result is then undefined).
+ *   lse       [B*Hq, Lq] contiguous fp32 output, lse[(b*Hq + h)*Lq + i], or
+ *             NULL.
+ *   Lq, Lk    query rows and key/value rows per head (>= 1); B*Hq*Lq and
+ *             B*Hkv*Lk must fit in int32.
+ *   valid_len NULL or B int32 values; values outside [0, Lk] are clamped and
+ *             reported by attn_status as ATTN_ERR_VALID_LEN.
+ *   the rest  as attn_fwd.
+ *
+ * Work and memory: attn_fwd's kernel, reading and writing through 4-D tensor
+ * maps built from the strides.  For ATTN_BF16 the fp16 copy of V in the
+ * per-call workspace is contiguous, B*Hkv*Lk*D*2 bytes (plus the tile flags).
+ * Errors: as attn_fwd, plus ATTN_ERR_STRIDE; nothing is queued on an
+ * argument error.
+ */
+attn_status_t attn_fwd_strided(const void* q, const attn_strides_t* q_strides, const void* k,
+                               const attn_strides_t* k_strides, const void* v,
+                               const attn_strides_t* v_strides, void* o,
+                               const attn_strides_t* o_strides, float* lse, int B, int Hq,
+                               int Hkv, int Lq, int Lk, int D, float sm_scale, int causal,
+                               const int32_t* valid_len, attn_dtype_t dtype,
+                               attn_stream_t stream);
 
 /*
  * attn_fwd_simt -- the same operation, same arguments and same contract as

@@ -107,3 +107,61 @@ def test_status_and_shutdown_without_device(lib):
     assert binding.STATUS_NAMES[st] == "ATTN_ERR_CUDA"
     assert code.value == 0
     attn.shutdown()  # harmless with nothing allocated
+
+
+# ------------------------------------------------------------------ attn_fwd_strided
+
+def _scall(**kw):
+    args = dict(q_ptr=A16, q_strides=None, k_ptr=A16, k_strides=None, v_ptr=A16, v_strides=None,
+                o_ptr=A16, o_strides=None, lse_ptr=None, B=2, Hq=4, Hkv=2, Lq=16, Lk=24, D=64,
+                sm_scale=0.125, causal=0, valid_len_ptr=None, dtype=attn.ATTN_BF16, stream=None)
+    args.update(kw)
+    return attn.fwd_strided_raw(**args)
+
+
+BLHD_Q = (16 * 4 * 64, 64, 4 * 64)    # [B, Lq, Hq, D] storage seen as [B, Hq, Lq, D]
+BLHD_KV = (24 * 2 * 64, 64, 2 * 64)
+
+
+@pytest.mark.parametrize("kw, expected", [
+    (dict(dtype=3), "ATTN_ERR_DTYPE"),
+    (dict(v_ptr=None), "ATTN_ERR_NULL"),
+    (dict(Lq=0), "ATTN_ERR_SHAPE"),
+    (dict(Lk=0), "ATTN_ERR_SHAPE"),
+    (dict(Lk=-3), "ATTN_ERR_SHAPE"),
+    (dict(B=1 << 12, Hkv=1 << 10, Hq=1 << 10, Lq=1, Lk=1 << 10), "ATTN_ERR_SHAPE"),
+    (dict(D=80), "ATTN_ERR_HEADDIM"),
+    (dict(Hq=5), "ATTN_ERR_HEADS"),
+    (dict(causal=-1), "ATTN_ERR_ARG"),
+    (dict(sm_scale=-0.5), "ATTN_ERR_SCALE"),
+    (dict(o_ptr=A16 + 2), "ATTN_ERR_ALIGN"),
+    # strides: positive multiples of 8 elements below 2^39 where the extent is > 1
+    (dict(q_strides=(16 * 4 * 64, 64, 68)), "ATTN_ERR_STRIDE"),
+    (dict(k_strides=(0, 24 * 64, 64)), "ATTN_ERR_STRIDE"),
+    (dict(v_strides=(2 * 24 * 64, -24 * 64, 64)), "ATTN_ERR_STRIDE"),
+    (dict(k_strides=(1 << 39, 24 * 64, 64)), "ATTN_ERR_STRIDE"),
+    (dict(v_strides=(2 * 24 * 64, 24 * 64, 4)), "ATTN_ERR_STRIDE"),
+    # O's elements must not overlap: rows closer than D, heads inside a row
+    (dict(o_strides=(4 * 16 * 64, 16 * 64, 32)), "ATTN_ERR_STRIDE"),
+    (dict(o_strides=(4 * 16 * 64, 8, 16 * 64)), "ATTN_ERR_STRIDE"),
+    (dict(o_strides=(64, 16 * 64, 64 * 4)), "ATTN_ERR_STRIDE"),
+])
+def test_strided_invalid_arguments_rejected_on_host(lib, kw, expected):
+    assert binding.STATUS_NAMES[_scall(**kw)] == expected
+
+
+@pytest.mark.parametrize("kw", [
+    dict(),                                                       # all contiguous
+    dict(q_strides=BLHD_Q, o_strides=BLHD_Q, k_strides=BLHD_KV, v_strides=BLHD_KV),
+    dict(k_strides=(999, 24 * 64, 64), B=1),                      # extent-1 batch: stride unused
+    dict(q_strides=(16 * 64, 7, 64), Hq=1, Hkv=1, o_strides=(16 * 64, 3, 64)),
+    dict(k_strides=(24 * 64 * 3, 64, 2 * 64 * 3)),                # a slice of packed [B, L, 3, H, D]
+    dict(q_strides=(0, 0, 0), o_strides=(0, 0, 0), B=1, Hq=1, Hkv=1, Lq=1),  # one row: no stride used
+    dict(v_strides=(64, 64, 64)),                                 # inputs may overlap themselves
+])
+def test_strided_valid_arguments_need_a_device(lib, kw):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present; covered by the gpu tests")
+    st = _scall(**kw)
+    assert binding.STATUS_NAMES[st] in ("ATTN_ERR_CUDA", "ATTN_ERR_ARCH")
