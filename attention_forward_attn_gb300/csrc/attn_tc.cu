@@ -9,25 +9,30 @@
 // How (one CTA per SM, persistent over work units):
 //   * work unit = (b, h_q, 128 query rows), one query tile; K/V streamed in
 //     tiles of 128 keys;
-//   * warp 4 (producer): TMA loads of the Q tile and of the K and V rings
+//   * warp 8 (producer): TMA loads of the Q tile and of the K and V rings
 //     (3 + 3 stages at D=128, 6 + 6 at D=64), 128-byte swizzled;
-//   * warps 5 and 6 (MMA issuers; one elected lane each issues): warp 6
-//     issues S(j) = Q K_j^T into one of three TMEM score buffers, warp 5
-//     issues O += P(j) V_j with P read from TMEM.  The scores run up to three
-//     key tiles ahead of the softmax (S(j+3) goes into the buffer P(j) came
-//     from, once PV(j) has completed), so the softmax never waits for scores
-//     and the tensor core has work queued while P(j) is being computed;
-//   * warps 0-3 (softmax, one thread per query row = TMEM lane): load the S
-//     row, mask (only on boundary tiles), row max, ex2.approx, row sum, write
-//     P into TMEM over the S columns, rescale the O row in TMEM when the max
-//     grew by more than 2^8 (exact after the final division), and finally
-//     O / l, staged in shared memory in the TMA layout and written by one
-//     TMA store per 64-column slab (a thread's own row would be 16 strided
-//     16-byte stores, one cache line each), and the LSE.  The staging tile is
-//     the V ring stage of the unit's last key tile: idle from its PV's
-//     completion until the producer refills it three V loads later, so the
-//     epilogue, not the PV issuer, releases that stage once the store has
-//     read it.
+//   * warps 9 and 10 (MMA issuers; one elected lane each issues): warp 10
+//     issues S(j) = Q K_j^T into one of SB TMEM score buffers (SB = 2 at
+//     D=128, 3 at D=64), warp 9 issues the P.V products with P read from
+//     TMEM.  The scores run up to SB key tiles ahead of the softmax (S(j+SB)
+//     goes into the buffer P(j) came from, once PV(j) has completed), so the
+//     tensor core has work queued while P(j) is being computed;
+//   * warps 0-7 (softmax, two warpgroups; a TMEM lane is a query row): warp w
+//     and warp w + 4 share the same 32 rows, warps 0-3 (half a) taking key
+//     columns 0-63 of every tile and warps 4-7 (half b) columns 64-127.  Each
+//     half keeps its own online softmax over its keys -- running max, sum and
+//     a partial accumulator, O_a or O_b in TMEM (O_h += P_h V_h) -- so the
+//     two never wait for each other inside a unit.  Per step a thread loads
+//     its 64 scores, masks them (only on boundary tiles), takes the max,
+//     ex2.approx, the sum, writes P into TMEM over its S columns and
+//     rescales its O_h row in TMEM when its max grew by more than 2^8 (exact
+//     after the final division).  The epilogue combines the halves
+//     (O = (O_a 2^(m_a-m) + O_b 2^(m_b-m)) / l), stages O in shared memory
+//     in the TMA layout (each half its D/2 columns) and writes it with one
+//     TMA store per 64-column slab, and the LSE.  The staging tile is the V
+//     ring stage of the unit's last key tile: idle from its PV's completion
+//     until the producer refills it, so the epilogue, not the PV issuer,
+//     releases that stage once the store has read it.
 // Causal units skip every key tile above the diagonal; padded units skip every
 // key tile at or beyond valid_len[b]; a unit with no visible key writes O = 0
 // and LSE = -inf without touching the tensor core.
@@ -60,16 +65,20 @@ namespace {
 
 constexpr int BM = 128;       // query rows per tile (TMEM lanes)
 constexpr int BN = 128;       // keys per K/V tile
-constexpr int kProducerWarp = 4;
-constexpr int kPvWarp = 5;     // P.V issuer; also allocates TMEM
-constexpr int kSWarp = 6;      // score issuer
-constexpr int kThreads = 224;  // softmax warpgroup, producer, two MMA issuers
-constexpr int kSoftmaxThreads = 128;
+constexpr int BH = BN / 2;    // keys of one half tile (one softmax warpgroup's columns)
+constexpr int kProducerWarp = 8;
+constexpr int kPvWarp = 9;     // P.V issuer; also allocates TMEM
+constexpr int kSWarp = 10;     // score issuer
+constexpr int kThreads = 352;  // two softmax warpgroups, producer, two MMA issuers
+constexpr int kSoftmaxThreads = 256;
 constexpr float kRescaleLog2 = 8.0f;  // rescale O only when the max grows by > 2^8
 constexpr float kLn2 = 0.69314718055994531f;
 
 template <int D>
 struct Cfg {
+  // D = 128: two score buffers (TMEM: 2 x 128 + O_a 128 + O_b 128 = 512
+  // columns); D = 64: three (3 x 128 + 64 + 64)
+  static constexpr int kScoreBufs = (D == 128) ? 2 : 3;
   static constexpr int kKStages = (D == 128) ? 3 : 6;
   static constexpr int kVStages = (D == 128) ? 3 : 6;
   static constexpr int kHalves = D / 64;           // 64-column (128-byte) slabs per row
@@ -83,19 +92,22 @@ struct Cfg {
   static constexpr int kOffBar = kOffV + kVStages * kKVBytes;
   static_assert(kQBytes == kKVBytes, "an O tile is staged in a V stage");
   // barrier block: q_full q_empty k_full[KS] k_empty[KS] v_full[VS] v_empty[VS]
-  // s_full[3] p_full[3] pv_done[3] o_full drain o_staged, then 32-bit words:
-  // TMEM base, abort flag
-  static constexpr int kScoreBufs = 3;
-  static constexpr int kNumBars = 2 + 2 * kKStages + 2 * kVStages + 3 * kScoreBufs + 3;
+  // s_full[SB] p_full[SB] pv_done[SB] o_full drain o_staged xch_m xch_s, then
+  // 32-bit words: TMEM base, abort flag; then the epilogue's exchange area
+  // (two floats per row)
+  static constexpr int kNumBars = 2 + 2 * kKStages + 2 * kVStages + 3 * kScoreBufs + 5;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kMiscBytes = 8;
-  static constexpr int kSmemBytes = kOffMisc + kMiscBytes + 1024;  // + slack to align the base
-  // TMEM columns: score buffers S_0, S_1, S_2 (fp32, BN each; P is written
-  // over the first columns of its score buffer), then O (fp32, D).
+  static constexpr int kOffXch = kOffMisc + kMiscBytes;
+  static constexpr int kSmemBytes = kOffXch + BM * 8 + 1024;  // + slack to align the base
+  // TMEM columns: score buffers S_b (fp32, BN each; each half's P is written
+  // over the first columns of that half), then the two partial accumulators:
+  // O_a (keys of the first half of every tile) and O_b (second half).
   static __device__ __forceinline__ uint32_t col_s(uint32_t b) { return b * BN; }
-  static constexpr uint32_t kColO = kScoreBufs * BN;
+  static constexpr uint32_t kColOa = kScoreBufs * BN;
+  static constexpr uint32_t kColOb = kColOa + D;
   static constexpr uint32_t kTmemCols = 512;
-  static_assert(kScoreBufs * BN + D <= 512, "TMEM budget");
+  static_assert(kScoreBufs * BN + 2 * D <= 512, "TMEM budget");
   static_assert(kSmemBytes <= 232448, "shared-memory budget");
 };
 
@@ -128,8 +140,12 @@ struct Bars {
   __device__ __forceinline__ uint32_t drain() const { return base + 8u * (3 + 2 * KS + 2 * VS + 3 * SB); }
   // every softmax thread has written its O row into the staging tile
   __device__ __forceinline__ uint32_t o_staged() const { return base + 8u * (4 + 2 * KS + 2 * VS + 3 * SB); }
+  // epilogue exchange: half b's (m_b, l_b) are in shared memory / half a's
+  // final scales are
+  __device__ __forceinline__ uint32_t xch_m() const { return base + 8u * (5 + 2 * KS + 2 * VS + 3 * SB); }
+  __device__ __forceinline__ uint32_t xch_s() const { return base + 8u * (6 + 2 * KS + 2 * VS + 3 * SB); }
   __device__ __forceinline__ uint32_t tmem_word() const {
-    return base + 8u * (5 + 2 * KS + 2 * VS + 3 * SB);
+    return base + 8u * (7 + 2 * KS + 2 * VS + 3 * SB);
   }
   __device__ __forceinline__ uint32_t abort_word() const { return tmem_word() + 4u; }
 };
@@ -376,36 +392,45 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t q_desc, uint6
   }
 }
 
-// O += P V: A = P from TMEM (16-bit pairs, 8 columns per 16 keys), B = V tile
-// as an MN-major 128-byte-swizzled operand (16 keys = two 8-row groups).
-// fp16 V tile (fp16 inputs, or the exact fp16 copy of a bf16 tile):
-// O += P V with fp16 P.  bf16 V tile (split): O += [P_hi | P_lo] [V; V], the
-// same V tile read twice.
+// O_h += P_h V_h for the two halves of a key tile (h = a: keys 0-63 into
+// O_a, h = b: keys 64-127 into O_b).  A = P_h from TMEM (16-bit pairs, 8
+// columns per 16 keys, at the start of its half's 64 score columns), B = the
+// half's rows of the V tile as an MN-major 128-byte-swizzled operand (16 keys
+// = two 8-row groups).  fp16 V tile (fp16 inputs, or the exact fp16 copy of
+// a bf16 tile): fp16 P.  bf16 V tile (split): O_h += [P_hi | P_lo] [V_h; V_h]
+// with P_lo in the 32 columns after P_hi, the same V rows read twice.
 template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint64_t v_desc,
-                                         bool accumulate, bool split) {
+__device__ __forceinline__ void issue_pv(uint32_t o_a, uint32_t o_b, uint32_t p_tmem,
+                                         uint64_t v_desc, bool accumulate, bool split) {
   const uint32_t idesc = split ? ptx::idesc_f16(BM, D, true, true) : ptx::idesc_f16(BM, D, false, true);
 #pragma unroll (D == 128 ? BN / 16 : 1)
-  for (int kk = 0; kk < BN / 16; ++kk)
-    ptx::mma_ts(d_tmem, p_tmem + kk * 8u, desc_add(v_desc, kk * 2048u), idesc,
-                (accumulate || kk > 0) ? 1u : 0u);
+  for (int kk = 0; kk < BN / 16; ++kk) {
+    const int h = kk / (BH / 16);
+    const int k4 = kk % (BH / 16);
+    ptx::mma_ts(h ? o_b : o_a, p_tmem + h * BH + k4 * 8u, desc_add(v_desc, kk * 2048u), idesc,
+                (accumulate || k4 > 0) ? 1u : 0u);
+  }
   if (split) {
 #pragma unroll 1
-    for (int kk = 0; kk < BN / 16; ++kk)
-      ptx::mma_ts(d_tmem, p_tmem + BN / 2 + kk * 8u, desc_add(v_desc, kk * 2048u), idesc, 1u);
+    for (int kk = 0; kk < BN / 16; ++kk) {
+      const int h = kk / (BH / 16);
+      const int k4 = kk % (BH / 16);
+      ptx::mma_ts(h ? o_b : o_a, p_tmem + h * BH + BH / 2 + k4 * 8u, desc_add(v_desc, kk * 2048u),
+                  idesc, 1u);
+    }
   }
 }
 
 
 // Two issuer warps (one elected lane each issues), so that one warp's
 // barrier waits and commits overlap the other's MMAs on the tensor core:
-//   * the S issuer (warp 6) issues every score tile in order, S(g) into
-//     buffer g % 3; before overwriting a buffer it waits until PV(g-3), which
-//     read P from it, has completed -- the scores run up to three key tiles
+//   * the S issuer issues every score tile in order, S(g) into buffer
+//     g % SB; before overwriting a buffer it waits until PV(g-SB), which
+//     read P from it, has completed -- the scores run up to SB key tiles
 //     ahead of the softmax;
-//   * the PV issuer (warp 5) issues PV(j) as soon as P(j) is in TMEM.
+//   * the PV issuer issues PV(j) (both halves) as soon as P(j) is in TMEM.
 // Per-buffer completion barriers (pv_done[b]) cannot run two phases ahead of
-// a waiter: PV(g+3) needs S(g+3), which the S issuer issues only after its
+// a waiter: PV(g+SB) needs S(g+SB), which the S issuer issues only after its
 // wait for PV(g).
 template <int D, bool BF16>
 __device__ void s_issuer_role(const KParams& p, const Bars<D>& br, uint32_t smem, uint32_t tmem) {
@@ -413,7 +438,7 @@ __device__ void s_issuer_role(const KParams& p, const Bars<D>& br, uint32_t smem
   constexpr uint32_t SB = C::kScoreBufs;
   uint32_t q_phase = 0;
   uint32_t kit = 0;
-  uint32_t g = 0;  // score tiles of all units so far: tile g uses buffer g % 3
+  uint32_t g = 0;  // score tiles of all units so far: tile g uses buffer g % SB
   // K-major operands (Q, K): leading byte offset unused with 128-byte swizzle,
   // 1024 bytes between 8-row groups
   const uint64_t q_desc = ptx::sdesc_sw128(smem + C::kOffQ, 16, 1024);
@@ -431,7 +456,7 @@ __device__ void s_issuer_role(const KParams& p, const Bars<D>& br, uint32_t smem
     q_phase ^= 1u;
     for (int j = 0; j < n; ++j, ++g) {
       const uint32_t b = g % SB;
-      // buffer b held P(g-3): wait until PV(g-3) has read it
+      // buffer b held P(g-SB): wait until PV(g-SB) has read it
       if (g >= SB && !__all_sync(0xffffffffu, wait_bar(br, p.status, br.pv_done(b),
                                                        ((g - SB) / SB) & 1u, kRoleMma))) {
         ok = false;
@@ -466,7 +491,8 @@ __device__ void pv_issuer_role(const KParams& p, const Bars<D>& br, uint32_t sme
   // MN-major V: 64-column slabs kSlabKV apart (leading), 1024 bytes between
   // 8-key groups (stride)
   const uint64_t v_desc0 = ptx::sdesc_sw128(smem + C::kOffV, C::kSlabKV, 1024);
-  const uint32_t t_o = tmem + C::kColO;
+  const uint32_t t_oa = tmem + C::kColOa;
+  const uint32_t t_ob = tmem + C::kColOb;
   bool ok = true;
 
   const int rounds = (p.n_units + gridDim.x - 1) / gridDim.x;
@@ -497,7 +523,8 @@ __device__ void pv_issuer_role(const KParams& p, const Bars<D>& br, uint32_t sme
       }
       ptx::tc_fence_after();
       if (elect_one())
-        issue_pv<D>(t_o, tmem + C::col_s(b), desc_add(v_desc0, sv * C::kKVBytes), j > 0, split);
+        issue_pv<D>(t_oa, t_ob, tmem + C::col_s(b), desc_add(v_desc0, sv * C::kKVBytes), j > 0,
+                    split);
       __syncwarp();
       commit_one(br.pv_done(b));
       // the unit's last V stage is released by the epilogue (it stages O)
@@ -514,20 +541,22 @@ __device__ void pv_issuer_role(const KParams& p, const Bars<D>& br, uint32_t sme
 
 // ------------------------------------------------------------------ softmax + epilogue
 
-// P for one score row (128 keys in registers), 32 keys at a time, written
-// over the row's S columns in TMEM; returns the row sum of P.  fp16 V tile:
-// P rounded to fp16 in columns [0, 64).  bf16 V tile (SPLIT): P = P_hi + P_lo
-// with P_hi = p truncated to bf16 (columns [0, 64)) and P_lo = bf16(p - P_hi)
-// (columns [64, 128)); a single bf16 P (unit roundoff 2^-8) is too coarse for
-// rows dominated by a few keys, the pair leaves a relative error below 2^-15.
-// Masked keys arrive as -inf scores and give P = 0.
+// P for one half row (64 keys in registers), 32 keys at a time, written over
+// the half's S columns in TMEM; returns the half row's sum of P.  fp16 V
+// tile: P rounded to fp16 in the half's columns [0, 32).  bf16 V tile
+// (SPLIT): P = P_hi + P_lo with P_hi = p truncated to bf16 (columns [0, 32))
+// and P_lo = bf16(p - P_hi) (columns [32, 64)); a single bf16 P (unit
+// roundoff 2^-8) is too coarse for rows dominated by a few keys, the pair
+// leaves a relative error below 2^-15.  Masked keys arrive as -inf scores and
+// give P = 0.
 template <bool SPLIT>
-__device__ __forceinline__ float exp_row(const uint32_t (&s)[BN], uint64_t sc2, uint64_t nm2, uint32_t t_s) {
-  uint64_t rsum2[4];  // independent partial row sums, two lanes each
+__device__ __forceinline__ float exp_half(const uint32_t (&s)[BH], uint64_t sc2, uint64_t nm2,
+                                          uint32_t t_s) {
+  uint64_t rsum2[4];  // independent partial sums, two lanes each
 #pragma unroll
   for (int k = 0; k < 4; ++k) rsum2[k] = 0ull;
 #pragma unroll
-  for (int qtr = 0; qtr < 4; ++qtr) {
+  for (int qtr = 0; qtr < BH / 32; ++qtr) {
     uint32_t hi[16];
     uint32_t lo[SPLIT ? 16 : 1];
 #pragma unroll
@@ -555,26 +584,39 @@ __device__ __forceinline__ float exp_row(const uint32_t (&s)[BN], uint64_t sc2, 
       }
     }
     ptx::tmem_st16(t_s + qtr * 16, hi);
-    if constexpr (SPLIT) ptx::tmem_st16(t_s + BN / 2 + qtr * 16, lo);
+    if constexpr (SPLIT) ptx::tmem_st16(t_s + BH / 2 + qtr * 16, lo);
   }
   float ra, rb;
   ptx::f2_unpack(ptx::f2_add(ptx::f2_add(rsum2[0], rsum2[1]), ptx::f2_add(rsum2[2], rsum2[3])), ra, rb);
   return ra + rb;
 }
 
+// Two softmax warpgroups share every query tile: warps 0-3 (half a) own key
+// columns 0-63 of each key tile and warps 4-7 (half b) columns 64-127, for
+// the same rows (warp w and w + 4 read the same TMEM lane quadrant).  Each
+// half runs its own online softmax -- running max m_h, sum l_h and the
+// partial accumulator O_h over its keys only -- so the two never wait for
+// each other while the tile streams; they meet once per unit, in the
+// epilogue, where the partial results combine exactly:
+//   m = max(m_a, m_b),  l = l_a 2^(m_a - m) + l_b 2^(m_b - m),
+//   O = (O_a 2^(m_a - m) + O_b 2^(m_b - m)) / l.
 template <int D, bool BF16>
 __device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t smem, uint32_t tmem,
                              const CUtensorMap* tm_o) {
   using C = Cfg<D>;
   constexpr int SB = C::kScoreBufs;
   const int lane_row = threadIdx.x & 127;           // row within the tile = TMEM lane
+  const int half = static_cast<int>(threadIdx.x) >> 7;  // 0: keys 0-63 of a tile, 1: 64-127
   const uint32_t quad = (threadIdx.x >> 5) & 3u;    // this warp's 32-lane TMEM quadrant
   const uint32_t lane_addr = (quad * 32u) << 16;
-  const uint32_t t_o = tmem + lane_addr + C::kColO;
+  const uint32_t t_oh = tmem + lane_addr + (half ? C::kColOb : C::kColOa);  // this half's O
+  const uint32_t t_oa = tmem + lane_addr + C::kColOa;
+  const uint32_t t_ob = tmem + lane_addr + C::kColOb;
+  const uint32_t xch = smem + C::kOffXch + static_cast<uint32_t>(lane_row) * 8u;
   const float scale_log2 = p.scale_log2;
   uint32_t o_phase = 0;
   uint32_t epi = 0;  // epilogues (staged O tiles) so far
-  uint32_t g = 0;    // score (and V) tiles of all units so far (buffer g % 3)
+  uint32_t g = 0;    // score (and V) tiles of all units so far (buffer g % SB)
   // thread 0: V stage still being read by the last O store (kNoStage: none)
   constexpr uint32_t kNoStage = 0xFFFFFFFFu;
   uint32_t pending_stage = kNoStage;
@@ -609,8 +651,8 @@ __device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t smem,
       if (vl < 0 || vl > p.Lk) atomicOr(p.status, kStatusValidLenClamped);
     }
     const int n = w.n;
-    if (n == 0) {  // no visible key: O = 0, LSE = -inf
-      if (row_ok) {
+    if (n == 0) {  // no visible key: O = 0, LSE = -inf (written by half a)
+      if (row_ok && half == 0) {
         // rows of O are d_o elements long (D = 16 and 32 run the D = 64 instance)
         const int64_t orow = w.b * p.o_sb + w.hq * p.o_sh + row * p.o_sl;
         uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.o) + orow * 2);
@@ -626,13 +668,13 @@ __device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t smem,
     const int z_kv = w.b * p.Hkv + w.hkv;
     // keys < key_lim are visible to this row
     const int key_lim = p.causal ? min(w.kv_len, row + 1) : w.kv_len;
-    float m = -INFINITY;  // running max, log2 units (scaled)
+    float m = -INFINITY;  // running max of this half's keys, log2 units (scaled)
     float l = 0.f;
     bool ok = true;
     for (int j = 0; j < n; ++j) {
       const uint32_t gg = g + static_cast<uint32_t>(j);
       const uint32_t b = gg % SB;
-      const uint32_t t_s = tmem + lane_addr + C::col_s(b);
+      const uint32_t t_s = tmem + lane_addr + C::col_s(b) + static_cast<uint32_t>(half * BH);
       // P format of this key tile: fp16 P, or the bf16 pair (split)
       if (j > 0 && (j & 31) == 0) fmask = v_fp16_mask<BF16>(p, z_kv, j, n);
       const bool split = BF16 && ((fmask >> (j & 31)) & 1u) == 0u;
@@ -642,10 +684,10 @@ __device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t smem,
         break;
       }
       ptx::tc_fence_after();
-      uint32_t s[BN];
-      ptx::tmem_ld128(t_s, s);
-      const int n0 = j * BN;
-      const bool masked = (n0 + BN > w.kv_len) || (p.causal && n0 + BN - 1 > w.m0);
+      uint32_t s[BH];
+      ptx::tmem_ld64(t_s, s);
+      const int n0 = j * BN + half * BH;  // key of column 0 of this half
+      const bool masked = (n0 + BH > w.kv_len) || (p.causal && n0 + BH - 1 > w.m0);
       const int c_lim = key_lim - n0;  // columns c < c_lim are visible
       // Boundary tiles only: invisible scores become -inf, so the max and the
       // exponentials below are the same code for every tile (one copy of the
@@ -653,14 +695,14 @@ __device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t smem,
       // because the scale is > 0 (a zero sm_scale arrives as FLT_MIN).
       if (masked) {
 #pragma unroll
-        for (int c = 0; c < BN; ++c) s[c] = (c < c_lim) ? s[c] : 0xFF800000u;
+        for (int c = 0; c < BH; ++c) s[c] = (c < c_lim) ? s[c] : 0xFF800000u;
       }
-      // row max: 8 independent chains of 3-input maxima
+      // max of the half row: 8 independent chains of 3-input maxima
       float mxk[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) mxk[k] = -INFINITY;
 #pragma unroll
-      for (int i = 0; i < BN / 2; ++i)
+      for (int i = 0; i < BH / 2; ++i)
         mxk[i & 7] = ptx::max3(mxk[i & 7], __uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1]));
       const float mx = ptx::max3(ptx::max3(mxk[0], mxk[1], mxk[2]), ptx::max3(mxk[3], mxk[4], mxk[5]),
                                  fmaxf(mxk[6], mxk[7]));
@@ -668,7 +710,7 @@ __device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t smem,
       const float m_new = fmaxf(m, m_tile);
       float alpha = 1.f;
       bool rescale = false;
-      if (m_new > m + kRescaleLog2) {  // also taken on the first tile (m = -inf)
+      if (m_new > m + kRescaleLog2) {  // also taken on the first visible key (m = -inf)
         alpha = ptx::ex2_approx(m - m_new);
         m = m_new;
         rescale = true;
@@ -676,20 +718,20 @@ __device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t smem,
       const float neg_m = (m == -INFINITY) ? 0.f : -m;
       const uint64_t sc2 = ptx::f2_pack(scale_log2, scale_log2);
       const uint64_t nm2 = ptx::f2_pack(neg_m, neg_m);
-      // P over the S columns (every S value is already in registers)
+      // P over the half's S columns (every S value is already in registers)
       float rowsum;
       if (!split) {
-        rowsum = exp_row<false>(s, sc2, nm2, t_s);
+        rowsum = exp_half<false>(s, sc2, nm2, t_s);
       } else if constexpr (BF16) {
-        rowsum = exp_row<true>(s, sc2, nm2, t_s);
+        rowsum = exp_half<true>(s, sc2, nm2, t_s);
       } else {
         rowsum = 0.f;
       }
       l = l * alpha + rowsum;
-      // O was accumulated against the old max: rescale it before PV(j) runs.
-      // PV(j-3) and earlier are complete (S(j) was issued after PV(j-3)
-      // completed); PV(j-2) and PV(j-1) may still be running: wait for
-      // PV(j-1) (the tensor core completes them in order).
+      // O_h was accumulated against the old max: rescale it before PV(j)
+      // runs.  PV(j-SB) and earlier are complete (S(j) was issued after
+      // PV(j-SB) completed); PV(j-1) may still be running: wait for it (the
+      // tensor core completes them in order).
       if (j > 0 && __any_sync(0xffffffffu, rescale)) {
         ok = wait_bar(br, p.status, br.pv_done((gg - 1u) % SB), ((gg - 1u) / SB) & 1u, kRoleSoftmax);
         if (!__all_sync(0xffffffffu, ok)) {
@@ -700,10 +742,10 @@ __device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t smem,
 #pragma unroll 1
         for (int c0 = 0; c0 < D; c0 += 32) {
           uint32_t o[32];
-          ptx::tmem_ld32(t_o + c0, o);
+          ptx::tmem_ld32(t_oh + c0, o);
 #pragma unroll
           for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-          ptx::tmem_st32(t_o + c0, o);
+          ptx::tmem_st32(t_oh + c0, o);
         }
       }
       ptx::tmem_st_wait();
@@ -725,24 +767,65 @@ __device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t smem,
     if (!__all_sync(0xffffffffu, ok)) return;
     o_phase ^= 1u;
     ptx::tc_fence_after();
+    // combine the halves: half b hands (m_b, l_b) to half a through shared
+    // memory; half a forms the final scales of O_a and O_b and the LSE and
+    // hands the scales back.  Half a's l is never 0 here: key 0 is visible to
+    // every row of a unit with n > 0.
+    float sa = 0.f, sb = 0.f;  // O = O_a * sa + O_b * sb
+    if (half == 1) {
+      ptx::st_shared_f32(xch, m);
+      ptx::st_shared_f32(xch + 4u, l);
+      ptx::mbar_arrive(br.xch_m());
+    } else {
+      ok = wait_bar(br, p.status, br.xch_m(), epi & 1u, kRoleEpilogue);
+    }
+    if (!__all_sync(0xffffffffu, ok)) return;
+    if (half == 0) {
+      const float mb = ptx::ld_shared_f32(xch);
+      const float lb = ptx::ld_shared_f32(xch + 4u);
+      const float mm = fmaxf(m, mb);
+      const float ea = ptx::ex2_approx(m - mm);
+      const float eb = (mb == -INFINITY) ? 0.f : ptx::ex2_approx(mb - mm);
+      const float ll = l * ea + lb * eb;
+      const float inv_l = 1.f / ll;
+      sa = ea * inv_l;
+      sb = eb * inv_l;
+      if (row_ok && p.lse != nullptr) p.lse[grow] = (mm + ptx::lg2_approx(ll)) * kLn2;
+      ptx::st_shared_f32(xch, sa);
+      ptx::st_shared_f32(xch + 4u, sb);
+      ptx::mbar_arrive(br.xch_s());
+    } else {
+      ok = wait_bar(br, p.status, br.xch_s(), epi & 1u, kRoleEpilogue);
+      if (!__all_sync(0xffffffffu, ok)) return;
+      sa = ptx::ld_shared_f32(xch);
+      sb = ptx::ld_shared_f32(xch + 4u);
+    }
     // staging tile: the V stage of this unit's last key tile (g counts V
     // tiles too); its PV has completed (o_full)
     const uint32_t vstage = (g - 1u) % C::kVStages;
     const uint32_t stage = smem + C::kOffV + vstage * C::kKVBytes;
-    // O / l as 16-bit pairs into the staging tile: 64-column slabs of 128-byte
-    // rows, the 16-byte chunk k of row r at chunk position k ^ (r % 8) (the
-    // 128-byte swizzle of the O tensor map)
-    const float inv_l = 1.f / l;
+    // O as 16-bit pairs into the staging tile, each half its D/2 columns:
+    // 64-column slabs of 128-byte rows, the 16-byte chunk k of row r at chunk
+    // position k ^ (r % 8) (the 128-byte swizzle of the O tensor map)
     const uint32_t stage_row = stage + static_cast<uint32_t>(lane_row) * 128u;
     const uint32_t rsw = static_cast<uint32_t>(lane_row) & 7u;
+    const uint64_t sa2 = ptx::f2_pack(sa, sa);
+    const uint64_t sb2 = ptx::f2_pack(sb, sb);
 #pragma unroll 1
-    for (int c0 = 0; c0 < D; c0 += 32) {
-      uint32_t o[32];
-      ptx::tmem_ld32(t_o + c0, o);
+    for (int c0 = half * (D / 2); c0 < (half + 1) * (D / 2); c0 += 32) {
+      uint32_t oa[32], ob[32];
+      ptx::tmem_ld32(t_oa + c0, oa);
+      ptx::tmem_ld32(t_ob + c0, ob);
       uint32_t h[16];
 #pragma unroll
-      for (int c = 0; c < 16; ++c)
-        h[c] = pack2<BF16>(__uint_as_float(o[2 * c]) * inv_l, __uint_as_float(o[2 * c + 1]) * inv_l);
+      for (int c = 0; c < 16; ++c) {
+        const uint64_t o2 = ptx::f2_fma(
+            ptx::f2_pack(__uint_as_float(oa[2 * c]), __uint_as_float(oa[2 * c + 1])), sa2,
+            ptx::f2_mul(ptx::f2_pack(__uint_as_float(ob[2 * c]), __uint_as_float(ob[2 * c + 1])), sb2));
+        float o0, o1;
+        ptx::f2_unpack(o2, o0, o1);
+        h[c] = pack2<BF16>(o0, o1);
+      }
       const uint32_t slab = stage_row + static_cast<uint32_t>(c0 / 64) * C::kSlabQ;
       const uint32_t k0 = static_cast<uint32_t>(c0 % 64) / 8u;
 #pragma unroll
@@ -763,7 +846,6 @@ __device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t smem,
       }
     }
     ++epi;
-    if (row_ok && p.lse != nullptr) p.lse[grow] = (m + ptx::lg2_approx(l)) * kLn2;
   }
 }
 
@@ -803,6 +885,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::mbar_init(br.o_full(), 1);
     ptx::mbar_init(br.drain(), 2);  // one commit from each issuer
     ptx::mbar_init(br.o_staged(), kSoftmaxThreads);
+    ptx::mbar_init(br.xch_m(), kSoftmaxThreads / 2);
+    ptx::mbar_init(br.xch_s(), kSoftmaxThreads / 2);
     ptx::st_shared_volatile(br.abort_word(), 0u);
     ptx::fence_barrier_init();
   }
@@ -829,7 +913,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kSWarp) {
     s_issuer_role<D, BF16>(p, br, smem, tmem);  // whole warp
   } else {
-    softmax_role<D, BF16>(p, br, smem, tmem, &tm_o);  // warps 0-3
+    softmax_role<D, BF16>(p, br, smem, tmem, &tm_o);  // warps 0-7
     // the last O stores read their staging tiles: finish before shared memory
     // goes (no stage needs releasing: the producer has no loads left)
     if (threadIdx.x == 0) ptx::bulk_wait_all();
