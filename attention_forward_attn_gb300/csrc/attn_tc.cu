@@ -456,12 +456,8 @@ __device__ void s_issuer_role(const KParams& p, const Bars<D>& br, uint32_t smem
     q_phase ^= 1u;
     for (int j = 0; j < n; ++j, ++g) {
       const uint32_t b = g % SB;
-      // buffer b held P(g-SB): wait until PV(g-SB) has read it
-      if (g >= SB && !__all_sync(0xffffffffu, wait_bar(br, p.status, br.pv_done(b),
-                                                       ((g - SB) / SB) & 1u, kRoleMma))) {
-        ok = false;
-        break;
-      }
+      // the K tile first: it normally landed long ago, and the wait for the
+      // buffer below is the one on the critical path
       const uint32_t sk = kit % C::kKStages;
       if (!__all_sync(0xffffffffu, wait_bar(br, p.status, br.k_full(sk),
                                             (kit / C::kKStages) & 1u, kRoleMma))) {
@@ -469,6 +465,12 @@ __device__ void s_issuer_role(const KParams& p, const Bars<D>& br, uint32_t smem
         break;
       }
       ++kit;
+      // buffer b held P(g-SB): wait until PV(g-SB) has read it
+      if (g >= SB && !__all_sync(0xffffffffu, wait_bar(br, p.status, br.pv_done(b),
+                                                       ((g - SB) / SB) & 1u, kRoleMma))) {
+        ok = false;
+        break;
+      }
       ptx::tc_fence_after();
       if (elect_one()) issue_qk<D, BF16>(tmem + C::col_s(b), q_desc, desc_add(k_desc0, sk * C::kKVBytes));
       __syncwarp();
@@ -671,6 +673,9 @@ __device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t smem,
     float m = -INFINITY;  // running max of this half's keys, log2 units (scaled)
     float l = 0.f;
     bool ok = true;
+    // S(gg) was seen complete by the look-ahead test of the previous step
+    // (the test is an acquire like a wait): no blocking wait needed
+    bool s_ready = false;
     for (int j = 0; j < n; ++j) {
       const uint32_t gg = g + static_cast<uint32_t>(j);
       const uint32_t b = gg % SB;
@@ -678,10 +683,12 @@ __device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t smem,
       // P format of this key tile: fp16 P, or the bf16 pair (split)
       if (j > 0 && (j & 31) == 0) fmask = v_fp16_mask<BF16>(p, z_kv, j, n);
       const bool split = BF16 && ((fmask >> (j & 31)) & 1u) == 0u;
-      ok = wait_bar(br, p.status, br.s_full(b), (gg / SB) & 1u, kRoleSoftmax);
-      if (!__all_sync(0xffffffffu, ok)) {
-        ok = false;
-        break;
+      if (!s_ready) {
+        ok = wait_bar(br, p.status, br.s_full(b), (gg / SB) & 1u, kRoleSoftmax);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
       }
       ptx::tc_fence_after();
       uint32_t s[BH];
@@ -716,6 +723,13 @@ __device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t smem,
         rescale = true;
       }
       const float neg_m = (m == -INFINITY) ? 0.f : -m;
+      // look ahead (non-blocking): has S(gg+1) completed?  Its answer is used
+      // at the next step, so the test's latency hides behind the exponentials.
+      // S(gg+1) may be the next unit's first tile: g counts every tile.  Only
+      // with three score buffers (D = 64), where the scores are normally
+      // ready; with two (D = 128) it measured slower.
+      if constexpr (SB > 2)
+        s_ready = __all_sync(0xffffffffu, ptx::mbar_test_wait(br.s_full((gg + 1u) % SB), ((gg + 1u) / SB) & 1u));
       const uint64_t sc2 = ptx::f2_pack(scale_log2, scale_log2);
       const uint64_t nm2 = ptx::f2_pack(neg_m, neg_m);
       // P over the half's S columns (every S value is already in registers)
