@@ -54,10 +54,10 @@ def _bind(path: str):
     i = ctypes.c_int
     i64 = ctypes.c_int64
     lib.oracle_attn_fwd_f64.argtypes = [p, p, p, p, p, i, i, i, i, i, i, ctypes.c_double,
-                                        i, p, p, i64, i]
+                                        i, p, p, i64, i64, p, i64, i]
     lib.oracle_attn_fwd_f64.restype = i
     lib.oracle_attn_fwd_u16.argtypes = [p, p, p, p, p, i, i, i, i, i, i, ctypes.c_double,
-                                        i, p, i, p, i64, i]
+                                        i, p, p, i64, i64, i, p, i64, i]
     lib.oracle_attn_fwd_u16.restype = i
     lib.oracle_decode.argtypes = [p, p, i64, i]
     lib.oracle_decode.restype = i
@@ -112,6 +112,20 @@ def _valid(valid_len, B):
     return vl
 
 
+def _mask(mask, B, Lq, Lk):
+    """(array, batch_stride, row_stride) of an explicit mask: None, or a
+    [B, Lq, Lk] / [1, Lq, Lk] / [Lq, Lk] array (nonzero keeps the position;
+    the last two are shared by every batch)."""
+    if mask is None:
+        return None, 0, 0
+    m = np.ascontiguousarray(np.asarray(mask) != 0, dtype=np.uint8)
+    if m.ndim == 2:
+        m = m[None]
+    if m.shape not in ((B, Lq, Lk), (1, Lq, Lk)):
+        raise ValueError("mask must be [B, Lq, Lk], [1, Lq, Lk] or [Lq, Lk]")
+    return m, (0 if m.shape[0] == 1 else Lq * Lk), Lk
+
+
 def _rows(rows):
     if rows is None:
         return None, 0
@@ -120,20 +134,22 @@ def _rows(rows):
 
 
 def attn_fwd_f64(q, k, v, sm_scale, causal=False, valid_len=None, rows=None, threads=0,
-                 _lib_override=None):
+                 _lib_override=None, mask=None):
     """Oracle on float64 inputs.
 
     q: [B, Hq, Lq, D]; k, v: [B, Hkv, Lk, D] (Lq = Lk is the pages' case; the
     causal mask compares absolute positions, key j visible to query i iff
     j <= i).  Returns (o, lse): o is [B, Hq, Lq, D] and lse [B*Hq, Lq] when
     ``rows`` is None, else o is [len(rows), D] and lse [len(rows)] for the
-    flat row indices r = (b*Hq + h_q)*Lq + i.
+    flat row indices r = (b*Hq + h_q)*Lq + i.  ``mask``: optional explicit
+    mask (see ``_mask``), intersected with the causal and padding masks.
     """
     q = np.ascontiguousarray(q, dtype=np.float64)
     k = np.ascontiguousarray(k, dtype=np.float64)
     v = np.ascontiguousarray(v, dtype=np.float64)
     B, Hq, Hkv, Lq, Lk, D = _shapes(q, k, v)
     vl = _valid(valid_len, B)
+    mk, msb, msr = _mask(mask, B, Lq, Lk)
     r, nr = _rows(rows)
     n_out = nr if r is not None else B * Hq * Lq
     o = np.empty((n_out, D), dtype=np.float64)
@@ -141,7 +157,7 @@ def attn_fwd_f64(q, k, v, sm_scale, causal=False, valid_len=None, rows=None, thr
     lib = _lib_override if _lib_override is not None else _load()
     rc = lib.oracle_attn_fwd_f64(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv,
                                  Lq, Lk, D, float(sm_scale), int(bool(causal)), _ptr(vl),
-                                 _ptr(r), nr, int(threads))
+                                 _ptr(mk), msb, msr, _ptr(r), nr, int(threads))
     if rc != 0:
         raise ValueError("oracle_attn_fwd_f64 failed with code %d" % rc)
     if r is None:
@@ -150,7 +166,7 @@ def attn_fwd_f64(q, k, v, sm_scale, causal=False, valid_len=None, rows=None, thr
 
 
 def attn_fwd_bits(q_bits, k_bits, v_bits, dtype, sm_scale, causal=False, valid_len=None,
-                  rows=None, threads=0):
+                  rows=None, threads=0, mask=None):
     """Oracle on raw fp16 (dtype=0) / bf16 (dtype=1) bit patterns (np.uint16 arrays).
 
     Same shapes and return convention as :func:`attn_fwd_f64`.
@@ -160,13 +176,14 @@ def attn_fwd_bits(q_bits, k_bits, v_bits, dtype, sm_scale, causal=False, valid_l
     v = np.ascontiguousarray(v_bits, dtype=np.uint16)
     B, Hq, Hkv, Lq, Lk, D = _shapes(q, k, v)
     vl = _valid(valid_len, B)
+    mk, msb, msr = _mask(mask, B, Lq, Lk)
     r, nr = _rows(rows)
     n_out = nr if r is not None else B * Hq * Lq
     o = np.empty((n_out, D), dtype=np.float64)
     lse = np.empty((n_out,), dtype=np.float64)
     rc = _load().oracle_attn_fwd_u16(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv,
                                      Lq, Lk, D, float(sm_scale), int(bool(causal)), _ptr(vl),
-                                     int(dtype), _ptr(r), nr, int(threads))
+                                     _ptr(mk), msb, msr, int(dtype), _ptr(r), nr, int(threads))
     if rc != 0:
         raise ValueError("oracle_attn_fwd_u16 failed with code %d" % rc)
     if r is None:

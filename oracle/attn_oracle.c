@@ -28,6 +28,13 @@
  * Head grouping (Triton-CUDA Attention page, "GQA"): h_kv = h_q // (Hq/Hkv),
  * integer division, never modulo.
  *
+ * Explicit mask ("masked multi head attention in CUDA", section 2.2: a
+ * [B, N, N] boolean matrix, or a float matrix of 0 for a kept and -inf for a
+ * removed position added to the scores -- the same set of kept positions):
+ * mask[b, i, j] == 0 removes key j from query i of batch b, for every head.
+ * All masks combine by intersection of their kept sets (the page's
+ * "combined mask").
+ *
  * Query and key lengths: the pages use one sequence length for Q, K and V.
  * Here Q has Lq rows and K/V have Lk rows (Lq = Lk is the pages' case); the
  * masks keep the pages' comparisons on absolute positions, so the causal
@@ -80,10 +87,18 @@ int oracle_decode(const uint16_t* in, double* out, int64_t n, int dtype) {
   return 0;
 }
 
+/* The explicit mask: element (b, i, j) at mask[b*batch_stride + i*row_stride + j]. */
+typedef struct {
+  const uint8_t* mask; /* NULL: no explicit mask */
+  int64_t batch_stride, row_stride;
+} oracle_mask_t;
+
 /* Is key j visible to query i of batch b? */
-static int key_visible(int64_t i, int64_t j, int b, int causal, const int32_t* valid_len) {
+static int key_visible(int64_t i, int64_t j, int b, int causal, const int32_t* valid_len,
+                       const oracle_mask_t* mk) {
   if (causal && j > i) return 0;
   if (valid_len != NULL && j >= (int64_t)valid_len[b]) return 0;
+  if (mk->mask != NULL && mk->mask[b * mk->batch_stride + i * mk->row_stride + j] == 0) return 0;
   return 1;
 }
 
@@ -93,12 +108,13 @@ static int key_visible(int64_t i, int64_t j, int b, int causal, const int32_t* v
  */
 static void one_row(const double* q_row, const double* k_head, const double* v_head,
                     int64_t i, int b, int Lk, int D, double sm_scale, int causal,
-                    const int32_t* valid_len, double* s, double* o_row, double* lse_out) {
+                    const int32_t* valid_len, const oracle_mask_t* mk, double* s, double* o_row,
+                    double* lse_out) {
   /* pass 1: scores of the visible keys and their maximum */
   double m = -INFINITY;
   int64_t n_visible = 0;
   for (int64_t j = 0; j < Lk; ++j) {
-    if (!key_visible(i, j, b, causal, valid_len)) continue;
+    if (!key_visible(i, j, b, causal, valid_len, mk)) continue;
     const double* k_row = k_head + j * (int64_t)D;
     double dot = 0.0;
     for (int d = 0; d < D; ++d) dot += q_row[d] * k_row[d];
@@ -114,14 +130,14 @@ static void one_row(const double* q_row, const double* k_head, const double* v_h
   /* pass 2: the normaliser l = sum_j exp(s_j - m); s_j is replaced by its weight */
   double l = 0.0;
   for (int64_t j = 0; j < Lk; ++j) {
-    if (!key_visible(i, j, b, causal, valid_len)) continue;
+    if (!key_visible(i, j, b, causal, valid_len, mk)) continue;
     s[j] = exp(s[j] - m);
     l += s[j];
   }
   /* pass 3: O = sum_j w_j v_j / l */
   for (int d = 0; d < D; ++d) o_row[d] = 0.0;
   for (int64_t j = 0; j < Lk; ++j) {
-    if (!key_visible(i, j, b, causal, valid_len)) continue;
+    if (!key_visible(i, j, b, causal, valid_len, mk)) continue;
     const double* v_row = v_head + j * (int64_t)D;
     for (int d = 0; d < D; ++d) o_row[d] += s[j] * v_row[d];
   }
@@ -140,7 +156,9 @@ static void one_row(const double* q_row, const double* k_head, const double* v_h
 int oracle_attn_fwd_f64(const double* q, const double* k, const double* v, double* o,
                         double* lse, int B, int Hq, int Hkv, int Lq, int Lk, int D,
                         double sm_scale, int causal, const int32_t* valid_len,
+                        const uint8_t* mask, int64_t mask_batch_stride, int64_t mask_row_stride,
                         const int64_t* rows, int64_t nrows, int threads) {
+  const oracle_mask_t mk = {mask, mask_batch_stride, mask_row_stride};
   if (B < 1 || Hq < 1 || Hkv < 1 || Lq < 1 || Lk < 1 || D < 1 || Hq % Hkv != 0) return 1;
   const int G = Hq / Hkv;
   const int64_t total = (int64_t)B * Hq * Lq;
@@ -173,7 +191,7 @@ int oracle_attn_fwd_f64(const double* q, const double* k, const double* v, doubl
       const double* q_row = q + r * (int64_t)D;
       const double* k_head = k + ((int64_t)b * Hkv + h_kv) * Lk * (int64_t)D;
       const double* v_head = v + ((int64_t)b * Hkv + h_kv) * Lk * (int64_t)D;
-      one_row(q_row, k_head, v_head, i, b, Lk, D, sm_scale, causal, valid_len, s,
+      one_row(q_row, k_head, v_head, i, b, Lk, D, sm_scale, causal, valid_len, &mk, s,
               o + n * (int64_t)D, lse + n);
     }
     free(s);
@@ -184,8 +202,9 @@ int oracle_attn_fwd_f64(const double* q, const double* k, const double* v, doubl
 /* Same as oracle_attn_fwd_f64, on raw fp16 (dtype 0) or bf16 (dtype 1) bits. */
 int oracle_attn_fwd_u16(const uint16_t* q, const uint16_t* k, const uint16_t* v, double* o,
                         double* lse, int B, int Hq, int Hkv, int Lq, int Lk, int D,
-                        double sm_scale, int causal, const int32_t* valid_len, int dtype,
-                        const int64_t* rows, int64_t nrows, int threads) {
+                        double sm_scale, int causal, const int32_t* valid_len,
+                        const uint8_t* mask, int64_t mask_batch_stride, int64_t mask_row_stride,
+                        int dtype, const int64_t* rows, int64_t nrows, int threads) {
   if (B < 1 || Hq < 1 || Hkv < 1 || Lq < 1 || Lk < 1 || D < 1 || Hq % Hkv != 0) return 1;
   if (dtype != 0 && dtype != 1) return 1;
   const int64_t nq = (int64_t)B * Hq * Lq * D;
@@ -199,7 +218,8 @@ int oracle_attn_fwd_u16(const uint16_t* q, const uint16_t* k, const uint16_t* v,
     oracle_decode(k, kd, nkv, dtype);
     oracle_decode(v, vd, nkv, dtype);
     rc = oracle_attn_fwd_f64(qd, kd, vd, o, lse, B, Hq, Hkv, Lq, Lk, D, sm_scale, causal,
-                             valid_len, rows, nrows, threads);
+                             valid_len, mask, mask_batch_stride, mask_row_stride, rows, nrows,
+                             threads);
   }
   free(qd);
   free(kd);

@@ -37,7 +37,7 @@ def _fwd_default(*a, **kw):
 
 # ---------------------------------------------------------------- references
 
-def brute_force(q, k, v, sm_scale, causal, valid_len):
+def brute_force(q, k, v, sm_scale, causal, valid_len, mask=None):
     """Attention by its definition at 50 digits: explicit mask, no max shift."""
     mpmath = pytest.importorskip("mpmath")
     mp = mpmath.mp
@@ -53,6 +53,7 @@ def brute_force(q, k, v, sm_scale, causal, valid_len):
             g = head_of[h]
             for i in range(Lq):
                 keep = [(not causal or i >= j) and (valid_len is None or j < valid_len[b])
+                        and (mask is None or mask[b if mask.shape[0] > 1 else 0][i][j] != 0)
                         for j in range(Lk)]
                 if not any(keep):
                     LSE[b * Hq + h, i] = -math.inf
@@ -70,8 +71,10 @@ def brute_force(q, k, v, sm_scale, causal, valid_len):
     return O, LSE
 
 
-def explicit_mask(B, Lq, Lk, causal, valid_len):
+def explicit_mask(B, Lq, Lk, causal, valid_len, mask=None):
     m = torch.ones(B, 1, Lq, Lk, dtype=torch.bool)
+    if mask is not None:
+        m &= torch.from_numpy(np.asarray(mask) != 0).reshape(-1, 1, Lq, Lk)
     if causal:
         # torch.tril keeps column j <= row i of the [Lq, Lk] matrix: top-left
         m &= torch.tril(torch.ones(Lq, Lk, dtype=torch.bool))
@@ -82,14 +85,14 @@ def explicit_mask(B, Lq, Lk, causal, valid_len):
     return m
 
 
-def torch_reference(q, k, v, sm_scale, causal, valid_len):
+def torch_reference(q, k, v, sm_scale, causal, valid_len, mask=None):
     qt, kt, vt = (torch.from_numpy(np.ascontiguousarray(x)) for x in (q, k, v))
     B, Hq, Lq, D = qt.shape
     Lk = kt.shape[2]
     G = Hq // kt.shape[1]
     kt = kt.repeat_interleave(G, dim=1)
     vt = vt.repeat_interleave(G, dim=1)
-    mask = explicit_mask(B, Lq, Lk, causal, valid_len)
+    mask = explicit_mask(B, Lq, Lk, causal, valid_len, mask)
     o = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=mask,
                                                          scale=sm_scale)
     scores = (qt @ kt.transpose(-1, -2)) * sm_scale
@@ -317,8 +320,64 @@ def pin_lengths(fwd):
                                                   lse_b.reshape(B, Hq, 5)], axis=2))
 
 
+def pin_explicit_mask(fwd):
+    """The explicit [B, Lq, Lk] mask: brute force, torch SDPA and the masks
+    it must reproduce exactly (all ones = none, tril = causal, key < valid_len
+    = padding, one mask shared by every batch)."""
+    rng = np.random.default_rng(8)
+    # brute force, combined with causal and padding, Lq != Lk, batch-broadcast
+    for (B, Hq, Hkv, Lq, Lk, D, causal, vl, shared) in [
+            (2, 2, 1, 6, 6, 3, False, None, False), (2, 4, 2, 7, 5, 4, True, [5, 3], False),
+            (1, 2, 2, 5, 8, 2, False, [7], True), (3, 2, 1, 4, 4, 5, True, None, True)]:
+        q, k, v = rand((B, Hq, Lq, D), rng, 1.5), rand((B, Hkv, Lk, D), rng), rand((B, Hkv, Lk, D), rng)
+        mk = (rng.random((1 if shared else B, Lq, Lk)) < 0.6).astype(np.uint8)
+        mk[0, 1, :] = 0  # one fully masked row
+        o, lse = fwd(q, k, v, 0.7, causal=causal, valid_len=vl, mask=mk)
+        o_ref, lse_ref = brute_force(q, k, v, 0.7, causal, vl, mk)
+        np.testing.assert_allclose(o, o_ref, rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(lse, lse_ref, rtol=1e-12, atol=1e-13)
+    # torch SDPA on medium shapes with random, block and empty-row masks
+    for (B, Hq, Hkv, Lq, Lk, D, causal, vl, dens) in [
+            (2, 4, 2, 33, 33, 16, False, None, 0.5), (2, 4, 1, 40, 57, 8, True, [50, 21], 0.2),
+            (3, 2, 2, 29, 29, 12, False, [29, 0, 11], 0.9)]:
+        q, k, v = rand((B, Hq, Lq, D), rng, 2.0), rand((B, Hkv, Lk, D), rng), rand((B, Hkv, Lk, D), rng)
+        mk = (rng.random((B, Lq, Lk)) < dens).astype(np.uint8)
+        mk[1, 3:9, :] = 0
+        o, lse = fwd(q, k, v, 0.3, causal=causal, valid_len=vl, mask=mk)
+        o_ref, lse_ref, empty = torch_reference(q, k, v, 0.3, causal, vl, mk)
+        keep = ~empty
+        np.testing.assert_allclose(o[keep], o_ref[keep], rtol=1e-11, atol=1e-12)
+        np.testing.assert_allclose(lse.reshape(B, Hq, Lq)[keep],
+                                   lse_ref.reshape(B, Hq, Lq)[keep], rtol=1e-12, atol=1e-12)
+        assert np.all(o[empty] == 0.0)
+        assert np.all(np.isneginf(lse.reshape(B, Hq, Lq)[empty]))
+    # masks that restate the implicit ones give identical results
+    B, Hq, Hkv, L, D = 2, 4, 2, 12, 6
+    q, k, v = rand((B, Hq, L, D), rng), rand((B, Hkv, L, D), rng), rand((B, Hkv, L, D), rng)
+    o0, l0 = fwd(q, k, v, 0.5)
+    o1, l1 = fwd(q, k, v, 0.5, mask=np.ones((B, L, L), np.uint8))
+    np.testing.assert_array_equal(o0, o1)
+    np.testing.assert_array_equal(l0, l1)
+    oc, lc = fwd(q, k, v, 0.5, causal=True)
+    om, lm = fwd(q, k, v, 0.5, mask=np.tril(np.ones((L, L), np.uint8)))
+    np.testing.assert_array_equal(oc, om)
+    np.testing.assert_array_equal(lc, lm)
+    vl = [7, 12]
+    op, lp = fwd(q, k, v, 0.5, valid_len=vl)
+    pm = np.stack([np.broadcast_to(np.arange(L) < x, (L, L)) for x in vl]).astype(np.uint8)
+    oq, lq = fwd(q, k, v, 0.5, mask=pm)
+    np.testing.assert_array_equal(op, oq)
+    np.testing.assert_array_equal(lp, lq)
+    # a shared mask equals the same mask repeated per batch
+    sm = (rng.random((L, L)) < 0.5).astype(np.uint8)
+    o2, l2 = fwd(q, k, v, 0.5, causal=True, mask=sm)
+    o3, l3 = fwd(q, k, v, 0.5, causal=True, mask=np.stack([sm, sm]))
+    np.testing.assert_array_equal(o2, o3)
+    np.testing.assert_array_equal(l2, l3)
+
+
 PINS = [pin_brute_force, pin_torch_sdpa, pin_golden, pin_invariants, pin_closed_forms,
-        pin_lengths]
+        pin_lengths, pin_explicit_mask]
 
 
 # ---------------------------------------------------------------- the tests
@@ -392,6 +451,11 @@ MUTANTS = {
     "key_head_stride_from_query_length": ("* Lk * (int64_t)D;", "* Lq * (int64_t)D;"),
     "row_split_by_key_length": ("const int64_t i = r % Lq;", "const int64_t i = r % Lk;"),
     "padding_on_query_index": ("j >= (int64_t)valid_len[b]", "i >= (int64_t)valid_len[b]"),
+    "mask_ignored": ("mk->mask[b * mk->batch_stride + i * mk->row_stride + j] == 0) return 0;",
+                     "mk->mask[b * mk->batch_stride + i * mk->row_stride + j] == 2) return 0;"),
+    "mask_row_off_by_one": ("mk->mask[b * mk->batch_stride + i * mk->row_stride + j]",
+                            "mk->mask[b * mk->batch_stride + (i > 0 ? i - 1 : 0) * mk->row_stride + j]"),
+    "mask_batch_ignored": ("mk->mask[b * mk->batch_stride + i", "mk->mask[0 * mk->batch_stride + i"),
     "log2_lse": ("*lse_out = m + log(l);", "*lse_out = m + log2(l);"),
     "lse_without_max": ("*lse_out = m + log(l);", "*lse_out = log(l);"),
     "no_normalisation": ("for (int d = 0; d < D; ++d) o_row[d] /= l;", ""),
