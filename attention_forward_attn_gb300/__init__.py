@@ -6,9 +6,10 @@ binding: argument marshalling only.  The library is loaded on first use and a
 missing or unbuilt library is an error, never a fallback.
 """
 from .binding import (ATTN_BF16, ATTN_F16, ATTN_OK, AttnError, attn_fwd, attn_fwd_host,
-                      attn_fwd_strided, declared_symbols, fwd_raw, fwd_strided_raw, host_plan,
-                      lib_path, load, query, shutdown, status, strerror)
+                      attn_fwd_strided, declared_symbols, fwd_masked_raw, fwd_raw,
+                      fwd_strided_raw, host_plan, lib_path, load, query, shutdown, status,
+                      strerror)
 
 __all__ = ["ATTN_BF16", "ATTN_F16", "ATTN_OK", "AttnError", "attn_fwd", "attn_fwd_host",
-           "attn_fwd_strided", "declared_symbols", "fwd_raw", "fwd_strided_raw", "host_plan",
-           "lib_path", "load", "query", "shutdown", "status", "strerror"]
+           "attn_fwd_strided", "declared_symbols", "fwd_masked_raw", "fwd_raw", "fwd_strided_raw",
+           "host_plan", "lib_path", "load", "query", "shutdown", "status", "strerror"]

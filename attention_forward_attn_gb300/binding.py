@@ -91,6 +91,10 @@ def load():
             lib.attn_fwd_strided.argtypes = [p, sp, p, sp, p, sp, p, sp, p, i, i, i, i, i, i,
                                              ctypes.c_float, i, p, i, p]
             lib.attn_fwd_strided.restype = i
+            i64 = ctypes.c_int64
+            lib.attn_fwd_masked.argtypes = [p, sp, p, sp, p, sp, p, sp, p, i, i, i, i, i, i,
+                                            ctypes.c_float, i, p, p, i64, i64, i, p]
+            lib.attn_fwd_masked.restype = i
             lib.attn_host_plan.argtypes = [i, i, i, i, i, i, ctypes.POINTER(Chunk), i,
                                            ctypes.POINTER(ctypes.c_int)]
             lib.attn_host_plan.restype = i
@@ -155,6 +159,18 @@ def fwd_strided_raw(q_ptr, q_strides, k_ptr, k_strides, v_ptr, v_strides, o_ptr,
         _strides_arg(v_strides), o_ptr, _strides_arg(o_strides), lse_ptr, int(B), int(Hq),
         int(Hkv), int(Lq), int(Lk), int(D), float(sm_scale), int(causal), valid_len_ptr,
         int(dtype), stream))
+
+
+def fwd_masked_raw(q_ptr, q_strides, k_ptr, k_strides, v_ptr, v_strides, o_ptr, o_strides,
+                   lse_ptr, B, Hq, Hkv, Lq, Lk, D, sm_scale, causal, valid_len_ptr, mask_ptr,
+                   mask_batch_stride, mask_row_stride, dtype, stream) -> int:
+    """Call attn_fwd_masked with raw integer pointers (strides as in
+    fwd_strided_raw); returns the status."""
+    return int(load().attn_fwd_masked(
+        q_ptr, _strides_arg(q_strides), k_ptr, _strides_arg(k_strides), v_ptr,
+        _strides_arg(v_strides), o_ptr, _strides_arg(o_strides), lse_ptr, int(B), int(Hq),
+        int(Hkv), int(Lq), int(Lk), int(D), float(sm_scale), int(causal), valid_len_ptr, mask_ptr,
+        int(mask_batch_stride), int(mask_row_stride), int(dtype), stream))
 
 
 def status(stream=None):
@@ -314,7 +330,7 @@ def attn_fwd_host(q, k, v, *, causal=False, sm_scale=None, valid_len=None, out=N
 
 
 def attn_fwd_strided(q, k, v, *, causal=False, sm_scale=None, valid_len=None, out=None, lse=None,
-                     return_lse=True, stream=None):
+                     return_lse=True, stream=None, mask=None):
     """Fused attention forward on strided CUDA tensors through attn_fwd_strided.
 
     q: [B, Hq, Lq, D]; k, v: [B, Hkv, Lk, D] -- any views whose last
@@ -322,8 +338,10 @@ def attn_fwd_strided(q, k, v, *, causal=False, sm_scale=None, valid_len=None, ou
     elements, e.g. ``x.transpose(1, 2)`` of a [B, L, H, D] tensor or slices of
     a packed QKV tensor; no copy is made.  Lq may differ from Lk (the causal
     mask keeps key j <= query i).  out: optional [B, Hq, Lq, D] view to write
-    (default: ``torch.empty_like(q)``).  Returns (o, lse) with lse float32
-    [B*Hq, Lq].
+    (default: ``torch.empty_like(q)``).  mask: optional explicit boolean
+    mask, a bool/uint8 CUDA tensor [B, Lq, Lk] or [Lq, Lk] (shared by every
+    batch) whose last dimension is contiguous (attn_fwd_masked).  Returns
+    (o, lse) with lse float32 [B*Hq, Lq].
     """
     import torch
     for name, t in (("q", q), ("k", k), ("v", v)):
@@ -350,10 +368,26 @@ def attn_fwd_strided(q, k, v, *, causal=False, sm_scale=None, valid_len=None, ou
         if valid_len.dtype != torch.int32 or not valid_len.is_cuda or valid_len.numel() != B:
             raise ValueError("valid_len must be an int32 CUDA tensor of B elements")
         vl_ptr = valid_len.data_ptr()
-    st = fwd_strided_raw(q.data_ptr(), q.stride()[:3], k.data_ptr(), k.stride()[:3], v.data_ptr(),
-                         v.stride()[:3], out.data_ptr(), out.stride()[:3],
-                         lse.data_ptr() if return_lse else None, B, Hq, Hkv, Lq, Lk, D, sm_scale,
-                         int(bool(causal)), vl_ptr, _dtype_code(q), _stream_handle(stream))
+    if mask is None:
+        st = fwd_strided_raw(q.data_ptr(), q.stride()[:3], k.data_ptr(), k.stride()[:3],
+                             v.data_ptr(), v.stride()[:3], out.data_ptr(), out.stride()[:3],
+                             lse.data_ptr() if return_lse else None, B, Hq, Hkv, Lq, Lk, D,
+                             sm_scale, int(bool(causal)), vl_ptr, _dtype_code(q),
+                             _stream_handle(stream))
+    else:
+        if mask.dtype not in (torch.bool, torch.uint8) or not mask.is_cuda:
+            raise ValueError("mask must be a bool or uint8 CUDA tensor")
+        if mask.dim() == 2:
+            mask = mask.unsqueeze(0)
+        if (mask.dim() != 3 or mask.shape[1:] != (Lq, Lk) or mask.shape[0] not in (1, B)
+                or (Lk > 1 and mask.stride(2) != 1)):
+            raise ValueError("mask must be [B, Lq, Lk] or [Lq, Lk] with a contiguous last dimension")
+        msb = 0 if mask.shape[0] == 1 else mask.stride(0)
+        st = fwd_masked_raw(q.data_ptr(), q.stride()[:3], k.data_ptr(), k.stride()[:3],
+                            v.data_ptr(), v.stride()[:3], out.data_ptr(), out.stride()[:3],
+                            lse.data_ptr() if return_lse else None, B, Hq, Hkv, Lq, Lk, D,
+                            sm_scale, int(bool(causal)), vl_ptr, mask.data_ptr(), msb,
+                            mask.stride(1), _dtype_code(q), _stream_handle(stream))
     if st != ATTN_OK:
-        raise AttnError(st, "attn_fwd_strided")
+        raise AttnError(st, "attn_fwd_masked" if mask is not None else "attn_fwd_strided")
     return out, (lse if return_lse else None)

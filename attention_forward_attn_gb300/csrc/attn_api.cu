@@ -231,6 +231,11 @@ Problem make_problem(const void* q, const void* k, const void* v, void* o, float
   p.valid_len = valid_len;
   p.status = status;
   p.vflags = nullptr;
+  p.mask = nullptr;
+  p.mask_sb = p.mask_sr = 0;
+  p.mbits = nullptr;
+  p.mflags = nullptr;
+  p.mlast = nullptr;
   p.B = B;
   p.Hq = Hq;
   p.Hkv = Hkv;
@@ -262,27 +267,36 @@ attn_status_t run_tc(Problem& p, int dev, DeviceState* st) {
   CUtensorMap maps[5];
   attn_status_t s = attn::encode_problem_maps(p, maps);
   if (s != ATTN_OK) return s;
+  // one stream-ordered workspace: for bf16 the contiguous fp16 copy of V
+  // and its per-tile flags, then for an explicit mask its packed form
+  const int64_t v_ws = p.bf16 ? (attn::vconv_workspace_bytes(p) + 255) / 256 * 256 : 0;
+  const int64_t m_ws = p.mask != nullptr ? attn::mask_workspace_bytes(p) : 0;
   void* ws = nullptr;
-  if (p.bf16) {
-    // workspace: contiguous fp16 copy of V, then the per-tile flags
+  if (v_ws + m_ws > 0) {
     cudaMemPool_t pool = nullptr;
     if ((s = workspace_pool(dev, st, &pool)) != ATTN_OK) return s;
-    cudaError_t e = cudaMallocFromPoolAsync(&ws, static_cast<size_t>(attn::vconv_workspace_bytes(p)),
-                                            pool, p.stream);
+    cudaError_t e = cudaMallocFromPoolAsync(&ws, static_cast<size_t>(v_ws + m_ws), pool, p.stream);
     if (e != cudaSuccess) return cuda_fail(e);
-    const size_t v_bytes = static_cast<size_t>(p.B) * p.Hkv * p.Lk * p.D * 2;
-    int* flags = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + v_bytes);
-    s = encode_map(&maps[3], ws, p.B, p.Hkv, p.Lk, p.D, attn::contiguous_strides(p.Hkv, p.Lk, p.D),
-                   cfg.block_n, false);
-    if (s == ATTN_OK) {
-      e = attn::launch_vconv(p, ws, flags);
+    if (p.mask != nullptr) {
+      attn::mask_arrays(p, static_cast<uint8_t*>(ws) + v_ws);
+      e = attn::launch_mask_pack(p);
       if (e != cudaSuccess) s = cuda_fail(e);
+    }
+    if (s == ATTN_OK && p.bf16) {
+      const size_t v_bytes = static_cast<size_t>(p.B) * p.Hkv * p.Lk * p.D * 2;
+      int* flags = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + v_bytes);
+      s = encode_map(&maps[3], ws, p.B, p.Hkv, p.Lk, p.D,
+                     attn::contiguous_strides(p.Hkv, p.Lk, p.D), cfg.block_n, false);
+      if (s == ATTN_OK) {
+        e = attn::launch_vconv(p, ws, flags);
+        if (e != cudaSuccess) s = cuda_fail(e);
+      }
+      p.vflags = flags;
     }
     if (s != ATTN_OK) {
       cudaFreeAsync(ws, p.stream);
       return s;
     }
-    p.vflags = flags;
   }
   cudaError_t e = attn::launch_tc(p, maps, st->num_sms);
   if (ws != nullptr) {
@@ -355,13 +369,14 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
   return run_tc(p, dev, st);
 }
 
-attn_status_t attn_fwd_strided(const void* q, const attn_strides_t* q_strides, const void* k,
-                               const attn_strides_t* k_strides, const void* v,
-                               const attn_strides_t* v_strides, void* o,
-                               const attn_strides_t* o_strides, float* lse, int B, int Hq,
-                               int Hkv, int Lq, int Lk, int D, float sm_scale, int causal,
-                               const int32_t* valid_len, attn_dtype_t dtype,
-                               attn_stream_t stream) {
+attn_status_t attn_fwd_masked(const void* q, const attn_strides_t* q_strides, const void* k,
+                              const attn_strides_t* k_strides, const void* v,
+                              const attn_strides_t* v_strides, void* o,
+                              const attn_strides_t* o_strides, float* lse, int B, int Hq, int Hkv,
+                              int Lq, int Lk, int D, float sm_scale, int causal,
+                              const int32_t* valid_len, const uint8_t* mask,
+                              int64_t mask_batch_stride, int64_t mask_row_stride,
+                              attn_dtype_t dtype, attn_stream_t stream) {
   // attn_fwd's checks with L = Lq, then the key length
   attn_status_t s =
       validate(q, k, v, o, lse, B, Hq, Hkv, Lq, D, sm_scale, causal, valid_len, dtype);
@@ -373,6 +388,11 @@ attn_status_t attn_fwd_strided(const void* q, const attn_strides_t* q_strides, c
   if ((s = strides_of(v_strides, B, Hkv, Lk, D, &sv)) != ATTN_OK) return s;
   if ((s = strides_of(o_strides, B, Hq, Lq, D, &so)) != ATTN_OK) return s;
   if (!no_self_overlap(so, B, Hq, Lq, D)) return ATTN_ERR_STRIDE;
+  if (mask != nullptr && (mask_batch_stride < 0 || mask_row_stride < 0)) return ATTN_ERR_STRIDE;
+  // the mask pre-pass runs one CTA per (b, 128-row block, 128-key tile)
+  if (mask != nullptr &&
+      static_cast<int64_t>(B) * ((Lq + 127) / 128) * ((Lk + 127) / 128) > INT32_MAX)
+    return ATTN_ERR_SHAPE;
   int dev = 0;
   DeviceState* st = nullptr;
   s = device_state(&dev, &st);
@@ -384,7 +404,21 @@ attn_status_t attn_fwd_strided(const void* q, const attn_strides_t* q_strides, c
   p.sk = sk;
   p.sv = sv;
   p.so = so;
+  p.mask = mask;
+  p.mask_sb = mask_batch_stride;
+  p.mask_sr = mask_row_stride;
   return run_tc(p, dev, st);
+}
+
+attn_status_t attn_fwd_strided(const void* q, const attn_strides_t* q_strides, const void* k,
+                               const attn_strides_t* k_strides, const void* v,
+                               const attn_strides_t* v_strides, void* o,
+                               const attn_strides_t* o_strides, float* lse, int B, int Hq,
+                               int Hkv, int Lq, int Lk, int D, float sm_scale, int causal,
+                               const int32_t* valid_len, attn_dtype_t dtype,
+                               attn_stream_t stream) {
+  return attn_fwd_masked(q, q_strides, k, k_strides, v, v_strides, o, o_strides, lse, B, Hq, Hkv,
+                         Lq, Lk, D, sm_scale, causal, valid_len, nullptr, 0, 0, dtype, stream);
 }
 
 attn_status_t attn_fwd_simt(const void* q, const void* k, const void* v, void* o, float* lse,

@@ -42,6 +42,13 @@ struct Problem {
   // bf16: per (b*Hkv + h, 128-key tile) flag from the V pre-pass (1 = exact
   // fp16 copy of the tile exists); null = no copy (every tile split)
   const int* vflags;
+  // explicit mask (null: none): the caller's bytes, and the packed form made
+  // by the mask pre-pass (attn_mask.cu)
+  const uint8_t* mask;
+  int64_t mask_sb, mask_sr;  // element strides of its batch (0: shared) and rows
+  const uint32_t* mbits;     // [B, Lq, n_kt, 4] words: bit c of word w = key 128t + 32w + c
+  const uint8_t* mflags;     // [B, n_mb, n_kt]: 0 no visible key, 1 all visible, 2 partial
+  const int* mlast;          // [B, n_mb]: last key tile with a visible key, or -1
   int B, Hq, Hkv;
   int Lq, Lk;              // query rows, key/value rows per head
   int D;
@@ -74,6 +81,13 @@ cudaError_t launch_tc(const Problem& p, const CUtensorMap* maps, int num_sms);
 // V, then one int flag per (b*Hkv + h, 128-key tile)), and its launch.
 int64_t vconv_workspace_bytes(const Problem& p);
 cudaError_t launch_vconv(const Problem& p, void* v16, int* flags);
+
+// Explicit-mask pre-pass (attn_mask.cu): bytes of its workspace for p, and
+// its launch (clears mlast first).  The workspace holds mbits, mflags and
+// mlast in that order; mask_arrays sets the three pointers of p into it.
+int64_t mask_workspace_bytes(const Problem& p);
+void mask_arrays(Problem& p, void* ws);
+cudaError_t launch_mask_pack(const Problem& p);
 
 // SIMT cross-check forward.
 cudaError_t launch_simt(const Problem& p);

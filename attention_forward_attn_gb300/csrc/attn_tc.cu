@@ -158,6 +158,10 @@ struct KParams {
   // bf16 only: per (b, h_kv, 128-key tile) 1 = the fp16 copy of the V tile is
   // exact, 0 = use the bf16 tile; null = no fp16 copy exists
   const int* vflags;
+  // explicit mask, packed by the pre-pass (null: none); see attn_mask.cu
+  const uint32_t* mbits;
+  const uint8_t* mflags;
+  const int* mlast;
   int n_kt;     // 128-key tiles per (b, h_kv)
   int B, Hq, Hkv, G;
   int Lq, Lk;   // query rows, key/value rows per head
@@ -170,8 +174,10 @@ struct KParams {
 };
 
 struct Unit {
-  int bh, b, hq, hkv, m0, kv_len;
-  int n;  // key tiles the query tile visits (0: no visible key)
+  int bh, b, hq, hkv, mb, m0, kv_len;
+  int n;     // key tiles in range of the causal and padding masks
+  int last;  // last key tile the unit visits (-1: none; with an explicit mask,
+             // tiles without a kept position are skipped)
 };
 
 // Units are ordered so that causal work runs heaviest-first (last row blocks
@@ -208,7 +214,28 @@ __device__ __forceinline__ Unit decode_unit(const KParams& p, int u) {
   w.kv_len = kv;
   const int hi = p.causal ? min(kv, w.m0 + BM) : kv;
   w.n = (hi + BN - 1) / BN;
+  w.mb = mb;
+  w.last = w.n - 1;
+  if (p.mflags != nullptr && w.last >= 0) {
+    const int64_t f0 = (static_cast<int64_t>(w.b) * p.n_mb + mb) * p.n_kt;
+    w.last = min(w.last, __ldg(p.mlast + static_cast<int64_t>(w.b) * p.n_mb + mb));
+    while (w.last >= 0 && __ldg(p.mflags + f0 + w.last) == 0) --w.last;
+  }
   return w;
+}
+
+// Explicit-mask flag of key tile j of unit w (0 none kept, 1 all, 2 partial);
+// 1 without an explicit mask.
+__device__ __forceinline__ int tile_flag(const KParams& p, const Unit& w, int j) {
+  if (p.mflags == nullptr) return 1;
+  return __ldg(p.mflags + (static_cast<int64_t>(w.b) * p.n_mb + w.mb) * p.n_kt + j);
+}
+
+// The first key tile >= j that unit w visits, or w.last + 1.  Every role
+// walks the same tiles in the same order.
+__device__ __forceinline__ int next_tile(const KParams& p, const Unit& w, int j) {
+  while (j <= w.last && tile_flag(p, w, j) == 0) ++j;
+  return j;
 }
 
 // Bounded mbarrier wait.  False: timed out (recorded) or another role aborted.
@@ -292,7 +319,7 @@ __device__ void producer_role(const KParams& p, const Bars<D>& br, uint32_t smem
   bool ok = true;
 
   // One K or V tile into the next slot of its ring.
-  auto load_kv = [&](bool is_v, int j, const Unit& w, int z_kv) -> bool {
+  auto load_kv = [&](bool is_v, int j, const Unit& w, int z_kv) -> bool {  // tile j of unit w
     uint32_t& it = is_v ? vit : kit;
     const uint32_t ns = is_v ? C::kVStages : C::kKStages;
     const uint32_t s = it % ns;
@@ -323,8 +350,7 @@ __device__ void producer_role(const KParams& p, const Bars<D>& br, uint32_t smem
     const int u = unit_of(r);
     if (u >= p.n_units) continue;
     const Unit w = decode_unit(p, u);
-    const int n = w.n;
-    if (n == 0) continue;
+    if (w.last < 0) continue;
     const int z_kv = w.b * p.Hkv + w.hkv;
     // Q: the buffer is free once the previous unit's last score MMA completed
     if (!wait_bar(br, p.status, br.q_empty(), (q_loads & 1u) ^ 1u, kRoleProducer)) break;
@@ -334,12 +360,19 @@ __device__ void producer_role(const KParams& p, const Bars<D>& br, uint32_t smem
     for (int h = 0; h < C::kHalves; ++h)
       ptx::tma_load_4d_hint(smem + C::kOffQ + h * C::kSlabQ, tm_q, br.q_full(), h * 64, w.m0, w.hq,
                             w.b, pol_stream);
-    // issue order = consumption order: K_0 K_1 K_2 | V_0 K_3 | V_1 K_4 | ...
-    const int lead = n < C::kScoreBufs ? n : C::kScoreBufs;
-    for (int i = 0; ok && i < lead; ++i) ok = load_kv(false, i, w, z_kv);
-    for (int j = 0; ok && j < n; ++j) {
+    // issue order = consumption order over the visited tiles t_0 t_1 ...:
+    // K(t_0) .. K(t_SB-1) | V(t_0) K(t_SB) | V(t_1) K(t_SB+1) | ...
+    int kj = next_tile(p, w, 0);  // next tile whose K is loaded
+    for (int i = 0; ok && i < C::kScoreBufs && kj <= w.last; ++i) {
+      ok = load_kv(false, kj, w, z_kv);
+      kj = next_tile(p, w, kj + 1);
+    }
+    for (int j = next_tile(p, w, 0); ok && j <= w.last; j = next_tile(p, w, j + 1)) {
       ok = load_kv(true, j, w, z_kv);
-      if (ok && j + C::kScoreBufs < n) ok = load_kv(false, j + C::kScoreBufs, w, z_kv);
+      if (ok && kj <= w.last) {
+        ok = load_kv(false, kj, w, z_kv);
+        kj = next_tile(p, w, kj + 1);
+      }
     }
   }
   // Never leave with a copy in flight: wait (bounded) for the last load of
@@ -450,11 +483,10 @@ __device__ void s_issuer_role(const KParams& p, const Bars<D>& br, uint32_t smem
     const int u = unit_of(r);
     if (u >= p.n_units) continue;
     const Unit w = decode_unit(p, u);
-    const int n = w.n;
-    if (n == 0) continue;
+    if (w.last < 0) continue;
     if (!__all_sync(0xffffffffu, wait_bar(br, p.status, br.q_full(), q_phase, kRoleMma))) break;
     q_phase ^= 1u;
-    for (int j = 0; j < n; ++j, ++g) {
+    for (int j = next_tile(p, w, 0); j <= w.last; j = next_tile(p, w, j + 1), ++g) {
       const uint32_t b = g % SB;
       // the K tile first: it normally landed long ago, and the wait for the
       // buffer below is the one on the critical path
@@ -476,7 +508,7 @@ __device__ void s_issuer_role(const KParams& p, const Bars<D>& br, uint32_t smem
       __syncwarp();
       commit_one(br.s_full(b));
       commit_one(br.k_empty(sk));
-      if (j == n - 1) commit_one(br.q_empty());  // Q is free once its last S completes
+      if (j == w.last) commit_one(br.q_empty());  // Q is free once its last S completes
     }
   }
   // Every MMA issued by this warp completes before TMEM is released.
@@ -502,12 +534,16 @@ __device__ void pv_issuer_role(const KParams& p, const Bars<D>& br, uint32_t sme
     const int u = unit_of(r);
     if (u >= p.n_units) continue;
     const Unit w = decode_unit(p, u);
-    const int n = w.n;
-    if (n == 0) continue;
+    if (w.last < 0) continue;
     const int z_kv = w.b * p.Hkv + w.hkv;
     uint32_t fmask = 0;
-    for (int j = 0; j < n; ++j, ++g) {
-      if ((j & 31) == 0) fmask = v_fp16_mask<BF16>(p, z_kv, j, n);
+    int fchunk = -1;  // 32-tile chunk fmask holds
+    bool first = true;
+    for (int j = next_tile(p, w, 0); j <= w.last; j = next_tile(p, w, j + 1), ++g) {
+      if ((j >> 5) != fchunk) {
+        fchunk = j >> 5;
+        fmask = v_fp16_mask<BF16>(p, z_kv, j & ~31, w.n);
+      }
       const uint32_t b = g % SB;
       const uint32_t sv = vit % C::kVStages;
       if (!__all_sync(0xffffffffu,
@@ -525,12 +561,13 @@ __device__ void pv_issuer_role(const KParams& p, const Bars<D>& br, uint32_t sme
       }
       ptx::tc_fence_after();
       if (elect_one())
-        issue_pv<D>(t_oa, t_ob, tmem + C::col_s(b), desc_add(v_desc0, sv * C::kKVBytes), j > 0,
+        issue_pv<D>(t_oa, t_ob, tmem + C::col_s(b), desc_add(v_desc0, sv * C::kKVBytes), !first,
                     split);
       __syncwarp();
+      first = false;
       commit_one(br.pv_done(b));
       // the unit's last V stage is released by the epilogue (it stages O)
-      if (j == n - 1) {
+      if (j == w.last) {
         commit_one(br.o_full());
       } else {
         commit_one(br.v_empty(sv));
@@ -652,8 +689,7 @@ __device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t smem,
       const int vl = p.valid_len[w.b];
       if (vl < 0 || vl > p.Lk) atomicOr(p.status, kStatusValidLenClamped);
     }
-    const int n = w.n;
-    if (n == 0) {  // no visible key: O = 0, LSE = -inf (written by half a)
+    if (w.last < 0) {  // no visible key: O = 0, LSE = -inf (written by half a)
       if (row_ok && half == 0) {
         // rows of O are d_o elements long (D = 16 and 32 run the D = 64 instance)
         const int64_t orow = w.b * p.o_sb + w.hq * p.o_sh + row * p.o_sl;
@@ -676,13 +712,25 @@ __device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t smem,
     // S(gg) was seen complete by the look-ahead test of the previous step
     // (the test is an acquire like a wait): no blocking wait needed
     bool s_ready = false;
-    for (int j = 0; j < n; ++j) {
-      const uint32_t gg = g + static_cast<uint32_t>(j);
+    int fchunk = 0;     // 32-tile chunk fmask holds
+    uint32_t cnt = 0;   // key tiles of this unit visited so far
+    for (int j = next_tile(p, w, 0); j <= w.last; j = next_tile(p, w, j + 1), ++cnt) {
+      const uint32_t gg = g + cnt;
       const uint32_t b = gg % SB;
       const uint32_t t_s = tmem + lane_addr + C::col_s(b) + static_cast<uint32_t>(half * BH);
       // P format of this key tile: fp16 P, or the bf16 pair (split)
-      if (j > 0 && (j & 31) == 0) fmask = v_fp16_mask<BF16>(p, z_kv, j, n);
+      if ((j >> 5) != fchunk) {
+        fchunk = j >> 5;
+        fmask = v_fp16_mask<BF16>(p, z_kv, j & ~31, w.n);
+      }
       const bool split = BF16 && ((fmask >> (j & 31)) & 1u) == 0u;
+      // explicit mask: this row's 64 bits of the half tile when the tile is
+      // partial (loaded before the wait, to hide its latency)
+      const bool partial = tile_flag(p, w, j) == 2;
+      uint2 keep = make_uint2(0xFFFFFFFFu, 0xFFFFFFFFu);
+      if (partial && row_ok)
+        keep = __ldg(reinterpret_cast<const uint2*>(
+            p.mbits + ((static_cast<int64_t>(w.b) * p.Lq + row) * p.n_kt + j) * 4 + half * 2));
       if (!s_ready) {
         ok = wait_bar(br, p.status, br.s_full(b), (gg / SB) & 1u, kRoleSoftmax);
         if (!__all_sync(0xffffffffu, ok)) {
@@ -694,15 +742,19 @@ __device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t smem,
       uint32_t s[BH];
       ptx::tmem_ld64(t_s, s);
       const int n0 = j * BN + half * BH;  // key of column 0 of this half
-      const bool masked = (n0 + BH > w.kv_len) || (p.causal && n0 + BH - 1 > w.m0);
+      const bool masked = partial || (n0 + BH > w.kv_len) || (p.causal && n0 + BH - 1 > w.m0);
       const int c_lim = key_lim - n0;  // columns c < c_lim are visible
-      // Boundary tiles only: invisible scores become -inf, so the max and the
-      // exponentials below are the same code for every tile (one copy of the
-      // unrolled loops keeps the hot code small); exp2(-inf * scale - m) = 0
-      // because the scale is > 0 (a zero sm_scale arrives as FLT_MIN).
+      // Boundary and partially masked tiles only: invisible scores become
+      // -inf, so the max and the exponentials below are the same code for
+      // every tile (one copy of the unrolled loops keeps the hot code small);
+      // exp2(-inf * scale - m) = 0 because the scale is > 0 (a zero sm_scale
+      // arrives as FLT_MIN).
       if (masked) {
 #pragma unroll
-        for (int c = 0; c < BH; ++c) s[c] = (c < c_lim) ? s[c] : 0xFF800000u;
+        for (int c = 0; c < BH; ++c) {
+          const uint32_t bit = ((c < 32 ? keep.x : keep.y) >> (c & 31)) & 1u;
+          s[c] = (c < c_lim && bit != 0u) ? s[c] : 0xFF800000u;
+        }
       }
       // max of the half row: 8 independent chains of 3-input maxima
       float mxk[8];
@@ -746,7 +798,7 @@ __device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t smem,
       // runs.  PV(j-SB) and earlier are complete (S(j) was issued after
       // PV(j-SB) completed); PV(j-1) may still be running: wait for it (the
       // tensor core completes them in order).
-      if (j > 0 && __any_sync(0xffffffffu, rescale)) {
+      if (cnt > 0 && __any_sync(0xffffffffu, rescale)) {
         ok = wait_bar(br, p.status, br.pv_done((gg - 1u) % SB), ((gg - 1u) / SB) & 1u, kRoleSoftmax);
         if (!__all_sync(0xffffffffu, ok)) {
           ok = false;
@@ -773,7 +825,7 @@ __device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t smem,
         pending_stage = kNoStage;
       }
     }
-    g += static_cast<uint32_t>(n);
+    g += cnt;
     if (!ok) return;
     decode_ahead();  // while the last P.V runs
     // epilogue
@@ -783,8 +835,7 @@ __device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t smem,
     ptx::tc_fence_after();
     // combine the halves: half b hands (m_b, l_b) to half a through shared
     // memory; half a forms the final scales of O_a and O_b and the LSE and
-    // hands the scales back.  Half a's l is never 0 here: key 0 is visible to
-    // every row of a unit with n > 0.
+    // hands the scales back.
     float sa = 0.f, sb = 0.f;  // O = O_a * sa + O_b * sb
     if (half == 1) {
       ptx::st_shared_f32(xch, m);
@@ -797,14 +848,16 @@ __device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t smem,
     if (half == 0) {
       const float mb = ptx::ld_shared_f32(xch);
       const float lb = ptx::ld_shared_f32(xch + 4u);
+      // a half (with an explicit mask: both) may have seen no visible key
       const float mm = fmaxf(m, mb);
-      const float ea = ptx::ex2_approx(m - mm);
+      const float ea = (m == -INFINITY) ? 0.f : ptx::ex2_approx(m - mm);
       const float eb = (mb == -INFINITY) ? 0.f : ptx::ex2_approx(mb - mm);
       const float ll = l * ea + lb * eb;
-      const float inv_l = 1.f / ll;
+      const float inv_l = ll > 0.f ? 1.f / ll : 0.f;  // no visible key: O = 0
       sa = ea * inv_l;
       sb = eb * inv_l;
-      if (row_ok && p.lse != nullptr) p.lse[grow] = (mm + ptx::lg2_approx(ll)) * kLn2;
+      if (row_ok && p.lse != nullptr)
+        p.lse[grow] = ll > 0.f ? (mm + ptx::lg2_approx(ll)) * kLn2 : -INFINITY;
       ptx::st_shared_f32(xch, sa);
       ptx::st_shared_f32(xch + 4u, sb);
       ptx::mbar_arrive(br.xch_s());
@@ -962,6 +1015,9 @@ cudaError_t launch_instance(const Problem& pr, const CUtensorMap* maps, int num_
   kp.valid_len = pr.valid_len;
   kp.status = pr.status;
   kp.vflags = pr.vflags;
+  kp.mbits = pr.mbits;
+  kp.mflags = pr.mflags;
+  kp.mlast = pr.mlast;
   kp.n_kt = (pr.Lk + BN - 1) / BN;
   kp.B = pr.B;
   kp.Hq = pr.Hq;

@@ -170,6 +170,42 @@ attn_status_t attn_fwd_strided(const void* q, const attn_strides_t* q_strides, c
                                attn_stream_t stream);
 
 /*
+ * attn_fwd_masked -- attn_fwd_strided with an explicit boolean mask.
+ *
+ * Defined by: "masked multi head attention in CUDA" (wzjinhao.cn) section
+ * 2.2: a padding mask given as a [B, N, N] boolean matrix, and the combined
+ * mask as a float matrix of 0 (kept) and -inf (removed) added to the scores --
+ * both name, per (b, query, key), whether the position takes part.  Here the
+ * mask is a byte matrix: key j is visible to query i of batch b iff
+ * mask[b*mask_batch_stride + i*mask_row_stride + j] != 0 (for every head) AND
+ * the causal and valid_len conditions of attn_fwd_strided hold.  A row with
+ * no visible key gets O = 0 and LSE = -inf.
+ *
+ * Arguments: as attn_fwd_strided, plus
+ *   mask               device pointer to uint8 values, any alignment; NULL
+ *                      makes the call identical to attn_fwd_strided.
+ *   mask_batch_stride  elements between batches (0: one [Lq, Lk] mask shared
+ *                      by every batch), >= 0.
+ *   mask_row_stride    elements between query rows, >= 0.
+ * The mask is read once per call by a pre-pass that packs it into bits and
+ * marks every (b, 128-row block, 128-key tile) as having no kept position
+ * (the attention kernel skips the tile: no loads, no tensor-core work), all
+ * positions kept (no masking work) or some (the bits are applied).
+ *
+ * Device memory: the per-call workspace of attn_fwd (bf16) plus
+ * B*Lq*ceil(Lk/128)*16 bytes of bits and a byte per tile.
+ * Errors: as attn_fwd_strided; negative mask strides give ATTN_ERR_STRIDE.
+ */
+attn_status_t attn_fwd_masked(const void* q, const attn_strides_t* q_strides, const void* k,
+                              const attn_strides_t* k_strides, const void* v,
+                              const attn_strides_t* v_strides, void* o,
+                              const attn_strides_t* o_strides, float* lse, int B, int Hq, int Hkv,
+                              int Lq, int Lk, int D, float sm_scale, int causal,
+                              const int32_t* valid_len, const uint8_t* mask,
+                              int64_t mask_batch_stride, int64_t mask_row_stride,
+                              attn_dtype_t dtype, attn_stream_t stream);
+
+/*
  * attn_fwd_simt -- the same operation, same arguments and same contract as
  * attn_fwd, computed by a plain SIMT kernel (one warp per query row, fp32
  * FMA dot products, online softmax over 32-key blocks; no tensor cores).

@@ -165,3 +165,39 @@ def test_strided_valid_arguments_need_a_device(lib, kw):
         pytest.skip("a GPU is present; covered by the gpu tests")
     st = _scall(**kw)
     assert binding.STATUS_NAMES[st] in ("ATTN_ERR_CUDA", "ATTN_ERR_ARCH")
+
+
+# ------------------------------------------------------------------ attn_fwd_masked
+
+def _mcall(**kw):
+    args = dict(q_ptr=A16, q_strides=None, k_ptr=A16, k_strides=None, v_ptr=A16, v_strides=None,
+                o_ptr=A16, o_strides=None, lse_ptr=None, B=2, Hq=4, Hkv=2, Lq=16, Lk=24, D=64,
+                sm_scale=0.125, causal=0, valid_len_ptr=None, mask_ptr=A16 + 3,
+                mask_batch_stride=16 * 24, mask_row_stride=24, dtype=attn.ATTN_BF16, stream=None)
+    args.update(kw)
+    return attn.fwd_masked_raw(**args)
+
+
+@pytest.mark.parametrize("kw, expected", [
+    (dict(mask_batch_stride=-1), "ATTN_ERR_STRIDE"),
+    (dict(mask_row_stride=-24), "ATTN_ERR_STRIDE"),
+    (dict(Lk=0), "ATTN_ERR_SHAPE"),
+    (dict(D=100), "ATTN_ERR_HEADDIM"),
+    (dict(q_ptr=None), "ATTN_ERR_NULL"),
+    (dict(o_strides=(4 * 16 * 64, 16 * 64, 16)), "ATTN_ERR_STRIDE"),
+    (dict(B=1 << 10, Hq=1, Hkv=1, Lq=1 << 20, Lk=1 << 20), "ATTN_ERR_SHAPE"),
+])
+def test_masked_invalid_arguments_rejected_on_host(lib, kw, expected):
+    assert binding.STATUS_NAMES[_mcall(**kw)] == expected
+
+
+@pytest.mark.parametrize("kw", [
+    dict(),                                     # unaligned mask pointer is fine (byte loads)
+    dict(mask_batch_stride=0),                  # one mask for every batch
+    dict(mask_ptr=None),                        # no mask: attn_fwd_strided
+])
+def test_masked_valid_arguments_need_a_device(lib, kw):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present; covered by the gpu tests")
+    assert binding.STATUS_NAMES[_mcall(**kw)] in ("ATTN_ERR_CUDA", "ATTN_ERR_ARCH")
