@@ -191,6 +191,7 @@ __device__ __forceinline__ int unit_of(int round) {
   return round * g + ((round & 1) ? (g - 1 - c) : c);
 }
 
+template <bool MASK>
 __device__ __forceinline__ Unit decode_unit(const KParams& p, int u) {
   Unit w;
   const int BH = p.B * p.Hq;
@@ -216,25 +217,36 @@ __device__ __forceinline__ Unit decode_unit(const KParams& p, int u) {
   w.n = (hi + BN - 1) / BN;
   w.mb = mb;
   w.last = w.n - 1;
-  if (p.mflags != nullptr && w.last >= 0) {
-    const int64_t f0 = (static_cast<int64_t>(w.b) * p.n_mb + mb) * p.n_kt;
-    w.last = min(w.last, __ldg(p.mlast + static_cast<int64_t>(w.b) * p.n_mb + mb));
-    while (w.last >= 0 && __ldg(p.mflags + f0 + w.last) == 0) --w.last;
+  if constexpr (MASK) {
+    if (w.last >= 0) {
+      const int64_t f0 = (static_cast<int64_t>(w.b) * p.n_mb + mb) * p.n_kt;
+      w.last = min(w.last, __ldg(p.mlast + static_cast<int64_t>(w.b) * p.n_mb + mb));
+      while (w.last >= 0 && __ldg(p.mflags + f0 + w.last) == 0) --w.last;
+    }
   }
   return w;
 }
 
 // Explicit-mask flag of key tile j of unit w (0 none kept, 1 all, 2 partial);
-// 1 without an explicit mask.
+// 1 without an explicit mask.  The kernel is instantiated with and without
+// the mask (MASK) so that the unmasked kernel carries none of its code: its
+// hot loop measured up to 25 % slower with the mask code compiled in.
+template <bool MASK>
 __device__ __forceinline__ int tile_flag(const KParams& p, const Unit& w, int j) {
-  if (p.mflags == nullptr) return 1;
-  return __ldg(p.mflags + (static_cast<int64_t>(w.b) * p.n_mb + w.mb) * p.n_kt + j);
+  if constexpr (!MASK) {
+    return 1;
+  } else {
+    return __ldg(p.mflags + (static_cast<int64_t>(w.b) * p.n_mb + w.mb) * p.n_kt + j);
+  }
 }
 
 // The first key tile >= j that unit w visits, or w.last + 1.  Every role
 // walks the same tiles in the same order.
+template <bool MASK>
 __device__ __forceinline__ int next_tile(const KParams& p, const Unit& w, int j) {
-  while (j <= w.last && tile_flag(p, w, j) == 0) ++j;
+  if constexpr (MASK) {
+    while (j <= w.last && tile_flag<MASK>(p, w, j) == 0) ++j;
+  }
   return j;
 }
 
@@ -305,7 +317,7 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 
 // ------------------------------------------------------------------ producer
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool MASK>
 __device__ void producer_role(const KParams& p, const Bars<D>& br, uint32_t smem,
                               const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                               const CUtensorMap* tm_v, const CUtensorMap* tm_v16) {
@@ -349,7 +361,7 @@ __device__ void producer_role(const KParams& p, const Bars<D>& br, uint32_t smem
   for (int r = 0; ok && r < rounds; ++r) {
     const int u = unit_of(r);
     if (u >= p.n_units) continue;
-    const Unit w = decode_unit(p, u);
+    const Unit w = decode_unit<MASK>(p, u);
     if (w.last < 0) continue;
     const int z_kv = w.b * p.Hkv + w.hkv;
     // Q: the buffer is free once the previous unit's last score MMA completed
@@ -362,16 +374,16 @@ __device__ void producer_role(const KParams& p, const Bars<D>& br, uint32_t smem
                             w.b, pol_stream);
     // issue order = consumption order over the visited tiles t_0 t_1 ...:
     // K(t_0) .. K(t_SB-1) | V(t_0) K(t_SB) | V(t_1) K(t_SB+1) | ...
-    int kj = next_tile(p, w, 0);  // next tile whose K is loaded
+    int kj = next_tile<MASK>(p, w, 0);  // next tile whose K is loaded
     for (int i = 0; ok && i < C::kScoreBufs && kj <= w.last; ++i) {
       ok = load_kv(false, kj, w, z_kv);
-      kj = next_tile(p, w, kj + 1);
+      kj = next_tile<MASK>(p, w, kj + 1);
     }
-    for (int j = next_tile(p, w, 0); ok && j <= w.last; j = next_tile(p, w, j + 1)) {
+    for (int j = next_tile<MASK>(p, w, 0); ok && j <= w.last; j = next_tile<MASK>(p, w, j + 1)) {
       ok = load_kv(true, j, w, z_kv);
       if (ok && kj <= w.last) {
         ok = load_kv(false, kj, w, z_kv);
-        kj = next_tile(p, w, kj + 1);
+        kj = next_tile<MASK>(p, w, kj + 1);
       }
     }
   }
@@ -465,7 +477,7 @@ __device__ __forceinline__ void issue_pv(uint32_t o_a, uint32_t o_b, uint32_t p_
 // Per-buffer completion barriers (pv_done[b]) cannot run two phases ahead of
 // a waiter: PV(g+SB) needs S(g+SB), which the S issuer issues only after its
 // wait for PV(g).
-template <int D, bool BF16>
+template <int D, bool BF16, bool MASK>
 __device__ void s_issuer_role(const KParams& p, const Bars<D>& br, uint32_t smem, uint32_t tmem) {
   using C = Cfg<D>;
   constexpr uint32_t SB = C::kScoreBufs;
@@ -482,11 +494,11 @@ __device__ void s_issuer_role(const KParams& p, const Bars<D>& br, uint32_t smem
   for (int r = 0; ok && r < rounds; ++r) {
     const int u = unit_of(r);
     if (u >= p.n_units) continue;
-    const Unit w = decode_unit(p, u);
+    const Unit w = decode_unit<MASK>(p, u);
     if (w.last < 0) continue;
     if (!__all_sync(0xffffffffu, wait_bar(br, p.status, br.q_full(), q_phase, kRoleMma))) break;
     q_phase ^= 1u;
-    for (int j = next_tile(p, w, 0); j <= w.last; j = next_tile(p, w, j + 1), ++g) {
+    for (int j = next_tile<MASK>(p, w, 0); j <= w.last; j = next_tile<MASK>(p, w, j + 1), ++g) {
       const uint32_t b = g % SB;
       // the K tile first: it normally landed long ago, and the wait for the
       // buffer below is the one on the critical path
@@ -516,7 +528,7 @@ __device__ void s_issuer_role(const KParams& p, const Bars<D>& br, uint32_t smem
   drain_wait(br.drain(), 0);
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool MASK>
 __device__ void pv_issuer_role(const KParams& p, const Bars<D>& br, uint32_t smem, uint32_t tmem) {
   using C = Cfg<D>;
   constexpr uint32_t SB = C::kScoreBufs;
@@ -533,13 +545,13 @@ __device__ void pv_issuer_role(const KParams& p, const Bars<D>& br, uint32_t sme
   for (int r = 0; ok && r < rounds; ++r) {
     const int u = unit_of(r);
     if (u >= p.n_units) continue;
-    const Unit w = decode_unit(p, u);
+    const Unit w = decode_unit<MASK>(p, u);
     if (w.last < 0) continue;
     const int z_kv = w.b * p.Hkv + w.hkv;
     uint32_t fmask = 0;
     int fchunk = -1;  // 32-tile chunk fmask holds
     bool first = true;
-    for (int j = next_tile(p, w, 0); j <= w.last; j = next_tile(p, w, j + 1), ++g) {
+    for (int j = next_tile<MASK>(p, w, 0); j <= w.last; j = next_tile<MASK>(p, w, j + 1), ++g) {
       if ((j >> 5) != fchunk) {
         fchunk = j >> 5;
         fmask = v_fp16_mask<BF16>(p, z_kv, j & ~31, w.n);
@@ -639,7 +651,7 @@ __device__ __forceinline__ float exp_half(const uint32_t (&s)[BH], uint64_t sc2,
 // epilogue, where the partial results combine exactly:
 //   m = max(m_a, m_b),  l = l_a 2^(m_a - m) + l_b 2^(m_b - m),
 //   O = (O_a 2^(m_a - m) + O_b 2^(m_b - m)) / l.
-template <int D, bool BF16>
+template <int D, bool BF16, bool MASK>
 __device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t smem, uint32_t tmem,
                              const CUtensorMap* tm_o) {
   using C = Cfg<D>;
@@ -669,7 +681,7 @@ __device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t smem,
   Unit w_next;
   uint32_t fmask_next = 0;
   if (u_next < p.n_units) {
-    w_next = decode_unit(p, u_next);
+    w_next = decode_unit<MASK>(p, u_next);
     fmask_next = v_fp16_mask<BF16>(p, w_next.b * p.Hkv + w_next.hkv, 0, w_next.n);
   }
   for (int r = 0; r < rounds && u_next < p.n_units; ++r) {
@@ -678,7 +690,7 @@ __device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t smem,
     auto decode_ahead = [&]() {
       u_next = unit_of(r + 1);
       if (u_next < p.n_units) {
-        w_next = decode_unit(p, u_next);
+        w_next = decode_unit<MASK>(p, u_next);
         fmask_next = v_fp16_mask<BF16>(p, w_next.b * p.Hkv + w_next.hkv, 0, w_next.n);
       }
     };
@@ -714,7 +726,7 @@ __device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t smem,
     bool s_ready = false;
     int fchunk = 0;     // 32-tile chunk fmask holds
     uint32_t cnt = 0;   // key tiles of this unit visited so far
-    for (int j = next_tile(p, w, 0); j <= w.last; j = next_tile(p, w, j + 1), ++cnt) {
+    for (int j = next_tile<MASK>(p, w, 0); j <= w.last; j = next_tile<MASK>(p, w, j + 1), ++cnt) {
       const uint32_t gg = g + cnt;
       const uint32_t b = gg % SB;
       const uint32_t t_s = tmem + lane_addr + C::col_s(b) + static_cast<uint32_t>(half * BH);
@@ -726,11 +738,13 @@ __device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t smem,
       const bool split = BF16 && ((fmask >> (j & 31)) & 1u) == 0u;
       // explicit mask: this row's 64 bits of the half tile when the tile is
       // partial (loaded before the wait, to hide its latency)
-      const bool partial = tile_flag(p, w, j) == 2;
+      const bool partial = MASK && tile_flag<MASK>(p, w, j) == 2;
       uint2 keep = make_uint2(0xFFFFFFFFu, 0xFFFFFFFFu);
-      if (partial && row_ok)
-        keep = __ldg(reinterpret_cast<const uint2*>(
-            p.mbits + ((static_cast<int64_t>(w.b) * p.Lq + row) * p.n_kt + j) * 4 + half * 2));
+      if constexpr (MASK) {
+        if (partial && row_ok)
+          keep = __ldg(reinterpret_cast<const uint2*>(
+              p.mbits + ((static_cast<int64_t>(w.b) * p.Lq + row) * p.n_kt + j) * 4 + half * 2));
+      }
       if (!s_ready) {
         ok = wait_bar(br, p.status, br.s_full(b), (gg / SB) & 1u, kRoleSoftmax);
         if (!__all_sync(0xffffffffu, ok)) {
@@ -750,10 +764,15 @@ __device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t smem,
       // exp2(-inf * scale - m) = 0 because the scale is > 0 (a zero sm_scale
       // arrives as FLT_MIN).
       if (masked) {
+        if constexpr (MASK) {
 #pragma unroll
-        for (int c = 0; c < BH; ++c) {
-          const uint32_t bit = ((c < 32 ? keep.x : keep.y) >> (c & 31)) & 1u;
-          s[c] = (c < c_lim && bit != 0u) ? s[c] : 0xFF800000u;
+          for (int c = 0; c < BH; ++c) {
+            const uint32_t bit = ((c < 32 ? keep.x : keep.y) >> (c & 31)) & 1u;
+            s[c] = (c < c_lim && bit != 0u) ? s[c] : 0xFF800000u;
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < BH; ++c) s[c] = (c < c_lim) ? s[c] : 0xFF800000u;
         }
       }
       // max of the half row: 8 independent chains of 3-input maxima
@@ -918,7 +937,7 @@ __device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t smem,
 
 // ------------------------------------------------------------------ kernel
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool MASK>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
@@ -974,13 +993,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = ptx::ld_shared_volatile(br.tmem_word());
 
   if (warp == kProducerWarp) {
-    if (lane == 0) producer_role<D, BF16>(p, br, smem, &tm_q, &tm_k, &tm_v, &tm_v16);
+    if (lane == 0) producer_role<D, BF16, MASK>(p, br, smem, &tm_q, &tm_k, &tm_v, &tm_v16);
   } else if (warp == kPvWarp) {
-    pv_issuer_role<D, BF16>(p, br, smem, tmem);  // whole warp
+    pv_issuer_role<D, BF16, MASK>(p, br, smem, tmem);  // whole warp
   } else if (warp == kSWarp) {
-    s_issuer_role<D, BF16>(p, br, smem, tmem);  // whole warp
+    s_issuer_role<D, BF16, MASK>(p, br, smem, tmem);  // whole warp
   } else {
-    softmax_role<D, BF16>(p, br, smem, tmem, &tm_o);  // warps 0-7
+    softmax_role<D, BF16, MASK>(p, br, smem, tmem, &tm_o);  // warps 0-7
     // the last O stores read their staging tiles: finish before shared memory
     // goes (no stage needs releasing: the producer has no loads left)
     if (threadIdx.x == 0) ptx::bulk_wait_all();
@@ -994,12 +1013,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool MASK>
 cudaError_t launch_instance(const Problem& pr, const CUtensorMap* maps, int num_sms) {
   using C = Cfg<D>;
   // the shared-memory opt-in is per device; set once per (D, dtype) instance and device
   static std::atomic<uint64_t> configured{0};
-  auto kern = attn_fwd_tc_kernel<D, BF16>;
+  auto kern = attn_fwd_tc_kernel<D, BF16, MASK>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -1062,13 +1081,20 @@ bool tc_config(int D, TcConfig* out) {
 // and V tile with zeros (Q.K^T and P.V unchanged; O's extra columns are 0)
 // and the O store writes only the D columns inside the tensor.
 cudaError_t launch_tc(const Problem& p, const CUtensorMap* maps, int num_sms) {
+  const bool mask = p.mflags != nullptr;
   if (p.D == 16 || p.D == 32 || p.D == 64) {
-    return p.bf16 ? launch_instance<64, true>(p, maps, num_sms)
-                  : launch_instance<64, false>(p, maps, num_sms);
+    if (mask)
+      return p.bf16 ? launch_instance<64, true, true>(p, maps, num_sms)
+                    : launch_instance<64, false, true>(p, maps, num_sms);
+    return p.bf16 ? launch_instance<64, true, false>(p, maps, num_sms)
+                  : launch_instance<64, false, false>(p, maps, num_sms);
   }
   if (p.D == 128) {
-    return p.bf16 ? launch_instance<128, true>(p, maps, num_sms)
-                  : launch_instance<128, false>(p, maps, num_sms);
+    if (mask)
+      return p.bf16 ? launch_instance<128, true, true>(p, maps, num_sms)
+                    : launch_instance<128, false, true>(p, maps, num_sms);
+    return p.bf16 ? launch_instance<128, true, false>(p, maps, num_sms)
+                  : launch_instance<128, false, false>(p, maps, num_sms);
   }
   return cudaErrorInvalidValue;
 }
