@@ -234,7 +234,8 @@ Problem make_problem(const void* q, const void* k, const void* v, void* o, float
   p.mask = nullptr;
   p.mask_sb = p.mask_sr = 0;
   p.mbits = nullptr;
-  p.mflags = nullptr;
+  p.mvis = nullptr;
+  p.mpart = nullptr;
   p.mlast = nullptr;
   p.B = B;
   p.Hq = Hq;

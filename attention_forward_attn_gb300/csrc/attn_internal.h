@@ -46,9 +46,11 @@ struct Problem {
   // by the mask pre-pass (attn_mask.cu)
   const uint8_t* mask;
   int64_t mask_sb, mask_sr;  // element strides of its batch (0: shared) and rows
-  const uint32_t* mbits;     // [B, Lq, n_kt, 4] words: bit c of word w = key 128t + 32w + c
-  const uint8_t* mflags;     // [B, n_mb, n_kt]: 0 no visible key, 1 all visible, 2 partial
-  const int* mlast;          // [B, n_mb]: last key tile with a visible key, or -1
+  // (mB = 1 when the mask is shared by every batch, else B)
+  const uint32_t* mbits;     // [mB, Lq, n_kt, 4] words: bit c of word w = key 128t + 32w + c
+  const uint32_t* mvis;      // [mB, n_mb, ceil(n_kt/32)]: bit t%32 = tile t has a kept position
+  const uint32_t* mpart;     // same layout: bit t%32 = tile t is partially kept
+  const int* mlast;          // [mB, n_mb]: last key tile with a kept position, or -1
   int B, Hq, Hkv;
   int Lq, Lk;              // query rows, key/value rows per head
   int D;
@@ -83,8 +85,9 @@ int64_t vconv_workspace_bytes(const Problem& p);
 cudaError_t launch_vconv(const Problem& p, void* v16, int* flags);
 
 // Explicit-mask pre-pass (attn_mask.cu): bytes of its workspace for p, and
-// its launch (clears mlast first).  The workspace holds mbits, mflags and
-// mlast in that order; mask_arrays sets the three pointers of p into it.
+// its launch (clears mvis, mpart and mlast first).  The workspace holds
+// mbits, mvis, mpart and mlast in that order; mask_arrays sets the four
+// pointers of p into it.
 int64_t mask_workspace_bytes(const Problem& p);
 void mask_arrays(Problem& p, void* ws);
 cudaError_t launch_mask_pack(const Problem& p);

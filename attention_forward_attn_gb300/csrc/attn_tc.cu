@@ -160,8 +160,11 @@ struct KParams {
   const int* vflags;
   // explicit mask, packed by the pre-pass (null: none); see attn_mask.cu
   const uint32_t* mbits;
-  const uint8_t* mflags;
+  const uint32_t* mvis;
+  const uint32_t* mpart;
   const int* mlast;
+  int n_ch;         // 32-tile words per row block in mvis / mpart
+  int mask_shared;  // 1: one mask for every batch (mask batch 0)
   int n_kt;     // 128-key tiles per (b, h_kv)
   int B, Hq, Hkv, G;
   int Lq, Lk;   // query rows, key/value rows per head
@@ -175,6 +178,7 @@ struct KParams {
 
 struct Unit {
   int bh, b, hq, hkv, mb, m0, kv_len;
+  int mblk;  // explicit mask: (mask batch, row block) index of its packed words
   int n;     // key tiles in range of the causal and padding masks
   int last;  // last key tile the unit visits (-1: none; with an explicit mask,
              // tiles without a kept position are skipped)
@@ -217,38 +221,68 @@ __device__ __forceinline__ Unit decode_unit(const KParams& p, int u) {
   w.n = (hi + BN - 1) / BN;
   w.mb = mb;
   w.last = w.n - 1;
+  w.mblk = 0;
   if constexpr (MASK) {
+    w.mblk = (p.mask_shared ? 0 : w.b) * p.n_mb + mb;
     if (w.last >= 0) {
-      const int64_t f0 = (static_cast<int64_t>(w.b) * p.n_mb + mb) * p.n_kt;
-      w.last = min(w.last, __ldg(p.mlast + static_cast<int64_t>(w.b) * p.n_mb + mb));
-      while (w.last >= 0 && __ldg(p.mflags + f0 + w.last) == 0) --w.last;
+      // the last tile in range that has a kept position
+      int last = min(w.last, __ldg(p.mlast + w.mblk));
+      const uint32_t* vis = p.mvis + static_cast<int64_t>(w.mblk) * p.n_ch;
+      while (last >= 0) {
+        const uint32_t word = __ldg(vis + (last >> 5)) & (0xFFFFFFFFu >> (31 - (last & 31)));
+        if (word != 0u) {
+          last = (last & ~31) + 31 - __clz(word);
+          break;
+        }
+        last = (last & ~31) - 1;
+      }
+      w.last = last;
     }
   }
   return w;
 }
 
-// Explicit-mask flag of key tile j of unit w (0 none kept, 1 all, 2 partial);
-// 1 without an explicit mask.  The kernel is instantiated with and without
-// the mask (MASK) so that the unmasked kernel carries none of its code: its
-// hot loop measured up to 25 % slower with the mask code compiled in.
+// The key tiles a unit visits, in order: 0 .. last without an explicit
+// mask; with one, the tiles that have a kept position, read from the
+// pre-pass's bit words 32 tiles at a time.  The kernel is instantiated with
+// and without the mask (MASK) so that the unmasked kernel carries none of
+// this code: its hot loop measured up to 25 % slower with it compiled in.
 template <bool MASK>
-__device__ __forceinline__ int tile_flag(const KParams& p, const Unit& w, int j) {
-  if constexpr (!MASK) {
-    return 1;
-  } else {
-    return __ldg(p.mflags + (static_cast<int64_t>(w.b) * p.n_mb + w.mb) * p.n_kt + j);
+struct TileWalk {
+  const uint32_t* vis = nullptr;
+  const uint32_t* part = nullptr;
+  int chunk = -1;        // 32-tile word held in v / pt
+  uint32_t v = 0, pt = 0;
+  __device__ __forceinline__ void init(const KParams& p, const Unit& w) {
+    if constexpr (MASK) {
+      vis = p.mvis + static_cast<int64_t>(w.mblk) * p.n_ch;
+      part = p.mpart + static_cast<int64_t>(w.mblk) * p.n_ch;
+      chunk = -1;
+    }
   }
-}
-
-// The first key tile >= j that unit w visits, or w.last + 1.  Every role
-// walks the same tiles in the same order.
-template <bool MASK>
-__device__ __forceinline__ int next_tile(const KParams& p, const Unit& w, int j) {
-  if constexpr (MASK) {
-    while (j <= w.last && tile_flag<MASK>(p, w, j) == 0) ++j;
+  // the first visited tile >= j, or a value > last
+  __device__ __forceinline__ int next(int j, int last) {
+    if constexpr (MASK) {
+      while (j <= last) {
+        const int c = j >> 5;
+        if (c != chunk) {
+          chunk = c;
+          v = __ldg(vis + c);
+          pt = __ldg(part + c);
+        }
+        const uint32_t rest = v >> (j & 31);
+        if (rest != 0u) return j + __ffs(static_cast<int>(rest)) - 1;
+        j = (c + 1) << 5;
+      }
+    }
+    return j;
   }
-  return j;
-}
+  // tile j (just returned by next) is partially kept
+  __device__ __forceinline__ bool partial(int j) const {
+    if constexpr (MASK) return ((pt >> (j & 31)) & 1u) != 0u;
+    return false;
+  }
+};
 
 // Bounded mbarrier wait.  False: timed out (recorded) or another role aborted.
 // (Everything is inlined: out-of-line calls do not mix with setmaxnreg.)
@@ -374,16 +408,19 @@ __device__ void producer_role(const KParams& p, const Bars<D>& br, uint32_t smem
                             w.b, pol_stream);
     // issue order = consumption order over the visited tiles t_0 t_1 ...:
     // K(t_0) .. K(t_SB-1) | V(t_0) K(t_SB) | V(t_1) K(t_SB+1) | ...
-    int kj = next_tile<MASK>(p, w, 0);  // next tile whose K is loaded
+    TileWalk<MASK> kw, vw;  // K runs ahead of V: one walker each
+    kw.init(p, w);
+    vw.init(p, w);
+    int kj = kw.next(0, w.last);  // next tile whose K is loaded
     for (int i = 0; ok && i < C::kScoreBufs && kj <= w.last; ++i) {
       ok = load_kv(false, kj, w, z_kv);
-      kj = next_tile<MASK>(p, w, kj + 1);
+      kj = kw.next(kj + 1, w.last);
     }
-    for (int j = next_tile<MASK>(p, w, 0); ok && j <= w.last; j = next_tile<MASK>(p, w, j + 1)) {
+    for (int j = vw.next(0, w.last); ok && j <= w.last; j = vw.next(j + 1, w.last)) {
       ok = load_kv(true, j, w, z_kv);
       if (ok && kj <= w.last) {
         ok = load_kv(false, kj, w, z_kv);
-        kj = next_tile<MASK>(p, w, kj + 1);
+        kj = kw.next(kj + 1, w.last);
       }
     }
   }
@@ -498,7 +535,9 @@ __device__ void s_issuer_role(const KParams& p, const Bars<D>& br, uint32_t smem
     if (w.last < 0) continue;
     if (!__all_sync(0xffffffffu, wait_bar(br, p.status, br.q_full(), q_phase, kRoleMma))) break;
     q_phase ^= 1u;
-    for (int j = next_tile<MASK>(p, w, 0); j <= w.last; j = next_tile<MASK>(p, w, j + 1), ++g) {
+    TileWalk<MASK> tw;
+    tw.init(p, w);
+    for (int j = tw.next(0, w.last); j <= w.last; j = tw.next(j + 1, w.last), ++g) {
       const uint32_t b = g % SB;
       // the K tile first: it normally landed long ago, and the wait for the
       // buffer below is the one on the critical path
@@ -551,7 +590,9 @@ __device__ void pv_issuer_role(const KParams& p, const Bars<D>& br, uint32_t sme
     uint32_t fmask = 0;
     int fchunk = -1;  // 32-tile chunk fmask holds
     bool first = true;
-    for (int j = next_tile<MASK>(p, w, 0); j <= w.last; j = next_tile<MASK>(p, w, j + 1), ++g) {
+    TileWalk<MASK> tw;
+    tw.init(p, w);
+    for (int j = tw.next(0, w.last); j <= w.last; j = tw.next(j + 1, w.last), ++g) {
       if ((j >> 5) != fchunk) {
         fchunk = j >> 5;
         fmask = v_fp16_mask<BF16>(p, z_kv, j & ~31, w.n);
@@ -726,7 +767,9 @@ __device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t smem,
     bool s_ready = false;
     int fchunk = 0;     // 32-tile chunk fmask holds
     uint32_t cnt = 0;   // key tiles of this unit visited so far
-    for (int j = next_tile<MASK>(p, w, 0); j <= w.last; j = next_tile<MASK>(p, w, j + 1), ++cnt) {
+    TileWalk<MASK> tw;
+    tw.init(p, w);
+    for (int j = tw.next(0, w.last); j <= w.last; j = tw.next(j + 1, w.last), ++cnt) {
       const uint32_t gg = g + cnt;
       const uint32_t b = gg % SB;
       const uint32_t t_s = tmem + lane_addr + C::col_s(b) + static_cast<uint32_t>(half * BH);
@@ -738,12 +781,13 @@ __device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t smem,
       const bool split = BF16 && ((fmask >> (j & 31)) & 1u) == 0u;
       // explicit mask: this row's 64 bits of the half tile when the tile is
       // partial (loaded before the wait, to hide its latency)
-      const bool partial = MASK && tile_flag<MASK>(p, w, j) == 2;
+      const bool partial = tw.partial(j);
       uint2 keep = make_uint2(0xFFFFFFFFu, 0xFFFFFFFFu);
       if constexpr (MASK) {
-        if (partial && row_ok)
-          keep = __ldg(reinterpret_cast<const uint2*>(
-              p.mbits + ((static_cast<int64_t>(w.b) * p.Lq + row) * p.n_kt + j) * 4 + half * 2));
+        if (partial && row_ok) {
+          const int64_t mrow = static_cast<int64_t>(p.mask_shared ? 0 : w.b) * p.Lq + row;
+          keep = __ldg(reinterpret_cast<const uint2*>(p.mbits + (mrow * p.n_kt + j) * 4 + half * 2));
+        }
       }
       if (!s_ready) {
         ok = wait_bar(br, p.status, br.s_full(b), (gg / SB) & 1u, kRoleSoftmax);
@@ -765,10 +809,29 @@ __device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t smem,
       // arrives as FLT_MIN).
       if (masked) {
         if constexpr (MASK) {
+          // columns >= c_lim leave the keep bits first; then per column one
+          // prmt replicates its bit (moved to a byte's sign) over a word and
+          // one logic op selects the score or -inf: about the cost of the
+          // implicit masks' compare-and-select (a per-column bit test
+          // measured ~30 % slower on every step, partial or not)
+          uint32_t kw[2] = {keep.x, keep.y};
 #pragma unroll
-          for (int c = 0; c < BH; ++c) {
-            const uint32_t bit = ((c < 32 ? keep.x : keep.y) >> (c & 31)) & 1u;
-            s[c] = (c < c_lim && bit != 0u) ? s[c] : 0xFF800000u;
+          for (int wd = 0; wd < 2; ++wd) {
+            const int n = c_lim - 32 * wd;  // columns of this word below c_lim
+            kw[wd] &= n >= 32 ? 0xFFFFFFFFu : (n <= 0 ? 0u : (1u << n) - 1u);
+          }
+#pragma unroll
+          for (int wd = 0; wd < 2; ++wd) {
+#pragma unroll
+            for (int c0 = 0; c0 < 8; ++c0) {
+              const uint32_t t = kw[wd] << (7 - c0);  // bit c0 + 8k -> sign of byte k
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const uint32_t m = ptx::prmt(t, 0u, 0x8888u + 0x1111u * k);
+                const int c = 32 * wd + 8 * k + c0;
+                s[c] = (s[c] & m) | (0xFF800000u & ~m);
+              }
+            }
           }
         } else {
 #pragma unroll
@@ -1035,8 +1098,10 @@ cudaError_t launch_instance(const Problem& pr, const CUtensorMap* maps, int num_
   kp.status = pr.status;
   kp.vflags = pr.vflags;
   kp.mbits = pr.mbits;
-  kp.mflags = pr.mflags;
+  kp.mvis = pr.mvis;
+  kp.mpart = pr.mpart;
   kp.mlast = pr.mlast;
+  kp.mask_shared = pr.mask_sb == 0 ? 1 : 0;
   kp.n_kt = (pr.Lk + BN - 1) / BN;
   kp.B = pr.B;
   kp.Hq = pr.Hq;
@@ -1049,6 +1114,7 @@ cudaError_t launch_instance(const Problem& pr, const CUtensorMap* maps, int num_
   kp.o_sh = pr.so.h;
   kp.o_sl = pr.so.l;
   kp.n_mb = (pr.Lq + BM - 1) / BM;
+  kp.n_ch = (kp.n_kt + 31) / 32;
   kp.n_units = pr.B * pr.Hq * kp.n_mb;
   // A zero scale is passed as the smallest normal float: every product
   // s * scale then rounds to zero exactly as with 0 (all visible keys get
@@ -1081,7 +1147,7 @@ bool tc_config(int D, TcConfig* out) {
 // and V tile with zeros (Q.K^T and P.V unchanged; O's extra columns are 0)
 // and the O store writes only the D columns inside the tensor.
 cudaError_t launch_tc(const Problem& p, const CUtensorMap* maps, int num_sms) {
-  const bool mask = p.mflags != nullptr;
+  const bool mask = p.mvis != nullptr;
   if (p.D == 16 || p.D == 32 || p.D == 64) {
     if (mask)
       return p.bf16 ? launch_instance<64, true, true>(p, maps, num_sms)

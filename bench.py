@@ -470,6 +470,102 @@ def run_gpu(args, w, world, rank, local):
     return line
 
 
+def mask_workloads(dev):
+    """The explicit-mask workloads: (name, workload, keep-mask builder, implicit
+    kwargs or None).  The builders return a bool [B or 1, L, L] device tensor."""
+    def padding(w, vl_d):
+        L = w.L
+        return torch.arange(L, device=dev)[None, None, :] < vl_d[:, None, None].expand(w.B, L, 1)
+
+    def tril(w, vl_d):
+        return torch.tril(torch.ones(w.L, w.L, dtype=torch.bool, device=dev))[None]
+
+    def band(w, vl_d):
+        i = torch.arange(w.L, device=dev)[:, None]
+        j = torch.arange(w.L, device=dev)[None, :]
+        return (((i - j).abs() < 512) | (j < 256))[None]
+
+    return [
+        ("C3 padding as an explicit [8,4096,4096] mask", wl.WORKLOADS["C3"], padding,
+         dict(causal=False, padded=True)),
+        ("C4 causal as an explicit tril [4096,4096] mask", wl.WORKLOADS["C4"], tril,
+         dict(causal=True, padded=False)),
+        ("C4 shapes, causal, band |i-j| < 512 plus keys < 256", wl.WORKLOADS["C4"], band, None),
+    ]
+
+
+def run_mask_workloads(args, local):
+    """One JSON line per explicit-mask workload: ms per attn_fwd_masked call
+    (mask pre-pass + bf16 V pre-pass + attention, L2 flushed before each call)
+    and, where the mask restates an implicit one, the implicit call's ms."""
+    import attention_forward_attn_gb300 as attn
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    attn.load()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    peaks, peak_src = load_peaks()
+    lines = []
+    for name, w, build, implicit in mask_workloads(dev):
+        q, k, v, vl = wl.workload_inputs(w)
+        q_d, k_d, v_d = q.to(dev), k.to(dev), v.to(dev)
+        vl_d = None if vl is None else vl.to(dev)
+        keep = build(w, vl_d)
+        causal_masked = implicit is None and w.causal
+        o_d = torch.empty_like(q_d)
+        lse_d = torch.empty((w.B * w.Hq, w.L), dtype=torch.float32, device=dev)
+
+        def timed(fn, n):
+            for _ in range(args.warmup):
+                flush.zero_()
+                fn()
+            ts = []
+            for _ in range(n):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                fn()
+                e1.record()
+                torch.cuda.synchronize(dev)
+                ts.append(e0.elapsed_time(e1))
+            st, code = attn.status()
+            if st != 0:
+                raise RuntimeError("device status %d (code %#x)" % (st, code))
+            return sorted(ts)[len(ts) // 2]
+
+        n = max(5, min(args.steps, 200))
+        ms_mask = timed(lambda: attn.attn_fwd_strided(q_d, k_d, v_d, causal=causal_masked,
+                                                      sm_scale=w.sm_scale, mask=keep, out=o_d,
+                                                      lse=lse_d), n)
+        ms_impl = None
+        if implicit is not None:
+            ms_impl = timed(lambda: attn.attn_fwd(q_d, k_d, v_d, causal=implicit["causal"],
+                                                  sm_scale=w.sm_scale,
+                                                  valid_len=vl_d if implicit["padded"] else None,
+                                                  out=o_d, lse=lse_d), n)
+        # visible (query, key) pairs of every head: the algorithmic work
+        vis = keep.expand(w.B, w.L, w.L)
+        if causal_masked:
+            vis = vis & torch.tril(torch.ones(w.L, w.L, dtype=torch.bool, device=dev))
+        pairs = float(vis.sum().item()) * w.Hq
+        flops = 4.0 * w.D * pairs
+        tf = flops / (ms_mask * 1e-3) / 1e12
+        lines.append({
+            "metric": "attention fwd TFLOP/s with an explicit boolean mask (algorithmic)",
+            "workload": name, "value": round(tf, 2), "unit": "TFLOP/s",
+            "ms_per_call": round(ms_mask, 4),
+            "implicit_ms_per_call": None if ms_impl is None else round(ms_impl, 4),
+            "visible_pairs_per_head_all_batches": int(pairs / w.Hq),
+            "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": peaks["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": round(tf / peaks["bf16_tflops"], 4),
+                         "peak_source": "%s bf16_tflops" % peak_src},
+            "timing": "median of %d calls, L2 flushed before each, CUDA events; the call includes "
+                      "the mask pre-pass and the bf16 V pre-pass" % n,
+            "dtype": w.dtype, "data": "synthetic"})
+        del keep, q_d, k_d, v_d, o_d, lse_d
+        torch.cuda.empty_cache()
+    return lines
+
+
 def _oracle_threads() -> int:
     import oracle
     return oracle.max_threads()
@@ -535,6 +631,8 @@ def main(argv=None):
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     ap.add_argument("--reference-budget-s", type=float, default=120.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--mask-workloads", action="store_true",
+                    help="instead of the headline line, one line per explicit-mask workload")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -546,6 +644,11 @@ def main(argv=None):
     if args.impl == "reference":
         if rank == 0:
             print(json.dumps(run_reference(args, w)), flush=True)
+        return 0
+    if args.mask_workloads:
+        if rank == 0:
+            for line in run_mask_workloads(args, local):
+                print(json.dumps(line), flush=True)
         return 0
 
     if world > 1:
