@@ -95,6 +95,8 @@ def load():
             lib.attn_fwd_masked.argtypes = [p, sp, p, sp, p, sp, p, sp, p, i, i, i, i, i, i,
                                             ctypes.c_float, i, p, p, i64, i64, i, p]
             lib.attn_fwd_masked.restype = i
+            lib.attn_fwd_f32.argtypes = [p, p, p, p, p, i, i, i, i, ctypes.c_float, i, p, i, p]
+            lib.attn_fwd_f32.restype = i
             lib.attn_host_plan.argtypes = [i, i, i, i, i, i, ctypes.POINTER(Chunk), i,
                                            ctypes.POINTER(ctypes.c_int)]
             lib.attn_host_plan.restype = i
@@ -390,4 +392,39 @@ def attn_fwd_strided(q, k, v, *, causal=False, sm_scale=None, valid_len=None, ou
                             mask.stride(1), _dtype_code(q), _stream_handle(stream))
     if st != ATTN_OK:
         raise AttnError(st, "attn_fwd_masked" if mask is not None else "attn_fwd_strided")
+    return out, (lse if return_lse else None)
+
+
+F32_KERNELS = {"naive": 0, "tiled_element": 1, "tiled_rowmax": 2}
+
+
+def attn_fwd_f32(q, k, v, *, kernel="tiled_rowmax", causal=False, sm_scale=None, valid_len=None,
+                 out=None, lse=None, return_lse=True, stream=None):
+    """fp32 attention forward with one of the comparison kernels of
+    attn_fwd_f32 ("naive", "tiled_element", "tiled_rowmax").  q, k, v: fp32
+    contiguous CUDA tensors [B, H, L, D] (D 64 or 128).  Returns (o, lse)."""
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not t.is_cuda or not t.is_contiguous() or t.dtype != torch.float32:
+            raise ValueError("%s must be a contiguous float32 CUDA tensor" % name)
+    B, H, L, D = q.shape
+    if k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("k and v must have q's shape [B, H, L, D]")
+    if sm_scale is None:
+        sm_scale = 1.0 / float(D) ** 0.5
+    if out is None:
+        out = torch.empty_like(q)
+    if return_lse and lse is None:
+        lse = torch.empty((B * H, L), dtype=torch.float32, device=q.device)
+    vl_ptr = None
+    if valid_len is not None:
+        if valid_len.dtype != torch.int32 or not valid_len.is_cuda or valid_len.numel() != B:
+            raise ValueError("valid_len must be an int32 CUDA tensor of B elements")
+        vl_ptr = valid_len.data_ptr()
+    st = int(load().attn_fwd_f32(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                 lse.data_ptr() if return_lse else None, B, H, L, D,
+                                 float(sm_scale), int(bool(causal)), vl_ptr, F32_KERNELS[kernel],
+                                 _stream_handle(stream)))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fwd_f32")
     return out, (lse if return_lse else None)

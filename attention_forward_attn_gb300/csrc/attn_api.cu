@@ -439,6 +439,36 @@ attn_status_t attn_fwd_simt(const void* q, const void* k, const void* v, void* o
   return ATTN_OK;
 }
 
+attn_status_t attn_fwd_f32(const float* q, const float* k, const float* v, float* o, float* lse,
+                           int B, int H, int L, int D, float sm_scale, int causal,
+                           const int32_t* valid_len, attn_f32_kernel_t kernel,
+                           attn_stream_t stream) {
+  if (q == nullptr || k == nullptr || v == nullptr || o == nullptr) return ATTN_ERR_NULL;
+  if (B < 1 || H < 1 || L < 1) return ATTN_ERR_SHAPE;
+  if (D != 64 && D != 128) return ATTN_ERR_HEADDIM;
+  if (causal != 0 && causal != 1) return ATTN_ERR_ARG;
+  if (kernel != ATTN_F32_NAIVE && kernel != ATTN_F32_TILED_ELEMENT &&
+      kernel != ATTN_F32_TILED_ROWMAX)
+    return ATTN_ERR_ARG;
+  if (!(sm_scale >= 0.f) || isinf(sm_scale)) return ATTN_ERR_SCALE;
+  // grid rows are (b, h) pairs; the naive kernel keeps a query's L scores in shared memory
+  if (static_cast<int64_t>(B) * H > 65535 || static_cast<int64_t>(B) * H * L > INT32_MAX)
+    return ATTN_ERR_SHAPE;
+  if (kernel == ATTN_F32_NAIVE && L > 50000) return ATTN_ERR_SHAPE;
+  if (!aligned(q, 4) || !aligned(k, 4) || !aligned(v, 4) || !aligned(o, 4) ||
+      (lse != nullptr && !aligned(lse, 4)) || (valid_len != nullptr && !aligned(valid_len, 4)))
+    return ATTN_ERR_ALIGN;
+  int dev = 0;
+  DeviceState* st = nullptr;
+  attn_status_t s = device_state(&dev, &st);
+  if (s != ATTN_OK) return s;
+  cudaError_t e = attn::launch_f32(q, k, v, o, lse, B, H, L, D, sm_scale, causal, valid_len,
+                                   static_cast<int>(kernel), st->status,
+                                   reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  return ATTN_OK;
+}
+
 attn_status_t attn_status(attn_stream_t stream, int* device_code) {
   if (device_code != nullptr) *device_code = 0;
   cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));

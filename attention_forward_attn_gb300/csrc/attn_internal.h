@@ -92,6 +92,12 @@ int64_t mask_workspace_bytes(const Problem& p);
 void mask_arrays(Problem& p, void* ws);
 cudaError_t launch_mask_pack(const Problem& p);
 
+// fp32 comparison kernels (attn_f32.cu): kernel 0 naive three-pass, 1 tiled
+// per-element online softmax, 2 tiled block rowmax.
+cudaError_t launch_f32(const float* q, const float* k, const float* v, float* o, float* lse,
+                       int B, int H, int L, int D, float sm_scale, int causal,
+                       const int32_t* valid_len, int kernel, int* status, cudaStream_t stream);
+
 // SIMT cross-check forward.
 cudaError_t launch_simt(const Problem& p);
 

@@ -566,6 +566,86 @@ def run_mask_workloads(args, local):
     return lines
 
 
+def run_relative_table(args, local):
+    """The comparison of "masked multi head attention in CUDA" section 6.1,
+    on this GPU: B=1, H=8, N=1024, D=64, fp32, causal mask, rows = the
+    unfused PyTorch path (scores, mask, softmax, then V; TF32 off, as the
+    page's section 5.3 asks), the naive three-pass kernel, the tiled kernel
+    with a per-element online softmax, the tiled kernel with the block row
+    max (the page's 1.0x), and the tcgen05 kernel on bf16 / fp16 copies of
+    the inputs.  Times: median of the timed calls, L2 flushed before each."""
+    import attention_forward_attn_gb300 as attn
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    attn.load()
+    B, H, L, D = 1, 8, 1024, 64
+    gen = torch.Generator().manual_seed(26)
+    q, k, v = (torch.randn(B, H, L, D, generator=gen).to(dev) for _ in range(3))
+    sm = 1.0 / D ** 0.5
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    keep = torch.tril(torch.ones(L, L, dtype=torch.bool, device=dev))
+    old_tf32 = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = False
+
+    def torch_unfused():
+        s_ = torch.matmul(q, k.transpose(-1, -2)) * sm
+        s_ = s_.masked_fill(~keep, float("-inf"))
+        return torch.matmul(torch.softmax(s_, dim=-1), v)
+
+    qb, kb, vb = q.bfloat16(), k.bfloat16(), v.bfloat16()
+    qh, kh, vh = q.half(), k.half(), v.half()
+    impls = [
+        ("PyTorch unfused (scores, mask, softmax, V), fp32", torch_unfused, 4.0),
+        ("naive CUDA kernel (three passes), fp32",
+         lambda: attn.attn_fwd_f32(q, k, v, kernel="naive", causal=True, sm_scale=sm), 3.2),
+        ("tiled CUDA kernel, per-element online softmax, fp32",
+         lambda: attn.attn_fwd_f32(q, k, v, kernel="tiled_element", causal=True, sm_scale=sm), 1.4),
+        ("tiled CUDA kernel, block row max, fp32",
+         lambda: attn.attn_fwd_f32(q, k, v, kernel="tiled_rowmax", causal=True, sm_scale=sm), 1.0),
+        ("tcgen05 kernel (attn_fwd), bf16 inputs",
+         lambda: attn.attn_fwd(qb, kb, vb, causal=True, sm_scale=sm), None),
+        ("tcgen05 kernel (attn_fwd), fp16 inputs",
+         lambda: attn.attn_fwd(qh, kh, vh, causal=True, sm_scale=sm), None),
+    ]
+    rows = []
+    n = max(5, min(args.steps, 100))
+    for name, fn, page in impls:
+        for _ in range(args.warmup):
+            flush.zero_()
+            fn()
+        torch.cuda.synchronize(dev)
+        base = torch.cuda.memory_allocated(dev)
+        torch.cuda.reset_peak_memory_stats(dev)
+        fn()
+        torch.cuda.synchronize(dev)
+        extra = torch.cuda.max_memory_allocated(dev) - base
+        ts = []
+        for _ in range(n):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize(dev)
+            ts.append(e0.elapsed_time(e1))
+        st, code = attn.status()
+        if st != 0:
+            raise RuntimeError("device status %d (code %#x)" % (st, code))
+        rows.append({"impl": name, "ms": round(sorted(ts)[n // 2], 4), "page_relative": page,
+                     "torch_peak_extra_bytes": int(extra)})
+    torch.backends.cuda.matmul.allow_tf32 = old_tf32
+    ref = [r for r in rows if r["page_relative"] == 1.0][0]["ms"]
+    for r in rows:
+        r["relative_to_tiled_rowmax"] = round(r["ms"] / ref, 3)
+    return {"metric": "relative time of attention implementations (masked multi head attention "
+                      "in CUDA, section 6.1), B=1 H=8 N=1024 D=64 causal",
+            "rows": rows, "timing": "median of %d calls, L2 flushed before each, CUDA events" % n,
+            "note": "page_relative: the page's own factors (one Ampere GPU, single runs); "
+                    "torch_peak_extra_bytes: device memory torch allocated during one call "
+                    "(the fused kernels allocate none through torch)",
+            "data": "synthetic N(0,1), seed 26"}
+
+
 def _oracle_threads() -> int:
     import oracle
     return oracle.max_threads()
@@ -633,6 +713,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--mask-workloads", action="store_true",
                     help="instead of the headline line, one line per explicit-mask workload")
+    ap.add_argument("--relative-table", action="store_true",
+                    help="instead of the headline line, the section 6.1 comparison table")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -644,6 +726,10 @@ def main(argv=None):
     if args.impl == "reference":
         if rank == 0:
             print(json.dumps(run_reference(args, w)), flush=True)
+        return 0
+    if args.relative_table:
+        if rank == 0:
+            print(json.dumps(run_relative_table(args, local)), flush=True)
         return 0
     if args.mask_workloads:
         if rank == 0:

@@ -216,6 +216,35 @@ attn_status_t attn_fwd_simt(const void* q, const void* k, const void* v, void* o
                             int B, int Hq, int Hkv, int L, int D, float sm_scale, int causal,
                             const int32_t* valid_len, attn_dtype_t dtype, attn_stream_t stream);
 
+/* The fp32 comparison kernels of attn_fwd_f32. */
+typedef enum {
+  ATTN_F32_NAIVE = 0,          /* three passes over the keys per query */
+  ATTN_F32_TILED_ELEMENT = 1,  /* tiled, online softmax updated after every key */
+  ATTN_F32_TILED_ROWMAX = 2    /* tiled, block row max first, one exponential per score */
+} attn_f32_kernel_t;
+
+/*
+ * attn_fwd_f32 -- the same operation on fp32 tensors, computed by one of the
+ * three CUDA kernels that "masked multi head attention in CUDA" (wzjinhao.cn)
+ * compares in section 6.1: the naive kernel of section 3.1 (one block per
+ * query, one thread per head column, three passes: scores and max, sum of
+ * exponentials, weighted sum of V), and the tiled kernels of sections
+ * 4.1-4.3 (Q tile resident in shared memory, K/V tiles of 32 keys, one thread
+ * per output element; online softmax after every key, or block row max with
+ * one exponential per score).  fp32 throughout, no tensor cores.  They exist
+ * to reproduce that comparison on this GPU; attn_fwd is the fast path.
+ *
+ * Arguments: q, k, v, o fp32 [B, H, L, D] contiguous device memory (4-byte
+ * aligned; multi-head, K and V with the same H); lse fp32 [B*H, L] or NULL;
+ * D 64 or 128; valid_len, causal, sm_scale as attn_fwd.  B*H <= 65535; the
+ * naive kernel keeps a query's L scores in shared memory (L <= 50000).
+ * Errors as attn_fwd (ATTN_ERR_ARG for an unknown kernel).
+ */
+attn_status_t attn_fwd_f32(const float* q, const float* k, const float* v, float* o, float* lse,
+                           int B, int H, int L, int D, float sm_scale, int causal,
+                           const int32_t* valid_len, attn_f32_kernel_t kernel,
+                           attn_stream_t stream);
+
 /*
  * attn_fwd_noalloc -- attn_fwd for callers that must not allocate device
  * memory.  The pages have no counterpart: this is a deployment variant.

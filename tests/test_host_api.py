@@ -201,3 +201,25 @@ def test_masked_valid_arguments_need_a_device(lib, kw):
     if torch.cuda.is_available():
         pytest.skip("a GPU is present; covered by the gpu tests")
     assert binding.STATUS_NAMES[_mcall(**kw)] in ("ATTN_ERR_CUDA", "ATTN_ERR_ARCH")
+
+
+# ------------------------------------------------------------------ attn_fwd_f32
+
+@pytest.mark.parametrize("args, expected", [
+    (dict(q=None), "ATTN_ERR_NULL"),
+    (dict(L=0), "ATTN_ERR_SHAPE"),
+    (dict(D=32), "ATTN_ERR_HEADDIM"),
+    (dict(kernel=3), "ATTN_ERR_ARG"),
+    (dict(causal=5), "ATTN_ERR_ARG"),
+    (dict(sm_scale=float("nan")), "ATTN_ERR_SCALE"),
+    (dict(B=300, H=300), "ATTN_ERR_SHAPE"),
+    (dict(L=60000, kernel=0), "ATTN_ERR_SHAPE"),
+    (dict(o=A16 + 2), "ATTN_ERR_ALIGN"),
+])
+def test_f32_invalid_arguments_rejected_on_host(lib, args, expected):
+    a = dict(q=A16, k=A16, v=A16, o=A16, lse=None, B=1, H=8, L=1024, D=64, sm_scale=0.125,
+             causal=1, valid_len=None, kernel=2, stream=None)
+    a.update(args)
+    st = lib.attn_fwd_f32(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["L"], a["D"],
+                          a["sm_scale"], a["causal"], a["valid_len"], a["kernel"], a["stream"])
+    assert binding.STATUS_NAMES[st] == expected
