@@ -59,6 +59,9 @@ def _bind(path: str):
     lib.oracle_attn_fwd_u16.argtypes = [p, p, p, p, p, i, i, i, i, i, i, ctypes.c_double,
                                         i, p, p, i64, i64, i, p, i64, i]
     lib.oracle_attn_fwd_u16.restype = i
+    lib.oracle_attn_bwd_f64.argtypes = [p, p, p, p, p, p, p, i, i, i, i, i, ctypes.c_double, i,
+                                        p, i]
+    lib.oracle_attn_bwd_f64.restype = i
     lib.oracle_decode.argtypes = [p, p, i64, i]
     lib.oracle_decode.restype = i
     lib.oracle_max_threads.argtypes = []
@@ -189,6 +192,29 @@ def attn_fwd_bits(q_bits, k_bits, v_bits, dtype, sm_scale, causal=False, valid_l
     if r is None:
         return o.reshape(B, Hq, Lq, D), lse.reshape(B * Hq, Lq)
     return o, lse
+
+
+def attn_bwd_f64(q, k, v, do, sm_scale, causal=False, valid_len=None, threads=0,
+                 _lib_override=None):
+    """Gradients (dq, dk, dv) of the attention forward for an output gradient
+    ``do``, from the definition (see oracle_attn_bwd_f64).  q, do:
+    [B, Hq, L, D]; k, v: [B, Hkv, L, D]; float64 results of the same shapes."""
+    q = np.ascontiguousarray(q, dtype=np.float64)
+    k = np.ascontiguousarray(k, dtype=np.float64)
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    do = np.ascontiguousarray(do, dtype=np.float64)
+    B, Hq, Hkv, Lq, Lk, D = _shapes(q, k, v)
+    if Lq != Lk or do.shape != q.shape:
+        raise ValueError("the backward oracle takes Lq == Lk and do shaped like q")
+    vl = _valid(valid_len, B)
+    dq, dk, dv = np.empty_like(q), np.empty_like(k), np.empty_like(v)
+    lib = _lib_override if _lib_override is not None else _load()
+    rc = lib.oracle_attn_bwd_f64(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv),
+                                 B, Hq, Hkv, Lq, D, float(sm_scale), int(bool(causal)), _ptr(vl),
+                                 int(threads))
+    if rc != 0:
+        raise ValueError("oracle_attn_bwd_f64 failed with code %d" % rc)
+    return dq, dk, dv
 
 
 def load_variant(path: str):

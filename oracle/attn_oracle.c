@@ -235,3 +235,105 @@ int oracle_max_threads(void) {
   return 1;
 #endif
 }
+
+/*
+ * Backward of the same operation, from its definition (the pages store the
+ * log-sum-exp "for the backward pass" -- tiny_flash_attn_triton.py -- but give
+ * no backward algorithm, so this is the derivative of
+ *   O = softmax(S) V,  S = sm_scale * Q K^T restricted to the visible keys,
+ * written out with the chain rule).  For a loss with gradient dO:
+ *   P_ij = exp(S_ij) / sum_j' exp(S_ij')            (visible j; 0 otherwise)
+ *   dV_j = sum_i P_ij dO_i
+ *   dP_ij = dO_i . V_j
+ *   dS_ij = P_ij (dP_ij - sum_j' P_ij' dP_ij')      (softmax Jacobian)
+ *   dQ_i = sm_scale sum_j dS_ij K_j,   dK_j = sm_scale sum_i dS_ij Q_i
+ * with K_j, V_j of head h_kv = h_q / (Hq/Hkv); dK and dV of a key/value head
+ * sum over the query heads that read it.  Rows without a visible key give
+ * nothing.  Float64, plain loops, one (b, h_kv) group per OpenMP task.
+ *
+ * q, dO: [B, Hq, L, D]; k, v: [B, Hkv, L, D]; dq like q, dk and dv like k.
+ * Returns 0, 1 on invalid arguments, 2 when scratch could not be allocated.
+ */
+int oracle_attn_bwd_f64(const double* q, const double* k, const double* v, const double* dO,
+                        double* dq, double* dk, double* dv, int B, int Hq, int Hkv, int L, int D,
+                        double sm_scale, int causal, const int32_t* valid_len, int threads) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || L < 1 || D < 1 || Hq % Hkv != 0) return 1;
+  const int G = Hq / Hkv;
+  const oracle_mask_t mk = {NULL, 0, 0};
+  memset(dq, 0, sizeof(double) * (size_t)B * Hq * L * D);
+  memset(dk, 0, sizeof(double) * (size_t)B * Hkv * L * D);
+  memset(dv, 0, sizeof(double) * (size_t)B * Hkv * L * D);
+#ifdef _OPENMP
+  if (threads > 0) omp_set_num_threads(threads);
+#else
+  (void)threads;
+#endif
+  int bad = 0;
+#pragma omp parallel
+  {
+    double* p = (double*)malloc(sizeof(double) * (size_t)L);   /* P_i. of one row */
+    double* dp = (double*)malloc(sizeof(double) * (size_t)L);  /* dP_i. of one row */
+    if (!p || !dp) {
+#pragma omp atomic write
+      bad = 1;
+    }
+#pragma omp for schedule(dynamic, 1)
+    for (int64_t grp = 0; grp < (int64_t)B * Hkv; ++grp) {
+      if (!p || !dp) continue;
+      const int b = (int)(grp / Hkv);
+      const int h_kv = (int)(grp % Hkv);
+      const double* k_head = k + grp * L * (int64_t)D;
+      const double* v_head = v + grp * L * (int64_t)D;
+      double* dk_head = dk + grp * L * (int64_t)D;
+      double* dv_head = dv + grp * L * (int64_t)D;
+      for (int g = 0; g < G; ++g) {
+        const int h_q = h_kv * G + g;
+        const int64_t qh = (int64_t)b * Hq + h_q;
+        for (int64_t i = 0; i < L; ++i) {
+          const double* q_row = q + (qh * L + i) * D;
+          const double* do_row = dO + (qh * L + i) * D;
+          double* dq_row = dq + (qh * L + i) * D;
+          /* P_i. by the definition (max subtracted for the exponentials) */
+          double m = -INFINITY;
+          int any = 0;
+          for (int64_t j = 0; j < L; ++j) {
+            if (!key_visible(i, j, b, causal, valid_len, &mk)) continue;
+            double dot = 0.0;
+            for (int d = 0; d < D; ++d) dot += q_row[d] * k_head[j * D + d];
+            p[j] = sm_scale * dot;
+            if (p[j] > m) m = p[j];
+            any = 1;
+          }
+          if (!any) continue;
+          double z = 0.0;
+          for (int64_t j = 0; j < L; ++j) {
+            if (!key_visible(i, j, b, causal, valid_len, &mk)) continue;
+            p[j] = exp(p[j] - m);
+            z += p[j];
+          }
+          double pdp = 0.0; /* sum_j P_ij dP_ij */
+          for (int64_t j = 0; j < L; ++j) {
+            if (!key_visible(i, j, b, causal, valid_len, &mk)) continue;
+            p[j] /= z;
+            double dot = 0.0;
+            for (int d = 0; d < D; ++d) dot += do_row[d] * v_head[j * D + d];
+            dp[j] = dot;
+            pdp += p[j] * dot;
+          }
+          for (int64_t j = 0; j < L; ++j) {
+            if (!key_visible(i, j, b, causal, valid_len, &mk)) continue;
+            const double ds = p[j] * (dp[j] - pdp);
+            for (int d = 0; d < D; ++d) {
+              dv_head[j * D + d] += p[j] * do_row[d];
+              dq_row[d] += sm_scale * ds * k_head[j * D + d];
+              dk_head[j * D + d] += sm_scale * ds * q_row[d];
+            }
+          }
+        }
+      }
+    }
+    free(p);
+    free(dp);
+  }
+  return bad ? 2 : 0;
+}
