@@ -95,6 +95,9 @@ def load():
             lib.attn_fwd_masked.argtypes = [p, sp, p, sp, p, sp, p, sp, p, i, i, i, i, i, i,
                                             ctypes.c_float, i, p, p, i64, i64, i, p]
             lib.attn_fwd_masked.restype = i
+            lib.attn_bwd.argtypes = [p, p, p, p, p, p, p, p, p, i, i, i, i, i, ctypes.c_float, i, p,
+                                     i, p]
+            lib.attn_bwd.restype = i
             lib.attn_fwd_f32.argtypes = [p, p, p, p, p, i, i, i, i, ctypes.c_float, i, p, i, p]
             lib.attn_fwd_f32.restype = i
             lib.attn_host_plan.argtypes = [i, i, i, i, i, i, ctypes.POINTER(Chunk), i,
@@ -428,3 +431,28 @@ def attn_fwd_f32(q, k, v, *, kernel="tiled_rowmax", causal=False, sm_scale=None,
     if st != ATTN_OK:
         raise AttnError(st, "attn_fwd_f32")
     return out, (lse if return_lse else None)
+
+
+def attn_bwd(q, k, v, o, lse, do, *, causal=False, sm_scale=None, valid_len=None, stream=None):
+    """Gradients (dq, dk, dv) of attn_fwd for the output gradient ``do``,
+    through attn_bwd.  q, o, do: [B, Hq, L, D]; k, v: [B, Hkv, L, D] (fp16 or
+    bf16, contiguous CUDA tensors); lse: the forward's [B*Hq, L] fp32 LSE."""
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("do", do)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("%s must be a contiguous CUDA tensor" % name)
+    B, Hq, L, D = q.shape
+    Hkv = k.shape[1]
+    if sm_scale is None:
+        sm_scale = 1.0 / float(D) ** 0.5
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    vl_ptr = None
+    if valid_len is not None:
+        vl_ptr = valid_len.data_ptr()
+    st = int(load().attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
+                             lse.contiguous().data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                             dv.data_ptr(), B, Hq, Hkv, L, D, float(sm_scale), int(bool(causal)),
+                             vl_ptr, _dtype_code(q), _stream_handle(stream)))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_bwd")
+    return dq, dk, dv

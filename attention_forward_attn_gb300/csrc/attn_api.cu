@@ -469,6 +469,44 @@ attn_status_t attn_fwd_f32(const float* q, const float* k, const float* v, float
   return ATTN_OK;
 }
 
+attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                       const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv,
+                       int L, int D, float sm_scale, int causal, const int32_t* valid_len,
+                       attn_dtype_t dtype, attn_stream_t stream) {
+  if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_DTYPE;
+  if (q == nullptr || k == nullptr || v == nullptr || o == nullptr || dO == nullptr ||
+      lse == nullptr || dq == nullptr || dk == nullptr || dv == nullptr)
+    return ATTN_ERR_NULL;
+  if (B < 1 || Hq < 1 || Hkv < 1 || L < 1) return ATTN_ERR_SHAPE;
+  if (D != 64 && D != 128) return ATTN_ERR_HEADDIM;
+  if (Hq % Hkv != 0) return ATTN_ERR_HEADS;
+  if (causal != 0 && causal != 1) return ATTN_ERR_ARG;
+  if (!(sm_scale >= 0.f) || isinf(sm_scale)) return ATTN_ERR_SCALE;
+  if (static_cast<int64_t>(B) * Hq * L > INT32_MAX || static_cast<int64_t>(B) * Hq > 65535)
+    return ATTN_ERR_SHAPE;
+  const void* p16[] = {q, k, v, o, dO, dq, dk, dv};
+  for (const void* ptr : p16)
+    if (!aligned(ptr, 2)) return ATTN_ERR_ALIGN;
+  if (!aligned(lse, 4) || (valid_len != nullptr && !aligned(valid_len, 4))) return ATTN_ERR_ALIGN;
+  int dev = 0;
+  DeviceState* st = nullptr;
+  attn_status_t s = device_state(&dev, &st);
+  if (s != ATTN_OK) return s;
+  cudaMemPool_t pool = nullptr;
+  if ((s = workspace_pool(dev, st, &pool)) != ATTN_OK) return s;
+  const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  void* ws = nullptr;
+  cudaError_t e = cudaMallocFromPoolAsync(&ws, static_cast<size_t>(attn::bwd_workspace_bytes(B, Hq, L)),
+                                          pool, cs);
+  if (e != cudaSuccess) return cuda_fail(e);
+  e = attn::launch_bwd(q, k, v, o, dO, lse, dq, dk, dv, static_cast<float*>(ws), B, Hq, Hkv, L, D,
+                       sm_scale, causal, valid_len, dtype == ATTN_BF16, cs);
+  const cudaError_t ef = cudaFreeAsync(ws, cs);
+  if (e == cudaSuccess) e = ef;
+  if (e != cudaSuccess) return cuda_fail(e);
+  return ATTN_OK;
+}
+
 attn_status_t attn_status(attn_stream_t stream, int* device_code) {
   if (device_code != nullptr) *device_code = 0;
   cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));

@@ -98,6 +98,14 @@ cudaError_t launch_f32(const float* q, const float* k, const float* v, float* o,
                        int B, int H, int L, int D, float sm_scale, int causal,
                        const int32_t* valid_len, int kernel, int* status, cudaStream_t stream);
 
+// Backward (attn_bwd.cu): bytes of its workspace (delta, fp32 [B*Hq, L])
+// and its launch (delta, dQ and dK/dV kernels on `stream`).
+int64_t bwd_workspace_bytes(int B, int Hq, int L);
+cudaError_t launch_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                       const float* lse, void* dq, void* dk, void* dv, float* delta, int B, int Hq,
+                       int Hkv, int L, int D, float sm_scale, int causal, const int32_t* valid_len,
+                       bool bf16, cudaStream_t stream);
+
 // SIMT cross-check forward.
 cudaError_t launch_simt(const Problem& p);
 

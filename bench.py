@@ -646,6 +646,66 @@ def run_relative_table(args, local):
             "data": "synthetic N(0,1), seed 26"}
 
 
+def run_backward(args, local):
+    """attn_bwd on the C4 and C2 shapes: ms per call (delta, dQ and dK/dV
+    kernels) with the forward's O and LSE already on the device, L2 flushed
+    before each call.  Work: the backward's five products (S recomputed, dP,
+    dQ, dK, dV) = 2.5x the forward's nominal FLOPs.  Roofline: the SIMT
+    kernels run on the FP32 units: 152 SMs x 128 FMA lanes x 2 FLOP x the
+    2070 MHz maximum SM clock = 80.6 TFLOP/s."""
+    import attention_forward_attn_gb300 as attn
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    attn.load()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    peaks, _src = load_peaks()
+    fp32_peak = 152 * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+    lines = []
+    for name in ("C4", "C2"):
+        w = wl.WORKLOADS[name]
+        q, k, v, vl = wl.workload_inputs(w)
+        q_d, k_d, v_d = q.to(dev), k.to(dev), v.to(dev)
+        vl_d = None if vl is None else vl.to(dev)
+        gen = torch.Generator().manual_seed(w.seed + 100)
+        do = torch.randn(q.shape, generator=gen).to(q.dtype).to(dev)
+        o, lse = attn.attn_fwd(q_d, k_d, v_d, causal=w.causal, sm_scale=w.sm_scale, valid_len=vl_d)
+
+        def call():
+            return attn.attn_bwd(q_d, k_d, v_d, o, lse, do, causal=w.causal, sm_scale=w.sm_scale,
+                                 valid_len=vl_d)
+
+        for _ in range(max(1, min(args.warmup, 3))):
+            flush.zero_()
+            call()
+        n = max(3, min(args.steps, 10))
+        ts = []
+        for _ in range(n):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            call()
+            e1.record()
+            torch.cuda.synchronize(dev)
+            ts.append(e0.elapsed_time(e1))
+        st, code = attn.status()
+        if st != 0:
+            raise RuntimeError("device status %d (code %#x)" % (st, code))
+        ms = sorted(ts)[n // 2]
+        tf = 2.5 * nominal_flops(w) / (ms * 1e-3) / 1e12
+        lines.append({"metric": "attention backward TFLOP/s (2.5x the forward's nominal FLOPs)",
+                      "workload": "%s shapes: %s" % (name, w.description), "value": round(tf, 3),
+                      "unit": "TFLOP/s", "ms_per_call": round(ms, 3),
+                      "roofline": {"bound": "alu", "achieved": round(tf, 3),
+                                   "peak": round(fp32_peak, 1), "unit": "TFLOP/s",
+                                   "frac": round(tf / fp32_peak, 4),
+                                   "peak_source": "152 SMs x 128 FP32 lanes x 2 x sm_max_mhz"},
+                      "timing": "median of %d calls, L2 flushed before each" % n,
+                      "dtype": w.dtype, "data": "synthetic"})
+        del q_d, k_d, v_d, o, lse, do
+        torch.cuda.empty_cache()
+    return lines
+
+
 def _oracle_threads() -> int:
     import oracle
     return oracle.max_threads()
@@ -715,6 +775,8 @@ def main(argv=None):
                     help="instead of the headline line, one line per explicit-mask workload")
     ap.add_argument("--relative-table", action="store_true",
                     help="instead of the headline line, the section 6.1 comparison table")
+    ap.add_argument("--backward", action="store_true",
+                    help="instead of the headline line, one line per backward workload")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -726,6 +788,11 @@ def main(argv=None):
     if args.impl == "reference":
         if rank == 0:
             print(json.dumps(run_reference(args, w)), flush=True)
+        return 0
+    if args.backward:
+        if rank == 0:
+            for line in run_backward(args, local):
+                print(json.dumps(line), flush=True)
         return 0
     if args.relative_table:
         if rank == 0:

@@ -216,6 +216,36 @@ attn_status_t attn_fwd_simt(const void* q, const void* k, const void* v, void* o
                             int B, int Hq, int Hkv, int L, int D, float sm_scale, int causal,
                             const int32_t* valid_len, attn_dtype_t dtype, attn_stream_t stream);
 
+/*
+ * attn_bwd -- gradients of attn_fwd: dQ, dK, dV for an output gradient dO.
+ *
+ * Defined by: tiny_flash_attn_triton.py stores the per-row log-sum-exp "for
+ * the backward pass"; the pages give no backward algorithm, so this is the
+ * derivative of O = softmax(sm_scale Q K^T + Mask) V from its definition,
+ * with the softmax rebuilt from that LSE: P_ij = exp(sm_scale q_i.k_j - LSE_i)
+ * on the visible keys, delta_i = dO_i . O_i, dS_ij = P_ij (dO_i.v_j - delta_i),
+ * dQ = sm_scale dS K, dK = sm_scale dS^T Q, dV = P^T dO; dK and dV of a
+ * key/value head sum over the query heads that read it (GQA/MQA).
+ *
+ * Arguments (device pointers, caller-owned; same layouts, dtype and masks as
+ * attn_fwd, 2-byte aligned):
+ *   q, k, v    the forward's inputs;  o the forward's output;
+ *   dO         [B, Hq, L, D] output gradient;
+ *   lse        [B*Hq, L] fp32, the forward's natural-log LSE (required);
+ *   dq         [B, Hq, L, D] out;  dk, dv  [B, Hkv, L, D] out (overwritten).
+ *   D          64 or 128.  B*Hq <= 65535.
+ * Work: SIMT kernels with fp32 arithmetic (delta; dQ per 64-row query tile;
+ * dK/dV per 64-key tile with all query heads of its group), the results
+ * rounded once to the input dtype.  Device memory: a stream-ordered fp32
+ * workspace of B*Hq*L*4 bytes from the library's pool.
+ * Errors: argument errors as attn_fwd (nothing is queued); device-side
+ * conditions through attn_status.
+ */
+attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                       const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv,
+                       int L, int D, float sm_scale, int causal, const int32_t* valid_len,
+                       attn_dtype_t dtype, attn_stream_t stream);
+
 /* The fp32 comparison kernels of attn_fwd_f32. */
 typedef enum {
   ATTN_F32_NAIVE = 0,          /* three passes over the keys per query */

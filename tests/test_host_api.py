@@ -223,3 +223,27 @@ def test_f32_invalid_arguments_rejected_on_host(lib, args, expected):
     st = lib.attn_fwd_f32(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["L"], a["D"],
                           a["sm_scale"], a["causal"], a["valid_len"], a["kernel"], a["stream"])
     assert binding.STATUS_NAMES[st] == expected
+
+
+# ------------------------------------------------------------------ attn_bwd
+
+@pytest.mark.parametrize("args, expected", [
+    (dict(dtype=4), "ATTN_ERR_DTYPE"),
+    (dict(lse=None), "ATTN_ERR_NULL"),
+    (dict(dv=None), "ATTN_ERR_NULL"),
+    (dict(L=0), "ATTN_ERR_SHAPE"),
+    (dict(D=32), "ATTN_ERR_HEADDIM"),
+    (dict(Hq=6, Hkv=4), "ATTN_ERR_HEADS"),
+    (dict(causal=3), "ATTN_ERR_ARG"),
+    (dict(sm_scale=-2.0), "ATTN_ERR_SCALE"),
+    (dict(dq=A16 + 1), "ATTN_ERR_ALIGN"),
+])
+def test_bwd_invalid_arguments_rejected_on_host(lib, args, expected):
+    a = dict(q=A16, k=A16, v=A16, o=A16, do=A16, lse=A16, dq=A16, dk=A16, dv=A16, B=1, Hq=4,
+             Hkv=2, L=64, D=64, sm_scale=0.125, causal=1, valid_len=None, dtype=attn.ATTN_BF16,
+             stream=None)
+    a.update(args)
+    st = lib.attn_bwd(a["q"], a["k"], a["v"], a["o"], a["do"], a["lse"], a["dq"], a["dk"], a["dv"],
+                      a["B"], a["Hq"], a["Hkv"], a["L"], a["D"], a["sm_scale"], a["causal"],
+                      a["valid_len"], a["dtype"], a["stream"])
+    assert binding.STATUS_NAMES[st] == expected
