@@ -484,9 +484,9 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
   if (!(sm_scale >= 0.f) || isinf(sm_scale)) return ATTN_ERR_SCALE;
   if (static_cast<int64_t>(B) * Hq * L > INT32_MAX || static_cast<int64_t>(B) * Hq > 65535)
     return ATTN_ERR_SHAPE;
-  const void* p16[] = {q, k, v, o, dO, dq, dk, dv};
+  const void* p16[] = {q, k, v, o, dO, dq, dk, dv};  // 16-byte vector loads and stores
   for (const void* ptr : p16)
-    if (!aligned(ptr, 2)) return ATTN_ERR_ALIGN;
+    if (!aligned(ptr, 16)) return ATTN_ERR_ALIGN;
   if (!aligned(lse, 4) || (valid_len != nullptr && !aligned(valid_len, 4))) return ATTN_ERR_ALIGN;
   int dev = 0;
   DeviceState* st = nullptr;

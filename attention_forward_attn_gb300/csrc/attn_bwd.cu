@@ -22,8 +22,9 @@
 //     query head of the group and every query tile that sees the keys stream
 //     through; P and dS of each block stay in shared memory, dK and dV
 //     accumulate in registers and are written once (no atomics).
-// Shared-memory rows are padded by one float, so that threads reading the
-// same column of different rows hit different banks.
+// Each thread owns 4 x 4 blocks of (query, key) pairs and of the dQ / dK / dV
+// products; the dot products read 16-byte vectors of transposed [D][64]
+// shared-memory tiles (one pair of loads per 16 FMAs).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <math.h>
@@ -78,23 +79,66 @@ __device__ __forceinline__ int kv_len_of(const BwdProblem& p, int b) {
   return vl < 0 ? 0 : (vl > p.L ? p.L : vl);
 }
 
-// Stage `rows` rows of a [.., L, D] 16-bit head (row r0 onwards) into fp32
-// shared memory with row stride D + 1; rows past L are zeros.
+// Stage rows r0 .. r0+63 of a [.., L, D] 16-bit head into fp32 shared memory
+// (rows past L are zeros).  Row-major [64][D]: consecutive threads take
+// consecutive columns.  Transposed [D][64]: a thread loads 8 columns of one row
+// with one 16-byte load and consecutive threads take consecutive rows, so a
+// warp's stores of one column fill 32 banks.
 template <int D, bool BF16>
-__device__ __forceinline__ void stage(float* dst, const void* src, int64_t head_row0, int r0,
-                                      int L) {
+__device__ __forceinline__ void stage_rm(float* rm, const void* src, int64_t head_row0, int r0,
+                                         int L) {
   for (int t = threadIdx.x; t < kT * D; t += kThreadsBwd) {
     const int r = t / D, c = t % D;
-    dst[r * (D + 1) + c] = r0 + r < L ? ld16<BF16>(src, (head_row0 + r0 + r) * D + c) : 0.f;
+    rm[r * D + c] = r0 + r < L ? ld16<BF16>(src, (head_row0 + r0 + r) * D + c) : 0.f;
   }
 }
 
+template <bool BF16>
+__device__ __forceinline__ float2 unpack16x2(uint32_t w) {
+  if constexpr (BF16) {
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+  } else {
+    return __half22float2(*reinterpret_cast<const __half2*>(&w));
+  }
+}
+
+template <int D, bool BF16>
+__device__ __forceinline__ void stage_tr(float* tr, const void* src, int64_t head_row0, int r0,
+                                         int L) {
+  for (int t = threadIdx.x; t < kT * (D / 8); t += kThreadsBwd) {
+    const int r = t % kT, c0 = (t / kT) * 8;
+    uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+    if (r0 + r < L)
+      raw = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(src) +
+                                            (head_row0 + r0 + r) * D + c0);
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 f = unpack16x2<BF16>(w[k]);
+      tr[(c0 + 2 * k) * kT + r] = f.x;
+      tr[(c0 + 2 * k + 1) * kT + r] = f.y;
+    }
+  }
+}
+
+__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+
+// 4x4 block of dot products: acc[a][b] += sum_e A[e][a0+a] B[e][b0+b] over
+// transposed [D][64] tiles (one 16-byte load of each operand per e).
 template <int D>
-__device__ __forceinline__ float dot_rows(const float* a, const float* b) {
-  float s = 0.f;
-#pragma unroll 16
-  for (int e = 0; e < D; ++e) s = fmaf(a[e], b[e], s);
-  return s;
+__device__ __forceinline__ void dot4x4(float (&acc)[4][4], const float* at, const float* bt, int a0,
+                                       int b0) {
+#pragma unroll 4
+  for (int e = 0; e < D; ++e) {
+    const float4 x = ld4(at + e * kT + a0);
+    const float4 y = ld4(bt + e * kT + b0);
+    const float xa[4] = {x.x, x.y, x.z, x.w};
+    const float yb[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(xa[a], yb[b], acc[a][b]);
+  }
 }
 
 // ------------------------------------------------------------------ delta
@@ -113,23 +157,28 @@ __global__ void __launch_bounds__(kThreadsBwd) bwd_delta_kernel(BwdProblem p, in
 
 // ------------------------------------------------------------------ dQ
 
+// Thread (ti, tj) of a 16 x 16 grid owns the 4 x 4 block of (query, key)
+// pairs (4 ti + a, 4 tj + b) of a 64 x 64 block, and the 4 x D/16 block of dQ
+// (rows 4 ti + a, columns tj + 16 c).
 template <int D>
 constexpr int dq_smem() {
-  return (4 * kT * (D + 1) + kT * (kT + 1) + 2 * kT) * static_cast<int>(sizeof(float));
+  // Q^T, dO^T, K^T, V^T [D][64]; K [64][D]; dS^T [64 keys][64]; LSE, delta
+  return (5 * kT * D + kT * kT + 2 * kT) * static_cast<int>(sizeof(float));
 }
 
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kThreadsBwd) bwd_dq_kernel(BwdProblem p) {
   extern __shared__ float sm[];
-  float* qs = sm;                       // [kT][D+1]
-  float* dos = qs + kT * (D + 1);       // [kT][D+1]
-  float* ks = dos + kT * (D + 1);       // [kT][D+1]
-  float* vs = ks + kT * (D + 1);        // [kT][D+1]
-  float* ds = vs + kT * (D + 1);        // [kT][kT+1]  dS of the block
-  float* lse_s = ds + kT * (kT + 1);    // [kT]
-  float* del_s = lse_s + kT;            // [kT]
-  constexpr int kGroups = kThreadsBwd / D;  // row groups of the dQ product
-  constexpr int kRowsPer = kT / kGroups;    // dQ rows per thread
+  float* qt = sm;                 // [D][64]
+  float* dot_ = qt + kT * D;      // [D][64]
+  float* kt = dot_ + kT * D;      // [D][64]
+  float* vt = kt + kT * D;        // [D][64]
+  float* kr = vt + kT * D;        // [64][D]
+  float* dst = kr + kT * D;       // [64 keys][64 queries]
+  float* lse_s = dst + kT * kT;   // [64]
+  float* del_s = lse_s + kT;      // [64]
+  constexpr int CQ = D / 16;      // dQ columns per thread
+  const int ti = threadIdx.x / 16, tj = threadIdx.x % 16;
   const int bh = blockIdx.y;
   const int b = bh / p.Hq;
   const int h_kv = (bh % p.Hq) / (p.Hq / p.Hkv);
@@ -137,136 +186,169 @@ __global__ void __launch_bounds__(kThreadsBwd) bwd_dq_kernel(BwdProblem p) {
   const int64_t q_row0 = static_cast<int64_t>(bh) * p.L;
   const int64_t kv_row0 = (static_cast<int64_t>(b) * p.Hkv + h_kv) * p.L;
   const int kv = kv_len_of(p, b);
-  stage<D, BF16>(qs, p.q, q_row0, i0, p.L);
-  stage<D, BF16>(dos, p.dO, q_row0, i0, p.L);
+  stage_tr<D, BF16>(qt, p.q, q_row0, i0, p.L);
+  stage_tr<D, BF16>(dot_, p.dO, q_row0, i0, p.L);
   for (int t = threadIdx.x; t < kT; t += kThreadsBwd) {
     const bool in = i0 + t < p.L;
     lse_s[t] = in ? p.lse[q_row0 + i0 + t] : -INFINITY;
     del_s[t] = in ? p.delta[q_row0 + i0 + t] : 0.f;
   }
-  float acc[kRowsPer];
+  float acc[4][CQ];
 #pragma unroll
-  for (int r = 0; r < kRowsPer; ++r) acc[r] = 0.f;
-  const int dcol = threadIdx.x % D, rgrp = threadIdx.x / D;
-  // keys any row of the tile sees: j < kv, and j <= the last row when causal
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int c = 0; c < CQ; ++c) acc[a][c] = 0.f;
   const int j_end = p.causal ? min(kv, i0 + kT) : kv;
   for (int j0 = 0; j0 < j_end; j0 += kT) {
     __syncthreads();
-    stage<D, BF16>(ks, p.k, kv_row0, j0, p.L);
-    stage<D, BF16>(vs, p.v, kv_row0, j0, p.L);
+    stage_rm<D, BF16>(kr, p.k, kv_row0, j0, p.L);
+    stage_tr<D, BF16>(kt, p.k, kv_row0, j0, p.L);
+    stage_tr<D, BF16>(vt, p.v, kv_row0, j0, p.L);
     __syncthreads();
-    // dS of the 64x64 block, one element per thread per pass
-    for (int e = threadIdx.x; e < kT * kT; e += kThreadsBwd) {
-      const int il = e / kT, jl = e % kT;
-      const int i = i0 + il, j = j0 + jl;
-      float d = 0.f;
+    float sc[4][4] = {}, dp[4][4] = {};
+    dot4x4<D>(sc, qt, kt, 4 * ti, 4 * tj);
+    dot4x4<D>(dp, dot_, vt, 4 * ti, 4 * tj);
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+      const int il = 4 * ti + a, i = i0 + il;
       const float lse = lse_s[il];
-      if (j < kv && (!p.causal || j <= i) && lse != -INFINITY) {
-        const float s = dot_rows<D>(qs + il * (D + 1), ks + jl * (D + 1)) * p.scale;
-        const float pr = expf(s - lse);
-        const float dp = dot_rows<D>(dos + il * (D + 1), vs + jl * (D + 1));
-        d = pr * (dp - del_s[il]);
+#pragma unroll
+      for (int bb = 0; bb < 4; ++bb) {
+        const int jl = 4 * tj + bb, j = j0 + jl;
+        float d = 0.f;
+        if (j < kv && (!p.causal || j <= i) && lse != -INFINITY)
+          d = expf(sc[a][bb] * p.scale - lse) * (dp[a][bb] - del_s[il]);
+        dst[jl * kT + il] = d;
       }
-      ds[il * (kT + 1) + jl] = d;
     }
     __syncthreads();
     // dQ_i += sum_j dS_ij k_j
     for (int jl = 0; jl < kT; ++jl) {
-      const float kv_ = ks[jl * (D + 1) + dcol];
+      const float4 d4 = ld4(dst + jl * kT + 4 * ti);
+      const float da[4] = {d4.x, d4.y, d4.z, d4.w};
 #pragma unroll
-      for (int r = 0; r < kRowsPer; ++r) acc[r] = fmaf(ds[(rgrp + kGroups * r) * (kT + 1) + jl], kv_, acc[r]);
+      for (int c = 0; c < CQ; ++c) {
+        const float kv_ = kr[jl * D + tj + 16 * c];
+#pragma unroll
+        for (int a = 0; a < 4; ++a) acc[a][c] = fmaf(da[a], kv_, acc[a][c]);
+      }
     }
   }
 #pragma unroll
-  for (int r = 0; r < kRowsPer; ++r) {
-    const int i = i0 + rgrp + kGroups * r;
-    if (i < p.L) st16<BF16>(p.dq, (q_row0 + i) * D + dcol, acc[r] * p.scale);
+  for (int a = 0; a < 4; ++a) {
+    const int i = i0 + 4 * ti + a;
+    if (i < p.L) {
+#pragma unroll
+      for (int c = 0; c < CQ; ++c) st16<BF16>(p.dq, (q_row0 + i) * D + tj + 16 * c, acc[a][c] * p.scale);
+    }
   }
 }
 
 // ------------------------------------------------------------------ dK, dV
 
+// Thread (ti, tj): the 4 x 4 block of (key, query) pairs (4 ti + a, 4 tj + b)
+// of a 64 x 64 block, and the 4 x D/16 blocks of dK and dV (rows 4 ti + a,
+// columns tj + 16 c).
 template <int D>
 constexpr int dkv_smem() {
-  return (4 * kT * (D + 1) + 2 * kT * (kT + 1) + 2 * kT) * static_cast<int>(sizeof(float));
+  // K^T, V^T, Q^T, dO^T [D][64]; Q, dO [64][D]; P, dS [64 queries][64 keys]; LSE, delta
+  return (6 * kT * D + 2 * kT * kT + 2 * kT) * static_cast<int>(sizeof(float));
 }
 
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kThreadsBwd) bwd_dkv_kernel(BwdProblem p) {
   extern __shared__ float sm[];
-  float* ks = sm;                       // [kT][D+1] resident
-  float* vs = ks + kT * (D + 1);        // [kT][D+1] resident
-  float* qs = vs + kT * (D + 1);        // [kT][D+1]
-  float* dos = qs + kT * (D + 1);       // [kT][D+1]
-  float* pt = dos + kT * (D + 1);       // [kT keys][kT+1]  P^T of the block
-  float* dst = pt + kT * (kT + 1);      // [kT keys][kT+1]  dS^T of the block
-  float* lse_s = dst + kT * (kT + 1);   // [kT]
-  float* del_s = lse_s + kT;            // [kT]
-  constexpr int kGroups = kThreadsBwd / D;
-  constexpr int kRowsPer = kT / kGroups;  // dK/dV rows per thread
-  const int bkv = blockIdx.y;             // b * Hkv + h_kv
+  float* kt = sm;                  // [D][64] resident
+  float* vt = kt + kT * D;         // [D][64] resident
+  float* qt = vt + kT * D;         // [D][64]
+  float* dot_ = qt + kT * D;       // [D][64]
+  float* qr = dot_ + kT * D;       // [64][D]
+  float* dor = qr + kT * D;        // [64][D]
+  float* pq = dor + kT * D;        // [64 queries][64 keys]  P
+  float* dq = pq + kT * kT;        // [64 queries][64 keys]  dS
+  float* lse_s = dq + kT * kT;     // [64]
+  float* del_s = lse_s + kT;       // [64]
+  constexpr int CK = D / 16;
+  const int ti = threadIdx.x / 16, tj = threadIdx.x % 16;
+  const int bkv = blockIdx.y;      // b * Hkv + h_kv
   const int b = bkv / p.Hkv;
   const int h_kv = bkv % p.Hkv;
   const int G = p.Hq / p.Hkv;
   const int j0 = blockIdx.x * kT;
   const int64_t kv_row0 = static_cast<int64_t>(bkv) * p.L;
   const int kv = kv_len_of(p, b);
-  const int dcol = threadIdx.x % D, rgrp = threadIdx.x / D;
-  float dk[kRowsPer], dv[kRowsPer];
+  float dk[4][CK], dv[4][CK];
 #pragma unroll
-  for (int r = 0; r < kRowsPer; ++r) dk[r] = dv[r] = 0.f;
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int c = 0; c < CK; ++c) dk[a][c] = dv[a][c] = 0.f;
   if (j0 < kv) {  // keys at or past valid_len have no gradient
-    stage<D, BF16>(ks, p.k, kv_row0, j0, p.L);
-    stage<D, BF16>(vs, p.v, kv_row0, j0, p.L);
-    // query rows that can see a key of the tile: i >= j0 when causal
-    const int i_begin = p.causal ? (j0 / kT) * kT : 0;
+    stage_tr<D, BF16>(kt, p.k, kv_row0, j0, p.L);
+    stage_tr<D, BF16>(vt, p.v, kv_row0, j0, p.L);
+    const int i_begin = p.causal ? j0 : 0;  // rows that see a key of the tile
     for (int g = 0; g < G; ++g) {
       const int64_t q_row0 = (static_cast<int64_t>(b) * p.Hq + h_kv * G + g) * p.L;
       for (int i0 = i_begin; i0 < p.L; i0 += kT) {
         __syncthreads();
-        stage<D, BF16>(qs, p.q, q_row0, i0, p.L);
-        stage<D, BF16>(dos, p.dO, q_row0, i0, p.L);
+        stage_rm<D, BF16>(qr, p.q, q_row0, i0, p.L);
+        stage_tr<D, BF16>(qt, p.q, q_row0, i0, p.L);
+        stage_rm<D, BF16>(dor, p.dO, q_row0, i0, p.L);
+        stage_tr<D, BF16>(dot_, p.dO, q_row0, i0, p.L);
         for (int t = threadIdx.x; t < kT; t += kThreadsBwd) {
           const bool in = i0 + t < p.L;
           lse_s[t] = in ? p.lse[q_row0 + i0 + t] : -INFINITY;
           del_s[t] = in ? p.delta[q_row0 + i0 + t] : 0.f;
         }
         __syncthreads();
-        for (int e = threadIdx.x; e < kT * kT; e += kThreadsBwd) {
-          const int jl = e / kT, il = e % kT;
-          const int i = i0 + il, j = j0 + jl;
-          float pr = 0.f, d = 0.f;
-          const float lse = lse_s[il];
-          if (j < kv && (!p.causal || j <= i) && lse != -INFINITY) {
-            const float s = dot_rows<D>(qs + il * (D + 1), ks + jl * (D + 1)) * p.scale;
-            pr = expf(s - lse);
-            const float dp = dot_rows<D>(dos + il * (D + 1), vs + jl * (D + 1));
-            d = pr * (dp - del_s[il]);
+        float sc[4][4] = {}, dp[4][4] = {};
+        dot4x4<D>(sc, kt, qt, 4 * ti, 4 * tj);   // [key a][query b]
+        dot4x4<D>(dp, vt, dot_, 4 * ti, 4 * tj);
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+          const int jl = 4 * ti + a, j = j0 + jl;
+#pragma unroll
+          for (int bb = 0; bb < 4; ++bb) {
+            const int il = 4 * tj + bb, i = i0 + il;
+            const float lse = lse_s[il];
+            float pr = 0.f, d = 0.f;
+            if (j < kv && (!p.causal || j <= i) && lse != -INFINITY) {
+              pr = expf(sc[a][bb] * p.scale - lse);
+              d = pr * (dp[a][bb] - del_s[il]);
+            }
+            pq[il * kT + jl] = pr;
+            dq[il * kT + jl] = d;
           }
-          pt[jl * (kT + 1) + il] = pr;
-          dst[jl * (kT + 1) + il] = d;
         }
         __syncthreads();
         // dV_j += sum_i P_ij dO_i,  dK_j += sum_i dS_ij q_i
         for (int il = 0; il < kT; ++il) {
-          const float dov = dos[il * (D + 1) + dcol];
-          const float qv = qs[il * (D + 1) + dcol];
+          const float4 p4 = ld4(pq + il * kT + 4 * ti);
+          const float4 s4 = ld4(dq + il * kT + 4 * ti);
+          const float pa[4] = {p4.x, p4.y, p4.z, p4.w};
+          const float sa[4] = {s4.x, s4.y, s4.z, s4.w};
 #pragma unroll
-          for (int r = 0; r < kRowsPer; ++r) {
-            const int jl = rgrp + kGroups * r;
-            dv[r] = fmaf(pt[jl * (kT + 1) + il], dov, dv[r]);
-            dk[r] = fmaf(dst[jl * (kT + 1) + il], qv, dk[r]);
+          for (int c = 0; c < CK; ++c) {
+            const float dov = dor[il * D + tj + 16 * c];
+            const float qv = qr[il * D + tj + 16 * c];
+#pragma unroll
+            for (int a = 0; a < 4; ++a) {
+              dv[a][c] = fmaf(pa[a], dov, dv[a][c]);
+              dk[a][c] = fmaf(sa[a], qv, dk[a][c]);
+            }
           }
         }
       }
     }
   }
 #pragma unroll
-  for (int r = 0; r < kRowsPer; ++r) {
-    const int j = j0 + rgrp + kGroups * r;
+  for (int a = 0; a < 4; ++a) {
+    const int j = j0 + 4 * ti + a;
     if (j < p.L) {
-      st16<BF16>(p.dk, (kv_row0 + j) * D + dcol, dk[r] * p.scale);
-      st16<BF16>(p.dv, (kv_row0 + j) * D + dcol, dv[r]);
+#pragma unroll
+      for (int c = 0; c < CK; ++c) {
+        st16<BF16>(p.dk, (kv_row0 + j) * D + tj + 16 * c, dk[a][c] * p.scale);
+        st16<BF16>(p.dv, (kv_row0 + j) * D + tj + 16 * c, dv[a][c]);
+      }
     }
   }
 }

@@ -228,7 +228,7 @@ attn_status_t attn_fwd_simt(const void* q, const void* k, const void* v, void* o
  * key/value head sum over the query heads that read it (GQA/MQA).
  *
  * Arguments (device pointers, caller-owned; same layouts, dtype and masks as
- * attn_fwd, 2-byte aligned):
+ * attn_fwd, 16-byte aligned):
  *   q, k, v    the forward's inputs;  o the forward's output;
  *   dO         [B, Hq, L, D] output gradient;
  *   lse        [B*Hq, L] fp32, the forward's natural-log LSE (required);
