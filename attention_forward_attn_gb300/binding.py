@@ -98,6 +98,8 @@ def load():
             lib.attn_bwd.argtypes = [p, p, p, p, p, p, p, p, p, i, i, i, i, i, ctypes.c_float, i, p,
                                      i, p]
             lib.attn_bwd.restype = i
+            lib.attn_bwd_simt.argtypes = lib.attn_bwd.argtypes
+            lib.attn_bwd_simt.restype = i
             lib.attn_fwd_f32.argtypes = [p, p, p, p, p, i, i, i, i, ctypes.c_float, i, p, i, p]
             lib.attn_fwd_f32.restype = i
             lib.attn_host_plan.argtypes = [i, i, i, i, i, i, ctypes.POINTER(Chunk), i,
@@ -433,11 +435,15 @@ def attn_fwd_f32(q, k, v, *, kernel="tiled_rowmax", causal=False, sm_scale=None,
     return out, (lse if return_lse else None)
 
 
-def attn_bwd(q, k, v, o, lse, do, *, causal=False, sm_scale=None, valid_len=None, stream=None):
+def attn_bwd(q, k, v, o, lse, do, *, causal=False, sm_scale=None, valid_len=None, stream=None,
+             impl="tc"):
     """Gradients (dq, dk, dv) of attn_fwd for the output gradient ``do``,
-    through attn_bwd.  q, o, do: [B, Hq, L, D]; k, v: [B, Hkv, L, D] (fp16 or
-    bf16, contiguous CUDA tensors); lse: the forward's [B*Hq, L] fp32 LSE."""
+    through attn_bwd (impl="tc", tensor cores) or attn_bwd_simt (impl="simt",
+    fp32 SIMT).  q, o, do: [B, Hq, L, D]; k, v: [B, Hkv, L, D] (fp16 or bf16,
+    contiguous CUDA tensors); lse: the forward's [B*Hq, L] fp32 LSE."""
     import torch
+    if impl not in ("tc", "simt"):
+        raise ValueError("impl must be 'tc' or 'simt'")
     for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("do", do)):
         if not t.is_cuda or not t.is_contiguous():
             raise ValueError("%s must be a contiguous CUDA tensor" % name)
@@ -449,10 +455,13 @@ def attn_bwd(q, k, v, o, lse, do, *, causal=False, sm_scale=None, valid_len=None
     vl_ptr = None
     if valid_len is not None:
         vl_ptr = valid_len.data_ptr()
-    st = int(load().attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
-                             lse.contiguous().data_ptr(), dq.data_ptr(), dk.data_ptr(),
-                             dv.data_ptr(), B, Hq, Hkv, L, D, float(sm_scale), int(bool(causal)),
-                             vl_ptr, _dtype_code(q), _stream_handle(stream)))
+    lse = lse.contiguous()
+    name = "attn_bwd" if impl == "tc" else "attn_bwd_simt"
+    st = int(getattr(load(), name)(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                   do.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                                   dv.data_ptr(), B, Hq, Hkv, L, D, float(sm_scale),
+                                   int(bool(causal)), vl_ptr, _dtype_code(q),
+                                   _stream_handle(stream)))
     if st != ATTN_OK:
-        raise AttnError(st, "attn_bwd")
+        raise AttnError(st, name)
     return dq, dk, dv

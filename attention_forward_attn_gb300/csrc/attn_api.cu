@@ -469,10 +469,13 @@ attn_status_t attn_fwd_f32(const float* q, const float* k, const float* v, float
   return ATTN_OK;
 }
 
-attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
-                       const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv,
-                       int L, int D, float sm_scale, int causal, const int32_t* valid_len,
-                       attn_dtype_t dtype, attn_stream_t stream) {
+namespace {
+
+// Arguments shared by the two backward entry points.
+attn_status_t bwd_validate(const void* q, const void* k, const void* v, const void* o,
+                           const void* dO, const float* lse, void* dq, void* dk, void* dv, int B,
+                           int Hq, int Hkv, int L, int D, float sm_scale, int causal,
+                           const int32_t* valid_len, attn_dtype_t dtype) {
   if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_DTYPE;
   if (q == nullptr || k == nullptr || v == nullptr || o == nullptr || dO == nullptr ||
       lse == nullptr || dq == nullptr || dk == nullptr || dv == nullptr)
@@ -484,14 +487,59 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
   if (!(sm_scale >= 0.f) || isinf(sm_scale)) return ATTN_ERR_SCALE;
   if (static_cast<int64_t>(B) * Hq * L > INT32_MAX || static_cast<int64_t>(B) * Hq > 65535)
     return ATTN_ERR_SHAPE;
-  const void* p16[] = {q, k, v, o, dO, dq, dk, dv};  // 16-byte vector loads and stores
+  const void* p16[] = {q, k, v, o, dO, dq, dk, dv};  // TMA bases, 16-byte vector loads and stores
   for (const void* ptr : p16)
     if (!aligned(ptr, 16)) return ATTN_ERR_ALIGN;
   if (!aligned(lse, 4) || (valid_len != nullptr && !aligned(valid_len, 4))) return ATTN_ERR_ALIGN;
+  return ATTN_OK;
+}
+
+}  // namespace
+
+attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                       const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv,
+                       int L, int D, float sm_scale, int causal, const int32_t* valid_len,
+                       attn_dtype_t dtype, attn_stream_t stream) {
+  attn_status_t s = bwd_validate(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, L, D, sm_scale,
+                                 causal, valid_len, dtype);
+  if (s != ATTN_OK) return s;
   int dev = 0;
   DeviceState* st = nullptr;
-  attn_status_t s = device_state(&dev, &st);
+  if ((s = device_state(&dev, &st)) != ATTN_OK) return s;
+  const bool bf16 = dtype == ATTN_BF16;
+  const attn::Strides sq = attn::contiguous_strides(Hq, L, D);
+  const attn::Strides skv = attn::contiguous_strides(Hkv, L, D);
+  CUtensorMap maps[4];
+  if ((s = encode_map(&maps[0], q, B, Hq, L, D, sq, 128, bf16)) != ATTN_OK ||
+      (s = encode_map(&maps[1], k, B, Hkv, L, D, skv, 128, bf16)) != ATTN_OK ||
+      (s = encode_map(&maps[2], v, B, Hkv, L, D, skv, 128, bf16)) != ATTN_OK ||
+      (s = encode_map(&maps[3], dO, B, Hq, L, D, sq, 128, bf16)) != ATTN_OK)
+    return s;
+  cudaMemPool_t pool = nullptr;
+  if ((s = workspace_pool(dev, st, &pool)) != ATTN_OK) return s;
+  const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  void* ws = nullptr;
+  cudaError_t e = cudaMallocFromPoolAsync(
+      &ws, static_cast<size_t>(attn::bwd_tc_workspace_bytes(B, Hq, L)), pool, cs);
+  if (e != cudaSuccess) return cuda_fail(e);
+  e = attn::launch_bwd_tc(maps, o, dO, lse, dq, dk, dv, ws, B, Hq, Hkv, L, D, sm_scale, causal,
+                          valid_len, bf16, st->status, cs);
+  const cudaError_t ef = cudaFreeAsync(ws, cs);
+  if (e == cudaSuccess) e = ef;
+  if (e != cudaSuccess) return cuda_fail(e);
+  return ATTN_OK;
+}
+
+attn_status_t attn_bwd_simt(const void* q, const void* k, const void* v, const void* o,
+                            const void* dO, const float* lse, void* dq, void* dk, void* dv, int B,
+                            int Hq, int Hkv, int L, int D, float sm_scale, int causal,
+                            const int32_t* valid_len, attn_dtype_t dtype, attn_stream_t stream) {
+  attn_status_t s = bwd_validate(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, L, D, sm_scale,
+                                 causal, valid_len, dtype);
   if (s != ATTN_OK) return s;
+  int dev = 0;
+  DeviceState* st = nullptr;
+  if ((s = device_state(&dev, &st)) != ATTN_OK) return s;
   cudaMemPool_t pool = nullptr;
   if ((s = workspace_pool(dev, st, &pool)) != ATTN_OK) return s;
   const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);

@@ -1,0 +1,916 @@
+// Tensor-core attention backward for sm_103a (tcgen05 + TMA + TMEM).
+//
+// What it computes (the derivative of O = softmax(sm_scale Q K^T + Mask) V,
+// with the softmax rebuilt from the LSE the forward stores "for the backward
+// pass", tiny_flash_attn_triton.py; the pages give no backward algorithm):
+//   P_ij = exp(sm_scale q_i.k_j - LSE_i) on visible keys, 0 elsewhere,
+//   delta_i = dO_i.O_i,  dP_ij = dO_i.v_j,  dS_ij = P_ij (dP_ij - delta_i),
+//   dQ = sm_scale dS K,  dK = sm_scale dS^T Q,  dV = P^T dO,
+// dK and dV of a key/value head summed over the query heads that read it.
+//
+// How: a pre-pass and two kernels, every product on the tensor core with an
+// fp32 accumulator in TMEM and P, dS rounded to the input dtype as operands:
+//   * pre-pass (one warp per row): delta_i and -LSE_i log2(e) into rows padded
+//     to a multiple of 128 (0 and -inf beyond L; -inf where the row sees no
+//     key), so that both kernels fetch them with aligned bulk copies;
+//   * dK/dV kernel, one CTA per (128-key tile, b, h_kv), K and V resident in
+//     shared memory.  Every (query head of the group, 128-row query tile) that
+//     sees the keys streams through a ring of Q, dO, LSE and delta stages.
+//     Per step: S^T = K Q^T and dP^T = V dO^T (keys in TMEM lanes), then two
+//     elementwise warpgroups (each 64 query columns of every key row) write
+//     P^T over the S^T columns and dS^T over the dP^T columns as 16-bit
+//     pairs, and dV += P^T dO, dK += dS^T Q read them from TMEM (dO and Q as
+//     MN-major operands).  TMEM: S^T, dP^T, dV, dK (512 columns at D = 128);
+//   * dQ kernel, one CTA per (128-row query tile, b, h_q), Q and dO resident,
+//     K and V streaming: S = Q K^T, dP = dO V^T, dS written to its own TMEM
+//     columns, dQ += dS K (K as MN-major operand).  TMEM: S, dP, dQ, dS.
+// Warp roles: warps 0-7 elementwise (TMEM lane = key row in the dK/dV kernel,
+// query row in the dQ kernel; warps w and w + 4 share a lane quadrant and
+// split the columns), warp 8 TMA producer, warp 9 MMA issuer (one elected
+// lane issues) and TMEM owner.  Causal tiles above the diagonal and key tiles
+// at or beyond valid_len[b] are never visited; masked (query, key) pairs get
+// P = 0, hence dS = 0.
+//
+// Every mbarrier wait is bounded as in the forward: on a timeout the waiting
+// role records it in the device status word and raises the CTA's abort flag;
+// the others leave too, the CTA drains its own copies and MMAs and frees its
+// TMEM.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <math.h>
+
+#include "attn_internal.h"
+#include "ptx.cuh"
+
+#ifndef ATTN_WAIT_LIMIT_NS
+#define ATTN_WAIT_LIMIT_NS 2000000000ull
+#endif
+
+namespace attn {
+namespace {
+
+constexpr int T = 128;             // query rows of a query tile = keys of a key tile
+constexpr int TH = 64;             // columns of one elementwise warpgroup
+constexpr int kEwThreads = 256;    // two elementwise warpgroups
+constexpr int kLoadWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreadsB = 320;
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct BwdTcParams {
+  const float* nlse2;  // [B*Hq, Lp] -LSE log2(e); -inf: no visible key, or row >= L
+  const float* delta;  // [B*Hq, Lp] dO.O; 0 for rows >= L
+  void* dq;
+  void* dk;
+  void* dv;
+  const int32_t* valid_len;
+  int* status;
+  int B, Hq, Hkv, L, Lp, G, n_t;  // n_t = tiles of 128 rows, Lp = 128 n_t
+  float scale_log2;               // sm_scale log2(e)
+  float sm_scale;
+  int causal;
+};
+
+// Shared-memory layout and TMEM columns, both kernels.  Every tile is 128
+// rows of 64-column (128-byte) swizzled slabs, 1024-byte aligned.
+template <int D>
+struct BCfg {
+  static constexpr int kTile = T * D * 2;
+  static constexpr int kSlab = T * 128;
+  // dK/dV kernel: K, V resident; stages of Q, dO, -LSE log2(e), delta
+  static constexpr int kvStages = (D == 128) ? 2 : 3;
+  static constexpr int kvOffK = 0;
+  static constexpr int kvOffV = kTile;
+  static constexpr int kvOffIn = 2 * kTile;
+  static constexpr int kvStageBytes = 2 * kTile + 1024;
+  static constexpr int kvOffBar = kvOffIn + kvStages * kvStageBytes;
+  // dQ kernel: Q, dO resident; stages of K, V
+  static constexpr int qStages = (D == 128) ? 2 : 4;
+  static constexpr int qOffQ = 0;
+  static constexpr int qOffDO = kTile;
+  static constexpr int qOffKV = 2 * kTile;
+  static constexpr int qStageBytes = 2 * kTile;
+  static constexpr int qOffBar = qOffKV + qStages * qStageBytes;
+  static constexpr int kBarBytes = 256;  // barriers, TMEM base word, abort flag
+  static constexpr int kvSmem = kvOffBar + kBarBytes + 1024;  // + slack to align the base
+  static constexpr int qSmem = qOffBar + kBarBytes + 1024;
+  static_assert(kvSmem <= 232448 && qSmem <= 232448, "shared-memory budget");
+  // TMEM columns
+  static constexpr uint32_t kColS = 0;      // S^T / S (fp32); P^T written over it (dK/dV kernel)
+  static constexpr uint32_t kColDP = T;     // dP^T / dP (fp32); dS^T written over it (dK/dV kernel)
+  static constexpr uint32_t kColAcc0 = 2 * T;      // dV (dK/dV kernel) / dQ (dQ kernel)
+  static constexpr uint32_t kColAcc1 = 2 * T + D;  // dK (dK/dV kernel) / dS (dQ kernel, 64 columns)
+  static constexpr uint32_t kTmemCols = 512;
+  static_assert(2 * T + 2 * D <= 512 && 2 * T + D + T / 2 <= 512, "TMEM budget");
+};
+
+// Barrier block: n_bars 8-byte barriers from `base`, then the TMEM base word
+// and the abort flag.
+struct BBars {
+  uint32_t base;
+  int n_bars;
+  __device__ __forceinline__ uint32_t bar(int i) const { return base + 8u * static_cast<uint32_t>(i); }
+  __device__ __forceinline__ uint32_t tmem_word() const { return bar(n_bars); }
+  __device__ __forceinline__ uint32_t abort_word() const { return tmem_word() + 4u; }
+};
+
+// Bounded mbarrier wait.  False: timed out (recorded) or another role aborted.
+__device__ __forceinline__ bool bwait(const BBars& br, int* status, uint32_t bar, uint32_t parity,
+                                      int role) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  for (;;) {
+#pragma unroll 1
+    for (int i = 0; i < 16; ++i)
+      if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (ptx::ld_shared_volatile(br.abort_word()) != 0u) return false;
+    if (ptx::globaltimer_ns() - t0 > ATTN_WAIT_LIMIT_NS) {
+      ptx::st_shared_volatile(br.abort_word(), 1u);
+      atomicOr(status, kStatusTimeout | role);
+      return false;
+    }
+  }
+}
+
+// Wait with a time limit and no abort check (draining in-flight work only).
+__device__ __forceinline__ void bdrain(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (!ptx::mbar_try_wait(bar, parity) && ptx::globaltimer_ns() - t0 < ATTN_WAIT_LIMIT_NS) {
+  }
+}
+
+__device__ __forceinline__ bool elect() {
+  uint32_t pred;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "elect.sync _|P, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, P;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
+__device__ __forceinline__ void commit(uint32_t bar) {
+  if (elect()) ptx::mma_commit(bar);
+  __syncwarp();
+}
+
+__device__ __forceinline__ uint64_t dadd(uint64_t desc, uint32_t bytes) { return desc + (bytes >> 4); }
+
+// d = A B^T over D with both operands K-major 128-row tiles (128 x 128 fp32
+// result): S^T = K Q^T, dP^T = V dO^T, S = Q K^T, dP = dO V^T.
+template <int D, bool BF16>
+__device__ __forceinline__ void mma_rows(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc) {
+  constexpr uint32_t idesc = ptx::idesc_f16(T, T, BF16, false);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = (kk / 4) * BCfg<D>::kSlab + (kk & 3) * 32u;
+    ptx::mma_ss(d_tmem, dadd(a_desc, off), dadd(b_desc, off), idesc, kk > 0 ? 1u : 0u);
+  }
+}
+
+// acc (+)= A X with A a 128 x 128 16-bit matrix in TMEM (two 64-column halves,
+// each packed into the first 32 columns of its half: P^T, dS^T) or packed
+// contiguously (dS of the dQ kernel, a_half = 32), and X a 128-row tile used
+// as an MN-major operand (X = dO, Q or K; 16 rows per MMA).
+template <int D, bool BF16>
+__device__ __forceinline__ void mma_acc(uint32_t acc, uint32_t a_tmem, uint32_t a_half,
+                                        uint64_t x_mn, bool accumulate) {
+  constexpr uint32_t idesc = ptx::idesc_f16(T, D, BF16, true);
+#pragma unroll
+  for (int kk = 0; kk < T / 16; ++kk) {
+    ptx::mma_ts(acc, a_tmem + (kk / 4) * a_half + (kk & 3) * 8u, dadd(x_mn, kk * 2048u), idesc,
+                (accumulate || kk > 0) ? 1u : 0u);
+  }
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t pk2(float lo, float hi) {
+  if constexpr (BF16) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  } else {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+}
+
+__device__ __forceinline__ int kv_len_of(const BwdTcParams& p, int b) {
+  if (p.valid_len == nullptr) return p.L;
+  const int vl = p.valid_len[b];
+  return vl < 0 ? 0 : (vl > p.L ? p.L : vl);
+}
+
+// ------------------------------------------------------------------ pre-pass
+
+// One warp per padded row r of [B*Hq, Lp]: delta = dO.O with 16-byte loads
+// (D/8 lanes), and -LSE log2(e).
+template <int D, bool BF16>
+__global__ void __launch_bounds__(256) bwd_tc_prep_kernel(const void* __restrict__ o,
+                                                          const void* __restrict__ dO,
+                                                          const float* __restrict__ lse,
+                                                          float* nlse2, float* delta, int L, int Lp,
+                                                          int64_t rows) {
+  const int64_t r = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  if (r >= rows) return;
+  const int lane = threadIdx.x & 31;
+  const int64_t bh = r / Lp;
+  const int i = static_cast<int>(r - bh * Lp);
+  float s = 0.f;
+  if (i < L && lane < D / 8) {
+    const int64_t e = (bh * L + i) * D + lane * 8;
+    const uint4 a = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(o) + e);
+    const uint4 g = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(dO) + e);
+    const uint32_t av[4] = {a.x, a.y, a.z, a.w}, gv[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      float2 fa, fg;
+      if constexpr (BF16) {
+        fa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&av[k]));
+        fg = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gv[k]));
+      } else {
+        fa = __half22float2(*reinterpret_cast<const __half2*>(&av[k]));
+        fg = __half22float2(*reinterpret_cast<const __half2*>(&gv[k]));
+      }
+      s = fmaf(fa.x, fg.x, s);
+      s = fmaf(fa.y, fg.y, s);
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+  if (lane == 0) {
+    float nl = -INFINITY;
+    if (i < L) {
+      const float x = lse[bh * L + i];
+      nl = (x == -INFINITY) ? -INFINITY : -x * kLog2e;
+    }
+    nlse2[r] = nl;
+    delta[r] = i < L ? s : 0.f;
+  }
+}
+
+// ------------------------------------------------------------------ dK, dV
+
+// Barrier indices of the dK/dV kernel (NS input stages).
+template <int NS>
+struct KvIdx {
+  static constexpr int kvFull = 0;            // K, V tiles landed
+  static constexpr int inFull = 1;            // [NS] Q, dO, -LSE log2(e), delta of a step landed
+  static constexpr int inEmpty = 1 + NS;      // [NS] the step's last MMA (dK) completed
+  static constexpr int sFull = 1 + 2 * NS;    // S^T in TMEM
+  static constexpr int dpFull = sFull + 1;    // dP^T in TMEM
+  static constexpr int pReady = sFull + 2;    // P^T written (256 arrivals)
+  static constexpr int dsReady = sFull + 3;   // dS^T written (256 arrivals)
+  static constexpr int dvDone = sFull + 4;    // dV MMA of the step completed (S^T columns free)
+  static constexpr int dkDone = sFull + 5;    // dK MMA completed (dP^T columns free)
+  static constexpr int accFull = sFull + 6;   // every MMA of the unit completed
+  static constexpr int drain = sFull + 7;
+  static constexpr int n = sFull + 8;
+};
+
+// Unit of the dK/dV kernel: key tile n of (b, h_kv).  Key tiles vary slowest
+// over the grid, so under causality the units with the most query tiles start
+// first.  Steps: every query head of the group (fastest) for every query tile
+// m >= m_lo.
+struct KvUnit {
+  int n, b, hkv, kv_len, m_lo, steps;
+};
+
+__device__ __forceinline__ KvUnit kv_unit(const BwdTcParams& p) {
+  const int per = p.B * p.Hkv;
+  KvUnit w;
+  w.n = static_cast<int>(blockIdx.x) / per;
+  const int z = static_cast<int>(blockIdx.x) - w.n * per;
+  w.b = z / p.Hkv;
+  w.hkv = z - w.b * p.Hkv;
+  w.kv_len = kv_len_of(p, w.b);
+  w.m_lo = p.causal ? w.n : 0;
+  w.steps = (w.n * T < w.kv_len) ? p.G * (p.n_t - w.m_lo) : 0;
+  return w;
+}
+
+template <int D>
+__device__ void dkv_producer(const BwdTcParams& p, const KvUnit& w, const BBars& br, uint32_t smem,
+                             const CUtensorMap* tm_q, const CUtensorMap* tm_k,
+                             const CUtensorMap* tm_v, const CUtensorMap* tm_do) {
+  using C = BCfg<D>;
+  constexpr int NS = C::kvStages;
+  using I = KvIdx<NS>;
+  if (w.steps == 0) return;
+  const uint64_t pol_keep = ptx::policy_evict_last();    // Q, dO: read by every key tile
+  const uint64_t pol_once = ptx::policy_evict_first();   // K, V: read once here
+  ptx::mbar_arrive_expect_tx(br.bar(I::kvFull), 2 * C::kTile);
+#pragma unroll
+  for (int h = 0; h < D / 64; ++h) {
+    ptx::tma_load_4d_hint(smem + C::kvOffK + h * C::kSlab, tm_k, br.bar(I::kvFull), h * 64, w.n * T,
+                          w.hkv, w.b, pol_once);
+    ptx::tma_load_4d_hint(smem + C::kvOffV + h * C::kSlab, tm_v, br.bar(I::kvFull), h * 64, w.n * T,
+                          w.hkv, w.b, pol_once);
+  }
+  int t = 0;
+  for (; t < w.steps; ++t) {
+    const uint32_t s = static_cast<uint32_t>(t % NS);
+    if (!bwait(br, p.status, br.bar(I::inEmpty + s), ((t / NS) & 1) ^ 1, kRoleProducer)) break;
+    const int mi = w.m_lo + t / p.G;
+    const int hq = w.hkv * p.G + t % p.G;
+    const uint32_t st = smem + C::kvOffIn + s * C::kvStageBytes;
+    const uint32_t full = br.bar(I::inFull + s);
+    ptx::mbar_arrive_expect_tx(full, 2 * C::kTile + 1024);
+#pragma unroll
+    for (int h = 0; h < D / 64; ++h) {
+      ptx::tma_load_4d_hint(st + h * C::kSlab, tm_q, full, h * 64, mi * T, hq, w.b, pol_keep);
+      ptx::tma_load_4d_hint(st + C::kTile + h * C::kSlab, tm_do, full, h * 64, mi * T, hq, w.b,
+                            pol_keep);
+    }
+    const int64_t row = (static_cast<int64_t>(w.b) * p.Hq + hq) * p.Lp + static_cast<int64_t>(mi) * T;
+    ptx::bulk_load(st + 2 * C::kTile, p.nlse2 + row, T * 4, full);
+    ptx::bulk_load(st + 2 * C::kTile + T * 4, p.delta + row, T * 4, full);
+  }
+  // never leave with a copy in flight: the last load of every stage
+  bdrain(br.bar(I::kvFull), 0);
+  for (int k = (t > NS ? t - NS : 0); k < t; ++k) bdrain(br.bar(I::inFull + k % NS), (k / NS) & 1);
+}
+
+template <int D, bool BF16>
+__device__ void dkv_mma(const BwdTcParams& p, const KvUnit& w, const BBars& br, uint32_t smem,
+                        uint32_t tmem) {
+  using C = BCfg<D>;
+  constexpr int NS = C::kvStages;
+  using I = KvIdx<NS>;
+  constexpr uint32_t kFull = 0xffffffffu;
+  if (w.steps > 0) {
+    // K-major operands: 1024 bytes between 8-row groups; MN-major: 64-column
+    // slabs kSlab apart
+    const uint64_t k_desc = ptx::sdesc_sw128(smem + C::kvOffK, 16, 1024);
+    const uint64_t v_desc = ptx::sdesc_sw128(smem + C::kvOffV, 16, 1024);
+    bool ok = __all_sync(kFull, bwait(br, p.status, br.bar(I::kvFull), 0, kRoleMma));
+    for (int t = 0; ok && t < w.steps; ++t) {
+      const uint32_t s = static_cast<uint32_t>(t % NS);
+      const uint32_t st = smem + C::kvOffIn + s * C::kvStageBytes;
+      ok = __all_sync(kFull, bwait(br, p.status, br.bar(I::inFull + s), (t / NS) & 1, kRoleMma));
+      // S^T(t) overwrites P^T(t-1): after dV(t-1) has read it
+      if (ok && t > 0) ok = __all_sync(kFull, bwait(br, p.status, br.bar(I::dvDone), (t - 1) & 1, kRoleMma));
+      if (!ok) break;
+      ptx::tc_fence_after();
+      if (elect()) mma_rows<D, BF16>(tmem + C::kColS, k_desc, ptx::sdesc_sw128(st, 16, 1024));
+      __syncwarp();
+      commit(br.bar(I::sFull));
+      // dP^T(t) overwrites dS^T(t-1): after dK(t-1) has read it
+      if (t > 0) ok = __all_sync(kFull, bwait(br, p.status, br.bar(I::dkDone), (t - 1) & 1, kRoleMma));
+      if (!ok) break;
+      ptx::tc_fence_after();
+      if (elect()) mma_rows<D, BF16>(tmem + C::kColDP, v_desc, ptx::sdesc_sw128(st + C::kTile, 16, 1024));
+      __syncwarp();
+      commit(br.bar(I::dpFull));
+      // dV += P^T dO
+      ok = __all_sync(kFull, bwait(br, p.status, br.bar(I::pReady), t & 1, kRoleMma));
+      if (!ok) break;
+      ptx::tc_fence_after();
+      if (elect())
+        mma_acc<D, BF16>(tmem + C::kColAcc0, tmem + C::kColS, TH,
+                         ptx::sdesc_sw128(st + C::kTile, C::kSlab, 1024), t > 0);
+      __syncwarp();
+      commit(br.bar(I::dvDone));
+      // dK += dS^T Q (unscaled; sm_scale is applied in the epilogue)
+      ok = __all_sync(kFull, bwait(br, p.status, br.bar(I::dsReady), t & 1, kRoleMma));
+      if (!ok) break;
+      ptx::tc_fence_after();
+      if (elect())
+        mma_acc<D, BF16>(tmem + C::kColAcc1, tmem + C::kColDP, TH, ptx::sdesc_sw128(st, C::kSlab, 1024),
+                         t > 0);
+      __syncwarp();
+      commit(br.bar(I::dkDone));
+      commit(br.bar(I::inEmpty + s));
+      if (t == w.steps - 1) commit(br.bar(I::accFull));
+    }
+  }
+  // every MMA issued here completes before TMEM is released
+  commit(br.bar(I::drain));
+  bdrain(br.bar(I::drain), 0);
+}
+
+// Store one 32-column chunk of an fp32 TMEM row, times `mul`, as 16-bit
+// values (16-byte stores; the thread owns the whole row).
+template <bool BF16>
+__device__ __forceinline__ void store_chunk(uint16_t* dst, const uint32_t (&r)[32], float mul,
+                                            bool store) {
+  uint32_t o16[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    o16[i] = pk2<BF16>(__uint_as_float(r[2 * i]) * mul, __uint_as_float(r[2 * i + 1]) * mul);
+  if (store) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      reinterpret_cast<uint4*>(dst)[q] = make_uint4(o16[4 * q], o16[4 * q + 1], o16[4 * q + 2], o16[4 * q + 3]);
+  }
+}
+
+// Elementwise warpgroups of the dK/dV kernel.  Thread: key row `row` of the
+// tile (TMEM lane), query columns [64 half, 64 half + 64) of every step.
+//   P^T = exp2(S^T sm_scale log2(e) - LSE log2(e)), zero where the key is at
+//   or beyond valid_len[b] or (diagonal tile, causal) after the query; kept in
+//   fp32 registers for dS and written to TMEM as 16-bit pairs;
+//   dS^T = P^T (dP^T - delta), written over the dP^T columns.
+// Epilogue: warpgroup 0 writes the dV row, warpgroup 1 the dK row (x sm_scale).
+template <int D, bool BF16>
+__device__ void dkv_elementwise(const BwdTcParams& p, const KvUnit& w, const BBars& br,
+                                uint32_t smem, uint32_t tmem) {
+  using C = BCfg<D>;
+  constexpr int NS = C::kvStages;
+  using I = KvIdx<NS>;
+  constexpr uint32_t kFull = 0xffffffffu;
+  const int row = threadIdx.x & 127;
+  const int half = static_cast<int>(threadIdx.x) >> 7;
+  const uint32_t lane_addr = (((threadIdx.x >> 5) & 3u) * 32u) << 16;
+  const uint32_t t_s = tmem + lane_addr + C::kColS + half * TH;
+  const uint32_t t_dp = tmem + lane_addr + C::kColDP + half * TH;
+  const bool key_ok = w.n * T + row < w.kv_len;
+  const uint64_t sc2 = ptx::f2_pack(p.scale_log2, p.scale_log2);
+  bool ok = true;
+  for (int t = 0; ok && t < w.steps; ++t) {
+    const uint32_t s = static_cast<uint32_t>(t % NS);
+    const uint32_t st = smem + C::kvOffIn + s * C::kvStageBytes;
+    const int mi = w.m_lo + t / p.G;
+    // the stage's -LSE log2(e) and delta are read from shared memory
+    ok = __all_sync(kFull, bwait(br, p.status, br.bar(I::inFull + s), (t / NS) & 1, kRoleSoftmax));
+    if (ok) ok = __all_sync(kFull, bwait(br, p.status, br.bar(I::sFull), t & 1, kRoleSoftmax));
+    if (!ok) break;
+    ptx::tc_fence_after();
+    uint32_t r[64];
+    ptx::tmem_ld64(t_s, r);
+    float pr[TH];
+    const uint32_t nl_addr = st + 2 * C::kTile + half * TH * 4;
+#pragma unroll
+    for (int c = 0; c < TH; c += 4) {
+      const uint4 nl = ptx::ld_shared_v4(nl_addr + c * 4);
+      const uint64_t x01 = ptx::f2_fma(ptx::f2_pack(__uint_as_float(r[c]), __uint_as_float(r[c + 1])),
+                                       sc2, ptx::f2_pack(__uint_as_float(nl.x), __uint_as_float(nl.y)));
+      const uint64_t x23 = ptx::f2_fma(ptx::f2_pack(__uint_as_float(r[c + 2]), __uint_as_float(r[c + 3])),
+                                       sc2, ptx::f2_pack(__uint_as_float(nl.z), __uint_as_float(nl.w)));
+      float x0, x1, x2, x3;
+      ptx::f2_unpack(x01, x0, x1);
+      ptx::f2_unpack(x23, x2, x3);
+      pr[c] = ptx::ex2_approx(x0);
+      pr[c + 1] = ptx::ex2_approx(x1);
+      pr[c + 2] = ptx::ex2_approx(x2);
+      pr[c + 3] = ptx::ex2_approx(x3);
+    }
+    // columns c < cmin hold queries before this key (diagonal tile, causal)
+    const int cmin = key_ok ? ((p.causal && mi == w.n) ? row - half * TH : 0) : TH;
+    if (cmin > 0) {
+#pragma unroll
+      for (int c = 0; c < TH; ++c) pr[c] = c < cmin ? 0.f : pr[c];
+    }
+    uint32_t pk[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) pk[i] = pk2<BF16>(pr[2 * i], pr[2 * i + 1]);
+    ptx::tmem_st32(t_s, pk);
+    ptx::tmem_st_wait();
+    ptx::tc_fence_before();
+    ptx::mbar_arrive(br.bar(I::pReady));
+
+    ok = __all_sync(kFull, bwait(br, p.status, br.bar(I::dpFull), t & 1, kRoleSoftmax));
+    if (!ok) break;
+    ptx::tc_fence_after();
+    ptx::tmem_ld64(t_dp, r);
+    const uint32_t dl_addr = st + 2 * C::kTile + T * 4 + half * TH * 4;
+#pragma unroll
+    for (int c = 0; c < TH; c += 4) {
+      const uint4 dl = ptx::ld_shared_v4(dl_addr + c * 4);
+      const uint64_t d01 = ptx::f2_mul(
+          ptx::f2_pack(pr[c], pr[c + 1]),
+          ptx::f2_sub(ptx::f2_pack(__uint_as_float(r[c]), __uint_as_float(r[c + 1])),
+                      ptx::f2_pack(__uint_as_float(dl.x), __uint_as_float(dl.y))));
+      const uint64_t d23 = ptx::f2_mul(
+          ptx::f2_pack(pr[c + 2], pr[c + 3]),
+          ptx::f2_sub(ptx::f2_pack(__uint_as_float(r[c + 2]), __uint_as_float(r[c + 3])),
+                      ptx::f2_pack(__uint_as_float(dl.z), __uint_as_float(dl.w))));
+      float a, b2, c2, d2;
+      ptx::f2_unpack(d01, a, b2);
+      ptx::f2_unpack(d23, c2, d2);
+      pk[c / 2] = pk2<BF16>(a, b2);
+      pk[c / 2 + 1] = pk2<BF16>(c2, d2);
+    }
+    ptx::tmem_st32(t_dp, pk);
+    ptx::tmem_st_wait();
+    ptx::tc_fence_before();
+    ptx::mbar_arrive(br.bar(I::dsReady));
+  }
+  if (!ok) return;
+  // epilogue: warpgroup 0 the dV row, warpgroup 1 the dK row
+  const int j = w.n * T + row;
+  const bool store = j < p.L;
+  uint16_t* dst = static_cast<uint16_t*>(half ? p.dk : p.dv) +
+                  ((static_cast<int64_t>(w.b) * p.Hkv + w.hkv) * p.L + j) * D;
+  if (w.steps == 0) {  // no query sees these keys
+    if (store)
+      for (int c = 0; c < D / 8; ++c) reinterpret_cast<uint4*>(dst)[c] = make_uint4(0u, 0u, 0u, 0u);
+    return;
+  }
+  if (!__all_sync(kFull, bwait(br, p.status, br.bar(I::accFull), 0, kRoleEpilogue))) return;
+  ptx::tc_fence_after();
+  const uint32_t t_acc = tmem + lane_addr + (half ? C::kColAcc1 : C::kColAcc0);
+  const float mul = half ? p.sm_scale : 1.f;
+#pragma unroll 1
+  for (int c0 = 0; c0 < D; c0 += 32) {
+    uint32_t r[32];
+    ptx::tmem_ld32(t_acc + c0, r);
+    store_chunk<BF16>(dst + c0, r, mul, store);
+  }
+}
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(kThreadsB, 1)
+    bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v,
+                      const __grid_constant__ CUtensorMap tm_do, const BwdTcParams p) {
+  using C = BCfg<D>;
+  using I = KvIdx<C::kvStages>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t smem = (ptx::smem_u32(smem_raw) + 1023u) & ~1023u;
+  const BBars br{smem + C::kvOffBar, I::n};
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const KvUnit w = kv_unit(p);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < I::n; ++i) {
+      const bool ew = (i == I::pReady || i == I::dsReady);
+      ptx::mbar_init(br.bar(i), ew ? kEwThreads : 1);
+    }
+    ptx::st_shared_volatile(br.abort_word(), 0u);
+    ptx::fence_barrier_init();
+    if (p.valid_len != nullptr && w.n == 0 && w.hkv == 0) {
+      const int vl = p.valid_len[w.b];
+      if (vl < 0 || vl > p.L) atomicOr(p.status, kStatusValidLenClamped);
+    }
+  }
+  if (warp == kLoadWarp && lane == 0) {
+    ptx::prefetch_tensormap(&tm_q);
+    ptx::prefetch_tensormap(&tm_do);
+  }
+  if (warp == kMmaWarp) {
+    ptx::tmem_alloc(br.tmem_word(), C::kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = ptx::ld_shared_volatile(br.tmem_word());
+  if (warp == kLoadWarp) {
+    if (lane == 0) dkv_producer<D>(p, w, br, smem, &tm_q, &tm_k, &tm_v, &tm_do);
+  } else if (warp == kMmaWarp) {
+    dkv_mma<D, BF16>(p, w, br, smem, tmem);
+  } else {
+    dkv_elementwise<D, BF16>(p, w, br, smem, tmem);
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ dQ
+
+// Barrier indices of the dQ kernel (NS key stages).
+template <int NS>
+struct QIdx {
+  static constexpr int qdFull = 0;           // Q, dO tiles landed
+  static constexpr int kvFull = 1;           // [NS] K, V of a key tile landed
+  static constexpr int kvEmpty = 1 + NS;     // [NS] the tile's last MMA (dQ) completed
+  static constexpr int sFull = 1 + 2 * NS;   // S in TMEM
+  static constexpr int dpFull = sFull + 1;   // dP in TMEM
+  static constexpr int sFree = sFull + 2;    // S read (256 arrivals)
+  static constexpr int dsReady = sFull + 3;  // dP read and dS written (256 arrivals)
+  static constexpr int dqDone = sFull + 4;   // dQ MMA of a key tile completed (dS columns free)
+  static constexpr int accFull = sFull + 5;
+  static constexpr int drain = sFull + 6;
+  static constexpr int n = sFull + 7;
+};
+
+// Unit of the dQ kernel: query tile m of (b, h_q), key tiles [0, steps).
+// Query tiles vary slowest, the last (longest under causality) first.
+struct QUnit {
+  int m, b, hq, hkv, kv_len, steps;
+};
+
+__device__ __forceinline__ QUnit q_unit(const BwdTcParams& p) {
+  const int per = p.B * p.Hq;
+  const int u = static_cast<int>(blockIdx.x) / per;
+  const int z = static_cast<int>(blockIdx.x) - u * per;
+  QUnit w;
+  w.m = p.n_t - 1 - u;
+  w.b = z / p.Hq;
+  w.hq = z - w.b * p.Hq;
+  w.hkv = w.hq / p.G;
+  w.kv_len = kv_len_of(p, w.b);
+  const int kt = (w.kv_len + T - 1) / T;
+  w.steps = min(p.causal ? w.m + 1 : p.n_t, kt);
+  return w;
+}
+
+template <int D>
+__device__ void dq_producer(const BwdTcParams& p, const QUnit& w, const BBars& br, uint32_t smem,
+                            const CUtensorMap* tm_q, const CUtensorMap* tm_k,
+                            const CUtensorMap* tm_v, const CUtensorMap* tm_do) {
+  using C = BCfg<D>;
+  constexpr int NS = C::qStages;
+  using I = QIdx<NS>;
+  if (w.steps == 0) return;
+  const uint64_t pol_keep = ptx::policy_evict_last();   // K, V: read by every query tile
+  const uint64_t pol_once = ptx::policy_evict_first();  // Q, dO: read once here
+  ptx::mbar_arrive_expect_tx(br.bar(I::qdFull), 2 * C::kTile);
+#pragma unroll
+  for (int h = 0; h < D / 64; ++h) {
+    ptx::tma_load_4d_hint(smem + C::qOffQ + h * C::kSlab, tm_q, br.bar(I::qdFull), h * 64, w.m * T,
+                          w.hq, w.b, pol_once);
+    ptx::tma_load_4d_hint(smem + C::qOffDO + h * C::kSlab, tm_do, br.bar(I::qdFull), h * 64,
+                          w.m * T, w.hq, w.b, pol_once);
+  }
+  int j = 0;
+  for (; j < w.steps; ++j) {
+    const uint32_t s = static_cast<uint32_t>(j % NS);
+    if (!bwait(br, p.status, br.bar(I::kvEmpty + s), ((j / NS) & 1) ^ 1, kRoleProducer)) break;
+    const uint32_t st = smem + C::qOffKV + s * C::qStageBytes;
+    const uint32_t full = br.bar(I::kvFull + s);
+    ptx::mbar_arrive_expect_tx(full, 2 * C::kTile);
+#pragma unroll
+    for (int h = 0; h < D / 64; ++h) {
+      ptx::tma_load_4d_hint(st + h * C::kSlab, tm_k, full, h * 64, j * T, w.hkv, w.b, pol_keep);
+      ptx::tma_load_4d_hint(st + C::kTile + h * C::kSlab, tm_v, full, h * 64, j * T, w.hkv, w.b,
+                            pol_keep);
+    }
+  }
+  bdrain(br.bar(I::qdFull), 0);
+  for (int k = (j > NS ? j - NS : 0); k < j; ++k) bdrain(br.bar(I::kvFull + k % NS), (k / NS) & 1);
+}
+
+// Issue order per key tile j: S(j) once S(j-1) has been read, dP(j) once
+// dP(j-1) has been read (dS(j-1) written), then dQ += dS(j-1) K(j-1); the
+// last dQ after the loop.
+template <int D, bool BF16>
+__device__ void dq_mma(const BwdTcParams& p, const QUnit& w, const BBars& br, uint32_t smem,
+                       uint32_t tmem) {
+  using C = BCfg<D>;
+  constexpr int NS = C::qStages;
+  using I = QIdx<NS>;
+  constexpr uint32_t kFull = 0xffffffffu;
+  if (w.steps > 0) {
+    const uint64_t q_desc = ptx::sdesc_sw128(smem + C::qOffQ, 16, 1024);
+    const uint64_t do_desc = ptx::sdesc_sw128(smem + C::qOffDO, 16, 1024);
+    bool ok = __all_sync(kFull, bwait(br, p.status, br.bar(I::qdFull), 0, kRoleMma));
+    int j = 0;
+    for (; ok && j < w.steps; ++j) {
+      const uint32_t s = static_cast<uint32_t>(j % NS);
+      const uint32_t st = smem + C::qOffKV + s * C::qStageBytes;
+      ok = __all_sync(kFull, bwait(br, p.status, br.bar(I::kvFull + s), (j / NS) & 1, kRoleMma));
+      if (ok && j > 0) ok = __all_sync(kFull, bwait(br, p.status, br.bar(I::sFree), (j - 1) & 1, kRoleMma));
+      if (!ok) break;
+      ptx::tc_fence_after();
+      if (elect()) mma_rows<D, BF16>(tmem + C::kColS, q_desc, ptx::sdesc_sw128(st, 16, 1024));
+      __syncwarp();
+      commit(br.bar(I::sFull));
+      if (j > 0) ok = __all_sync(kFull, bwait(br, p.status, br.bar(I::dsReady), (j - 1) & 1, kRoleMma));
+      if (!ok) break;
+      ptx::tc_fence_after();
+      if (elect()) mma_rows<D, BF16>(tmem + C::kColDP, do_desc, ptx::sdesc_sw128(st + C::kTile, 16, 1024));
+      __syncwarp();
+      commit(br.bar(I::dpFull));
+      if (j > 0) {
+        const uint32_t sp = static_cast<uint32_t>((j - 1) % NS);
+        const uint32_t kp = smem + C::qOffKV + sp * C::qStageBytes;
+        if (elect())
+          mma_acc<D, BF16>(tmem + C::kColAcc0, tmem + C::kColAcc1, TH / 2,
+                           ptx::sdesc_sw128(kp, C::kSlab, 1024), j - 1 > 0);
+        __syncwarp();
+        commit(br.bar(I::dqDone));
+        commit(br.bar(I::kvEmpty + sp));
+      }
+    }
+    if (ok && j == w.steps &&
+        __all_sync(kFull, bwait(br, p.status, br.bar(I::dsReady), (j - 1) & 1, kRoleMma))) {
+      const uint32_t sp = static_cast<uint32_t>((j - 1) % NS);
+      ptx::tc_fence_after();
+      if (elect())
+        mma_acc<D, BF16>(tmem + C::kColAcc0, tmem + C::kColAcc1, TH / 2,
+                         ptx::sdesc_sw128(smem + C::qOffKV + sp * C::qStageBytes, C::kSlab, 1024),
+                         j - 1 > 0);
+      __syncwarp();
+      commit(br.bar(I::dqDone));
+      commit(br.bar(I::kvEmpty + sp));
+      commit(br.bar(I::accFull));
+    }
+  }
+  commit(br.bar(I::drain));
+  bdrain(br.bar(I::drain), 0);
+}
+
+// Elementwise warpgroups of the dQ kernel.  Thread: query row `row` (TMEM
+// lane), key columns [64 half, 64 half + 64) of every key tile; its LSE and
+// delta are two registers.  P = exp2(S sm_scale log2(e) - LSE log2(e)), zero
+// for keys at or beyond valid_len[b] and (diagonal tile, causal) after the
+// query; dS = P (dP - delta) into the dS columns (16-bit pairs) once the
+// previous dQ MMA has read them.  Epilogue: warpgroup h writes dQ columns
+// [h D/2, (h + 1) D/2) of its row, times sm_scale.
+template <int D, bool BF16>
+__device__ void dq_elementwise(const BwdTcParams& p, const QUnit& w, const BBars& br, uint32_t tmem) {
+  using C = BCfg<D>;
+  constexpr int NS = C::qStages;
+  using I = QIdx<NS>;
+  constexpr uint32_t kFull = 0xffffffffu;
+  const int row = threadIdx.x & 127;
+  const int half = static_cast<int>(threadIdx.x) >> 7;
+  const uint32_t lane_addr = (((threadIdx.x >> 5) & 3u) * 32u) << 16;
+  const uint32_t t_s = tmem + lane_addr + C::kColS + half * TH;
+  const uint32_t t_dp = tmem + lane_addr + C::kColDP + half * TH;
+  const uint32_t t_ds = tmem + lane_addr + C::kColAcc1 + half * (TH / 2);
+  const int64_t g_row = (static_cast<int64_t>(w.b) * p.Hq + w.hq) * p.Lp + static_cast<int64_t>(w.m) * T + row;
+  const float nl = w.steps > 0 ? p.nlse2[g_row] : 0.f;
+  const float dl = w.steps > 0 ? p.delta[g_row] : 0.f;
+  const uint64_t sc2 = ptx::f2_pack(p.scale_log2, p.scale_log2);
+  const uint64_t nl2 = ptx::f2_pack(nl, nl);
+  const uint64_t dl2 = ptx::f2_pack(dl, dl);
+  bool ok = true;
+  for (int j = 0; ok && j < w.steps; ++j) {
+    ok = __all_sync(kFull, bwait(br, p.status, br.bar(I::sFull), j & 1, kRoleSoftmax));
+    if (!ok) break;
+    ptx::tc_fence_after();
+    uint32_t r[64];
+    ptx::tmem_ld64(t_s, r);
+    float pr[TH];
+#pragma unroll
+    for (int c = 0; c < TH; c += 2) {
+      const uint64_t x = ptx::f2_fma(ptx::f2_pack(__uint_as_float(r[c]), __uint_as_float(r[c + 1])), sc2, nl2);
+      float x0, x1;
+      ptx::f2_unpack(x, x0, x1);
+      pr[c] = ptx::ex2_approx(x0);
+      pr[c + 1] = ptx::ex2_approx(x1);
+    }
+    ptx::tc_fence_before();
+    ptx::mbar_arrive(br.bar(I::sFree));
+    // visible key columns: c < climit (causal diagonal tile; last key tile)
+    int climit = TH;
+    if (p.causal && j == w.m) climit = min(climit, row - half * TH + 1);
+    climit = min(climit, w.kv_len - j * T - half * TH);
+    if (climit < TH) {
+#pragma unroll
+      for (int c = 0; c < TH; ++c) pr[c] = c < climit ? pr[c] : 0.f;
+    }
+    ok = __all_sync(kFull, bwait(br, p.status, br.bar(I::dpFull), j & 1, kRoleSoftmax));
+    if (!ok) break;
+    ptx::tc_fence_after();
+    ptx::tmem_ld64(t_dp, r);
+    uint32_t pk[32];
+#pragma unroll
+    for (int c = 0; c < TH; c += 2) {
+      const uint64_t d = ptx::f2_mul(
+          ptx::f2_pack(pr[c], pr[c + 1]),
+          ptx::f2_sub(ptx::f2_pack(__uint_as_float(r[c]), __uint_as_float(r[c + 1])), dl2));
+      float a, b2;
+      ptx::f2_unpack(d, a, b2);
+      pk[c / 2] = pk2<BF16>(a, b2);
+    }
+    // the dS columns held dS(j-1): wait until dQ(j-1) has read them
+    if (j > 0) ok = __all_sync(kFull, bwait(br, p.status, br.bar(I::dqDone), (j - 1) & 1, kRoleSoftmax));
+    if (!ok) break;
+    ptx::tc_fence_after();
+    ptx::tmem_st32(t_ds, pk);
+    ptx::tmem_st_wait();
+    ptx::tc_fence_before();
+    ptx::mbar_arrive(br.bar(I::dsReady));
+  }
+  if (!ok) return;
+  const int i = w.m * T + row;
+  const bool store = i < p.L;
+  uint16_t* dst = static_cast<uint16_t*>(p.dq) +
+                  ((static_cast<int64_t>(w.b) * p.Hq + w.hq) * p.L + i) * D + half * (D / 2);
+  if (w.steps == 0) {  // no visible key: dQ = 0
+    if (store)
+      for (int c = 0; c < D / 16; ++c) reinterpret_cast<uint4*>(dst)[c] = make_uint4(0u, 0u, 0u, 0u);
+    return;
+  }
+  if (!__all_sync(kFull, bwait(br, p.status, br.bar(I::accFull), 0, kRoleEpilogue))) return;
+  ptx::tc_fence_after();
+  const uint32_t t_acc = tmem + lane_addr + C::kColAcc0 + half * (D / 2);
+#pragma unroll 1
+  for (int c0 = 0; c0 < D / 2; c0 += 32) {
+    uint32_t r[32];
+    ptx::tmem_ld32(t_acc + c0, r);
+    store_chunk<BF16>(dst + c0, r, p.sm_scale, store);
+  }
+}
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(kThreadsB, 1)
+    bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v,
+                     const __grid_constant__ CUtensorMap tm_do, const BwdTcParams p) {
+  using C = BCfg<D>;
+  using I = QIdx<C::qStages>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t smem = (ptx::smem_u32(smem_raw) + 1023u) & ~1023u;
+  const BBars br{smem + C::qOffBar, I::n};
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const QUnit w = q_unit(p);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < I::n; ++i) {
+      const bool ew = (i == I::sFree || i == I::dsReady);
+      ptx::mbar_init(br.bar(i), ew ? kEwThreads : 1);
+    }
+    ptx::st_shared_volatile(br.abort_word(), 0u);
+    ptx::fence_barrier_init();
+  }
+  if (warp == kLoadWarp && lane == 0) {
+    ptx::prefetch_tensormap(&tm_k);
+    ptx::prefetch_tensormap(&tm_v);
+  }
+  if (warp == kMmaWarp) {
+    ptx::tmem_alloc(br.tmem_word(), C::kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = ptx::ld_shared_volatile(br.tmem_word());
+  if (warp == kLoadWarp) {
+    if (lane == 0) dq_producer<D>(p, w, br, smem, &tm_q, &tm_k, &tm_v, &tm_do);
+  } else if (warp == kMmaWarp) {
+    dq_mma<D, BF16>(p, w, br, smem, tmem);
+  } else {
+    dq_elementwise<D, BF16>(p, w, br, tmem);
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+template <int D, bool BF16>
+cudaError_t launch_bwd_tc_d(const CUtensorMap (&maps)[4], const BwdTcParams& p, const void* o,
+                            const void* dO, const float* lse, float* nlse2, float* delta,
+                            cudaStream_t stream) {
+  using C = BCfg<D>;
+  const int64_t rows = static_cast<int64_t>(p.B) * p.Hq * p.Lp;
+  bwd_tc_prep_kernel<D, BF16><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
+      o, dO, lse, nlse2, delta, p.L, p.Lp, rows);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(bwd_dkv_tc_kernel<D, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           C::kvSmem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(bwd_dq_tc_kernel<D, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::qSmem);
+  if (e != cudaSuccess) return e;
+  bwd_dkv_tc_kernel<D, BF16><<<static_cast<unsigned>(p.n_t * p.B * p.Hkv), kThreadsB, C::kvSmem, stream>>>(
+      maps[0], maps[1], maps[2], maps[3], p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  bwd_dq_tc_kernel<D, BF16><<<static_cast<unsigned>(p.n_t * p.B * p.Hq), kThreadsB, C::qSmem, stream>>>(
+      maps[0], maps[1], maps[2], maps[3], p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int64_t bwd_tc_workspace_bytes(int B, int Hq, int L) {
+  const int64_t lp = (static_cast<int64_t>(L) + T - 1) / T * T;
+  return 2 * static_cast<int64_t>(B) * Hq * lp * 4;
+}
+
+cudaError_t launch_bwd_tc(const CUtensorMap (&maps)[4], const void* o, const void* dO,
+                          const float* lse, void* dq, void* dk, void* dv, void* workspace, int B,
+                          int Hq, int Hkv, int L, int D, float sm_scale, int causal,
+                          const int32_t* valid_len, bool bf16, int* status, cudaStream_t stream) {
+  BwdTcParams p;
+  p.n_t = (L + T - 1) / T;
+  p.Lp = p.n_t * T;
+  float* nlse2 = static_cast<float*>(workspace);
+  float* delta = nlse2 + static_cast<int64_t>(B) * Hq * p.Lp;
+  p.nlse2 = nlse2;
+  p.delta = delta;
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.valid_len = valid_len;
+  p.status = status;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.L = L;
+  p.G = Hq / Hkv;
+  p.scale_log2 = sm_scale * kLog2e;
+  p.sm_scale = sm_scale;
+  p.causal = causal;
+  if (D == 64)
+    return bf16 ? launch_bwd_tc_d<64, true>(maps, p, o, dO, lse, nlse2, delta, stream)
+                : launch_bwd_tc_d<64, false>(maps, p, o, dO, lse, nlse2, delta, stream);
+  if (D == 128)
+    return bf16 ? launch_bwd_tc_d<128, true>(maps, p, o, dO, lse, nlse2, delta, stream)
+                : launch_bwd_tc_d<128, false>(maps, p, o, dO, lse, nlse2, delta, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace attn

@@ -106,6 +106,16 @@ cudaError_t launch_bwd(const void* q, const void* k, const void* v, const void* 
                        int Hkv, int L, int D, float sm_scale, int causal, const int32_t* valid_len,
                        bool bf16, cudaStream_t stream);
 
+// Tensor-core backward (attn_bwd_tc.cu): bytes of its workspace (-LSE log2(e)
+// and delta, fp32 [B*Hq, L rounded up to 128] each) and its launch (pre-pass,
+// dK/dV and dQ kernels on `stream`).  maps: Q, K, V, dO as encode_map makes
+// them with 128-row boxes.  D 64 or 128.
+int64_t bwd_tc_workspace_bytes(int B, int Hq, int L);
+cudaError_t launch_bwd_tc(const CUtensorMap (&maps)[4], const void* o, const void* dO,
+                          const float* lse, void* dq, void* dk, void* dv, void* workspace, int B,
+                          int Hq, int Hkv, int L, int D, float sm_scale, int causal,
+                          const int32_t* valid_len, bool bf16, int* status, cudaStream_t stream);
+
 // SIMT cross-check forward.
 cudaError_t launch_simt(const Problem& p);
 

@@ -647,19 +647,22 @@ def run_relative_table(args, local):
 
 
 def run_backward(args, local):
-    """attn_bwd on the C4 and C2 shapes: ms per call (delta, dQ and dK/dV
-    kernels) with the forward's O and LSE already on the device, L2 flushed
-    before each call.  Work: the backward's five products (S recomputed, dP,
-    dQ, dK, dV) = 2.5x the forward's nominal FLOPs.  Roofline: the SIMT
-    kernels run on the FP32 units: 152 SMs x 128 FMA lanes x 2 FLOP x the
-    2070 MHz maximum SM clock = 80.6 TFLOP/s."""
+    """attn_bwd (tensor cores) and attn_bwd_simt (fp32 SIMT) on the C4 and C2
+    shapes: ms per call with the forward's O and LSE already on the device,
+    L2 flushed before each call.  Work: the backward's five products (S
+    recomputed, dP, dQ, dK, dV) = 2.5x the forward's nominal FLOPs.  The
+    tensor-core path executes seven (S and dP in both of its kernels), 3.5x.
+    Rooflines: tensor -- the measured bf16 burst peak (fp16 runs at the same
+    rate), against the executed products; SIMT -- the FP32 units, 152 SMs x
+    128 FMA lanes x 2 FLOP x the 2070 MHz maximum SM clock = 80.6 TFLOP/s."""
     import attention_forward_attn_gb300 as attn
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     attn.load()
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-    peaks, _src = load_peaks()
+    peaks, src = load_peaks()
     fp32_peak = 152 * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+    tc_peak = peaks["bf16_tflops"]
     lines = []
     for name in ("C4", "C2"):
         w = wl.WORKLOADS[name]
@@ -669,38 +672,44 @@ def run_backward(args, local):
         gen = torch.Generator().manual_seed(w.seed + 100)
         do = torch.randn(q.shape, generator=gen).to(q.dtype).to(dev)
         o, lse = attn.attn_fwd(q_d, k_d, v_d, causal=w.causal, sm_scale=w.sm_scale, valid_len=vl_d)
+        for impl in ("tc", "simt"):
+            def call():
+                return attn.attn_bwd(q_d, k_d, v_d, o, lse, do, causal=w.causal,
+                                     sm_scale=w.sm_scale, valid_len=vl_d, impl=impl)
 
-        def call():
-            return attn.attn_bwd(q_d, k_d, v_d, o, lse, do, causal=w.causal, sm_scale=w.sm_scale,
-                                 valid_len=vl_d)
-
-        for _ in range(max(1, min(args.warmup, 3))):
-            flush.zero_()
-            call()
-        n = max(3, min(args.steps, 10))
-        ts = []
-        for _ in range(n):
-            flush.zero_()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
-            call()
-            e1.record()
-            torch.cuda.synchronize(dev)
-            ts.append(e0.elapsed_time(e1))
-        st, code = attn.status()
-        if st != 0:
-            raise RuntimeError("device status %d (code %#x)" % (st, code))
-        ms = sorted(ts)[n // 2]
-        tf = 2.5 * nominal_flops(w) / (ms * 1e-3) / 1e12
-        lines.append({"metric": "attention backward TFLOP/s (2.5x the forward's nominal FLOPs)",
-                      "workload": "%s shapes: %s" % (name, w.description), "value": round(tf, 3),
-                      "unit": "TFLOP/s", "ms_per_call": round(ms, 3),
-                      "roofline": {"bound": "alu", "achieved": round(tf, 3),
-                                   "peak": round(fp32_peak, 1), "unit": "TFLOP/s",
-                                   "frac": round(tf / fp32_peak, 4),
-                                   "peak_source": "152 SMs x 128 FP32 lanes x 2 x sm_max_mhz"},
-                      "timing": "median of %d calls, L2 flushed before each" % n,
-                      "dtype": w.dtype, "data": "synthetic"})
+            for _ in range(max(1, min(args.warmup, 3))):
+                flush.zero_()
+                call()
+            n = max(3, min(args.steps, 10 if impl == "simt" else 50))
+            ts = []
+            for _ in range(n):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                call()
+                e1.record()
+                torch.cuda.synchronize(dev)
+                ts.append(e0.elapsed_time(e1))
+            st, code = attn.status()
+            if st != 0:
+                raise RuntimeError("device status %d (code %#x)" % (st, code))
+            ms = sorted(ts)[n // 2]
+            tf = 2.5 * nominal_flops(w) / (ms * 1e-3) / 1e12
+            if impl == "tc":
+                ex = 3.5 * nominal_flops(w) / (ms * 1e-3) / 1e12
+                roof = {"bound": "tensor", "achieved": round(ex, 3), "peak": tc_peak,
+                        "unit": "TFLOP/s", "frac": round(ex / tc_peak, 4),
+                        "peak_source": "bf16_tflops of %s (burst), executed products (3.5x)" % src}
+            else:
+                roof = {"bound": "alu", "achieved": round(tf, 3), "peak": round(fp32_peak, 1),
+                        "unit": "TFLOP/s", "frac": round(tf / fp32_peak, 4),
+                        "peak_source": "152 SMs x 128 FP32 lanes x 2 x sm_max_mhz"}
+            lines.append({"metric": "attention backward TFLOP/s (2.5x the forward's nominal FLOPs)",
+                          "impl": "attn_bwd" if impl == "tc" else "attn_bwd_simt",
+                          "workload": "%s shapes: %s" % (name, w.description), "value": round(tf, 3),
+                          "unit": "TFLOP/s", "ms_per_call": round(ms, 3), "roofline": roof,
+                          "timing": "median of %d calls, L2 flushed before each" % n,
+                          "dtype": w.dtype, "data": "synthetic"})
         del q_d, k_d, v_d, o, lse, do
         torch.cuda.empty_cache()
     return lines

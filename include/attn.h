@@ -234,17 +234,35 @@ attn_status_t attn_fwd_simt(const void* q, const void* k, const void* v, void* o
  *   lse        [B*Hq, L] fp32, the forward's natural-log LSE (required);
  *   dq         [B, Hq, L, D] out;  dk, dv  [B, Hkv, L, D] out (overwritten).
  *   D          64 or 128.  B*Hq <= 65535.
- * Work: SIMT kernels with fp32 arithmetic (delta; dQ per 64-row query tile;
- * dK/dV per 64-key tile with all query heads of its group), the results
- * rounded once to the input dtype.  Device memory: a stream-ordered fp32
- * workspace of B*Hq*L*4 bytes from the library's pool.
+ * Work: a pre-pass (delta and the LSE in base 2, in rows padded to 128) and
+ * two tensor-core kernels (tcgen05, fp32 accumulators in tensor memory): dK/dV
+ * per 128-key tile with K and V resident and every query tile and query head
+ * of the group streaming through; dQ per 128-row query tile with K and V
+ * streaming.  P and dS are rounded to the input dtype as MMA operands, every
+ * sum is accumulated in fp32, each result rounded once to the input dtype.
+ * No atomics: the result does not depend on scheduling.  Device memory: a
+ * stream-ordered fp32 workspace of 2*B*Hq*ceil(L/128)*128*4 bytes from the
+ * library's pool.
  * Errors: argument errors as attn_fwd (nothing is queued); device-side
- * conditions through attn_status.
+ * conditions (bounded-wait timeout, clamped valid_len) through attn_status.
  */
 attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
                        const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv,
                        int L, int D, float sm_scale, int causal, const int32_t* valid_len,
                        attn_dtype_t dtype, attn_stream_t stream);
+
+/*
+ * attn_bwd_simt -- the same gradients computed by SIMT kernels with fp32
+ * arithmetic throughout (P and dS are never rounded to 16 bits): delta; dQ per
+ * 64-row query tile; dK/dV per 64-key tile with all query heads of its group;
+ * 4 x 4 register blocks over transposed shared-memory tiles.  A cross-check of
+ * attn_bwd, and much slower.  Same arguments, preconditions and errors
+ * as attn_bwd; workspace B*Hq*L*4 bytes.
+ */
+attn_status_t attn_bwd_simt(const void* q, const void* k, const void* v, const void* o,
+                            const void* dO, const float* lse, void* dq, void* dk, void* dv, int B,
+                            int Hq, int Hkv, int L, int D, float sm_scale, int causal,
+                            const int32_t* valid_len, attn_dtype_t dtype, attn_stream_t stream);
 
 /* The fp32 comparison kernels of attn_fwd_f32. */
 typedef enum {

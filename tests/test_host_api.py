@@ -238,12 +238,13 @@ def test_f32_invalid_arguments_rejected_on_host(lib, args, expected):
     (dict(sm_scale=-2.0), "ATTN_ERR_SCALE"),
     (dict(dq=A16 + 1), "ATTN_ERR_ALIGN"),
 ])
-def test_bwd_invalid_arguments_rejected_on_host(lib, args, expected):
+@pytest.mark.parametrize("entry", ["attn_bwd", "attn_bwd_simt"])
+def test_bwd_invalid_arguments_rejected_on_host(lib, args, expected, entry):
     a = dict(q=A16, k=A16, v=A16, o=A16, do=A16, lse=A16, dq=A16, dk=A16, dv=A16, B=1, Hq=4,
              Hkv=2, L=64, D=64, sm_scale=0.125, causal=1, valid_len=None, dtype=attn.ATTN_BF16,
              stream=None)
     a.update(args)
-    st = lib.attn_bwd(a["q"], a["k"], a["v"], a["o"], a["do"], a["lse"], a["dq"], a["dk"], a["dv"],
-                      a["B"], a["Hq"], a["Hkv"], a["L"], a["D"], a["sm_scale"], a["causal"],
-                      a["valid_len"], a["dtype"], a["stream"])
+    st = getattr(lib, entry)(a["q"], a["k"], a["v"], a["o"], a["do"], a["lse"], a["dq"], a["dk"],
+                             a["dv"], a["B"], a["Hq"], a["Hkv"], a["L"], a["D"], a["sm_scale"],
+                             a["causal"], a["valid_len"], a["dtype"], a["stream"])
     assert binding.STATUS_NAMES[st] == expected
