@@ -23,7 +23,8 @@
 //     MN-major operands).  TMEM: S^T, dP^T, dV, dK (512 columns at D = 128);
 //   * dQ kernel, one CTA per (128-row query tile, b, h_q), Q and dO resident,
 //     K and V streaming: S = Q K^T, dP = dO V^T, dS written to its own TMEM
-//     columns, dQ += dS K (K as MN-major operand).  TMEM: S, dP, dQ, dS.
+//     columns (two buffers), dQ += dS K (K as MN-major operand).  TMEM: S,
+//     dP, dQ, dS x 2.
 // Warp roles: warps 0-7 elementwise (TMEM lane = key row in the dK/dV kernel,
 // query row in the dQ kernel; warps w and w + 4 share a lane quadrant and
 // split the columns), warp 8 TMA producer, warp 9 MMA issuer (one elected
@@ -99,9 +100,9 @@ struct BCfg {
   static constexpr uint32_t kColS = 0;      // S^T / S (fp32); P^T written over it (dK/dV kernel)
   static constexpr uint32_t kColDP = T;     // dP^T / dP (fp32); dS^T written over it (dK/dV kernel)
   static constexpr uint32_t kColAcc0 = 2 * T;      // dV (dK/dV kernel) / dQ (dQ kernel)
-  static constexpr uint32_t kColAcc1 = 2 * T + D;  // dK (dK/dV kernel) / dS (dQ kernel, 64 columns)
+  static constexpr uint32_t kColAcc1 = 2 * T + D;  // dK (dK/dV kernel) / dS (dQ kernel, 2 x 64 columns)
   static constexpr uint32_t kTmemCols = 512;
-  static_assert(2 * T + 2 * D <= 512 && 2 * T + D + T / 2 <= 512, "TMEM budget");
+  static_assert(2 * T + 2 * D <= 512 && 2 * T + D + T <= 512, "TMEM budget");
 };
 
 // Barrier block: n_bars 8-byte barriers from `base`, then the TMEM base word
@@ -202,22 +203,25 @@ __device__ __forceinline__ int kv_len_of(const BwdTcParams& p, int b) {
 
 // ------------------------------------------------------------------ pre-pass
 
-// One warp per padded row r of [B*Hq, Lp]: delta = dO.O with 16-byte loads
-// (D/8 lanes), and -LSE log2(e).
+// Padded rows r of [B*Hq, Lp], D/8 lanes per row (32*8/D rows per warp):
+// delta = dO.O with 16-byte loads, and -LSE log2(e).
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) bwd_tc_prep_kernel(const void* __restrict__ o,
                                                           const void* __restrict__ dO,
                                                           const float* __restrict__ lse,
                                                           float* nlse2, float* delta, int L, int Lp,
                                                           int64_t rows) {
-  const int64_t r = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
-  if (r >= rows) return;
+  constexpr int LPR = D / 8;     // lanes per row
+  constexpr int RPW = 32 / LPR;  // rows per warp
   const int lane = threadIdx.x & 31;
+  const int64_t r = (static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5)) * RPW + lane / LPR;
+  const int sub = lane % LPR;
   const int64_t bh = r / Lp;
   const int i = static_cast<int>(r - bh * Lp);
+  const bool live = r < rows && i < L;
   float s = 0.f;
-  if (i < L && lane < D / 8) {
-    const int64_t e = (bh * L + i) * D + lane * 8;
+  if (live) {
+    const int64_t e = (bh * L + i) * D + sub * 8;
     const uint4 a = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(o) + e);
     const uint4 g = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(dO) + e);
     const uint32_t av[4] = {a.x, a.y, a.z, a.w}, gv[4] = {g.x, g.y, g.z, g.w};
@@ -236,8 +240,8 @@ __global__ void __launch_bounds__(256) bwd_tc_prep_kernel(const void* __restrict
     }
   }
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-  if (lane == 0) {
+  for (int off = LPR / 2; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+  if (sub == 0 && r < rows) {
     float nl = -INFINITY;
     if (i < L) {
       const float x = lse[bh * L + i];
@@ -330,6 +334,13 @@ __device__ void dkv_producer(const BwdTcParams& p, const KvUnit& w, const BBars&
   for (int k = (t > NS ? t - NS : 0); k < t; ++k) bdrain(br.bar(I::inFull + k % NS), (k / NS) & 1);
 }
 
+// Issue order: S^T(0), dP^T(0), then per step t
+//   dV(t) once P^T(t) is written;
+//   S^T(t+1) once dV(t) has completed (it read P^T(t) from the S^T columns);
+//   dK(t) once dS^T(t) is written;
+//   dP^T(t+1) once dK(t) has completed (it read dS^T(t) from the dP^T columns);
+// so S^T(t+1) runs on the tensor core while the elementwise warps compute
+// dS^T(t), and dP^T(t+1) while they compute P^T(t+1).
 template <int D, bool BF16>
 __device__ void dkv_mma(const BwdTcParams& p, const KvUnit& w, const BBars& br, uint32_t smem,
                         uint32_t tmem) {
@@ -337,50 +348,63 @@ __device__ void dkv_mma(const BwdTcParams& p, const KvUnit& w, const BBars& br, 
   constexpr int NS = C::kvStages;
   using I = KvIdx<NS>;
   constexpr uint32_t kFull = 0xffffffffu;
+  auto stage = [&](int t) { return smem + C::kvOffIn + static_cast<uint32_t>(t % NS) * C::kvStageBytes; };
+  auto wait = [&](int bar, uint32_t parity) {
+    return __all_sync(kFull, bwait(br, p.status, br.bar(bar), parity, kRoleMma));
+  };
   if (w.steps > 0) {
     // K-major operands: 1024 bytes between 8-row groups; MN-major: 64-column
     // slabs kSlab apart
     const uint64_t k_desc = ptx::sdesc_sw128(smem + C::kvOffK, 16, 1024);
     const uint64_t v_desc = ptx::sdesc_sw128(smem + C::kvOffV, 16, 1024);
-    bool ok = __all_sync(kFull, bwait(br, p.status, br.bar(I::kvFull), 0, kRoleMma));
-    for (int t = 0; ok && t < w.steps; ++t) {
-      const uint32_t s = static_cast<uint32_t>(t % NS);
-      const uint32_t st = smem + C::kvOffIn + s * C::kvStageBytes;
-      ok = __all_sync(kFull, bwait(br, p.status, br.bar(I::inFull + s), (t / NS) & 1, kRoleMma));
-      // S^T(t) overwrites P^T(t-1): after dV(t-1) has read it
-      if (ok && t > 0) ok = __all_sync(kFull, bwait(br, p.status, br.bar(I::dvDone), (t - 1) & 1, kRoleMma));
-      if (!ok) break;
+    auto issue_s = [&](int t) {  // S^T(t) = K Q(t)^T
       ptx::tc_fence_after();
-      if (elect()) mma_rows<D, BF16>(tmem + C::kColS, k_desc, ptx::sdesc_sw128(st, 16, 1024));
+      if (elect()) mma_rows<D, BF16>(tmem + C::kColS, k_desc, ptx::sdesc_sw128(stage(t), 16, 1024));
       __syncwarp();
       commit(br.bar(I::sFull));
-      // dP^T(t) overwrites dS^T(t-1): after dK(t-1) has read it
-      if (t > 0) ok = __all_sync(kFull, bwait(br, p.status, br.bar(I::dkDone), (t - 1) & 1, kRoleMma));
-      if (!ok) break;
+    };
+    auto issue_dp = [&](int t) {  // dP^T(t) = V dO(t)^T
       ptx::tc_fence_after();
-      if (elect()) mma_rows<D, BF16>(tmem + C::kColDP, v_desc, ptx::sdesc_sw128(st + C::kTile, 16, 1024));
+      if (elect())
+        mma_rows<D, BF16>(tmem + C::kColDP, v_desc, ptx::sdesc_sw128(stage(t) + C::kTile, 16, 1024));
       __syncwarp();
       commit(br.bar(I::dpFull));
+    };
+    bool ok = wait(I::kvFull, 0) && wait(I::inFull, 0);
+    if (ok) {
+      issue_s(0);
+      issue_dp(0);
+    }
+    for (int t = 0; ok && t < w.steps; ++t) {
+      const uint32_t st = stage(t);
+      const bool more = t + 1 < w.steps;
       // dV += P^T dO
-      ok = __all_sync(kFull, bwait(br, p.status, br.bar(I::pReady), t & 1, kRoleMma));
-      if (!ok) break;
+      if (!(ok = wait(I::pReady, t & 1))) break;
       ptx::tc_fence_after();
       if (elect())
         mma_acc<D, BF16>(tmem + C::kColAcc0, tmem + C::kColS, TH,
                          ptx::sdesc_sw128(st + C::kTile, C::kSlab, 1024), t > 0);
       __syncwarp();
       commit(br.bar(I::dvDone));
+      if (more) {
+        if (!(ok = wait(I::inFull + (t + 1) % NS, ((t + 1) / NS) & 1) && wait(I::dvDone, t & 1))) break;
+        issue_s(t + 1);
+      }
       // dK += dS^T Q (unscaled; sm_scale is applied in the epilogue)
-      ok = __all_sync(kFull, bwait(br, p.status, br.bar(I::dsReady), t & 1, kRoleMma));
-      if (!ok) break;
+      if (!(ok = wait(I::dsReady, t & 1))) break;
       ptx::tc_fence_after();
       if (elect())
         mma_acc<D, BF16>(tmem + C::kColAcc1, tmem + C::kColDP, TH, ptx::sdesc_sw128(st, C::kSlab, 1024),
                          t > 0);
       __syncwarp();
       commit(br.bar(I::dkDone));
-      commit(br.bar(I::inEmpty + s));
-      if (t == w.steps - 1) commit(br.bar(I::accFull));
+      commit(br.bar(I::inEmpty + t % NS));
+      if (more) {
+        if (!(ok = wait(I::dkDone, t & 1))) break;
+        issue_dp(t + 1);
+      } else {
+        commit(br.bar(I::accFull));
+      }
     }
   }
   // every MMA issued here completes before TMEM is released
@@ -572,7 +596,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
 
 // ------------------------------------------------------------------ dQ
 
-// Barrier indices of the dQ kernel (NS key stages).
+// Barrier indices of the dQ kernel (NS key stages, two dS buffers).
 template <int NS>
 struct QIdx {
   static constexpr int qdFull = 0;           // Q, dO tiles landed
@@ -581,11 +605,12 @@ struct QIdx {
   static constexpr int sFull = 1 + 2 * NS;   // S in TMEM
   static constexpr int dpFull = sFull + 1;   // dP in TMEM
   static constexpr int sFree = sFull + 2;    // S read (256 arrivals)
-  static constexpr int dsReady = sFull + 3;  // dP read and dS written (256 arrivals)
-  static constexpr int dqDone = sFull + 4;   // dQ MMA of a key tile completed (dS columns free)
-  static constexpr int accFull = sFull + 5;
-  static constexpr int drain = sFull + 6;
-  static constexpr int n = sFull + 7;
+  static constexpr int dpFree = sFull + 3;   // dP read (256 arrivals)
+  static constexpr int dsReady = sFull + 4;  // [2] dS written into buffer b (256 arrivals)
+  static constexpr int dqDone = sFull + 6;   // [2] dQ MMA reading buffer b completed
+  static constexpr int accFull = sFull + 8;
+  static constexpr int drain = sFull + 9;
+  static constexpr int n = sFull + 10;
 };
 
 // Unit of the dQ kernel: query tile m of (b, h_q), key tiles [0, steps).
@@ -645,9 +670,10 @@ __device__ void dq_producer(const BwdTcParams& p, const QUnit& w, const BBars& b
   for (int k = (j > NS ? j - NS : 0); k < j; ++k) bdrain(br.bar(I::kvFull + k % NS), (k / NS) & 1);
 }
 
-// Issue order per key tile j: S(j) once S(j-1) has been read, dP(j) once
-// dP(j-1) has been read (dS(j-1) written), then dQ += dS(j-1) K(j-1); the
-// last dQ after the loop.
+// Issue order: S(0), dP(0), then per key tile j
+//   S(j+1) once S(j) has been read, dP(j+1) once dP(j) has been read,
+//   dQ += dS(j) K(j) once dS(j) is written (dS buffer j % 2);
+// the elementwise warps compute dS(j) while S(j+1) and dP(j+1) run.
 template <int D, bool BF16>
 __device__ void dq_mma(const BwdTcParams& p, const QUnit& w, const BBars& br, uint32_t smem,
                        uint32_t tmem) {
@@ -655,50 +681,48 @@ __device__ void dq_mma(const BwdTcParams& p, const QUnit& w, const BBars& br, ui
   constexpr int NS = C::qStages;
   using I = QIdx<NS>;
   constexpr uint32_t kFull = 0xffffffffu;
+  auto stage = [&](int j) { return smem + C::qOffKV + static_cast<uint32_t>(j % NS) * C::qStageBytes; };
+  auto wait = [&](int bar, uint32_t parity) {
+    return __all_sync(kFull, bwait(br, p.status, br.bar(bar), parity, kRoleMma));
+  };
   if (w.steps > 0) {
     const uint64_t q_desc = ptx::sdesc_sw128(smem + C::qOffQ, 16, 1024);
     const uint64_t do_desc = ptx::sdesc_sw128(smem + C::qOffDO, 16, 1024);
-    bool ok = __all_sync(kFull, bwait(br, p.status, br.bar(I::qdFull), 0, kRoleMma));
-    int j = 0;
-    for (; ok && j < w.steps; ++j) {
-      const uint32_t s = static_cast<uint32_t>(j % NS);
-      const uint32_t st = smem + C::qOffKV + s * C::qStageBytes;
-      ok = __all_sync(kFull, bwait(br, p.status, br.bar(I::kvFull + s), (j / NS) & 1, kRoleMma));
-      if (ok && j > 0) ok = __all_sync(kFull, bwait(br, p.status, br.bar(I::sFree), (j - 1) & 1, kRoleMma));
-      if (!ok) break;
+    auto issue_s = [&](int j) {  // S(j) = Q K(j)^T
       ptx::tc_fence_after();
-      if (elect()) mma_rows<D, BF16>(tmem + C::kColS, q_desc, ptx::sdesc_sw128(st, 16, 1024));
+      if (elect()) mma_rows<D, BF16>(tmem + C::kColS, q_desc, ptx::sdesc_sw128(stage(j), 16, 1024));
       __syncwarp();
       commit(br.bar(I::sFull));
-      if (j > 0) ok = __all_sync(kFull, bwait(br, p.status, br.bar(I::dsReady), (j - 1) & 1, kRoleMma));
-      if (!ok) break;
-      ptx::tc_fence_after();
-      if (elect()) mma_rows<D, BF16>(tmem + C::kColDP, do_desc, ptx::sdesc_sw128(st + C::kTile, 16, 1024));
-      __syncwarp();
-      commit(br.bar(I::dpFull));
-      if (j > 0) {
-        const uint32_t sp = static_cast<uint32_t>((j - 1) % NS);
-        const uint32_t kp = smem + C::qOffKV + sp * C::qStageBytes;
-        if (elect())
-          mma_acc<D, BF16>(tmem + C::kColAcc0, tmem + C::kColAcc1, TH / 2,
-                           ptx::sdesc_sw128(kp, C::kSlab, 1024), j - 1 > 0);
-        __syncwarp();
-        commit(br.bar(I::dqDone));
-        commit(br.bar(I::kvEmpty + sp));
-      }
-    }
-    if (ok && j == w.steps &&
-        __all_sync(kFull, bwait(br, p.status, br.bar(I::dsReady), (j - 1) & 1, kRoleMma))) {
-      const uint32_t sp = static_cast<uint32_t>((j - 1) % NS);
+    };
+    auto issue_dp = [&](int j) {  // dP(j) = dO V(j)^T
       ptx::tc_fence_after();
       if (elect())
-        mma_acc<D, BF16>(tmem + C::kColAcc0, tmem + C::kColAcc1, TH / 2,
-                         ptx::sdesc_sw128(smem + C::qOffKV + sp * C::qStageBytes, C::kSlab, 1024),
-                         j - 1 > 0);
+        mma_rows<D, BF16>(tmem + C::kColDP, do_desc, ptx::sdesc_sw128(stage(j) + C::kTile, 16, 1024));
       __syncwarp();
-      commit(br.bar(I::dqDone));
-      commit(br.bar(I::kvEmpty + sp));
-      commit(br.bar(I::accFull));
+      commit(br.bar(I::dpFull));
+    };
+    bool ok = wait(I::qdFull, 0) && wait(I::kvFull, 0);
+    if (ok) {
+      issue_s(0);
+      issue_dp(0);
+    }
+    for (int j = 0; ok && j < w.steps; ++j) {
+      const int b = j & 1;
+      if (j + 1 < w.steps) {
+        if (!(ok = wait(I::kvFull + (j + 1) % NS, ((j + 1) / NS) & 1) && wait(I::sFree, j & 1))) break;
+        issue_s(j + 1);
+        if (!(ok = wait(I::dpFree, j & 1))) break;
+        issue_dp(j + 1);
+      }
+      if (!(ok = wait(I::dsReady + b, (j >> 1) & 1))) break;
+      ptx::tc_fence_after();
+      if (elect())
+        mma_acc<D, BF16>(tmem + C::kColAcc0, tmem + C::kColAcc1 + b * (T / 2), TH / 2,
+                         ptx::sdesc_sw128(stage(j), C::kSlab, 1024), j > 0);
+      __syncwarp();
+      commit(br.bar(I::dqDone + b));
+      commit(br.bar(I::kvEmpty + j % NS));
+      if (j + 1 == w.steps) commit(br.bar(I::accFull));
     }
   }
   commit(br.bar(I::drain));
@@ -709,8 +733,8 @@ __device__ void dq_mma(const BwdTcParams& p, const QUnit& w, const BBars& br, ui
 // lane), key columns [64 half, 64 half + 64) of every key tile; its LSE and
 // delta are two registers.  P = exp2(S sm_scale log2(e) - LSE log2(e)), zero
 // for keys at or beyond valid_len[b] and (diagonal tile, causal) after the
-// query; dS = P (dP - delta) into the dS columns (16-bit pairs) once the
-// previous dQ MMA has read them.  Epilogue: warpgroup h writes dQ columns
+// query; dS = P (dP - delta) into dS buffer j % 2 (16-bit pairs) once the dQ
+// MMA of key tile j - 2 has read it.  Epilogue: warpgroup h writes dQ columns
 // [h D/2, (h + 1) D/2) of its row, times sm_scale.
 template <int D, bool BF16>
 __device__ void dq_elementwise(const BwdTcParams& p, const QUnit& w, const BBars& br, uint32_t tmem) {
@@ -723,7 +747,7 @@ __device__ void dq_elementwise(const BwdTcParams& p, const QUnit& w, const BBars
   const uint32_t lane_addr = (((threadIdx.x >> 5) & 3u) * 32u) << 16;
   const uint32_t t_s = tmem + lane_addr + C::kColS + half * TH;
   const uint32_t t_dp = tmem + lane_addr + C::kColDP + half * TH;
-  const uint32_t t_ds = tmem + lane_addr + C::kColAcc1 + half * (TH / 2);
+  const uint32_t t_ds = tmem + lane_addr + C::kColAcc1 + half * (TH / 2);  // + (j % 2) * 64
   const int64_t g_row = (static_cast<int64_t>(w.b) * p.Hq + w.hq) * p.Lp + static_cast<int64_t>(w.m) * T + row;
   const float nl = w.steps > 0 ? p.nlse2[g_row] : 0.f;
   const float dl = w.steps > 0 ? p.delta[g_row] : 0.f;
@@ -760,6 +784,8 @@ __device__ void dq_elementwise(const BwdTcParams& p, const QUnit& w, const BBars
     if (!ok) break;
     ptx::tc_fence_after();
     ptx::tmem_ld64(t_dp, r);
+    ptx::tc_fence_before();
+    ptx::mbar_arrive(br.bar(I::dpFree));
     uint32_t pk[32];
 #pragma unroll
     for (int c = 0; c < TH; c += 2) {
@@ -770,14 +796,16 @@ __device__ void dq_elementwise(const BwdTcParams& p, const QUnit& w, const BBars
       ptx::f2_unpack(d, a, b2);
       pk[c / 2] = pk2<BF16>(a, b2);
     }
-    // the dS columns held dS(j-1): wait until dQ(j-1) has read them
-    if (j > 0) ok = __all_sync(kFull, bwait(br, p.status, br.bar(I::dqDone), (j - 1) & 1, kRoleSoftmax));
+    // buffer j % 2 held dS(j-2): wait until dQ(j-2) has read it
+    const int b = j & 1;
+    if (j >= 2)
+      ok = __all_sync(kFull, bwait(br, p.status, br.bar(I::dqDone + b), ((j >> 1) - 1) & 1, kRoleSoftmax));
     if (!ok) break;
     ptx::tc_fence_after();
-    ptx::tmem_st32(t_ds, pk);
+    ptx::tmem_st32(t_ds + b * (T / 2), pk);
     ptx::tmem_st_wait();
     ptx::tc_fence_before();
-    ptx::mbar_arrive(br.bar(I::dsReady));
+    ptx::mbar_arrive(br.bar(I::dsReady + b));
   }
   if (!ok) return;
   const int i = w.m * T + row;
@@ -815,7 +843,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   const QUnit w = q_unit(p);
   if (threadIdx.x == 0) {
     for (int i = 0; i < I::n; ++i) {
-      const bool ew = (i == I::sFree || i == I::dsReady);
+      const bool ew = (i == I::sFree || i == I::dpFree || i == I::dsReady || i == I::dsReady + 1);
       ptx::mbar_init(br.bar(i), ew ? kEwThreads : 1);
     }
     ptx::st_shared_volatile(br.abort_word(), 0u);
@@ -854,7 +882,8 @@ cudaError_t launch_bwd_tc_d(const CUtensorMap (&maps)[4], const BwdTcParams& p, 
                             cudaStream_t stream) {
   using C = BCfg<D>;
   const int64_t rows = static_cast<int64_t>(p.B) * p.Hq * p.Lp;
-  bwd_tc_prep_kernel<D, BF16><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
+  constexpr int kRowsPerBlock = 8 * (32 / (D / 8));
+  bwd_tc_prep_kernel<D, BF16><<<static_cast<unsigned>((rows + kRowsPerBlock - 1) / kRowsPerBlock), 256, 0, stream>>>(
       o, dO, lse, nlse2, delta, p.L, p.Lp, rows);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;

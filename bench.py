@@ -664,7 +664,8 @@ def run_backward(args, local):
     fp32_peak = 152 * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
     tc_peak = peaks["bf16_tflops"]
     lines = []
-    for name in ("C4", "C2"):
+    impls = ("tc", "simt") if args.bwd_impl == "both" else (args.bwd_impl,)
+    for name in args.bwd_workloads.split(","):
         w = wl.WORKLOADS[name]
         q, k, v, vl = wl.workload_inputs(w)
         q_d, k_d, v_d = q.to(dev), k.to(dev), v.to(dev)
@@ -672,7 +673,7 @@ def run_backward(args, local):
         gen = torch.Generator().manual_seed(w.seed + 100)
         do = torch.randn(q.shape, generator=gen).to(q.dtype).to(dev)
         o, lse = attn.attn_fwd(q_d, k_d, v_d, causal=w.causal, sm_scale=w.sm_scale, valid_len=vl_d)
-        for impl in ("tc", "simt"):
+        for impl in impls:
             def call():
                 return attn.attn_bwd(q_d, k_d, v_d, o, lse, do, causal=w.causal,
                                      sm_scale=w.sm_scale, valid_len=vl_d, impl=impl)
@@ -786,6 +787,10 @@ def main(argv=None):
                     help="instead of the headline line, the section 6.1 comparison table")
     ap.add_argument("--backward", action="store_true",
                     help="instead of the headline line, one line per backward workload")
+    ap.add_argument("--bwd-impl", default="both", choices=["both", "tc", "simt"],
+                    help="--backward: which backward (attn_bwd, attn_bwd_simt or both)")
+    ap.add_argument("--bwd-workloads", default="C4,C2",
+                    help="--backward: comma-separated workload shapes")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
