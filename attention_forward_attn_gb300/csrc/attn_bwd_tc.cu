@@ -85,13 +85,15 @@ struct BCfg {
   static constexpr int kvOffIn = 2 * kTile;
   static constexpr int kvStageBytes = 2 * kTile + 1024;
   static constexpr int kvOffBar = kvOffIn + kvStages * kvStageBytes;
-  // dQ kernel: Q, dO resident; stages of K, V
-  static constexpr int qStages = (D == 128) ? 2 : 4;
+  // dQ kernel: Q, dO resident; a K ring and a V ring (V is released a step
+  // earlier than K: after dP, K only after dQ)
+  static constexpr int qKStages = (D == 128) ? 3 : 6;
+  static constexpr int qVStages = (D == 128) ? 2 : 4;
   static constexpr int qOffQ = 0;
   static constexpr int qOffDO = kTile;
-  static constexpr int qOffKV = 2 * kTile;
-  static constexpr int qStageBytes = 2 * kTile;
-  static constexpr int qOffBar = qOffKV + qStages * qStageBytes;
+  static constexpr int qOffK = 2 * kTile;
+  static constexpr int qOffV = qOffK + qKStages * kTile;
+  static constexpr int qOffBar = qOffV + qVStages * kTile;
   static constexpr int kBarBytes = 256;  // barriers, TMEM base word, abort flag
   static constexpr int kvSmem = kvOffBar + kBarBytes + 1024;  // + slack to align the base
   static constexpr int qSmem = qOffBar + kBarBytes + 1024;
@@ -596,13 +598,15 @@ __global__ void __launch_bounds__(kThreadsB, 1)
 
 // ------------------------------------------------------------------ dQ
 
-// Barrier indices of the dQ kernel (NS key stages, two dS buffers).
-template <int NS>
+// Barrier indices of the dQ kernel (KS K stages, VS V stages, two dS buffers).
+template <int KS, int VS>
 struct QIdx {
-  static constexpr int qdFull = 0;           // Q, dO tiles landed
-  static constexpr int kvFull = 1;           // [NS] K, V of a key tile landed
-  static constexpr int kvEmpty = 1 + NS;     // [NS] the tile's last MMA (dQ) completed
-  static constexpr int sFull = 1 + 2 * NS;   // S in TMEM
+  static constexpr int qdFull = 0;                // Q, dO tiles landed
+  static constexpr int kFull = 1;                 // [KS] K tile landed
+  static constexpr int kEmpty = 1 + KS;           // [KS] its last MMA (dQ) completed
+  static constexpr int vFull = 1 + 2 * KS;        // [VS] V tile landed
+  static constexpr int vEmpty = 1 + 2 * KS + VS;  // [VS] its MMA (dP) completed
+  static constexpr int sFull = 1 + 2 * KS + 2 * VS;  // S in TMEM
   static constexpr int dpFull = sFull + 1;   // dP in TMEM
   static constexpr int sFree = sFull + 2;    // S read (256 arrivals)
   static constexpr int dpFree = sFull + 3;   // dP read (256 arrivals)
@@ -639,8 +643,8 @@ __device__ void dq_producer(const BwdTcParams& p, const QUnit& w, const BBars& b
                             const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                             const CUtensorMap* tm_v, const CUtensorMap* tm_do) {
   using C = BCfg<D>;
-  constexpr int NS = C::qStages;
-  using I = QIdx<NS>;
+  constexpr int KS = C::qKStages, VS = C::qVStages;
+  using I = QIdx<KS, VS>;
   if (w.steps == 0) return;
   const uint64_t pol_keep = ptx::policy_evict_last();   // K, V: read by every query tile
   const uint64_t pol_once = ptx::policy_evict_first();  // Q, dO: read once here
@@ -652,22 +656,30 @@ __device__ void dq_producer(const BwdTcParams& p, const QUnit& w, const BBars& b
     ptx::tma_load_4d_hint(smem + C::qOffDO + h * C::kSlab, tm_do, br.bar(I::qdFull), h * 64,
                           w.m * T, w.hq, w.b, pol_once);
   }
-  int j = 0;
-  for (; j < w.steps; ++j) {
-    const uint32_t s = static_cast<uint32_t>(j % NS);
-    if (!bwait(br, p.status, br.bar(I::kvEmpty + s), ((j / NS) & 1) ^ 1, kRoleProducer)) break;
-    const uint32_t st = smem + C::qOffKV + s * C::qStageBytes;
-    const uint32_t full = br.bar(I::kvFull + s);
-    ptx::mbar_arrive_expect_tx(full, 2 * C::kTile);
+  // K(j) then V(j): K's slot frees after dQ(j - KS), V's after dP(j - VS),
+  // which completes earlier
+  int nk = 0, nv = 0;  // K and V tiles issued
+  for (int j = 0; j < w.steps; ++j) {
+    if (!bwait(br, p.status, br.bar(I::kEmpty + j % KS), ((j / KS) & 1) ^ 1, kRoleProducer)) break;
+    const uint32_t kf = br.bar(I::kFull + j % KS);
+    ptx::mbar_arrive_expect_tx(kf, C::kTile);
 #pragma unroll
-    for (int h = 0; h < D / 64; ++h) {
-      ptx::tma_load_4d_hint(st + h * C::kSlab, tm_k, full, h * 64, j * T, w.hkv, w.b, pol_keep);
-      ptx::tma_load_4d_hint(st + C::kTile + h * C::kSlab, tm_v, full, h * 64, j * T, w.hkv, w.b,
-                            pol_keep);
-    }
+    for (int h = 0; h < D / 64; ++h)
+      ptx::tma_load_4d_hint(smem + C::qOffK + (j % KS) * C::kTile + h * C::kSlab, tm_k, kf, h * 64,
+                            j * T, w.hkv, w.b, pol_keep);
+    ++nk;
+    if (!bwait(br, p.status, br.bar(I::vEmpty + j % VS), ((j / VS) & 1) ^ 1, kRoleProducer)) break;
+    const uint32_t vf = br.bar(I::vFull + j % VS);
+    ptx::mbar_arrive_expect_tx(vf, C::kTile);
+#pragma unroll
+    for (int h = 0; h < D / 64; ++h)
+      ptx::tma_load_4d_hint(smem + C::qOffV + (j % VS) * C::kTile + h * C::kSlab, tm_v, vf, h * 64,
+                            j * T, w.hkv, w.b, pol_keep);
+    ++nv;
   }
   bdrain(br.bar(I::qdFull), 0);
-  for (int k = (j > NS ? j - NS : 0); k < j; ++k) bdrain(br.bar(I::kvFull + k % NS), (k / NS) & 1);
+  for (int k = (nk > KS ? nk - KS : 0); k < nk; ++k) bdrain(br.bar(I::kFull + k % KS), (k / KS) & 1);
+  for (int k = (nv > VS ? nv - VS : 0); k < nv; ++k) bdrain(br.bar(I::vFull + k % VS), (k / VS) & 1);
 }
 
 // Issue order: S(0), dP(0), then per key tile j
@@ -678,10 +690,11 @@ template <int D, bool BF16>
 __device__ void dq_mma(const BwdTcParams& p, const QUnit& w, const BBars& br, uint32_t smem,
                        uint32_t tmem) {
   using C = BCfg<D>;
-  constexpr int NS = C::qStages;
-  using I = QIdx<NS>;
+  constexpr int KS = C::qKStages, VS = C::qVStages;
+  using I = QIdx<KS, VS>;
   constexpr uint32_t kFull = 0xffffffffu;
-  auto stage = [&](int j) { return smem + C::qOffKV + static_cast<uint32_t>(j % NS) * C::qStageBytes; };
+  auto k_tile = [&](int j) { return smem + C::qOffK + static_cast<uint32_t>(j % KS) * C::kTile; };
+  auto v_tile = [&](int j) { return smem + C::qOffV + static_cast<uint32_t>(j % VS) * C::kTile; };
   auto wait = [&](int bar, uint32_t parity) {
     return __all_sync(kFull, bwait(br, p.status, br.bar(bar), parity, kRoleMma));
   };
@@ -690,38 +703,37 @@ __device__ void dq_mma(const BwdTcParams& p, const QUnit& w, const BBars& br, ui
     const uint64_t do_desc = ptx::sdesc_sw128(smem + C::qOffDO, 16, 1024);
     auto issue_s = [&](int j) {  // S(j) = Q K(j)^T
       ptx::tc_fence_after();
-      if (elect()) mma_rows<D, BF16>(tmem + C::kColS, q_desc, ptx::sdesc_sw128(stage(j), 16, 1024));
+      if (elect()) mma_rows<D, BF16>(tmem + C::kColS, q_desc, ptx::sdesc_sw128(k_tile(j), 16, 1024));
       __syncwarp();
       commit(br.bar(I::sFull));
     };
-    auto issue_dp = [&](int j) {  // dP(j) = dO V(j)^T
+    auto issue_dp = [&](int j) {  // dP(j) = dO V(j)^T; V(j) is free once it completes
       ptx::tc_fence_after();
       if (elect())
-        mma_rows<D, BF16>(tmem + C::kColDP, do_desc, ptx::sdesc_sw128(stage(j) + C::kTile, 16, 1024));
+        mma_rows<D, BF16>(tmem + C::kColDP, do_desc, ptx::sdesc_sw128(v_tile(j), 16, 1024));
       __syncwarp();
       commit(br.bar(I::dpFull));
+      commit(br.bar(I::vEmpty + j % VS));
     };
-    bool ok = wait(I::qdFull, 0) && wait(I::kvFull, 0);
-    if (ok) {
-      issue_s(0);
-      issue_dp(0);
-    }
+    bool ok = wait(I::qdFull, 0) && wait(I::kFull, 0);
+    if (ok) issue_s(0);
+    if (ok && (ok = wait(I::vFull, 0))) issue_dp(0);
     for (int j = 0; ok && j < w.steps; ++j) {
       const int b = j & 1;
       if (j + 1 < w.steps) {
-        if (!(ok = wait(I::kvFull + (j + 1) % NS, ((j + 1) / NS) & 1) && wait(I::sFree, j & 1))) break;
+        if (!(ok = wait(I::kFull + (j + 1) % KS, ((j + 1) / KS) & 1) && wait(I::sFree, j & 1))) break;
         issue_s(j + 1);
-        if (!(ok = wait(I::dpFree, j & 1))) break;
+        if (!(ok = wait(I::vFull + (j + 1) % VS, ((j + 1) / VS) & 1) && wait(I::dpFree, j & 1))) break;
         issue_dp(j + 1);
       }
       if (!(ok = wait(I::dsReady + b, (j >> 1) & 1))) break;
       ptx::tc_fence_after();
       if (elect())
         mma_acc<D, BF16>(tmem + C::kColAcc0, tmem + C::kColAcc1 + b * (T / 2), TH / 2,
-                         ptx::sdesc_sw128(stage(j), C::kSlab, 1024), j > 0);
+                         ptx::sdesc_sw128(k_tile(j), C::kSlab, 1024), j > 0);
       __syncwarp();
       commit(br.bar(I::dqDone + b));
-      commit(br.bar(I::kvEmpty + j % NS));
+      commit(br.bar(I::kEmpty + j % KS));
       if (j + 1 == w.steps) commit(br.bar(I::accFull));
     }
   }
@@ -739,8 +751,7 @@ __device__ void dq_mma(const BwdTcParams& p, const QUnit& w, const BBars& br, ui
 template <int D, bool BF16>
 __device__ void dq_elementwise(const BwdTcParams& p, const QUnit& w, const BBars& br, uint32_t tmem) {
   using C = BCfg<D>;
-  constexpr int NS = C::qStages;
-  using I = QIdx<NS>;
+  using I = QIdx<C::qKStages, C::qVStages>;
   constexpr uint32_t kFull = 0xffffffffu;
   const int row = threadIdx.x & 127;
   const int half = static_cast<int>(threadIdx.x) >> 7;
@@ -834,7 +845,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
                      const __grid_constant__ CUtensorMap tm_v,
                      const __grid_constant__ CUtensorMap tm_do, const BwdTcParams p) {
   using C = BCfg<D>;
-  using I = QIdx<C::qStages>;
+  using I = QIdx<C::qKStages, C::qVStages>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t smem = (ptx::smem_u32(smem_raw) + 1023u) & ~1023u;
   const BBars br{smem + C::qOffBar, I::n};
