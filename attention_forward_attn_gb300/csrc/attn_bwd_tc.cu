@@ -50,12 +50,20 @@
 namespace attn {
 namespace {
 
-constexpr int T = 128;             // query rows of a query tile = keys of a key tile
-constexpr int TH = 64;             // columns of one elementwise warpgroup
-constexpr int kEwThreads = 256;    // two elementwise warpgroups
-constexpr int kLoadWarp = 8;
-constexpr int kMmaWarp = 9;
-constexpr int kThreadsB = 320;
+// Elementwise warpgroups per CTA: each takes T / kGroups columns of every
+// 128 x 128 step.  Two (64 columns per thread) measured 2-4 % faster than
+// four (32 columns, twice the warps per sub-partition).
+#ifndef ATTN_BWD_EW_GROUPS
+#define ATTN_BWD_EW_GROUPS 2
+#endif
+constexpr int T = 128;                       // query rows of a query tile = keys of a key tile
+constexpr int kGroups = ATTN_BWD_EW_GROUPS;  // elementwise warpgroups
+constexpr int TH = T / kGroups;              // columns of one elementwise warpgroup
+constexpr int kEwThreads = 128 * kGroups;
+constexpr int kLoadWarp = 4 * kGroups;
+constexpr int kMmaWarp = 4 * kGroups + 1;
+constexpr int kThreadsB = 32 * (4 * kGroups + 2);
+static_assert(kGroups == 2 || kGroups == 4, "two or four elementwise warpgroups");
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct BwdTcParams {
@@ -171,18 +179,40 @@ __device__ __forceinline__ void mma_rows(uint32_t d_tmem, uint64_t a_desc, uint6
   }
 }
 
-// acc (+)= A X with A a 128 x 128 16-bit matrix in TMEM (two 64-column halves,
-// each packed into the first 32 columns of its half: P^T, dS^T) or packed
-// contiguously (dS of the dQ kernel, a_half = 32), and X a 128-row tile used
-// as an MN-major operand (X = dO, Q or K; 16 rows per MMA).
+// acc (+)= A X with A a 128 x 128 16-bit matrix in TMEM, one TH-column block
+// per elementwise warpgroup, each packed into the first TH/2 columns of its
+// block (P^T, dS^T: a_group = TH) or all packed contiguously (dS of the dQ
+// kernel: a_group = TH/2), and X a 128-row tile used as an MN-major operand
+// (X = dO, Q or K; 16 rows per MMA).
 template <int D, bool BF16>
-__device__ __forceinline__ void mma_acc(uint32_t acc, uint32_t a_tmem, uint32_t a_half,
+__device__ __forceinline__ void mma_acc(uint32_t acc, uint32_t a_tmem, uint32_t a_group,
                                         uint64_t x_mn, bool accumulate) {
   constexpr uint32_t idesc = ptx::idesc_f16(T, D, BF16, true);
+  constexpr int kPerGroup = TH / 16;  // MMAs (16 K values each) per warpgroup block
 #pragma unroll
   for (int kk = 0; kk < T / 16; ++kk) {
-    ptx::mma_ts(acc, a_tmem + (kk / 4) * a_half + (kk & 3) * 8u, dadd(x_mn, kk * 2048u), idesc,
-                (accumulate || kk > 0) ? 1u : 0u);
+    ptx::mma_ts(acc, a_tmem + (kk / kPerGroup) * a_group + (kk % kPerGroup) * 8u,
+                dadd(x_mn, kk * 2048u), idesc, (accumulate || kk > 0) ? 1u : 0u);
+  }
+}
+
+// N = TH consecutive fp32 columns of this thread's TMEM lane; N/2 packed columns back.
+template <int N>
+__device__ __forceinline__ void ld_th(uint32_t taddr, uint32_t (&r)[N]) {
+  static_assert(N == 32 || N == 64, "32 or 64 columns");
+  if constexpr (N == 64) {
+    ptx::tmem_ld64(taddr, r);
+  } else {
+    ptx::tmem_ld32(taddr, r);
+  }
+}
+template <int N>
+__device__ __forceinline__ void st_th2(uint32_t taddr, const uint32_t (&r)[N]) {
+  static_assert(N == 16 || N == 32, "16 or 32 packed columns");
+  if constexpr (N == 32) {
+    ptx::tmem_st32(taddr, r);
+  } else {
+    ptx::tmem_st16(taddr, r);
   }
 }
 
@@ -431,12 +461,13 @@ __device__ __forceinline__ void store_chunk(uint16_t* dst, const uint32_t (&r)[3
 }
 
 // Elementwise warpgroups of the dK/dV kernel.  Thread: key row `row` of the
-// tile (TMEM lane), query columns [64 half, 64 half + 64) of every step.
+// tile (TMEM lane), query columns [TH grp, TH grp + TH) of every step.
 //   P^T = exp2(S^T sm_scale log2(e) - LSE log2(e)), zero where the key is at
 //   or beyond valid_len[b] or (diagonal tile, causal) after the query; kept in
 //   fp32 registers for dS and written to TMEM as 16-bit pairs;
 //   dS^T = P^T (dP^T - delta), written over the dP^T columns.
-// Epilogue: warpgroup 0 writes the dV row, warpgroup 1 the dK row (x sm_scale).
+// Epilogue: the first half of the warpgroups write dV, the second dK (x
+// sm_scale), each a D / (kGroups / 2)-column part of the row.
 template <int D, bool BF16>
 __device__ void dkv_elementwise(const BwdTcParams& p, const KvUnit& w, const BBars& br,
                                 uint32_t smem, uint32_t tmem) {
@@ -445,10 +476,10 @@ __device__ void dkv_elementwise(const BwdTcParams& p, const KvUnit& w, const BBa
   using I = KvIdx<NS>;
   constexpr uint32_t kFull = 0xffffffffu;
   const int row = threadIdx.x & 127;
-  const int half = static_cast<int>(threadIdx.x) >> 7;
+  const int grp = static_cast<int>(threadIdx.x) >> 7;
   const uint32_t lane_addr = (((threadIdx.x >> 5) & 3u) * 32u) << 16;
-  const uint32_t t_s = tmem + lane_addr + C::kColS + half * TH;
-  const uint32_t t_dp = tmem + lane_addr + C::kColDP + half * TH;
+  const uint32_t t_s = tmem + lane_addr + C::kColS + grp * TH;
+  const uint32_t t_dp = tmem + lane_addr + C::kColDP + grp * TH;
   const bool key_ok = w.n * T + row < w.kv_len;
   const uint64_t sc2 = ptx::f2_pack(p.scale_log2, p.scale_log2);
   bool ok = true;
@@ -461,10 +492,10 @@ __device__ void dkv_elementwise(const BwdTcParams& p, const KvUnit& w, const BBa
     if (ok) ok = __all_sync(kFull, bwait(br, p.status, br.bar(I::sFull), t & 1, kRoleSoftmax));
     if (!ok) break;
     ptx::tc_fence_after();
-    uint32_t r[64];
-    ptx::tmem_ld64(t_s, r);
+    uint32_t r[TH];
+    ld_th(t_s, r);
     float pr[TH];
-    const uint32_t nl_addr = st + 2 * C::kTile + half * TH * 4;
+    const uint32_t nl_addr = st + 2 * C::kTile + grp * TH * 4;
 #pragma unroll
     for (int c = 0; c < TH; c += 4) {
       const uint4 nl = ptx::ld_shared_v4(nl_addr + c * 4);
@@ -481,15 +512,15 @@ __device__ void dkv_elementwise(const BwdTcParams& p, const KvUnit& w, const BBa
       pr[c + 3] = ptx::ex2_approx(x3);
     }
     // columns c < cmin hold queries before this key (diagonal tile, causal)
-    const int cmin = key_ok ? ((p.causal && mi == w.n) ? row - half * TH : 0) : TH;
+    const int cmin = key_ok ? ((p.causal && mi == w.n) ? row - grp * TH : 0) : TH;
     if (cmin > 0) {
 #pragma unroll
       for (int c = 0; c < TH; ++c) pr[c] = c < cmin ? 0.f : pr[c];
     }
-    uint32_t pk[32];
+    uint32_t pk[TH / 2];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) pk[i] = pk2<BF16>(pr[2 * i], pr[2 * i + 1]);
-    ptx::tmem_st32(t_s, pk);
+    for (int i = 0; i < TH / 2; ++i) pk[i] = pk2<BF16>(pr[2 * i], pr[2 * i + 1]);
+    st_th2(t_s, pk);
     ptx::tmem_st_wait();
     ptx::tc_fence_before();
     ptx::mbar_arrive(br.bar(I::pReady));
@@ -497,8 +528,8 @@ __device__ void dkv_elementwise(const BwdTcParams& p, const KvUnit& w, const BBa
     ok = __all_sync(kFull, bwait(br, p.status, br.bar(I::dpFull), t & 1, kRoleSoftmax));
     if (!ok) break;
     ptx::tc_fence_after();
-    ptx::tmem_ld64(t_dp, r);
-    const uint32_t dl_addr = st + 2 * C::kTile + T * 4 + half * TH * 4;
+    ld_th(t_dp, r);
+    const uint32_t dl_addr = st + 2 * C::kTile + T * 4 + grp * TH * 4;
 #pragma unroll
     for (int c = 0; c < TH; c += 4) {
       const uint4 dl = ptx::ld_shared_v4(dl_addr + c * 4);
@@ -516,28 +547,32 @@ __device__ void dkv_elementwise(const BwdTcParams& p, const KvUnit& w, const BBa
       pk[c / 2] = pk2<BF16>(a, b2);
       pk[c / 2 + 1] = pk2<BF16>(c2, d2);
     }
-    ptx::tmem_st32(t_dp, pk);
+    st_th2(t_dp, pk);
     ptx::tmem_st_wait();
     ptx::tc_fence_before();
     ptx::mbar_arrive(br.bar(I::dsReady));
   }
   if (!ok) return;
-  // epilogue: warpgroup 0 the dV row, warpgroup 1 the dK row
+  // epilogue: warpgroups [0, kGroups/2) the dV row, the others the dK row,
+  // kPart columns each
+  constexpr int kPart = D / (kGroups / 2);
+  const bool is_dk = grp >= kGroups / 2;
+  const int c_lo = (grp % (kGroups / 2)) * kPart;
   const int j = w.n * T + row;
   const bool store = j < p.L;
-  uint16_t* dst = static_cast<uint16_t*>(half ? p.dk : p.dv) +
-                  ((static_cast<int64_t>(w.b) * p.Hkv + w.hkv) * p.L + j) * D;
+  uint16_t* dst = static_cast<uint16_t*>(is_dk ? p.dk : p.dv) +
+                  ((static_cast<int64_t>(w.b) * p.Hkv + w.hkv) * p.L + j) * D + c_lo;
   if (w.steps == 0) {  // no query sees these keys
     if (store)
-      for (int c = 0; c < D / 8; ++c) reinterpret_cast<uint4*>(dst)[c] = make_uint4(0u, 0u, 0u, 0u);
+      for (int c = 0; c < kPart / 8; ++c) reinterpret_cast<uint4*>(dst)[c] = make_uint4(0u, 0u, 0u, 0u);
     return;
   }
   if (!__all_sync(kFull, bwait(br, p.status, br.bar(I::accFull), 0, kRoleEpilogue))) return;
   ptx::tc_fence_after();
-  const uint32_t t_acc = tmem + lane_addr + (half ? C::kColAcc1 : C::kColAcc0);
-  const float mul = half ? p.sm_scale : 1.f;
+  const uint32_t t_acc = tmem + lane_addr + (is_dk ? C::kColAcc1 : C::kColAcc0) + c_lo;
+  const float mul = is_dk ? p.sm_scale : 1.f;
 #pragma unroll 1
-  for (int c0 = 0; c0 < D; c0 += 32) {
+  for (int c0 = 0; c0 < kPart; c0 += 32) {
     uint32_t r[32];
     ptx::tmem_ld32(t_acc + c0, r);
     store_chunk<BF16>(dst + c0, r, mul, store);
@@ -742,23 +777,23 @@ __device__ void dq_mma(const BwdTcParams& p, const QUnit& w, const BBars& br, ui
 }
 
 // Elementwise warpgroups of the dQ kernel.  Thread: query row `row` (TMEM
-// lane), key columns [64 half, 64 half + 64) of every key tile; its LSE and
+// lane), key columns [TH grp, TH grp + TH) of every key tile; its LSE and
 // delta are two registers.  P = exp2(S sm_scale log2(e) - LSE log2(e)), zero
 // for keys at or beyond valid_len[b] and (diagonal tile, causal) after the
 // query; dS = P (dP - delta) into dS buffer j % 2 (16-bit pairs) once the dQ
-// MMA of key tile j - 2 has read it.  Epilogue: warpgroup h writes dQ columns
-// [h D/2, (h + 1) D/2) of its row, times sm_scale.
+// MMA of key tile j - 2 has read it.  Epilogue: warpgroup g < kEpi writes dQ
+// columns [g D/kEpi, (g + 1) D/kEpi) of its row, times sm_scale.
 template <int D, bool BF16>
 __device__ void dq_elementwise(const BwdTcParams& p, const QUnit& w, const BBars& br, uint32_t tmem) {
   using C = BCfg<D>;
   using I = QIdx<C::qKStages, C::qVStages>;
   constexpr uint32_t kFull = 0xffffffffu;
   const int row = threadIdx.x & 127;
-  const int half = static_cast<int>(threadIdx.x) >> 7;
+  const int grp = static_cast<int>(threadIdx.x) >> 7;
   const uint32_t lane_addr = (((threadIdx.x >> 5) & 3u) * 32u) << 16;
-  const uint32_t t_s = tmem + lane_addr + C::kColS + half * TH;
-  const uint32_t t_dp = tmem + lane_addr + C::kColDP + half * TH;
-  const uint32_t t_ds = tmem + lane_addr + C::kColAcc1 + half * (TH / 2);  // + (j % 2) * 64
+  const uint32_t t_s = tmem + lane_addr + C::kColS + grp * TH;
+  const uint32_t t_dp = tmem + lane_addr + C::kColDP + grp * TH;
+  const uint32_t t_ds = tmem + lane_addr + C::kColAcc1 + grp * (TH / 2);  // + (j % 2) * 64
   const int64_t g_row = (static_cast<int64_t>(w.b) * p.Hq + w.hq) * p.Lp + static_cast<int64_t>(w.m) * T + row;
   const float nl = w.steps > 0 ? p.nlse2[g_row] : 0.f;
   const float dl = w.steps > 0 ? p.delta[g_row] : 0.f;
@@ -770,8 +805,8 @@ __device__ void dq_elementwise(const BwdTcParams& p, const QUnit& w, const BBars
     ok = __all_sync(kFull, bwait(br, p.status, br.bar(I::sFull), j & 1, kRoleSoftmax));
     if (!ok) break;
     ptx::tc_fence_after();
-    uint32_t r[64];
-    ptx::tmem_ld64(t_s, r);
+    uint32_t r[TH];
+    ld_th(t_s, r);
     float pr[TH];
 #pragma unroll
     for (int c = 0; c < TH; c += 2) {
@@ -785,8 +820,8 @@ __device__ void dq_elementwise(const BwdTcParams& p, const QUnit& w, const BBars
     ptx::mbar_arrive(br.bar(I::sFree));
     // visible key columns: c < climit (causal diagonal tile; last key tile)
     int climit = TH;
-    if (p.causal && j == w.m) climit = min(climit, row - half * TH + 1);
-    climit = min(climit, w.kv_len - j * T - half * TH);
+    if (p.causal && j == w.m) climit = min(climit, row - grp * TH + 1);
+    climit = min(climit, w.kv_len - j * T - grp * TH);
     if (climit < TH) {
 #pragma unroll
       for (int c = 0; c < TH; ++c) pr[c] = c < climit ? pr[c] : 0.f;
@@ -794,10 +829,10 @@ __device__ void dq_elementwise(const BwdTcParams& p, const QUnit& w, const BBars
     ok = __all_sync(kFull, bwait(br, p.status, br.bar(I::dpFull), j & 1, kRoleSoftmax));
     if (!ok) break;
     ptx::tc_fence_after();
-    ptx::tmem_ld64(t_dp, r);
+    ld_th(t_dp, r);
     ptx::tc_fence_before();
     ptx::mbar_arrive(br.bar(I::dpFree));
-    uint32_t pk[32];
+    uint32_t pk[TH / 2];
 #pragma unroll
     for (int c = 0; c < TH; c += 2) {
       const uint64_t d = ptx::f2_mul(
@@ -813,26 +848,29 @@ __device__ void dq_elementwise(const BwdTcParams& p, const QUnit& w, const BBars
       ok = __all_sync(kFull, bwait(br, p.status, br.bar(I::dqDone + b), ((j >> 1) - 1) & 1, kRoleSoftmax));
     if (!ok) break;
     ptx::tc_fence_after();
-    ptx::tmem_st32(t_ds + b * (T / 2), pk);
+    st_th2(t_ds + b * (T / 2), pk);
     ptx::tmem_st_wait();
     ptx::tc_fence_before();
     ptx::mbar_arrive(br.bar(I::dsReady + b));
   }
-  if (!ok) return;
+  // epilogue: kEpi warpgroups, kPart columns each (32-column loads)
+  constexpr int kEpi = (kGroups < D / 32) ? kGroups : D / 32;
+  constexpr int kPart = D / kEpi;
+  if (!ok || grp >= kEpi) return;
   const int i = w.m * T + row;
   const bool store = i < p.L;
   uint16_t* dst = static_cast<uint16_t*>(p.dq) +
-                  ((static_cast<int64_t>(w.b) * p.Hq + w.hq) * p.L + i) * D + half * (D / 2);
+                  ((static_cast<int64_t>(w.b) * p.Hq + w.hq) * p.L + i) * D + grp * kPart;
   if (w.steps == 0) {  // no visible key: dQ = 0
     if (store)
-      for (int c = 0; c < D / 16; ++c) reinterpret_cast<uint4*>(dst)[c] = make_uint4(0u, 0u, 0u, 0u);
+      for (int c = 0; c < kPart / 8; ++c) reinterpret_cast<uint4*>(dst)[c] = make_uint4(0u, 0u, 0u, 0u);
     return;
   }
   if (!__all_sync(kFull, bwait(br, p.status, br.bar(I::accFull), 0, kRoleEpilogue))) return;
   ptx::tc_fence_after();
-  const uint32_t t_acc = tmem + lane_addr + C::kColAcc0 + half * (D / 2);
+  const uint32_t t_acc = tmem + lane_addr + C::kColAcc0 + grp * kPart;
 #pragma unroll 1
-  for (int c0 = 0; c0 < D / 2; c0 += 32) {
+  for (int c0 = 0; c0 < kPart; c0 += 32) {
     uint32_t r[32];
     ptx::tmem_ld32(t_acc + c0, r);
     store_chunk<BF16>(dst + c0, r, p.sm_scale, store);
