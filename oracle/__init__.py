@@ -62,6 +62,9 @@ def _bind(path: str):
     lib.oracle_attn_bwd_f64.argtypes = [p, p, p, p, p, p, p, i, i, i, i, i, ctypes.c_double, i,
                                         p, i]
     lib.oracle_attn_bwd_f64.restype = i
+    lib.oracle_attn_bwd_rows_f64.argtypes = [p, p, p, p, i, i, i, i, i, ctypes.c_double, i, p,
+                                             p, i64, p, p, p, i64, p, p, p, i]
+    lib.oracle_attn_bwd_rows_f64.restype = i
     lib.oracle_decode.argtypes = [p, p, i64, i]
     lib.oracle_decode.restype = i
     lib.oracle_max_threads.argtypes = []
@@ -215,6 +218,38 @@ def attn_bwd_f64(q, k, v, do, sm_scale, causal=False, valid_len=None, threads=0,
     if rc != 0:
         raise ValueError("oracle_attn_bwd_f64 failed with code %d" % rc)
     return dq, dk, dv
+
+
+def attn_bwd_rows_f64(q, k, v, do, sm_scale, causal=False, valid_len=None, q_rows=(),
+                      k_rows=(), threads=0, _lib_override=None):
+    """Selected rows of :func:`attn_bwd_f64`'s gradients (see
+    oracle_attn_bwd_rows_f64): dQ for flat query rows ``q_rows`` (index
+    (b*Hq + h_q)*L + i) and dK, dV for flat key rows ``k_rows`` (index
+    (b*Hkv + h_kv)*L + j).  Returns dq [n_q, D], qmag [n_q, 3] (sum_j |dS_ij|,
+    sum_d |dO_id O_id|, visible keys), dk, dv [n_k, D], kmag [n_k, 4]
+    (sum_i |dS_ij|, sum_i P_ij, sum_i P_ij sum_d |dO_id O_id|, visible queries)."""
+    q = np.ascontiguousarray(q, dtype=np.float64)
+    k = np.ascontiguousarray(k, dtype=np.float64)
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    do = np.ascontiguousarray(do, dtype=np.float64)
+    B, Hq, Hkv, Lq, Lk, D = _shapes(q, k, v)
+    if Lq != Lk or do.shape != q.shape:
+        raise ValueError("the backward oracle takes Lq == Lk and do shaped like q")
+    vl = _valid(valid_len, B)
+    qr = np.ascontiguousarray(np.asarray(q_rows, dtype=np.int64).reshape(-1))
+    kr = np.ascontiguousarray(np.asarray(k_rows, dtype=np.int64).reshape(-1))
+    dq = np.empty((qr.size, D))
+    qmag = np.empty((qr.size, 3))
+    dk, dv = np.empty((kr.size, D)), np.empty((kr.size, D))
+    kmag = np.empty((kr.size, 4))
+    lib = _lib_override if _lib_override is not None else _load()
+    rc = lib.oracle_attn_bwd_rows_f64(_ptr(q), _ptr(k), _ptr(v), _ptr(do), B, Hq, Hkv, Lq, D,
+                                      float(sm_scale), int(bool(causal)), _ptr(vl), _ptr(qr),
+                                      qr.size, _ptr(dq), _ptr(qmag), _ptr(kr), kr.size, _ptr(dk),
+                                      _ptr(dv), _ptr(kmag), int(threads))
+    if rc != 0:
+        raise ValueError("oracle_attn_bwd_rows_f64 failed with code %d" % rc)
+    return dq, qmag, dk, dv, kmag
 
 
 def load_variant(path: str):

@@ -337,3 +337,214 @@ int oracle_attn_bwd_f64(const double* q, const double* k, const double* v, const
   }
   return bad ? 2 : 0;
 }
+
+/*
+ * Statistics of query row i (q_row, do_row) against the keys of its K/V head,
+ * from the definition: the maximum m of the visible scores s_j = sm_scale *
+ * q_i.k_j, z = sum_j exp(s_j - m), delta = sum_j P_ij dP_ij with
+ * P_ij = exp(s_j - m) / z and dP_ij = dO_i.v_j.  s: scratch of L doubles.
+ * Returns the number of visible keys (0: the row sees none; m, z, delta unset).
+ */
+static int64_t row_stats(const double* q_row, const double* do_row, const double* k_head,
+                         const double* v_head, int64_t i, int b, int L, int D, double sm_scale,
+                         int causal, const int32_t* valid_len, double* s, double* m_out,
+                         double* z_out, double* delta_out) {
+  const oracle_mask_t mk = {NULL, 0, 0};
+  double m = -INFINITY;
+  int64_t n = 0;
+  for (int64_t j = 0; j < L; ++j) {
+    if (!key_visible(i, j, b, causal, valid_len, &mk)) continue;
+    double dot = 0.0;
+    for (int d = 0; d < D; ++d) dot += q_row[d] * k_head[j * D + d];
+    s[j] = sm_scale * dot;
+    if (s[j] > m) m = s[j];
+    ++n;
+  }
+  if (n == 0) return 0;
+  double z = 0.0, acc = 0.0;
+  for (int64_t j = 0; j < L; ++j) {
+    if (!key_visible(i, j, b, causal, valid_len, &mk)) continue;
+    const double e = exp(s[j] - m);
+    double dp = 0.0;
+    for (int d = 0; d < D; ++d) dp += do_row[d] * v_head[j * D + d];
+    z += e;
+    acc += e * dp;
+  }
+  *m_out = m;
+  *z_out = z;
+  *delta_out = acc / z;
+  return n;
+}
+
+/*
+ * Selected rows of the gradients of oracle_attn_bwd_f64 (same inputs and
+ * definition), for checks at sizes where the full backward is too slow:
+ *   dQ rows q_rows[r] (flat index (b*Hq + h_q)*L + i), r < n_q -> dq[r*D ..];
+ *   dK, dV rows k_rows[r] (flat index (b*Hkv + h_kv)*L + j), r < n_k ->
+ *   dk[r*D ..], dv[r*D ..].
+ * A key row sums over every query row of its group's G query heads, so the
+ * statistics of those rows are computed once per group that a sampled key
+ * row belongs to.  Also, per row, magnitudes a tolerance can be built on
+ * (w_i = sum_d |dO_id O_id|, O_i the forward's output row):
+ *   qmag[3r ..]: sum_j |dS_ij|, w_i, visible keys;
+ *   kmag[4r ..]: sum_i |dS_ij|, sum_i P_ij, sum_i P_ij w_i, visible queries
+ * (sums over the G query heads of the key's group).
+ */
+int oracle_attn_bwd_rows_f64(const double* q, const double* k, const double* v, const double* dO,
+                             int B, int Hq, int Hkv, int L, int D, double sm_scale, int causal,
+                             const int32_t* valid_len, const int64_t* q_rows, int64_t n_q,
+                             double* dq, double* qmag, const int64_t* k_rows, int64_t n_k,
+                             double* dk, double* dv, double* kmag, int threads) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || L < 1 || D < 1 || Hq % Hkv != 0) return 1;
+  const int G = Hq / Hkv;
+  const oracle_mask_t mk = {NULL, 0, 0};
+  for (int64_t r = 0; r < n_q; ++r)
+    if (q_rows[r] < 0 || q_rows[r] >= (int64_t)B * Hq * L) return 1;
+  for (int64_t r = 0; r < n_k; ++r)
+    if (k_rows[r] < 0 || k_rows[r] >= (int64_t)B * Hkv * L) return 1;
+#ifdef _OPENMP
+  if (threads > 0) omp_set_num_threads(threads);
+#else
+  (void)threads;
+#endif
+  int bad = 0;
+  /* dQ rows */
+#pragma omp parallel
+  {
+    double* s = (double*)malloc(sizeof(double) * (size_t)L);
+    if (!s) {
+#pragma omp atomic write
+      bad = 1;
+    }
+#pragma omp for schedule(dynamic, 1)
+    for (int64_t r = 0; r < n_q; ++r) {
+      if (!s) continue;
+      const int64_t qh = q_rows[r] / L;
+      const int64_t i = q_rows[r] % L;
+      const int b = (int)(qh / Hq);
+      const int64_t kvh = (int64_t)b * Hkv + (qh % Hq) / G;
+      const double* q_row = q + q_rows[r] * D;
+      const double* do_row = dO + q_rows[r] * D;
+      const double* k_head = k + kvh * L * (int64_t)D;
+      const double* v_head = v + kvh * L * (int64_t)D;
+      double* dq_row = dq + r * D;
+      double m = 0.0, z = 1.0, delta = 0.0, sabs = 0.0, w = 0.0;
+      for (int d = 0; d < D; ++d) dq_row[d] = 0.0;
+      const int64_t n = row_stats(q_row, do_row, k_head, v_head, i, b, L, D, sm_scale, causal,
+                                  valid_len, s, &m, &z, &delta);
+      if (n > 0) {
+        double* o_row = (double*)calloc((size_t)D, sizeof(double));
+        for (int64_t j = 0; j < L; ++j) {
+          if (!key_visible(i, j, b, causal, valid_len, &mk)) continue;
+          const double p = exp(s[j] - m) / z;
+          double dp = 0.0;
+          for (int d = 0; d < D; ++d) dp += do_row[d] * v_head[j * D + d];
+          const double ds = p * (dp - delta);
+          const double* k_j = k_head + j * D;
+          sabs += fabs(ds);
+          for (int d = 0; d < D; ++d) {
+            dq_row[d] += sm_scale * ds * k_j[d];
+            if (o_row) o_row[d] += p * v_head[j * D + d];
+          }
+        }
+        if (o_row) {
+          for (int d = 0; d < D; ++d) w += fabs(do_row[d] * o_row[d]);
+        } else {
+#pragma omp atomic write
+          bad = 1;
+        }
+        free(o_row);
+      }
+      qmag[3 * r] = sabs;
+      qmag[3 * r + 1] = w;
+      qmag[3 * r + 2] = (double)n;
+    }
+    free(s);
+  }
+  /* dK, dV rows: group by K/V head, row statistics of the group's query rows once */
+  for (int64_t r0 = 0; r0 < n_k && !bad; ++r0) {
+    const int64_t kvh = k_rows[r0] / L;
+    int seen = 0;
+    for (int64_t r = 0; r < r0; ++r) seen |= (k_rows[r] / L == kvh);
+    if (seen) continue;
+    const int b = (int)(kvh / Hkv);
+    const int h_kv = (int)(kvh % Hkv);
+    const double* k_head = k + kvh * L * (int64_t)D;
+    const double* v_head = v + kvh * L * (int64_t)D;
+    const int64_t nrow = (int64_t)G * L;
+    double* st = (double*)malloc(sizeof(double) * 4 * (size_t)nrow);  /* m, z, delta, w */
+    if (!st) return 2;
+#pragma omp parallel
+    {
+      double* s = (double*)malloc(sizeof(double) * (size_t)L);
+      double* o_row = (double*)malloc(sizeof(double) * (size_t)D);
+      if (!s || !o_row) {
+#pragma omp atomic write
+        bad = 1;
+      }
+#pragma omp for schedule(dynamic, 16)
+      for (int64_t gi = 0; gi < nrow; ++gi) {
+        if (!s || !o_row) continue;
+        const int64_t qrow = ((int64_t)b * Hq + (int64_t)h_kv * G + gi / L) * L + gi % L;
+        const int64_t i = gi % L;
+        double m = 0.0, z = 1.0, delta = 0.0, w = 0.0;
+        const int64_t n = row_stats(q + qrow * D, dO + qrow * D, k_head, v_head, i, b, L, D,
+                                    sm_scale, causal, valid_len, s, &m, &z, &delta);
+        if (n > 0) {
+          for (int d = 0; d < D; ++d) o_row[d] = 0.0;
+          for (int64_t j = 0; j < L; ++j) {
+            if (!key_visible(i, j, b, causal, valid_len, &mk)) continue;
+            const double p = exp(s[j] - m) / z;
+            for (int d = 0; d < D; ++d) o_row[d] += p * v_head[j * D + d];
+          }
+          for (int d = 0; d < D; ++d) w += fabs(dO[qrow * D + d] * o_row[d]);
+        }
+        st[4 * gi] = n > 0 ? m : INFINITY;  /* +inf: the row sees no key */
+        st[4 * gi + 1] = z;
+        st[4 * gi + 2] = delta;
+        st[4 * gi + 3] = w;
+      }
+      free(s);
+      free(o_row);
+    }
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = r0; r < n_k; ++r) {
+      if (k_rows[r] / L != kvh) continue;
+      const int64_t j = k_rows[r] % L;
+      const double* k_row = k_head + j * D;
+      const double* v_row = v_head + j * D;
+      double* dk_row = dk + r * D;
+      double* dv_row = dv + r * D;
+      double sabs = 0.0, psum = 0.0, pw = 0.0, nvis = 0.0;
+      for (int d = 0; d < D; ++d) dk_row[d] = dv_row[d] = 0.0;
+      for (int64_t gi = 0; gi < nrow; ++gi) {
+        const int64_t i = gi % L;
+        if (st[4 * gi] == INFINITY || !key_visible(i, j, b, causal, valid_len, &mk)) continue;
+        const int64_t qrow = ((int64_t)b * Hq + (int64_t)h_kv * G + gi / L) * L + i;
+        const double* q_row = q + qrow * D;
+        const double* do_row = dO + qrow * D;
+        double dot = 0.0, dp = 0.0;
+        for (int d = 0; d < D; ++d) {
+          dot += q_row[d] * k_row[d];
+          dp += do_row[d] * v_row[d];
+        }
+        const double p = exp(sm_scale * dot - st[4 * gi]) / st[4 * gi + 1];
+        const double ds = p * (dp - st[4 * gi + 2]);
+        for (int d = 0; d < D; ++d) {
+          dv_row[d] += p * do_row[d];
+          dk_row[d] += sm_scale * ds * q_row[d];
+        }
+        sabs += fabs(ds);
+        psum += p;
+        pw += p * st[4 * gi + 3];
+        nvis += 1.0;
+      }
+      kmag[4 * r] = sabs;
+      kmag[4 * r + 1] = psum;
+      kmag[4 * r + 2] = pw;
+      kmag[4 * r + 3] = nvis;
+    }
+    free(st);
+  }
+  return bad ? 2 : 0;
+}
