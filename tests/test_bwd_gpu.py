@@ -164,3 +164,59 @@ def test_bwd_tc_deterministic_and_close_to_simt():
         assert torch.equal(x.view(torch.int16), y.view(torch.int16))
         diff = (x.float() - z.float()).abs()
         assert float(diff.max()) <= 0.02 * float(z.float().abs().max()), float(diff.max())
+
+
+@pytest.mark.parametrize("name", ["C4", "C2", "C3"])
+def test_bwd_full_size_sampled_rows(name):
+    """The workload's full shapes and masks: attn_bwd against the oracle on
+    sampled rows -- dQ rows on tile boundaries of several heads and batches,
+    dK/dV rows of two K/V heads (the first and the last) -- from
+    oracle.attn_bwd_rows_f64.  Bound: the same terms as run_case, with the
+    per-element sums over keys / queries bounded through the oracle's row
+    magnitudes and the largest |k|, |q|, |dO|:
+        dQ: sm_scale max|k| (u w_i + u sum_j |dS_ij| + a n_i)
+        dK: sm_scale max|q| (u sum_i P_ij w_i + u sum_i |dS_ij| + a n_j)
+        dV: max|dO| (u sum_i P_ij + a n_j)
+    plus 1e-2 |g| and 1e-4 max|g| (w_i = sum_d |dO_id O_id|)."""
+    w = wl.WORKLOADS[name]
+    q, k, v, vl = wl.workload_inputs(w)
+    do = torch.randn(q.shape, generator=torch.Generator().manual_seed(w.seed + 100)).to(q.dtype)
+    dev = torch.device("cuda")
+    qd, kd, vd, dod = q.to(dev), k.to(dev), v.to(dev), do.to(dev)
+    vld = None if vl is None else vl.to(dev)
+    o, lse = attn.attn_fwd(qd, kd, vd, causal=w.causal, sm_scale=w.sm_scale, valid_len=vld)
+    dq, dk, dv = attn.attn_bwd(qd, kd, vd, o, lse, dod, causal=w.causal, sm_scale=w.sm_scale,
+                               valid_len=vld)
+    assert attn.status() == (attn.ATTN_OK, 0)
+    B, Hq, L, D = q.shape
+    Hkv = k.shape[1]
+    rng = np.random.default_rng(w.seed)
+    rows = sorted({0, 1, 127, 128, 255, L // 2, L - 129, L - 1} | set(rng.integers(0, L, 6).tolist()))
+    heads = sorted({0, 5 % Hq, Hq - 1, Hq // 2 + 3})
+    qr = np.array([(b * Hq + h) * L + i for b in sorted({0, B - 1}) for h in heads for i in rows])
+    kr = np.array([(z * L) + j for z in (0, B * Hkv - 1) for j in rows])
+    f = lambda t: t.double().numpy()
+    vl_np = None if vl is None else vl.numpy()
+    r_dq, qm, r_dk, r_dv, km = oracle.attn_bwd_rows_f64(f(q), f(k), f(v), f(do), w.sm_scale,
+                                                        causal=w.causal, valid_len=vl_np,
+                                                        q_rows=qr, k_rows=kr)
+    u = 2.0 ** -8 if w.dtype == wl.BF16 else 2.0 ** -11
+    a = 0.0 if w.dtype == wl.BF16 else 2.0 ** -25
+    mq, mk, mdo = (float(t.float().abs().max()) for t in (q, k, do))
+    sm = w.sm_scale
+    extra = {
+        "dq": sm * mk * (u * qm[:, 1] + u * qm[:, 0] + a * qm[:, 2]),
+        "dk": sm * mq * (u * km[:, 2] + u * km[:, 0] + a * km[:, 3]),
+        "dv": mdo * (u * km[:, 1] + a * km[:, 3]),
+    }
+    got = {"dq": dq.reshape(-1, D)[torch.from_numpy(qr).to(dev)],
+           "dk": dk.reshape(-1, D)[torch.from_numpy(kr).to(dev)],
+           "dv": dv.reshape(-1, D)[torch.from_numpy(kr).to(dev)]}
+    for gname, ref in (("dq", r_dq), ("dk", r_dk), ("dv", r_dv)):
+        g = got[gname].float().cpu().double().numpy()
+        err = np.abs(g - ref)
+        bound = 1e-2 * np.abs(ref) + 1e-4 * np.abs(ref).max() + extra[gname][:, None]
+        assert np.all(err <= bound), "%s %s: %d of %d elements out of tolerance (max err %g, ref max %g)" % (
+            name, gname, int((err > bound).sum()), err.size, float(err.max()), float(np.abs(ref).max()))
+    if vl is not None and int(vl[0]) == 0:  # keys of an empty batch: exact zeros
+        assert float(dk[0].abs().max()) == 0.0 and float(dv[0].abs().max()) == 0.0
