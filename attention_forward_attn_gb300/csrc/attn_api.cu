@@ -475,13 +475,13 @@ namespace {
 attn_status_t bwd_validate(const void* q, const void* k, const void* v, const void* o,
                            const void* dO, const float* lse, void* dq, void* dk, void* dv, int B,
                            int Hq, int Hkv, int L, int D, float sm_scale, int causal,
-                           const int32_t* valid_len, attn_dtype_t dtype) {
+                           const int32_t* valid_len, attn_dtype_t dtype, bool small_d) {
   if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_DTYPE;
   if (q == nullptr || k == nullptr || v == nullptr || o == nullptr || dO == nullptr ||
       lse == nullptr || dq == nullptr || dk == nullptr || dv == nullptr)
     return ATTN_ERR_NULL;
   if (B < 1 || Hq < 1 || Hkv < 1 || L < 1) return ATTN_ERR_SHAPE;
-  if (D != 64 && D != 128) return ATTN_ERR_HEADDIM;
+  if (D != 64 && D != 128 && !(small_d && (D == 16 || D == 32))) return ATTN_ERR_HEADDIM;
   if (Hq % Hkv != 0) return ATTN_ERR_HEADS;
   if (causal != 0 && causal != 1) return ATTN_ERR_ARG;
   if (!(sm_scale >= 0.f) || isinf(sm_scale)) return ATTN_ERR_SCALE;
@@ -501,7 +501,7 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
                        int L, int D, float sm_scale, int causal, const int32_t* valid_len,
                        attn_dtype_t dtype, attn_stream_t stream) {
   attn_status_t s = bwd_validate(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, L, D, sm_scale,
-                                 causal, valid_len, dtype);
+                                 causal, valid_len, dtype, true);
   if (s != ATTN_OK) return s;
   int dev = 0;
   DeviceState* st = nullptr;
@@ -535,7 +535,7 @@ attn_status_t attn_bwd_simt(const void* q, const void* k, const void* v, const v
                             int Hq, int Hkv, int L, int D, float sm_scale, int causal,
                             const int32_t* valid_len, attn_dtype_t dtype, attn_stream_t stream) {
   attn_status_t s = bwd_validate(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, L, D, sm_scale,
-                                 causal, valid_len, dtype);
+                                 causal, valid_len, dtype, false);
   if (s != ATTN_OK) return s;
   int dev = 0;
   DeviceState* st = nullptr;

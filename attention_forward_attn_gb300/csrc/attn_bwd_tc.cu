@@ -75,6 +75,7 @@ struct BwdTcParams {
   const int32_t* valid_len;
   int* status;
   int B, Hq, Hkv, L, Lp, G, n_t;  // n_t = tiles of 128 rows, Lp = 128 n_t
+  int dg;                         // head dimension in memory: D, or 16 / 32 on the D = 64 kernels
   float scale_log2;               // sm_scale log2(e)
   float sm_scale;
   int causal;
@@ -444,20 +445,26 @@ __device__ void dkv_mma(const BwdTcParams& p, const KvUnit& w, const BBars& br, 
   bdrain(br.bar(I::drain), 0);
 }
 
-// Store one 32-column chunk of an fp32 TMEM row, times `mul`, as 16-bit
-// values (16-byte stores; the thread owns the whole row).
+// Store the first `ncols` (a multiple of 8, at most 32) columns of a
+// 32-column chunk of an fp32 TMEM row, times `mul`, as 16-bit values
+// (16-byte stores; the thread owns the whole row).
 template <bool BF16>
 __device__ __forceinline__ void store_chunk(uint16_t* dst, const uint32_t (&r)[32], float mul,
-                                            bool store) {
+                                            int ncols) {
   uint32_t o16[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i)
     o16[i] = pk2<BF16>(__uint_as_float(r[2 * i]) * mul, __uint_as_float(r[2 * i + 1]) * mul);
-  if (store) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
+  for (int q = 0; q < 4; ++q)
+    if (q * 8 < ncols)
       reinterpret_cast<uint4*>(dst)[q] = make_uint4(o16[4 * q], o16[4 * q + 1], o16[4 * q + 2], o16[4 * q + 3]);
-  }
+}
+
+// Columns of [c_lo, c_lo + part) inside a row of dg columns.
+__device__ __forceinline__ int cols_in(int dg, int c_lo, int part) {
+  const int n = dg - c_lo;
+  return n < 0 ? 0 : (n > part ? part : n);
 }
 
 // Elementwise warpgroups of the dK/dV kernel.  Thread: key row `row` of the
@@ -559,12 +566,11 @@ __device__ void dkv_elementwise(const BwdTcParams& p, const KvUnit& w, const BBa
   const bool is_dk = grp >= kGroups / 2;
   const int c_lo = (grp % (kGroups / 2)) * kPart;
   const int j = w.n * T + row;
-  const bool store = j < p.L;
+  const int nv = j < p.L ? cols_in(p.dg, c_lo, kPart) : 0;  // columns this thread stores
   uint16_t* dst = static_cast<uint16_t*>(is_dk ? p.dk : p.dv) +
-                  ((static_cast<int64_t>(w.b) * p.Hkv + w.hkv) * p.L + j) * D + c_lo;
+                  ((static_cast<int64_t>(w.b) * p.Hkv + w.hkv) * p.L + j) * p.dg + c_lo;
   if (w.steps == 0) {  // no query sees these keys
-    if (store)
-      for (int c = 0; c < kPart / 8; ++c) reinterpret_cast<uint4*>(dst)[c] = make_uint4(0u, 0u, 0u, 0u);
+    for (int c = 0; c < nv / 8; ++c) reinterpret_cast<uint4*>(dst)[c] = make_uint4(0u, 0u, 0u, 0u);
     return;
   }
   if (!__all_sync(kFull, bwait(br, p.status, br.bar(I::accFull), 0, kRoleEpilogue))) return;
@@ -575,7 +581,7 @@ __device__ void dkv_elementwise(const BwdTcParams& p, const KvUnit& w, const BBa
   for (int c0 = 0; c0 < kPart; c0 += 32) {
     uint32_t r[32];
     ptx::tmem_ld32(t_acc + c0, r);
-    store_chunk<BF16>(dst + c0, r, mul, store);
+    store_chunk<BF16>(dst + c0, r, mul, nv - c0);
   }
 }
 
@@ -858,12 +864,11 @@ __device__ void dq_elementwise(const BwdTcParams& p, const QUnit& w, const BBars
   constexpr int kPart = D / kEpi;
   if (!ok || grp >= kEpi) return;
   const int i = w.m * T + row;
-  const bool store = i < p.L;
+  const int nv = i < p.L ? cols_in(p.dg, grp * kPart, kPart) : 0;  // columns this thread stores
   uint16_t* dst = static_cast<uint16_t*>(p.dq) +
-                  ((static_cast<int64_t>(w.b) * p.Hq + w.hq) * p.L + i) * D + grp * kPart;
+                  ((static_cast<int64_t>(w.b) * p.Hq + w.hq) * p.L + i) * p.dg + grp * kPart;
   if (w.steps == 0) {  // no visible key: dQ = 0
-    if (store)
-      for (int c = 0; c < kPart / 8; ++c) reinterpret_cast<uint4*>(dst)[c] = make_uint4(0u, 0u, 0u, 0u);
+    for (int c = 0; c < nv / 8; ++c) reinterpret_cast<uint4*>(dst)[c] = make_uint4(0u, 0u, 0u, 0u);
     return;
   }
   if (!__all_sync(kFull, bwait(br, p.status, br.bar(I::accFull), 0, kRoleEpilogue))) return;
@@ -873,7 +878,7 @@ __device__ void dq_elementwise(const BwdTcParams& p, const QUnit& w, const BBars
   for (int c0 = 0; c0 < kPart; c0 += 32) {
     uint32_t r[32];
     ptx::tmem_ld32(t_acc + c0, r);
-    store_chunk<BF16>(dst + c0, r, p.sm_scale, store);
+    store_chunk<BF16>(dst + c0, r, p.sm_scale, nv - c0);
   }
 }
 
@@ -925,15 +930,28 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   }
 }
 
+// The pre-pass for rows of DR columns in memory.
+template <int DR, bool BF16>
+void launch_prep(const BwdTcParams& p, const void* o, const void* dO, const float* lse,
+                 float* nlse2, float* delta, cudaStream_t stream) {
+  const int64_t rows = static_cast<int64_t>(p.B) * p.Hq * p.Lp;
+  constexpr int kRowsPerBlock = 8 * (32 / (DR / 8));
+  bwd_tc_prep_kernel<DR, BF16><<<static_cast<unsigned>((rows + kRowsPerBlock - 1) / kRowsPerBlock),
+                                 256, 0, stream>>>(o, dO, lse, nlse2, delta, p.L, p.Lp, rows);
+}
+
 template <int D, bool BF16>
 cudaError_t launch_bwd_tc_d(const CUtensorMap (&maps)[4], const BwdTcParams& p, const void* o,
                             const void* dO, const float* lse, float* nlse2, float* delta,
                             cudaStream_t stream) {
   using C = BCfg<D>;
-  const int64_t rows = static_cast<int64_t>(p.B) * p.Hq * p.Lp;
-  constexpr int kRowsPerBlock = 8 * (32 / (D / 8));
-  bwd_tc_prep_kernel<D, BF16><<<static_cast<unsigned>((rows + kRowsPerBlock - 1) / kRowsPerBlock), 256, 0, stream>>>(
-      o, dO, lse, nlse2, delta, p.L, p.Lp, rows);
+  if (p.dg == 16) {
+    launch_prep<16, BF16>(p, o, dO, lse, nlse2, delta, stream);
+  } else if (p.dg == 32) {
+    launch_prep<32, BF16>(p, o, dO, lse, nlse2, delta, stream);
+  } else {
+    launch_prep<D, BF16>(p, o, dO, lse, nlse2, delta, stream);
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(bwd_dkv_tc_kernel<D, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -982,7 +1000,12 @@ cudaError_t launch_bwd_tc(const CUtensorMap (&maps)[4], const void* o, const voi
   p.scale_log2 = sm_scale * kLog2e;
   p.sm_scale = sm_scale;
   p.causal = causal;
-  if (D == 64)
+  p.dg = D;
+  // D = 16 and 32 run the D = 64 kernels: their tensor maps have an inner
+  // extent of D with 64-column boxes, so TMA fills columns D..63 of every Q,
+  // K, V and dO tile with zeros (S and dP unchanged; the extra columns of dQ,
+  // dK and dV are 0) and the epilogues store only the D columns.
+  if (D == 16 || D == 32 || D == 64)
     return bf16 ? launch_bwd_tc_d<64, true>(maps, p, o, dO, lse, nlse2, delta, stream)
                 : launch_bwd_tc_d<64, false>(maps, p, o, dO, lse, nlse2, delta, stream);
   if (D == 128)

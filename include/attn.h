@@ -233,7 +233,8 @@ attn_status_t attn_fwd_simt(const void* q, const void* k, const void* v, void* o
  *   dO         [B, Hq, L, D] output gradient;
  *   lse        [B*Hq, L] fp32, the forward's natural-log LSE (required);
  *   dq         [B, Hq, L, D] out;  dk, dv  [B, Hkv, L, D] out (overwritten).
- *   D          64 or 128.  B*Hq <= 65535.
+ *   D          16, 32, 64 or 128 (16 and 32 run the D = 64 kernels on
+ *              zero-filled columns).  B*Hq <= 65535.
  * Work: a pre-pass (delta and the LSE in base 2, in rows padded to 128) and
  * two tensor-core kernels (tcgen05, fp32 accumulators in tensor memory): dK/dV
  * per 128-key tile with K and V resident and every query tile and query head
@@ -257,7 +258,7 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
  * 64-row query tile; dK/dV per 64-key tile with all query heads of its group;
  * 4 x 4 register blocks over transposed shared-memory tiles.  A cross-check of
  * attn_bwd, and much slower.  Same arguments, preconditions and errors
- * as attn_bwd; workspace B*Hq*L*4 bytes.
+ * as attn_bwd except D: 64 or 128 only; workspace B*Hq*L*4 bytes.
  */
 attn_status_t attn_bwd_simt(const void* q, const void* k, const void* v, const void* o,
                             const void* dO, const float* lse, void* dq, void* dk, void* dv, int B,

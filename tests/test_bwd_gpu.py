@@ -220,3 +220,42 @@ def test_bwd_full_size_sampled_rows(name):
             name, gname, int((err > bound).sum()), err.size, float(err.max()), float(np.abs(ref).max()))
     if vl is not None and int(vl[0]) == 0:  # keys of an empty batch: exact zeros
         assert float(dk[0].abs().max()) == 0.0 and float(dv[0].abs().max()) == 0.0
+
+
+@pytest.mark.parametrize("D, dtype", [(16, wl.BF16), (32, wl.F16), (32, wl.BF16), (16, wl.F16)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_tc_small_head_dims(D, dtype, causal):
+    """D = 16 and 32 (the D = 64 kernels on zero-filled columns)."""
+    run_case(2, 4, 2, 200, D, dtype, causal, [200, 0] if causal else [131, 200], seed=D + 7,
+             impl="tc")
+
+
+@pytest.mark.parametrize("D", [16, 32, 64, 128])
+def test_bwd_tc_writes_only_its_outputs(D):
+    """dQ, dK, dV written through the C ABI into buffers with guard regions on
+    both sides (ragged L, an empty batch): every guard element keeps its
+    sentinel, and the outputs match the binding's."""
+    B, Hq, Hkv, L = 2, 4, 2, 173
+    q, k, v, vl = wl.make_inputs(B, Hq, Hkv, L, D, wl.BF16, seed=D, valid_len=[173, 0])
+    do = torch.randn(B, Hq, L, D, generator=torch.Generator().manual_seed(D + 1)).to(torch.bfloat16)
+    dev = torch.device("cuda")
+    qd, kd, vd, dod, vld = q.to(dev), k.to(dev), v.to(dev), do.to(dev), vl.to(dev)
+    sm = 1.0 / math.sqrt(D)
+    o, lse = attn.attn_fwd(qd, kd, vd, causal=True, sm_scale=sm, valid_len=vld)
+    ref = attn.attn_bwd(qd, kd, vd, o, lse, dod, causal=True, sm_scale=sm, valid_len=vld)
+    guard = 4096
+    bufs = []
+    for t in ref:
+        n = t.numel()
+        bufs.append(torch.full((n + 2 * guard,), 0x7BCD, dtype=torch.int16, device=dev))
+    views = [b[guard:guard + t.numel()] for b, t in zip(bufs, ref)]
+    lib = attn.load()
+    st = lib.attn_bwd(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o.data_ptr(), dod.data_ptr(),
+                      lse.data_ptr(), views[0].data_ptr(), views[1].data_ptr(), views[2].data_ptr(),
+                      B, Hq, Hkv, L, D, sm, 1, vld.data_ptr(), attn.ATTN_BF16, None)
+    assert st == attn.ATTN_OK
+    assert attn.status() == (attn.ATTN_OK, 0)
+    for b, vw, t in zip(bufs, views, ref):
+        hb = b.cpu()
+        assert bool((hb[:guard] == 0x7BCD).all()) and bool((hb[guard + t.numel():] == 0x7BCD).all())
+        assert torch.equal(vw, t.contiguous().view(torch.int16).reshape(-1))

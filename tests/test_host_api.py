@@ -232,7 +232,8 @@ def test_f32_invalid_arguments_rejected_on_host(lib, args, expected):
     (dict(lse=None), "ATTN_ERR_NULL"),
     (dict(dv=None), "ATTN_ERR_NULL"),
     (dict(L=0), "ATTN_ERR_SHAPE"),
-    (dict(D=32), "ATTN_ERR_HEADDIM"),
+    (dict(D=48), "ATTN_ERR_HEADDIM"),
+    (dict(D=256), "ATTN_ERR_HEADDIM"),
     (dict(Hq=6, Hkv=4), "ATTN_ERR_HEADS"),
     (dict(causal=3), "ATTN_ERR_ARG"),
     (dict(sm_scale=-2.0), "ATTN_ERR_SCALE"),
@@ -240,6 +241,17 @@ def test_f32_invalid_arguments_rejected_on_host(lib, args, expected):
 ])
 @pytest.mark.parametrize("entry", ["attn_bwd", "attn_bwd_simt"])
 def test_bwd_invalid_arguments_rejected_on_host(lib, args, expected, entry):
+    _bwd_call(lib, entry, args, expected)
+
+
+@pytest.mark.parametrize("D", [16, 32])
+def test_bwd_simt_rejects_small_head_dims(lib, D):
+    """attn_bwd takes D = 16 and 32 (the D = 64 kernels on zero-filled
+    columns); the SIMT cross-check does not."""
+    _bwd_call(lib, "attn_bwd_simt", dict(D=D), "ATTN_ERR_HEADDIM")
+
+
+def _bwd_call(lib, entry, args, expected):
     a = dict(q=A16, k=A16, v=A16, o=A16, do=A16, lse=A16, dq=A16, dk=A16, dv=A16, B=1, Hq=4,
              Hkv=2, L=64, D=64, sm_scale=0.125, causal=1, valid_len=None, dtype=attn.ATTN_BF16,
              stream=None)
