@@ -168,6 +168,16 @@ __device__ __forceinline__ void commit(uint32_t bar) {
 
 __device__ __forceinline__ uint64_t dadd(uint64_t desc, uint32_t bytes) { return desc + (bytes >> 4); }
 
+// Untiled bulk copy global -> shared of `bytes` bytes (both addresses 16-byte
+// aligned, size a multiple of 16), completion counted on `bar` in bytes.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
 // d = A B^T over D with both operands K-major 128-row tiles (128 x 128 fp32
 // result): S^T = K Q^T, dP^T = V dO^T, S = Q K^T, dP = dO V^T.
 template <int D, bool BF16>
@@ -359,8 +369,8 @@ __device__ void dkv_producer(const BwdTcParams& p, const KvUnit& w, const BBars&
                             pol_keep);
     }
     const int64_t row = (static_cast<int64_t>(w.b) * p.Hq + hq) * p.Lp + static_cast<int64_t>(mi) * T;
-    ptx::bulk_load(st + 2 * C::kTile, p.nlse2 + row, T * 4, full);
-    ptx::bulk_load(st + 2 * C::kTile + T * 4, p.delta + row, T * 4, full);
+    bulk_load(st + 2 * C::kTile, p.nlse2 + row, T * 4, full);
+    bulk_load(st + 2 * C::kTile + T * 4, p.delta + row, T * 4, full);
   }
   // never leave with a copy in flight: the last load of every stage
   bdrain(br.bar(I::kvFull), 0);
