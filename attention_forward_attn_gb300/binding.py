@@ -100,6 +100,9 @@ def load():
             lib.attn_bwd.restype = i
             lib.attn_bwd_simt.argtypes = lib.attn_bwd.argtypes
             lib.attn_bwd_simt.restype = i
+            lib.attn_bwd_strided.argtypes = [p, sp, p, sp, p, sp, p, sp, p, sp, p, p, sp, p, sp, p,
+                                             sp, i, i, i, i, i, ctypes.c_float, i, p, i, p]
+            lib.attn_bwd_strided.restype = i
             lib.attn_fwd_f32.argtypes = [p, p, p, p, p, i, i, i, i, ctypes.c_float, i, p, i, p]
             lib.attn_fwd_f32.restype = i
             lib.attn_host_plan.argtypes = [i, i, i, i, i, i, ctypes.POINTER(Chunk), i,
@@ -436,32 +439,56 @@ def attn_fwd_f32(q, k, v, *, kernel="tiled_rowmax", causal=False, sm_scale=None,
 
 
 def attn_bwd(q, k, v, o, lse, do, *, causal=False, sm_scale=None, valid_len=None, stream=None,
-             impl="tc"):
-    """Gradients (dq, dk, dv) of attn_fwd for the output gradient ``do``,
-    through attn_bwd (impl="tc", tensor cores) or attn_bwd_simt (impl="simt",
-    fp32 SIMT).  q, o, do: [B, Hq, L, D]; k, v: [B, Hkv, L, D] (fp16 or bf16,
-    contiguous CUDA tensors); lse: the forward's [B*Hq, L] fp32 LSE."""
+             impl="tc", dq=None, dk=None, dv=None):
+    """Gradients (dq, dk, dv) of attn_fwd for the output gradient ``do``.
+
+    impl="tc": attn_bwd_strided (tensor cores).  q, o, do: [B, Hq, L, D]; k, v:
+    [B, Hkv, L, D] -- fp16 or bf16 CUDA views whose last dimension is
+    contiguous and whose other strides are multiples of 8 elements (e.g.
+    ``x.transpose(1, 2)`` of [B, L, H, D] tensors); dq, dk, dv: optional
+    output views of the same shapes (default: new contiguous tensors).
+    impl="simt": attn_bwd_simt (fp32 SIMT), contiguous tensors only.
+    lse: the forward's [B*Hq, L] fp32 LSE."""
     import torch
     if impl not in ("tc", "simt"):
         raise ValueError("impl must be 'tc' or 'simt'")
-    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("do", do)):
-        if not t.is_cuda or not t.is_contiguous():
-            raise ValueError("%s must be a contiguous CUDA tensor" % name)
+    named = (("q", q), ("k", k), ("v", v), ("o", o), ("do", do))
+    for name, t in named:
+        if not t.is_cuda or t.dim() != 4 or (t.shape[3] > 1 and t.stride(3) != 1):
+            raise ValueError("%s must be a 4-D CUDA tensor with a contiguous last dimension" % name)
+        if impl == "simt" and not t.is_contiguous():
+            raise ValueError("impl='simt' takes contiguous tensors (%s is not)" % name)
     B, Hq, L, D = q.shape
     Hkv = k.shape[1]
     if sm_scale is None:
         sm_scale = 1.0 / float(D) ** 0.5
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dq = torch.empty_like(q, memory_format=torch.contiguous_format) if dq is None else dq
+    dk = torch.empty_like(k, memory_format=torch.contiguous_format) if dk is None else dk
+    dv = torch.empty_like(v, memory_format=torch.contiguous_format) if dv is None else dv
+    for name, t, ref in (("dq", dq, q), ("dk", dk, k), ("dv", dv, v)):
+        if t.shape != ref.shape or t.dtype != ref.dtype or not t.is_cuda:
+            raise ValueError("%s must be a CUDA tensor shaped and typed like %s" % (name, name[1:]))
+        if impl == "simt" and not t.is_contiguous():
+            raise ValueError("impl='simt' takes contiguous tensors (%s is not)" % name)
     vl_ptr = None
     if valid_len is not None:
         vl_ptr = valid_len.data_ptr()
     lse = lse.contiguous()
-    name = "attn_bwd" if impl == "tc" else "attn_bwd_simt"
-    st = int(getattr(load(), name)(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                                   do.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
-                                   dv.data_ptr(), B, Hq, Hkv, L, D, float(sm_scale),
-                                   int(bool(causal)), vl_ptr, _dtype_code(q),
-                                   _stream_handle(stream)))
+    if impl == "tc":
+        st3 = lambda t: _strides_arg((t.stride(0), t.stride(1), t.stride(2)))
+        name = "attn_bwd_strided"
+        st = int(load().attn_bwd_strided(
+            q.data_ptr(), st3(q), k.data_ptr(), st3(k), v.data_ptr(), st3(v), o.data_ptr(), st3(o),
+            do.data_ptr(), st3(do), lse.data_ptr(), dq.data_ptr(), st3(dq), dk.data_ptr(), st3(dk),
+            dv.data_ptr(), st3(dv), B, Hq, Hkv, L, D, float(sm_scale), int(bool(causal)), vl_ptr,
+            _dtype_code(q), _stream_handle(stream)))
+    else:
+        name = "attn_bwd_simt"
+        st = int(load().attn_bwd_simt(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                      do.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                                      dv.data_ptr(), B, Hq, Hkv, L, D, float(sm_scale),
+                                      int(bool(causal)), vl_ptr, _dtype_code(q),
+                                      _stream_handle(stream)))
     if st != ATTN_OK:
         raise AttnError(st, name)
     return dq, dk, dv

@@ -496,24 +496,41 @@ attn_status_t bwd_validate(const void* q, const void* k, const void* v, const vo
 
 }  // namespace
 
-attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
-                       const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv,
-                       int L, int D, float sm_scale, int causal, const int32_t* valid_len,
-                       attn_dtype_t dtype, attn_stream_t stream) {
+attn_status_t attn_bwd_strided(const void* q, const attn_strides_t* q_strides, const void* k,
+                               const attn_strides_t* k_strides, const void* v,
+                               const attn_strides_t* v_strides, const void* o,
+                               const attn_strides_t* o_strides, const void* dO,
+                               const attn_strides_t* do_strides, const float* lse, void* dq,
+                               const attn_strides_t* dq_strides, void* dk,
+                               const attn_strides_t* dk_strides, void* dv,
+                               const attn_strides_t* dv_strides, int B, int Hq, int Hkv, int L,
+                               int D, float sm_scale, int causal, const int32_t* valid_len,
+                               attn_dtype_t dtype, attn_stream_t stream) {
   attn_status_t s = bwd_validate(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, L, D, sm_scale,
                                  causal, valid_len, dtype, true);
   if (s != ATTN_OK) return s;
+  attn::Strides sq, sk, sv, so, sdo, sdq, sdk, sdv;
+  if ((s = strides_of(q_strides, B, Hq, L, D, &sq)) != ATTN_OK ||
+      (s = strides_of(k_strides, B, Hkv, L, D, &sk)) != ATTN_OK ||
+      (s = strides_of(v_strides, B, Hkv, L, D, &sv)) != ATTN_OK ||
+      (s = strides_of(o_strides, B, Hq, L, D, &so)) != ATTN_OK ||
+      (s = strides_of(do_strides, B, Hq, L, D, &sdo)) != ATTN_OK ||
+      (s = strides_of(dq_strides, B, Hq, L, D, &sdq)) != ATTN_OK ||
+      (s = strides_of(dk_strides, B, Hkv, L, D, &sdk)) != ATTN_OK ||
+      (s = strides_of(dv_strides, B, Hkv, L, D, &sdv)) != ATTN_OK)
+    return s;
+  if (!no_self_overlap(sdq, B, Hq, L, D) || !no_self_overlap(sdk, B, Hkv, L, D) ||
+      !no_self_overlap(sdv, B, Hkv, L, D))
+    return ATTN_ERR_STRIDE;
   int dev = 0;
   DeviceState* st = nullptr;
   if ((s = device_state(&dev, &st)) != ATTN_OK) return s;
   const bool bf16 = dtype == ATTN_BF16;
-  const attn::Strides sq = attn::contiguous_strides(Hq, L, D);
-  const attn::Strides skv = attn::contiguous_strides(Hkv, L, D);
   CUtensorMap maps[4];
   if ((s = encode_map(&maps[0], q, B, Hq, L, D, sq, 128, bf16)) != ATTN_OK ||
-      (s = encode_map(&maps[1], k, B, Hkv, L, D, skv, 128, bf16)) != ATTN_OK ||
-      (s = encode_map(&maps[2], v, B, Hkv, L, D, skv, 128, bf16)) != ATTN_OK ||
-      (s = encode_map(&maps[3], dO, B, Hq, L, D, sq, 128, bf16)) != ATTN_OK)
+      (s = encode_map(&maps[1], k, B, Hkv, L, D, sk, 128, bf16)) != ATTN_OK ||
+      (s = encode_map(&maps[2], v, B, Hkv, L, D, sv, 128, bf16)) != ATTN_OK ||
+      (s = encode_map(&maps[3], dO, B, Hq, L, D, sdo, 128, bf16)) != ATTN_OK)
     return s;
   cudaMemPool_t pool = nullptr;
   if ((s = workspace_pool(dev, st, &pool)) != ATTN_OK) return s;
@@ -522,12 +539,21 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
   cudaError_t e = cudaMallocFromPoolAsync(
       &ws, static_cast<size_t>(attn::bwd_tc_workspace_bytes(B, Hq, L)), pool, cs);
   if (e != cudaSuccess) return cuda_fail(e);
-  e = attn::launch_bwd_tc(maps, o, dO, lse, dq, dk, dv, ws, B, Hq, Hkv, L, D, sm_scale, causal,
-                          valid_len, bf16, st->status, cs);
+  e = attn::launch_bwd_tc(maps, o, so, dO, sdo, lse, dq, sdq, dk, sdk, dv, sdv, ws, B, Hq, Hkv, L,
+                          D, sm_scale, causal, valid_len, bf16, st->status, cs);
   const cudaError_t ef = cudaFreeAsync(ws, cs);
   if (e == cudaSuccess) e = ef;
   if (e != cudaSuccess) return cuda_fail(e);
   return ATTN_OK;
+}
+
+attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                       const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv,
+                       int L, int D, float sm_scale, int causal, const int32_t* valid_len,
+                       attn_dtype_t dtype, attn_stream_t stream) {
+  return attn_bwd_strided(q, nullptr, k, nullptr, v, nullptr, o, nullptr, dO, nullptr, lse, dq,
+                          nullptr, dk, nullptr, dv, nullptr, B, Hq, Hkv, L, D, sm_scale, causal,
+                          valid_len, dtype, stream);
 }
 
 attn_status_t attn_bwd_simt(const void* q, const void* k, const void* v, const void* o,

@@ -76,6 +76,7 @@ struct BwdTcParams {
   int* status;
   int B, Hq, Hkv, L, Lp, G, n_t;  // n_t = tiles of 128 rows, Lp = 128 n_t
   int dg;                         // head dimension in memory: D, or 16 / 32 on the D = 64 kernels
+  Strides sdq, sdk, sdv;          // element strides (batch, head, row) of the outputs
   float scale_log2;               // sm_scale log2(e)
   float sm_scale;
   int causal;
@@ -252,8 +253,9 @@ template <int D, bool BF16>
 __global__ void __launch_bounds__(256) bwd_tc_prep_kernel(const void* __restrict__ o,
                                                           const void* __restrict__ dO,
                                                           const float* __restrict__ lse,
-                                                          float* nlse2, float* delta, int L, int Lp,
-                                                          int64_t rows) {
+                                                          float* nlse2, float* delta, int Hq, int L,
+                                                          int Lp, int64_t rows, Strides so,
+                                                          Strides sdo) {
   constexpr int LPR = D / 8;     // lanes per row
   constexpr int RPW = 32 / LPR;  // rows per warp
   const int lane = threadIdx.x & 31;
@@ -264,9 +266,11 @@ __global__ void __launch_bounds__(256) bwd_tc_prep_kernel(const void* __restrict
   const bool live = r < rows && i < L;
   float s = 0.f;
   if (live) {
-    const int64_t e = (bh * L + i) * D + sub * 8;
-    const uint4 a = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(o) + e);
-    const uint4 g = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(dO) + e);
+    const int64_t b = bh / Hq, h = bh - b * Hq;
+    const int64_t eo = b * so.b + h * so.h + i * so.l + sub * 8;
+    const int64_t eg = b * sdo.b + h * sdo.h + i * sdo.l + sub * 8;
+    const uint4 a = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(o) + eo);
+    const uint4 g = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(dO) + eg);
     const uint32_t av[4] = {a.x, a.y, a.z, a.w}, gv[4] = {g.x, g.y, g.z, g.w};
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -577,8 +581,9 @@ __device__ void dkv_elementwise(const BwdTcParams& p, const KvUnit& w, const BBa
   const int c_lo = (grp % (kGroups / 2)) * kPart;
   const int j = w.n * T + row;
   const int nv = j < p.L ? cols_in(p.dg, c_lo, kPart) : 0;  // columns this thread stores
-  uint16_t* dst = static_cast<uint16_t*>(is_dk ? p.dk : p.dv) +
-                  ((static_cast<int64_t>(w.b) * p.Hkv + w.hkv) * p.L + j) * p.dg + c_lo;
+  const Strides& so = is_dk ? p.sdk : p.sdv;
+  uint16_t* dst = static_cast<uint16_t*>(is_dk ? p.dk : p.dv) + w.b * so.b + w.hkv * so.h +
+                  static_cast<int64_t>(j) * so.l + c_lo;
   if (w.steps == 0) {  // no query sees these keys
     for (int c = 0; c < nv / 8; ++c) reinterpret_cast<uint4*>(dst)[c] = make_uint4(0u, 0u, 0u, 0u);
     return;
@@ -875,8 +880,8 @@ __device__ void dq_elementwise(const BwdTcParams& p, const QUnit& w, const BBars
   if (!ok || grp >= kEpi) return;
   const int i = w.m * T + row;
   const int nv = i < p.L ? cols_in(p.dg, grp * kPart, kPart) : 0;  // columns this thread stores
-  uint16_t* dst = static_cast<uint16_t*>(p.dq) +
-                  ((static_cast<int64_t>(w.b) * p.Hq + w.hq) * p.L + i) * p.dg + grp * kPart;
+  uint16_t* dst = static_cast<uint16_t*>(p.dq) + w.b * p.sdq.b + w.hq * p.sdq.h +
+                  static_cast<int64_t>(i) * p.sdq.l + grp * kPart;
   if (w.steps == 0) {  // no visible key: dQ = 0
     for (int c = 0; c < nv / 8; ++c) reinterpret_cast<uint4*>(dst)[c] = make_uint4(0u, 0u, 0u, 0u);
     return;
@@ -942,25 +947,27 @@ __global__ void __launch_bounds__(kThreadsB, 1)
 
 // The pre-pass for rows of DR columns in memory.
 template <int DR, bool BF16>
-void launch_prep(const BwdTcParams& p, const void* o, const void* dO, const float* lse,
-                 float* nlse2, float* delta, cudaStream_t stream) {
+void launch_prep(const BwdTcParams& p, const void* o, const Strides& so, const void* dO,
+                 const Strides& sdo, const float* lse, float* nlse2, float* delta,
+                 cudaStream_t stream) {
   const int64_t rows = static_cast<int64_t>(p.B) * p.Hq * p.Lp;
   constexpr int kRowsPerBlock = 8 * (32 / (DR / 8));
   bwd_tc_prep_kernel<DR, BF16><<<static_cast<unsigned>((rows + kRowsPerBlock - 1) / kRowsPerBlock),
-                                 256, 0, stream>>>(o, dO, lse, nlse2, delta, p.L, p.Lp, rows);
+                                 256, 0, stream>>>(o, dO, lse, nlse2, delta, p.Hq, p.L, p.Lp, rows,
+                                                   so, sdo);
 }
 
 template <int D, bool BF16>
 cudaError_t launch_bwd_tc_d(const CUtensorMap (&maps)[4], const BwdTcParams& p, const void* o,
-                            const void* dO, const float* lse, float* nlse2, float* delta,
-                            cudaStream_t stream) {
+                            const Strides& so, const void* dO, const Strides& sdo,
+                            const float* lse, float* nlse2, float* delta, cudaStream_t stream) {
   using C = BCfg<D>;
   if (p.dg == 16) {
-    launch_prep<16, BF16>(p, o, dO, lse, nlse2, delta, stream);
+    launch_prep<16, BF16>(p, o, so, dO, sdo, lse, nlse2, delta, stream);
   } else if (p.dg == 32) {
-    launch_prep<32, BF16>(p, o, dO, lse, nlse2, delta, stream);
+    launch_prep<32, BF16>(p, o, so, dO, sdo, lse, nlse2, delta, stream);
   } else {
-    launch_prep<D, BF16>(p, o, dO, lse, nlse2, delta, stream);
+    launch_prep<D, BF16>(p, o, so, dO, sdo, lse, nlse2, delta, stream);
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -986,11 +993,16 @@ int64_t bwd_tc_workspace_bytes(int B, int Hq, int L) {
   return 2 * static_cast<int64_t>(B) * Hq * lp * 4;
 }
 
-cudaError_t launch_bwd_tc(const CUtensorMap (&maps)[4], const void* o, const void* dO,
-                          const float* lse, void* dq, void* dk, void* dv, void* workspace, int B,
-                          int Hq, int Hkv, int L, int D, float sm_scale, int causal,
-                          const int32_t* valid_len, bool bf16, int* status, cudaStream_t stream) {
+cudaError_t launch_bwd_tc(const CUtensorMap (&maps)[4], const void* o, const Strides& so,
+                          const void* dO, const Strides& sdo, const float* lse, void* dq,
+                          const Strides& sdq, void* dk, const Strides& sdk, void* dv,
+                          const Strides& sdv, void* workspace, int B, int Hq, int Hkv, int L, int D,
+                          float sm_scale, int causal, const int32_t* valid_len, bool bf16,
+                          int* status, cudaStream_t stream) {
   BwdTcParams p;
+  p.sdq = sdq;
+  p.sdk = sdk;
+  p.sdv = sdv;
   p.n_t = (L + T - 1) / T;
   p.Lp = p.n_t * T;
   float* nlse2 = static_cast<float*>(workspace);
@@ -1016,11 +1028,11 @@ cudaError_t launch_bwd_tc(const CUtensorMap (&maps)[4], const void* o, const voi
   // K, V and dO tile with zeros (S and dP unchanged; the extra columns of dQ,
   // dK and dV are 0) and the epilogues store only the D columns.
   if (D == 16 || D == 32 || D == 64)
-    return bf16 ? launch_bwd_tc_d<64, true>(maps, p, o, dO, lse, nlse2, delta, stream)
-                : launch_bwd_tc_d<64, false>(maps, p, o, dO, lse, nlse2, delta, stream);
+    return bf16 ? launch_bwd_tc_d<64, true>(maps, p, o, so, dO, sdo, lse, nlse2, delta, stream)
+                : launch_bwd_tc_d<64, false>(maps, p, o, so, dO, sdo, lse, nlse2, delta, stream);
   if (D == 128)
-    return bf16 ? launch_bwd_tc_d<128, true>(maps, p, o, dO, lse, nlse2, delta, stream)
-                : launch_bwd_tc_d<128, false>(maps, p, o, dO, lse, nlse2, delta, stream);
+    return bf16 ? launch_bwd_tc_d<128, true>(maps, p, o, so, dO, sdo, lse, nlse2, delta, stream)
+                : launch_bwd_tc_d<128, false>(maps, p, o, so, dO, sdo, lse, nlse2, delta, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -109,12 +109,15 @@ cudaError_t launch_bwd(const void* q, const void* k, const void* v, const void* 
 // Tensor-core backward (attn_bwd_tc.cu): bytes of its workspace (-LSE log2(e)
 // and delta, fp32 [B*Hq, L rounded up to 128] each) and its launch (pre-pass,
 // dK/dV and dQ kernels on `stream`).  maps: Q, K, V, dO as encode_map makes
-// them with 128-row boxes.  D 64 or 128.
+// them with 128-row boxes.  so, sdo: element strides of O and dO (read by the
+// pre-pass); sdq, sdk, sdv: of the outputs.  D 16, 32, 64 or 128.
 int64_t bwd_tc_workspace_bytes(int B, int Hq, int L);
-cudaError_t launch_bwd_tc(const CUtensorMap (&maps)[4], const void* o, const void* dO,
-                          const float* lse, void* dq, void* dk, void* dv, void* workspace, int B,
-                          int Hq, int Hkv, int L, int D, float sm_scale, int causal,
-                          const int32_t* valid_len, bool bf16, int* status, cudaStream_t stream);
+cudaError_t launch_bwd_tc(const CUtensorMap (&maps)[4], const void* o, const Strides& so,
+                          const void* dO, const Strides& sdo, const float* lse, void* dq,
+                          const Strides& sdq, void* dk, const Strides& sdk, void* dv,
+                          const Strides& sdv, void* workspace, int B, int Hq, int Hkv, int L, int D,
+                          float sm_scale, int causal, const int32_t* valid_len, bool bf16,
+                          int* status, cudaStream_t stream);
 
 // SIMT cross-check forward.
 cudaError_t launch_simt(const Problem& p);

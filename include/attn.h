@@ -50,7 +50,7 @@ typedef enum {
   ATTN_ERR_VALID_LEN = 11, /* device side: a valid_len value was outside [0, L] and was clamped */
   ATTN_ERR_ARG = 12,       /* another invalid argument (causal not 0/1, NULL out-pointer, ...) */
   ATTN_ERR_SCRATCH = 13,   /* attn_fwd_noalloc: the call needs more scratch than its static array holds */
-  ATTN_ERR_STRIDE = 14     /* attn_fwd_strided: a stride is invalid, or O's elements overlap */
+  ATTN_ERR_STRIDE = 14     /* a stride is invalid, or an output's elements overlap (strided entry points) */
 } attn_status_t;
 
 /*
@@ -251,6 +251,25 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
                        const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv,
                        int L, int D, float sm_scale, int causal, const int32_t* valid_len,
                        attn_dtype_t dtype, attn_stream_t stream);
+
+/*
+ * attn_bwd_strided -- attn_bwd on strided operands: each of q, k, v, o, dO,
+ * dq, dk and dv takes an attn_strides_t (NULL: contiguous [B, H, L, D]) with
+ * the rules of attn_fwd_strided (positive multiples of 8 elements below
+ * 2^39; the stride of an extent-1 dimension is ignored; rows of D elements
+ * contiguous).  dq, dk and dv must not overlap themselves (ATTN_ERR_STRIDE).
+ * Everything else as attn_bwd, which is this call with every stride NULL.
+ */
+attn_status_t attn_bwd_strided(const void* q, const attn_strides_t* q_strides, const void* k,
+                               const attn_strides_t* k_strides, const void* v,
+                               const attn_strides_t* v_strides, const void* o,
+                               const attn_strides_t* o_strides, const void* dO,
+                               const attn_strides_t* do_strides, const float* lse, void* dq,
+                               const attn_strides_t* dq_strides, void* dk,
+                               const attn_strides_t* dk_strides, void* dv,
+                               const attn_strides_t* dv_strides, int B, int Hq, int Hkv, int L,
+                               int D, float sm_scale, int causal, const int32_t* valid_len,
+                               attn_dtype_t dtype, attn_stream_t stream);
 
 /*
  * attn_bwd_simt -- the same gradients computed by SIMT kernels with fp32

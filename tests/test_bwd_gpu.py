@@ -259,3 +259,40 @@ def test_bwd_tc_writes_only_its_outputs(D):
         hb = b.cpu()
         assert bool((hb[:guard] == 0x7BCD).all()) and bool((hb[guard + t.numel():] == 0x7BCD).all())
         assert torch.equal(vw, t.contiguous().view(torch.int16).reshape(-1))
+
+
+@pytest.mark.parametrize("D", [32, 64, 128])
+@pytest.mark.parametrize("layout", ["blhd", "packed_qkv"])
+def test_bwd_strided_matches_contiguous(D, layout):
+    """attn_bwd on strided views -- [B, L, H, D] tensors, or Q, K, V as slices
+    of one packed [B, L, Hq + 2 Hkv, D] tensor -- with dQ, dK, dV written
+    into [B, L, H, D + 8] buffers (padded rows): the gradients are identical
+    bit for bit to the contiguous call's, and the padding keeps its
+    sentinel."""
+    B, Hq, Hkv, L = 2, 8, 2, 300
+    q, k, v, vl = wl.make_inputs(B, Hq, Hkv, L, D, wl.BF16, seed=D + 3, valid_len=[300, 111])
+    do = torch.randn(B, Hq, L, D, generator=torch.Generator().manual_seed(D + 4)).to(torch.bfloat16)
+    dev = torch.device("cuda")
+    qd, kd, vd, dod, vld = q.to(dev), k.to(dev), v.to(dev), do.to(dev), vl.to(dev)
+    sm = 1.0 / math.sqrt(D)
+    o, lse = attn.attn_fwd(qd, kd, vd, causal=True, sm_scale=sm, valid_len=vld)
+    ref = attn.attn_bwd(qd, kd, vd, o, lse, dod, causal=True, sm_scale=sm, valid_len=vld)
+    blhd = lambda t: t.transpose(1, 2).contiguous().transpose(1, 2)
+    if layout == "blhd":
+        qs, ks, vs = blhd(qd), blhd(kd), blhd(vd)
+    else:
+        packed = torch.cat([qd.transpose(1, 2), kd.transpose(1, 2), vd.transpose(1, 2)], dim=2).contiguous()
+        qs = packed[:, :, :Hq].transpose(1, 2)
+        ks = packed[:, :, Hq:Hq + Hkv].transpose(1, 2)
+        vs = packed[:, :, Hq + Hkv:].transpose(1, 2)
+    os_, dos = blhd(o), blhd(dod)
+    sentinel = -12345.0
+    bufs = [torch.full((B, L, H, D + 8), sentinel, dtype=torch.bfloat16, device=dev)
+            for H in (Hq, Hkv, Hkv)]
+    outs = [b[..., :D].transpose(1, 2) for b in bufs]
+    got = attn.attn_bwd(qs, ks, vs, os_, lse, dos, causal=True, sm_scale=sm, valid_len=vld,
+                        dq=outs[0], dk=outs[1], dv=outs[2])
+    assert attn.status() == (attn.ATTN_OK, 0)
+    for g, r, b in zip(got, ref, bufs):
+        assert torch.equal(g.contiguous().view(torch.int16), r.contiguous().view(torch.int16))
+        assert bool((b[..., D:] == sentinel).all())

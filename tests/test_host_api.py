@@ -260,3 +260,23 @@ def _bwd_call(lib, entry, args, expected):
                              a["dv"], a["B"], a["Hq"], a["Hkv"], a["L"], a["D"], a["sm_scale"],
                              a["causal"], a["valid_len"], a["dtype"], a["stream"])
     assert binding.STATUS_NAMES[st] == expected
+
+
+@pytest.mark.parametrize("which, strides, expected", [
+    ("q", (4 * 64 * 64, 64 * 64, 63), "ATTN_ERR_STRIDE"),       # seq stride not a multiple of 8
+    ("dq", (4 * 64 * 64, 64 * 64, 32), "ATTN_ERR_STRIDE"),      # rows of dq overlap (32 < D)
+    ("dk", (2 * 64 * 64, 0, 64), "ATTN_ERR_STRIDE"),            # head stride 0 with Hkv = 2
+    ("do", (4 * 64 * 64, 64 * 64, 1 << 40), "ATTN_ERR_STRIDE"),  # stride too large
+    ("dv", (2 * 64 * 64, 64, 60), "ATTN_ERR_STRIDE"),           # rows of dv overlap
+])
+def test_bwd_strided_stride_validation(lib, which, strides, expected):
+    """attn_bwd_strided rejects invalid strides on the host, before any
+    device work (the fake addresses are never dereferenced: every case here
+    fails validation)."""
+    names = ["q", "k", "v", "o", "do", "dq", "dk", "dv"]
+    st = {n: None for n in names}
+    st[which] = ctypes.byref(binding.Strides(*strides))
+    rc = lib.attn_bwd_strided(A16, st["q"], A16, st["k"], A16, st["v"], A16, st["o"], A16, st["do"],
+                              A16, A16, st["dq"], A16, st["dk"], A16, st["dv"], 1, 4, 2, 64, 64,
+                              0.125, 1, None, attn.ATTN_BF16, None)
+    assert binding.STATUS_NAMES[rc] == expected
