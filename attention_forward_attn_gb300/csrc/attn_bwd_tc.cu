@@ -16,11 +16,13 @@
 //   * dK/dV kernel, one CTA per (128-key tile, b, h_kv), K and V resident in
 //     shared memory.  Every (query head of the group, 128-row query tile) that
 //     sees the keys streams through a ring of Q, dO, LSE and delta stages.
-//     Per step: S^T = K Q^T and dP^T = V dO^T (keys in TMEM lanes), then two
-//     elementwise warpgroups (each 64 query columns of every key row) write
-//     P^T over the S^T columns and dS^T over the dP^T columns as 16-bit
-//     pairs, and dV += P^T dO, dK += dS^T Q read them from TMEM (dO and Q as
-//     MN-major operands).  TMEM: S^T, dP^T, dV, dK (512 columns at D = 128);
+//     Per step: S^T = K Q^T and dP^T = V dO^T (keys in TMEM lanes, two
+//     128-column regions that swap roles every step), then two elementwise
+//     warpgroups (each 64 query columns of every key row) write P^T and dS^T
+//     as 16-bit pairs into the S^T region, and dV += P^T dO, dK += dS^T Q
+//     read them from TMEM (dO and Q as MN-major operands); the next S^T goes
+//     into the dP^T region as soon as dP^T has been read.  TMEM: the two
+//     regions, dV, dK (512 columns at D = 128);
 //   * dQ kernel, one CTA per (128-row query tile, b, h_q), Q and dO resident,
 //     K and V streaming: S = Q K^T, dP = dO V^T, dS written to its own TMEM
 //     columns (two buffers), dQ += dS K (K as MN-major operand).  TMEM: S,
@@ -109,8 +111,10 @@ struct BCfg {
   static constexpr int qSmem = qOffBar + kBarBytes + 1024;
   static_assert(kvSmem <= 232448 && qSmem <= 232448, "shared-memory budget");
   // TMEM columns
-  static constexpr uint32_t kColS = 0;      // S^T / S (fp32); P^T written over it (dK/dV kernel)
-  static constexpr uint32_t kColDP = T;     // dP^T / dP (fp32); dS^T written over it (dK/dV kernel)
+  // dK/dV kernel: regions [0, 128) and [128, 256) hold S^T and dP^T of a
+  // step, swapping every step (region_x / region_y); dQ kernel: S and dP
+  static constexpr uint32_t kColS = 0;      // S (fp32, dQ kernel)
+  static constexpr uint32_t kColDP = T;     // dP (fp32, dQ kernel)
   static constexpr uint32_t kColAcc0 = 2 * T;      // dV (dK/dV kernel) / dQ (dQ kernel)
   static constexpr uint32_t kColAcc1 = 2 * T + D;  // dK (dK/dV kernel) / dS (dQ kernel, 2 x 64 columns)
   static constexpr uint32_t kTmemCols = 512;
@@ -309,10 +313,10 @@ struct KvIdx {
   static constexpr int inEmpty = 1 + NS;      // [NS] the step's last MMA (dK) completed
   static constexpr int sFull = 1 + 2 * NS;    // S^T in TMEM
   static constexpr int dpFull = sFull + 1;    // dP^T in TMEM
-  static constexpr int pReady = sFull + 2;    // P^T written (256 arrivals)
-  static constexpr int dsReady = sFull + 3;   // dS^T written (256 arrivals)
-  static constexpr int dvDone = sFull + 4;    // dV MMA of the step completed (S^T columns free)
-  static constexpr int dkDone = sFull + 5;    // dK MMA completed (dP^T columns free)
+  static constexpr int pReady = sFull + 2;    // P^T written (elementwise arrivals)
+  static constexpr int dsReady = sFull + 3;   // dS^T written (elementwise arrivals)
+  static constexpr int dpFree = sFull + 4;    // dP^T read (elementwise arrivals)
+  static constexpr int dkDone = sFull + 5;    // dV and dK MMAs of the step completed
   static constexpr int accFull = sFull + 6;   // every MMA of the unit completed
   static constexpr int drain = sFull + 7;
   static constexpr int n = sFull + 8;
@@ -381,13 +385,19 @@ __device__ void dkv_producer(const BwdTcParams& p, const KvUnit& w, const BBars&
   for (int k = (t > NS ? t - NS : 0); k < t; ++k) bdrain(br.bar(I::inFull + k % NS), (k / NS) & 1);
 }
 
+// TMEM regions: step t's S^T goes to X_t and its dP^T to Y_t, with X and Y
+// swapping every step (X_t = A for even t, B for odd; A = columns [0, 128),
+// B = [128, 256)).  P^T(t) and dS^T(t) are both written into X_t (each
+// elementwise warpgroup packs them into the first and second 32 columns of
+// its 64-column block), so Y_t is free as soon as dP^T(t) has been read.
 // Issue order: S^T(0), dP^T(0), then per step t
 //   dV(t) once P^T(t) is written;
-//   S^T(t+1) once dV(t) has completed (it read P^T(t) from the S^T columns);
+//   S^T(t+1) into Y_t once dP^T(t) has been read (during the dS^T(t) math);
 //   dK(t) once dS^T(t) is written;
-//   dP^T(t+1) once dK(t) has completed (it read dS^T(t) from the dP^T columns);
-// so S^T(t+1) runs on the tensor core while the elementwise warps compute
-// dS^T(t), and dP^T(t+1) while they compute P^T(t+1).
+//   dP^T(t+1) into X_t once dV(t) and dK(t), which read X_t, have completed.
+__device__ __forceinline__ uint32_t region_x(int t) { return (t & 1) ? 128u : 0u; }
+__device__ __forceinline__ uint32_t region_y(int t) { return (t & 1) ? 0u : 128u; }
+
 template <int D, bool BF16>
 __device__ void dkv_mma(const BwdTcParams& p, const KvUnit& w, const BBars& br, uint32_t smem,
                         uint32_t tmem) {
@@ -404,16 +414,16 @@ __device__ void dkv_mma(const BwdTcParams& p, const KvUnit& w, const BBars& br, 
     // slabs kSlab apart
     const uint64_t k_desc = ptx::sdesc_sw128(smem + C::kvOffK, 16, 1024);
     const uint64_t v_desc = ptx::sdesc_sw128(smem + C::kvOffV, 16, 1024);
-    auto issue_s = [&](int t) {  // S^T(t) = K Q(t)^T
+    auto issue_s = [&](int t) {  // S^T(t) = K Q(t)^T into X_t
       ptx::tc_fence_after();
-      if (elect()) mma_rows<D, BF16>(tmem + C::kColS, k_desc, ptx::sdesc_sw128(stage(t), 16, 1024));
+      if (elect()) mma_rows<D, BF16>(tmem + region_x(t), k_desc, ptx::sdesc_sw128(stage(t), 16, 1024));
       __syncwarp();
       commit(br.bar(I::sFull));
     };
-    auto issue_dp = [&](int t) {  // dP^T(t) = V dO(t)^T
+    auto issue_dp = [&](int t) {  // dP^T(t) = V dO(t)^T into Y_t
       ptx::tc_fence_after();
       if (elect())
-        mma_rows<D, BF16>(tmem + C::kColDP, v_desc, ptx::sdesc_sw128(stage(t) + C::kTile, 16, 1024));
+        mma_rows<D, BF16>(tmem + region_y(t), v_desc, ptx::sdesc_sw128(stage(t) + C::kTile, 16, 1024));
       __syncwarp();
       commit(br.bar(I::dpFull));
     };
@@ -429,20 +439,19 @@ __device__ void dkv_mma(const BwdTcParams& p, const KvUnit& w, const BBars& br, 
       if (!(ok = wait(I::pReady, t & 1))) break;
       ptx::tc_fence_after();
       if (elect())
-        mma_acc<D, BF16>(tmem + C::kColAcc0, tmem + C::kColS, TH,
+        mma_acc<D, BF16>(tmem + C::kColAcc0, tmem + region_x(t), TH,
                          ptx::sdesc_sw128(st + C::kTile, C::kSlab, 1024), t > 0);
       __syncwarp();
-      commit(br.bar(I::dvDone));
       if (more) {
-        if (!(ok = wait(I::inFull + (t + 1) % NS, ((t + 1) / NS) & 1) && wait(I::dvDone, t & 1))) break;
+        if (!(ok = wait(I::inFull + (t + 1) % NS, ((t + 1) / NS) & 1) && wait(I::dpFree, t & 1))) break;
         issue_s(t + 1);
       }
       // dK += dS^T Q (unscaled; sm_scale is applied in the epilogue)
       if (!(ok = wait(I::dsReady, t & 1))) break;
       ptx::tc_fence_after();
       if (elect())
-        mma_acc<D, BF16>(tmem + C::kColAcc1, tmem + C::kColDP, TH, ptx::sdesc_sw128(st, C::kSlab, 1024),
-                         t > 0);
+        mma_acc<D, BF16>(tmem + C::kColAcc1, tmem + region_x(t) + TH / 2, TH,
+                         ptx::sdesc_sw128(st, C::kSlab, 1024), t > 0);
       __syncwarp();
       commit(br.bar(I::dkDone));
       commit(br.bar(I::inEmpty + t % NS));
@@ -485,8 +494,9 @@ __device__ __forceinline__ int cols_in(int dg, int c_lo, int part) {
 // tile (TMEM lane), query columns [TH grp, TH grp + TH) of every step.
 //   P^T = exp2(S^T sm_scale log2(e) - LSE log2(e)), zero where the key is at
 //   or beyond valid_len[b] or (diagonal tile, causal) after the query; kept in
-//   fp32 registers for dS and written to TMEM as 16-bit pairs;
-//   dS^T = P^T (dP^T - delta), written over the dP^T columns.
+//   fp32 registers for dS and written to TMEM as 16-bit pairs over the first
+//   TH/2 S^T columns of the thread's block;
+//   dS^T = P^T (dP^T - delta), written over the next TH/2.
 // Epilogue: the first half of the warpgroups write dV, the second dK (x
 // sm_scale), each a D / (kGroups / 2)-column part of the row.
 template <int D, bool BF16>
@@ -499,8 +509,7 @@ __device__ void dkv_elementwise(const BwdTcParams& p, const KvUnit& w, const BBa
   const int row = threadIdx.x & 127;
   const int grp = static_cast<int>(threadIdx.x) >> 7;
   const uint32_t lane_addr = (((threadIdx.x >> 5) & 3u) * 32u) << 16;
-  const uint32_t t_s = tmem + lane_addr + C::kColS + grp * TH;
-  const uint32_t t_dp = tmem + lane_addr + C::kColDP + grp * TH;
+  const uint32_t t_grp = tmem + lane_addr + grp * TH;  // + region_x(t) / region_y(t)
   const bool key_ok = w.n * T + row < w.kv_len;
   const uint64_t sc2 = ptx::f2_pack(p.scale_log2, p.scale_log2);
   bool ok = true;
@@ -512,6 +521,8 @@ __device__ void dkv_elementwise(const BwdTcParams& p, const KvUnit& w, const BBa
     ok = __all_sync(kFull, bwait(br, p.status, br.bar(I::inFull + s), (t / NS) & 1, kRoleSoftmax));
     if (ok) ok = __all_sync(kFull, bwait(br, p.status, br.bar(I::sFull), t & 1, kRoleSoftmax));
     if (!ok) break;
+    const uint32_t t_s = t_grp + region_x(t);   // S^T(t), then P^T(t) and dS^T(t)
+    const uint32_t t_dp = t_grp + region_y(t);  // dP^T(t)
     ptx::tc_fence_after();
     uint32_t r[TH];
     ld_th(t_s, r);
@@ -550,6 +561,8 @@ __device__ void dkv_elementwise(const BwdTcParams& p, const KvUnit& w, const BBa
     if (!ok) break;
     ptx::tc_fence_after();
     ld_th(t_dp, r);
+    ptx::tc_fence_before();
+    ptx::mbar_arrive(br.bar(I::dpFree));  // the MMA issuer may now write S^T(t+1) there
     const uint32_t dl_addr = st + 2 * C::kTile + T * 4 + grp * TH * 4;
 #pragma unroll
     for (int c = 0; c < TH; c += 4) {
@@ -568,7 +581,7 @@ __device__ void dkv_elementwise(const BwdTcParams& p, const KvUnit& w, const BBa
       pk[c / 2] = pk2<BF16>(a, b2);
       pk[c / 2 + 1] = pk2<BF16>(c2, d2);
     }
-    st_th2(t_dp, pk);
+    st_th2(t_s + TH / 2, pk);
     ptx::tmem_st_wait();
     ptx::tc_fence_before();
     ptx::mbar_arrive(br.bar(I::dsReady));
@@ -615,7 +628,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   const KvUnit w = kv_unit(p);
   if (threadIdx.x == 0) {
     for (int i = 0; i < I::n; ++i) {
-      const bool ew = (i == I::pReady || i == I::dsReady);
+      const bool ew = (i == I::pReady || i == I::dsReady || i == I::dpFree);
       ptx::mbar_init(br.bar(i), ew ? kEwThreads : 1);
     }
     ptx::st_shared_volatile(br.abort_word(), 0u);
