@@ -537,10 +537,11 @@ attn_status_t attn_bwd_strided(const void* q, const attn_strides_t* q_strides, c
   const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   void* ws = nullptr;
   cudaError_t e = cudaMallocFromPoolAsync(
-      &ws, static_cast<size_t>(attn::bwd_tc_workspace_bytes(B, Hq, L)), pool, cs);
+      &ws, static_cast<size_t>(attn::bwd_tc_workspace_bytes(B, Hq, Hkv, L, D, st->num_sms)), pool,
+      cs);
   if (e != cudaSuccess) return cuda_fail(e);
   e = attn::launch_bwd_tc(maps, o, so, dO, sdo, lse, dq, sdq, dk, sdk, dv, sdv, ws, B, Hq, Hkv, L,
-                          D, sm_scale, causal, valid_len, bf16, st->status, cs);
+                          D, sm_scale, causal, valid_len, bf16, st->num_sms, st->status, cs);
   const cudaError_t ef = cudaFreeAsync(ws, cs);
   if (e == cudaSuccess) e = ef;
   if (e != cudaSuccess) return cuda_fail(e);

@@ -79,6 +79,8 @@ struct BwdTcParams {
   int B, Hq, Hkv, L, Lp, G, n_t;  // n_t = tiles of 128 rows, Lp = 128 n_t
   int dg;                         // head dimension in memory: D, or 16 / 32 on the D = 64 kernels
   Strides sdq, sdk, sdv;          // element strides (batch, head, row) of the outputs
+  int splits;                     // CTAs per key tile of the dK/dV kernel (see bwd_tc_splits)
+  float* part;                    // splits > 1: fp32 partial dV, dK [splits][2][B*Hkv*L][dg]
   float scale_log2;               // sm_scale log2(e)
   float sm_scale;
   int causal;
@@ -322,24 +324,38 @@ struct KvIdx {
   static constexpr int n = sFull + 8;
 };
 
-// Unit of the dK/dV kernel: key tile n of (b, h_kv).  Key tiles vary slowest
-// over the grid, so under causality the units with the most query tiles start
-// first.  Steps: every query head of the group (fastest) for every query tile
-// m >= m_lo.
+// Unit of the dK/dV kernel: split s of key tile n of (b, h_kv).  The steps of
+// a key tile -- every query head of the group (fastest) for every query tile
+// m >= m_lo -- are cut into `splits` contiguous ranges, one per CTA; with more
+// than one, each CTA writes fp32 partial sums that bwd_dkv_reduce_kernel adds
+// up.  Key tiles vary slowest over the grid, so under causality the units
+// with the most query tiles start first.
 struct KvUnit {
-  int n, b, hkv, kv_len, m_lo, steps;
+  int n, s, b, hkv, kv_len, m_lo, t0, steps;  // steps [t0, t0 + steps) of the key tile
 };
 
+template <bool SPLIT>
 __device__ __forceinline__ KvUnit kv_unit(const BwdTcParams& p) {
   const int per = p.B * p.Hkv;
+  const int splits = SPLIT ? p.splits : 1;
   KvUnit w;
-  w.n = static_cast<int>(blockIdx.x) / per;
-  const int z = static_cast<int>(blockIdx.x) - w.n * per;
+  w.n = static_cast<int>(blockIdx.x) / (per * splits);
+  const int r = static_cast<int>(blockIdx.x) - w.n * per * splits;
+  w.s = SPLIT ? r / per : 0;
+  const int z = r - w.s * per;
   w.b = z / p.Hkv;
   w.hkv = z - w.b * p.Hkv;
   w.kv_len = kv_len_of(p, w.b);
   w.m_lo = p.causal ? w.n : 0;
-  w.steps = (w.n * T < w.kv_len) ? p.G * (p.n_t - w.m_lo) : 0;
+  const int total = (w.n * T < w.kv_len) ? p.G * (p.n_t - w.m_lo) : 0;
+  if constexpr (SPLIT) {
+    const int chunk = (total + splits - 1) / splits;
+    w.t0 = min(total, w.s * chunk);
+    w.steps = min(total, w.t0 + chunk) - w.t0;
+  } else {
+    w.t0 = 0;
+    w.steps = total;
+  }
   return w;
 }
 
@@ -365,8 +381,8 @@ __device__ void dkv_producer(const BwdTcParams& p, const KvUnit& w, const BBars&
   for (; t < w.steps; ++t) {
     const uint32_t s = static_cast<uint32_t>(t % NS);
     if (!bwait(br, p.status, br.bar(I::inEmpty + s), ((t / NS) & 1) ^ 1, kRoleProducer)) break;
-    const int mi = w.m_lo + t / p.G;
-    const int hq = w.hkv * p.G + t % p.G;
+    const int mi = w.m_lo + (w.t0 + t) / p.G;  // t0 = 0 without splits
+    const int hq = w.hkv * p.G + (w.t0 + t) % p.G;
     const uint32_t st = smem + C::kvOffIn + s * C::kvStageBytes;
     const uint32_t full = br.bar(I::inFull + s);
     ptx::mbar_arrive_expect_tx(full, 2 * C::kTile + 1024);
@@ -499,7 +515,7 @@ __device__ __forceinline__ int cols_in(int dg, int c_lo, int part) {
 //   dS^T = P^T (dP^T - delta), written over the next TH/2.
 // Epilogue: the first half of the warpgroups write dV, the second dK (x
 // sm_scale), each a D / (kGroups / 2)-column part of the row.
-template <int D, bool BF16>
+template <int D, bool BF16, bool SPLIT>
 __device__ void dkv_elementwise(const BwdTcParams& p, const KvUnit& w, const BBars& br,
                                 uint32_t smem, uint32_t tmem) {
   using C = BCfg<D>;
@@ -516,7 +532,7 @@ __device__ void dkv_elementwise(const BwdTcParams& p, const KvUnit& w, const BBa
   for (int t = 0; ok && t < w.steps; ++t) {
     const uint32_t s = static_cast<uint32_t>(t % NS);
     const uint32_t st = smem + C::kvOffIn + s * C::kvStageBytes;
-    const int mi = w.m_lo + t / p.G;
+    const int mi = w.m_lo + ((SPLIT ? w.t0 : 0) + t) / p.G;
     // the stage's -LSE log2(e) and delta are read from shared memory
     ok = __all_sync(kFull, bwait(br, p.status, br.bar(I::inFull + s), (t / NS) & 1, kRoleSoftmax));
     if (ok) ok = __all_sync(kFull, bwait(br, p.status, br.bar(I::sFull), t & 1, kRoleSoftmax));
@@ -597,8 +613,19 @@ __device__ void dkv_elementwise(const BwdTcParams& p, const KvUnit& w, const BBa
   const Strides& so = is_dk ? p.sdk : p.sdv;
   uint16_t* dst = static_cast<uint16_t*>(is_dk ? p.dk : p.dv) + w.b * so.b + w.hkv * so.h +
                   static_cast<int64_t>(j) * so.l + c_lo;
-  if (w.steps == 0) {  // no query sees these keys
-    for (int c = 0; c < nv / 8; ++c) reinterpret_cast<uint4*>(dst)[c] = make_uint4(0u, 0u, 0u, 0u);
+  // split key tiles: unscaled fp32 partial rows, summed by bwd_dkv_reduce_kernel
+  float* part = p.part + ((static_cast<int64_t>(w.s) * 2 + (is_dk ? 1 : 0)) * p.B * p.Hkv * p.L +
+                          (static_cast<int64_t>(w.b) * p.Hkv + w.hkv) * p.L + j) * p.dg + c_lo;
+  constexpr bool split = SPLIT;
+  if (w.steps == 0) {  // no query sees these keys (in this split)
+    for (int c = 0; c < nv / 8; ++c) {
+      if (split) {
+        reinterpret_cast<float4*>(part)[2 * c] = make_float4(0.f, 0.f, 0.f, 0.f);
+        reinterpret_cast<float4*>(part)[2 * c + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      } else {
+        reinterpret_cast<uint4*>(dst)[c] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
     return;
   }
   if (!__all_sync(kFull, bwait(br, p.status, br.bar(I::accFull), 0, kRoleEpilogue))) return;
@@ -609,11 +636,58 @@ __device__ void dkv_elementwise(const BwdTcParams& p, const KvUnit& w, const BBa
   for (int c0 = 0; c0 < kPart; c0 += 32) {
     uint32_t r[32];
     ptx::tmem_ld32(t_acc + c0, r);
-    store_chunk<BF16>(dst + c0, r, mul, nv - c0);
+    if (split) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (c0 + q * 4 < nv)
+          reinterpret_cast<float4*>(part + c0)[q] =
+              make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                          __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+    } else {
+      store_chunk<BF16>(dst + c0, r, mul, nv - c0);
+    }
   }
 }
 
-template <int D, bool BF16>
+// dV and dK of split key tiles: the `splits` fp32 partials of every element
+// added in split order (deterministic), dK times sm_scale, rounded once to
+// the input dtype.  One thread per 8 consecutive elements of a row.
+template <bool BF16>
+__global__ void __launch_bounds__(256) bwd_dkv_reduce_kernel(const BwdTcParams p) {
+  const int64_t rows = static_cast<int64_t>(p.B) * p.Hkv * p.L;
+  const int64_t per_row = p.dg / 8;
+  const int64_t v = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x;
+  if (v >= 2 * rows * per_row) return;
+  const int which = static_cast<int>(v / (rows * per_row));  // 0: dV, 1: dK
+  const int64_t e = v - which * rows * per_row;
+  const int64_t row = e / per_row;
+  const int col = static_cast<int>(e - row * per_row) * 8;
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+  for (int sp = 0; sp < p.splits; ++sp) {
+    const float4* src = reinterpret_cast<const float4*>(
+        p.part + ((static_cast<int64_t>(sp) * 2 + which) * rows + row) * p.dg + col);
+    const float4 a = src[0], b = src[1];
+    acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+    acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+  }
+  const float mul = which ? p.sm_scale : 1.f;
+  const int64_t z = row / p.L;  // b * Hkv + h_kv
+  const int64_t j = row - z * p.L;
+  const int64_t sb = which ? p.sdk.b : p.sdv.b;
+  const int64_t sh = which ? p.sdk.h : p.sdv.h;
+  const int64_t sl = which ? p.sdk.l : p.sdv.l;
+  uint16_t* dst = static_cast<uint16_t*>(which ? p.dk : p.dv) + (z / p.Hkv) * sb + (z % p.Hkv) * sh +
+                  j * sl + col;
+  *reinterpret_cast<uint4*>(dst) = make_uint4(pk2<BF16>(acc[0] * mul, acc[1] * mul),
+                                              pk2<BF16>(acc[2] * mul, acc[3] * mul),
+                                              pk2<BF16>(acc[4] * mul, acc[5] * mul),
+                                              pk2<BF16>(acc[6] * mul, acc[7] * mul));
+}
+
+// SPLIT: key tiles split over several CTAs (p.splits > 1), fp32 partial rows.
+template <int D, bool BF16, bool SPLIT>
 __global__ void __launch_bounds__(kThreadsB, 1)
     bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v,
@@ -625,7 +699,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   const BBars br{smem + C::kvOffBar, I::n};
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const KvUnit w = kv_unit(p);
+  const KvUnit w = kv_unit<SPLIT>(p);
   if (threadIdx.x == 0) {
     for (int i = 0; i < I::n; ++i) {
       const bool ew = (i == I::pReady || i == I::dsReady || i == I::dpFree);
@@ -655,7 +729,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   } else if (warp == kMmaWarp) {
     dkv_mma<D, BF16>(p, w, br, smem, tmem);
   } else {
-    dkv_elementwise<D, BF16>(p, w, br, smem, tmem);
+    dkv_elementwise<D, BF16, SPLIT>(p, w, br, smem, tmem);
   }
   ptx::tc_fence_before();
   __syncthreads();
@@ -984,16 +1058,22 @@ cudaError_t launch_bwd_tc_d(const CUtensorMap (&maps)[4], const BwdTcParams& p, 
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(bwd_dkv_tc_kernel<D, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           C::kvSmem);
+  auto dkv = p.splits > 1 ? bwd_dkv_tc_kernel<D, BF16, true> : bwd_dkv_tc_kernel<D, BF16, false>;
+  e = cudaFuncSetAttribute(dkv, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kvSmem);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(bwd_dq_tc_kernel<D, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::qSmem);
   if (e != cudaSuccess) return e;
-  bwd_dkv_tc_kernel<D, BF16><<<static_cast<unsigned>(p.n_t * p.B * p.Hkv), kThreadsB, C::kvSmem, stream>>>(
+  dkv<<<static_cast<unsigned>(p.n_t * p.B * p.Hkv * p.splits), kThreadsB, C::kvSmem, stream>>>(
       maps[0], maps[1], maps[2], maps[3], p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  if (p.splits > 1) {
+    const int64_t vecs = 2 * static_cast<int64_t>(p.B) * p.Hkv * p.L * (p.dg / 8);
+    bwd_dkv_reduce_kernel<BF16><<<static_cast<unsigned>((vecs + 255) / 256), 256, 0, stream>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   bwd_dq_tc_kernel<D, BF16><<<static_cast<unsigned>(p.n_t * p.B * p.Hq), kThreadsB, C::qSmem, stream>>>(
       maps[0], maps[1], maps[2], maps[3], p);
   return cudaGetLastError();
@@ -1001,9 +1081,23 @@ cudaError_t launch_bwd_tc_d(const CUtensorMap (&maps)[4], const BwdTcParams& p, 
 
 }  // namespace
 
-int64_t bwd_tc_workspace_bytes(int B, int Hq, int L) {
+// CTAs per key tile of the dK/dV kernel: 1 when its (key tile, b, h_kv) units
+// alone fill four waves of the GPU, else enough splits of each key tile's
+// steps to do so (at most 16) -- with few K/V heads (MQA), one CTA per key
+// tile would run every query head of the group and leave SMs idle.
+int bwd_tc_splits(int B, int Hkv, int L, int num_sms) {
+  const int64_t units = static_cast<int64_t>((L + T - 1) / T) * B * Hkv;
+  const int64_t target = 4 * static_cast<int64_t>(num_sms > 0 ? num_sms : 1);
+  if (units >= target) return 1;
+  const int64_t s = (target + units - 1) / units;
+  return static_cast<int>(s < 16 ? s : 16);
+}
+
+int64_t bwd_tc_workspace_bytes(int B, int Hq, int Hkv, int L, int D, int num_sms) {
   const int64_t lp = (static_cast<int64_t>(L) + T - 1) / T * T;
-  return 2 * static_cast<int64_t>(B) * Hq * lp * 4;
+  const int splits = bwd_tc_splits(B, Hkv, L, num_sms);
+  const int64_t part = splits > 1 ? static_cast<int64_t>(splits) * 2 * B * Hkv * L * D * 4 : 0;
+  return 2 * static_cast<int64_t>(B) * Hq * lp * 4 + part;
 }
 
 cudaError_t launch_bwd_tc(const CUtensorMap (&maps)[4], const void* o, const Strides& so,
@@ -1011,8 +1105,9 @@ cudaError_t launch_bwd_tc(const CUtensorMap (&maps)[4], const void* o, const Str
                           const Strides& sdq, void* dk, const Strides& sdk, void* dv,
                           const Strides& sdv, void* workspace, int B, int Hq, int Hkv, int L, int D,
                           float sm_scale, int causal, const int32_t* valid_len, bool bf16,
-                          int* status, cudaStream_t stream) {
+                          int num_sms, int* status, cudaStream_t stream) {
   BwdTcParams p;
+  p.splits = bwd_tc_splits(B, Hkv, L, num_sms);
   p.sdq = sdq;
   p.sdk = sdk;
   p.sdv = sdv;
@@ -1020,6 +1115,7 @@ cudaError_t launch_bwd_tc(const CUtensorMap (&maps)[4], const void* o, const Str
   p.Lp = p.n_t * T;
   float* nlse2 = static_cast<float*>(workspace);
   float* delta = nlse2 + static_cast<int64_t>(B) * Hq * p.Lp;
+  p.part = delta + static_cast<int64_t>(B) * Hq * p.Lp;  // used when splits > 1
   p.nlse2 = nlse2;
   p.delta = delta;
   p.dq = dq;

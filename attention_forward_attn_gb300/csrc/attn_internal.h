@@ -110,14 +110,17 @@ cudaError_t launch_bwd(const void* q, const void* k, const void* v, const void* 
 // and delta, fp32 [B*Hq, L rounded up to 128] each) and its launch (pre-pass,
 // dK/dV and dQ kernels on `stream`).  maps: Q, K, V, dO as encode_map makes
 // them with 128-row boxes.  so, sdo: element strides of O and dO (read by the
-// pre-pass); sdq, sdk, sdv: of the outputs.  D 16, 32, 64 or 128.
-int64_t bwd_tc_workspace_bytes(int B, int Hq, int L);
+// pre-pass); sdq, sdk, sdv: of the outputs.  D 16, 32, 64 or 128.  With few
+// key tiles per SM the dK/dV kernel splits each key tile over several CTAs
+// (bwd_tc_splits) and the workspace also holds their fp32 partial sums.
+int bwd_tc_splits(int B, int Hkv, int L, int num_sms);
+int64_t bwd_tc_workspace_bytes(int B, int Hq, int Hkv, int L, int D, int num_sms);
 cudaError_t launch_bwd_tc(const CUtensorMap (&maps)[4], const void* o, const Strides& so,
                           const void* dO, const Strides& sdo, const float* lse, void* dq,
                           const Strides& sdq, void* dk, const Strides& sdk, void* dv,
                           const Strides& sdv, void* workspace, int B, int Hq, int Hkv, int L, int D,
                           float sm_scale, int causal, const int32_t* valid_len, bool bf16,
-                          int* status, cudaStream_t stream);
+                          int num_sms, int* status, cudaStream_t stream);
 
 // SIMT cross-check forward.
 cudaError_t launch_simt(const Problem& p);
