@@ -59,11 +59,11 @@ def _bind(path: str):
     lib.oracle_attn_fwd_u16.argtypes = [p, p, p, p, p, i, i, i, i, i, i, ctypes.c_double,
                                         i, p, p, i64, i64, i, p, i64, i]
     lib.oracle_attn_fwd_u16.restype = i
-    lib.oracle_attn_bwd_f64.argtypes = [p, p, p, p, p, p, p, i, i, i, i, i, ctypes.c_double, i,
-                                        p, i]
+    lib.oracle_attn_bwd_f64.argtypes = [p, p, p, p, p, p, p, i, i, i, i, i, i, ctypes.c_double,
+                                        i, p, i]
     lib.oracle_attn_bwd_f64.restype = i
-    lib.oracle_attn_bwd_rows_f64.argtypes = [p, p, p, p, i, i, i, i, i, ctypes.c_double, i, p,
-                                             p, i64, p, p, p, i64, p, p, p, i]
+    lib.oracle_attn_bwd_rows_f64.argtypes = [p, p, p, p, i, i, i, i, i, i, ctypes.c_double, i,
+                                             p, p, i64, p, p, p, i64, p, p, p, i]
     lib.oracle_attn_bwd_rows_f64.restype = i
     lib.oracle_decode.argtypes = [p, p, i64, i]
     lib.oracle_decode.restype = i
@@ -201,20 +201,20 @@ def attn_bwd_f64(q, k, v, do, sm_scale, causal=False, valid_len=None, threads=0,
                  _lib_override=None):
     """Gradients (dq, dk, dv) of the attention forward for an output gradient
     ``do``, from the definition (see oracle_attn_bwd_f64).  q, do:
-    [B, Hq, L, D]; k, v: [B, Hkv, L, D]; float64 results of the same shapes."""
+    [B, Hq, Lq, D]; k, v: [B, Hkv, Lk, D]; float64 results of the same shapes."""
     q = np.ascontiguousarray(q, dtype=np.float64)
     k = np.ascontiguousarray(k, dtype=np.float64)
     v = np.ascontiguousarray(v, dtype=np.float64)
     do = np.ascontiguousarray(do, dtype=np.float64)
     B, Hq, Hkv, Lq, Lk, D = _shapes(q, k, v)
-    if Lq != Lk or do.shape != q.shape:
-        raise ValueError("the backward oracle takes Lq == Lk and do shaped like q")
+    if do.shape != q.shape:
+        raise ValueError("do must be shaped like q")
     vl = _valid(valid_len, B)
     dq, dk, dv = np.empty_like(q), np.empty_like(k), np.empty_like(v)
     lib = _lib_override if _lib_override is not None else _load()
     rc = lib.oracle_attn_bwd_f64(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv),
-                                 B, Hq, Hkv, Lq, D, float(sm_scale), int(bool(causal)), _ptr(vl),
-                                 int(threads))
+                                 B, Hq, Hkv, Lq, Lk, D, float(sm_scale), int(bool(causal)),
+                                 _ptr(vl), int(threads))
     if rc != 0:
         raise ValueError("oracle_attn_bwd_f64 failed with code %d" % rc)
     return dq, dk, dv
@@ -224,8 +224,8 @@ def attn_bwd_rows_f64(q, k, v, do, sm_scale, causal=False, valid_len=None, q_row
                       k_rows=(), threads=0, _lib_override=None):
     """Selected rows of :func:`attn_bwd_f64`'s gradients (see
     oracle_attn_bwd_rows_f64): dQ for flat query rows ``q_rows`` (index
-    (b*Hq + h_q)*L + i) and dK, dV for flat key rows ``k_rows`` (index
-    (b*Hkv + h_kv)*L + j).  Returns dq [n_q, D], qmag [n_q, 3] (sum_j |dS_ij|,
+    (b*Hq + h_q)*Lq + i) and dK, dV for flat key rows ``k_rows`` (index
+    (b*Hkv + h_kv)*Lk + j).  Returns dq [n_q, D], qmag [n_q, 3] (sum_j |dS_ij|,
     sum_d |dO_id O_id|, visible keys), dk, dv [n_k, D], kmag [n_k, 4]
     (sum_i |dS_ij|, sum_i P_ij, sum_i P_ij sum_d |dO_id O_id|, visible queries)."""
     q = np.ascontiguousarray(q, dtype=np.float64)
@@ -233,8 +233,8 @@ def attn_bwd_rows_f64(q, k, v, do, sm_scale, causal=False, valid_len=None, q_row
     v = np.ascontiguousarray(v, dtype=np.float64)
     do = np.ascontiguousarray(do, dtype=np.float64)
     B, Hq, Hkv, Lq, Lk, D = _shapes(q, k, v)
-    if Lq != Lk or do.shape != q.shape:
-        raise ValueError("the backward oracle takes Lq == Lk and do shaped like q")
+    if do.shape != q.shape:
+        raise ValueError("do must be shaped like q")
     vl = _valid(valid_len, B)
     qr = np.ascontiguousarray(np.asarray(q_rows, dtype=np.int64).reshape(-1))
     kr = np.ascontiguousarray(np.asarray(k_rows, dtype=np.int64).reshape(-1))
@@ -243,7 +243,7 @@ def attn_bwd_rows_f64(q, k, v, do, sm_scale, causal=False, valid_len=None, q_row
     dk, dv = np.empty((kr.size, D)), np.empty((kr.size, D))
     kmag = np.empty((kr.size, 4))
     lib = _lib_override if _lib_override is not None else _load()
-    rc = lib.oracle_attn_bwd_rows_f64(_ptr(q), _ptr(k), _ptr(v), _ptr(do), B, Hq, Hkv, Lq, D,
+    rc = lib.oracle_attn_bwd_rows_f64(_ptr(q), _ptr(k), _ptr(v), _ptr(do), B, Hq, Hkv, Lq, Lk, D,
                                       float(sm_scale), int(bool(causal)), _ptr(vl), _ptr(qr),
                                       qr.size, _ptr(dq), _ptr(qmag), _ptr(kr), kr.size, _ptr(dk),
                                       _ptr(dv), _ptr(kmag), int(threads))

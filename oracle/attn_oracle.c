@@ -251,18 +251,20 @@ int oracle_max_threads(void) {
  * sum over the query heads that read it.  Rows without a visible key give
  * nothing.  Float64, plain loops, one (b, h_kv) group per OpenMP task.
  *
- * q, dO: [B, Hq, L, D]; k, v: [B, Hkv, L, D]; dq like q, dk and dv like k.
+ * q, dO: [B, Hq, Lq, D]; k, v: [B, Hkv, Lk, D]; dq like q, dk and dv like k
+ * (Lq = Lk is the pages' case; the masks compare absolute positions as in
+ * the forward).
  * Returns 0, 1 on invalid arguments, 2 when scratch could not be allocated.
  */
 int oracle_attn_bwd_f64(const double* q, const double* k, const double* v, const double* dO,
-                        double* dq, double* dk, double* dv, int B, int Hq, int Hkv, int L, int D,
+                        double* dq, double* dk, double* dv, int B, int Hq, int Hkv, int Lq, int Lk, int D,
                         double sm_scale, int causal, const int32_t* valid_len, int threads) {
-  if (B < 1 || Hq < 1 || Hkv < 1 || L < 1 || D < 1 || Hq % Hkv != 0) return 1;
+  if (B < 1 || Hq < 1 || Hkv < 1 || Lq < 1 || Lk < 1 || D < 1 || Hq % Hkv != 0) return 1;
   const int G = Hq / Hkv;
   const oracle_mask_t mk = {NULL, 0, 0};
-  memset(dq, 0, sizeof(double) * (size_t)B * Hq * L * D);
-  memset(dk, 0, sizeof(double) * (size_t)B * Hkv * L * D);
-  memset(dv, 0, sizeof(double) * (size_t)B * Hkv * L * D);
+  memset(dq, 0, sizeof(double) * (size_t)B * Hq * Lq * D);
+  memset(dk, 0, sizeof(double) * (size_t)B * Hkv * Lk * D);
+  memset(dv, 0, sizeof(double) * (size_t)B * Hkv * Lk * D);
 #ifdef _OPENMP
   if (threads > 0) omp_set_num_threads(threads);
 #else
@@ -271,8 +273,8 @@ int oracle_attn_bwd_f64(const double* q, const double* k, const double* v, const
   int bad = 0;
 #pragma omp parallel
   {
-    double* p = (double*)malloc(sizeof(double) * (size_t)L);   /* P_i. of one row */
-    double* dp = (double*)malloc(sizeof(double) * (size_t)L);  /* dP_i. of one row */
+    double* p = (double*)malloc(sizeof(double) * (size_t)Lk);   /* P_i. of one row */
+    double* dp = (double*)malloc(sizeof(double) * (size_t)Lk);  /* dP_i. of one row */
     if (!p || !dp) {
 #pragma omp atomic write
       bad = 1;
@@ -282,21 +284,21 @@ int oracle_attn_bwd_f64(const double* q, const double* k, const double* v, const
       if (!p || !dp) continue;
       const int b = (int)(grp / Hkv);
       const int h_kv = (int)(grp % Hkv);
-      const double* k_head = k + grp * L * (int64_t)D;
-      const double* v_head = v + grp * L * (int64_t)D;
-      double* dk_head = dk + grp * L * (int64_t)D;
-      double* dv_head = dv + grp * L * (int64_t)D;
+      const double* k_head = k + grp * Lk * (int64_t)D;
+      const double* v_head = v + grp * Lk * (int64_t)D;
+      double* dk_head = dk + grp * Lk * (int64_t)D;
+      double* dv_head = dv + grp * Lk * (int64_t)D;
       for (int g = 0; g < G; ++g) {
         const int h_q = h_kv * G + g;
         const int64_t qh = (int64_t)b * Hq + h_q;
-        for (int64_t i = 0; i < L; ++i) {
-          const double* q_row = q + (qh * L + i) * D;
-          const double* do_row = dO + (qh * L + i) * D;
-          double* dq_row = dq + (qh * L + i) * D;
+        for (int64_t i = 0; i < Lq; ++i) {
+          const double* q_row = q + (qh * Lq + i) * D;
+          const double* do_row = dO + (qh * Lq + i) * D;
+          double* dq_row = dq + (qh * Lq + i) * D;
           /* P_i. by the definition (max subtracted for the exponentials) */
           double m = -INFINITY;
           int any = 0;
-          for (int64_t j = 0; j < L; ++j) {
+          for (int64_t j = 0; j < Lk; ++j) {
             if (!key_visible(i, j, b, causal, valid_len, &mk)) continue;
             double dot = 0.0;
             for (int d = 0; d < D; ++d) dot += q_row[d] * k_head[j * D + d];
@@ -306,13 +308,13 @@ int oracle_attn_bwd_f64(const double* q, const double* k, const double* v, const
           }
           if (!any) continue;
           double z = 0.0;
-          for (int64_t j = 0; j < L; ++j) {
+          for (int64_t j = 0; j < Lk; ++j) {
             if (!key_visible(i, j, b, causal, valid_len, &mk)) continue;
             p[j] = exp(p[j] - m);
             z += p[j];
           }
           double pdp = 0.0; /* sum_j P_ij dP_ij */
-          for (int64_t j = 0; j < L; ++j) {
+          for (int64_t j = 0; j < Lk; ++j) {
             if (!key_visible(i, j, b, causal, valid_len, &mk)) continue;
             p[j] /= z;
             double dot = 0.0;
@@ -320,7 +322,7 @@ int oracle_attn_bwd_f64(const double* q, const double* k, const double* v, const
             dp[j] = dot;
             pdp += p[j] * dot;
           }
-          for (int64_t j = 0; j < L; ++j) {
+          for (int64_t j = 0; j < Lk; ++j) {
             if (!key_visible(i, j, b, causal, valid_len, &mk)) continue;
             const double ds = p[j] * (dp[j] - pdp);
             for (int d = 0; d < D; ++d) {
@@ -342,17 +344,17 @@ int oracle_attn_bwd_f64(const double* q, const double* k, const double* v, const
  * Statistics of query row i (q_row, do_row) against the keys of its K/V head,
  * from the definition: the maximum m of the visible scores s_j = sm_scale *
  * q_i.k_j, z = sum_j exp(s_j - m), delta = sum_j P_ij dP_ij with
- * P_ij = exp(s_j - m) / z and dP_ij = dO_i.v_j.  s: scratch of L doubles.
+ * P_ij = exp(s_j - m) / z and dP_ij = dO_i.v_j.  s: scratch of Lk doubles.
  * Returns the number of visible keys (0: the row sees none; m, z, delta unset).
  */
 static int64_t row_stats(const double* q_row, const double* do_row, const double* k_head,
-                         const double* v_head, int64_t i, int b, int L, int D, double sm_scale,
+                         const double* v_head, int64_t i, int b, int Lk, int D, double sm_scale,
                          int causal, const int32_t* valid_len, double* s, double* m_out,
                          double* z_out, double* delta_out) {
   const oracle_mask_t mk = {NULL, 0, 0};
   double m = -INFINITY;
   int64_t n = 0;
-  for (int64_t j = 0; j < L; ++j) {
+  for (int64_t j = 0; j < Lk; ++j) {
     if (!key_visible(i, j, b, causal, valid_len, &mk)) continue;
     double dot = 0.0;
     for (int d = 0; d < D; ++d) dot += q_row[d] * k_head[j * D + d];
@@ -362,7 +364,7 @@ static int64_t row_stats(const double* q_row, const double* do_row, const double
   }
   if (n == 0) return 0;
   double z = 0.0, acc = 0.0;
-  for (int64_t j = 0; j < L; ++j) {
+  for (int64_t j = 0; j < Lk; ++j) {
     if (!key_visible(i, j, b, causal, valid_len, &mk)) continue;
     const double e = exp(s[j] - m);
     double dp = 0.0;
@@ -379,8 +381,8 @@ static int64_t row_stats(const double* q_row, const double* do_row, const double
 /*
  * Selected rows of the gradients of oracle_attn_bwd_f64 (same inputs and
  * definition), for checks at sizes where the full backward is too slow:
- *   dQ rows q_rows[r] (flat index (b*Hq + h_q)*L + i), r < n_q -> dq[r*D ..];
- *   dK, dV rows k_rows[r] (flat index (b*Hkv + h_kv)*L + j), r < n_k ->
+ *   dQ rows q_rows[r] (flat index (b*Hq + h_q)*Lq + i), r < n_q -> dq[r*D ..];
+ *   dK, dV rows k_rows[r] (flat index (b*Hkv + h_kv)*Lk + j), r < n_k ->
  *   dk[r*D ..], dv[r*D ..].
  * A key row sums over every query row of its group's G query heads, so the
  * statistics of those rows are computed once per group that a sampled key
@@ -391,17 +393,18 @@ static int64_t row_stats(const double* q_row, const double* do_row, const double
  * (sums over the G query heads of the key's group).
  */
 int oracle_attn_bwd_rows_f64(const double* q, const double* k, const double* v, const double* dO,
-                             int B, int Hq, int Hkv, int L, int D, double sm_scale, int causal,
+                             int B, int Hq, int Hkv, int Lq, int Lk, int D, double sm_scale,
+                             int causal,
                              const int32_t* valid_len, const int64_t* q_rows, int64_t n_q,
                              double* dq, double* qmag, const int64_t* k_rows, int64_t n_k,
                              double* dk, double* dv, double* kmag, int threads) {
-  if (B < 1 || Hq < 1 || Hkv < 1 || L < 1 || D < 1 || Hq % Hkv != 0) return 1;
+  if (B < 1 || Hq < 1 || Hkv < 1 || Lq < 1 || Lk < 1 || D < 1 || Hq % Hkv != 0) return 1;
   const int G = Hq / Hkv;
   const oracle_mask_t mk = {NULL, 0, 0};
   for (int64_t r = 0; r < n_q; ++r)
-    if (q_rows[r] < 0 || q_rows[r] >= (int64_t)B * Hq * L) return 1;
+    if (q_rows[r] < 0 || q_rows[r] >= (int64_t)B * Hq * Lq) return 1;
   for (int64_t r = 0; r < n_k; ++r)
-    if (k_rows[r] < 0 || k_rows[r] >= (int64_t)B * Hkv * L) return 1;
+    if (k_rows[r] < 0 || k_rows[r] >= (int64_t)B * Hkv * Lk) return 1;
 #ifdef _OPENMP
   if (threads > 0) omp_set_num_threads(threads);
 #else
@@ -411,7 +414,7 @@ int oracle_attn_bwd_rows_f64(const double* q, const double* k, const double* v, 
   /* dQ rows */
 #pragma omp parallel
   {
-    double* s = (double*)malloc(sizeof(double) * (size_t)L);
+    double* s = (double*)malloc(sizeof(double) * (size_t)Lk);
     if (!s) {
 #pragma omp atomic write
       bad = 1;
@@ -419,22 +422,22 @@ int oracle_attn_bwd_rows_f64(const double* q, const double* k, const double* v, 
 #pragma omp for schedule(dynamic, 1)
     for (int64_t r = 0; r < n_q; ++r) {
       if (!s) continue;
-      const int64_t qh = q_rows[r] / L;
-      const int64_t i = q_rows[r] % L;
+      const int64_t qh = q_rows[r] / Lq;
+      const int64_t i = q_rows[r] % Lq;
       const int b = (int)(qh / Hq);
       const int64_t kvh = (int64_t)b * Hkv + (qh % Hq) / G;
       const double* q_row = q + q_rows[r] * D;
       const double* do_row = dO + q_rows[r] * D;
-      const double* k_head = k + kvh * L * (int64_t)D;
-      const double* v_head = v + kvh * L * (int64_t)D;
+      const double* k_head = k + kvh * Lk * (int64_t)D;
+      const double* v_head = v + kvh * Lk * (int64_t)D;
       double* dq_row = dq + r * D;
       double m = 0.0, z = 1.0, delta = 0.0, sabs = 0.0, w = 0.0;
       for (int d = 0; d < D; ++d) dq_row[d] = 0.0;
-      const int64_t n = row_stats(q_row, do_row, k_head, v_head, i, b, L, D, sm_scale, causal,
+      const int64_t n = row_stats(q_row, do_row, k_head, v_head, i, b, Lk, D, sm_scale, causal,
                                   valid_len, s, &m, &z, &delta);
       if (n > 0) {
         double* o_row = (double*)calloc((size_t)D, sizeof(double));
-        for (int64_t j = 0; j < L; ++j) {
+        for (int64_t j = 0; j < Lk; ++j) {
           if (!key_visible(i, j, b, causal, valid_len, &mk)) continue;
           const double p = exp(s[j] - m) / z;
           double dp = 0.0;
@@ -463,20 +466,20 @@ int oracle_attn_bwd_rows_f64(const double* q, const double* k, const double* v, 
   }
   /* dK, dV rows: group by K/V head, row statistics of the group's query rows once */
   for (int64_t r0 = 0; r0 < n_k && !bad; ++r0) {
-    const int64_t kvh = k_rows[r0] / L;
+    const int64_t kvh = k_rows[r0] / Lk;
     int seen = 0;
-    for (int64_t r = 0; r < r0; ++r) seen |= (k_rows[r] / L == kvh);
+    for (int64_t r = 0; r < r0; ++r) seen |= (k_rows[r] / Lk == kvh);
     if (seen) continue;
     const int b = (int)(kvh / Hkv);
     const int h_kv = (int)(kvh % Hkv);
-    const double* k_head = k + kvh * L * (int64_t)D;
-    const double* v_head = v + kvh * L * (int64_t)D;
-    const int64_t nrow = (int64_t)G * L;
+    const double* k_head = k + kvh * Lk * (int64_t)D;
+    const double* v_head = v + kvh * Lk * (int64_t)D;
+    const int64_t nrow = (int64_t)G * Lq;
     double* st = (double*)malloc(sizeof(double) * 4 * (size_t)nrow);  /* m, z, delta, w */
     if (!st) return 2;
 #pragma omp parallel
     {
-      double* s = (double*)malloc(sizeof(double) * (size_t)L);
+      double* s = (double*)malloc(sizeof(double) * (size_t)Lk);
       double* o_row = (double*)malloc(sizeof(double) * (size_t)D);
       if (!s || !o_row) {
 #pragma omp atomic write
@@ -485,14 +488,14 @@ int oracle_attn_bwd_rows_f64(const double* q, const double* k, const double* v, 
 #pragma omp for schedule(dynamic, 16)
       for (int64_t gi = 0; gi < nrow; ++gi) {
         if (!s || !o_row) continue;
-        const int64_t qrow = ((int64_t)b * Hq + (int64_t)h_kv * G + gi / L) * L + gi % L;
-        const int64_t i = gi % L;
+        const int64_t qrow = ((int64_t)b * Hq + (int64_t)h_kv * G + gi / Lq) * Lq + gi % Lq;
+        const int64_t i = gi % Lq;
         double m = 0.0, z = 1.0, delta = 0.0, w = 0.0;
-        const int64_t n = row_stats(q + qrow * D, dO + qrow * D, k_head, v_head, i, b, L, D,
+        const int64_t n = row_stats(q + qrow * D, dO + qrow * D, k_head, v_head, i, b, Lk, D,
                                     sm_scale, causal, valid_len, s, &m, &z, &delta);
         if (n > 0) {
           for (int d = 0; d < D; ++d) o_row[d] = 0.0;
-          for (int64_t j = 0; j < L; ++j) {
+          for (int64_t j = 0; j < Lk; ++j) {
             if (!key_visible(i, j, b, causal, valid_len, &mk)) continue;
             const double p = exp(s[j] - m) / z;
             for (int d = 0; d < D; ++d) o_row[d] += p * v_head[j * D + d];
@@ -509,8 +512,8 @@ int oracle_attn_bwd_rows_f64(const double* q, const double* k, const double* v, 
     }
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t r = r0; r < n_k; ++r) {
-      if (k_rows[r] / L != kvh) continue;
-      const int64_t j = k_rows[r] % L;
+      if (k_rows[r] / Lk != kvh) continue;
+      const int64_t j = k_rows[r] % Lk;
       const double* k_row = k_head + j * D;
       const double* v_row = v_head + j * D;
       double* dk_row = dk + r * D;
@@ -518,9 +521,9 @@ int oracle_attn_bwd_rows_f64(const double* q, const double* k, const double* v, 
       double sabs = 0.0, psum = 0.0, pw = 0.0, nvis = 0.0;
       for (int d = 0; d < D; ++d) dk_row[d] = dv_row[d] = 0.0;
       for (int64_t gi = 0; gi < nrow; ++gi) {
-        const int64_t i = gi % L;
+        const int64_t i = gi % Lq;
         if (st[4 * gi] == INFINITY || !key_visible(i, j, b, causal, valid_len, &mk)) continue;
-        const int64_t qrow = ((int64_t)b * Hq + (int64_t)h_kv * G + gi / L) * L + i;
+        const int64_t qrow = ((int64_t)b * Hq + (int64_t)h_kv * G + gi / Lq) * Lq + i;
         const double* q_row = q + qrow * D;
         const double* do_row = dO + qrow * D;
         double dot = 0.0, dp = 0.0;

@@ -53,29 +53,33 @@ def finite_differences(q, k, v, do, sm, causal, vl, h=1e-6):
 
 def torch_grads(q, k, v, do, sm, causal, vl):
     qt, kt, vt = (torch.tensor(x, dtype=torch.float64, requires_grad=True) for x in (q, k, v))
-    B, Hq, L, D = q.shape
+    B, Hq, Lq, D = q.shape
+    Lk = k.shape[2]
     G = Hq // k.shape[1]
-    mask = torch.ones(B, 1, L, L, dtype=torch.bool)
-    if causal:
-        mask &= torch.tril(torch.ones(L, L, dtype=torch.bool))
+    mask = torch.ones(B, 1, Lq, Lk, dtype=torch.bool)
+    if causal:  # top-left: key j visible to query i iff j <= i
+        mask &= torch.tril(torch.ones(Lq, Lk, dtype=torch.bool))
     if vl is not None:
         for b in range(B):
-            mask[b, :, :, :] &= (torch.arange(L) < int(vl[b]))[None, :]
+            mask[b, :, :, :] &= (torch.arange(Lk) < int(vl[b]))[None, :]
     empty = ~mask.any(dim=-1, keepdim=True)
     o = torch.nn.functional.scaled_dot_product_attention(
         qt, kt.repeat_interleave(G, dim=1), vt.repeat_interleave(G, dim=1),
         attn_mask=mask | empty, scale=sm)  # rows with no key: any finite stand-in, zeroed below
-    o = o.masked_fill(empty.expand(B, Hq, L, 1), 0.0)
+    o = o.masked_fill(empty.expand(B, Hq, Lq, 1), 0.0)
     (o * torch.from_numpy(do)).sum().backward()
     return qt.grad.numpy(), kt.grad.numpy(), vt.grad.numpy()
 
 
 def pin_finite_differences(bwd):
     rng = np.random.default_rng(11)
-    for (B, Hq, Hkv, L, D, causal, vl) in [(1, 2, 1, 4, 3, True, None), (2, 2, 2, 5, 2, False, [3, 5]),
-                                           (1, 4, 2, 4, 3, True, [3])]:
-        q, k, v = rand((B, Hq, L, D), rng), rand((B, Hkv, L, D), rng), rand((B, Hkv, L, D), rng)
-        do = rand((B, Hq, L, D), rng)
+    for (B, Hq, Hkv, Lq, Lk, D, causal, vl) in [
+            (1, 2, 1, 4, 4, 3, True, None), (2, 2, 2, 5, 5, 2, False, [3, 5]),
+            (1, 4, 2, 4, 4, 3, True, [3]),
+            (1, 2, 1, 3, 6, 2, True, None),      # Lq < Lk
+            (2, 2, 1, 6, 3, 2, True, [3, 2])]:   # Lq > Lk: late queries see every key
+        q, k, v = rand((B, Hq, Lq, D), rng), rand((B, Hkv, Lk, D), rng), rand((B, Hkv, Lk, D), rng)
+        do = rand((B, Hq, Lq, D), rng)
         got = bwd(q, k, v, do, 0.8, causal=causal, valid_len=vl)
         ref = finite_differences(q, k, v, do, 0.8, causal, vl)
         for g, r in zip(got, ref):
@@ -84,10 +88,13 @@ def pin_finite_differences(bwd):
 
 def pin_torch_autograd(bwd):
     rng = np.random.default_rng(12)
-    for (B, Hq, Hkv, L, D, causal, vl) in [(2, 4, 2, 23, 8, True, [23, 9]), (1, 6, 3, 31, 16, False, None),
-                                           (3, 2, 1, 17, 4, True, [0, 17, 5])]:
-        q, k, v = rand((B, Hq, L, D), rng, 1.5), rand((B, Hkv, L, D), rng), rand((B, Hkv, L, D), rng)
-        do = rand((B, Hq, L, D), rng)
+    for (B, Hq, Hkv, Lq, Lk, D, causal, vl) in [
+            (2, 4, 2, 23, 23, 8, True, [23, 9]), (1, 6, 3, 31, 31, 16, False, None),
+            (3, 2, 1, 17, 17, 4, True, [0, 17, 5]),
+            (2, 4, 2, 19, 27, 8, True, [27, 9]), (1, 2, 1, 29, 12, 4, True, None),
+            (2, 2, 2, 9, 21, 6, False, [21, 4])]:
+        q, k, v = rand((B, Hq, Lq, D), rng, 1.5), rand((B, Hkv, Lk, D), rng), rand((B, Hkv, Lk, D), rng)
+        do = rand((B, Hq, Lq, D), rng)
         sm = 1.0 / math.sqrt(D)
         got = bwd(q, k, v, do, sm, causal=causal, valid_len=vl)
         ref = torch_grads(q, k, v, do, sm, causal, vl)

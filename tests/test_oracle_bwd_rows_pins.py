@@ -17,29 +17,31 @@ import pytest
 
 import oracle
 
-CASES = [  # B, Hq, Hkv, L, D, causal, valid_len
-    (2, 4, 2, 37, 8, True, [37, 11]),
-    (1, 6, 3, 29, 5, False, None),
-    (2, 4, 1, 23, 4, True, [0, 23]),
-    (3, 2, 2, 19, 6, False, [5, 19, 1]),
+CASES = [  # B, Hq, Hkv, Lq, Lk, D, causal, valid_len
+    (2, 4, 2, 37, 37, 8, True, [37, 11]),
+    (1, 6, 3, 29, 29, 5, False, None),
+    (2, 4, 1, 23, 23, 4, True, [0, 23]),
+    (3, 2, 2, 19, 19, 6, False, [5, 19, 1]),
+    (2, 4, 2, 17, 31, 8, True, [31, 6]),
+    (1, 2, 1, 33, 14, 4, True, None),
 ]
 
 
 def inputs(case, seed):
-    B, Hq, Hkv, L, D, causal, vl = case
+    B, Hq, Hkv, Lq, Lk, D, causal, vl = case
     rng = np.random.default_rng(seed)
-    return (rng.standard_normal((B, Hq, L, D)), rng.standard_normal((B, Hkv, L, D)),
-            rng.standard_normal((B, Hkv, L, D)), rng.standard_normal((B, Hq, L, D)))
+    return (rng.standard_normal((B, Hq, Lq, D)), rng.standard_normal((B, Hkv, Lk, D)),
+            rng.standard_normal((B, Hkv, Lk, D)), rng.standard_normal((B, Hq, Lq, D)))
 
 
 def pin_rows_match_full(rows_fn):
     for n, case in enumerate(CASES):
-        B, Hq, Hkv, L, D, causal, vl = case
+        B, Hq, Hkv, Lq, Lk, D, causal, vl = case
         q, k, v, do = inputs(case, 40 + n)
         dq, dk, dv = oracle.attn_bwd_f64(q, k, v, do, 0.6, causal=causal, valid_len=vl)
         rng = np.random.default_rng(n)
-        qr = rng.permutation(B * Hq * L)
-        kr = rng.permutation(B * Hkv * L)
+        qr = rng.permutation(B * Hq * Lq)
+        kr = rng.permutation(B * Hkv * Lk)
         dq2, _, dk2, dv2, _ = rows_fn(q, k, v, do, 0.6, causal=causal, valid_len=vl, q_rows=qr,
                                       k_rows=kr)
         np.testing.assert_allclose(dq2, dq.reshape(-1, D)[qr], rtol=1e-11, atol=1e-12)
@@ -48,14 +50,15 @@ def pin_rows_match_full(rows_fn):
 
 
 def brute_magnitudes(q, k, v, do, sm, causal, vl):
-    B, Hq, L, D = q.shape
+    B, Hq, Lq, D = q.shape
+    Lk = k.shape[2]
     G = Hq // k.shape[1]
-    qm = np.zeros((B, Hq, L, 3))
-    km = np.zeros((B, k.shape[1], L, 4))
+    qm = np.zeros((B, Hq, Lq, 3))
+    km = np.zeros((B, k.shape[1], Lk, 4))
     for b in range(B):
-        vis = np.ones((L, L), dtype=bool)
+        vis = np.ones((Lq, Lk), dtype=bool)
         if causal:
-            vis &= np.tri(L, dtype=bool)
+            vis &= np.tri(Lq, Lk, dtype=bool)
         if vl is not None:
             vis[:, vl[b]:] = False
         for h in range(Hq):
@@ -80,10 +83,10 @@ def brute_magnitudes(q, k, v, do, sm, causal, vl):
 
 def pin_magnitudes(rows_fn):
     for n, case in enumerate(CASES):
-        B, Hq, Hkv, L, D, causal, vl = case
+        B, Hq, Hkv, Lq, Lk, D, causal, vl = case
         q, k, v, do = inputs(case, 60 + n)
         _, qm, _, _, km = rows_fn(q, k, v, do, 0.6, causal=causal, valid_len=vl,
-                                  q_rows=np.arange(B * Hq * L), k_rows=np.arange(B * Hkv * L))
+                                  q_rows=np.arange(B * Hq * Lq), k_rows=np.arange(B * Hkv * Lk))
         qm_ref, km_ref = brute_magnitudes(q, k, v, do, 0.6, causal, vl)
         qm_ref[qm_ref[:, 2] == 0, :2] = 0.0  # rows with no key: no dS, O = 0
         np.testing.assert_allclose(qm, qm_ref, rtol=1e-11, atol=1e-12)
@@ -108,8 +111,8 @@ def test_bwd_rows_rejects_out_of_range_rows():
 
 MUTANTS = {
     "delta_dropped": ("const double ds = p * (dp - st[4 * gi + 2]);", "const double ds = p * dp;"),
-    "wrong_query_head": ("const int64_t qrow = ((int64_t)b * Hq + (int64_t)h_kv * G + gi / L) * L + i;",
-                         "const int64_t qrow = ((int64_t)b * Hq + gi / L) * L + i;"),
+    "wrong_query_head": ("const int64_t qrow = ((int64_t)b * Hq + (int64_t)h_kv * G + gi / Lq) * Lq + i;",
+                         "const int64_t qrow = ((int64_t)b * Hq + gi / Lq) * Lq + i;"),
     "p_not_normalised": ("const double p = exp(sm_scale * dot - st[4 * gi]) / st[4 * gi + 1];",
                          "const double p = exp(sm_scale * dot - st[4 * gi]);"),
     "dq_wrong_kv_head": ("const int64_t kvh = (int64_t)b * Hkv + (qh % Hq) / G;",
