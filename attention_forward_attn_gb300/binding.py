@@ -101,7 +101,7 @@ def load():
             lib.attn_bwd_simt.argtypes = lib.attn_bwd.argtypes
             lib.attn_bwd_simt.restype = i
             lib.attn_bwd_strided.argtypes = [p, sp, p, sp, p, sp, p, sp, p, sp, p, p, sp, p, sp, p,
-                                             sp, i, i, i, i, i, ctypes.c_float, i, p, i, p]
+                                             sp, i, i, i, i, i, i, ctypes.c_float, i, p, i, p]
             lib.attn_bwd_strided.restype = i
             lib.attn_fwd_f32.argtypes = [p, p, p, p, p, i, i, i, i, ctypes.c_float, i, p, i, p]
             lib.attn_fwd_f32.restype = i
@@ -442,8 +442,8 @@ def attn_bwd(q, k, v, o, lse, do, *, causal=False, sm_scale=None, valid_len=None
              impl="tc", dq=None, dk=None, dv=None):
     """Gradients (dq, dk, dv) of attn_fwd for the output gradient ``do``.
 
-    impl="tc": attn_bwd_strided (tensor cores).  q, o, do: [B, Hq, L, D]; k, v:
-    [B, Hkv, L, D] -- fp16 or bf16 CUDA views whose last dimension is
+    impl="tc": attn_bwd_strided (tensor cores).  q, o, do: [B, Hq, Lq, D]; k, v:
+    [B, Hkv, Lk, D] (Lq may differ from Lk) -- fp16 or bf16 CUDA views whose last dimension is
     contiguous and whose other strides are multiples of 8 elements (e.g.
     ``x.transpose(1, 2)`` of [B, L, H, D] tensors); dq, dk, dv: optional
     output views of the same shapes (default: new contiguous tensors).
@@ -459,7 +459,9 @@ def attn_bwd(q, k, v, o, lse, do, *, causal=False, sm_scale=None, valid_len=None
         if impl == "simt" and not t.is_contiguous():
             raise ValueError("impl='simt' takes contiguous tensors (%s is not)" % name)
     B, Hq, L, D = q.shape
-    Hkv = k.shape[1]
+    Hkv, Lk = k.shape[1], k.shape[2]
+    if impl == "simt" and Lk != L:
+        raise ValueError("impl='simt' takes equal query and key lengths")
     if sm_scale is None:
         sm_scale = 1.0 / float(D) ** 0.5
     dq = torch.empty_like(q, memory_format=torch.contiguous_format) if dq is None else dq
@@ -480,7 +482,7 @@ def attn_bwd(q, k, v, o, lse, do, *, causal=False, sm_scale=None, valid_len=None
         st = int(load().attn_bwd_strided(
             q.data_ptr(), st3(q), k.data_ptr(), st3(k), v.data_ptr(), st3(v), o.data_ptr(), st3(o),
             do.data_ptr(), st3(do), lse.data_ptr(), dq.data_ptr(), st3(dq), dk.data_ptr(), st3(dk),
-            dv.data_ptr(), st3(dv), B, Hq, Hkv, L, D, float(sm_scale), int(bool(causal)), vl_ptr,
+            dv.data_ptr(), st3(dv), B, Hq, Hkv, L, Lk, D, float(sm_scale), int(bool(causal)), vl_ptr,
             _dtype_code(q), _stream_handle(stream)))
     else:
         name = "attn_bwd_simt"

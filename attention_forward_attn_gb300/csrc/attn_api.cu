@@ -474,18 +474,19 @@ namespace {
 // Arguments shared by the two backward entry points.
 attn_status_t bwd_validate(const void* q, const void* k, const void* v, const void* o,
                            const void* dO, const float* lse, void* dq, void* dk, void* dv, int B,
-                           int Hq, int Hkv, int L, int D, float sm_scale, int causal,
+                           int Hq, int Hkv, int Lq, int Lk, int D, float sm_scale, int causal,
                            const int32_t* valid_len, attn_dtype_t dtype, bool small_d) {
   if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_DTYPE;
   if (q == nullptr || k == nullptr || v == nullptr || o == nullptr || dO == nullptr ||
       lse == nullptr || dq == nullptr || dk == nullptr || dv == nullptr)
     return ATTN_ERR_NULL;
-  if (B < 1 || Hq < 1 || Hkv < 1 || L < 1) return ATTN_ERR_SHAPE;
+  if (B < 1 || Hq < 1 || Hkv < 1 || Lq < 1 || Lk < 1) return ATTN_ERR_SHAPE;
   if (D != 64 && D != 128 && !(small_d && (D == 16 || D == 32))) return ATTN_ERR_HEADDIM;
   if (Hq % Hkv != 0) return ATTN_ERR_HEADS;
   if (causal != 0 && causal != 1) return ATTN_ERR_ARG;
   if (!(sm_scale >= 0.f) || isinf(sm_scale)) return ATTN_ERR_SCALE;
-  if (static_cast<int64_t>(B) * Hq * L > INT32_MAX || static_cast<int64_t>(B) * Hq > 65535)
+  if (static_cast<int64_t>(B) * Hq * Lq > INT32_MAX || static_cast<int64_t>(B) * Hkv * Lk > INT32_MAX ||
+      static_cast<int64_t>(B) * Hq > 65535)
     return ATTN_ERR_SHAPE;
   const void* p16[] = {q, k, v, o, dO, dq, dk, dv};  // TMA bases, 16-byte vector loads and stores
   for (const void* ptr : p16)
@@ -503,45 +504,46 @@ attn_status_t attn_bwd_strided(const void* q, const attn_strides_t* q_strides, c
                                const attn_strides_t* do_strides, const float* lse, void* dq,
                                const attn_strides_t* dq_strides, void* dk,
                                const attn_strides_t* dk_strides, void* dv,
-                               const attn_strides_t* dv_strides, int B, int Hq, int Hkv, int L,
-                               int D, float sm_scale, int causal, const int32_t* valid_len,
-                               attn_dtype_t dtype, attn_stream_t stream) {
-  attn_status_t s = bwd_validate(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, L, D, sm_scale,
+                               const attn_strides_t* dv_strides, int B, int Hq, int Hkv, int Lq,
+                               int Lk, int D, float sm_scale, int causal,
+                               const int32_t* valid_len, attn_dtype_t dtype,
+                               attn_stream_t stream) {
+  attn_status_t s = bwd_validate(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, Lq, Lk, D, sm_scale,
                                  causal, valid_len, dtype, true);
   if (s != ATTN_OK) return s;
   attn::Strides sq, sk, sv, so, sdo, sdq, sdk, sdv;
-  if ((s = strides_of(q_strides, B, Hq, L, D, &sq)) != ATTN_OK ||
-      (s = strides_of(k_strides, B, Hkv, L, D, &sk)) != ATTN_OK ||
-      (s = strides_of(v_strides, B, Hkv, L, D, &sv)) != ATTN_OK ||
-      (s = strides_of(o_strides, B, Hq, L, D, &so)) != ATTN_OK ||
-      (s = strides_of(do_strides, B, Hq, L, D, &sdo)) != ATTN_OK ||
-      (s = strides_of(dq_strides, B, Hq, L, D, &sdq)) != ATTN_OK ||
-      (s = strides_of(dk_strides, B, Hkv, L, D, &sdk)) != ATTN_OK ||
-      (s = strides_of(dv_strides, B, Hkv, L, D, &sdv)) != ATTN_OK)
+  if ((s = strides_of(q_strides, B, Hq, Lq, D, &sq)) != ATTN_OK ||
+      (s = strides_of(k_strides, B, Hkv, Lk, D, &sk)) != ATTN_OK ||
+      (s = strides_of(v_strides, B, Hkv, Lk, D, &sv)) != ATTN_OK ||
+      (s = strides_of(o_strides, B, Hq, Lq, D, &so)) != ATTN_OK ||
+      (s = strides_of(do_strides, B, Hq, Lq, D, &sdo)) != ATTN_OK ||
+      (s = strides_of(dq_strides, B, Hq, Lq, D, &sdq)) != ATTN_OK ||
+      (s = strides_of(dk_strides, B, Hkv, Lk, D, &sdk)) != ATTN_OK ||
+      (s = strides_of(dv_strides, B, Hkv, Lk, D, &sdv)) != ATTN_OK)
     return s;
-  if (!no_self_overlap(sdq, B, Hq, L, D) || !no_self_overlap(sdk, B, Hkv, L, D) ||
-      !no_self_overlap(sdv, B, Hkv, L, D))
+  if (!no_self_overlap(sdq, B, Hq, Lq, D) || !no_self_overlap(sdk, B, Hkv, Lk, D) ||
+      !no_self_overlap(sdv, B, Hkv, Lk, D))
     return ATTN_ERR_STRIDE;
   int dev = 0;
   DeviceState* st = nullptr;
   if ((s = device_state(&dev, &st)) != ATTN_OK) return s;
   const bool bf16 = dtype == ATTN_BF16;
   CUtensorMap maps[4];
-  if ((s = encode_map(&maps[0], q, B, Hq, L, D, sq, 128, bf16)) != ATTN_OK ||
-      (s = encode_map(&maps[1], k, B, Hkv, L, D, sk, 128, bf16)) != ATTN_OK ||
-      (s = encode_map(&maps[2], v, B, Hkv, L, D, sv, 128, bf16)) != ATTN_OK ||
-      (s = encode_map(&maps[3], dO, B, Hq, L, D, sdo, 128, bf16)) != ATTN_OK)
+  if ((s = encode_map(&maps[0], q, B, Hq, Lq, D, sq, 128, bf16)) != ATTN_OK ||
+      (s = encode_map(&maps[1], k, B, Hkv, Lk, D, sk, 128, bf16)) != ATTN_OK ||
+      (s = encode_map(&maps[2], v, B, Hkv, Lk, D, sv, 128, bf16)) != ATTN_OK ||
+      (s = encode_map(&maps[3], dO, B, Hq, Lq, D, sdo, 128, bf16)) != ATTN_OK)
     return s;
   cudaMemPool_t pool = nullptr;
   if ((s = workspace_pool(dev, st, &pool)) != ATTN_OK) return s;
   const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   void* ws = nullptr;
   cudaError_t e = cudaMallocFromPoolAsync(
-      &ws, static_cast<size_t>(attn::bwd_tc_workspace_bytes(B, Hq, Hkv, L, D, st->num_sms)), pool,
-      cs);
+      &ws, static_cast<size_t>(attn::bwd_tc_workspace_bytes(B, Hq, Hkv, Lq, Lk, D, st->num_sms)),
+      pool, cs);
   if (e != cudaSuccess) return cuda_fail(e);
-  e = attn::launch_bwd_tc(maps, o, so, dO, sdo, lse, dq, sdq, dk, sdk, dv, sdv, ws, B, Hq, Hkv, L,
-                          D, sm_scale, causal, valid_len, bf16, st->num_sms, st->status, cs);
+  e = attn::launch_bwd_tc(maps, o, so, dO, sdo, lse, dq, sdq, dk, sdk, dv, sdv, ws, B, Hq, Hkv, Lq,
+                          Lk, D, sm_scale, causal, valid_len, bf16, st->num_sms, st->status, cs);
   const cudaError_t ef = cudaFreeAsync(ws, cs);
   if (e == cudaSuccess) e = ef;
   if (e != cudaSuccess) return cuda_fail(e);
@@ -553,7 +555,7 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
                        int L, int D, float sm_scale, int causal, const int32_t* valid_len,
                        attn_dtype_t dtype, attn_stream_t stream) {
   return attn_bwd_strided(q, nullptr, k, nullptr, v, nullptr, o, nullptr, dO, nullptr, lse, dq,
-                          nullptr, dk, nullptr, dv, nullptr, B, Hq, Hkv, L, D, sm_scale, causal,
+                          nullptr, dk, nullptr, dv, nullptr, B, Hq, Hkv, L, L, D, sm_scale, causal,
                           valid_len, dtype, stream);
 }
 
@@ -561,7 +563,7 @@ attn_status_t attn_bwd_simt(const void* q, const void* k, const void* v, const v
                             const void* dO, const float* lse, void* dq, void* dk, void* dv, int B,
                             int Hq, int Hkv, int L, int D, float sm_scale, int causal,
                             const int32_t* valid_len, attn_dtype_t dtype, attn_stream_t stream) {
-  attn_status_t s = bwd_validate(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, L, D, sm_scale,
+  attn_status_t s = bwd_validate(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, L, L, D, sm_scale,
                                  causal, valid_len, dtype, false);
   if (s != ATTN_OK) return s;
   int dev = 0;

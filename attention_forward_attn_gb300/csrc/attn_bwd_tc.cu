@@ -76,7 +76,10 @@ struct BwdTcParams {
   void* dv;
   const int32_t* valid_len;
   int* status;
-  int B, Hq, Hkv, L, Lp, G, n_t;  // n_t = tiles of 128 rows, Lp = 128 n_t
+  int B, Hq, Hkv, G;
+  int Lq, Lk;      // query and key lengths
+  int n_tq, n_tk;  // 128-row query tiles, 128-key tiles
+  int Lqp;         // 128 n_tq: rows of the -LSE log2(e) and delta arrays
   int dg;                         // head dimension in memory: D, or 16 / 32 on the D = 64 kernels
   Strides sdq, sdk, sdv;          // element strides (batch, head, row) of the outputs
   int splits;                     // CTAs per key tile of the dK/dV kernel (see bwd_tc_splits)
@@ -246,9 +249,9 @@ __device__ __forceinline__ uint32_t pk2(float lo, float hi) {
 }
 
 __device__ __forceinline__ int kv_len_of(const BwdTcParams& p, int b) {
-  if (p.valid_len == nullptr) return p.L;
+  if (p.valid_len == nullptr) return p.Lk;
   const int vl = p.valid_len[b];
-  return vl < 0 ? 0 : (vl > p.L ? p.L : vl);
+  return vl < 0 ? 0 : (vl > p.Lk ? p.Lk : vl);
 }
 
 // ------------------------------------------------------------------ pre-pass
@@ -347,7 +350,7 @@ __device__ __forceinline__ KvUnit kv_unit(const BwdTcParams& p) {
   w.hkv = z - w.b * p.Hkv;
   w.kv_len = kv_len_of(p, w.b);
   w.m_lo = p.causal ? w.n : 0;
-  const int total = (w.n * T < w.kv_len) ? p.G * (p.n_t - w.m_lo) : 0;
+  const int total = (w.n * T < w.kv_len && w.m_lo < p.n_tq) ? p.G * (p.n_tq - w.m_lo) : 0;
   if constexpr (SPLIT) {
     const int chunk = (total + splits - 1) / splits;
     w.t0 = min(total, w.s * chunk);
@@ -392,7 +395,7 @@ __device__ void dkv_producer(const BwdTcParams& p, const KvUnit& w, const BBars&
       ptx::tma_load_4d_hint(st + C::kTile + h * C::kSlab, tm_do, full, h * 64, mi * T, hq, w.b,
                             pol_keep);
     }
-    const int64_t row = (static_cast<int64_t>(w.b) * p.Hq + hq) * p.Lp + static_cast<int64_t>(mi) * T;
+    const int64_t row = (static_cast<int64_t>(w.b) * p.Hq + hq) * p.Lqp + static_cast<int64_t>(mi) * T;
     bulk_load(st + 2 * C::kTile, p.nlse2 + row, T * 4, full);
     bulk_load(st + 2 * C::kTile + T * 4, p.delta + row, T * 4, full);
   }
@@ -609,13 +612,13 @@ __device__ void dkv_elementwise(const BwdTcParams& p, const KvUnit& w, const BBa
   const bool is_dk = grp >= kGroups / 2;
   const int c_lo = (grp % (kGroups / 2)) * kPart;
   const int j = w.n * T + row;
-  const int nv = j < p.L ? cols_in(p.dg, c_lo, kPart) : 0;  // columns this thread stores
+  const int nv = j < p.Lk ? cols_in(p.dg, c_lo, kPart) : 0;  // columns this thread stores
   const Strides& so = is_dk ? p.sdk : p.sdv;
   uint16_t* dst = static_cast<uint16_t*>(is_dk ? p.dk : p.dv) + w.b * so.b + w.hkv * so.h +
                   static_cast<int64_t>(j) * so.l + c_lo;
   // split key tiles: unscaled fp32 partial rows, summed by bwd_dkv_reduce_kernel
-  float* part = p.part + ((static_cast<int64_t>(w.s) * 2 + (is_dk ? 1 : 0)) * p.B * p.Hkv * p.L +
-                          (static_cast<int64_t>(w.b) * p.Hkv + w.hkv) * p.L + j) * p.dg + c_lo;
+  float* part = p.part + ((static_cast<int64_t>(w.s) * 2 + (is_dk ? 1 : 0)) * p.B * p.Hkv * p.Lk +
+                          (static_cast<int64_t>(w.b) * p.Hkv + w.hkv) * p.Lk + j) * p.dg + c_lo;
   constexpr bool split = SPLIT;
   if (w.steps == 0) {  // no query sees these keys (in this split)
     for (int c = 0; c < nv / 8; ++c) {
@@ -654,7 +657,7 @@ __device__ void dkv_elementwise(const BwdTcParams& p, const KvUnit& w, const BBa
 // the input dtype.  One thread per 8 consecutive elements of a row.
 template <bool BF16>
 __global__ void __launch_bounds__(256) bwd_dkv_reduce_kernel(const BwdTcParams p) {
-  const int64_t rows = static_cast<int64_t>(p.B) * p.Hkv * p.L;
+  const int64_t rows = static_cast<int64_t>(p.B) * p.Hkv * p.Lk;
   const int64_t per_row = p.dg / 8;
   const int64_t v = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x;
   if (v >= 2 * rows * per_row) return;
@@ -673,8 +676,8 @@ __global__ void __launch_bounds__(256) bwd_dkv_reduce_kernel(const BwdTcParams p
     acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
   }
   const float mul = which ? p.sm_scale : 1.f;
-  const int64_t z = row / p.L;  // b * Hkv + h_kv
-  const int64_t j = row - z * p.L;
+  const int64_t z = row / p.Lk;  // b * Hkv + h_kv
+  const int64_t j = row - z * p.Lk;
   const int64_t sb = which ? p.sdk.b : p.sdv.b;
   const int64_t sh = which ? p.sdk.h : p.sdv.h;
   const int64_t sl = which ? p.sdk.l : p.sdv.l;
@@ -709,7 +712,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     ptx::fence_barrier_init();
     if (p.valid_len != nullptr && w.n == 0 && w.hkv == 0) {
       const int vl = p.valid_len[w.b];
-      if (vl < 0 || vl > p.L) atomicOr(p.status, kStatusValidLenClamped);
+      if (vl < 0 || vl > p.Lk) atomicOr(p.status, kStatusValidLenClamped);
     }
   }
   if (warp == kLoadWarp && lane == 0) {
@@ -771,13 +774,13 @@ __device__ __forceinline__ QUnit q_unit(const BwdTcParams& p) {
   const int u = static_cast<int>(blockIdx.x) / per;
   const int z = static_cast<int>(blockIdx.x) - u * per;
   QUnit w;
-  w.m = p.n_t - 1 - u;
+  w.m = p.n_tq - 1 - u;
   w.b = z / p.Hq;
   w.hq = z - w.b * p.Hq;
   w.hkv = w.hq / p.G;
   w.kv_len = kv_len_of(p, w.b);
   const int kt = (w.kv_len + T - 1) / T;
-  w.steps = min(p.causal ? w.m + 1 : p.n_t, kt);
+  w.steps = min(p.causal ? min(w.m + 1, p.n_tk) : p.n_tk, kt);
   return w;
 }
 
@@ -902,7 +905,7 @@ __device__ void dq_elementwise(const BwdTcParams& p, const QUnit& w, const BBars
   const uint32_t t_s = tmem + lane_addr + C::kColS + grp * TH;
   const uint32_t t_dp = tmem + lane_addr + C::kColDP + grp * TH;
   const uint32_t t_ds = tmem + lane_addr + C::kColAcc1 + grp * (TH / 2);  // + (j % 2) * 64
-  const int64_t g_row = (static_cast<int64_t>(w.b) * p.Hq + w.hq) * p.Lp + static_cast<int64_t>(w.m) * T + row;
+  const int64_t g_row = (static_cast<int64_t>(w.b) * p.Hq + w.hq) * p.Lqp + static_cast<int64_t>(w.m) * T + row;
   const float nl = w.steps > 0 ? p.nlse2[g_row] : 0.f;
   const float dl = w.steps > 0 ? p.delta[g_row] : 0.f;
   const uint64_t sc2 = ptx::f2_pack(p.scale_log2, p.scale_log2);
@@ -966,7 +969,7 @@ __device__ void dq_elementwise(const BwdTcParams& p, const QUnit& w, const BBars
   constexpr int kPart = D / kEpi;
   if (!ok || grp >= kEpi) return;
   const int i = w.m * T + row;
-  const int nv = i < p.L ? cols_in(p.dg, grp * kPart, kPart) : 0;  // columns this thread stores
+  const int nv = i < p.Lq ? cols_in(p.dg, grp * kPart, kPart) : 0;  // columns this thread stores
   uint16_t* dst = static_cast<uint16_t*>(p.dq) + w.b * p.sdq.b + w.hq * p.sdq.h +
                   static_cast<int64_t>(i) * p.sdq.l + grp * kPart;
   if (w.steps == 0) {  // no visible key: dQ = 0
@@ -1037,10 +1040,10 @@ template <int DR, bool BF16>
 void launch_prep(const BwdTcParams& p, const void* o, const Strides& so, const void* dO,
                  const Strides& sdo, const float* lse, float* nlse2, float* delta,
                  cudaStream_t stream) {
-  const int64_t rows = static_cast<int64_t>(p.B) * p.Hq * p.Lp;
+  const int64_t rows = static_cast<int64_t>(p.B) * p.Hq * p.Lqp;
   constexpr int kRowsPerBlock = 8 * (32 / (DR / 8));
   bwd_tc_prep_kernel<DR, BF16><<<static_cast<unsigned>((rows + kRowsPerBlock - 1) / kRowsPerBlock),
-                                 256, 0, stream>>>(o, dO, lse, nlse2, delta, p.Hq, p.L, p.Lp, rows,
+                                 256, 0, stream>>>(o, dO, lse, nlse2, delta, p.Hq, p.Lq, p.Lqp, rows,
                                                    so, sdo);
 }
 
@@ -1064,17 +1067,17 @@ cudaError_t launch_bwd_tc_d(const CUtensorMap (&maps)[4], const BwdTcParams& p, 
     e = cudaFuncSetAttribute(bwd_dq_tc_kernel<D, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::qSmem);
   if (e != cudaSuccess) return e;
-  dkv<<<static_cast<unsigned>(p.n_t * p.B * p.Hkv * p.splits), kThreadsB, C::kvSmem, stream>>>(
+  dkv<<<static_cast<unsigned>(p.n_tk * p.B * p.Hkv * p.splits), kThreadsB, C::kvSmem, stream>>>(
       maps[0], maps[1], maps[2], maps[3], p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (p.splits > 1) {
-    const int64_t vecs = 2 * static_cast<int64_t>(p.B) * p.Hkv * p.L * (p.dg / 8);
+    const int64_t vecs = 2 * static_cast<int64_t>(p.B) * p.Hkv * p.Lk * (p.dg / 8);
     bwd_dkv_reduce_kernel<BF16><<<static_cast<unsigned>((vecs + 255) / 256), 256, 0, stream>>>(p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  bwd_dq_tc_kernel<D, BF16><<<static_cast<unsigned>(p.n_t * p.B * p.Hq), kThreadsB, C::qSmem, stream>>>(
+  bwd_dq_tc_kernel<D, BF16><<<static_cast<unsigned>(p.n_tq * p.B * p.Hq), kThreadsB, C::qSmem, stream>>>(
       maps[0], maps[1], maps[2], maps[3], p);
   return cudaGetLastError();
 }
@@ -1085,37 +1088,40 @@ cudaError_t launch_bwd_tc_d(const CUtensorMap (&maps)[4], const BwdTcParams& p, 
 // alone fill four waves of the GPU, else enough splits of each key tile's
 // steps to do so (at most 16) -- with few K/V heads (MQA), one CTA per key
 // tile would run every query head of the group and leave SMs idle.
-int bwd_tc_splits(int B, int Hkv, int L, int num_sms) {
-  const int64_t units = static_cast<int64_t>((L + T - 1) / T) * B * Hkv;
+int bwd_tc_splits(int B, int Hkv, int Lk, int num_sms) {
+  const int64_t units = static_cast<int64_t>((Lk + T - 1) / T) * B * Hkv;
   const int64_t target = 4 * static_cast<int64_t>(num_sms > 0 ? num_sms : 1);
   if (units >= target) return 1;
   const int64_t s = (target + units - 1) / units;
   return static_cast<int>(s < 16 ? s : 16);
 }
 
-int64_t bwd_tc_workspace_bytes(int B, int Hq, int Hkv, int L, int D, int num_sms) {
-  const int64_t lp = (static_cast<int64_t>(L) + T - 1) / T * T;
-  const int splits = bwd_tc_splits(B, Hkv, L, num_sms);
-  const int64_t part = splits > 1 ? static_cast<int64_t>(splits) * 2 * B * Hkv * L * D * 4 : 0;
-  return 2 * static_cast<int64_t>(B) * Hq * lp * 4 + part;
+int64_t bwd_tc_workspace_bytes(int B, int Hq, int Hkv, int Lq, int Lk, int D, int num_sms) {
+  const int64_t lqp = (static_cast<int64_t>(Lq) + T - 1) / T * T;
+  const int splits = bwd_tc_splits(B, Hkv, Lk, num_sms);
+  const int64_t part = splits > 1 ? static_cast<int64_t>(splits) * 2 * B * Hkv * Lk * D * 4 : 0;
+  return 2 * static_cast<int64_t>(B) * Hq * lqp * 4 + part;
 }
 
 cudaError_t launch_bwd_tc(const CUtensorMap (&maps)[4], const void* o, const Strides& so,
                           const void* dO, const Strides& sdo, const float* lse, void* dq,
                           const Strides& sdq, void* dk, const Strides& sdk, void* dv,
-                          const Strides& sdv, void* workspace, int B, int Hq, int Hkv, int L, int D,
-                          float sm_scale, int causal, const int32_t* valid_len, bool bf16,
-                          int num_sms, int* status, cudaStream_t stream) {
+                          const Strides& sdv, void* workspace, int B, int Hq, int Hkv, int Lq,
+                          int Lk, int D, float sm_scale, int causal, const int32_t* valid_len,
+                          bool bf16, int num_sms, int* status, cudaStream_t stream) {
   BwdTcParams p;
-  p.splits = bwd_tc_splits(B, Hkv, L, num_sms);
+  p.splits = bwd_tc_splits(B, Hkv, Lk, num_sms);
   p.sdq = sdq;
   p.sdk = sdk;
   p.sdv = sdv;
-  p.n_t = (L + T - 1) / T;
-  p.Lp = p.n_t * T;
+  p.Lq = Lq;
+  p.Lk = Lk;
+  p.n_tq = (Lq + T - 1) / T;
+  p.n_tk = (Lk + T - 1) / T;
+  p.Lqp = p.n_tq * T;
   float* nlse2 = static_cast<float*>(workspace);
-  float* delta = nlse2 + static_cast<int64_t>(B) * Hq * p.Lp;
-  p.part = delta + static_cast<int64_t>(B) * Hq * p.Lp;  // used when splits > 1
+  float* delta = nlse2 + static_cast<int64_t>(B) * Hq * p.Lqp;
+  p.part = delta + static_cast<int64_t>(B) * Hq * p.Lqp;  // used when splits > 1
   p.nlse2 = nlse2;
   p.delta = delta;
   p.dq = dq;
@@ -1126,7 +1132,6 @@ cudaError_t launch_bwd_tc(const CUtensorMap (&maps)[4], const void* o, const Str
   p.B = B;
   p.Hq = Hq;
   p.Hkv = Hkv;
-  p.L = L;
   p.G = Hq / Hkv;
   p.scale_log2 = sm_scale * kLog2e;
   p.sm_scale = sm_scale;

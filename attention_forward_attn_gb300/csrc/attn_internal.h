@@ -113,14 +113,14 @@ cudaError_t launch_bwd(const void* q, const void* k, const void* v, const void* 
 // pre-pass); sdq, sdk, sdv: of the outputs.  D 16, 32, 64 or 128.  With few
 // key tiles per SM the dK/dV kernel splits each key tile over several CTAs
 // (bwd_tc_splits) and the workspace also holds their fp32 partial sums.
-int bwd_tc_splits(int B, int Hkv, int L, int num_sms);
-int64_t bwd_tc_workspace_bytes(int B, int Hq, int Hkv, int L, int D, int num_sms);
+int bwd_tc_splits(int B, int Hkv, int Lk, int num_sms);
+int64_t bwd_tc_workspace_bytes(int B, int Hq, int Hkv, int Lq, int Lk, int D, int num_sms);
 cudaError_t launch_bwd_tc(const CUtensorMap (&maps)[4], const void* o, const Strides& so,
                           const void* dO, const Strides& sdo, const float* lse, void* dq,
                           const Strides& sdq, void* dk, const Strides& sdk, void* dv,
-                          const Strides& sdv, void* workspace, int B, int Hq, int Hkv, int L, int D,
-                          float sm_scale, int causal, const int32_t* valid_len, bool bf16,
-                          int num_sms, int* status, cudaStream_t stream);
+                          const Strides& sdv, void* workspace, int B, int Hq, int Hkv, int Lq,
+                          int Lk, int D, float sm_scale, int causal, const int32_t* valid_len,
+                          bool bf16, int num_sms, int* status, cudaStream_t stream);
 
 // SIMT cross-check forward.
 cudaError_t launch_simt(const Problem& p);

@@ -253,12 +253,15 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
                        attn_dtype_t dtype, attn_stream_t stream);
 
 /*
- * attn_bwd_strided -- attn_bwd on strided operands: each of q, k, v, o, dO,
- * dq, dk and dv takes an attn_strides_t (NULL: contiguous [B, H, L, D]) with
- * the rules of attn_fwd_strided (positive multiples of 8 elements below
- * 2^39; the stride of an extent-1 dimension is ignored; rows of D elements
- * contiguous).  dq, dk and dv must not overlap themselves (ATTN_ERR_STRIDE).
- * Everything else as attn_bwd, which is this call with every stride NULL.
+ * attn_bwd_strided -- attn_bwd on strided operands with separate query and
+ * key lengths: q, o, dO, dq are [B, Hq, Lq, D], k, v, dk, dv [B, Hkv, Lk, D],
+ * lse [B*Hq, Lq]; the masks as in attn_fwd_strided (causal keeps key j <= query
+ * i, valid_len clamped to [0, Lk]).  Each of q, k, v, o, dO, dq, dk and dv
+ * takes an attn_strides_t (NULL: contiguous) with the rules of
+ * attn_fwd_strided (positive multiples of 8 elements below 2^39; the stride of
+ * an extent-1 dimension is ignored; rows of D elements contiguous).  dq, dk
+ * and dv must not overlap themselves (ATTN_ERR_STRIDE).  Everything else as
+ * attn_bwd, which is this call with Lq = Lk = L and every stride NULL.
  */
 attn_status_t attn_bwd_strided(const void* q, const attn_strides_t* q_strides, const void* k,
                                const attn_strides_t* k_strides, const void* v,
@@ -267,9 +270,10 @@ attn_status_t attn_bwd_strided(const void* q, const attn_strides_t* q_strides, c
                                const attn_strides_t* do_strides, const float* lse, void* dq,
                                const attn_strides_t* dq_strides, void* dk,
                                const attn_strides_t* dk_strides, void* dv,
-                               const attn_strides_t* dv_strides, int B, int Hq, int Hkv, int L,
-                               int D, float sm_scale, int causal, const int32_t* valid_len,
-                               attn_dtype_t dtype, attn_stream_t stream);
+                               const attn_strides_t* dv_strides, int B, int Hq, int Hkv, int Lq,
+                               int Lk, int D, float sm_scale, int causal,
+                               const int32_t* valid_len, attn_dtype_t dtype,
+                               attn_stream_t stream);
 
 /*
  * attn_bwd_simt -- the same gradients computed by SIMT kernels with fp32

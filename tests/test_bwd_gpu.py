@@ -46,11 +46,11 @@ def _lib(cuda_lib_path):
     attn.status()
 
 
-def visible(B, L, causal, vl):
-    """[B, L, L] bool: key j visible to query i."""
-    m = np.ones((B, L, L), dtype=bool)
+def visible(B, Lq, Lk, causal, vl):
+    """[B, Lq, Lk] bool: key j visible to query i (causal: j <= i)."""
+    m = np.ones((B, Lq, Lk), dtype=bool)
     if causal:
-        m &= np.tri(L, dtype=bool)[None]
+        m &= np.tri(Lq, Lk, dtype=bool)[None]
     if vl is not None:
         for b in range(B):
             m[b, :, int(vl[b]):] = False
@@ -62,7 +62,7 @@ def operand_terms(qf, kf, vf, dof, sm, causal, vl, lse_ref):
     |dO|, |q|, |k| over the same index sets, per gradient element (float64)."""
     B, Hq, L, D = qf.shape
     G = Hq // kf.shape[1]
-    vis = visible(B, L, causal, vl)
+    vis = visible(B, L, kf.shape[2], causal, vl)
     tv, tk, tq = np.zeros_like(vf), np.zeros_like(kf), np.zeros_like(qf)
     av, ak, aq = np.zeros_like(vf), np.zeros_like(kf), np.zeros_like(qf)
     for b in range(B):
@@ -84,15 +84,15 @@ def operand_terms(qf, kf, vf, dof, sm, causal, vl, lse_ref):
     return (tq, tk, tv), (aq, ak, av)
 
 
-def run_case(B, Hq, Hkv, L, D, dtype, causal, vl, seed, impl):
-    q, k, v, vl_t = wl.make_inputs(B, Hq, Hkv, L, D, dtype, seed=seed, valid_len=vl)
+def run_case(B, Hq, Hkv, L, D, dtype, causal, vl, seed, impl, Lk=None):
+    q, k, v, vl_t = wl.make_inputs(B, Hq, Hkv, L, D, dtype, seed=seed, valid_len=vl, Lk=Lk)
     gen = torch.Generator().manual_seed(seed + 1)
     do = torch.randn(B, Hq, L, D, generator=gen).to(wl.TORCH_DTYPE[dtype])
     dev = torch.device("cuda")
     qd, kd, vd, dod = q.to(dev), k.to(dev), v.to(dev), do.to(dev)
     vld = None if vl_t is None else vl_t.to(dev)
     sm = 1.0 / math.sqrt(D)
-    o, lse = attn.attn_fwd(qd, kd, vd, causal=causal, sm_scale=sm, valid_len=vld)
+    o, lse = attn.attn_fwd_strided(qd, kd, vd, causal=causal, sm_scale=sm, valid_len=vld)
     dq, dk, dv = attn.attn_bwd(qd, kd, vd, o, lse, dod, causal=causal, sm_scale=sm, valid_len=vld,
                                impl=impl)
     st, code = attn.status()
@@ -296,3 +296,14 @@ def test_bwd_strided_matches_contiguous(D, layout):
     for g, r, b in zip(got, ref, bufs):
         assert torch.equal(g.contiguous().view(torch.int16), r.contiguous().view(torch.int16))
         assert bool((b[..., D:] == sentinel).all())
+
+
+@pytest.mark.parametrize("Lq, Lk, causal, vl", [(200, 333, True, [333, 77]), (333, 200, True, None),
+                                                (129, 260, False, [260, 3]), (300, 129, False, None),
+                                                (100, 400, True, [400, 0])])
+@pytest.mark.parametrize("D, dtype", [(128, wl.BF16), (64, wl.F16)])
+def test_bwd_tc_query_and_key_lengths(Lq, Lk, causal, vl, D, dtype):
+    """Lq != Lk (the forward's top-left causal reading): fewer queries than keys
+    (keys after the last query get zero gradients under causality), more
+    queries than keys (late queries see every key), padding, an empty batch."""
+    run_case(2, 4, 2, Lq, D, dtype, causal, vl, seed=Lq + Lk + D, impl="tc", Lk=Lk)

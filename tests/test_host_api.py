@@ -277,6 +277,6 @@ def test_bwd_strided_stride_validation(lib, which, strides, expected):
     st = {n: None for n in names}
     st[which] = ctypes.byref(binding.Strides(*strides))
     rc = lib.attn_bwd_strided(A16, st["q"], A16, st["k"], A16, st["v"], A16, st["o"], A16, st["do"],
-                              A16, A16, st["dq"], A16, st["dk"], A16, st["dv"], 1, 4, 2, 64, 64,
+                              A16, A16, st["dq"], A16, st["dk"], A16, st["dv"], 1, 4, 2, 64, 64, 64,
                               0.125, 1, None, attn.ATTN_BF16, None)
     assert binding.STATUS_NAMES[rc] == expected
