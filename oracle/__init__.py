@@ -60,10 +60,10 @@ def _bind(path: str):
                                         i, p, p, i64, i64, i, p, i64, i]
     lib.oracle_attn_fwd_u16.restype = i
     lib.oracle_attn_bwd_f64.argtypes = [p, p, p, p, p, p, p, i, i, i, i, i, i, ctypes.c_double,
-                                        i, p, i]
+                                        i, p, p, i64, i64, i]
     lib.oracle_attn_bwd_f64.restype = i
     lib.oracle_attn_bwd_rows_f64.argtypes = [p, p, p, p, i, i, i, i, i, i, ctypes.c_double, i,
-                                             p, p, i64, p, p, p, i64, p, p, p, i]
+                                             p, p, i64, i64, p, i64, p, p, p, i64, p, p, p, i]
     lib.oracle_attn_bwd_rows_f64.restype = i
     lib.oracle_decode.argtypes = [p, p, i64, i]
     lib.oracle_decode.restype = i
@@ -198,10 +198,11 @@ def attn_fwd_bits(q_bits, k_bits, v_bits, dtype, sm_scale, causal=False, valid_l
 
 
 def attn_bwd_f64(q, k, v, do, sm_scale, causal=False, valid_len=None, threads=0,
-                 _lib_override=None):
+                 _lib_override=None, mask=None):
     """Gradients (dq, dk, dv) of the attention forward for an output gradient
     ``do``, from the definition (see oracle_attn_bwd_f64).  q, do:
-    [B, Hq, Lq, D]; k, v: [B, Hkv, Lk, D]; float64 results of the same shapes."""
+    [B, Hq, Lq, D]; k, v: [B, Hkv, Lk, D]; float64 results of the same shapes.
+    mask: an explicit mask as for :func:`attn_fwd_f64`."""
     q = np.ascontiguousarray(q, dtype=np.float64)
     k = np.ascontiguousarray(k, dtype=np.float64)
     v = np.ascontiguousarray(v, dtype=np.float64)
@@ -210,18 +211,19 @@ def attn_bwd_f64(q, k, v, do, sm_scale, causal=False, valid_len=None, threads=0,
     if do.shape != q.shape:
         raise ValueError("do must be shaped like q")
     vl = _valid(valid_len, B)
+    mk, msb, msr = _mask(mask, B, Lq, Lk)
     dq, dk, dv = np.empty_like(q), np.empty_like(k), np.empty_like(v)
     lib = _lib_override if _lib_override is not None else _load()
     rc = lib.oracle_attn_bwd_f64(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv),
                                  B, Hq, Hkv, Lq, Lk, D, float(sm_scale), int(bool(causal)),
-                                 _ptr(vl), int(threads))
+                                 _ptr(vl), _ptr(mk), msb, msr, int(threads))
     if rc != 0:
         raise ValueError("oracle_attn_bwd_f64 failed with code %d" % rc)
     return dq, dk, dv
 
 
 def attn_bwd_rows_f64(q, k, v, do, sm_scale, causal=False, valid_len=None, q_rows=(),
-                      k_rows=(), threads=0, _lib_override=None):
+                      k_rows=(), threads=0, _lib_override=None, mask=None):
     """Selected rows of :func:`attn_bwd_f64`'s gradients (see
     oracle_attn_bwd_rows_f64): dQ for flat query rows ``q_rows`` (index
     (b*Hq + h_q)*Lq + i) and dK, dV for flat key rows ``k_rows`` (index
@@ -236,6 +238,7 @@ def attn_bwd_rows_f64(q, k, v, do, sm_scale, causal=False, valid_len=None, q_row
     if do.shape != q.shape:
         raise ValueError("do must be shaped like q")
     vl = _valid(valid_len, B)
+    mk, msb, msr = _mask(mask, B, Lq, Lk)
     qr = np.ascontiguousarray(np.asarray(q_rows, dtype=np.int64).reshape(-1))
     kr = np.ascontiguousarray(np.asarray(k_rows, dtype=np.int64).reshape(-1))
     dq = np.empty((qr.size, D))
@@ -244,7 +247,8 @@ def attn_bwd_rows_f64(q, k, v, do, sm_scale, causal=False, valid_len=None, q_row
     kmag = np.empty((kr.size, 4))
     lib = _lib_override if _lib_override is not None else _load()
     rc = lib.oracle_attn_bwd_rows_f64(_ptr(q), _ptr(k), _ptr(v), _ptr(do), B, Hq, Hkv, Lq, Lk, D,
-                                      float(sm_scale), int(bool(causal)), _ptr(vl), _ptr(qr),
+                                      float(sm_scale), int(bool(causal)), _ptr(vl), _ptr(mk), msb,
+                                      msr, _ptr(qr),
                                       qr.size, _ptr(dq), _ptr(qmag), _ptr(kr), kr.size, _ptr(dk),
                                       _ptr(dv), _ptr(kmag), int(threads))
     if rc != 0:

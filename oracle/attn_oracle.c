@@ -253,15 +253,17 @@ int oracle_max_threads(void) {
  *
  * q, dO: [B, Hq, Lq, D]; k, v: [B, Hkv, Lk, D]; dq like q, dk and dv like k
  * (Lq = Lk is the pages' case; the masks compare absolute positions as in
- * the forward).
+ * the forward).  mask: the forward's explicit mask (NULL: none), combined
+ * with the causal and padding masks by intersection.
  * Returns 0, 1 on invalid arguments, 2 when scratch could not be allocated.
  */
 int oracle_attn_bwd_f64(const double* q, const double* k, const double* v, const double* dO,
                         double* dq, double* dk, double* dv, int B, int Hq, int Hkv, int Lq, int Lk, int D,
-                        double sm_scale, int causal, const int32_t* valid_len, int threads) {
+                        double sm_scale, int causal, const int32_t* valid_len, const uint8_t* mask,
+                        int64_t mask_batch_stride, int64_t mask_row_stride, int threads) {
   if (B < 1 || Hq < 1 || Hkv < 1 || Lq < 1 || Lk < 1 || D < 1 || Hq % Hkv != 0) return 1;
   const int G = Hq / Hkv;
-  const oracle_mask_t mk = {NULL, 0, 0};
+  const oracle_mask_t mk = {mask, mask_batch_stride, mask_row_stride};  /* explicit mask or none */
   memset(dq, 0, sizeof(double) * (size_t)B * Hq * Lq * D);
   memset(dk, 0, sizeof(double) * (size_t)B * Hkv * Lk * D);
   memset(dv, 0, sizeof(double) * (size_t)B * Hkv * Lk * D);
@@ -349,9 +351,9 @@ int oracle_attn_bwd_f64(const double* q, const double* k, const double* v, const
  */
 static int64_t row_stats(const double* q_row, const double* do_row, const double* k_head,
                          const double* v_head, int64_t i, int b, int Lk, int D, double sm_scale,
-                         int causal, const int32_t* valid_len, double* s, double* m_out,
-                         double* z_out, double* delta_out) {
-  const oracle_mask_t mk = {NULL, 0, 0};
+                         int causal, const int32_t* valid_len, const oracle_mask_t* mkp,
+                         double* s, double* m_out, double* z_out, double* delta_out) {
+  const oracle_mask_t mk = *mkp;
   double m = -INFINITY;
   int64_t n = 0;
   for (int64_t j = 0; j < Lk; ++j) {
@@ -390,17 +392,19 @@ static int64_t row_stats(const double* q_row, const double* do_row, const double
  * (w_i = sum_d |dO_id O_id|, O_i the forward's output row):
  *   qmag[3r ..]: sum_j |dS_ij|, w_i, visible keys;
  *   kmag[4r ..]: sum_i |dS_ij|, sum_i P_ij, sum_i P_ij w_i, visible queries
- * (sums over the G query heads of the key's group).
+ * (sums over the G query heads of the key's group).  mask: as in
+ * oracle_attn_bwd_f64.
  */
 int oracle_attn_bwd_rows_f64(const double* q, const double* k, const double* v, const double* dO,
                              int B, int Hq, int Hkv, int Lq, int Lk, int D, double sm_scale,
-                             int causal,
-                             const int32_t* valid_len, const int64_t* q_rows, int64_t n_q,
+                             int causal, const int32_t* valid_len, const uint8_t* mask,
+                             int64_t mask_batch_stride, int64_t mask_row_stride,
+                             const int64_t* q_rows, int64_t n_q,
                              double* dq, double* qmag, const int64_t* k_rows, int64_t n_k,
                              double* dk, double* dv, double* kmag, int threads) {
   if (B < 1 || Hq < 1 || Hkv < 1 || Lq < 1 || Lk < 1 || D < 1 || Hq % Hkv != 0) return 1;
   const int G = Hq / Hkv;
-  const oracle_mask_t mk = {NULL, 0, 0};
+  const oracle_mask_t mk = {mask, mask_batch_stride, mask_row_stride};  /* the rows' key sets */
   for (int64_t r = 0; r < n_q; ++r)
     if (q_rows[r] < 0 || q_rows[r] >= (int64_t)B * Hq * Lq) return 1;
   for (int64_t r = 0; r < n_k; ++r)
@@ -434,7 +438,7 @@ int oracle_attn_bwd_rows_f64(const double* q, const double* k, const double* v, 
       double m = 0.0, z = 1.0, delta = 0.0, sabs = 0.0, w = 0.0;
       for (int d = 0; d < D; ++d) dq_row[d] = 0.0;
       const int64_t n = row_stats(q_row, do_row, k_head, v_head, i, b, Lk, D, sm_scale, causal,
-                                  valid_len, s, &m, &z, &delta);
+                                  valid_len, &mk, s, &m, &z, &delta);
       if (n > 0) {
         double* o_row = (double*)calloc((size_t)D, sizeof(double));
         for (int64_t j = 0; j < Lk; ++j) {
@@ -492,7 +496,7 @@ int oracle_attn_bwd_rows_f64(const double* q, const double* k, const double* v, 
         const int64_t i = gi % Lq;
         double m = 0.0, z = 1.0, delta = 0.0, w = 0.0;
         const int64_t n = row_stats(q + qrow * D, dO + qrow * D, k_head, v_head, i, b, Lk, D,
-                                    sm_scale, causal, valid_len, s, &m, &z, &delta);
+                                    sm_scale, causal, valid_len, &mk, s, &m, &z, &delta);
         if (n > 0) {
           for (int d = 0; d < D; ++d) o_row[d] = 0.0;
           for (int64_t j = 0; j < Lk; ++j) {

@@ -30,9 +30,9 @@ def rand(shape, rng, scale=1.0):
     return rng.standard_normal(shape) * scale
 
 
-def finite_differences(q, k, v, do, sm, causal, vl, h=1e-6):
+def finite_differences(q, k, v, do, sm, causal, vl, h=1e-6, mask=None):
     def loss(qq, kk, vv):
-        o, _ = oracle.attn_fwd_f64(qq, kk, vv, sm, causal=causal, valid_len=vl)
+        o, _ = oracle.attn_fwd_f64(qq, kk, vv, sm, causal=causal, valid_len=vl, mask=mask)
         return float(np.sum(o * do))
 
     grads = []
@@ -51,7 +51,7 @@ def finite_differences(q, k, v, do, sm, causal, vl, h=1e-6):
     return grads
 
 
-def torch_grads(q, k, v, do, sm, causal, vl):
+def torch_grads(q, k, v, do, sm, causal, vl, explicit=None):
     qt, kt, vt = (torch.tensor(x, dtype=torch.float64, requires_grad=True) for x in (q, k, v))
     B, Hq, Lq, D = q.shape
     Lk = k.shape[2]
@@ -62,6 +62,8 @@ def torch_grads(q, k, v, do, sm, causal, vl):
     if vl is not None:
         for b in range(B):
             mask[b, :, :, :] &= (torch.arange(Lk) < int(vl[b]))[None, :]
+    if explicit is not None:  # [B, Lq, Lk] or [Lq, Lk], nonzero keeps
+        mask &= torch.from_numpy(np.asarray(explicit) != 0).reshape(-1, 1, Lq, Lk)
     empty = ~mask.any(dim=-1, keepdim=True)
     o = torch.nn.functional.scaled_dot_product_attention(
         qt, kt.repeat_interleave(G, dim=1), vt.repeat_interleave(G, dim=1),
@@ -123,7 +125,34 @@ def pin_closed_forms(bwd):
             np.testing.assert_allclose(dv[b, h].sum(axis=0), want, rtol=1e-12, atol=1e-12)
 
 
-PINS = [pin_finite_differences, pin_torch_autograd, pin_closed_forms]
+def pin_explicit_mask(bwd):
+    """An explicit [B, Lq, Lk] (or shared [Lq, Lk]) mask combined with causal
+    and padding: finite differences of the masked forward oracle, and
+    autograd through the masked SDPA."""
+    rng = np.random.default_rng(14)
+    for (B, Hq, Hkv, Lq, Lk, D, causal, vl, shared) in [
+            (2, 2, 1, 4, 5, 2, False, None, False), (1, 2, 2, 5, 5, 3, True, [4], True)]:
+        q, k, v = rand((B, Hq, Lq, D), rng), rand((B, Hkv, Lk, D), rng), rand((B, Hkv, Lk, D), rng)
+        do = rand((B, Hq, Lq, D), rng)
+        mk = (rng.random((Lq, Lk) if shared else (B, Lq, Lk)) < 0.6).astype(np.uint8)
+        mk[..., 0, :] = 0  # a query row that sees no key
+        got = bwd(q, k, v, do, 0.8, causal=causal, valid_len=vl, mask=mk)
+        ref = finite_differences(q, k, v, do, 0.8, causal, vl, mask=mk)
+        for g, r in zip(got, ref):
+            np.testing.assert_allclose(g, r, rtol=1e-6, atol=1e-8)
+    for (B, Hq, Hkv, Lq, Lk, D, causal, vl) in [(2, 4, 2, 21, 27, 8, True, [27, 9]),
+                                                 (3, 2, 1, 17, 13, 4, False, None)]:
+        q, k, v = rand((B, Hq, Lq, D), rng, 1.5), rand((B, Hkv, Lk, D), rng), rand((B, Hkv, Lk, D), rng)
+        do = rand((B, Hq, Lq, D), rng)
+        mk = (rng.random((B, Lq, Lk)) < 0.5).astype(np.uint8)
+        mk[0, 3:7, :] = 0
+        got = bwd(q, k, v, do, 0.3, causal=causal, valid_len=vl, mask=mk)
+        ref = torch_grads(q, k, v, do, 0.3, causal, vl, explicit=mk)
+        for g, r in zip(got, ref):
+            np.testing.assert_allclose(g, r, rtol=1e-10, atol=1e-11)
+
+
+PINS = [pin_finite_differences, pin_torch_autograd, pin_closed_forms, pin_explicit_mask]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
@@ -139,6 +168,8 @@ MUTANTS = {
                      "dk_head[j * D + d] += sm_scale * ds * k_head[j * D + d];"),
     "dv_without_p": ("dv_head[j * D + d] += p[j] * do_row[d];", "dv_head[j * D + d] += do_row[d];"),
     "one_query_head": ("for (int g = 0; g < G; ++g) {", "for (int g = 0; g < 1; ++g) {"),
+    "mask_ignored": ("const oracle_mask_t mk = {mask, mask_batch_stride, mask_row_stride};  /* explicit mask or none */",
+                     "const oracle_mask_t mk = {NULL, 0, 0};"),
 }
 
 

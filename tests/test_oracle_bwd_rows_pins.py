@@ -93,7 +93,25 @@ def pin_magnitudes(rows_fn):
         np.testing.assert_allclose(km, km_ref, rtol=1e-11, atol=1e-12)
 
 
-PINS = [pin_rows_match_full, pin_magnitudes]
+def pin_rows_match_full_masked(rows_fn):
+    """With an explicit mask (per batch and shared), also against the full
+    backward oracle."""
+    for n, (case, shared) in enumerate([(CASES[0], False), (CASES[4], True), (CASES[5], False)]):
+        B, Hq, Hkv, Lq, Lk, D, causal, vl = case
+        q, k, v, do = inputs(case, 80 + n)
+        rng = np.random.default_rng(90 + n)
+        mk = (rng.random((Lq, Lk) if shared else (B, Lq, Lk)) < 0.5).astype(np.uint8)
+        dq, dk, dv = oracle.attn_bwd_f64(q, k, v, do, 0.6, causal=causal, valid_len=vl, mask=mk)
+        qr = rng.permutation(B * Hq * Lq)
+        kr = rng.permutation(B * Hkv * Lk)
+        dq2, _, dk2, dv2, _ = rows_fn(q, k, v, do, 0.6, causal=causal, valid_len=vl, q_rows=qr,
+                                      k_rows=kr, mask=mk)
+        np.testing.assert_allclose(dq2, dq.reshape(-1, D)[qr], rtol=1e-11, atol=1e-12)
+        np.testing.assert_allclose(dk2, dk.reshape(-1, D)[kr], rtol=1e-11, atol=1e-12)
+        np.testing.assert_allclose(dv2, dv.reshape(-1, D)[kr], rtol=1e-11, atol=1e-12)
+
+
+PINS = [pin_rows_match_full, pin_magnitudes, pin_rows_match_full_masked]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
@@ -117,6 +135,8 @@ MUTANTS = {
                          "const double p = exp(sm_scale * dot - st[4 * gi]);"),
     "dq_wrong_kv_head": ("const int64_t kvh = (int64_t)b * Hkv + (qh % Hq) / G;",
                          "const int64_t kvh = (int64_t)b * Hkv + (qh % Hq) % Hkv;"),
+    "mask_ignored": ("const oracle_mask_t mk = {mask, mask_batch_stride, mask_row_stride};  /* the rows' key sets */",
+                     "const oracle_mask_t mk = {NULL, 0, 0};"),
 }
 
 
