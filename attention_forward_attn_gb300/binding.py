@@ -103,6 +103,8 @@ def load():
             lib.attn_bwd_strided.argtypes = [p, sp, p, sp, p, sp, p, sp, p, sp, p, p, sp, p, sp, p,
                                              sp, i, i, i, i, i, i, ctypes.c_float, i, p, i, p]
             lib.attn_bwd_strided.restype = i
+            lib.attn_bwd_masked.argtypes = lib.attn_bwd_strided.argtypes[:-2] + [p, i64, i64, i, p]
+            lib.attn_bwd_masked.restype = i
             lib.attn_fwd_f32.argtypes = [p, p, p, p, p, i, i, i, i, ctypes.c_float, i, p, i, p]
             lib.attn_fwd_f32.restype = i
             lib.attn_host_plan.argtypes = [i, i, i, i, i, i, ctypes.POINTER(Chunk), i,
@@ -439,7 +441,7 @@ def attn_fwd_f32(q, k, v, *, kernel="tiled_rowmax", causal=False, sm_scale=None,
 
 
 def attn_bwd(q, k, v, o, lse, do, *, causal=False, sm_scale=None, valid_len=None, stream=None,
-             impl="tc", dq=None, dk=None, dv=None):
+             impl="tc", dq=None, dk=None, dv=None, mask=None):
     """Gradients (dq, dk, dv) of attn_fwd for the output gradient ``do``.
 
     impl="tc": attn_bwd_strided (tensor cores).  q, o, do: [B, Hq, Lq, D]; k, v:
@@ -448,7 +450,9 @@ def attn_bwd(q, k, v, o, lse, do, *, causal=False, sm_scale=None, valid_len=None
     ``x.transpose(1, 2)`` of [B, L, H, D] tensors); dq, dk, dv: optional
     output views of the same shapes (default: new contiguous tensors).
     impl="simt": attn_bwd_simt (fp32 SIMT), contiguous tensors only.
-    lse: the forward's [B*Hq, L] fp32 LSE."""
+    lse: the forward's [B*Hq, L] fp32 LSE.  mask: the forward's explicit
+    boolean mask (a bool/uint8 CUDA tensor [B, Lq, Lk] or [Lq, Lk] with a
+    contiguous last dimension; impl="tc" only, through attn_bwd_masked)."""
     import torch
     if impl not in ("tc", "simt"):
         raise ValueError("impl must be 'tc' or 'simt'")
@@ -476,14 +480,30 @@ def attn_bwd(q, k, v, o, lse, do, *, causal=False, sm_scale=None, valid_len=None
     if valid_len is not None:
         vl_ptr = valid_len.data_ptr()
     lse = lse.contiguous()
+    if mask is not None:
+        if impl != "tc":
+            raise ValueError("an explicit mask takes impl='tc'")
+        if mask.dtype not in (torch.bool, torch.uint8) or not mask.is_cuda:
+            raise ValueError("mask must be a bool or uint8 CUDA tensor")
+        if mask.dim() == 2:
+            mask = mask.unsqueeze(0)
+        if (mask.dim() != 3 or mask.shape[1:] != (L, Lk) or mask.shape[0] not in (1, B)
+                or (Lk > 1 and mask.stride(2) != 1)):
+            raise ValueError("mask must be [B, Lq, Lk] or [Lq, Lk] with a contiguous last dimension")
     if impl == "tc":
         st3 = lambda t: _strides_arg((t.stride(0), t.stride(1), t.stride(2)))
-        name = "attn_bwd_strided"
-        st = int(load().attn_bwd_strided(
-            q.data_ptr(), st3(q), k.data_ptr(), st3(k), v.data_ptr(), st3(v), o.data_ptr(), st3(o),
-            do.data_ptr(), st3(do), lse.data_ptr(), dq.data_ptr(), st3(dq), dk.data_ptr(), st3(dk),
-            dv.data_ptr(), st3(dv), B, Hq, Hkv, L, Lk, D, float(sm_scale), int(bool(causal)), vl_ptr,
-            _dtype_code(q), _stream_handle(stream)))
+        args = [q.data_ptr(), st3(q), k.data_ptr(), st3(k), v.data_ptr(), st3(v), o.data_ptr(),
+                st3(o), do.data_ptr(), st3(do), lse.data_ptr(), dq.data_ptr(), st3(dq),
+                dk.data_ptr(), st3(dk), dv.data_ptr(), st3(dv), B, Hq, Hkv, L, Lk, D,
+                float(sm_scale), int(bool(causal)), vl_ptr]
+        if mask is None:
+            name = "attn_bwd_strided"
+            st = int(load().attn_bwd_strided(*args, _dtype_code(q), _stream_handle(stream)))
+        else:
+            name = "attn_bwd_masked"
+            msb = 0 if mask.shape[0] == 1 else mask.stride(0)
+            st = int(load().attn_bwd_masked(*args, mask.data_ptr(), msb, mask.stride(1),
+                                            _dtype_code(q), _stream_handle(stream)))
     else:
         name = "attn_bwd_simt"
         st = int(load().attn_bwd_simt(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),

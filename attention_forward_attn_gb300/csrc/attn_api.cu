@@ -497,20 +497,21 @@ attn_status_t bwd_validate(const void* q, const void* k, const void* v, const vo
 
 }  // namespace
 
-attn_status_t attn_bwd_strided(const void* q, const attn_strides_t* q_strides, const void* k,
-                               const attn_strides_t* k_strides, const void* v,
-                               const attn_strides_t* v_strides, const void* o,
-                               const attn_strides_t* o_strides, const void* dO,
-                               const attn_strides_t* do_strides, const float* lse, void* dq,
-                               const attn_strides_t* dq_strides, void* dk,
-                               const attn_strides_t* dk_strides, void* dv,
-                               const attn_strides_t* dv_strides, int B, int Hq, int Hkv, int Lq,
-                               int Lk, int D, float sm_scale, int causal,
-                               const int32_t* valid_len, attn_dtype_t dtype,
-                               attn_stream_t stream) {
+attn_status_t attn_bwd_masked(const void* q, const attn_strides_t* q_strides, const void* k,
+                              const attn_strides_t* k_strides, const void* v,
+                              const attn_strides_t* v_strides, const void* o,
+                              const attn_strides_t* o_strides, const void* dO,
+                              const attn_strides_t* do_strides, const float* lse, void* dq,
+                              const attn_strides_t* dq_strides, void* dk,
+                              const attn_strides_t* dk_strides, void* dv,
+                              const attn_strides_t* dv_strides, int B, int Hq, int Hkv, int Lq,
+                              int Lk, int D, float sm_scale, int causal, const int32_t* valid_len,
+                              const uint8_t* mask, int64_t mask_batch_stride,
+                              int64_t mask_row_stride, attn_dtype_t dtype, attn_stream_t stream) {
   attn_status_t s = bwd_validate(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, Lq, Lk, D, sm_scale,
                                  causal, valid_len, dtype, true);
   if (s != ATTN_OK) return s;
+  if (mask != nullptr && (mask_batch_stride < 0 || mask_row_stride < 0)) return ATTN_ERR_STRIDE;
   attn::Strides sq, sk, sv, so, sdo, sdq, sdk, sdv;
   if ((s = strides_of(q_strides, B, Hq, Lq, D, &sq)) != ATTN_OK ||
       (s = strides_of(k_strides, B, Hkv, Lk, D, &sk)) != ATTN_OK ||
@@ -539,15 +540,34 @@ attn_status_t attn_bwd_strided(const void* q, const attn_strides_t* q_strides, c
   const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   void* ws = nullptr;
   cudaError_t e = cudaMallocFromPoolAsync(
-      &ws, static_cast<size_t>(attn::bwd_tc_workspace_bytes(B, Hq, Hkv, Lq, Lk, D, st->num_sms)),
+      &ws,
+      static_cast<size_t>(attn::bwd_tc_workspace_bytes(
+          B, Hq, Hkv, Lq, Lk, D, st->num_sms, mask == nullptr ? 0 : (mask_batch_stride == 0 ? 1 : B))),
       pool, cs);
   if (e != cudaSuccess) return cuda_fail(e);
   e = attn::launch_bwd_tc(maps, o, so, dO, sdo, lse, dq, sdq, dk, sdk, dv, sdv, ws, B, Hq, Hkv, Lq,
-                          Lk, D, sm_scale, causal, valid_len, bf16, st->num_sms, st->status, cs);
+                          Lk, D, sm_scale, causal, valid_len, mask, mask_batch_stride,
+                          mask_row_stride, bf16, st->num_sms, st->status, cs);
   const cudaError_t ef = cudaFreeAsync(ws, cs);
   if (e == cudaSuccess) e = ef;
   if (e != cudaSuccess) return cuda_fail(e);
   return ATTN_OK;
+}
+
+attn_status_t attn_bwd_strided(const void* q, const attn_strides_t* q_strides, const void* k,
+                               const attn_strides_t* k_strides, const void* v,
+                               const attn_strides_t* v_strides, const void* o,
+                               const attn_strides_t* o_strides, const void* dO,
+                               const attn_strides_t* do_strides, const float* lse, void* dq,
+                               const attn_strides_t* dq_strides, void* dk,
+                               const attn_strides_t* dk_strides, void* dv,
+                               const attn_strides_t* dv_strides, int B, int Hq, int Hkv, int Lq,
+                               int Lk, int D, float sm_scale, int causal,
+                               const int32_t* valid_len, attn_dtype_t dtype,
+                               attn_stream_t stream) {
+  return attn_bwd_masked(q, q_strides, k, k_strides, v, v_strides, o, o_strides, dO, do_strides,
+                         lse, dq, dq_strides, dk, dk_strides, dv, dv_strides, B, Hq, Hkv, Lq, Lk, D,
+                         sm_scale, causal, valid_len, nullptr, 0, 0, dtype, stream);
 }
 
 attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,

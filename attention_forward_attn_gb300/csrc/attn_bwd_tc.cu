@@ -84,6 +84,12 @@ struct BwdTcParams {
   Strides sdq, sdk, sdv;          // element strides (batch, head, row) of the outputs
   int splits;                     // CTAs per key tile of the dK/dV kernel (see bwd_tc_splits)
   float* part;                    // splits > 1: fp32 partial dV, dK [splits][2][B*Hkv*L][dg]
+  // explicit mask (bwd_mask_pack_kernel): bit i%32 of a word = the mask at
+  // (query i, key j); rbits [mB][Lq][n_tk][4] words over the keys of a tile,
+  // cbits [mB][Lk][n_tq][4] over the queries of a tile; mB = 1 when shared
+  const uint32_t* rbits;
+  const uint32_t* cbits;
+  int mask_shared;
   float scale_log2;               // sm_scale log2(e)
   float sm_scale;
   int causal;
@@ -308,6 +314,56 @@ __global__ void __launch_bounds__(256) bwd_tc_prep_kernel(const void* __restrict
   }
 }
 
+// Explicit mask -> bits, one CTA per (key tile, query tile, mask batch): the
+// 128 x 128 block of mask bytes is staged in shared memory (rows padded to
+// 132 bytes, so a warp reading one column touches 32 banks), then warp
+// ballots write each query row's 128 key bits (rbits) and each key row's 128
+// query bits (cbits).  Positions outside [0, Lq) x [0, Lk) are 0.
+__global__ void __launch_bounds__(256) bwd_mask_pack_kernel(const uint8_t* __restrict__ mask,
+                                                            int64_t msb, int64_t msr, int Lq,
+                                                            int Lk, int n_tq, int n_tk,
+                                                            uint32_t* rbits, uint32_t* cbits) {
+  constexpr int kPitch = 132;
+  __shared__ uint8_t blk[T * kPitch];
+  const int n = blockIdx.x, m = blockIdx.y, mb = blockIdx.z;
+  const uint8_t* src = mask + mb * msb;
+  for (int idx = threadIdx.x; idx < T * T; idx += 256) {
+    const int r = idx / T, c = idx % T;
+    const int i = m * T + r, j = n * T + c;
+    blk[r * kPitch + c] = (i < Lq && j < Lk) ? (src[static_cast<int64_t>(i) * msr + j] != 0) : 0;
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int r = warp; r < T; r += 8) {  // query row r of the block: its 128 key bits
+    uint32_t wd[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) wd[q] = __ballot_sync(0xffffffffu, blk[r * kPitch + q * 32 + lane] != 0);
+    const int i = m * T + r;
+    if (lane == 0 && i < Lq)
+      *reinterpret_cast<uint4*>(rbits + ((static_cast<int64_t>(mb) * Lq + i) * n_tk + n) * 4) =
+          make_uint4(wd[0], wd[1], wd[2], wd[3]);
+  }
+  for (int c = warp; c < T; c += 8) {  // key column c of the block: its 128 query bits
+    uint32_t wd[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) wd[q] = __ballot_sync(0xffffffffu, blk[(q * 32 + lane) * kPitch + c] != 0);
+    const int j = n * T + c;
+    if (lane == 0 && j < Lk)
+      *reinterpret_cast<uint4*>(cbits + ((static_cast<int64_t>(mb) * Lk + j) * n_tq + m) * 4) =
+          make_uint4(wd[0], wd[1], wd[2], wd[3]);
+  }
+}
+
+// The TH mask bits of this thread's columns (bit c: column TH grp + c) from a
+// 4-word row of 128 bits.
+__device__ __forceinline__ uint64_t mask_bits(const uint32_t* words, int grp) {
+  if constexpr (TH == 64) {
+    return *reinterpret_cast<const uint64_t*>(words + 2 * grp);
+  } else {
+    return words[grp];
+  }
+}
+
 // ------------------------------------------------------------------ dK, dV
 
 // Barrier indices of the dK/dV kernel (NS input stages).
@@ -518,7 +574,7 @@ __device__ __forceinline__ int cols_in(int dg, int c_lo, int part) {
 //   dS^T = P^T (dP^T - delta), written over the next TH/2.
 // Epilogue: the first half of the warpgroups write dV, the second dK (x
 // sm_scale), each a D / (kGroups / 2)-column part of the row.
-template <int D, bool BF16, bool SPLIT>
+template <int D, bool BF16, bool SPLIT, bool MASK>
 __device__ void dkv_elementwise(const BwdTcParams& p, const KvUnit& w, const BBars& br,
                                 uint32_t smem, uint32_t tmem) {
   using C = BCfg<D>;
@@ -536,6 +592,13 @@ __device__ void dkv_elementwise(const BwdTcParams& p, const KvUnit& w, const BBa
     const uint32_t s = static_cast<uint32_t>(t % NS);
     const uint32_t st = smem + C::kvOffIn + s * C::kvStageBytes;
     const int mi = w.m_lo + ((SPLIT ? w.t0 : 0) + t) / p.G;
+    // explicit mask: this key row's bits over the query tile (loaded first)
+    uint64_t mbits = ~0ull;
+    if constexpr (MASK) {
+      const int j = w.n * T + row;
+      const int64_t mb = p.mask_shared ? 0 : w.b;
+      mbits = j < p.Lk ? mask_bits(p.cbits + ((mb * p.Lk + j) * p.n_tq + mi) * 4, grp) : 0ull;
+    }
     // the stage's -LSE log2(e) and delta are read from shared memory
     ok = __all_sync(kFull, bwait(br, p.status, br.bar(I::inFull + s), (t / NS) & 1, kRoleSoftmax));
     if (ok) ok = __all_sync(kFull, bwait(br, p.status, br.bar(I::sFull), t & 1, kRoleSoftmax));
@@ -567,6 +630,10 @@ __device__ void dkv_elementwise(const BwdTcParams& p, const KvUnit& w, const BBa
     if (cmin > 0) {
 #pragma unroll
       for (int c = 0; c < TH; ++c) pr[c] = c < cmin ? 0.f : pr[c];
+    }
+    if constexpr (MASK) {
+#pragma unroll
+      for (int c = 0; c < TH; ++c) pr[c] = ((mbits >> c) & 1ull) ? pr[c] : 0.f;
     }
     uint32_t pk[TH / 2];
 #pragma unroll
@@ -690,7 +757,8 @@ __global__ void __launch_bounds__(256) bwd_dkv_reduce_kernel(const BwdTcParams p
 }
 
 // SPLIT: key tiles split over several CTAs (p.splits > 1), fp32 partial rows.
-template <int D, bool BF16, bool SPLIT>
+// MASK: an explicit mask (p.cbits).
+template <int D, bool BF16, bool SPLIT, bool MASK>
 __global__ void __launch_bounds__(kThreadsB, 1)
     bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v,
@@ -732,7 +800,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   } else if (warp == kMmaWarp) {
     dkv_mma<D, BF16>(p, w, br, smem, tmem);
   } else {
-    dkv_elementwise<D, BF16, SPLIT>(p, w, br, smem, tmem);
+    dkv_elementwise<D, BF16, SPLIT, MASK>(p, w, br, smem, tmem);
   }
   ptx::tc_fence_before();
   __syncthreads();
@@ -894,7 +962,7 @@ __device__ void dq_mma(const BwdTcParams& p, const QUnit& w, const BBars& br, ui
 // query; dS = P (dP - delta) into dS buffer j % 2 (16-bit pairs) once the dQ
 // MMA of key tile j - 2 has read it.  Epilogue: warpgroup g < kEpi writes dQ
 // columns [g D/kEpi, (g + 1) D/kEpi) of its row, times sm_scale.
-template <int D, bool BF16>
+template <int D, bool BF16, bool MASK>
 __device__ void dq_elementwise(const BwdTcParams& p, const QUnit& w, const BBars& br, uint32_t tmem) {
   using C = BCfg<D>;
   using I = QIdx<C::qKStages, C::qVStages>;
@@ -913,6 +981,13 @@ __device__ void dq_elementwise(const BwdTcParams& p, const QUnit& w, const BBars
   const uint64_t dl2 = ptx::f2_pack(dl, dl);
   bool ok = true;
   for (int j = 0; ok && j < w.steps; ++j) {
+    // explicit mask: this query row's bits over the key tile (loaded first)
+    uint64_t mbits = ~0ull;
+    if constexpr (MASK) {
+      const int i = w.m * T + row;
+      const int64_t mb = p.mask_shared ? 0 : w.b;
+      mbits = i < p.Lq ? mask_bits(p.rbits + ((mb * p.Lq + i) * p.n_tk + j) * 4, grp) : 0ull;
+    }
     ok = __all_sync(kFull, bwait(br, p.status, br.bar(I::sFull), j & 1, kRoleSoftmax));
     if (!ok) break;
     ptx::tc_fence_after();
@@ -936,6 +1011,10 @@ __device__ void dq_elementwise(const BwdTcParams& p, const QUnit& w, const BBars
     if (climit < TH) {
 #pragma unroll
       for (int c = 0; c < TH; ++c) pr[c] = c < climit ? pr[c] : 0.f;
+    }
+    if constexpr (MASK) {
+#pragma unroll
+      for (int c = 0; c < TH; ++c) pr[c] = ((mbits >> c) & 1ull) ? pr[c] : 0.f;
     }
     ok = __all_sync(kFull, bwait(br, p.status, br.bar(I::dpFull), j & 1, kRoleSoftmax));
     if (!ok) break;
@@ -987,7 +1066,7 @@ __device__ void dq_elementwise(const BwdTcParams& p, const QUnit& w, const BBars
   }
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool MASK>
 __global__ void __launch_bounds__(kThreadsB, 1)
     bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v,
@@ -1025,7 +1104,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   } else if (warp == kMmaWarp) {
     dq_mma<D, BF16>(p, w, br, smem, tmem);
   } else {
-    dq_elementwise<D, BF16>(p, w, br, tmem);
+    dq_elementwise<D, BF16, MASK>(p, w, br, tmem);
   }
   ptx::tc_fence_before();
   __syncthreads();
@@ -1047,7 +1126,7 @@ void launch_prep(const BwdTcParams& p, const void* o, const Strides& so, const v
                                                    so, sdo);
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool MASK>
 cudaError_t launch_bwd_tc_d(const CUtensorMap (&maps)[4], const BwdTcParams& p, const void* o,
                             const Strides& so, const void* dO, const Strides& sdo,
                             const float* lse, float* nlse2, float* delta, cudaStream_t stream) {
@@ -1061,11 +1140,12 @@ cudaError_t launch_bwd_tc_d(const CUtensorMap (&maps)[4], const BwdTcParams& p, 
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  auto dkv = p.splits > 1 ? bwd_dkv_tc_kernel<D, BF16, true> : bwd_dkv_tc_kernel<D, BF16, false>;
+  auto dkv = p.splits > 1 ? bwd_dkv_tc_kernel<D, BF16, true, MASK>
+                          : bwd_dkv_tc_kernel<D, BF16, false, MASK>;
   e = cudaFuncSetAttribute(dkv, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kvSmem);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(bwd_dq_tc_kernel<D, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::qSmem);
+    e = cudaFuncSetAttribute(bwd_dq_tc_kernel<D, BF16, MASK>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::qSmem);
   if (e != cudaSuccess) return e;
   dkv<<<static_cast<unsigned>(p.n_tk * p.B * p.Hkv * p.splits), kThreadsB, C::kvSmem, stream>>>(
       maps[0], maps[1], maps[2], maps[3], p);
@@ -1077,9 +1157,19 @@ cudaError_t launch_bwd_tc_d(const CUtensorMap (&maps)[4], const BwdTcParams& p, 
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  bwd_dq_tc_kernel<D, BF16><<<static_cast<unsigned>(p.n_tq * p.B * p.Hq), kThreadsB, C::qSmem, stream>>>(
-      maps[0], maps[1], maps[2], maps[3], p);
+  bwd_dq_tc_kernel<D, BF16, MASK>
+      <<<static_cast<unsigned>(p.n_tq * p.B * p.Hq), kThreadsB, C::qSmem, stream>>>(
+          maps[0], maps[1], maps[2], maps[3], p);
   return cudaGetLastError();
+}
+
+template <int D, bool BF16>
+cudaError_t launch_bwd_tc_m(const CUtensorMap (&maps)[4], const BwdTcParams& p, const void* o,
+                            const Strides& so, const void* dO, const Strides& sdo,
+                            const float* lse, float* nlse2, float* delta, cudaStream_t stream) {
+  return p.rbits != nullptr
+             ? launch_bwd_tc_d<D, BF16, true>(maps, p, o, so, dO, sdo, lse, nlse2, delta, stream)
+             : launch_bwd_tc_d<D, BF16, false>(maps, p, o, so, dO, sdo, lse, nlse2, delta, stream);
 }
 
 }  // namespace
@@ -1096,11 +1186,16 @@ int bwd_tc_splits(int B, int Hkv, int Lk, int num_sms) {
   return static_cast<int>(s < 16 ? s : 16);
 }
 
-int64_t bwd_tc_workspace_bytes(int B, int Hq, int Hkv, int Lq, int Lk, int D, int num_sms) {
+// Workspace: -LSE log2(e) and delta [B*Hq, Lq rounded up to 128], the fp32
+// partials of split key tiles, the explicit mask's row and column bits.
+int64_t bwd_tc_workspace_bytes(int B, int Hq, int Hkv, int Lq, int Lk, int D, int num_sms,
+                               int mask_batches) {
   const int64_t lqp = (static_cast<int64_t>(Lq) + T - 1) / T * T;
+  const int64_t lkp = (static_cast<int64_t>(Lk) + T - 1) / T * T;
   const int splits = bwd_tc_splits(B, Hkv, Lk, num_sms);
   const int64_t part = splits > 1 ? static_cast<int64_t>(splits) * 2 * B * Hkv * Lk * D * 4 : 0;
-  return 2 * static_cast<int64_t>(B) * Hq * lqp * 4 + part;
+  const int64_t bits = static_cast<int64_t>(mask_batches) * (Lq * (lkp / 8) + Lk * (lqp / 8));
+  return 2 * static_cast<int64_t>(B) * Hq * lqp * 4 + part + bits;
 }
 
 cudaError_t launch_bwd_tc(const CUtensorMap (&maps)[4], const void* o, const Strides& so,
@@ -1108,6 +1203,7 @@ cudaError_t launch_bwd_tc(const CUtensorMap (&maps)[4], const void* o, const Str
                           const Strides& sdq, void* dk, const Strides& sdk, void* dv,
                           const Strides& sdv, void* workspace, int B, int Hq, int Hkv, int Lq,
                           int Lk, int D, float sm_scale, int causal, const int32_t* valid_len,
+                          const uint8_t* mask, int64_t mask_batch_stride, int64_t mask_row_stride,
                           bool bf16, int num_sms, int* status, cudaStream_t stream) {
   BwdTcParams p;
   p.splits = bwd_tc_splits(B, Hkv, Lk, num_sms);
@@ -1122,6 +1218,23 @@ cudaError_t launch_bwd_tc(const CUtensorMap (&maps)[4], const void* o, const Str
   float* nlse2 = static_cast<float*>(workspace);
   float* delta = nlse2 + static_cast<int64_t>(B) * Hq * p.Lqp;
   p.part = delta + static_cast<int64_t>(B) * Hq * p.Lqp;  // used when splits > 1
+  const int64_t part_floats =
+      p.splits > 1 ? static_cast<int64_t>(p.splits) * 2 * B * Hkv * Lk * D : 0;
+  p.rbits = nullptr;
+  p.cbits = nullptr;
+  p.mask_shared = mask_batch_stride == 0 ? 1 : 0;
+  if (mask != nullptr) {
+    const int mB = p.mask_shared ? 1 : B;
+    uint32_t* rbits = reinterpret_cast<uint32_t*>(p.part + part_floats);
+    uint32_t* cbits = rbits + static_cast<int64_t>(mB) * Lq * ((Lk + T - 1) / T) * 4;
+    p.rbits = rbits;
+    p.cbits = cbits;
+    bwd_mask_pack_kernel<<<dim3((Lk + T - 1) / T, (Lq + T - 1) / T, mB), 256, 0, stream>>>(
+        mask, mask_batch_stride, mask_row_stride, Lq, Lk, (Lq + T - 1) / T, (Lk + T - 1) / T,
+        rbits, cbits);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   p.nlse2 = nlse2;
   p.delta = delta;
   p.dq = dq;
@@ -1142,11 +1255,11 @@ cudaError_t launch_bwd_tc(const CUtensorMap (&maps)[4], const void* o, const Str
   // K, V and dO tile with zeros (S and dP unchanged; the extra columns of dQ,
   // dK and dV are 0) and the epilogues store only the D columns.
   if (D == 16 || D == 32 || D == 64)
-    return bf16 ? launch_bwd_tc_d<64, true>(maps, p, o, so, dO, sdo, lse, nlse2, delta, stream)
-                : launch_bwd_tc_d<64, false>(maps, p, o, so, dO, sdo, lse, nlse2, delta, stream);
+    return bf16 ? launch_bwd_tc_m<64, true>(maps, p, o, so, dO, sdo, lse, nlse2, delta, stream)
+                : launch_bwd_tc_m<64, false>(maps, p, o, so, dO, sdo, lse, nlse2, delta, stream);
   if (D == 128)
-    return bf16 ? launch_bwd_tc_d<128, true>(maps, p, o, so, dO, sdo, lse, nlse2, delta, stream)
-                : launch_bwd_tc_d<128, false>(maps, p, o, so, dO, sdo, lse, nlse2, delta, stream);
+    return bf16 ? launch_bwd_tc_m<128, true>(maps, p, o, so, dO, sdo, lse, nlse2, delta, stream)
+                : launch_bwd_tc_m<128, false>(maps, p, o, so, dO, sdo, lse, nlse2, delta, stream);
   return cudaErrorInvalidValue;
 }
 

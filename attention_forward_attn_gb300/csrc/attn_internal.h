@@ -114,12 +114,14 @@ cudaError_t launch_bwd(const void* q, const void* k, const void* v, const void* 
 // key tiles per SM the dK/dV kernel splits each key tile over several CTAs
 // (bwd_tc_splits) and the workspace also holds their fp32 partial sums.
 int bwd_tc_splits(int B, int Hkv, int Lk, int num_sms);
-int64_t bwd_tc_workspace_bytes(int B, int Hq, int Hkv, int Lq, int Lk, int D, int num_sms);
+int64_t bwd_tc_workspace_bytes(int B, int Hq, int Hkv, int Lq, int Lk, int D, int num_sms,
+                               int mask_batches);
 cudaError_t launch_bwd_tc(const CUtensorMap (&maps)[4], const void* o, const Strides& so,
                           const void* dO, const Strides& sdo, const float* lse, void* dq,
                           const Strides& sdq, void* dk, const Strides& sdk, void* dv,
                           const Strides& sdv, void* workspace, int B, int Hq, int Hkv, int Lq,
                           int Lk, int D, float sm_scale, int causal, const int32_t* valid_len,
+                          const uint8_t* mask, int64_t mask_batch_stride, int64_t mask_row_stride,
                           bool bf16, int num_sms, int* status, cudaStream_t stream);
 
 // SIMT cross-check forward.

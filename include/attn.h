@@ -276,6 +276,29 @@ attn_status_t attn_bwd_strided(const void* q, const attn_strides_t* q_strides, c
                                attn_stream_t stream);
 
 /*
+ * attn_bwd_masked -- attn_bwd_strided with the explicit boolean mask of
+ * attn_fwd_masked (mask[b*mask_batch_stride + i*mask_row_stride + j] != 0
+ * keeps key j for query i; mask_batch_stride 0: one [Lq, Lk] mask for every
+ * batch; intersected with causal and valid_len).  A pre-pass packs the mask
+ * into bits over keys (for the dQ kernel) and over queries (for the dK/dV
+ * kernel); every masked (query, key) pair gets P = 0.  The workspace grows by
+ * 2 bits per position (1 for each layout) per mask batch.  Same arguments,
+ * preconditions and errors as attn_bwd_strided; negative mask strides give
+ * ATTN_ERR_STRIDE.
+ */
+attn_status_t attn_bwd_masked(const void* q, const attn_strides_t* q_strides, const void* k,
+                              const attn_strides_t* k_strides, const void* v,
+                              const attn_strides_t* v_strides, const void* o,
+                              const attn_strides_t* o_strides, const void* dO,
+                              const attn_strides_t* do_strides, const float* lse, void* dq,
+                              const attn_strides_t* dq_strides, void* dk,
+                              const attn_strides_t* dk_strides, void* dv,
+                              const attn_strides_t* dv_strides, int B, int Hq, int Hkv, int Lq,
+                              int Lk, int D, float sm_scale, int causal, const int32_t* valid_len,
+                              const uint8_t* mask, int64_t mask_batch_stride,
+                              int64_t mask_row_stride, attn_dtype_t dtype, attn_stream_t stream);
+
+/*
  * attn_bwd_simt -- the same gradients computed by SIMT kernels with fp32
  * arithmetic throughout (P and dS are never rounded to 16 bits): delta; dQ per
  * 64-row query tile; dK/dV per 64-key tile with all query heads of its group;

@@ -46,23 +46,26 @@ def _lib(cuda_lib_path):
     attn.status()
 
 
-def visible(B, Lq, Lk, causal, vl):
-    """[B, Lq, Lk] bool: key j visible to query i (causal: j <= i)."""
+def visible(B, Lq, Lk, causal, vl, mask=None):
+    """[B, Lq, Lk] bool: key j visible to query i (causal: j <= i; explicit
+    mask [B or 1, Lq, Lk])."""
     m = np.ones((B, Lq, Lk), dtype=bool)
     if causal:
         m &= np.tri(Lq, Lk, dtype=bool)[None]
+    if mask is not None:
+        m &= np.asarray(mask).reshape(-1, Lq, Lk) != 0
     if vl is not None:
         for b in range(B):
             m[b, :, int(vl[b]):] = False
     return m
 
 
-def operand_terms(qf, kf, vf, dof, sm, causal, vl, lse_ref):
+def operand_terms(qf, kf, vf, dof, sm, causal, vl, lse_ref, mask=None):
     """sum_i P |dO|, sum_i |dS| |q|, sum_j |dS| |k| and the plain sums of
     |dO|, |q|, |k| over the same index sets, per gradient element (float64)."""
     B, Hq, L, D = qf.shape
     G = Hq // kf.shape[1]
-    vis = visible(B, L, kf.shape[2], causal, vl)
+    vis = visible(B, L, kf.shape[2], causal, vl, mask)
     tv, tk, tq = np.zeros_like(vf), np.zeros_like(kf), np.zeros_like(qf)
     av, ak, aq = np.zeros_like(vf), np.zeros_like(kf), np.zeros_like(qf)
     for b in range(B):
@@ -84,7 +87,7 @@ def operand_terms(qf, kf, vf, dof, sm, causal, vl, lse_ref):
     return (tq, tk, tv), (aq, ak, av)
 
 
-def run_case(B, Hq, Hkv, L, D, dtype, causal, vl, seed, impl, Lk=None):
+def run_case(B, Hq, Hkv, L, D, dtype, causal, vl, seed, impl, Lk=None, mask=None):
     q, k, v, vl_t = wl.make_inputs(B, Hq, Hkv, L, D, dtype, seed=seed, valid_len=vl, Lk=Lk)
     gen = torch.Generator().manual_seed(seed + 1)
     do = torch.randn(B, Hq, L, D, generator=gen).to(wl.TORCH_DTYPE[dtype])
@@ -92,24 +95,26 @@ def run_case(B, Hq, Hkv, L, D, dtype, causal, vl, seed, impl, Lk=None):
     qd, kd, vd, dod = q.to(dev), k.to(dev), v.to(dev), do.to(dev)
     vld = None if vl_t is None else vl_t.to(dev)
     sm = 1.0 / math.sqrt(D)
-    o, lse = attn.attn_fwd_strided(qd, kd, vd, causal=causal, sm_scale=sm, valid_len=vld)
+    md = None if mask is None else torch.from_numpy(mask).to(dev)
+    o, lse = attn.attn_fwd_strided(qd, kd, vd, causal=causal, sm_scale=sm, valid_len=vld, mask=md)
     dq, dk, dv = attn.attn_bwd(qd, kd, vd, o, lse, dod, causal=causal, sm_scale=sm, valid_len=vld,
-                               impl=impl)
+                               impl=impl, mask=md)
     st, code = attn.status()
     assert st == attn.ATTN_OK, "device status %d (code %#x)" % (st, code)
     f = lambda t: t.double().numpy()
     vl_np = None if vl is None else np.array(vl, np.int32)
     qf, kf, vf, dof = f(q), f(k), f(v), f(do)
-    ref = oracle.attn_bwd_f64(qf, kf, vf, dof, sm, causal=causal, valid_len=vl_np)
+    ref = oracle.attn_bwd_f64(qf, kf, vf, dof, sm, causal=causal, valid_len=vl_np, mask=mask)
     u = 2.0 ** -8 if dtype == wl.BF16 else 2.0 ** -11
-    o_ref, lse_ref = oracle.attn_fwd_f64(qf, kf, vf, sm, causal=causal, valid_len=vl_np)
+    o_ref, lse_ref = oracle.attn_fwd_f64(qf, kf, vf, sm, causal=causal, valid_len=vl_np, mask=mask)
     e = u * np.sum(np.abs(dof * o_ref), axis=-1, keepdims=True)   # [B, Hq, L, 1]
-    pk, _ = oracle.attn_fwd_f64(qf, kf, kf, sm, causal=causal, valid_len=vl_np)
-    _, _, pq = oracle.attn_bwd_f64(qf, kf, vf, e * np.abs(qf), sm, causal=causal, valid_len=vl_np)
+    pk, _ = oracle.attn_fwd_f64(qf, kf, kf, sm, causal=causal, valid_len=vl_np, mask=mask)
+    _, _, pq = oracle.attn_bwd_f64(qf, kf, vf, e * np.abs(qf), sm, causal=causal, valid_len=vl_np,
+                                   mask=mask)
     terms = [sm * e * np.abs(pk), sm * pq, np.zeros_like(vf)]
     if impl == "tc":
         rel, ab = operand_terms(qf, kf, vf, dof, sm, causal, vl_np,
-                                lse_ref.reshape(B, Hq, L).astype(np.float64))
+                                lse_ref.reshape(B, Hq, L).astype(np.float64), mask)
         a = 0.0 if dtype == wl.BF16 else 2.0 ** -25
         scale = (sm, sm, 1.0)
         terms = [t + c * (u * r + a * s) for t, c, r, s in zip(terms, scale, rel, ab)]
@@ -307,3 +312,99 @@ def test_bwd_tc_query_and_key_lengths(Lq, Lk, causal, vl, D, dtype):
     (keys after the last query get zero gradients under causality), more
     queries than keys (late queries see every key), padding, an empty batch."""
     run_case(2, 4, 2, Lq, D, dtype, causal, vl, seed=Lq + Lk + D, impl="tc", Lk=Lk)
+
+
+def make_mask(kind, B, Lq, Lk, rng):
+    if kind.startswith("random"):
+        m = rng.random((B, Lq, Lk)) < float(kind.split("_")[1])
+    elif kind == "blocks":  # whole 128 x 128 tiles kept or removed, plus a ragged edge
+        tiles = rng.random((B, (Lq + 127) // 128, (Lk + 127) // 128)) < 0.5
+        tiles[:, :, 0] = True
+        m = np.repeat(np.repeat(tiles, 128, axis=1), 128, axis=2)[:, :Lq, :Lk].copy()
+        m[:, :, Lk // 3: Lk // 3 + 5] = False
+    elif kind == "empty_rows":  # fully masked rows and a fully masked batch
+        m = rng.random((B, Lq, Lk)) < 0.4
+        m[0, 5:140, :] = False
+        m[-1] = False
+    elif kind == "shared":  # one [Lq, Lk] mask for every batch
+        m = rng.random((Lq, Lk)) < 0.3
+    else:
+        raise ValueError(kind)
+    return m.astype(np.uint8)
+
+
+@pytest.mark.parametrize("kind", ["random_0.5", "random_0.05", "blocks", "empty_rows", "shared"])
+@pytest.mark.parametrize("D, dtype", [(128, wl.BF16), (64, wl.F16), (32, wl.BF16)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_masked_matches_oracle(kind, D, dtype, causal):
+    """The explicit mask of attn_fwd_masked in the backward (attn_bwd_masked),
+    intersected with causal and padding, Lq != Lk."""
+    B, Lq, Lk = 2, 300, 400
+    rng = np.random.default_rng(hash((kind, D, causal)) % 1000)
+    mk = make_mask(kind, B, Lq, Lk, rng)
+    run_case(B, 4, 2, Lq, D, dtype, causal, [400, 233], seed=900 + D, impl="tc", Lk=Lk, mask=mk)
+
+
+def test_bwd_restated_causal_mask_bit_identical():
+    """C4's shapes: a shared tril mask with causal=False gives the gradients of
+    causal=True bit for bit (the masked pairs get P = 0 exactly, and the
+    extra tiles add exact zeros)."""
+    w = wl.WORKLOADS["C4"]
+    q, k, v, _ = wl.workload_inputs(w)
+    do = torch.randn(q.shape, generator=torch.Generator().manual_seed(w.seed + 100)).to(q.dtype)
+    dev = torch.device("cuda")
+    qd, kd, vd, dod = q.to(dev), k.to(dev), v.to(dev), do.to(dev)
+    o, lse = attn.attn_fwd(qd, kd, vd, causal=True, sm_scale=w.sm_scale)
+    ref = attn.attn_bwd(qd, kd, vd, o, lse, dod, causal=True, sm_scale=w.sm_scale)
+    tril = torch.tril(torch.ones(w.L, w.L, dtype=torch.bool, device=dev))
+    got = attn.attn_bwd(qd, kd, vd, o, lse, dod, sm_scale=w.sm_scale, mask=tril)
+    assert attn.status() == (attn.ATTN_OK, 0)
+    for g, r in zip(got, ref):
+        assert torch.equal(g.view(torch.int16), r.view(torch.int16))
+
+
+def test_bwd_masked_full_size_sampled_rows():
+    """C4's shapes with the block-sparse masks of the forward's test (a local
+    band plus the first keys, random partial tiles; per batch), causal:
+    sampled dQ rows and the dK/dV rows of two K/V heads against the oracle,
+    with the magnitude-based bound of test_bwd_full_size_sampled_rows."""
+    w = wl.WORKLOADS["C4"]
+    q, k, v, _ = wl.workload_inputs(w)
+    L = w.L
+    i = np.arange(L)[:, None]
+    j = np.arange(L)[None, :]
+    keep = (np.abs(i - j) < 512) | (j < 256)
+    rng = np.random.default_rng(5)
+    for mb in range(L // 128):
+        t = rng.integers(0, L // 128)
+        keep[mb * 128:(mb + 1) * 128, t * 128:(t + 1) * 128] |= rng.random((128, 128)) < 0.3
+    mk = np.stack([keep, ~np.roll(keep, 1, axis=1) | (j == 0), keep, keep]).astype(np.uint8)
+    do = torch.randn(q.shape, generator=torch.Generator().manual_seed(w.seed + 7)).to(q.dtype)
+    dev = torch.device("cuda")
+    qd, kd, vd, dod, md = q.to(dev), k.to(dev), v.to(dev), do.to(dev), torch.from_numpy(mk).to(dev)
+    o, lse = attn.attn_fwd_strided(qd, kd, vd, causal=True, sm_scale=w.sm_scale, mask=md)
+    dq, dk, dv = attn.attn_bwd(qd, kd, vd, o, lse, dod, causal=True, sm_scale=w.sm_scale, mask=md)
+    assert attn.status() == (attn.ATTN_OK, 0)
+    B, Hq, _, D = q.shape
+    Hkv = k.shape[1]
+    rows = sorted({0, 1, 127, 128, 511, 512, 2047, 2048, L - 1} | set(rng.integers(0, L, 6).tolist()))
+    qr = np.array([(b * Hq + h) * L + r for b in (0, 1) for h in (0, 5, 31) for r in rows])
+    kr = np.array([z * L + r for z in (0, Hkv + 3) for r in rows])  # batch 0 head 0, batch 1 head 3
+    f = lambda t: t.double().numpy()
+    r_dq, qm, r_dk, r_dv, km = oracle.attn_bwd_rows_f64(f(q), f(k), f(v), f(do), w.sm_scale,
+                                                        causal=True, q_rows=qr, k_rows=kr, mask=mk)
+    u = 2.0 ** -8
+    mq, mkk, mdo = (float(t.float().abs().max()) for t in (q, k, do))
+    sm = w.sm_scale
+    extra = {"dq": sm * mkk * (u * qm[:, 1] + u * qm[:, 0]),
+             "dk": sm * mq * (u * km[:, 2] + u * km[:, 0]),
+             "dv": mdo * u * km[:, 1]}
+    got = {"dq": dq.reshape(-1, D)[torch.from_numpy(qr).to(dev)],
+           "dk": dk.reshape(-1, D)[torch.from_numpy(kr).to(dev)],
+           "dv": dv.reshape(-1, D)[torch.from_numpy(kr).to(dev)]}
+    for gname, ref in (("dq", r_dq), ("dk", r_dk), ("dv", r_dv)):
+        g = got[gname].float().cpu().double().numpy()
+        err = np.abs(g - ref)
+        bound = 1e-2 * np.abs(ref) + 1e-4 * np.abs(ref).max() + extra[gname][:, None]
+        assert np.all(err <= bound), "%s: %d of %d out of tolerance (max err %g, ref max %g)" % (
+            gname, int((err > bound).sum()), err.size, float(err.max()), float(np.abs(ref).max()))
