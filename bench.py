@@ -666,17 +666,21 @@ def run_backward(args, local):
     lines = []
     impls = ("tc", "simt") if args.bwd_impl == "both" else (args.bwd_impl,)
     for name in args.bwd_workloads.split(","):
-        w = wl.WORKLOADS[name]
+        # "C4M": C4's shapes with its causal mask given as an explicit boolean
+        # [L, L] mask (attn_bwd_masked; every tile computed, none skipped)
+        masked = name.endswith("M")
+        w = wl.WORKLOADS[name[:-1] if masked else name]
         q, k, v, vl = wl.workload_inputs(w)
         q_d, k_d, v_d = q.to(dev), k.to(dev), v.to(dev)
         vl_d = None if vl is None else vl.to(dev)
         gen = torch.Generator().manual_seed(w.seed + 100)
         do = torch.randn(q.shape, generator=gen).to(q.dtype).to(dev)
         o, lse = attn.attn_fwd(q_d, k_d, v_d, causal=w.causal, sm_scale=w.sm_scale, valid_len=vl_d)
-        for impl in impls:
+        mk = torch.tril(torch.ones(w.L, w.L, dtype=torch.bool, device=dev)) if masked else None
+        for impl in (("tc",) if masked else impls):
             def call():
-                return attn.attn_bwd(q_d, k_d, v_d, o, lse, do, causal=w.causal,
-                                     sm_scale=w.sm_scale, valid_len=vl_d, impl=impl)
+                return attn.attn_bwd(q_d, k_d, v_d, o, lse, do, causal=w.causal and not masked,
+                                     sm_scale=w.sm_scale, valid_len=vl_d, impl=impl, mask=mk)
 
             for _ in range(max(1, min(args.warmup, 3))):
                 flush.zero_()
@@ -706,8 +710,11 @@ def run_backward(args, local):
                         "unit": "TFLOP/s", "frac": round(tf / fp32_peak, 4),
                         "peak_source": "152 SMs x 128 FP32 lanes x 2 x sm_max_mhz"}
             lines.append({"metric": "attention backward TFLOP/s (2.5x the forward's nominal FLOPs)",
-                          "impl": "attn_bwd" if impl == "tc" else "attn_bwd_simt",
-                          "workload": "%s shapes: %s" % (name, w.description), "value": round(tf, 3),
+                          "impl": ("attn_bwd_masked" if masked else "attn_bwd") if impl == "tc"
+                          else "attn_bwd_simt",
+                          "workload": "%s shapes: %s%s" % (name, w.description,
+                                                           ", as an explicit tril mask" if masked else ""),
+                          "value": round(tf, 3),
                           "unit": "TFLOP/s", "ms_per_call": round(ms, 3), "roofline": roof,
                           "timing": "median of %d calls, L2 flushed before each" % n,
                           "dtype": w.dtype, "data": "synthetic"})

@@ -280,3 +280,13 @@ def test_bwd_strided_stride_validation(lib, which, strides, expected):
                               A16, A16, st["dq"], A16, st["dk"], A16, st["dv"], 1, 4, 2, 64, 64, 64,
                               0.125, 1, None, attn.ATTN_BF16, None)
     assert binding.STATUS_NAMES[rc] == expected
+
+
+@pytest.mark.parametrize("msb, msr", [(-1, 64), (0, -64)])
+def test_bwd_masked_negative_mask_strides_rejected(lib, msb, msr):
+    """attn_bwd_masked rejects negative mask strides on the host (the fake
+    addresses are never dereferenced: the call fails validation)."""
+    rc = lib.attn_bwd_masked(A16, None, A16, None, A16, None, A16, None, A16, None, A16, A16, None,
+                             A16, None, A16, None, 1, 4, 2, 64, 64, 64, 0.125, 1, None, A16, msb,
+                             msr, attn.ATTN_BF16, None)
+    assert binding.STATUS_NAMES[rc] == "ATTN_ERR_STRIDE"
