@@ -90,6 +90,13 @@ struct BwdTcParams {
   const uint32_t* rbits;
   const uint32_t* cbits;
   int mask_shared;
+  // tiles with a kept position (bwd_mask_lists_kernel): per key tile the
+  // query tiles to visit, ascending (klist [mB][n_tk][n_tq], kcount
+  // [mB][n_tk]); per query tile the key tiles (qlist [mB][n_tq][n_tk], qcount)
+  const int* klist;
+  const int* kcount;
+  const int* qlist;
+  const int* qcount;
   float scale_log2;               // sm_scale log2(e)
   float sm_scale;
   int causal;
@@ -322,10 +329,13 @@ __global__ void __launch_bounds__(256) bwd_tc_prep_kernel(const void* __restrict
 __global__ void __launch_bounds__(256) bwd_mask_pack_kernel(const uint8_t* __restrict__ mask,
                                                             int64_t msb, int64_t msr, int Lq,
                                                             int Lk, int n_tq, int n_tk,
-                                                            uint32_t* rbits, uint32_t* cbits) {
+                                                            uint32_t* rbits, uint32_t* cbits,
+                                                            uint8_t* vis) {
   constexpr int kPitch = 132;
   __shared__ uint8_t blk[T * kPitch];
+  __shared__ int any_kept;
   const int n = blockIdx.x, m = blockIdx.y, mb = blockIdx.z;
+  if (threadIdx.x == 0) any_kept = 0;
   const uint8_t* src = mask + mb * msb;
   for (int idx = threadIdx.x; idx < T * T; idx += 256) {
     const int r = idx / T, c = idx % T;
@@ -342,6 +352,7 @@ __global__ void __launch_bounds__(256) bwd_mask_pack_kernel(const uint8_t* __res
     if (lane == 0 && i < Lq)
       *reinterpret_cast<uint4*>(rbits + ((static_cast<int64_t>(mb) * Lq + i) * n_tk + n) * 4) =
           make_uint4(wd[0], wd[1], wd[2], wd[3]);
+    if (lane == 0 && (wd[0] | wd[1] | wd[2] | wd[3]) != 0u) any_kept = 1;
   }
   for (int c = warp; c < T; c += 8) {  // key column c of the block: its 128 query bits
     uint32_t wd[4];
@@ -351,6 +362,36 @@ __global__ void __launch_bounds__(256) bwd_mask_pack_kernel(const uint8_t* __res
     if (lane == 0 && j < Lk)
       *reinterpret_cast<uint4*>(cbits + ((static_cast<int64_t>(mb) * Lk + j) * n_tq + m) * 4) =
           make_uint4(wd[0], wd[1], wd[2], wd[3]);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) vis[(static_cast<int64_t>(mb) * n_tq + m) * n_tk + n] = any_kept ? 1 : 0;
+}
+
+// From the block flags: per key tile n the query tiles with a kept position
+// (under causality only m >= n), per query tile m the key tiles (causal: only
+// j <= m), each list ascending.  One thread per list.
+__global__ void __launch_bounds__(256) bwd_mask_lists_kernel(const uint8_t* __restrict__ vis,
+                                                             int mB, int n_tq, int n_tk,
+                                                             int causal, int* klist, int* kcount,
+                                                             int* qlist, int* qcount) {
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x;
+  const int64_t nk = static_cast<int64_t>(mB) * n_tk;
+  if (t < nk) {
+    const int64_t mb = t / n_tk;
+    const int n = static_cast<int>(t - mb * n_tk);
+    int c = 0;
+    for (int m = causal ? n : 0; m < n_tq; ++m)
+      if (vis[(mb * n_tq + m) * n_tk + n]) klist[t * n_tq + c++] = m;
+    kcount[t] = c;
+  } else if (t < nk + static_cast<int64_t>(mB) * n_tq) {
+    const int64_t u = t - nk;
+    const int64_t mb = u / n_tq;
+    const int m = static_cast<int>(u - mb * n_tq);
+    const int jend = causal ? min(m + 1, n_tk) : n_tk;
+    int c = 0;
+    for (int j = 0; j < jend; ++j)
+      if (vis[(mb * n_tq + m) * n_tk + j]) qlist[u * n_tk + c++] = j;
+    qcount[u] = c;
   }
 }
 
@@ -391,9 +432,16 @@ struct KvIdx {
 // with the most query tiles start first.
 struct KvUnit {
   int n, s, b, hkv, kv_len, m_lo, t0, steps;  // steps [t0, t0 + steps) of the key tile
+  const int* tiles;  // explicit mask: the query tiles to visit (else every m >= m_lo)
 };
 
-template <bool SPLIT>
+// Query tile of step t of a dK/dV unit.
+__device__ __forceinline__ int kv_qtile(const KvUnit& w, int G, int t) {
+  const int k = (w.t0 + t) / G;
+  return w.tiles != nullptr ? w.tiles[k] : w.m_lo + k;
+}
+
+template <bool SPLIT, bool MASK>
 __device__ __forceinline__ KvUnit kv_unit(const BwdTcParams& p) {
   const int per = p.B * p.Hkv;
   const int splits = SPLIT ? p.splits : 1;
@@ -406,7 +454,13 @@ __device__ __forceinline__ KvUnit kv_unit(const BwdTcParams& p) {
   w.hkv = z - w.b * p.Hkv;
   w.kv_len = kv_len_of(p, w.b);
   w.m_lo = p.causal ? w.n : 0;
-  const int total = (w.n * T < w.kv_len && w.m_lo < p.n_tq) ? p.G * (p.n_tq - w.m_lo) : 0;
+  int total = (w.n * T < w.kv_len && w.m_lo < p.n_tq) ? p.G * (p.n_tq - w.m_lo) : 0;
+  w.tiles = nullptr;
+  if constexpr (MASK) {  // only the query tiles with a kept position
+    const int64_t kl = (p.mask_shared ? 0 : static_cast<int64_t>(w.b)) * p.n_tk + w.n;
+    w.tiles = p.klist + kl * p.n_tq;
+    total = (w.n * T < w.kv_len) ? p.G * p.kcount[kl] : 0;
+  }
   if constexpr (SPLIT) {
     const int chunk = (total + splits - 1) / splits;
     w.t0 = min(total, w.s * chunk);
@@ -440,7 +494,7 @@ __device__ void dkv_producer(const BwdTcParams& p, const KvUnit& w, const BBars&
   for (; t < w.steps; ++t) {
     const uint32_t s = static_cast<uint32_t>(t % NS);
     if (!bwait(br, p.status, br.bar(I::inEmpty + s), ((t / NS) & 1) ^ 1, kRoleProducer)) break;
-    const int mi = w.m_lo + (w.t0 + t) / p.G;  // t0 = 0 without splits
+    const int mi = kv_qtile(w, p.G, t);
     const int hq = w.hkv * p.G + (w.t0 + t) % p.G;
     const uint32_t st = smem + C::kvOffIn + s * C::kvStageBytes;
     const uint32_t full = br.bar(I::inFull + s);
@@ -591,7 +645,7 @@ __device__ void dkv_elementwise(const BwdTcParams& p, const KvUnit& w, const BBa
   for (int t = 0; ok && t < w.steps; ++t) {
     const uint32_t s = static_cast<uint32_t>(t % NS);
     const uint32_t st = smem + C::kvOffIn + s * C::kvStageBytes;
-    const int mi = w.m_lo + ((SPLIT ? w.t0 : 0) + t) / p.G;
+    const int mi = MASK ? kv_qtile(w, p.G, t) : w.m_lo + ((SPLIT ? w.t0 : 0) + t) / p.G;
     // explicit mask: this key row's bits over the query tile (loaded first)
     uint64_t mbits = ~0ull;
     if constexpr (MASK) {
@@ -770,7 +824,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   const BBars br{smem + C::kvOffBar, I::n};
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const KvUnit w = kv_unit<SPLIT>(p);
+  const KvUnit w = kv_unit<SPLIT, MASK>(p);
   if (threadIdx.x == 0) {
     for (int i = 0; i < I::n; ++i) {
       const bool ew = (i == I::pReady || i == I::dsReady || i == I::dpFree);
@@ -835,8 +889,15 @@ struct QIdx {
 // Query tiles vary slowest, the last (longest under causality) first.
 struct QUnit {
   int m, b, hq, hkv, kv_len, steps;
+  const int* tiles;  // explicit mask: the key tiles to visit (else 0, 1, ...)
 };
 
+// Key tile of step j of a dQ unit.
+__device__ __forceinline__ int q_ktile(const QUnit& w, int j) {
+  return w.tiles != nullptr ? w.tiles[j] : j;
+}
+
+template <bool MASK>
 __device__ __forceinline__ QUnit q_unit(const BwdTcParams& p) {
   const int per = p.B * p.Hq;
   const int u = static_cast<int>(blockIdx.x) / per;
@@ -849,6 +910,15 @@ __device__ __forceinline__ QUnit q_unit(const BwdTcParams& p) {
   w.kv_len = kv_len_of(p, w.b);
   const int kt = (w.kv_len + T - 1) / T;
   w.steps = min(p.causal ? min(w.m + 1, p.n_tk) : p.n_tk, kt);
+  w.tiles = nullptr;
+  if constexpr (MASK) {  // the listed key tiles below the valid_len cut
+    const int64_t ql = (p.mask_shared ? 0 : static_cast<int64_t>(w.b)) * p.n_tq + w.m;
+    w.tiles = p.qlist + ql * p.n_tk;
+    const int cnt = p.qcount[ql];
+    int k = 0;
+    while (k < cnt && w.tiles[k] < kt) ++k;
+    w.steps = k;
+  }
   return w;
 }
 
@@ -874,13 +944,14 @@ __device__ void dq_producer(const BwdTcParams& p, const QUnit& w, const BBars& b
   // which completes earlier
   int nk = 0, nv = 0;  // K and V tiles issued
   for (int j = 0; j < w.steps; ++j) {
+    const int kj = q_ktile(w, j);  // the key tile of step j
     if (!bwait(br, p.status, br.bar(I::kEmpty + j % KS), ((j / KS) & 1) ^ 1, kRoleProducer)) break;
     const uint32_t kf = br.bar(I::kFull + j % KS);
     ptx::mbar_arrive_expect_tx(kf, C::kTile);
 #pragma unroll
     for (int h = 0; h < D / 64; ++h)
       ptx::tma_load_4d_hint(smem + C::qOffK + (j % KS) * C::kTile + h * C::kSlab, tm_k, kf, h * 64,
-                            j * T, w.hkv, w.b, pol_keep);
+                            kj * T, w.hkv, w.b, pol_keep);
     ++nk;
     if (!bwait(br, p.status, br.bar(I::vEmpty + j % VS), ((j / VS) & 1) ^ 1, kRoleProducer)) break;
     const uint32_t vf = br.bar(I::vFull + j % VS);
@@ -888,7 +959,7 @@ __device__ void dq_producer(const BwdTcParams& p, const QUnit& w, const BBars& b
 #pragma unroll
     for (int h = 0; h < D / 64; ++h)
       ptx::tma_load_4d_hint(smem + C::qOffV + (j % VS) * C::kTile + h * C::kSlab, tm_v, vf, h * 64,
-                            j * T, w.hkv, w.b, pol_keep);
+                            kj * T, w.hkv, w.b, pol_keep);
     ++nv;
   }
   bdrain(br.bar(I::qdFull), 0);
@@ -986,7 +1057,8 @@ __device__ void dq_elementwise(const BwdTcParams& p, const QUnit& w, const BBars
     if constexpr (MASK) {
       const int i = w.m * T + row;
       const int64_t mb = p.mask_shared ? 0 : w.b;
-      mbits = i < p.Lq ? mask_bits(p.rbits + ((mb * p.Lq + i) * p.n_tk + j) * 4, grp) : 0ull;
+      mbits = i < p.Lq ? mask_bits(p.rbits + ((mb * p.Lq + i) * p.n_tk + q_ktile(w, j)) * 4, grp)
+                       : 0ull;
     }
     ok = __all_sync(kFull, bwait(br, p.status, br.bar(I::sFull), j & 1, kRoleSoftmax));
     if (!ok) break;
@@ -1006,8 +1078,9 @@ __device__ void dq_elementwise(const BwdTcParams& p, const QUnit& w, const BBars
     ptx::mbar_arrive(br.bar(I::sFree));
     // visible key columns: c < climit (causal diagonal tile; last key tile)
     int climit = TH;
-    if (p.causal && j == w.m) climit = min(climit, row - grp * TH + 1);
-    climit = min(climit, w.kv_len - j * T - grp * TH);
+    const int kj = MASK ? q_ktile(w, j) : j;  // the key tile of step j
+    if (p.causal && kj == w.m) climit = min(climit, row - grp * TH + 1);
+    climit = min(climit, w.kv_len - kj * T - grp * TH);
     if (climit < TH) {
 #pragma unroll
       for (int c = 0; c < TH; ++c) pr[c] = c < climit ? pr[c] : 0.f;
@@ -1078,7 +1151,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   const BBars br{smem + C::qOffBar, I::n};
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const QUnit w = q_unit(p);
+  const QUnit w = q_unit<MASK>(p);
   if (threadIdx.x == 0) {
     for (int i = 0; i < I::n; ++i) {
       const bool ew = (i == I::sFree || i == I::dpFree || i == I::dsReady || i == I::dsReady + 1);
@@ -1195,7 +1268,10 @@ int64_t bwd_tc_workspace_bytes(int B, int Hq, int Hkv, int Lq, int Lk, int D, in
   const int splits = bwd_tc_splits(B, Hkv, Lk, num_sms);
   const int64_t part = splits > 1 ? static_cast<int64_t>(splits) * 2 * B * Hkv * Lk * D * 4 : 0;
   const int64_t bits = static_cast<int64_t>(mask_batches) * (Lq * (lkp / 8) + Lk * (lqp / 8));
-  return 2 * static_cast<int64_t>(B) * Hq * lqp * 4 + part + bits;
+  const int64_t ntq = lqp / T, ntk = lkp / T;
+  const int64_t flags = (static_cast<int64_t>(mask_batches) * ntq * ntk + 15) / 16 * 16;
+  const int64_t lists = static_cast<int64_t>(mask_batches) * (2 * ntq * ntk + ntq + ntk) * 4;
+  return 2 * static_cast<int64_t>(B) * Hq * lqp * 4 + part + bits + (mask_batches ? flags + lists : 0);
 }
 
 cudaError_t launch_bwd_tc(const CUtensorMap (&maps)[4], const void* o, const Strides& so,
@@ -1222,17 +1298,32 @@ cudaError_t launch_bwd_tc(const CUtensorMap (&maps)[4], const void* o, const Str
       p.splits > 1 ? static_cast<int64_t>(p.splits) * 2 * B * Hkv * Lk * D : 0;
   p.rbits = nullptr;
   p.cbits = nullptr;
+  p.klist = p.kcount = p.qlist = p.qcount = nullptr;
   p.mask_shared = mask_batch_stride == 0 ? 1 : 0;
   if (mask != nullptr) {
     const int mB = p.mask_shared ? 1 : B;
     uint32_t* rbits = reinterpret_cast<uint32_t*>(p.part + part_floats);
     uint32_t* cbits = rbits + static_cast<int64_t>(mB) * Lq * ((Lk + T - 1) / T) * 4;
+    const int ntq = (Lq + T - 1) / T, ntk = (Lk + T - 1) / T;
+    uint8_t* vis = reinterpret_cast<uint8_t*>(cbits + static_cast<int64_t>(mB) * Lk * ntq * 4);
+    int* klist = reinterpret_cast<int*>(vis + (static_cast<int64_t>(mB) * ntq * ntk + 15) / 16 * 16);
+    int* kcount = klist + static_cast<int64_t>(mB) * ntk * ntq;
+    int* qlist = kcount + static_cast<int64_t>(mB) * ntk;
+    int* qcount = qlist + static_cast<int64_t>(mB) * ntq * ntk;
     p.rbits = rbits;
     p.cbits = cbits;
-    bwd_mask_pack_kernel<<<dim3((Lk + T - 1) / T, (Lq + T - 1) / T, mB), 256, 0, stream>>>(
-        mask, mask_batch_stride, mask_row_stride, Lq, Lk, (Lq + T - 1) / T, (Lk + T - 1) / T,
-        rbits, cbits);
-    const cudaError_t e = cudaGetLastError();
+    p.klist = klist;
+    p.kcount = kcount;
+    p.qlist = qlist;
+    p.qcount = qcount;
+    bwd_mask_pack_kernel<<<dim3(ntk, ntq, mB), 256, 0, stream>>>(
+        mask, mask_batch_stride, mask_row_stride, Lq, Lk, ntq, ntk, rbits, cbits, vis);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int64_t nlists = static_cast<int64_t>(mB) * (ntk + ntq);
+    bwd_mask_lists_kernel<<<static_cast<unsigned>((nlists + 255) / 256), 256, 0, stream>>>(
+        vis, mB, ntq, ntk, causal, klist, kcount, qlist, qcount);
+    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   p.nlse2 = nlse2;
