@@ -10,9 +10,9 @@
 //
 // How: a pre-pass and two kernels, every product on the tensor core with an
 // fp32 accumulator in TMEM and P, dS rounded to the input dtype as operands:
-//   * pre-pass (one warp per row): delta_i and -LSE_i log2(e) into rows padded
-//     to a multiple of 128 (0 and -inf beyond L; -inf where the row sees no
-//     key), so that both kernels fetch them with aligned bulk copies;
+//   * pre-pass (D/8 lanes per row): delta_i and -LSE_i log2(e) into rows
+//     padded to a multiple of 128 (0 and -inf beyond Lq; -inf where the row
+//     sees no key), so that both kernels fetch them with aligned bulk copies;
 //   * dK/dV kernel, one CTA per (128-key tile, b, h_kv), K and V resident in
 //     shared memory.  Every (query head of the group, 128-row query tile) that
 //     sees the keys streams through a ring of Q, dO, LSE and delta stages.
@@ -22,7 +22,9 @@
 //     as 16-bit pairs into the S^T region, and dV += P^T dO, dK += dS^T Q
 //     read them from TMEM (dO and Q as MN-major operands); the next S^T goes
 //     into the dP^T region as soon as dP^T has been read.  TMEM: the two
-//     regions, dV, dK (512 columns at D = 128);
+//     regions, dV, dK (512 columns at D = 128).  With too few key tiles for
+//     the GPU (MQA), each key tile's steps are split over several CTAs that
+//     write fp32 partials, summed in a fixed order by a reduction kernel;
 //   * dQ kernel, one CTA per (128-row query tile, b, h_q), Q and dO resident,
 //     K and V streaming: S = Q K^T, dP = dO V^T, dS written to its own TMEM
 //     columns (two buffers), dQ += dS K (K as MN-major operand).  TMEM: S,
@@ -32,7 +34,11 @@
 // split the columns), warp 8 TMA producer, warp 9 MMA issuer (one elected
 // lane issues) and TMEM owner.  Causal tiles above the diagonal and key tiles
 // at or beyond valid_len[b] are never visited; masked (query, key) pairs get
-// P = 0, hence dS = 0.
+// P = 0, hence dS = 0.  An explicit mask is packed into bits over keys and
+// over queries by a pre-pass, which also lists the 128 x 128 blocks that keep
+// any position; the MASK instances visit only those.  Separate query and key
+// lengths (causal top-left) and strided operands throughout; D = 16 and 32 run
+// the D = 64 instances on zero-filled columns.
 //
 // Every mbarrier wait is bounded as in the forward: on a timeout the waiting
 // role records it in the device status word and raises the CTA's abort flag;
