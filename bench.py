@@ -648,7 +648,8 @@ def run_relative_table(args, local):
 
 def run_backward(args, local):
     """attn_bwd (tensor cores) and attn_bwd_simt (fp32 SIMT) on the C4, C2 and
-    C5 shapes (--bwd-workloads): ms per call with the forward's O and LSE already on the device,
+    C5 shapes, and attn_bwd_masked on C4M -- C4 with its causal mask given as
+    an explicit tril mask -- (--bwd-workloads): ms per call with the forward's O and LSE already on the device,
     L2 flushed before each call.  Work: the backward's five products (S
     recomputed, dP, dQ, dK, dV) = 2.5x the forward's nominal FLOPs.  The
     tensor-core path executes seven (S and dP in both of its kernels), 3.5x.
@@ -796,7 +797,7 @@ def main(argv=None):
                     help="instead of the headline line, one line per backward workload")
     ap.add_argument("--bwd-impl", default="both", choices=["both", "tc", "simt"],
                     help="--backward: which backward (attn_bwd, attn_bwd_simt or both)")
-    ap.add_argument("--bwd-workloads", default="C4,C2,C5",
+    ap.add_argument("--bwd-workloads", default="C4,C4M,C2,C5",
                     help="--backward: comma-separated workload shapes")
     args = ap.parse_args(argv)
     if args.warmup < 3:
