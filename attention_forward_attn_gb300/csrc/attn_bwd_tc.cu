@@ -448,12 +448,12 @@ __device__ __forceinline__ int kv_qtile(const KvUnit& w, int G, int t) {
 }
 
 template <bool SPLIT, bool MASK>
-__device__ __forceinline__ KvUnit kv_unit(const BwdTcParams& p) {
+__device__ __forceinline__ KvUnit kv_unit(const BwdTcParams& p, int unit) {
   const int per = p.B * p.Hkv;
   const int splits = SPLIT ? p.splits : 1;
   KvUnit w;
-  w.n = static_cast<int>(blockIdx.x) / (per * splits);
-  const int r = static_cast<int>(blockIdx.x) - w.n * per * splits;
+  w.n = unit / (per * splits);
+  const int r = unit - w.n * per * splits;
   w.s = SPLIT ? r / per : 0;
   const int z = r - w.s * per;
   w.b = z / p.Hkv;
@@ -816,13 +816,12 @@ __global__ void __launch_bounds__(256) bwd_dkv_reduce_kernel(const BwdTcParams p
                                               pk2<BF16>(acc[6] * mul, acc[7] * mul));
 }
 
-// SPLIT: key tiles split over several CTAs (p.splits > 1), fp32 partial rows.
-// MASK: an explicit mask (p.cbits).
+// One CTA of the dK/dV kernel on unit `unit`.  SPLIT: key tiles split over
+// several CTAs (p.splits > 1), fp32 partial rows.  MASK: an explicit mask.
 template <int D, bool BF16, bool SPLIT, bool MASK>
-__global__ void __launch_bounds__(kThreadsB, 1)
-    bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                      const __grid_constant__ CUtensorMap tm_v,
-                      const __grid_constant__ CUtensorMap tm_do, const BwdTcParams p) {
+__device__ __forceinline__ void dkv_cta(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
+                                        const CUtensorMap* tm_v, const CUtensorMap* tm_do,
+                                        const BwdTcParams& p, int unit) {
   using C = BCfg<D>;
   using I = KvIdx<C::kvStages>;
   extern __shared__ uint8_t smem_raw[];
@@ -830,7 +829,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   const BBars br{smem + C::kvOffBar, I::n};
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const KvUnit w = kv_unit<SPLIT, MASK>(p);
+  const KvUnit w = kv_unit<SPLIT, MASK>(p, unit);
   if (threadIdx.x == 0) {
     for (int i = 0; i < I::n; ++i) {
       const bool ew = (i == I::pReady || i == I::dsReady || i == I::dpFree);
@@ -844,8 +843,8 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     }
   }
   if (warp == kLoadWarp && lane == 0) {
-    ptx::prefetch_tensormap(&tm_q);
-    ptx::prefetch_tensormap(&tm_do);
+    ptx::prefetch_tensormap(tm_q);
+    ptx::prefetch_tensormap(tm_do);
   }
   if (warp == kMmaWarp) {
     ptx::tmem_alloc(br.tmem_word(), C::kTmemCols);
@@ -856,7 +855,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = ptx::ld_shared_volatile(br.tmem_word());
   if (warp == kLoadWarp) {
-    if (lane == 0) dkv_producer<D>(p, w, br, smem, &tm_q, &tm_k, &tm_v, &tm_do);
+    if (lane == 0) dkv_producer<D>(p, w, br, smem, tm_q, tm_k, tm_v, tm_do);
   } else if (warp == kMmaWarp) {
     dkv_mma<D, BF16>(p, w, br, smem, tmem);
   } else {
@@ -904,10 +903,10 @@ __device__ __forceinline__ int q_ktile(const QUnit& w, int j) {
 }
 
 template <bool MASK>
-__device__ __forceinline__ QUnit q_unit(const BwdTcParams& p) {
+__device__ __forceinline__ QUnit q_unit(const BwdTcParams& p, int unit) {
   const int per = p.B * p.Hq;
-  const int u = static_cast<int>(blockIdx.x) / per;
-  const int z = static_cast<int>(blockIdx.x) - u * per;
+  const int u = unit / per;
+  const int z = unit - u * per;
   QUnit w;
   w.m = p.n_tq - 1 - u;
   w.b = z / p.Hq;
@@ -1145,11 +1144,11 @@ __device__ void dq_elementwise(const BwdTcParams& p, const QUnit& w, const BBars
   }
 }
 
+// One CTA of the dQ kernel on unit `unit`.
 template <int D, bool BF16, bool MASK>
-__global__ void __launch_bounds__(kThreadsB, 1)
-    bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                     const __grid_constant__ CUtensorMap tm_v,
-                     const __grid_constant__ CUtensorMap tm_do, const BwdTcParams p) {
+__device__ __forceinline__ void dq_cta(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
+                                       const CUtensorMap* tm_v, const CUtensorMap* tm_do,
+                                       const BwdTcParams& p, int unit) {
   using C = BCfg<D>;
   using I = QIdx<C::qKStages, C::qVStages>;
   extern __shared__ uint8_t smem_raw[];
@@ -1157,7 +1156,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   const BBars br{smem + C::qOffBar, I::n};
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const QUnit w = q_unit<MASK>(p);
+  const QUnit w = q_unit<MASK>(p, unit);
   if (threadIdx.x == 0) {
     for (int i = 0; i < I::n; ++i) {
       const bool ew = (i == I::sFree || i == I::dpFree || i == I::dsReady || i == I::dsReady + 1);
@@ -1167,8 +1166,8 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     ptx::fence_barrier_init();
   }
   if (warp == kLoadWarp && lane == 0) {
-    ptx::prefetch_tensormap(&tm_k);
-    ptx::prefetch_tensormap(&tm_v);
+    ptx::prefetch_tensormap(tm_k);
+    ptx::prefetch_tensormap(tm_v);
   }
   if (warp == kMmaWarp) {
     ptx::tmem_alloc(br.tmem_word(), C::kTmemCols);
@@ -1179,7 +1178,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = ptx::ld_shared_volatile(br.tmem_word());
   if (warp == kLoadWarp) {
-    if (lane == 0) dq_producer<D>(p, w, br, smem, &tm_q, &tm_k, &tm_v, &tm_do);
+    if (lane == 0) dq_producer<D>(p, w, br, smem, tm_q, tm_k, tm_v, tm_do);
   } else if (warp == kMmaWarp) {
     dq_mma<D, BF16>(p, w, br, smem, tmem);
   } else {
@@ -1190,6 +1189,44 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   if (warp == kMmaWarp) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+// The dK/dV and dQ kernels: the same CTA bodies, launched one after the
+// other, or (ATTN_BWD_FUSED) as one grid -- the dK/dV units first, then the
+// dQ units -- so that dQ CTAs take the SMs the dK/dV kernel's tail leaves idle.
+#ifndef ATTN_BWD_FUSED
+#define ATTN_BWD_FUSED 1
+#endif
+
+template <int D, bool BF16, bool SPLIT, bool MASK>
+__global__ void __launch_bounds__(kThreadsB, 1)
+    bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v,
+                      const __grid_constant__ CUtensorMap tm_do, const BwdTcParams p) {
+  dkv_cta<D, BF16, SPLIT, MASK>(&tm_q, &tm_k, &tm_v, &tm_do, p, static_cast<int>(blockIdx.x));
+}
+
+template <int D, bool BF16, bool MASK>
+__global__ void __launch_bounds__(kThreadsB, 1)
+    bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v,
+                     const __grid_constant__ CUtensorMap tm_do, const BwdTcParams p) {
+  dq_cta<D, BF16, MASK>(&tm_q, &tm_k, &tm_v, &tm_do, p, static_cast<int>(blockIdx.x));
+}
+
+template <int D, bool BF16, bool SPLIT, bool MASK>
+__global__ void __launch_bounds__(kThreadsB, 1)
+    bwd_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
+                        const __grid_constant__ CUtensorMap tm_k,
+                        const __grid_constant__ CUtensorMap tm_v,
+                        const __grid_constant__ CUtensorMap tm_do, const BwdTcParams p,
+                        int n_dkv) {
+  const int u = static_cast<int>(blockIdx.x);
+  if (u < n_dkv) {
+    dkv_cta<D, BF16, SPLIT, MASK>(&tm_q, &tm_k, &tm_v, &tm_do, p, u);
+  } else {
+    dq_cta<D, BF16, MASK>(&tm_q, &tm_k, &tm_v, &tm_do, p, u - n_dkv);
   }
 }
 
@@ -1219,27 +1256,41 @@ cudaError_t launch_bwd_tc_d(const CUtensorMap (&maps)[4], const BwdTcParams& p, 
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  auto dkv = p.splits > 1 ? bwd_dkv_tc_kernel<D, BF16, true, MASK>
-                          : bwd_dkv_tc_kernel<D, BF16, false, MASK>;
-  e = cudaFuncSetAttribute(dkv, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kvSmem);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(bwd_dq_tc_kernel<D, BF16, MASK>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::qSmem);
-  if (e != cudaSuccess) return e;
-  dkv<<<static_cast<unsigned>(p.n_tk * p.B * p.Hkv * p.splits), kThreadsB, C::kvSmem, stream>>>(
-      maps[0], maps[1], maps[2], maps[3], p);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  if (p.splits > 1) {
-    const int64_t vecs = 2 * static_cast<int64_t>(p.B) * p.Hkv * p.Lk * (p.dg / 8);
-    bwd_dkv_reduce_kernel<BF16><<<static_cast<unsigned>((vecs + 255) / 256), 256, 0, stream>>>(p);
+  const int n_dkv = p.n_tk * p.B * p.Hkv * p.splits;
+  const int n_dq = p.n_tq * p.B * p.Hq;
+  if (ATTN_BWD_FUSED) {
+    constexpr int smem = C::kvSmem > C::qSmem ? C::kvSmem : C::qSmem;
+    auto fused = p.splits > 1 ? bwd_fused_tc_kernel<D, BF16, true, MASK>
+                              : bwd_fused_tc_kernel<D, BF16, false, MASK>;
+    e = cudaFuncSetAttribute(fused, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    fused<<<static_cast<unsigned>(n_dkv + n_dq), kThreadsB, smem, stream>>>(maps[0], maps[1], maps[2],
+                                                                           maps[3], p, n_dkv);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  } else {
+    auto dkv = p.splits > 1 ? bwd_dkv_tc_kernel<D, BF16, true, MASK>
+                            : bwd_dkv_tc_kernel<D, BF16, false, MASK>;
+    e = cudaFuncSetAttribute(dkv, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kvSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(bwd_dq_tc_kernel<D, BF16, MASK>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, C::qSmem);
+    if (e != cudaSuccess) return e;
+    dkv<<<static_cast<unsigned>(n_dkv), kThreadsB, C::kvSmem, stream>>>(maps[0], maps[1], maps[2],
+                                                                       maps[3], p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    bwd_dq_tc_kernel<D, BF16, MASK><<<static_cast<unsigned>(n_dq), kThreadsB, C::qSmem, stream>>>(
+        maps[0], maps[1], maps[2], maps[3], p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  bwd_dq_tc_kernel<D, BF16, MASK>
-      <<<static_cast<unsigned>(p.n_tq * p.B * p.Hq), kThreadsB, C::qSmem, stream>>>(
-          maps[0], maps[1], maps[2], maps[3], p);
-  return cudaGetLastError();
+  if (p.splits > 1) {  // after every dK/dV CTA has written its partials
+    const int64_t vecs = 2 * static_cast<int64_t>(p.B) * p.Hkv * p.Lk * (p.dg / 8);
+    bwd_dkv_reduce_kernel<BF16><<<static_cast<unsigned>((vecs + 255) / 256), 256, 0, stream>>>(p);
+    e = cudaGetLastError();
+  }
+  return e;
 }
 
 template <int D, bool BF16>
