@@ -236,14 +236,17 @@ attn_status_t attn_fwd_simt(const void* q, const void* k, const void* v, void* o
  *   D          16, 32, 64 or 128 (16 and 32 run the D = 64 kernels on
  *              zero-filled columns).  B*Hq <= 65535.
  * Work: a pre-pass (delta and the LSE in base 2, in rows padded to 128) and
- * two tensor-core kernels (tcgen05, fp32 accumulators in tensor memory): dK/dV
- * per 128-key tile with K and V resident and every query tile and query head
- * of the group streaming through; dQ per 128-row query tile with K and V
- * streaming.  P and dS are rounded to the input dtype as MMA operands, every
- * sum is accumulated in fp32, each result rounded once to the input dtype.
- * No atomics: the result does not depend on scheduling.  Device memory: a
- * stream-ordered fp32 workspace of 2*B*Hq*ceil(L/128)*128*4 bytes from the
- * library's pool.
+ * one launch of two tensor-core CTA kinds (tcgen05, fp32 accumulators in
+ * tensor memory): dK/dV per 128-key tile with K and V resident and every query
+ * tile and query head of the group streaming through; dQ per 128-row query
+ * tile with K and V streaming.  When the (key tile, b, h_kv) units are too few
+ * for the GPU (few K/V heads, e.g. MQA), each key tile's work is split over
+ * several CTAs whose fp32 partials a reduction adds in a fixed order.  P and
+ * dS are rounded to the input dtype as MMA operands, every sum is accumulated
+ * in fp32, each result rounded once to the input dtype.  No atomics: the
+ * result does not depend on scheduling.  Device memory: a stream-ordered
+ * workspace from the library's pool of 2*B*Hq*ceil(L/128)*128*4 bytes, plus
+ * splits*2*B*Hkv*L*D*4 bytes of partials when split (at most 16 splits).
  * Errors: argument errors as attn_fwd (nothing is queued); device-side
  * conditions (bounded-wait timeout, clamped valid_len) through attn_status.
  */
