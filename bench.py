@@ -128,8 +128,10 @@ class ClockSampler:
 
     def start(self):
         try:
-            os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
-            self.path = os.path.join(ROOT, "gpurun_out", "clocks_bench_%d.csv" % os.getpid())
+            # raw samples (the JSON line carries their summary): ATTN_BENCH_OUT or bench_out/
+            out = os.environ.get("ATTN_BENCH_OUT", os.path.join(ROOT, "bench_out"))
+            os.makedirs(out, exist_ok=True)
+            self.path = os.path.join(out, "clocks_bench_%d.csv" % os.getpid())
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.QUERY,
