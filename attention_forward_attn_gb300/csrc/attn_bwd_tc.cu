@@ -1258,7 +1258,7 @@ cudaError_t launch_bwd_tc_d(const CUtensorMap (&maps)[4], const BwdTcParams& p, 
   if (e != cudaSuccess) return e;
   const int n_dkv = p.n_tk * p.B * p.Hkv * p.splits;
   const int n_dq = p.n_tq * p.B * p.Hq;
-  if (ATTN_BWD_FUSED) {
+  if constexpr (ATTN_BWD_FUSED != 0) {
     constexpr int smem = C::kvSmem > C::qSmem ? C::kvSmem : C::qSmem;
     auto fused = p.splits > 1 ? bwd_fused_tc_kernel<D, BF16, true, MASK>
                               : bwd_fused_tc_kernel<D, BF16, false, MASK>;
