@@ -37,6 +37,9 @@ UNIT = "TFLOP/s"
 L2_FLUSH_BYTES = 256 << 20          # > 129 MB L2
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "attn_fwd_tc_dram_traffic.txt")
+# --backward's default shapes; a trailing M: that workload's causal mask given as an
+# explicit tril mask (attn_bwd_masked)
+BWD_WORKLOADS = "C4,C4M,C2,C5"
 KERNEL_SOURCES = [os.path.join(ROOT, "attention_forward_attn_gb300", "csrc", f)
                   for f in ("attn_tc.cu", "attn_vconv.cu", "ptx.cuh")]
 
@@ -799,7 +802,7 @@ def main(argv=None):
                     help="instead of the headline line, one line per backward workload")
     ap.add_argument("--bwd-impl", default="both", choices=["both", "tc", "simt"],
                     help="--backward: which backward (attn_bwd, attn_bwd_simt or both)")
-    ap.add_argument("--bwd-workloads", default="C4,C4M,C2,C5",
+    ap.add_argument("--bwd-workloads", default=BWD_WORKLOADS,
                     help="--backward: comma-separated workload shapes")
     args = ap.parse_args(argv)
     if args.warmup < 3:

@@ -100,3 +100,14 @@ def test_reference_arm_only_rank0_prints(monkeypatch):
 def test_warmup_floor():
     with pytest.raises(SystemExit):
         bench.main(["--warmup", "2"])
+
+
+def test_backward_default_workloads_exist():
+    """bench.py --backward's default shape list names real workloads (a
+    trailing M: the workload's causal mask as an explicit mask, which needs
+    a causal workload)."""
+    for name in bench.BWD_WORKLOADS.split(","):
+        base = name[:-1] if name.endswith("M") else name
+        assert base in wl.WORKLOADS, name
+        if name.endswith("M"):
+            assert wl.WORKLOADS[base].causal, name
