@@ -14,6 +14,7 @@ causal and padding masks.
   sampled rows (tile-boundary rows of every head group).
 """
 import math
+import zlib
 
 import numpy as np
 import pytest
@@ -85,7 +86,7 @@ def make_mask(kind, B, Lq, Lk, rng):
 @pytest.mark.parametrize("causal", [False, True])
 def test_masks_full_compare(kind, D, dtype, causal):
     B, Hq, Hkv, Lq, Lk = 3, 4, 2, 300, 400
-    rng = np.random.default_rng(hash((kind, D, causal)) % 1000)
+    rng = np.random.default_rng(zlib.crc32(("%s/%d/%d" % (kind, D, causal)).encode()) % 1000)
     vl = [400, 261, 77]
     q, k, v, vl_t = wl.make_inputs(B, Hq, Hkv, Lq, D, dtype, seed=700 + D, valid_len=vl, Lk=Lk)
     mk = make_mask(kind, B, Lq, Lk, rng)
