@@ -145,6 +145,16 @@ static void one_row(const double* q_row, const double* k_head, const double* v_h
   *lse_out = m + log(l);
 }
 
+/* Threads for one call: `threads` when > 0, else the OpenMP default. */
+static int oracle_threads(int threads) {
+#ifdef _OPENMP
+  return threads > 0 ? threads : omp_get_max_threads();
+#else
+  (void)threads;
+  return 1;
+#endif
+}
+
 /*
  * q: [B, Hq, Lq, D]; k, v: [B, Hkv, Lk, D] (contiguous, float64).
  * rows == NULL: every row r = (b*Hq + h_q)*Lq + i, written to o[r*D..], lse[r].
@@ -166,13 +176,10 @@ int oracle_attn_fwd_f64(const double* q, const double* k, const double* v, doubl
   if (rows)
     for (int64_t n = 0; n < nrows; ++n)
       if (rows[n] < 0 || rows[n] >= total) return 1;
-#ifdef _OPENMP
-  if (threads > 0) omp_set_num_threads(threads);
-#else
-  (void)threads;
-#endif
+  /* the thread count of this call only (the process-wide default is left as it is) */
+  const int nthr = oracle_threads(threads);
   int bad = 0;
-#pragma omp parallel
+#pragma omp parallel num_threads(nthr)
   {
     double* s = (double*)malloc(sizeof(double) * (size_t)Lk);
     if (!s) {
@@ -267,13 +274,10 @@ int oracle_attn_bwd_f64(const double* q, const double* k, const double* v, const
   memset(dq, 0, sizeof(double) * (size_t)B * Hq * Lq * D);
   memset(dk, 0, sizeof(double) * (size_t)B * Hkv * Lk * D);
   memset(dv, 0, sizeof(double) * (size_t)B * Hkv * Lk * D);
-#ifdef _OPENMP
-  if (threads > 0) omp_set_num_threads(threads);
-#else
-  (void)threads;
-#endif
+  /* the thread count of this call only (the process-wide default is left as it is) */
+  const int nthr = oracle_threads(threads);
   int bad = 0;
-#pragma omp parallel
+#pragma omp parallel num_threads(nthr)
   {
     double* p = (double*)malloc(sizeof(double) * (size_t)Lk);   /* P_i. of one row */
     double* dp = (double*)malloc(sizeof(double) * (size_t)Lk);  /* dP_i. of one row */
@@ -409,14 +413,11 @@ int oracle_attn_bwd_rows_f64(const double* q, const double* k, const double* v, 
     if (q_rows[r] < 0 || q_rows[r] >= (int64_t)B * Hq * Lq) return 1;
   for (int64_t r = 0; r < n_k; ++r)
     if (k_rows[r] < 0 || k_rows[r] >= (int64_t)B * Hkv * Lk) return 1;
-#ifdef _OPENMP
-  if (threads > 0) omp_set_num_threads(threads);
-#else
-  (void)threads;
-#endif
+  /* the thread count of this call only (the process-wide default is left as it is) */
+  const int nthr = oracle_threads(threads);
   int bad = 0;
   /* dQ rows */
-#pragma omp parallel
+#pragma omp parallel num_threads(nthr)
   {
     double* s = (double*)malloc(sizeof(double) * (size_t)Lk);
     if (!s) {
@@ -481,7 +482,7 @@ int oracle_attn_bwd_rows_f64(const double* q, const double* k, const double* v, 
     const int64_t nrow = (int64_t)G * Lq;
     double* st = (double*)malloc(sizeof(double) * 4 * (size_t)nrow);  /* m, z, delta, w */
     if (!st) return 2;
-#pragma omp parallel
+#pragma omp parallel num_threads(nthr)
     {
       double* s = (double*)malloc(sizeof(double) * (size_t)Lk);
       double* o_row = (double*)malloc(sizeof(double) * (size_t)D);
@@ -514,7 +515,7 @@ int oracle_attn_bwd_rows_f64(const double* q, const double* k, const double* v, 
       free(s);
       free(o_row);
     }
-#pragma omp parallel for schedule(dynamic, 1)
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthr)
     for (int64_t r = r0; r < n_k; ++r) {
       if (k_rows[r] / Lk != kvh) continue;
       const int64_t j = k_rows[r] % Lk;
