@@ -4,9 +4,9 @@ Tolerance, per element (both kernels, every case):
     |o - o_ref| <= 2e-3 + 1e-2 * |o_ref|     on O,
     |lse - lse_ref| <= 1e-4                  on LSE (and -inf exactly where the oracle has -inf).
 Small shapes are compared in full (several 128-row tiles, ragged tails,
-every mask); the five benchmark workloads are compared in full (C1, C2) or on
-sampled rows (C3-C5: tile-boundary rows, rows of every batch and head,
-random rows), plus properties that hold at any size.
+every mask), and so are the five benchmark workloads: every row of every head
+of C1-C5 against the oracle run over the whole workload, with the maximum
+absolute and relative errors and the worst error-to-bound ratio reported.
 """
 import math
 
@@ -153,51 +153,45 @@ def test_deterministic():
 
 # ------------------------------------------------------------------ the five workloads
 
-def sample_rows(w, vl, n_random, rng):
-    """Flat row indices: boundary rows of tiles/units of every batch and head, plus random rows."""
-    L = w.L
-    rows_in_head = {0, 1, 127, 128, 129, 255, 256, 257, L // 2, L - 257, L - 256, L - 129,
-                    L - 128, L - 2, L - 1}
-    if vl is not None:
-        for x in vl.tolist():
-            rows_in_head |= {max(0, x - 1), min(L - 1, x), min(L - 1, x + 1)}
-    rows_in_head = sorted(r for r in rows_in_head if 0 <= r < L)
-    heads = range(w.B * w.Hq)
-    picked_heads = sorted(set(rng.choice(w.B * w.Hq, size=min(16, w.B * w.Hq), replace=False)) |
-                          {h * w.Hq + (w.Hq - 1) for h in range(w.B)} | {h * w.Hq for h in range(w.B)})
-    rows = [bh * L + i for bh in picked_heads for i in rows_in_head]
-    rows += list(rng.choice(w.B * w.Hq * L, size=n_random, replace=False))
-    return np.array(sorted(set(int(r) for r in rows)), dtype=np.int64)
+def error_summary(o, lse, o_ref, lse_ref):
+    """Margins of a full comparison: max |o - o_ref|, max |o - o_ref| / |o_ref|
+    over |o_ref| >= 1e-3, the worst ratio of error to the O bound, the number of
+    O elements over the bound, and the max LSE error over finite rows."""
+    o = o.reshape(o_ref.shape)
+    err = np.abs(o - o_ref)
+    aref = np.abs(o_ref)
+    big = aref >= 1e-3
+    neg = np.isneginf(lse_ref)
+    lerr = np.abs(lse.reshape(lse_ref.shape)[~neg] - lse_ref[~neg])
+    return {
+        "max_abs_err_O": float(err.max()),
+        "max_rel_err_O": float((err[big] / aref[big]).max()) if big.any() else 0.0,
+        "worst_err_over_bound_O": float((err / (O_ATOL + O_RTOL * aref)).max()),
+        "n_over_bound_O": int((err > O_ATOL + O_RTOL * aref).sum()),
+        "max_err_LSE": float(lerr.max()) if lerr.size else 0.0,
+    }
 
 
 @pytest.mark.parametrize("name", ["C1", "C2", "C3", "C4", "C5"])
 def test_workload(name):
+    """Every output element of the workload against the oracle run over all of it."""
     w = wl.WORKLOADS[name]
     q, k, v, vl = wl.workload_inputs(w)
     o, lse = run_gpu(q, k, v, w.causal, vl, w.sm_scale)
     # properties at full size
     assert np.all(np.isfinite(o))
     if vl is not None:
-        vlist = vl.tolist()
-        for b, x in enumerate(vlist):
+        for b, x in enumerate(vl.tolist()):
             if x == 0:
                 assert np.all(o.reshape(w.B, w.Hq, w.L, w.D)[b] == 0.0)
                 assert np.all(np.isneginf(lse.reshape(w.B, w.Hq, w.L)[b]))
-    finite_rows = np.isfinite(lse)
-    qb, kb, vb = wl.bits(q), wl.bits(k), wl.bits(v)
-    code = wl.dtype_code(w.dtype)
-    vln = None if vl is None else vl.numpy()
-    if name in ("C1", "C2"):
-        o_ref, lse_ref = oracle.attn_fwd_bits(qb, kb, vb, code, w.sm_scale, causal=w.causal,
-                                              valid_len=vln)
-        check(o, lse, o_ref, lse_ref, name)
-        return
-    rng = np.random.default_rng(w.seed)
-    rows = sample_rows(w, vl, 3000, rng)
-    o_ref, lse_ref = oracle.attn_fwd_bits(qb, kb, vb, code, w.sm_scale, causal=w.causal,
-                                          valid_len=vln, rows=rows)
-    check(o.reshape(-1, w.D)[rows], lse.reshape(-1)[rows], o_ref, lse_ref, name)
-    assert finite_rows.sum() > 0
+    assert np.isfinite(lse).sum() > 0
+    o_ref, lse_ref = oracle.attn_fwd_bits(wl.bits(q), wl.bits(k), wl.bits(v),
+                                          wl.dtype_code(w.dtype), w.sm_scale, causal=w.causal,
+                                          valid_len=None if vl is None else vl.numpy())
+    summary = error_summary(o, lse, o_ref, lse_ref)
+    print("%s parity: %s" % (name, summary))
+    check(o, lse, o_ref, lse_ref, "%s %s" % (name, summary))
 
 
 @pytest.mark.parametrize("name", ["C3", "C4", "C5"])
