@@ -116,11 +116,10 @@ extern "C" attn_status_t attn_fwd_noalloc(const void* q, const void* k, const vo
   // P.V (Problem::vflags stays null); the fourth map is never read
   CUtensorMap maps[5];
   if ((s = attn::encode_problem_maps(p, maps)) != ATTN_OK) return s;
-  // The status word must start at zero for this call: the array keeps
-  // whatever the previous call (on any stream) left in it.
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  e = cudaMemsetAsync(d->scratch, 0, sizeof(int) * kStatusWordsPerCall, st);
-  if (e != cudaSuccess) return attn::cuda_fail(e);
+  // The status word is not cleared here: it started at zero when the module
+  // was loaded, the kernel only ORs conditions into it, and attn_status
+  // clears it after reading -- so, as attn_fwd's word does, it keeps every
+  // condition until attn_status reads it.
   e = attn::launch_tc(p, maps, d->num_sms);
   if (e != cudaSuccess) return attn::cuda_fail(e);
   {

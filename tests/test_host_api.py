@@ -2,6 +2,7 @@
 every function include/attn.h declares, and rejects bad arguments before
 touching a device."""
 import ctypes
+import os
 
 import pytest
 
@@ -290,3 +291,53 @@ def test_bwd_masked_negative_mask_strides_rejected(lib, msb, msr):
                              A16, None, A16, None, 1, 4, 2, 64, 64, 64, 0.125, 1, None, A16, msb,
                              msr, attn.ATTN_BF16, None)
     assert binding.STATUS_NAMES[rc] == "ATTN_ERR_STRIDE"
+
+
+def test_noalloc_source_calls_no_allocator():
+    """attn_fwd_noalloc's translation unit, comments stripped, calls no
+    allocating routine: no cudaMalloc* / cudaFree* / pool call and not the
+    library's workspace pool (a regression there would not show in free
+    device memory once the pool holds memory from earlier attn_fwd calls)."""
+    import re
+    src = os.path.join(os.path.dirname(attn.__file__), "csrc", "attn_noalloc.cu")
+    text = open(src).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    for name in ("cudaMalloc", "cudaFree", "MemPool", "device_pool", "workspace_pool", "malloc(",
+                 "new ", "cuMem"):
+        assert name not in text, name
+    assert "cudaGetSymbolAddress" in text
+
+
+def test_forward_workspace_sizes(lib):
+    """attn_fwd_workspace_size (host-only): fp16 needs none; bf16 needs the
+    fp16 copy of V plus one int flag per (b, h_kv, 128-key tile), rounded up
+    to 256 bytes; a mask adds its packed form, once when shared."""
+    B, Hq, Hkv, L, D = 3, 8, 2, 1000, 64
+    assert attn.fwd_workspace_size(B, Hq, Hkv, L, L, D, attn.ATTN_F16) == 0
+    v16 = B * Hkv * L * D * 2 + B * Hkv * 8 * 4
+    assert attn.fwd_workspace_size(B, Hq, Hkv, L, L, D, attn.ATTN_BF16) == (v16 + 255) // 256 * 256
+    shared = attn.fwd_workspace_size(B, Hq, Hkv, L, L, D, attn.ATTN_F16, mask_batches=1)
+    per_batch = attn.fwd_workspace_size(B, Hq, Hkv, L, L, D, attn.ATTN_F16, mask_batches=B)
+    assert 0 < shared < per_batch
+    assert shared >= L * 8 * 16  # one bit per position, 16 bytes per (row, key tile)
+    with pytest.raises(binding.AttnError):
+        attn.fwd_workspace_size(B, Hq, Hkv, L, L, D, attn.ATTN_F16, mask_batches=2)
+    with pytest.raises(binding.AttnError):
+        attn.fwd_workspace_size(B, 3, 2, L, L, D, attn.ATTN_F16)
+
+
+@pytest.mark.parametrize("ws, nbytes", [(None, 0), (None, 1 << 30), (A16 + 16, 1 << 30),
+                                        (A16, 16)])
+def test_bad_forward_workspace_rejected_on_host(lib, ws, nbytes):
+    st = lib.attn_fwd_ws(A16, A16, A16, A16, None, 1, 2, 1, 16, 64, 0.125, 0, None,
+                         attn.ATTN_BF16, ws, nbytes, None)
+    assert binding.STATUS_NAMES[st] == "ATTN_ERR_WORKSPACE"
+
+
+def test_bad_backward_workspace_pointer_rejected_on_host(lib):
+    args = [A16, None, A16, None, A16, None, A16, None, A16, None, A16, A16, None, A16, None, A16,
+            None, 1, 2, 1, 16, 16, 64, 0.125, 0, None, None, 0, 0, attn.ATTN_BF16]
+    for ws in (None, A16 + 16):
+        st = lib.attn_bwd_masked_ws(*args, ws, 1 << 20, None)
+        assert binding.STATUS_NAMES[st] == "ATTN_ERR_WORKSPACE"

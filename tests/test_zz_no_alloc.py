@@ -2,11 +2,12 @@
 memory (servers that reserve all device memory at start-up, latency-bound
 loops, runtimes that account only for their own allocator).
 
-It must give the same results as attn_fwd (within the parity tolerance used
-everywhere in these tests), on two calls in a row that share its static
-scratch array, must not change the device's free memory, and must report
-device-side conditions through attn_status.  This file is collected last on
-purpose; it passes alone in a fresh process and after the other tests.
+It must give the same results as attn_fwd and as the float64 oracle (within
+the parity tolerance used everywhere in these tests), on two calls in a row
+that share its static scratch array, must not change the device's free
+memory, and must report device-side conditions through attn_status, keeping
+them until attn_status reads them.  This file is collected last on purpose; it
+passes alone in a fresh process and after the other tests.
 """
 import math
 
@@ -14,6 +15,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import attention_forward_attn_gb300 as attn
 from attention_forward_attn_gb300 import workloads as wl
 
@@ -37,6 +39,13 @@ def _call(entry, q, k, v, o, lse, causal, vl, sm):
                         None if vl is None else vl.data_ptr(),
                         attn.ATTN_BF16 if q.dtype == torch.bfloat16 else attn.ATTN_F16,
                         torch.cuda.current_stream().cuda_stream or None, entry=entry)
+
+
+def _close_np(o, lse, o_ref, lse_ref):
+    assert np.all(np.abs(o - o_ref) <= O_ATOL + O_RTOL * np.abs(o_ref))
+    neg = np.isneginf(lse_ref)
+    assert np.array_equal(np.isneginf(lse), neg)
+    assert np.all(np.abs(lse[~neg] - lse_ref[~neg]) <= LSE_ATOL)
 
 
 def _close(o, lse, o_ref, lse_ref):
@@ -76,6 +85,13 @@ def test_noalloc_matches_attn_fwd_twice(B, Hq, Hkv, L, D, dtype, causal, valid_l
     assert free[1] == free[0], "device free memory changed across attn_fwd_noalloc"
     for o, lse in outs:
         _close(o, lse, o_ref, lse_ref)
+    # and against the oracle itself (two results each within the bound of
+    # the oracle may be twice the bound apart from each other)
+    o64, lse64 = oracle.attn_fwd_bits(wl.bits(q.cpu()), wl.bits(k.cpu()), wl.bits(v.cpu()),
+                                      wl.dtype_code(dtype), sm, causal=causal,
+                                      valid_len=None if vl is None else vl.cpu().numpy())
+    for o, lse in outs:
+        _close_np(o.float().cpu().numpy().reshape(o64.shape), lse.cpu().numpy(), o64, lse64)
 
 
 def test_noalloc_reports_device_status_and_clears_it():
@@ -90,6 +106,13 @@ def test_noalloc_reports_device_status_and_clears_it():
     st, code = attn.status()
     assert st == 11 and (code & 2)          # ATTN_ERR_VALID_LEN from the static word
     assert attn.status() == (attn.ATTN_OK, 0)  # read-and-clear
+    # a condition stays in the word until attn_status reads it, even when a
+    # later call on the same stream has none
+    assert _call("attn_fwd_noalloc", q, k, v, o1, l1, True, vl_bad, 0.09) == attn.ATTN_OK
+    assert _call("attn_fwd_noalloc", q, k, v, o1, l1, True, vl_ok, 0.09) == attn.ATTN_OK
+    st, code = attn.status()
+    assert st == 11 and (code & 2)
+    assert attn.status() == (attn.ATTN_OK, 0)
     # the clamped call equals an in-range call with the clamped lengths
     assert _call(None, q, k, v, o2, l2, True, vl_ok, 0.09) == attn.ATTN_OK
     assert attn.status() == (attn.ATTN_OK, 0)
