@@ -20,7 +20,7 @@ STATUS_NAMES = {
     0: "ATTN_OK", 1: "ATTN_ERR_NULL", 2: "ATTN_ERR_ALIGN", 3: "ATTN_ERR_SHAPE",
     4: "ATTN_ERR_HEADS", 5: "ATTN_ERR_HEADDIM", 6: "ATTN_ERR_DTYPE", 7: "ATTN_ERR_SCALE",
     8: "ATTN_ERR_ARCH", 9: "ATTN_ERR_CUDA", 10: "ATTN_ERR_TIMEOUT", 11: "ATTN_ERR_VALID_LEN",
-    12: "ATTN_ERR_ARG", 13: "ATTN_ERR_SCRATCH", 14: "ATTN_ERR_STRIDE",
+    12: "ATTN_ERR_ARG", 13: "ATTN_ERR_SCRATCH", 14: "ATTN_ERR_STRIDE", 15: "ATTN_ERR_WORKSPACE",
 }
 ATTN_OK = 0
 
@@ -105,6 +105,21 @@ def load():
             lib.attn_bwd_strided.restype = i
             lib.attn_bwd_masked.argtypes = lib.attn_bwd_strided.argtypes[:-2] + [p, i64, i64, i, p]
             lib.attn_bwd_masked.restype = i
+            sz = ctypes.c_size_t
+            lib.attn_fwd_ws.argtypes = fwd_args[:-1] + [p, sz, p]
+            lib.attn_fwd_ws.restype = i
+            lib.attn_fwd_masked_ws.argtypes = lib.attn_fwd_masked.argtypes[:-1] + [p, sz, p]
+            lib.attn_fwd_masked_ws.restype = i
+            lib.attn_fwd_workspace_size.argtypes = [i, i, i, i, i, i, i, i, ctypes.POINTER(sz)]
+            lib.attn_fwd_workspace_size.restype = i
+            lib.attn_bwd_ws.argtypes = lib.attn_bwd.argtypes[:-1] + [p, sz, p]
+            lib.attn_bwd_ws.restype = i
+            lib.attn_bwd_masked_ws.argtypes = lib.attn_bwd_masked.argtypes[:-1] + [p, sz, p]
+            lib.attn_bwd_masked_ws.restype = i
+            lib.attn_bwd_workspace_size.argtypes = [i, i, i, i, i, i, i, ctypes.POINTER(sz)]
+            lib.attn_bwd_workspace_size.restype = i
+            lib.attn_workspace_pool_stats.argtypes = [i, ctypes.POINTER(sz), ctypes.POINTER(sz)]
+            lib.attn_workspace_pool_stats.restype = i
             lib.attn_fwd_f32.argtypes = [p, p, p, p, p, i, i, i, i, ctypes.c_float, i, p, i, p]
             lib.attn_fwd_f32.restype = i
             lib.attn_host_plan.argtypes = [i, i, i, i, i, i, ctypes.POINTER(Chunk), i,
@@ -192,6 +207,38 @@ def status(stream=None):
     return st, int(code.value)
 
 
+def fwd_workspace_size(B, Hq, Hkv, Lq, Lk, D, dtype, mask_batches=0) -> int:
+    """attn_fwd_workspace_size: device bytes one forward call needs."""
+    n = ctypes.c_size_t(0)
+    st = int(load().attn_fwd_workspace_size(int(B), int(Hq), int(Hkv), int(Lq), int(Lk), int(D),
+                                            int(dtype), int(mask_batches), ctypes.byref(n)))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fwd_workspace_size")
+    return int(n.value)
+
+
+def bwd_workspace_size(B, Hq, Hkv, Lq, Lk, D, mask_batches=0) -> int:
+    """attn_bwd_workspace_size: device bytes one tensor-core backward call needs
+    on the current device."""
+    n = ctypes.c_size_t(0)
+    st = int(load().attn_bwd_workspace_size(int(B), int(Hq), int(Hkv), int(Lq), int(Lk), int(D),
+                                            int(mask_batches), ctypes.byref(n)))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_bwd_workspace_size")
+    return int(n.value)
+
+
+def pool_stats(reset_high_water=False):
+    """attn_workspace_pool_stats -> (reserved bytes, high-water bytes) of the
+    library's workspace pool on the current device."""
+    r, h = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    st = int(load().attn_workspace_pool_stats(int(bool(reset_high_water)), ctypes.byref(r),
+                                              ctypes.byref(h)))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_workspace_pool_stats")
+    return int(r.value), int(h.value)
+
+
 def query(D: int, dtype: int = ATTN_BF16) -> dict:
     caps = Caps()
     st = int(load().attn_query(int(D), int(dtype), ctypes.byref(caps)))
@@ -234,6 +281,29 @@ def _stream_handle(stream):
     return stream.cuda_stream or None
 
 
+def _workspace(nbytes, like, stream, workspace):
+    """(pointer, bytes) of the workspace for a *_ws call: the caller's uint8
+    CUDA tensor, or a new one from torch's allocator (the library then
+    allocates nothing for the call).  A tensor used on a stream other than
+    torch's current one is recorded on it, so torch does not hand its memory
+    out again before the call's kernels finish.  Returns (None, 0, None) when
+    nbytes is 0; the third value keeps the tensor alive."""
+    import torch
+    if nbytes == 0:
+        return None, 0, None
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=like.device)
+        if stream is not None and not (isinstance(stream, int) and stream == 0):
+            s = stream if isinstance(stream, torch.cuda.Stream) else torch.cuda.ExternalStream(
+                int(stream))
+            if s != torch.cuda.current_stream(like.device):
+                workspace.record_stream(s)
+    elif (not workspace.is_cuda or workspace.dtype != torch.uint8 or not workspace.is_contiguous()
+          or workspace.numel() < nbytes):
+        raise ValueError("workspace must be a contiguous uint8 CUDA tensor of >= %d bytes" % nbytes)
+    return workspace.data_ptr(), workspace.numel(), workspace
+
+
 def _dtype_code(t):
     import torch
     if t.dtype == torch.float16:
@@ -244,13 +314,17 @@ def _dtype_code(t):
 
 
 def attn_fwd(q, k, v, *, causal=False, sm_scale=None, valid_len=None, out=None, lse=None,
-             return_lse=True, stream=None, simt=False):
+             return_lse=True, stream=None, simt=False, workspace=None):
     """Fused attention forward on CUDA tensors.
 
     q: [B, Hq, L, D]; k, v: [B, Hkv, L, D] (or [B, L, D] for MQA); fp16/bf16,
     contiguous, on the current CUDA device.  valid_len: int32 CUDA tensor [B]
     or None.  Returns (o, lse) with o like q and lse float32 [B*Hq, L]
-    (lse is None when return_lse is False).
+    (lse is None when return_lse is False).  The call goes through
+    attn_fwd_ws: its workspace (bf16: the fp16 copy of V) is ``workspace``, a
+    uint8 CUDA tensor of at least fwd_workspace_size(...) bytes, or one torch
+    allocates; workspace="pool" calls attn_fwd, which takes it from the
+    library's own pool instead.
     """
     import torch
     if k.dim() == 3:
@@ -277,12 +351,22 @@ def attn_fwd(q, k, v, *, causal=False, sm_scale=None, valid_len=None, out=None, 
         if valid_len.dtype != torch.int32 or not valid_len.is_cuda or valid_len.numel() != B:
             raise ValueError("valid_len must be an int32 CUDA tensor of B elements")
         vl_ptr = valid_len.data_ptr()
-    st = fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                 lse.data_ptr() if (return_lse and lse is not None) else None,
-                 B, Hq, Hkv, L, D, sm_scale, int(bool(causal)), vl_ptr, _dtype_code(q),
-                 _stream_handle(stream), simt=simt)
+    lse_ptr = lse.data_ptr() if (return_lse and lse is not None) else None
+    if simt or (isinstance(workspace, str) and workspace == "pool"):
+        st = fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse_ptr,
+                     B, Hq, Hkv, L, D, sm_scale, int(bool(causal)), vl_ptr, _dtype_code(q),
+                     _stream_handle(stream), simt=simt)
+        name = "attn_fwd_simt" if simt else "attn_fwd"
+    else:
+        need = fwd_workspace_size(B, Hq, Hkv, L, L, D, _dtype_code(q))
+        ws_ptr, ws_bytes, _keep = _workspace(need, q, stream, workspace)
+        st = int(load().attn_fwd_ws(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                    lse_ptr, B, Hq, Hkv, L, D, float(sm_scale),
+                                    int(bool(causal)), vl_ptr, _dtype_code(q), ws_ptr, ws_bytes,
+                                    _stream_handle(stream)))
+        name = "attn_fwd_ws"
     if st != ATTN_OK:
-        raise AttnError(st, "attn_fwd_simt" if simt else "attn_fwd")
+        raise AttnError(st, name)
     return out, (lse if return_lse else None)
 
 
@@ -342,7 +426,7 @@ def attn_fwd_host(q, k, v, *, causal=False, sm_scale=None, valid_len=None, out=N
 
 
 def attn_fwd_strided(q, k, v, *, causal=False, sm_scale=None, valid_len=None, out=None, lse=None,
-                     return_lse=True, stream=None, mask=None):
+                     return_lse=True, stream=None, mask=None, workspace=None):
     """Fused attention forward on strided CUDA tensors through attn_fwd_strided.
 
     q: [B, Hq, Lq, D]; k, v: [B, Hkv, Lk, D] -- any views whose last
@@ -353,7 +437,9 @@ def attn_fwd_strided(q, k, v, *, causal=False, sm_scale=None, valid_len=None, ou
     (default: ``torch.empty_like(q)``).  mask: optional explicit boolean
     mask, a bool/uint8 CUDA tensor [B, Lq, Lk] or [Lq, Lk] (shared by every
     batch) whose last dimension is contiguous (attn_fwd_masked).  Returns
-    (o, lse) with lse float32 [B*Hq, Lq].
+    (o, lse) with lse float32 [B*Hq, Lq].  The call goes through
+    attn_fwd_masked_ws, with ``workspace`` as in attn_fwd (workspace="pool":
+    attn_fwd_strided / attn_fwd_masked and the library's pool).
     """
     import torch
     for name, t in (("q", q), ("k", k), ("v", v)):
@@ -380,13 +466,8 @@ def attn_fwd_strided(q, k, v, *, causal=False, sm_scale=None, valid_len=None, ou
         if valid_len.dtype != torch.int32 or not valid_len.is_cuda or valid_len.numel() != B:
             raise ValueError("valid_len must be an int32 CUDA tensor of B elements")
         vl_ptr = valid_len.data_ptr()
-    if mask is None:
-        st = fwd_strided_raw(q.data_ptr(), q.stride()[:3], k.data_ptr(), k.stride()[:3],
-                             v.data_ptr(), v.stride()[:3], out.data_ptr(), out.stride()[:3],
-                             lse.data_ptr() if return_lse else None, B, Hq, Hkv, Lq, Lk, D,
-                             sm_scale, int(bool(causal)), vl_ptr, _dtype_code(q),
-                             _stream_handle(stream))
-    else:
+    msb = msr = 0
+    if mask is not None:
         if mask.dtype not in (torch.bool, torch.uint8) or not mask.is_cuda:
             raise ValueError("mask must be a bool or uint8 CUDA tensor")
         if mask.dim() == 2:
@@ -395,13 +476,35 @@ def attn_fwd_strided(q, k, v, *, causal=False, sm_scale=None, valid_len=None, ou
                 or (Lk > 1 and mask.stride(2) != 1)):
             raise ValueError("mask must be [B, Lq, Lk] or [Lq, Lk] with a contiguous last dimension")
         msb = 0 if mask.shape[0] == 1 else mask.stride(0)
-        st = fwd_masked_raw(q.data_ptr(), q.stride()[:3], k.data_ptr(), k.stride()[:3],
-                            v.data_ptr(), v.stride()[:3], out.data_ptr(), out.stride()[:3],
-                            lse.data_ptr() if return_lse else None, B, Hq, Hkv, Lq, Lk, D,
-                            sm_scale, int(bool(causal)), vl_ptr, mask.data_ptr(), msb,
-                            mask.stride(1), _dtype_code(q), _stream_handle(stream))
+        msr = mask.stride(1)
+    lse_ptr = lse.data_ptr() if return_lse else None
+    if isinstance(workspace, str) and workspace == "pool":
+        if mask is None:
+            st = fwd_strided_raw(q.data_ptr(), q.stride()[:3], k.data_ptr(), k.stride()[:3],
+                                 v.data_ptr(), v.stride()[:3], out.data_ptr(), out.stride()[:3],
+                                 lse_ptr, B, Hq, Hkv, Lq, Lk, D, sm_scale, int(bool(causal)),
+                                 vl_ptr, _dtype_code(q), _stream_handle(stream))
+        else:
+            st = fwd_masked_raw(q.data_ptr(), q.stride()[:3], k.data_ptr(), k.stride()[:3],
+                                v.data_ptr(), v.stride()[:3], out.data_ptr(), out.stride()[:3],
+                                lse_ptr, B, Hq, Hkv, Lq, Lk, D, sm_scale, int(bool(causal)),
+                                vl_ptr, mask.data_ptr(), msb, msr, _dtype_code(q),
+                                _stream_handle(stream))
+        name = "attn_fwd_masked" if mask is not None else "attn_fwd_strided"
+    else:
+        mb = 0 if mask is None else (1 if msb == 0 else B)
+        need = fwd_workspace_size(B, Hq, Hkv, Lq, Lk, D, _dtype_code(q), mb)
+        ws_ptr, ws_bytes, _keep = _workspace(need, q, stream, workspace)
+        st = int(load().attn_fwd_masked_ws(
+            q.data_ptr(), _strides_arg(q.stride()[:3]), k.data_ptr(), _strides_arg(k.stride()[:3]),
+            v.data_ptr(), _strides_arg(v.stride()[:3]), out.data_ptr(),
+            _strides_arg(out.stride()[:3]), lse_ptr, int(B), int(Hq), int(Hkv), int(Lq), int(Lk),
+            int(D), float(sm_scale), int(bool(causal)), vl_ptr,
+            None if mask is None else mask.data_ptr(), int(msb), int(msr), _dtype_code(q),
+            ws_ptr, ws_bytes, _stream_handle(stream)))
+        name = "attn_fwd_masked_ws"
     if st != ATTN_OK:
-        raise AttnError(st, "attn_fwd_masked" if mask is not None else "attn_fwd_strided")
+        raise AttnError(st, name)
     return out, (lse if return_lse else None)
 
 
@@ -441,7 +544,7 @@ def attn_fwd_f32(q, k, v, *, kernel="tiled_rowmax", causal=False, sm_scale=None,
 
 
 def attn_bwd(q, k, v, o, lse, do, *, causal=False, sm_scale=None, valid_len=None, stream=None,
-             impl="tc", dq=None, dk=None, dv=None, mask=None):
+             impl="tc", dq=None, dk=None, dv=None, mask=None, workspace=None):
     """Gradients (dq, dk, dv) of attn_fwd for the output gradient ``do``.
 
     impl="tc": attn_bwd_strided (tensor cores).  q, o, do: [B, Hq, Lq, D]; k, v:
@@ -452,7 +555,10 @@ def attn_bwd(q, k, v, o, lse, do, *, causal=False, sm_scale=None, valid_len=None
     impl="simt": attn_bwd_simt (fp32 SIMT), contiguous tensors only.
     lse: the forward's [B*Hq, L] fp32 LSE.  mask: the forward's explicit
     boolean mask (a bool/uint8 CUDA tensor [B, Lq, Lk] or [Lq, Lk] with a
-    contiguous last dimension; impl="tc" only, through attn_bwd_masked)."""
+    contiguous last dimension; impl="tc" only, through attn_bwd_masked).
+    impl="tc" goes through attn_bwd_masked_ws with ``workspace`` as in
+    attn_fwd (a uint8 CUDA tensor of >= bwd_workspace_size(...) bytes, None:
+    torch allocates one, "pool": the library's pool)."""
     import torch
     if impl not in ("tc", "simt"):
         raise ValueError("impl must be 'tc' or 'simt'")
@@ -496,14 +602,24 @@ def attn_bwd(q, k, v, o, lse, do, *, causal=False, sm_scale=None, valid_len=None
                 st3(o), do.data_ptr(), st3(do), lse.data_ptr(), dq.data_ptr(), st3(dq),
                 dk.data_ptr(), st3(dk), dv.data_ptr(), st3(dv), B, Hq, Hkv, L, Lk, D,
                 float(sm_scale), int(bool(causal)), vl_ptr]
-        if mask is None:
-            name = "attn_bwd_strided"
-            st = int(load().attn_bwd_strided(*args, _dtype_code(q), _stream_handle(stream)))
+        msb = 0 if (mask is None or mask.shape[0] == 1) else mask.stride(0)
+        if isinstance(workspace, str) and workspace == "pool":
+            if mask is None:
+                name = "attn_bwd_strided"
+                st = int(load().attn_bwd_strided(*args, _dtype_code(q), _stream_handle(stream)))
+            else:
+                name = "attn_bwd_masked"
+                st = int(load().attn_bwd_masked(*args, mask.data_ptr(), msb, mask.stride(1),
+                                                _dtype_code(q), _stream_handle(stream)))
         else:
-            name = "attn_bwd_masked"
-            msb = 0 if mask.shape[0] == 1 else mask.stride(0)
-            st = int(load().attn_bwd_masked(*args, mask.data_ptr(), msb, mask.stride(1),
-                                            _dtype_code(q), _stream_handle(stream)))
+            name = "attn_bwd_masked_ws"
+            mb = 0 if mask is None else (1 if msb == 0 else B)
+            need = bwd_workspace_size(B, Hq, Hkv, L, Lk, D, mb)
+            ws_ptr, ws_bytes, _keep = _workspace(need, q, stream, workspace)
+            st = int(load().attn_bwd_masked_ws(
+                *args, None if mask is None else mask.data_ptr(), msb,
+                0 if mask is None else mask.stride(1), _dtype_code(q), ws_ptr, ws_bytes,
+                _stream_handle(stream)))
     else:
         name = "attn_bwd_simt"
         st = int(load().attn_bwd_simt(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),

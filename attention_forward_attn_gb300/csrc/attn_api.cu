@@ -2,8 +2,11 @@
 //
 // Validates arguments (no device synchronisation), keeps one device status
 // word per GPU, encodes the TMA tensor maps of Q, K and V, and launches the
-// kernels on the caller's stream.  bf16 calls take a stream-ordered workspace
-// (the fp16 copy of V and its tile flags) from a per-device pool owned here.
+// kernels on the caller's stream.  Calls that need a workspace (bf16: the
+// fp16 copy of V and its tile flags; an explicit mask: its packed form; the
+// backward: its row statistics) take it from the caller (the *_ws entry
+// points) or, when none is given, from a per-device stream-ordered pool owned
+// here.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -259,25 +262,61 @@ using attn::make_problem;
 
 namespace {
 
-// The tensor-core path for a validated problem on the current device: for
-// bf16, the stream-ordered workspace and the V pre-pass, then the attention
-// kernel, then the workspace returned to the pool.
-attn_status_t run_tc(Problem& p, int dev, DeviceState* st) {
-  attn::TcConfig cfg;
-  if (!attn::tc_config(p.D, &cfg)) return ATTN_ERR_HEADDIM;
-  CUtensorMap maps[5];
-  attn_status_t s = attn::encode_problem_maps(p, maps);
-  if (s != ATTN_OK) return s;
-  // one stream-ordered workspace: for bf16 the contiguous fp16 copy of V
-  // and its per-tile flags, then for an explicit mask its packed form
+// A workspace the caller supplies (the *_ws entry points).
+struct CallerWorkspace {
+  void* ptr;
+  size_t bytes;
+};
+
+// Caller workspaces start on a 256-byte boundary (every part inside is
+// placed at a multiple of 256 bytes from it).
+constexpr uintptr_t kWorkspaceAlign = 256;
+
+// Check a caller workspace against the bytes a call needs.
+attn_status_t check_workspace(const CallerWorkspace* cws, int64_t need) {
+  if (cws == nullptr || need == 0) return ATTN_OK;
+  if (cws->ptr == nullptr || !aligned(cws->ptr, kWorkspaceAlign) ||
+      cws->bytes < static_cast<size_t>(need))
+    return ATTN_ERR_WORKSPACE;
+  return ATTN_OK;
+}
+
+// Bytes of the forward's workspace: for bf16 the contiguous fp16 copy of V
+// and its per-tile flags (rounded up to 256 bytes), then for an explicit mask
+// its packed form.
+int64_t fwd_workspace_bytes(const Problem& p, int64_t* v_part) {
   const int64_t v_ws = p.bf16 ? (attn::vconv_workspace_bytes(p) + 255) / 256 * 256 : 0;
   const int64_t m_ws = p.mask != nullptr ? attn::mask_workspace_bytes(p) : 0;
+  if (v_part != nullptr) *v_part = v_ws;
+  return v_ws + m_ws;
+}
+
+// The tensor-core path for a validated problem on the current device: the
+// workspace (the caller's, or a stream-ordered one from the pool), for bf16
+// the V pre-pass, the mask pre-pass, then the attention kernel, then a pool
+// workspace is returned to the pool.
+attn_status_t run_tc(Problem& p, int dev, DeviceState* st, const CallerWorkspace* cws) {
+  attn::TcConfig cfg;
+  if (!attn::tc_config(p.D, &cfg)) return ATTN_ERR_HEADDIM;
+  int64_t v_ws = 0;
+  const int64_t need = fwd_workspace_bytes(p, &v_ws);
+  attn_status_t s = check_workspace(cws, need);
+  if (s != ATTN_OK) return s;
+  CUtensorMap maps[5];
+  s = attn::encode_problem_maps(p, maps);
+  if (s != ATTN_OK) return s;
   void* ws = nullptr;
-  if (v_ws + m_ws > 0) {
-    cudaMemPool_t pool = nullptr;
-    if ((s = workspace_pool(dev, st, &pool)) != ATTN_OK) return s;
-    cudaError_t e = cudaMallocFromPoolAsync(&ws, static_cast<size_t>(v_ws + m_ws), pool, p.stream);
-    if (e != cudaSuccess) return cuda_fail(e);
+  const bool pooled = cws == nullptr && need > 0;
+  if (need > 0) {
+    cudaError_t e = cudaSuccess;
+    if (pooled) {
+      cudaMemPool_t pool = nullptr;
+      if ((s = workspace_pool(dev, st, &pool)) != ATTN_OK) return s;
+      e = cudaMallocFromPoolAsync(&ws, static_cast<size_t>(need), pool, p.stream);
+      if (e != cudaSuccess) return cuda_fail(e);
+    } else {
+      ws = cws->ptr;
+    }
     if (p.mask != nullptr) {
       attn::mask_arrays(p, static_cast<uint8_t*>(ws) + v_ws);
       e = attn::launch_mask_pack(p);
@@ -295,12 +334,12 @@ attn_status_t run_tc(Problem& p, int dev, DeviceState* st) {
       p.vflags = flags;
     }
     if (s != ATTN_OK) {
-      cudaFreeAsync(ws, p.stream);
+      if (pooled) cudaFreeAsync(ws, p.stream);
       return s;
     }
   }
   cudaError_t e = attn::launch_tc(p, maps, st->num_sms);
-  if (ws != nullptr) {
+  if (pooled) {
     const cudaError_t ef = cudaFreeAsync(ws, p.stream);
     if (e == cudaSuccess) e = ef;
   }
@@ -356,28 +395,35 @@ bool no_self_overlap(const attn::Strides& s, int B, int H, int L, int D) {
 
 extern "C" {
 
-attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
-                       int Hq, int Hkv, int L, int D, float sm_scale, int causal,
-                       const int32_t* valid_len, attn_dtype_t dtype, attn_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+attn_status_t fwd_contiguous(const void* q, const void* k, const void* v, void* o, float* lse,
+                             int B, int Hq, int Hkv, int L, int D, float sm_scale, int causal,
+                             const int32_t* valid_len, attn_dtype_t dtype, attn_stream_t stream,
+                             const CallerWorkspace* cws) {
   attn_status_t s = validate(q, k, v, o, lse, B, Hq, Hkv, L, D, sm_scale, causal, valid_len, dtype);
   if (s != ATTN_OK) return s;
+  Problem p = make_problem(q, k, v, o, lse, B, Hq, Hkv, L, D, sm_scale, causal, valid_len, dtype,
+                           stream, nullptr);
+  // a caller workspace is checked before anything touches the device
+  if ((s = check_workspace(cws, fwd_workspace_bytes(p, nullptr))) != ATTN_OK) return s;
   int dev = 0;
   DeviceState* st = nullptr;
   s = device_state(&dev, &st);
   if (s != ATTN_OK) return s;
-  Problem p = make_problem(q, k, v, o, lse, B, Hq, Hkv, L, D, sm_scale, causal, valid_len, dtype,
-                           stream, st->status);
-  return run_tc(p, dev, st);
+  p.status = st->status;
+  return run_tc(p, dev, st, cws);
 }
 
-attn_status_t attn_fwd_masked(const void* q, const attn_strides_t* q_strides, const void* k,
-                              const attn_strides_t* k_strides, const void* v,
-                              const attn_strides_t* v_strides, void* o,
-                              const attn_strides_t* o_strides, float* lse, int B, int Hq, int Hkv,
-                              int Lq, int Lk, int D, float sm_scale, int causal,
-                              const int32_t* valid_len, const uint8_t* mask,
-                              int64_t mask_batch_stride, int64_t mask_row_stride,
-                              attn_dtype_t dtype, attn_stream_t stream) {
+attn_status_t fwd_masked(const void* q, const attn_strides_t* q_strides, const void* k,
+                         const attn_strides_t* k_strides, const void* v,
+                         const attn_strides_t* v_strides, void* o, const attn_strides_t* o_strides,
+                         float* lse, int B, int Hq, int Hkv, int Lq, int Lk, int D, float sm_scale,
+                         int causal, const int32_t* valid_len, const uint8_t* mask,
+                         int64_t mask_batch_stride, int64_t mask_row_stride, attn_dtype_t dtype,
+                         attn_stream_t stream, const CallerWorkspace* cws) {
   // attn_fwd's checks with L = Lq, then the key length
   attn_status_t s =
       validate(q, k, v, o, lse, B, Hq, Hkv, Lq, D, sm_scale, causal, valid_len, dtype);
@@ -394,12 +440,8 @@ attn_status_t attn_fwd_masked(const void* q, const attn_strides_t* q_strides, co
   if (mask != nullptr &&
       static_cast<int64_t>(B) * ((Lq + 127) / 128) * ((Lk + 127) / 128) > INT32_MAX)
     return ATTN_ERR_SHAPE;
-  int dev = 0;
-  DeviceState* st = nullptr;
-  s = device_state(&dev, &st);
-  if (s != ATTN_OK) return s;
   Problem p = make_problem(q, k, v, o, lse, B, Hq, Hkv, Lq, D, sm_scale, causal, valid_len, dtype,
-                           stream, st->status);
+                           stream, nullptr);
   p.Lk = Lk;
   p.sq = sq;
   p.sk = sk;
@@ -408,7 +450,81 @@ attn_status_t attn_fwd_masked(const void* q, const attn_strides_t* q_strides, co
   p.mask = mask;
   p.mask_sb = mask_batch_stride;
   p.mask_sr = mask_row_stride;
-  return run_tc(p, dev, st);
+  if ((s = check_workspace(cws, fwd_workspace_bytes(p, nullptr))) != ATTN_OK) return s;
+  int dev = 0;
+  DeviceState* st = nullptr;
+  s = device_state(&dev, &st);
+  if (s != ATTN_OK) return s;
+  p.status = st->status;
+  return run_tc(p, dev, st, cws);
+}
+
+}  // namespace
+
+extern "C" {
+
+attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                       int Hq, int Hkv, int L, int D, float sm_scale, int causal,
+                       const int32_t* valid_len, attn_dtype_t dtype, attn_stream_t stream) {
+  return fwd_contiguous(q, k, v, o, lse, B, Hq, Hkv, L, D, sm_scale, causal, valid_len, dtype,
+                        stream, nullptr);
+}
+
+attn_status_t attn_fwd_ws(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                          int Hq, int Hkv, int L, int D, float sm_scale, int causal,
+                          const int32_t* valid_len, attn_dtype_t dtype, void* workspace,
+                          size_t workspace_bytes, attn_stream_t stream) {
+  const CallerWorkspace cws{workspace, workspace_bytes};
+  return fwd_contiguous(q, k, v, o, lse, B, Hq, Hkv, L, D, sm_scale, causal, valid_len, dtype,
+                        stream, &cws);
+}
+
+attn_status_t attn_fwd_masked(const void* q, const attn_strides_t* q_strides, const void* k,
+                              const attn_strides_t* k_strides, const void* v,
+                              const attn_strides_t* v_strides, void* o,
+                              const attn_strides_t* o_strides, float* lse, int B, int Hq, int Hkv,
+                              int Lq, int Lk, int D, float sm_scale, int causal,
+                              const int32_t* valid_len, const uint8_t* mask,
+                              int64_t mask_batch_stride, int64_t mask_row_stride,
+                              attn_dtype_t dtype, attn_stream_t stream) {
+  return fwd_masked(q, q_strides, k, k_strides, v, v_strides, o, o_strides, lse, B, Hq, Hkv, Lq,
+                    Lk, D, sm_scale, causal, valid_len, mask, mask_batch_stride, mask_row_stride,
+                    dtype, stream, nullptr);
+}
+
+attn_status_t attn_fwd_masked_ws(const void* q, const attn_strides_t* q_strides, const void* k,
+                                 const attn_strides_t* k_strides, const void* v,
+                                 const attn_strides_t* v_strides, void* o,
+                                 const attn_strides_t* o_strides, float* lse, int B, int Hq,
+                                 int Hkv, int Lq, int Lk, int D, float sm_scale, int causal,
+                                 const int32_t* valid_len, const uint8_t* mask,
+                                 int64_t mask_batch_stride, int64_t mask_row_stride,
+                                 attn_dtype_t dtype, void* workspace, size_t workspace_bytes,
+                                 attn_stream_t stream) {
+  const CallerWorkspace cws{workspace, workspace_bytes};
+  return fwd_masked(q, q_strides, k, k_strides, v, v_strides, o, o_strides, lse, B, Hq, Hkv, Lq,
+                    Lk, D, sm_scale, causal, valid_len, mask, mask_batch_stride, mask_row_stride,
+                    dtype, stream, &cws);
+}
+
+attn_status_t attn_fwd_workspace_size(int B, int Hq, int Hkv, int Lq, int Lk, int D,
+                                      attn_dtype_t dtype, int mask_batches, size_t* bytes) {
+  if (bytes == nullptr) return ATTN_ERR_ARG;
+  *bytes = 0;
+  if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_DTYPE;
+  if (B < 1 || Hq < 1 || Hkv < 1 || Lq < 1 || Lk < 1) return ATTN_ERR_SHAPE;
+  if (D != 16 && D != 32 && D != 64 && D != 128) return ATTN_ERR_HEADDIM;
+  if (Hq % Hkv != 0) return ATTN_ERR_HEADS;
+  if (mask_batches != 0 && mask_batches != 1 && mask_batches != B) return ATTN_ERR_ARG;
+  Problem p = make_problem(nullptr, nullptr, nullptr, nullptr, nullptr, B, Hq, Hkv, Lq, D, 1.f, 0,
+                           nullptr, dtype, nullptr, nullptr);
+  p.Lk = Lk;
+  if (mask_batches != 0) {
+    p.mask = reinterpret_cast<const uint8_t*>(kWorkspaceAlign);  // only "a mask is given"
+    p.mask_sb = mask_batches == 1 ? 0 : 1;  // 0: one mask shared by every batch
+  }
+  *bytes = static_cast<size_t>(fwd_workspace_bytes(p, nullptr));
+  return ATTN_OK;
 }
 
 attn_status_t attn_fwd_strided(const void* q, const attn_strides_t* q_strides, const void* k,
@@ -497,17 +613,19 @@ attn_status_t bwd_validate(const void* q, const void* k, const void* v, const vo
 
 }  // namespace
 
-attn_status_t attn_bwd_masked(const void* q, const attn_strides_t* q_strides, const void* k,
-                              const attn_strides_t* k_strides, const void* v,
-                              const attn_strides_t* v_strides, const void* o,
-                              const attn_strides_t* o_strides, const void* dO,
-                              const attn_strides_t* do_strides, const float* lse, void* dq,
-                              const attn_strides_t* dq_strides, void* dk,
-                              const attn_strides_t* dk_strides, void* dv,
-                              const attn_strides_t* dv_strides, int B, int Hq, int Hkv, int Lq,
-                              int Lk, int D, float sm_scale, int causal, const int32_t* valid_len,
-                              const uint8_t* mask, int64_t mask_batch_stride,
-                              int64_t mask_row_stride, attn_dtype_t dtype, attn_stream_t stream) {
+namespace {
+
+attn_status_t bwd_masked(const void* q, const attn_strides_t* q_strides, const void* k,
+                         const attn_strides_t* k_strides, const void* v,
+                         const attn_strides_t* v_strides, const void* o,
+                         const attn_strides_t* o_strides, const void* dO,
+                         const attn_strides_t* do_strides, const float* lse, void* dq,
+                         const attn_strides_t* dq_strides, void* dk,
+                         const attn_strides_t* dk_strides, void* dv,
+                         const attn_strides_t* dv_strides, int B, int Hq, int Hkv, int Lq, int Lk,
+                         int D, float sm_scale, int causal, const int32_t* valid_len,
+                         const uint8_t* mask, int64_t mask_batch_stride, int64_t mask_row_stride,
+                         attn_dtype_t dtype, attn_stream_t stream, const CallerWorkspace* cws) {
   attn_status_t s = bwd_validate(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, Lq, Lk, D, sm_scale,
                                  causal, valid_len, dtype, true);
   if (s != ATTN_OK) return s;
@@ -525,6 +643,10 @@ attn_status_t attn_bwd_masked(const void* q, const attn_strides_t* q_strides, co
   if (!no_self_overlap(sdq, B, Hq, Lq, D) || !no_self_overlap(sdk, B, Hkv, Lk, D) ||
       !no_self_overlap(sdv, B, Hkv, Lk, D))
     return ATTN_ERR_STRIDE;
+  // a caller workspace: pointer and alignment checked before the device is
+  // touched (the backward always needs one); its size needs the SM count
+  if (cws != nullptr && (cws->ptr == nullptr || !aligned(cws->ptr, kWorkspaceAlign)))
+    return ATTN_ERR_WORKSPACE;
   int dev = 0;
   DeviceState* st = nullptr;
   if ((s = device_state(&dev, &st)) != ATTN_OK) return s;
@@ -535,22 +657,124 @@ attn_status_t attn_bwd_masked(const void* q, const attn_strides_t* q_strides, co
       (s = encode_map(&maps[2], v, B, Hkv, Lk, D, sv, 128, bf16)) != ATTN_OK ||
       (s = encode_map(&maps[3], dO, B, Hq, Lq, D, sdo, 128, bf16)) != ATTN_OK)
     return s;
-  cudaMemPool_t pool = nullptr;
-  if ((s = workspace_pool(dev, st, &pool)) != ATTN_OK) return s;
+  const int64_t need = attn::bwd_tc_workspace_bytes(
+      B, Hq, Hkv, Lq, Lk, D, st->num_sms, mask == nullptr ? 0 : (mask_batch_stride == 0 ? 1 : B));
+  if ((s = check_workspace(cws, need)) != ATTN_OK) return s;
   const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   void* ws = nullptr;
-  cudaError_t e = cudaMallocFromPoolAsync(
-      &ws,
-      static_cast<size_t>(attn::bwd_tc_workspace_bytes(
-          B, Hq, Hkv, Lq, Lk, D, st->num_sms, mask == nullptr ? 0 : (mask_batch_stride == 0 ? 1 : B))),
-      pool, cs);
-  if (e != cudaSuccess) return cuda_fail(e);
+  cudaError_t e = cudaSuccess;
+  if (cws != nullptr) {
+    ws = cws->ptr;
+  } else {
+    cudaMemPool_t pool = nullptr;
+    if ((s = workspace_pool(dev, st, &pool)) != ATTN_OK) return s;
+    e = cudaMallocFromPoolAsync(&ws, static_cast<size_t>(need), pool, cs);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
   e = attn::launch_bwd_tc(maps, o, so, dO, sdo, lse, dq, sdq, dk, sdk, dv, sdv, ws, B, Hq, Hkv, Lq,
                           Lk, D, sm_scale, causal, valid_len, mask, mask_batch_stride,
                           mask_row_stride, bf16, st->num_sms, st->status, cs);
-  const cudaError_t ef = cudaFreeAsync(ws, cs);
-  if (e == cudaSuccess) e = ef;
+  if (cws == nullptr) {
+    const cudaError_t ef = cudaFreeAsync(ws, cs);
+    if (e == cudaSuccess) e = ef;
+  }
   if (e != cudaSuccess) return cuda_fail(e);
+  return ATTN_OK;
+}
+
+}  // namespace
+
+attn_status_t attn_bwd_masked(const void* q, const attn_strides_t* q_strides, const void* k,
+                              const attn_strides_t* k_strides, const void* v,
+                              const attn_strides_t* v_strides, const void* o,
+                              const attn_strides_t* o_strides, const void* dO,
+                              const attn_strides_t* do_strides, const float* lse, void* dq,
+                              const attn_strides_t* dq_strides, void* dk,
+                              const attn_strides_t* dk_strides, void* dv,
+                              const attn_strides_t* dv_strides, int B, int Hq, int Hkv, int Lq,
+                              int Lk, int D, float sm_scale, int causal, const int32_t* valid_len,
+                              const uint8_t* mask, int64_t mask_batch_stride,
+                              int64_t mask_row_stride, attn_dtype_t dtype, attn_stream_t stream) {
+  return bwd_masked(q, q_strides, k, k_strides, v, v_strides, o, o_strides, dO, do_strides, lse,
+                    dq, dq_strides, dk, dk_strides, dv, dv_strides, B, Hq, Hkv, Lq, Lk, D,
+                    sm_scale, causal, valid_len, mask, mask_batch_stride, mask_row_stride, dtype,
+                    stream, nullptr);
+}
+
+attn_status_t attn_bwd_masked_ws(const void* q, const attn_strides_t* q_strides, const void* k,
+                                 const attn_strides_t* k_strides, const void* v,
+                                 const attn_strides_t* v_strides, const void* o,
+                                 const attn_strides_t* o_strides, const void* dO,
+                                 const attn_strides_t* do_strides, const float* lse, void* dq,
+                                 const attn_strides_t* dq_strides, void* dk,
+                                 const attn_strides_t* dk_strides, void* dv,
+                                 const attn_strides_t* dv_strides, int B, int Hq, int Hkv, int Lq,
+                                 int Lk, int D, float sm_scale, int causal,
+                                 const int32_t* valid_len, const uint8_t* mask,
+                                 int64_t mask_batch_stride, int64_t mask_row_stride,
+                                 attn_dtype_t dtype, void* workspace, size_t workspace_bytes,
+                                 attn_stream_t stream) {
+  const CallerWorkspace cws{workspace, workspace_bytes};
+  return bwd_masked(q, q_strides, k, k_strides, v, v_strides, o, o_strides, dO, do_strides, lse,
+                    dq, dq_strides, dk, dk_strides, dv, dv_strides, B, Hq, Hkv, Lq, Lk, D,
+                    sm_scale, causal, valid_len, mask, mask_batch_stride, mask_row_stride, dtype,
+                    stream, &cws);
+}
+
+attn_status_t attn_bwd_ws(const void* q, const void* k, const void* v, const void* o,
+                          const void* dO, const float* lse, void* dq, void* dk, void* dv, int B,
+                          int Hq, int Hkv, int L, int D, float sm_scale, int causal,
+                          const int32_t* valid_len, attn_dtype_t dtype, void* workspace,
+                          size_t workspace_bytes, attn_stream_t stream) {
+  return attn_bwd_masked_ws(q, nullptr, k, nullptr, v, nullptr, o, nullptr, dO, nullptr, lse, dq,
+                            nullptr, dk, nullptr, dv, nullptr, B, Hq, Hkv, L, L, D, sm_scale,
+                            causal, valid_len, nullptr, 0, 0, dtype, workspace, workspace_bytes,
+                            stream);
+}
+
+attn_status_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int Lq, int Lk, int D,
+                                      int mask_batches, size_t* bytes) {
+  if (bytes == nullptr) return ATTN_ERR_ARG;
+  *bytes = 0;
+  if (B < 1 || Hq < 1 || Hkv < 1 || Lq < 1 || Lk < 1) return ATTN_ERR_SHAPE;
+  if (D != 16 && D != 32 && D != 64 && D != 128) return ATTN_ERR_HEADDIM;
+  if (Hq % Hkv != 0) return ATTN_ERR_HEADS;
+  if (mask_batches != 0 && mask_batches != 1 && mask_batches != B) return ATTN_ERR_ARG;
+  int dev = 0;
+  DeviceState* st = nullptr;
+  attn_status_t s = device_state(&dev, &st);
+  if (s != ATTN_OK) return s;
+  *bytes = static_cast<size_t>(
+      attn::bwd_tc_workspace_bytes(B, Hq, Hkv, Lq, Lk, D, st->num_sms, mask_batches));
+  return ATTN_OK;
+}
+
+attn_status_t attn_workspace_pool_stats(int reset_high_water, size_t* reserved_bytes,
+                                        size_t* high_water_bytes) {
+  if (reserved_bytes != nullptr) *reserved_bytes = 0;
+  if (high_water_bytes != nullptr) *high_water_bytes = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_ARCH;
+  cudaMemPool_t pool = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    pool = g_dev[dev].pool;
+  }
+  if (pool == nullptr) return ATTN_OK;
+  uint64_t reserved = 0, high = 0;
+  if ((e = cudaMemPoolGetAttribute(pool, cudaMemPoolAttrReservedMemCurrent, &reserved)) !=
+          cudaSuccess ||
+      (e = cudaMemPoolGetAttribute(pool, cudaMemPoolAttrUsedMemHigh, &high)) != cudaSuccess)
+    return cuda_fail(e);
+  if (reserved_bytes != nullptr) *reserved_bytes = static_cast<size_t>(reserved);
+  if (high_water_bytes != nullptr) *high_water_bytes = static_cast<size_t>(high);
+  if (reset_high_water) {
+    uint64_t zero = 0;
+    e = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrUsedMemHigh, &zero);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
   return ATTN_OK;
 }
 
@@ -681,6 +905,8 @@ const char* attn_strerror(attn_status_t status) {
       return "the call needs more scratch than attn_fwd_noalloc's static array holds";
     case ATTN_ERR_STRIDE:
       return "a stride is not a positive multiple of 8 elements below 2^39, or O's elements overlap";
+    case ATTN_ERR_WORKSPACE:
+      return "the workspace is NULL, not 256-byte aligned, or smaller than the call needs";
   }
   return "unknown status";
 }

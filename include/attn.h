@@ -19,6 +19,7 @@
 #ifndef ATTN_GB300_ATTN_H
 #define ATTN_GB300_ATTN_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -50,7 +51,8 @@ typedef enum {
   ATTN_ERR_VALID_LEN = 11, /* device side: a valid_len value was outside [0, L] and was clamped */
   ATTN_ERR_ARG = 12,       /* another invalid argument (causal not 0/1, NULL out-pointer, ...) */
   ATTN_ERR_SCRATCH = 13,   /* attn_fwd_noalloc: the call needs more scratch than its static array holds */
-  ATTN_ERR_STRIDE = 14     /* a stride is invalid, or an output's elements overlap (strided entry points) */
+  ATTN_ERR_STRIDE = 14,    /* a stride is invalid, or an output's elements overlap (strided entry points) */
+  ATTN_ERR_WORKSPACE = 15  /* *_ws entry points: the workspace is NULL, misaligned or too small */
 } attn_status_t;
 
 /*
@@ -104,10 +106,52 @@ typedef enum {
  * cudaFreeAsync on the same stream after the kernel, so calls on different
  * streams never share it and repeated calls reuse the pool's memory.
  * attn_shutdown destroys the pools.  ATTN_F16 calls take no workspace.
+ * attn_fwd_ws is the same call with the workspace supplied by the caller.
  */
 attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                        int B, int Hq, int Hkv, int L, int D, float sm_scale, int causal,
                        const int32_t* valid_len, attn_dtype_t dtype, attn_stream_t stream);
+
+/*
+ * attn_fwd_workspace_size -- bytes of device workspace one forward call needs
+ * (attn_fwd_ws, attn_fwd_masked_ws) for these sizes.
+ *
+ * The pages say nothing about memory management; the contract is that the
+ * caller's framework allocates all per-call device memory (the library only
+ * owns its status word).  The workspace holds, for ATTN_BF16, the fp16 copy
+ * of V and one flag per (b, h_kv, 128-key tile) that attn_fwd describes, and,
+ * for an explicit mask, the packed bit form attn_fwd_masked describes.
+ *   B, Hq, Hkv, Lq, Lk, D, dtype   as the call will pass them (Lq = Lk = L
+ *                  for attn_fwd_ws).
+ *   mask_batches   0 without an explicit mask, 1 for one [Lq, Lk] mask
+ *                  shared by every batch (mask batch stride 0), B for one
+ *                  mask per batch.
+ *   bytes          receives the size; 0 when the call needs no workspace
+ *                  (ATTN_F16 without a mask).
+ * Host-only, needs no device.  Errors: ATTN_ERR_ARG (bytes NULL, or
+ * mask_batches not 0, 1 or B), and attn_fwd's shape, head and dtype errors.
+ */
+attn_status_t attn_fwd_workspace_size(int B, int Hq, int Hkv, int Lq, int Lk, int D,
+                                      attn_dtype_t dtype, int mask_batches, size_t* bytes);
+
+/*
+ * attn_fwd_ws -- attn_fwd with a caller-supplied workspace: the library
+ * allocates no per-call device memory.
+ *
+ * Defined by: the same operation, arguments and results as attn_fwd, bit for
+ * bit.  workspace: a DEVICE buffer owned by the caller, 256-byte aligned, of
+ * at least workspace_bytes >= attn_fwd_workspace_size(...) bytes (NULL with 0
+ * bytes is accepted when the size is 0).  Its contents on entry do not matter;
+ * the call overwrites it on `stream` and reads it until its kernels finish, so
+ * the caller must not reuse or free it before then (stream order is enough;
+ * two calls in flight at once on different streams need two workspaces).
+ * Errors: as attn_fwd, plus ATTN_ERR_WORKSPACE when the workspace is NULL,
+ * misaligned or too small for the call (checked on the host, nothing queued).
+ */
+attn_status_t attn_fwd_ws(const void* q, const void* k, const void* v, void* o, float* lse,
+                          int B, int Hq, int Hkv, int L, int D, float sm_scale, int causal,
+                          const int32_t* valid_len, attn_dtype_t dtype, void* workspace,
+                          size_t workspace_bytes, attn_stream_t stream);
 
 /* Element strides of one [B, H, L, D] operand of attn_fwd_strided: how many
  * elements apart (b, h, i, d) and (b + 1, h, i, d), (b, h + 1, i, d) and
@@ -206,6 +250,23 @@ attn_status_t attn_fwd_masked(const void* q, const attn_strides_t* q_strides, co
                               attn_dtype_t dtype, attn_stream_t stream);
 
 /*
+ * attn_fwd_masked_ws -- attn_fwd_masked (and, with mask NULL,
+ * attn_fwd_strided) with a caller-supplied workspace, on the terms of
+ * attn_fwd_ws: same arguments, results and errors as attn_fwd_masked, plus
+ * workspace / workspace_bytes sized by attn_fwd_workspace_size with
+ * mask_batches = 0 (no mask), 1 (mask_batch_stride 0) or B.
+ */
+attn_status_t attn_fwd_masked_ws(const void* q, const attn_strides_t* q_strides, const void* k,
+                                 const attn_strides_t* k_strides, const void* v,
+                                 const attn_strides_t* v_strides, void* o,
+                                 const attn_strides_t* o_strides, float* lse, int B, int Hq,
+                                 int Hkv, int Lq, int Lk, int D, float sm_scale, int causal,
+                                 const int32_t* valid_len, const uint8_t* mask,
+                                 int64_t mask_batch_stride, int64_t mask_row_stride,
+                                 attn_dtype_t dtype, void* workspace, size_t workspace_bytes,
+                                 attn_stream_t stream);
+
+/*
  * attn_fwd_simt -- the same operation, same arguments and same contract as
  * attn_fwd, computed by a plain SIMT kernel (one warp per query row, fp32
  * FMA dot products, online softmax over 32-key blocks; no tensor cores).
@@ -302,6 +363,63 @@ attn_status_t attn_bwd_masked(const void* q, const attn_strides_t* q_strides, co
                               int64_t mask_row_stride, attn_dtype_t dtype, attn_stream_t stream);
 
 /*
+ * attn_bwd_workspace_size -- bytes of device workspace one tensor-core
+ * backward call needs (attn_bwd_ws, attn_bwd_masked_ws): the row statistics
+ * of its pre-pass, the fp32 partial sums when key tiles are split over
+ * several CTAs, and the packed mask.  mask_batches: 0 without an explicit
+ * mask, 1 for a mask shared by every batch, B for one per batch.  The size
+ * depends on the current device's SM count (the split), so the call looks at
+ * the current device (sm_103 required; on the first call on a device the
+ * library also allocates its status word there).  Errors: ATTN_ERR_ARG
+ * (bytes NULL, mask_batches not 0, 1 or B), the shape, head and head-dim
+ * errors of attn_bwd, ATTN_ERR_ARCH, ATTN_ERR_CUDA.
+ */
+attn_status_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int Lq, int Lk, int D,
+                                      int mask_batches, size_t* bytes);
+
+/*
+ * attn_bwd_ws / attn_bwd_masked_ws -- attn_bwd and attn_bwd_masked (mask
+ * NULL: attn_bwd_strided) with a caller-supplied workspace instead of one
+ * from the library's pool: the library allocates no per-call device memory.
+ * Same arguments, results and errors as those calls, plus workspace (a
+ * 256-byte aligned DEVICE buffer owned by the caller, contents on entry
+ * irrelevant, in use until the call's kernels finish on `stream`) of
+ * workspace_bytes >= attn_bwd_workspace_size(...) bytes; ATTN_ERR_WORKSPACE
+ * when it is NULL, misaligned or too small (nothing queued).
+ */
+attn_status_t attn_bwd_ws(const void* q, const void* k, const void* v, const void* o,
+                          const void* dO, const float* lse, void* dq, void* dk, void* dv, int B,
+                          int Hq, int Hkv, int L, int D, float sm_scale, int causal,
+                          const int32_t* valid_len, attn_dtype_t dtype, void* workspace,
+                          size_t workspace_bytes, attn_stream_t stream);
+attn_status_t attn_bwd_masked_ws(const void* q, const attn_strides_t* q_strides, const void* k,
+                                 const attn_strides_t* k_strides, const void* v,
+                                 const attn_strides_t* v_strides, const void* o,
+                                 const attn_strides_t* o_strides, const void* dO,
+                                 const attn_strides_t* do_strides, const float* lse, void* dq,
+                                 const attn_strides_t* dq_strides, void* dk,
+                                 const attn_strides_t* dk_strides, void* dv,
+                                 const attn_strides_t* dv_strides, int B, int Hq, int Hkv, int Lq,
+                                 int Lk, int D, float sm_scale, int causal,
+                                 const int32_t* valid_len, const uint8_t* mask,
+                                 int64_t mask_batch_stride, int64_t mask_row_stride,
+                                 attn_dtype_t dtype, void* workspace, size_t workspace_bytes,
+                                 attn_stream_t stream);
+
+/*
+ * attn_workspace_pool_stats -- memory of the workspace pool the library keeps
+ * on the current device for calls made without a caller workspace:
+ * *reserved_bytes the pool's reserved device memory, *high_water_bytes the
+ * most it had handed out at once since the last reset (both 0 when no call
+ * on this device has needed the pool).  reset_high_water != 0 resets the
+ * high-water mark after reading it.  Either pointer may be NULL.  Lets a
+ * caller account for the library's memory, and check that its *_ws calls
+ * take none from the pool.
+ */
+attn_status_t attn_workspace_pool_stats(int reset_high_water, size_t* reserved_bytes,
+                                        size_t* high_water_bytes);
+
+/*
  * attn_bwd_simt -- the same gradients computed by SIMT kernels with fp32
  * arithmetic throughout (P and dS are never rounded to 16 bits): delta; dQ per
  * 64-row query tile; dK/dV per 64-key tile with all query heads of its group;
@@ -373,12 +491,14 @@ attn_status_t attn_fwd_f32(const float* q, const float* k, const float* v, float
  * when it does (the array itself, a one-time cost).  Make that first call
  * before any stream capture begins on the device.
  *
- * Sharing: every call on a device uses the same array.  Each call clears the
- * status word on its stream (cudaMemsetAsync) before its kernel, so the word
- * holds only the latest call's conditions; attn_status reads and clears it
- * together with attn_fwd's word.  Calls whose executions overlap on the GPU
- * (different streams without ordering) race on the word: order them, or read
- * attn_status between them, if their device-side status matters.
+ * Sharing: every call on a device uses the same array.  The status word
+ * starts at zero when the library's device data is loaded, each call ORs its
+ * conditions into it, and attn_status reads and clears it together with
+ * attn_fwd's word -- so, as with attn_fwd, it holds every condition since the
+ * last attn_status.  Nothing else in the array must start at zero.  Calls
+ * whose executions overlap on the GPU (different streams without ordering)
+ * race on the word's read-and-clear: order them, or read attn_status between
+ * them, if their device-side status matters.
  */
 attn_status_t attn_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
                                int B, int Hq, int Hkv, int L, int D, float sm_scale, int causal,
@@ -465,8 +585,10 @@ attn_status_t attn_host_plan(int B, int Hq, int Hkv, int L, int D, attn_dtype_t 
  * attn_status -- synchronise `stream`, then read and clear the device status
  * word of the current device.  *device_code (may be NULL) receives the raw
  * word: bit 0 a bounded wait timed out, bit 1 a valid_len value was clamped;
- * bits 8..15 name the waiting role of the first timeout (1 producer, 2 MMA
- * issuer, 3 softmax, 4 epilogue).  Returns ATTN_OK, ATTN_ERR_TIMEOUT,
+ * bits 8..11 are a set of role flags, one per waiting role that timed out
+ * (0x100 the TMA producer, 0x200 an MMA issuer, 0x400 the softmax, 0x800 the
+ * epilogue), ORed over every timed-out wait of every CTA and call since the
+ * word was last read.  Returns ATTN_OK, ATTN_ERR_TIMEOUT,
  * ATTN_ERR_VALID_LEN (timeout wins when both are set) or ATTN_ERR_CUDA when
  * the synchronisation itself reported an error.
  */
