@@ -74,5 +74,40 @@ def build_library(force: bool = False, extra_flags=()) -> str:
     return LIB_PATH
 
 
+# A test-only library: the same objects, except that the tensor-core forward
+# is compiled so that CTA 0 skips one K-tile load and every bounded wait gives
+# up after 20 ms.  The tests use it to drive the timeout path (the waiting
+# roles record ATTN_ERR_TIMEOUT, the CTA drains and frees its TMEM, the kernel
+# returns); the product never loads it.
+WAIT_TEST_LIB_PATH = os.path.join(PKG, "libattn_waittest.so")
+WAIT_TEST_FLAGS = ["-DATTN_TEST_DROP_K_LOAD=1", "-DATTN_WAIT_LIMIT_NS=20000000ull"]
+WAIT_TEST_SOURCE = "attn_tc.cu"
+
+
+def build_wait_test_library() -> str:
+    """Build libattn_waittest.so next to libattn.so (see WAIT_TEST_FLAGS); returns its path."""
+    build_library()
+    inputs = _inputs()
+    if (os.path.exists(WAIT_TEST_LIB_PATH) and
+            all(os.path.getmtime(f) <= os.path.getmtime(WAIT_TEST_LIB_PATH) for f in inputs)):
+        return WAIT_TEST_LIB_PATH
+    src = os.path.join(CSRC, WAIT_TEST_SOURCE)
+    obj = os.path.join(BUILD, WAIT_TEST_SOURCE + ".waittest.o")
+    cmd = [nvcc()] + ARCH_FLAGS + NVCC_FLAGS + WAIT_TEST_FLAGS + ["-c", src, "-o", obj]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError("nvcc failed for %s:\n%s\n%s" % (src, " ".join(cmd), r.stderr))
+    objs = [os.path.join(BUILD, os.path.basename(x) + ".o") for x in sources()
+            if os.path.basename(x) != WAIT_TEST_SOURCE] + [obj]
+    tmp = WAIT_TEST_LIB_PATH + ".tmp.%d" % os.getpid()
+    cmd = [nvcc()] + ARCH_FLAGS + ["-shared", "-Xcompiler", "-fPIC", "-cudart", "static"] + objs + [
+        "-o", tmp]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError("link failed:\n%s\n%s" % (" ".join(cmd), r.stderr))
+    os.replace(tmp, WAIT_TEST_LIB_PATH)
+    return WAIT_TEST_LIB_PATH
+
+
 if __name__ == "__main__":
     print(build_library(force=True))

@@ -373,6 +373,12 @@ __device__ void producer_role(const KParams& p, const Bars<D>& br, uint32_t smem
     if (!wait_bar(br, p.status, is_v ? br.v_empty(s) : br.k_empty(s), par ^ 1u, kRoleProducer))
       return false;
     ++it;
+#ifdef ATTN_TEST_DROP_K_LOAD
+    // Test build only (a separate library, never libattn.so): CTA 0 skips
+    // its first K-tile load, so the waits for that tile can end only by their
+    // time limit -- the path that reports ATTN_ERR_TIMEOUT.
+    if (!is_v && blockIdx.x == 0 && it == 1) return true;
+#endif
     const uint32_t full = is_v ? br.v_full(s) : br.k_full(s);
     const uint32_t dst = smem + (is_v ? C::kOffV : C::kOffK) + s * C::kKVBytes;
     // bf16 V: the exact fp16 copy of the tile when there is one
