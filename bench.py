@@ -1,16 +1,22 @@
 #!/usr/bin/env python3
 """Benchmark of the fused attention forward on GB300.
 
-One step = one attn_fwd call over the whole workload (every query row of every
+One call = one attn_fwd over the whole workload (every query row of every
 head).  Default workload C4: causal GQA, bf16, Q [4,32,4096,128], K/V
-[4,8,4096,128] -- the configuration the throughput target is quoted on.
+[4,8,4096,128] -- the configuration the throughput target is quoted on.  A
+timed step is a block of calls (enough for about 120 ms of device time, so
+the clock sampler sees the GPU under load), each call bracketed by its own
+CUDA events with L2 flushed before it; the step's time is the sum.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload C1..C5]
     python bench.py --impl reference ...   # the float64 CPU oracle, bounded samples
 
-Prints ONE JSON line (rank 0).  Multi-GPU (torchrun): every rank runs an
-independent replica of the workload (the forward has no exchange step);
-value = all ranks' FLOPs / the slowest rank's time.
+Prints ONE JSON line (rank 0): the headline workload, and under "workloads"
+every one of C1-C5 (timing, roofline fractions, and the whole output compared
+with the float64 oracle, whose run over that workload is also the CPU
+baseline).  Multi-GPU (torchrun): every rank runs an independent replica of
+the workload (the forward has no exchange step); value = all ranks' FLOPs /
+the slowest rank's time.
 """
 from __future__ import annotations
 
@@ -268,22 +274,21 @@ def copies_only_ms(dev, host_in, host_out, reps=5):
     return best
 
 
-def time_graph_loop(attn, w, q_d, k_d, v_d, vl_d, o_d, lse_d, dev, calls=1000, reps=5):
+def time_graph_loop(attn, w, x, dev, calls=1000, reps=5):
     """Per-call time of `calls` attn_fwd calls captured in one CUDA graph
     (inputs resident, no L2 flush: the whole problem of a launch-bound
-    workload fits in L2)."""
+    workload fits in L2).  x: the workload's Inputs."""
     side = torch.cuda.Stream(dev)
     side.wait_stream(torch.cuda.current_stream(dev))
     with torch.cuda.stream(side):
-        attn.attn_fwd(q_d, k_d, v_d, causal=w.causal, sm_scale=w.sm_scale, valid_len=vl_d,
-                      out=o_d, lse=lse_d)
+        x.call(attn, side)
     torch.cuda.current_stream(dev).wait_stream(side)
     torch.cuda.synchronize(dev)
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
+        cap = torch.cuda.current_stream(dev)
         for _ in range(calls):
-            attn.attn_fwd(q_d, k_d, v_d, causal=w.causal, sm_scale=w.sm_scale, valid_len=vl_d,
-                          out=o_d, lse=lse_d)
+            x.call(attn, cap)
     g.replay()
     torch.cuda.synchronize(dev)
     best = float("inf")
@@ -305,58 +310,163 @@ def time_graph_loop(attn, w, q_d, k_d, v_d, vl_d, o_d, lse_d, dev, calls=1000, r
             "timing": "CUDA events around one replay of the graph, best of %d" % reps}
 
 
+O_ATOL, O_RTOL, LSE_ATOL = 2e-3, 1e-2, 1e-4
+PARITY_BOUND = "|o - o_ref| <= 2e-3 + 1e-2 |o_ref| per element; |lse - lse_ref| <= 1e-4, -inf matched"
+
+
+def parity_summary(o, lse, o_ref, lse_ref) -> dict:
+    """The GPU's O and LSE against the oracle's, every element: max abs and max
+    rel error of O (rel over |o_ref| >= 1e-3), the worst error-to-bound ratio,
+    the number of O elements over the bound, the LSE error and -inf pattern."""
+    o = o.reshape(o_ref.shape)
+    err = np.abs(o - o_ref)
+    aref = np.abs(o_ref)
+    bound = O_ATOL + O_RTOL * aref
+    big = aref >= 1e-3
+    lse = lse.reshape(lse_ref.shape)
+    neg = np.isneginf(lse_ref)
+    lerr = np.abs(lse[~neg] - lse_ref[~neg])
+    n_over = int((err > bound).sum()) + int(np.sum(~np.isfinite(o)))
+    n_lse_over = int((lerr > LSE_ATOL).sum()) + int((np.isneginf(lse) != neg).sum())
+    return {
+        "rows_compared": int(lse_ref.size),
+        "max_abs_err_O": float(err.max()) if err.size else 0.0,
+        "max_rel_err_O": float((err[big] / aref[big]).max()) if big.any() else 0.0,
+        "worst_err_over_bound_O": round(float((err / bound).max()), 4) if err.size else 0.0,
+        "max_err_LSE": float(lerr.max()) if lerr.size else 0.0,
+        "n_over_bound": n_over + n_lse_over,
+        "bound": PARITY_BOUND,
+    }
+
+
+def oracle_full(w, q, k, v, vl, threads: int = 0):
+    """The float64 oracle over every row of the workload, timed: (o_ref, lse_ref,
+    seconds).  This is the CPU-baseline leg; its outputs are also the parity
+    reference."""
+    import oracle
+    t0 = time.perf_counter()
+    o_ref, lse_ref = oracle.attn_fwd_bits(wl.bits(q), wl.bits(k), wl.bits(v), wl.dtype_code(w.dtype),
+                                          w.sm_scale, causal=w.causal,
+                                          valid_len=None if vl is None else vl.numpy(),
+                                          threads=threads)
+    return o_ref, lse_ref, time.perf_counter() - t0
+
+
+def time_calls(call, n, flush, stream):
+    """Device ms of n calls, each bracketed by its own CUDA events on `stream`,
+    with L2 flushed (a 256 MB write) before each, outside the events."""
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(n)]
+    for e0, e1 in ev:
+        flush.zero_()
+        e0.record(stream)
+        call()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return [e0.elapsed_time(e1) for e0, e1 in ev]
+
+
+class Inputs:
+    """One workload's seeded inputs on the host and on the device, with outputs."""
+
+    def __init__(self, w, dev, attn):
+        self.w = w
+        self.q, self.k, self.v, self.vl = wl.workload_inputs(w)
+        self.q_d, self.k_d, self.v_d = self.q.to(dev), self.k.to(dev), self.v.to(dev)
+        self.vl_d = None if self.vl is None else self.vl.to(dev)
+        self.o_d = torch.empty_like(self.q_d)
+        self.lse_d = torch.empty((w.B * w.Hq, w.L), dtype=torch.float32, device=dev)
+        # the call's workspace (bf16: the fp16 copy of V), allocated once by torch
+        n = attn.fwd_workspace_size(w.B, w.Hq, w.Hkv, w.L, w.L, w.D,
+                                    attn.ATTN_BF16 if w.dtype == "bf16" else attn.ATTN_F16)
+        self.ws = torch.empty(n, dtype=torch.uint8, device=dev) if n else None
+
+    def call(self, attn, stream):
+        w = self.w
+        attn.attn_fwd(self.q_d, self.k_d, self.v_d, causal=w.causal, sm_scale=w.sm_scale,
+                      valid_len=self.vl_d, out=self.o_d, lse=self.lse_d, stream=stream,
+                      workspace=self.ws)
+
+
+def work_record(w, vl, ms_list, peaks):
+    """Timing and roofline fractions of one workload from per-call device ms."""
+    vln = None if vl is None else vl.numpy()
+    nom = nominal_flops(w)
+    alg = algorithmic_flops(w, vln)
+    b = sum(io_bytes(w).values())
+    med = statistics.median(ms_list)
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    gbs = b / (med * 1e-3) / 1e9
+    return {
+        "workload": "%s: %s" % (w.name, w.description),
+        "valid_len": None if vl is None else vl.tolist(),
+        "calls_timed": len(ms_list),
+        "ms_median": round(med, 5),
+        "ms_p10": round(float(np.percentile(ms_list, 10)), 5),
+        "ms_p90": round(float(np.percentile(ms_list, 90)), 5),
+        "tflops_nominal": round(nom / (med * 1e-3) / 1e12, 3),
+        "tflops_algorithmic": round(alg / (med * 1e-3) / 1e12, 3),
+        "tensor_peak_frac_algorithmic": round(alg / (med * 1e-3) / 1e12 / peak, 4),
+        "hbm_min_bytes": b,
+        "hbm_gbs_at_min_bytes": round(gbs, 1),
+        "hbm_peak_frac": round(gbs / hbm, 4),
+        "nominal_flops": nom,
+        "algorithmic_flops": alg,
+    }
+
+
 def run_gpu(args, w, world, rank, local):
     import attention_forward_attn_gb300 as attn
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     attn.load()
-    q, k, v, vl = wl.workload_inputs(w)
-    q_d, k_d, v_d = q.to(dev), k.to(dev), v.to(dev)
-    vl_d = None if vl is None else vl.to(dev)
-    o_d = torch.empty_like(q_d)
-    lse_d = torch.empty((w.B * w.Hq, w.L), dtype=torch.float32, device=dev)
+    peaks, peak_src = load_peaks()
+    x = Inputs(w, dev, attn)
+    q, k, v, vl = x.q, x.k, x.v, x.vl
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def step():
-        attn.attn_fwd(q_d, k_d, v_d, causal=w.causal, sm_scale=w.sm_scale, valid_len=vl_d,
-                      out=o_d, lse=lse_d, stream=stream)
+    def call():
+        x.call(attn, stream)
 
-    for _ in range(args.warmup):
+    # calls per step: enough for ~args.step_ms of device time (estimated from
+    # three calls after two untimed ones)
+    for _ in range(2):
         flush.zero_()
-        step()
+        call()
+    est = statistics.median(time_calls(call, 3, flush, stream))
+    R = args.calls_per_step or int(max(1, min(2000, math.ceil(args.step_ms / max(est, 1e-3)))))
+    for _ in range(args.warmup):
+        for _ in range(R):
+            flush.zero_()
+            call()
     st, code = attn.status(stream)
     if st != 0:
         raise RuntimeError("device status after warm-up: %d (code %#x)" % (st, code))
 
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     sampler = ClockSampler(local)
     barrier(world)
     torch.cuda.synchronize(dev)
     sampler.start()
     wall0 = time.perf_counter()
-    for s in range(args.steps):
-        flush.zero_()                     # L2 flushed between timed steps
-        starts[s].record(stream)
-        step()
-        ends[s].record(stream)
-    torch.cuda.synchronize(dev)
+    per_call = time_calls(call, args.steps * R, flush, stream)
     wall = time.perf_counter() - wall0
     clocks = sampler.stop()
     barrier(world)
     st, code = attn.status(stream)
     if st != 0:
         raise RuntimeError("device status after timing: %d (code %#x)" % (st, code))
-    ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
-    ms_mean = sum(ms) / len(ms)
+    step_ms = [sum(per_call[s * R:(s + 1) * R]) for s in range(args.steps)]
+    ms_mean = sum(step_ms) / len(step_ms)
     ms_max_rank = reduce_max(ms_mean, world)
+    call_ms_mean = ms_mean / R
 
     # launch-bound workloads: the same call captured 1000 times in one CUDA
     # graph and replayed, so the per-call device time excludes launch latency
     graph_loop = None
-    if ms_mean < 0.05:
-        graph_loop = time_graph_loop(attn, w, q_d, k_d, v_d, vl_d, o_d, lse_d, dev)
+    if call_ms_mean < 0.05:
+        graph_loop = time_graph_loop(attn, w, x, dev)
 
     # end to end through the public API: attn_fwd_host takes the pinned host
     # buffers, copies the inputs in and the outputs back, pipelined with the kernels
@@ -364,7 +474,7 @@ def run_gpu(args, w, world, rank, local):
     vl_h = None if vl is None else vl.pin_memory()
     o_h = torch.empty(q.shape, dtype=q.dtype).pin_memory()
     lse_h = torch.empty((w.B * w.Hq, w.L), dtype=torch.float32).pin_memory()
-    e2e_steps = max(3, min(args.steps, args.e2e_steps))
+    e2e_steps = max(3, args.e2e_steps)
 
     def e2e_step():
         attn.attn_fwd_host(q_h, k_h, v_h, causal=w.causal, sm_scale=w.sm_scale, valid_len=vl_h,
@@ -392,24 +502,29 @@ def run_gpu(args, w, world, rank, local):
         raise RuntimeError("device status after e2e: %d (code %#x)" % (st, code))
     link_ms = copies_only_ms(dev, [q_h, k_h, v_h] + ([vl_h] if vl_h is not None else []),
                              [o_h, lse_h])
+    del q_h, k_h, v_h, vl_h, o_h, lse_h
 
     # results
     vln = None if vl is None else vl.numpy()
     nom = nominal_flops(w)
     alg = algorithmic_flops(w, vln)
-    peaks, peak_src = load_peaks()
-    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    ms_med = statistics.median(ms)
-    achieved = alg / (ms_mean * 1e-3) / 1e12
+    # the timed region is seconds of back-to-back calls (the power cap can
+    # act): the sustained peak is the denominator; the burst one is reported too
+    peak_burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    achieved = alg / (call_ms_mean * 1e-3) / 1e12
     b = io_bytes(w)
+    launches_per_call = 2 if w.dtype == "bf16" else 1
     line = {
         "metric": METRIC,
-        "value": round(aggregate(nom, ms_max_rank * 1e-3, world), 3),
+        "value": round(aggregate(nom * R, ms_max_rank * 1e-3, world), 3),
         "unit": UNIT,
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
         "ms_per_step": round(ms_max_rank, 5),
+        "ms_per_call": round(ms_max_rank / R, 5),
+        "calls_per_step": R,
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -421,15 +536,17 @@ def run_gpu(args, w, world, rank, local):
             "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "L": w.L, "D": w.D, "causal": w.causal,
             "valid_len": None if vl is None else vl.tolist(), "sm_scale": w.sm_scale,
             "parallelism": "replicas x%d (no exchange step)" % world,
-            "l2": "flushed between timed steps (256 MB write, outside the events)",
-            "timing": "CUDA events around each attn_fwd call on its stream (%s)" % (
-                "bf16: V pre-pass + attention kernel" if w.dtype == "bf16" else "attention kernel"),
-            "ms_median": round(ms_med, 5),
-            "ms_p10": round(float(np.percentile(ms, 10)), 5),
-            "ms_p90": round(float(np.percentile(ms, 90)), 5),
+            "l2": "flushed before every timed call (256 MB write, outside the events)",
+            "timing": ("a step = %d attn_fwd calls, each bracketed by CUDA events on its stream "
+                       "(%s); the step's time is the sum of its calls' times" % (
+                           R, "bf16: V pre-pass + attention kernel" if w.dtype == "bf16"
+                           else "attention kernel")),
+            "ms_per_call_median": round(statistics.median(per_call), 5),
+            "ms_per_call_p10": round(float(np.percentile(per_call, 10)), 5),
+            "ms_per_call_p90": round(float(np.percentile(per_call, 90)), 5),
             "wall_s_timed_region": round(wall, 4),
-            "nominal_flops": nom,
-            "algorithmic_flops": alg,
+            "nominal_flops_per_call": nom,
+            "algorithmic_flops_per_call": alg,
         },
         "roofline": {
             "bound": "tensor",
@@ -437,11 +554,14 @@ def run_gpu(args, w, world, rank, local):
             "peak": peak,
             "unit": "TFLOP/s",
             "frac": round(achieved / peak, 4),
-            "peak_source": "%s bf16_tflops (burst; kernel timed alone)" % peak_src,
+            "peak_source": ("%s bf16_tflops_sustained (the timed region is %.1f s of back-to-back "
+                            "calls)" % (peak_src, wall)),
+            "peak_burst": peak_burst,
+            "frac_of_burst_peak": round(achieved / peak_burst, 4),
             "traffic": committed_traffic(w.name),
             "traffic_unit": "bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum)",
             "hbm_min_bytes": sum(b.values()),
-            "hbm_gbs_at_min_bytes": round(sum(b.values()) / (ms_mean * 1e-3) / 1e9, 1),
+            "hbm_gbs_at_min_bytes": round(sum(b.values()) / (call_ms_mean * 1e-3) / 1e9, 1),
             "hbm_peak_gbs": float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])),
         },
         "e2e": {
@@ -452,27 +572,103 @@ def run_gpu(args, w, world, rank, local):
             "ms_per_step": round(e2e_ms, 4),
             "steps": e2e_steps,
             "path": ("attn_fwd_host (C ABI via the binding): pinned host Q/K/V/O/LSE, "
-                     "copies pipelined with the kernels in %d chunks" % len(e2e_chunks)),
+                     "copies pipelined with the kernels in %d chunks; one call per step" % len(
+                         e2e_chunks)),
             "copies_only_ms_per_step": round(link_ms, 4),
             "host_queue_ms_per_step": round(host_s * 1e3 / e2e_steps, 4),
         },
         # attn_fwd launches the attention kernel, preceded for bf16 by the
         # kernel that makes the fp16 copy of V
-        "gpu_launches": args.steps * (2 if w.dtype == "bf16" else 1),
+        "gpu_launches": args.steps * R * launches_per_call,
         "graph_loop": graph_loop,
         "clocks": clocks,
     }
-    if rank == 0 and not args.no_cpu_baseline:
-        rng = np.random.default_rng(1234)
-        tfl, det = oracle_sample(w, q, k, v, vl, args.cpu_budget_s, rng)
-        line["cpu_baseline"] = {
-            "value": round(tfl, 6), "unit": UNIT, "cores": _oracle_threads(),
-            "kind": "oracle",
-            "sample": "%d random query rows of %s (%.1f s of float64 oracle work, scaled by "
-                      "nominal/algorithmic FLOPs %.4f)" % (det["rows"], w.name, det["seconds"],
-                                                          det["nominal_per_algorithmic"]),
-        }
+    if rank != 0 or args.no_cpu_baseline:
+        return line
+
+    # The CPU-baseline leg: the float64 oracle over the whole workload, timed
+    # on the host cores; its outputs are the parity reference for the GPU's.
+    # First the headline workload, then (unless --no-workloads) every other one.
+    call()
+    torch.cuda.synchronize(dev)
+    o_gpu = x.o_d.float().cpu().numpy()
+    lse_gpu = x.lse_d.cpu().numpy()
+    threads = _oracle_threads()
+    o_ref, lse_ref, secs = oracle_full(w, q, k, v, vl)
+    line["parity"] = dict(workload=w.name, **parity_summary(o_gpu, lse_gpu, o_ref, lse_ref))
+    del o_gpu, lse_gpu, o_ref, lse_ref
+    line["cpu_baseline"] = {
+        "value": round(nom / secs / 1e12, 6), "unit": UNIT, "cores": threads, "kind": "oracle",
+        "sample": "the whole workload: all %d query rows of %s (%.1f s of float64 oracle work)" % (
+            w.B * w.Hq * w.L, w.name, secs),
+        "single_thread": single_thread_times(),
+    }
+    headline = work_record(w, vl, per_call, peaks)
+    headline["parity"] = line["parity"]
+    headline["cpu_oracle_s"] = round(secs, 2)
+    if graph_loop is not None:
+        headline["graph_loop"] = graph_loop
+    del x
+    torch.cuda.empty_cache()
+    if args.no_workloads:
+        return line
+    recs = {}
+    for name in sorted(wl.WORKLOADS):
+        if name == w.name:
+            recs[name] = headline
+            continue
+        wk = wl.WORKLOADS[name]
+        y = Inputs(wk, dev, attn)
+
+        def call_y():
+            y.call(attn, stream)
+
+        for _ in range(3):
+            flush.zero_()
+            call_y()
+        ms = time_calls(call_y, args.workload_calls, flush, stream)
+        st, code = attn.status(stream)
+        if st != 0:
+            raise RuntimeError("device status on %s: %d (code %#x)" % (name, st, code))
+        rec = work_record(wk, y.vl, ms, peaks)
+        if statistics.median(ms) < 0.05:
+            rec["graph_loop"] = time_graph_loop(attn, wk, y, dev)
+        call_y()
+        torch.cuda.synchronize(dev)
+        o_gpu = y.o_d.float().cpu().numpy()
+        lse_gpu = y.lse_d.cpu().numpy()
+        o_ref, lse_ref, secs = oracle_full(wk, y.q, y.k, y.v, y.vl)
+        rec["parity"] = parity_summary(o_gpu, lse_gpu, o_ref, lse_ref)
+        rec["cpu_oracle_s"] = round(secs, 2)
+        recs[name] = rec
+        del y, o_gpu, lse_gpu, o_ref, lse_ref
+        torch.cuda.empty_cache()
+    line["workloads"] = recs
+    line["workloads_note"] = (
+        "per workload: %d calls (the headline: the timed steps' calls), L2 flushed before each, "
+        "CUDA events; fractions of the %s peaks (bf16_tflops burst, hbm_gbs) from algorithmic "
+        "FLOPs and the minimum bytes Q+K+V+O+LSE; parity: the whole output against the float64 "
+        "oracle run over the whole workload on %d host cores (cpu_oracle_s)" % (
+            args.workload_calls, peak_src, threads))
     return line
+
+
+def single_thread_times():
+    """The oracle on one host thread: C1 whole, and C2 on a random sample of
+    query rows of about 5 s (scaled to the whole workload)."""
+    out = {}
+    w1 = wl.WORKLOADS["C1"]
+    q, k, v, vl = wl.workload_inputs(w1)
+    _, _, secs = oracle_full(w1, q, k, v, vl, threads=1)
+    out["C1"] = {"seconds": round(secs, 4), "tflops": round(nominal_flops(w1) / secs / 1e12, 6),
+                 "rows": "all %d" % (w1.B * w1.Hq * w1.L)}
+    w2 = wl.WORKLOADS["C2"]
+    q, k, v, vl = wl.workload_inputs(w2)
+    tfl, det = oracle_sample(w2, q, k, v, vl, 5.0, np.random.default_rng(4321), threads=1)
+    out["C2"] = {"seconds": round(det["seconds"], 3), "tflops": round(tfl, 6),
+                 "rows": "%d random of %d" % (det["rows"], w2.B * w2.Hq * w2.L),
+                 "seconds_whole_workload_extrapolated": round(nominal_flops(w2) / (tfl * 1e12), 1)}
+    return out
 
 
 def mask_workloads(dev):
@@ -737,23 +933,27 @@ def _oracle_threads() -> int:
 # ------------------------------------------------------------------ reference arm
 
 def run_reference(args, w):
-    """The float64 CPU oracle as the reference arm: each step a bounded sample."""
+    """The float64 CPU oracle as the reference arm: each step a bounded random
+    sample of the workload's query rows.  value: the sampled rows' work (in the
+    metric's nominal-FLOP convention) over the time they took; ms_per_step: the
+    measured time of a step's sample."""
     q, k, v, vl = wl.workload_inputs(w)
     rng = np.random.default_rng(99)
     per_step = max(0.2, args.reference_budget_s / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
         oracle_sample(w, q, k, v, vl, per_step, rng)
-    vals, secs, rows = [], [], 0
+    flops, secs, rows = 0.0, [], 0
     t0 = time.perf_counter()
     for _ in range(args.steps):
         tfl, det = oracle_sample(w, q, k, v, vl, per_step, rng)
-        vals.append(tfl)
+        flops += tfl * 1e12 * det["seconds"]
         secs.append(det["seconds"])
         rows += det["rows"]
     wall = time.perf_counter() - t0
-    value = sum(vals) / len(vals)
+    value = flops / sum(secs) / 1e12
     nom = nominal_flops(w)
     cores = _oracle_threads()
+    ms_step = sum(secs) / len(secs) * 1e3
     line = {
         "impl": "reference",
         "metric": METRIC,
@@ -762,7 +962,7 @@ def run_reference(args, w):
         "n_gpus": 1,
         "steps": args.steps,
         "warmup": args.warmup,
-        "ms_per_step": round(nom / (value * 1e12) * 1e3, 3),
+        "ms_per_step": round(ms_step, 3),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -770,8 +970,10 @@ def run_reference(args, w):
         "data": "synthetic: seeded N(0,1) rounded to %s, decoded to float64" % w.dtype,
         "config": {"workload": "%s: %s" % (w.name, w.description), "B": w.B, "Hq": w.Hq,
                    "Hkv": w.Hkv, "L": w.L, "D": w.D, "causal": w.causal,
-                   "ms_per_step_note": "extrapolated: the whole workload at the sampled rate",
-                   "wall_s": round(wall, 2)},
+                   "step": "a random sample of %d query rows on average (of %d)" % (
+                       rows // max(1, args.steps), w.B * w.Hq * w.L),
+                   "ms_whole_workload_extrapolated": round(nom / (value * 1e12) * 1e3, 1),
+                   "wall_s_timed_steps": round(wall, 2)},
         "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": cores,
                          "kind": "oracle",
                          "sample": "%d random query rows per step on average (%.2f s each)" % (
@@ -786,14 +988,23 @@ def run_reference(args, w):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="C4", choices=sorted(wl.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     ap.add_argument("--reference-budget-s", type=float, default=120.0)
-    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true",
+                    help="skip the oracle leg (CPU baseline and parity)")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="only the headline workload (no per-workload record)")
+    ap.add_argument("--calls-per-step", type=int, default=0,
+                    help="attn_fwd calls per timed step (0: enough for --step-ms)")
+    ap.add_argument("--step-ms", type=float, default=120.0,
+                    help="device time a timed step aims at when --calls-per-step is 0")
+    ap.add_argument("--workload-calls", type=int, default=30,
+                    help="timed calls per workload of the per-workload record")
     ap.add_argument("--mask-workloads", action="store_true",
                     help="instead of the headline line, one line per explicit-mask workload")
     ap.add_argument("--relative-table", action="store_true",

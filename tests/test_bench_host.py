@@ -111,3 +111,40 @@ def test_backward_default_workloads_exist():
         assert base in wl.WORKLOADS, name
         if name.endswith("M"):
             assert wl.WORKLOADS[base].causal, name
+
+
+def test_reference_arm_step_time_is_measured(monkeypatch):
+    """ms_per_step is the measured time of a step's sample, so K steps fit in
+    the timed wall time; the whole-workload time is reported apart."""
+    for var in ("WORLD_SIZE", "RANK", "LOCAL_RANK"):
+        monkeypatch.delenv(var, raising=False)
+    buf = io.StringIO()
+    with redirect_stdout(buf):
+        rc = bench.main(["--impl", "reference", "--workload", "C2", "--steps", "3",
+                         "--warmup", "3", "--reference-budget-s", "1.2"])
+    line = json.loads(buf.getvalue().strip().splitlines()[-1])
+    assert rc == 0
+    assert line["steps"] * line["ms_per_step"] * 1e-3 <= line["config"]["wall_s_timed_steps"]
+    assert line["config"]["ms_whole_workload_extrapolated"] > line["ms_per_step"]
+
+
+def test_parity_summary_counts_planted_errors():
+    """The bench's comparison finds errors planted in a copy of an oracle-shaped
+    output: one O element just over the bound, one LSE off by 2e-4, one -inf
+    lost; exact copies give zero."""
+    rng = np.random.default_rng(0)
+    o_ref = rng.standard_normal((2, 3, 8, 4))
+    lse_ref = rng.standard_normal((6, 8))
+    lse_ref[1, 2] = -np.inf
+    s = bench.parity_summary(o_ref.copy(), lse_ref.copy(), o_ref, lse_ref)
+    assert s["n_over_bound"] == 0 and s["max_abs_err_O"] == 0 and s["max_err_LSE"] == 0
+    o = o_ref.copy()
+    o[1, 2, 3, 1] += 1.01 * (2e-3 + 1e-2 * abs(o_ref[1, 2, 3, 1]))
+    lse = lse_ref.copy()
+    lse[4, 4] += 2e-4
+    lse[1, 2] = 0.0
+    s = bench.parity_summary(o, lse, o_ref, lse_ref)
+    assert s["n_over_bound"] == 3
+    assert 1.0 < s["worst_err_over_bound_O"] < 1.02
+    assert s["max_err_LSE"] == pytest.approx(2e-4)
+    assert s["rows_compared"] == 48
