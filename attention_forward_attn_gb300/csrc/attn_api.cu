@@ -854,6 +854,7 @@ attn_status_t attn_status(attn_stream_t stream, int* device_code) {
   if (s != ATTN_OK) return s;
   if (device_code != nullptr) *device_code = code;
   if (code & attn::kStatusTimeout) return ATTN_ERR_TIMEOUT;
+  if (code & attn::kStatusLayout) return ATTN_ERR_ARCH;
   if (code & attn::kStatusValidLenClamped) return ATTN_ERR_VALID_LEN;
   return ATTN_OK;
 }

@@ -13,6 +13,7 @@ namespace attn {
 enum : int {
   kStatusTimeout = 1 << 0,
   kStatusValidLenClamped = 1 << 1,
+  kStatusLayout = 1 << 2,  // a kernel's shared-memory layout did not fit what it was given
   kRoleProducer = 1 << 8,
   kRoleMma = 2 << 8,
   kRoleSoftmax = 4 << 8,

@@ -69,8 +69,23 @@ constexpr int BH = BN / 2;    // keys of one half tile (one softmax warpgroup's 
 constexpr int kProducerWarp = 8;
 constexpr int kPvWarp = 9;     // P.V issuer; also allocates TMEM
 constexpr int kSWarp = 10;     // score issuer
-constexpr int kThreads = 352;  // two softmax warpgroups, producer, two MMA issuers
+constexpr int kEpiWarp0 = 12;  // warps 12-15: epilogue (warp 12 + q reads TMEM lane quadrant q)
+// warpgroups: softmax half a, softmax half b, control (producer, two issuers,
+// an idle warp), epilogue
+constexpr int kThreads = 512;
 constexpr int kSoftmaxThreads = 256;
+constexpr int kEpiThreads = 128;
+// Register split between warpgroups (setmaxnreg).  The CTA is launched with
+// kLaunchRegs registers per thread (the __launch_bounds__(512, 1) ceiling);
+// the softmax warpgroups take kSoftmaxRegs, the control and epilogue
+// warpgroups kOtherRegs.  The split must add up to exactly the launch pool,
+// or an increase could wait forever: launch_instance refuses a build whose
+// register count differs.
+constexpr int kLaunchRegs = 128;
+constexpr int kSoftmaxRegs = 168;
+constexpr int kOtherRegs = 88;
+static_assert(2 * 128 * kSoftmaxRegs + 2 * 128 * kOtherRegs == kThreads * kLaunchRegs,
+              "register split must equal the launch pool");
 constexpr float kRescaleLog2 = 8.0f;  // rescale O only when the max grows by > 2^8
 constexpr float kLn2 = 0.69314718055994531f;
 
@@ -92,14 +107,16 @@ struct Cfg {
   static constexpr int kOffBar = kOffV + kVStages * kKVBytes;
   static_assert(kQBytes == kKVBytes, "an O tile is staged in a V stage");
   // barrier block: q_full q_empty k_full[KS] k_empty[KS] v_full[VS] v_empty[VS]
-  // s_full[SB] p_full[SB] pv_done[SB] o_full drain o_staged xch_m xch_s, then
-  // 32-bit words: TMEM base, abort flag; then the epilogue's exchange area
-  // (two floats per row)
-  static constexpr int kNumBars = 2 + 2 * kKStages + 2 * kVStages + 3 * kScoreBufs + 5;
+  // s_full[SB] p_full[SB] pv_done[SB] o_full drain o_staged ml_full ml_empty
+  // o_free, then 32-bit words: TMEM base, abort flag; then the row statistics
+  // the softmax hands to the epilogue (m_a, l_a, m_b, l_b per row)
+  static constexpr int kNumBars = 2 + 2 * kKStages + 2 * kVStages + 3 * kScoreBufs + 6;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kMiscBytes = 8;
   static constexpr int kOffXch = kOffMisc + kMiscBytes;
-  static constexpr int kSmemBytes = kOffXch + BM * 8 + 1024;  // + slack to align the base
+  // Dynamic shared memory starts 1024-byte aligned (the tiles need it); the
+  // kernel checks that the layout fits what it was given.
+  static constexpr int kSmemBytes = kOffXch + BM * 16;
   // TMEM columns: score buffers S_b (fp32, BN each; each half's P is written
   // over the first columns of that half), then the two partial accumulators:
   // O_a (keys of the first half of every tile) and O_b (second half).
@@ -138,14 +155,15 @@ struct Bars {
   }
   __device__ __forceinline__ uint32_t o_full() const { return base + 8u * (2 + 2 * KS + 2 * VS + 3 * SB); }
   __device__ __forceinline__ uint32_t drain() const { return base + 8u * (3 + 2 * KS + 2 * VS + 3 * SB); }
-  // every softmax thread has written its O row into the staging tile
+  // every epilogue thread has written its O row into the staging tile
   __device__ __forceinline__ uint32_t o_staged() const { return base + 8u * (4 + 2 * KS + 2 * VS + 3 * SB); }
-  // epilogue exchange: half b's (m_b, l_b) are in shared memory / half a's
-  // final scales are
-  __device__ __forceinline__ uint32_t xch_m() const { return base + 8u * (5 + 2 * KS + 2 * VS + 3 * SB); }
-  __device__ __forceinline__ uint32_t xch_s() const { return base + 8u * (6 + 2 * KS + 2 * VS + 3 * SB); }
+  // the softmax has written the unit's row statistics / the epilogue has read them
+  __device__ __forceinline__ uint32_t ml_full() const { return base + 8u * (5 + 2 * KS + 2 * VS + 3 * SB); }
+  __device__ __forceinline__ uint32_t ml_empty() const { return base + 8u * (6 + 2 * KS + 2 * VS + 3 * SB); }
+  // the epilogue has read O_a and O_b out of TMEM (the next unit may overwrite them)
+  __device__ __forceinline__ uint32_t o_free() const { return base + 8u * (7 + 2 * KS + 2 * VS + 3 * SB); }
   __device__ __forceinline__ uint32_t tmem_word() const {
-    return base + 8u * (7 + 2 * KS + 2 * VS + 3 * SB);
+    return base + 8u * (8 + 2 * KS + 2 * VS + 3 * SB);
   }
   __device__ __forceinline__ uint32_t abort_word() const { return tmem_word() + 4u; }
 };
@@ -472,7 +490,7 @@ template <int D, bool BF16>
 __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t q_desc, uint64_t k_desc) {
   using C = Cfg<D>;
   constexpr uint32_t idesc = ptx::idesc_f16(BM, BN, BF16, false);
-#pragma unroll (D == 128 ? D / 16 : 1)
+#pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
     const uint32_t off = (kk & 3) * 32u;
     ptx::mma_ss(d_tmem, desc_add(q_desc, (kk / 4) * C::kSlabQ + off),
@@ -491,7 +509,7 @@ template <int D>
 __device__ __forceinline__ void issue_pv(uint32_t o_a, uint32_t o_b, uint32_t p_tmem,
                                          uint64_t v_desc, bool accumulate, bool split) {
   const uint32_t idesc = split ? ptx::idesc_f16(BM, D, true, true) : ptx::idesc_f16(BM, D, false, true);
-#pragma unroll (D == 128 ? BN / 16 : 1)
+#pragma unroll
   for (int kk = 0; kk < BN / 16; ++kk) {
     const int h = kk / (BH / 16);
     const int k4 = kk % (BH / 16);
@@ -584,6 +602,7 @@ __device__ void pv_issuer_role(const KParams& p, const Bars<D>& br, uint32_t sme
   const uint64_t v_desc0 = ptx::sdesc_sw128(smem + C::kOffV, C::kSlabKV, 1024);
   const uint32_t t_oa = tmem + C::kColOa;
   const uint32_t t_ob = tmem + C::kColOb;
+  uint32_t units = 0;  // units with key tiles issued so far
   bool ok = true;
 
   const int rounds = (p.n_units + gridDim.x - 1) / gridDim.x;
@@ -618,6 +637,13 @@ __device__ void pv_issuer_role(const KParams& p, const Bars<D>& br, uint32_t sme
         ok = false;
         break;
       }
+      // The unit's first P.V overwrites O_a and O_b: the epilogue must have
+      // read the previous unit's out of TMEM (it normally has, long before)
+      if (first && units > 0 &&
+          !__all_sync(0xffffffffu, wait_bar(br, p.status, br.o_free(), (units - 1u) & 1u, kRoleMma))) {
+        ok = false;
+        break;
+      }
       ptx::tc_fence_after();
       if (elect_one())
         issue_pv<D>(t_oa, t_ob, tmem + C::col_s(b), desc_add(v_desc0, sv * C::kKVBytes), !first,
@@ -632,6 +658,7 @@ __device__ void pv_issuer_role(const KParams& p, const Bars<D>& br, uint32_t sme
         commit_one(br.v_empty(sv));
       }
     }
+    ++units;
   }
   commit_one(br.drain());
   drain_wait(br.drain(), 0);
@@ -699,8 +726,7 @@ __device__ __forceinline__ float exp_half(const uint32_t (&s)[BH], uint64_t sc2,
 //   m = max(m_a, m_b),  l = l_a 2^(m_a - m) + l_b 2^(m_b - m),
 //   O = (O_a 2^(m_a - m) + O_b 2^(m_b - m)) / l.
 template <int D, bool BF16, bool MASK>
-__device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t smem, uint32_t tmem,
-                             const CUtensorMap* tm_o) {
+__device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t smem, uint32_t tmem) {
   using C = Cfg<D>;
   constexpr int SB = C::kScoreBufs;
   const int lane_row = threadIdx.x & 127;           // row within the tile = TMEM lane
@@ -710,14 +736,11 @@ __device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t smem,
   const uint32_t t_oh = tmem + lane_addr + (half ? C::kColOb : C::kColOa);  // this half's O
   const uint32_t t_oa = tmem + lane_addr + C::kColOa;
   const uint32_t t_ob = tmem + lane_addr + C::kColOb;
-  const uint32_t xch = smem + C::kOffXch + static_cast<uint32_t>(lane_row) * 8u;
+  // this row's statistics for the epilogue: (m_a, l_a) then (m_b, l_b)
+  const uint32_t xch = smem + C::kOffXch + static_cast<uint32_t>(lane_row) * 16u + half * 8u;
   const float scale_log2 = p.scale_log2;
-  uint32_t o_phase = 0;
-  uint32_t epi = 0;  // epilogues (staged O tiles) so far
+  uint32_t epi = 0;  // units with key tiles done so far (their statistics handed over)
   uint32_t g = 0;    // score (and V) tiles of all units so far (buffer g % SB)
-  // thread 0: V stage still being read by the last O store (kNoStage: none)
-  constexpr uint32_t kNoStage = 0xFFFFFFFFu;
-  uint32_t pending_stage = kNoStage;
 
   // Each unit is decoded one unit ahead, with the fp16 flags of its first
   // 32 key tiles: during the previous unit's wait for its last P.V, where the
@@ -743,22 +766,11 @@ __device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t smem,
     };
     const int row = w.m0 + lane_row;
     const bool row_ok = row < p.Lq;
-    const int64_t grow = static_cast<int64_t>(w.bh) * p.Lq + row;  // LSE row
     if (threadIdx.x == 0 && p.valid_len != nullptr) {
       const int vl = p.valid_len[w.b];
       if (vl < 0 || vl > p.Lk) atomicOr(p.status, kStatusValidLenClamped);
     }
-    if (w.last < 0) {  // no visible key: O = 0, LSE = -inf (written by half a)
-      if (row_ok && half == 0) {
-        // rows of O are d_o elements long (D = 16 and 32 run the D = 64 instance)
-        const int64_t orow = w.b * p.o_sb + w.hq * p.o_sh + row * p.o_sl;
-        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.o) + orow * 2);
-#pragma unroll
-        for (int c = 0; c < D / 8; ++c) {
-          if (c < p.d_o / 8) dst[c] = make_uint4(0u, 0u, 0u, 0u);
-        }
-        if (p.lse != nullptr) p.lse[grow] = -INFINITY;
-      }
+    if (w.last < 0) {  // no visible key: the epilogue writes O = 0, LSE = -inf
       decode_ahead();
       continue;
     }
@@ -905,75 +917,122 @@ __device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t smem,
       ptx::tmem_st_wait();
       ptx::tc_fence_before();
       ptx::mbar_arrive(br.p_full(b));
-      // one step after an O store was issued its source has long been read:
-      // hand that V stage back to the producer
-      if (threadIdx.x == 0 && pending_stage != kNoStage) {
-        ptx::bulk_wait_read_all();
-        ptx::mbar_arrive(br.v_empty(pending_stage));
-        pending_stage = kNoStage;
-      }
     }
     g += cnt;
     if (!ok) return;
-    decode_ahead();  // while the last P.V runs
-    // epilogue
-    ok = wait_bar(br, p.status, br.o_full(), o_phase, kRoleEpilogue);
-    if (!__all_sync(0xffffffffu, ok)) return;
-    o_phase ^= 1u;
-    ptx::tc_fence_after();
-    // combine the halves: half b hands (m_b, l_b) to half a through shared
-    // memory; half a forms the final scales of O_a and O_b and the LSE and
-    // hands the scales back.
-    float sa = 0.f, sb = 0.f;  // O = O_a * sa + O_b * sb
-    if (half == 1) {
-      ptx::st_shared_f32(xch, m);
-      ptx::st_shared_f32(xch + 4u, l);
-      ptx::mbar_arrive(br.xch_m());
-    } else {
-      ok = wait_bar(br, p.status, br.xch_m(), epi & 1u, kRoleEpilogue);
-    }
-    if (!__all_sync(0xffffffffu, ok)) return;
-    if (half == 0) {
-      const float mb = ptx::ld_shared_f32(xch);
-      const float lb = ptx::ld_shared_f32(xch + 4u);
-      // a half (with an explicit mask: both) may have seen no visible key
-      const float mm = fmaxf(m, mb);
-      const float ea = (m == -INFINITY) ? 0.f : ptx::ex2_approx(m - mm);
-      const float eb = (mb == -INFINITY) ? 0.f : ptx::ex2_approx(mb - mm);
-      const float ll = l * ea + lb * eb;
-      const float inv_l = ll > 0.f ? 1.f / ll : 0.f;  // no visible key: O = 0
-      sa = ea * inv_l;
-      sb = eb * inv_l;
-      if (row_ok && p.lse != nullptr)
-        p.lse[grow] = ll > 0.f ? (mm + ptx::lg2_approx(ll)) * kLn2 : -INFINITY;
-      ptx::st_shared_f32(xch, sa);
-      ptx::st_shared_f32(xch + 4u, sb);
-      ptx::mbar_arrive(br.xch_s());
-    } else {
-      ok = wait_bar(br, p.status, br.xch_s(), epi & 1u, kRoleEpilogue);
+    decode_ahead();
+    // Hand this half's row statistics to the epilogue warpgroup, which
+    // combines the halves and writes O and the LSE once the unit's last P.V
+    // has completed; meanwhile this warp goes on with the next unit.  The
+    // slot is free once the epilogue has read the previous unit's values.
+    if (epi > 0) {
+      ok = wait_bar(br, p.status, br.ml_empty(), (epi - 1u) & 1u, kRoleSoftmax);
       if (!__all_sync(0xffffffffu, ok)) return;
-      sa = ptx::ld_shared_f32(xch);
-      sb = ptx::ld_shared_f32(xch + 4u);
     }
-    // staging tile: the V stage of this unit's last key tile (g counts V
-    // tiles too); its PV has completed (o_full)
+    ptx::st_shared_f32(xch, m);
+    ptx::st_shared_f32(xch + 4u, l);
+    ptx::mbar_arrive(br.ml_full());
+    ++epi;
+  }
+}
+
+// ------------------------------------------------------------------ epilogue
+
+// Warps 12-15, one query row per thread (warp 12 + q reads TMEM lane quadrant
+// q), one unit behind the softmax.  Per unit: the two halves' statistics give
+//   m = max(m_a, m_b),  l = l_a 2^(m_a - m) + l_b 2^(m_b - m),
+//   O = (O_a 2^(m_a - m) + O_b 2^(m_b - m)) / l,  LSE = ln 2 (m + log2 l);
+// O_a and O_b are read out of TMEM as soon as the unit's last P.V has
+// completed (then o_free lets the next unit's first P.V overwrite them), O is
+// staged in the V ring stage of the unit's last key tile in the TMA layout
+// and written with one TMA store per 64-column slab, and the stage is handed
+// back to the producer once the store has read it.  A unit with no visible
+// key gets O = 0 and LSE = -inf with plain stores.
+template <int D, bool BF16, bool MASK>
+__device__ void epilogue_role(const KParams& p, const Bars<D>& br, uint32_t smem, uint32_t tmem,
+                              const CUtensorMap* tm_o) {
+  using C = Cfg<D>;
+  const int t = static_cast<int>(threadIdx.x) - kEpiWarp0 * 32;  // row within the tile = TMEM lane
+  const uint32_t quad = static_cast<uint32_t>(t) >> 5;
+  const uint32_t lane_addr = (quad * 32u) << 16;
+  const uint32_t t_oa = tmem + lane_addr + C::kColOa;
+  const uint32_t t_ob = tmem + lane_addr + C::kColOb;
+  const uint32_t xch = smem + C::kOffXch + static_cast<uint32_t>(t) * 16u;
+  const bool leader = t == 0;  // issues the O stores
+  uint32_t epi = 0;            // units with key tiles so far
+  uint32_t g = 0;              // V tiles of all units so far (the staging stage)
+  const int rounds = (p.n_units + gridDim.x - 1) / gridDim.x;
+  for (int r = 0; r < rounds; ++r) {
+    const int u = unit_of(r);
+    if (u >= p.n_units) break;
+    const Unit w = decode_unit<MASK>(p, u);
+    const int row = w.m0 + t;
+    const bool row_ok = row < p.Lq;
+    const int64_t grow = static_cast<int64_t>(w.bh) * p.Lq + row;  // LSE row
+    if (w.last < 0) {  // no visible key: O = 0, LSE = -inf
+      if (row_ok) {
+        // rows of O are d_o elements long (D = 16 and 32 run the D = 64 instance)
+        const int64_t orow = w.b * p.o_sb + w.hq * p.o_sh + row * p.o_sl;
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.o) + orow * 2);
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) {
+          if (c < p.d_o / 8) dst[c] = make_uint4(0u, 0u, 0u, 0u);
+        }
+        if (p.lse != nullptr) p.lse[grow] = -INFINITY;
+      }
+      continue;
+    }
+    // visited key tiles of the unit (the staging stage is the last one's)
+    uint32_t n_tiles = static_cast<uint32_t>(w.last) + 1u;
+    if constexpr (MASK) {
+      TileWalk<MASK> tw;
+      tw.init(p, w);
+      n_tiles = 0;
+      for (int j = tw.next(0, w.last); j <= w.last; j = tw.next(j + 1, w.last)) ++n_tiles;
+    }
+    g += n_tiles;
+    // the row statistics of both halves
+    if (!__all_sync(0xffffffffu, wait_bar(br, p.status, br.ml_full(), epi & 1u, kRoleEpilogue)))
+      return;
+    const float ma = ptx::ld_shared_f32(xch), la = ptx::ld_shared_f32(xch + 4u);
+    const float mb = ptx::ld_shared_f32(xch + 8u), lb = ptx::ld_shared_f32(xch + 12u);
+    ptx::mbar_arrive(br.ml_empty());
+    // a half (with an explicit mask: both) may have seen no visible key
+    const float mm = fmaxf(ma, mb);
+    const float ea = (ma == -INFINITY) ? 0.f : ptx::ex2_approx(ma - mm);
+    const float eb = (mb == -INFINITY) ? 0.f : ptx::ex2_approx(mb - mm);
+    const float ll = la * ea + lb * eb;
+    const float inv_l = ll > 0.f ? 1.f / ll : 0.f;  // no visible key: O = 0
+    const float sa = ea * inv_l, sb = eb * inv_l;
+    if (row_ok && p.lse != nullptr)
+      p.lse[grow] = ll > 0.f ? (mm + ptx::lg2_approx(ll)) * kLn2 : -INFINITY;
+    // O_a and O_b: complete once the unit's last P.V is
+    if (!__all_sync(0xffffffffu, wait_bar(br, p.status, br.o_full(), epi & 1u, kRoleEpilogue)))
+      return;
+    ptx::tc_fence_after();
+    // staging tile: the V stage of this unit's last key tile; its P.V has
+    // completed (o_full)
     const uint32_t vstage = (g - 1u) % C::kVStages;
     const uint32_t stage = smem + C::kOffV + vstage * C::kKVBytes;
-    // O as 16-bit pairs into the staging tile, each half its D/2 columns:
-    // 64-column slabs of 128-byte rows, the 16-byte chunk k of row r at chunk
-    // position k ^ (r % 8) (the 128-byte swizzle of the O tensor map)
-    const uint32_t stage_row = stage + static_cast<uint32_t>(lane_row) * 128u;
-    const uint32_t rsw = static_cast<uint32_t>(lane_row) & 7u;
+    // O as 16-bit pairs into the staging tile: 64-column slabs of 128-byte
+    // rows, the 16-byte chunk k of row r at chunk position k ^ (r % 8) (the
+    // 128-byte swizzle of the O tensor map)
+    const uint32_t stage_row = stage + static_cast<uint32_t>(t) * 128u;
+    const uint32_t rsw = static_cast<uint32_t>(t) & 7u;
     const uint64_t sa2 = ptx::f2_pack(sa, sa);
     const uint64_t sb2 = ptx::f2_pack(sb, sb);
 #pragma unroll 1
-    for (int c0 = half * (D / 2); c0 < (half + 1) * (D / 2); c0 += 32) {
-      uint32_t oa[32], ob[32];
-      ptx::tmem_ld32(t_oa + c0, oa);
-      ptx::tmem_ld32(t_ob + c0, ob);
-      uint32_t h[16];
+    for (int c0 = 0; c0 < D; c0 += 16) {
+      uint32_t oa[16], ob[16];
+      ptx::tmem_ld16(t_oa + c0, oa);
+      ptx::tmem_ld16(t_ob + c0, ob);
+      if (c0 + 16 == D) {  // every TMEM read of this unit is done
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(br.o_free());
+      }
+      uint32_t h[8];
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
+      for (int c = 0; c < 8; ++c) {
         const uint64_t o2 = ptx::f2_fma(
             ptx::f2_pack(__uint_as_float(oa[2 * c]), __uint_as_float(oa[2 * c + 1])), sa2,
             ptx::f2_mul(ptx::f2_pack(__uint_as_float(ob[2 * c]), __uint_as_float(ob[2 * c + 1])), sb2));
@@ -984,22 +1043,24 @@ __device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t smem,
       const uint32_t slab = stage_row + static_cast<uint32_t>(c0 / 64) * C::kSlabQ;
       const uint32_t k0 = static_cast<uint32_t>(c0 % 64) / 8u;
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
+      for (int i = 0; i < 2; ++i)
         ptx::st_shared_v4(slab + (((k0 + i) ^ rsw) << 4),
                           make_uint4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]));
     }
     ptx::fence_proxy_async_shared();  // the generic-proxy writes, before the TMA reads them
     ptx::mbar_arrive(br.o_staged());
-    if (threadIdx.x == 0) {
+    if (leader) {
       // rows past Lq are outside the tensor map and are not written
-      if (wait_bar(br, p.status, br.o_staged(), epi & 1u, kRoleEpilogue)) {
+      if (!wait_bar(br, p.status, br.o_staged(), epi & 1u, kRoleEpilogue)) return;
 #pragma unroll
-        for (int hs = 0; hs < C::kHalves; ++hs)
-          ptx::tma_store_4d(tm_o, stage + hs * C::kSlabQ, hs * 64, w.m0, w.hq, w.b);
-        ptx::bulk_commit_group();
-        pending_stage = vstage;  // released after the next softmax step
-      }
+      for (int hs = 0; hs < C::kHalves; ++hs)
+        ptx::tma_store_4d(tm_o, stage + hs * C::kSlabQ, hs * 64, w.m0, w.hq, w.b);
+      ptx::bulk_commit_group();
+      // once the store has read the staging tile, the producer may refill it
+      ptx::bulk_wait_read_all();
+      ptx::mbar_arrive(br.v_empty(vstage));
     }
+    __syncwarp();
     ++epi;
   }
 }
@@ -1016,6 +1077,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t smem = (ptx::smem_u32(smem_raw) + 1023u) & ~1023u;
+  // the layout needs a 1024-byte aligned base and no more than kSmemBytes:
+  // otherwise leave at once (every thread alike, before any barrier exists)
+  if (smem != ptx::smem_u32(smem_raw)) {
+    if (threadIdx.x == 0) atomicOr(p.status, kStatusLayout);
+    return;
+  }
   const Bars<D> br{smem + C::kOffBar};
 
   const int warp = threadIdx.x >> 5;
@@ -1039,9 +1106,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int b = 0; b < C::kScoreBufs; ++b) ptx::mbar_init(br.pv_done(b), 1);
     ptx::mbar_init(br.o_full(), 1);
     ptx::mbar_init(br.drain(), 2);  // one commit from each issuer
-    ptx::mbar_init(br.o_staged(), kSoftmaxThreads);
-    ptx::mbar_init(br.xch_m(), kSoftmaxThreads / 2);
-    ptx::mbar_init(br.xch_s(), kSoftmaxThreads / 2);
+    ptx::mbar_init(br.o_staged(), kEpiThreads);
+    ptx::mbar_init(br.ml_full(), kSoftmaxThreads);
+    ptx::mbar_init(br.ml_empty(), kEpiThreads);
+    ptx::mbar_init(br.o_free(), kEpiThreads);
     ptx::st_shared_volatile(br.abort_word(), 0u);
     ptx::fence_barrier_init();
   }
@@ -1051,7 +1119,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::prefetch_tensormap(&tm_v);
     if constexpr (BF16) ptx::prefetch_tensormap(&tm_v16);
   }
-  if (threadIdx.x == 0) ptx::prefetch_tensormap(&tm_o);
+  if (warp == kEpiWarp0 && lane == 0) ptx::prefetch_tensormap(&tm_o);
   if (warp == kPvWarp) {
     ptx::tmem_alloc(br.tmem_word(), C::kTmemCols);
     ptx::tmem_relinquish();
@@ -1061,17 +1129,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = ptx::ld_shared_volatile(br.tmem_word());
 
-  if (warp == kProducerWarp) {
-    if (lane == 0) producer_role<D, BF16, MASK>(p, br, smem, &tm_q, &tm_k, &tm_v, &tm_v16);
-  } else if (warp == kPvWarp) {
-    pv_issuer_role<D, BF16, MASK>(p, br, smem, tmem);  // whole warp
-  } else if (warp == kSWarp) {
-    s_issuer_role<D, BF16, MASK>(p, br, smem, tmem);  // whole warp
+  if (warp >= kEpiWarp0) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kOtherRegs));
+    epilogue_role<D, BF16, MASK>(p, br, smem, tmem, &tm_o);  // warps 12-15
+    // the last O store: complete before the CTA (and its shared memory) goes
+    if (warp == kEpiWarp0 && lane == 0) ptx::bulk_wait_all();
+  } else if (warp >= kProducerWarp) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kOtherRegs));
+    if (warp == kProducerWarp) {
+      if (lane == 0) producer_role<D, BF16, MASK>(p, br, smem, &tm_q, &tm_k, &tm_v, &tm_v16);
+    } else if (warp == kPvWarp) {
+      pv_issuer_role<D, BF16, MASK>(p, br, smem, tmem);  // whole warp
+    } else if (warp == kSWarp) {
+      s_issuer_role<D, BF16, MASK>(p, br, smem, tmem);  // whole warp
+    }
+    // warp 11 has no role
   } else {
-    softmax_role<D, BF16, MASK>(p, br, smem, tmem, &tm_o);  // warps 0-7
-    // the last O stores read their staging tiles: finish before shared memory
-    // goes (no stage needs releasing: the producer has no loads left)
-    if (threadIdx.x == 0) ptx::bulk_wait_all();
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
+    softmax_role<D, BF16, MASK>(p, br, smem, tmem);  // warps 0-7
   }
 
   ptx::tc_fence_before();
@@ -1093,6 +1168,12 @@ cudaError_t launch_instance(const Problem& pr, const CUtensorMap* maps, int num_
   if (e != cudaSuccess) return e;
   const uint64_t bit = dev < 64 ? (1ull << dev) : 0ull;
   if (bit == 0 || (configured.load(std::memory_order_relaxed) & bit) == 0) {
+    // The setmaxnreg split is only safe when the CTA is launched with exactly
+    // kLaunchRegs registers per thread: refuse to launch anything else.
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidKernelImage;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit, std::memory_order_relaxed);

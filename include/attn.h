@@ -584,13 +584,15 @@ attn_status_t attn_host_plan(int B, int Hq, int Hkv, int L, int D, attn_dtype_t 
 /*
  * attn_status -- synchronise `stream`, then read and clear the device status
  * word of the current device.  *device_code (may be NULL) receives the raw
- * word: bit 0 a bounded wait timed out, bit 1 a valid_len value was clamped;
+ * word: bit 0 a bounded wait timed out, bit 1 a valid_len value was clamped,
+ * bit 2 a kernel found its shared memory smaller or less aligned than its
+ * layout needs (it then did nothing; reported as ATTN_ERR_ARCH);
  * bits 8..11 are a set of role flags, one per waiting role that timed out
  * (0x100 the TMA producer, 0x200 an MMA issuer, 0x400 the softmax, 0x800 the
  * epilogue), ORed over every timed-out wait of every CTA and call since the
  * word was last read.  Returns ATTN_OK, ATTN_ERR_TIMEOUT,
  * ATTN_ERR_VALID_LEN (timeout wins when both are set) or ATTN_ERR_CUDA when
- * the synchronisation itself reported an error.
+ * the synchronisation itself reported an error (ATTN_ERR_ARCH for bit 2).
  */
 attn_status_t attn_status(attn_stream_t stream, int* device_code);
 

@@ -82,7 +82,7 @@ def test_query_static_fields(lib):
         caps = attn.query(D, attn.ATTN_BF16)
         assert caps["block_m"] == 128 and caps["block_n"] == 128
         assert caps["q_tiles_per_cta"] == 1 and caps["kv_stages"] == stages
-        assert caps["threads"] == 352 and caps["tmem_cols"] == 512
+        assert caps["threads"] == 512 and caps["tmem_cols"] == 512
         assert 0 < caps["smem_bytes"] <= 232448
         assert caps["lse_natural_log"] == 1
     with pytest.raises(attn.AttnError):
