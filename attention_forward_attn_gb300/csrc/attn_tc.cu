@@ -69,9 +69,12 @@ constexpr int BH = BN / 2;    // keys of one half tile (one softmax warpgroup's 
 constexpr int kProducerWarp = 8;
 constexpr int kPvWarp = 9;     // P.V issuer; also allocates TMEM
 constexpr int kSWarp = 10;     // score issuer
+constexpr int kDecodeWarp = 11;  // decodes the CTA's units ahead of the softmax
 constexpr int kEpiWarp0 = 12;  // warps 12-15: epilogue (warp 12 + q reads TMEM lane quadrant q)
+constexpr int kUnitSlots = 4;  // decoded units in flight (shared-memory ring)
+constexpr int kUnitWords = 12; // 32-bit words per ring slot
 // warpgroups: softmax half a, softmax half b, control (producer, two issuers,
-// an idle warp), epilogue
+// unit decoder), epilogue
 constexpr int kThreads = 512;
 constexpr int kSoftmaxThreads = 256;
 constexpr int kEpiThreads = 128;
@@ -82,8 +85,8 @@ constexpr int kEpiThreads = 128;
 // or an increase could wait forever: launch_instance refuses a build whose
 // register count differs.
 constexpr int kLaunchRegs = 128;
-constexpr int kSoftmaxRegs = 168;
-constexpr int kOtherRegs = 88;
+constexpr int kSoftmaxRegs = 160;
+constexpr int kOtherRegs = 96;
 static_assert(2 * 128 * kSoftmaxRegs + 2 * 128 * kOtherRegs == kThreads * kLaunchRegs,
               "register split must equal the launch pool");
 constexpr float kRescaleLog2 = 8.0f;  // rescale O only when the max grows by > 2^8
@@ -108,15 +111,17 @@ struct Cfg {
   static_assert(kQBytes == kKVBytes, "an O tile is staged in a V stage");
   // barrier block: q_full q_empty k_full[KS] k_empty[KS] v_full[VS] v_empty[VS]
   // s_full[SB] p_full[SB] pv_done[SB] o_full drain o_staged ml_full ml_empty
-  // o_free, then 32-bit words: TMEM base, abort flag; then the row statistics
-  // the softmax hands to the epilogue (m_a, l_a, m_b, l_b per row)
-  static constexpr int kNumBars = 2 + 2 * kKStages + 2 * kVStages + 3 * kScoreBufs + 6;
+  // o_free unit_full[kUnitSlots] unit_empty[kUnitSlots], then 32-bit words:
+  // TMEM base, abort flag; then the row statistics the softmax hands to the
+  // epilogue (m_a, l_a, m_b, l_b per row); then the ring of decoded units
+  static constexpr int kNumBars = 2 + 2 * kKStages + 2 * kVStages + 3 * kScoreBufs + 6 + 2 * kUnitSlots;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kMiscBytes = 8;
-  static constexpr int kOffXch = kOffMisc + kMiscBytes;
+  static constexpr int kOffXch = (kOffMisc + kMiscBytes + 15) / 16 * 16;  // 16-byte aligned
+  static constexpr int kOffRing = kOffXch + BM * 16;                      // 16-byte aligned
   // Dynamic shared memory starts 1024-byte aligned (the tiles need it); the
   // kernel checks that the layout fits what it was given.
-  static constexpr int kSmemBytes = kOffXch + BM * 16;
+  static constexpr int kSmemBytes = kOffRing + kUnitSlots * kUnitWords * 4;
   // TMEM columns: score buffers S_b (fp32, BN each; each half's P is written
   // over the first columns of that half), then the two partial accumulators:
   // O_a (keys of the first half of every tile) and O_b (second half).
@@ -126,6 +131,7 @@ struct Cfg {
   static constexpr uint32_t kTmemCols = 512;
   static_assert(kScoreBufs * BN + 2 * D <= 512, "TMEM budget");
   static_assert(kSmemBytes <= 232448, "shared-memory budget");
+  static_assert(kOffRing % 16 == 0, "ring slots are read with 16-byte accesses");
 };
 
 // Shared-memory addresses of the barriers (32-bit, one base + constants).
@@ -162,8 +168,15 @@ struct Bars {
   __device__ __forceinline__ uint32_t ml_empty() const { return base + 8u * (6 + 2 * KS + 2 * VS + 3 * SB); }
   // the epilogue has read O_a and O_b out of TMEM (the next unit may overwrite them)
   __device__ __forceinline__ uint32_t o_free() const { return base + 8u * (7 + 2 * KS + 2 * VS + 3 * SB); }
+  // ring slot s holds a decoded unit / the softmax has read it
+  __device__ __forceinline__ uint32_t unit_full(uint32_t s) const {
+    return base + 8u * (8 + 2 * KS + 2 * VS + 3 * SB + s);
+  }
+  __device__ __forceinline__ uint32_t unit_empty(uint32_t s) const {
+    return base + 8u * (8 + 2 * KS + 2 * VS + 3 * SB + kUnitSlots + s);
+  }
   __device__ __forceinline__ uint32_t tmem_word() const {
-    return base + 8u * (8 + 2 * KS + 2 * VS + 3 * SB);
+    return base + 8u * (8 + 2 * KS + 2 * VS + 3 * SB + 2 * kUnitSlots);
   }
   __device__ __forceinline__ uint32_t abort_word() const { return tmem_word() + 4u; }
 };
@@ -664,6 +677,70 @@ __device__ void pv_issuer_role(const KParams& p, const Bars<D>& br, uint32_t sme
   drain_wait(br.drain(), 0);
 }
 
+// ------------------------------------------------------------------ unit decoder
+
+// A decoded unit and its fp16-flag mask in a ring slot (kUnitWords words).
+__device__ __forceinline__ void write_unit(uint32_t slot_addr, const Unit& w, uint32_t fmask) {
+  const uint32_t v[kUnitWords] = {static_cast<uint32_t>(w.bh), static_cast<uint32_t>(w.b),
+                                  static_cast<uint32_t>(w.hq), static_cast<uint32_t>(w.hkv),
+                                  static_cast<uint32_t>(w.mb), static_cast<uint32_t>(w.m0),
+                                  static_cast<uint32_t>(w.kv_len), static_cast<uint32_t>(w.mblk),
+                                  static_cast<uint32_t>(w.n), static_cast<uint32_t>(w.last), fmask, 0u};
+#pragma unroll
+  for (int i = 0; i < kUnitWords; i += 4)
+    ptx::st_shared_v4(slot_addr + i * 4, make_uint4(v[i], v[i + 1], v[i + 2], v[i + 3]));
+}
+
+__device__ __forceinline__ Unit read_unit(uint32_t slot_addr, uint32_t* fmask) {
+  const uint4 a = ptx::ld_shared_v4(slot_addr);
+  const uint4 b = ptx::ld_shared_v4(slot_addr + 16u);
+  const uint4 c = ptx::ld_shared_v4(slot_addr + 32u);
+  Unit w;
+  w.bh = static_cast<int>(a.x);
+  w.b = static_cast<int>(a.y);
+  w.hq = static_cast<int>(a.z);
+  w.hkv = static_cast<int>(a.w);
+  w.mb = static_cast<int>(b.x);
+  w.m0 = static_cast<int>(b.y);
+  w.kv_len = static_cast<int>(b.z);
+  w.mblk = static_cast<int>(b.w);
+  w.n = static_cast<int>(c.x);
+  w.last = static_cast<int>(c.y);
+  *fmask = c.z;
+  return w;
+}
+
+// Warp 11: decodes the CTA's units in order, kUnitSlots ahead of the
+// softmax, and checks valid_len (values outside [0, Lk] are clamped by the
+// decode and reported in the status word).
+template <int D, bool BF16, bool MASK>
+__device__ void decoder_role(const KParams& p, const Bars<D>& br, uint32_t smem) {
+  using C = Cfg<D>;
+  const int rounds = (p.n_units + gridDim.x - 1) / gridDim.x;
+  const bool lead = (threadIdx.x & 31) == 0;
+  for (int r = 0; r < rounds; ++r) {
+    const int u = unit_of(r);
+    if (u >= p.n_units) break;
+    const Unit w = decode_unit<MASK>(p, u);
+    const uint32_t fmask = v_fp16_mask<BF16>(p, w.b * p.Hkv + w.hkv, 0, w.n);  // whole warp
+    if (lead && p.valid_len != nullptr) {
+      const int vl = p.valid_len[w.b];
+      if (vl < 0 || vl > p.Lk) atomicOr(p.status, kStatusValidLenClamped);
+    }
+    const uint32_t slot = static_cast<uint32_t>(r) % kUnitSlots;
+    if (r >= kUnitSlots &&
+        !__all_sync(0xffffffffu, wait_bar(br, p.status, br.unit_empty(slot),
+                                          (static_cast<uint32_t>(r) / kUnitSlots - 1u) & 1u,
+                                          kRoleProducer)))
+      return;
+    if (lead) {
+      write_unit(smem + C::kOffRing + slot * (kUnitWords * 4), w, fmask);
+      ptx::mbar_arrive(br.unit_full(slot));  // release: the slot's words before the arrive
+    }
+    __syncwarp();
+  }
+}
+
 // ------------------------------------------------------------------ softmax + epilogue
 
 // P for one half row (64 keys in registers), 32 keys at a time, written over
@@ -742,38 +819,24 @@ __device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t smem,
   uint32_t epi = 0;  // units with key tiles done so far (their statistics handed over)
   uint32_t g = 0;    // score (and V) tiles of all units so far (buffer g % SB)
 
-  // Each unit is decoded one unit ahead, with the fp16 flags of its first
-  // 32 key tiles: during the previous unit's wait for its last P.V, where the
-  // integer divisions and the flag load cost nothing.  Unit indices grow
-  // with the round, so the first one past the end ends the loop.
+  // Units come decoded, with the fp16 flags of their first 32 key tiles,
+  // from the decoder warp through a shared-memory ring: the integer
+  // divisions and the global loads of valid_len and the flags stay off the
+  // softmax warps.  Unit indices grow with the round, so the first one past
+  // the end ends the loop.
   const int rounds = (p.n_units + gridDim.x - 1) / gridDim.x;
-  int u_next = unit_of(0);
-  Unit w_next;
-  uint32_t fmask_next = 0;
-  if (u_next < p.n_units) {
-    w_next = decode_unit<MASK>(p, u_next);
-    fmask_next = v_fp16_mask<BF16>(p, w_next.b * p.Hkv + w_next.hkv, 0, w_next.n);
-  }
-  for (int r = 0; r < rounds && u_next < p.n_units; ++r) {
-    const Unit w = w_next;
-    uint32_t fmask = fmask_next;
-    auto decode_ahead = [&]() {
-      u_next = unit_of(r + 1);
-      if (u_next < p.n_units) {
-        w_next = decode_unit<MASK>(p, u_next);
-        fmask_next = v_fp16_mask<BF16>(p, w_next.b * p.Hkv + w_next.hkv, 0, w_next.n);
-      }
-    };
+  for (int r = 0; r < rounds; ++r) {
+    if (unit_of(r) >= p.n_units) break;
+    const uint32_t slot = static_cast<uint32_t>(r) % kUnitSlots;
+    if (!__all_sync(0xffffffffu, wait_bar(br, p.status, br.unit_full(slot),
+                                          (static_cast<uint32_t>(r) / kUnitSlots) & 1u, kRoleSoftmax)))
+      return;
+    uint32_t fmask;
+    const Unit w = read_unit(smem + C::kOffRing + slot * (kUnitWords * 4), &fmask);
+    ptx::mbar_arrive(br.unit_empty(slot));
     const int row = w.m0 + lane_row;
     const bool row_ok = row < p.Lq;
-    if (threadIdx.x == 0 && p.valid_len != nullptr) {
-      const int vl = p.valid_len[w.b];
-      if (vl < 0 || vl > p.Lk) atomicOr(p.status, kStatusValidLenClamped);
-    }
-    if (w.last < 0) {  // no visible key: the epilogue writes O = 0, LSE = -inf
-      decode_ahead();
-      continue;
-    }
+    if (w.last < 0) continue;  // no visible key: the epilogue writes O = 0, LSE = -inf
     const int z_kv = w.b * p.Hkv + w.hkv;
     // keys < key_lim are visible to this row
     const int key_lim = p.causal ? min(w.kv_len, row + 1) : w.kv_len;
@@ -920,7 +983,6 @@ __device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t smem,
     }
     g += cnt;
     if (!ok) return;
-    decode_ahead();
     // Hand this half's row statistics to the epilogue warpgroup, which
     // combines the halves and writes O and the LSE once the unit's last P.V
     // has completed; meanwhile this warp goes on with the next unit.  The
@@ -1110,6 +1172,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::mbar_init(br.ml_full(), kSoftmaxThreads);
     ptx::mbar_init(br.ml_empty(), kEpiThreads);
     ptx::mbar_init(br.o_free(), kEpiThreads);
+    for (int s = 0; s < kUnitSlots; ++s) {
+      ptx::mbar_init(br.unit_full(s), 1);
+      ptx::mbar_init(br.unit_empty(s), kSoftmaxThreads);
+    }
     ptx::st_shared_volatile(br.abort_word(), 0u);
     ptx::fence_barrier_init();
   }
@@ -1142,8 +1208,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       pv_issuer_role<D, BF16, MASK>(p, br, smem, tmem);  // whole warp
     } else if (warp == kSWarp) {
       s_issuer_role<D, BF16, MASK>(p, br, smem, tmem);  // whole warp
+    } else {
+      decoder_role<D, BF16, MASK>(p, br, smem);  // warp 11, whole warp
     }
-    // warp 11 has no role
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
     softmax_role<D, BF16, MASK>(p, br, smem, tmem);  // warps 0-7
