@@ -878,16 +878,17 @@ __device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t smem,
         }
       }
       ptx::tc_fence_after();
+      // the half row's scores with their maximum, reduced by the load itself
       uint32_t s[BH];
-      ptx::tmem_ld64(t_s, s);
+      float mx = ptx::tmem_ld64_max(t_s, s);
       const int n0 = j * BN + half * BH;  // key of column 0 of this half
       const bool masked = partial || (n0 + BH > w.kv_len) || (p.causal && n0 + BH - 1 > w.m0);
       const int c_lim = key_lim - n0;  // columns c < c_lim are visible
       // Boundary and partially masked tiles only: invisible scores become
-      // -inf, so the max and the exponentials below are the same code for
-      // every tile (one copy of the unrolled loops keeps the hot code small);
-      // exp2(-inf * scale - m) = 0 because the scale is > 0 (a zero sm_scale
-      // arrives as FLT_MIN).
+      // -inf and the maximum is taken again over what is left, so the
+      // exponentials below are the same code for every tile (one copy of the
+      // unrolled loop keeps the hot code small); exp2(-inf * scale - m) = 0
+      // because the scale is > 0 (a zero sm_scale arrives as FLT_MIN).
       if (masked) {
         if constexpr (MASK) {
           // columns >= c_lim leave the keep bits first; then per column one
@@ -918,16 +919,16 @@ __device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t smem,
 #pragma unroll
           for (int c = 0; c < BH; ++c) s[c] = (c < c_lim) ? s[c] : 0xFF800000u;
         }
+        // max of the visible scores: 8 independent chains of 3-input maxima
+        float mxk[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mxk[k] = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < BH / 2; ++i)
+          mxk[i & 7] = ptx::max3(mxk[i & 7], __uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1]));
+        mx = ptx::max3(ptx::max3(mxk[0], mxk[1], mxk[2]), ptx::max3(mxk[3], mxk[4], mxk[5]),
+                       fmaxf(mxk[6], mxk[7]));
       }
-      // max of the half row: 8 independent chains of 3-input maxima
-      float mxk[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) mxk[k] = -INFINITY;
-#pragma unroll
-      for (int i = 0; i < BH / 2; ++i)
-        mxk[i & 7] = ptx::max3(mxk[i & 7], __uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1]));
-      const float mx = ptx::max3(ptx::max3(mxk[0], mxk[1], mxk[2]), ptx::max3(mxk[3], mxk[4], mxk[5]),
-                                 fmaxf(mxk[6], mxk[7]));
       const float m_tile = (mx == -INFINITY) ? -INFINITY : mx * scale_log2;
       const float m_new = fmaxf(m, m_tile);
       float alpha = 1.f;
