@@ -10,29 +10,32 @@
 //   * work unit = (b, h_q, 128 query rows), one query tile; K/V streamed in
 //     tiles of 128 keys;
 //   * warp 8 (producer): TMA loads of the Q tile and of the K and V rings
-//     (3 + 3 stages at D=128, 6 + 6 at D=64), 128-byte swizzled;
+//     (2 + 3 stages at D=128, 6 + 6 at D=64), 128-byte swizzled;
 //   * warps 9 and 10 (MMA issuers; one elected lane each issues): warp 10
-//     issues S(j) = Q K_j^T into one of SB TMEM score buffers (SB = 2 at
-//     D=128, 3 at D=64), warp 9 issues the P.V products with P read from
-//     TMEM.  The scores run up to SB key tiles ahead of the softmax (S(j+SB)
-//     goes into the buffer P(j) came from, once PV(j) has completed), so the
-//     tensor core has work queued while P(j) is being computed;
+//     issues S(j) = Q K_j^T into one of three TMEM score buffers, warp 9
+//     issues the P.V products with P read from TMEM.  The scores run up to
+//     three key tiles ahead of the softmax (S(j+3) goes into the buffer P(j)
+//     came from, once PV(j) has completed), so the tensor core has work
+//     queued while P(j) is being computed;
 //   * warps 0-7 (softmax, two warpgroups; a TMEM lane is a query row): warp w
 //     and warp w + 4 share the same 32 rows, warps 0-3 (half a) taking key
-//     columns 0-63 of every tile and warps 4-7 (half b) columns 64-127.  Each
-//     half keeps its own online softmax over its keys -- running max, sum and
-//     a partial accumulator, O_a or O_b in TMEM (O_h += P_h V_h) -- so the
-//     two never wait for each other inside a unit.  Per step a thread loads
-//     its 64 scores, masks them (only on boundary tiles), takes the max,
-//     ex2.approx, the sum, writes P into TMEM over its S columns and
-//     rescales its O_h row in TMEM when its max grew by more than 2^8 (exact
-//     after the final division).  The epilogue combines the halves
-//     (O = (O_a 2^(m_a-m) + O_b 2^(m_b-m)) / l), stages O in shared memory
-//     in the TMA layout (each half its D/2 columns) and writes it with one
-//     TMA store per 64-column slab, and the LSE.  The staging tile is the V
-//     ring stage of the unit's last key tile: idle from its PV's completion
-//     until the producer refills it, so the epilogue, not the PV issuer,
-//     releases that stage once the store has read it.
+//     columns 0-63 of every tile and warps 4-7 (half b) columns 64-127.  Per
+//     step a thread loads its 64 scores with their maximum (tcgen05.ld.red),
+//     masks them (only on boundary tiles), ex2.approx, the sum, writes P into
+//     TMEM over its S columns and rescales O in TMEM when the max grew by
+//     more than 2^8 (exact after the final division).  D = 64: each half
+//     keeps its own online softmax -- running max, sum and a partial
+//     accumulator, O_a or O_b (O_h += P_h V_h) -- so the two never wait for
+//     each other inside a unit, and the epilogue combines them
+//     (O = (O_a 2^(m_a-m) + O_b 2^(m_b-m)) / l).  D = 128: TMEM holds three
+//     score buffers only next to one 128-column accumulator, so the halves
+//     share O and agree on the running max at every step through shared
+//     memory.  The epilogue warpgroup stages O in shared memory in the TMA
+//     layout and writes it with one TMA store per 64-column slab, and the
+//     LSE.  The staging tile is the V ring stage of the unit's last key tile:
+//     idle from its PV's completion until the producer refills it, so the
+//     epilogue, not the PV issuer, releases that stage once the store has
+//     read it.
 // Causal units skip every key tile above the diagonal; padded units skip every
 // key tile at or beyond valid_len[b]; a unit with no visible key writes O = 0
 // and LSE = -inf without touching the tensor core.
@@ -94,10 +97,15 @@ constexpr float kLn2 = 0.69314718055994531f;
 
 template <int D>
 struct Cfg {
-  // D = 128: two score buffers (TMEM: 2 x 128 + O_a 128 + O_b 128 = 512
-  // columns); D = 64: three (3 x 128 + 64 + 64)
-  static constexpr int kScoreBufs = (D == 128) ? 2 : 3;
-  static constexpr int kKStages = (D == 128) ? 3 : 6;
+  // Three score buffers at both head dimensions.  D = 64: the two halves keep
+  // separate accumulators O_a, O_b (TMEM: 3 x 128 + 64 + 64 = 512 columns).
+  // D = 128: two 128-column accumulators would leave room for two score
+  // buffers only, so the halves share one O (3 x 128 + 128) and agree on a
+  // common running max every step (kSharedO, see the softmax).
+  static constexpr bool kSharedO = (D == 128);
+  static constexpr int kScoreBufs = 3;
+  // D = 128: 2 K + 3 V stages (3 + 2 measured 3 % slower at C4 and C5)
+  static constexpr int kKStages = (D == 128) ? 2 : 6;
   static constexpr int kVStages = (D == 128) ? 3 : 6;
   static constexpr int kHalves = D / 64;           // 64-column (128-byte) slabs per row
   static constexpr int kQBytes = BM * D * 2;
@@ -119,17 +127,22 @@ struct Cfg {
   static constexpr int kMiscBytes = 8;
   static constexpr int kOffXch = (kOffMisc + kMiscBytes + 15) / 16 * 16;  // 16-byte aligned
   static constexpr int kOffRing = kOffXch + BM * 16;                      // 16-byte aligned
+  // kSharedO: the per-step max exchange between the halves, one 32-bit word
+  // per (step parity, half, row)
+  static constexpr int kOffMx = kOffRing + kUnitSlots * kUnitWords * 4;
+  static constexpr int kMxBytes = kSharedO ? 2 * 2 * BM * 4 : 0;
   // Dynamic shared memory starts 1024-byte aligned (the tiles need it); the
   // kernel checks that the layout fits what it was given.
-  static constexpr int kSmemBytes = kOffRing + kUnitSlots * kUnitWords * 4;
+  static constexpr int kSmemBytes = kOffMx + kMxBytes;
   // TMEM columns: score buffers S_b (fp32, BN each; each half's P is written
-  // over the first columns of that half), then the two partial accumulators:
-  // O_a (keys of the first half of every tile) and O_b (second half).
+  // over the first columns of that half), then the accumulators: O_a (keys
+  // of the first half of every tile) and O_b (second half), or the one
+  // shared O (kColOa == kColOb).
   static __device__ __forceinline__ uint32_t col_s(uint32_t b) { return b * BN; }
   static constexpr uint32_t kColOa = kScoreBufs * BN;
-  static constexpr uint32_t kColOb = kColOa + D;
+  static constexpr uint32_t kColOb = kSharedO ? kColOa : kColOa + D;
   static constexpr uint32_t kTmemCols = 512;
-  static_assert(kScoreBufs * BN + 2 * D <= 512, "TMEM budget");
+  static_assert(kScoreBufs * BN + (kSharedO ? 1 : 2) * D <= 512, "TMEM budget");
   static_assert(kSmemBytes <= 232448, "shared-memory budget");
   static_assert(kOffRing % 16 == 0, "ring slots are read with 16-byte accesses");
 };
@@ -512,7 +525,7 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t q_desc, uint6
 }
 
 // O_h += P_h V_h for the two halves of a key tile (h = a: keys 0-63 into
-// O_a, h = b: keys 64-127 into O_b).  A = P_h from TMEM (16-bit pairs, 8
+// O_a, h = b: keys 64-127 into O_b; with a shared O both into it).  A = P_h from TMEM (16-bit pairs, 8
 // columns per 16 keys, at the start of its half's 64 score columns), B = the
 // half's rows of the V tile as an MN-major 128-byte-swizzled operand (16 keys
 // = two 8-row groups).  fp16 V tile (fp16 inputs, or the exact fp16 copy of
@@ -526,8 +539,10 @@ __device__ __forceinline__ void issue_pv(uint32_t o_a, uint32_t o_b, uint32_t p_
   for (int kk = 0; kk < BN / 16; ++kk) {
     const int h = kk / (BH / 16);
     const int k4 = kk % (BH / 16);
+    // a unit's first product starts its accumulator (the shared O: once)
+    const bool acc = accumulate || (Cfg<D>::kSharedO ? kk > 0 : k4 > 0);
     ptx::mma_ts(h ? o_b : o_a, p_tmem + h * BH + k4 * 8u, desc_add(v_desc, kk * 2048u), idesc,
-                (accumulate || k4 > 0) ? 1u : 0u);
+                acc ? 1u : 0u);
   }
   if (split) {
 #pragma unroll 1
@@ -793,15 +808,61 @@ __device__ __forceinline__ float exp_half(const uint32_t (&s)[BH], uint64_t sc2,
   return ra + rb;
 }
 
+// Shared O (D = 128): the two halves of a row agree on one running max at
+// every step.  Each thread publishes its half row's maximum in a shared-memory
+// word per (step parity, half, row) and reads its partner's (the other half,
+// same row).  The word's lowest bit carries bit 1 of the exchange count: a
+// slot holds either this exchange's value or the one two exchanges back (a
+// partner cannot get further ahead, since it needs this thread's next value
+// to pass its next exchange), and the two differ in that bit; the slots start
+// with the bit set, which no exchange 0 or 1 writes.  The value itself is the
+// maximum with its two lowest mantissa bits cleared (at most 3 ulp below it),
+// whatever the count: both halves take the maximum of the same two values, so
+// they agree bit for bit, and the result does not depend on how many
+// exchanges came before (the schedule of units over CTAs).  The lowered max
+// only shifts the offset of the exponentials, exact after the final division.
+// A half with no visible key publishes -FLT_MAX, read back as -inf.  The wait
+// for the partner is bounded like every other wait.
+template <class BarsT>
+__device__ __forceinline__ bool exchange_max(const BarsT& br, int* status, uint32_t mine0,
+                                             uint32_t other0, uint32_t& xs, float& mx) {
+  const uint32_t off = (xs & 1u) * (2u * BM * 4u);
+  const uint32_t tag = (xs >> 1) & 1u;
+  ++xs;
+  const uint32_t v = ((mx == -INFINITY) ? 0xFF7FFFFFu : __float_as_uint(mx)) & ~3u;
+  const uint32_t w = v | tag;
+  ptx::st_shared_volatile(mine0 + off, w);
+  uint32_t o = ptx::ld_shared_volatile(other0 + off);
+  if ((o & 1u) != tag) {
+    const uint64_t t0 = ptx::globaltimer_ns();
+    for (;;) {
+#pragma unroll 1
+      for (int i = 0; i < 16 && (o & 1u) != tag; ++i) o = ptx::ld_shared_volatile(other0 + off);
+      if ((o & 1u) == tag) break;
+      if (ptx::ld_shared_volatile(br.abort_word()) != 0u) return false;
+      if (ptx::globaltimer_ns() - t0 > ATTN_WAIT_LIMIT_NS) {
+        ptx::st_shared_volatile(br.abort_word(), 1u);
+        atomicOr(status, kStatusTimeout | kRoleSoftmax);
+        return false;
+      }
+    }
+  }
+  const float r = fmaxf(__uint_as_float(v), __uint_as_float(o & ~3u));
+  mx = (r < -1.0e38f) ? -INFINITY : r;
+  return true;
+}
+
 // Two softmax warpgroups share every query tile: warps 0-3 (half a) own key
 // columns 0-63 of each key tile and warps 4-7 (half b) columns 64-127, for
-// the same rows (warp w and w + 4 read the same TMEM lane quadrant).  Each
-// half runs its own online softmax -- running max m_h, sum l_h and the
-// partial accumulator O_h over its keys only -- so the two never wait for
-// each other while the tile streams; they meet once per unit, in the
+// the same rows (warp w and w + 4 read the same TMEM lane quadrant).  At
+// D = 64 each half runs its own online softmax -- running max m_h, sum l_h
+// and the partial accumulator O_h over its keys only -- so the two never wait
+// for each other while the tile streams; they meet once per unit, in the
 // epilogue, where the partial results combine exactly:
 //   m = max(m_a, m_b),  l = l_a 2^(m_a - m) + l_b 2^(m_b - m),
 //   O = (O_a 2^(m_a - m) + O_b 2^(m_b - m)) / l.
+// At D = 128 (shared O) the halves exchange their maxima every step, so
+// m_a = m_b and the same formulas reduce to O / (l_a + l_b).
 template <int D, bool BF16, bool MASK>
 __device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t smem, uint32_t tmem) {
   using C = Cfg<D>;
@@ -810,11 +871,17 @@ __device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t smem,
   const int half = static_cast<int>(threadIdx.x) >> 7;  // 0: keys 0-63 of a tile, 1: 64-127
   const uint32_t quad = (threadIdx.x >> 5) & 3u;    // this warp's 32-lane TMEM quadrant
   const uint32_t lane_addr = (quad * 32u) << 16;
-  const uint32_t t_oh = tmem + lane_addr + (half ? C::kColOb : C::kColOa);  // this half's O
-  const uint32_t t_oa = tmem + lane_addr + C::kColOa;
-  const uint32_t t_ob = tmem + lane_addr + C::kColOb;
+  // the O columns this half rescales: its own accumulator, or its half of
+  // the shared one
+  constexpr int kOCols = C::kSharedO ? D / 2 : D;
+  const uint32_t t_oh =
+      tmem + lane_addr + (C::kSharedO ? C::kColOa + half * kOCols : (half ? C::kColOb : C::kColOa));
   // this row's statistics for the epilogue: (m_a, l_a) then (m_b, l_b)
   const uint32_t xch = smem + C::kOffXch + static_cast<uint32_t>(lane_row) * 16u + half * 8u;
+  // shared O: this thread's and its partner's max-exchange slots (parity 0)
+  const uint32_t mx_mine = smem + C::kOffMx + static_cast<uint32_t>(half * BM + lane_row) * 4u;
+  const uint32_t mx_other = smem + C::kOffMx + static_cast<uint32_t>((half ^ 1) * BM + lane_row) * 4u;
+  uint32_t xs = 0;  // max exchanges so far
   const float scale_log2 = p.scale_log2;
   uint32_t epi = 0;  // units with key tiles done so far (their statistics handed over)
   uint32_t g = 0;    // score (and V) tiles of all units so far (buffer g % SB)
@@ -929,6 +996,13 @@ __device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t smem,
         mx = ptx::max3(ptx::max3(mxk[0], mxk[1], mxk[2]), ptx::max3(mxk[3], mxk[4], mxk[5]),
                        fmaxf(mxk[6], mxk[7]));
       }
+      // shared O: the row's max over both halves (the same value in both)
+      if constexpr (C::kSharedO) {
+        if (!__all_sync(0xffffffffu, exchange_max(br, p.status, mx_mine, mx_other, xs, mx))) {
+          ok = false;
+          break;
+        }
+      }
       const float m_tile = (mx == -INFINITY) ? -INFINITY : mx * scale_log2;
       const float m_new = fmaxf(m, m_tile);
       float alpha = 1.f;
@@ -941,9 +1015,9 @@ __device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t smem,
       const float neg_m = (m == -INFINITY) ? 0.f : -m;
       // look ahead (non-blocking): has S(gg+1) completed?  Its answer is used
       // at the next step, so the test's latency hides behind the exponentials.
-      // S(gg+1) may be the next unit's first tile: g counts every tile.  Only
-      // with three score buffers (D = 64), where the scores are normally
-      // ready; with two (D = 128) it measured slower.
+      // S(gg+1) may be the next unit's first tile: g counts every tile.  With
+      // three score buffers the scores are normally ready (with two, at
+      // D = 128 before the shared O, it measured slower).
       if constexpr (SB > 2)
         s_ready = __all_sync(0xffffffffu, ptx::mbar_test_wait(br.s_full((gg + 1u) % SB), ((gg + 1u) / SB) & 1u));
       const uint64_t sc2 = ptx::f2_pack(scale_log2, scale_log2);
@@ -970,7 +1044,7 @@ __device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t smem,
         }
         ptx::tc_fence_after();
 #pragma unroll 1
-        for (int c0 = 0; c0 < D; c0 += 32) {
+        for (int c0 = 0; c0 < kOCols; c0 += 32) {
           uint32_t o[32];
           ptx::tmem_ld32(t_oh + c0, o);
 #pragma unroll
@@ -1086,9 +1160,9 @@ __device__ void epilogue_role(const KParams& p, const Bars<D>& br, uint32_t smem
     const uint64_t sb2 = ptx::f2_pack(sb, sb);
 #pragma unroll 1
     for (int c0 = 0; c0 < D; c0 += 16) {
-      uint32_t oa[16], ob[16];
+      uint32_t oa[16], ob[C::kSharedO ? 1 : 16];
       ptx::tmem_ld16(t_oa + c0, oa);
-      ptx::tmem_ld16(t_ob + c0, ob);
+      if constexpr (!C::kSharedO) ptx::tmem_ld16(t_ob + c0, ob);
       if (c0 + 16 == D) {  // every TMEM read of this unit is done
         ptx::tc_fence_before();
         ptx::mbar_arrive(br.o_free());
@@ -1096,9 +1170,15 @@ __device__ void epilogue_role(const KParams& p, const Bars<D>& br, uint32_t smem
       uint32_t h[8];
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
-        const uint64_t o2 = ptx::f2_fma(
-            ptx::f2_pack(__uint_as_float(oa[2 * c]), __uint_as_float(oa[2 * c + 1])), sa2,
-            ptx::f2_mul(ptx::f2_pack(__uint_as_float(ob[2 * c]), __uint_as_float(ob[2 * c + 1])), sb2));
+        const uint64_t a2 = ptx::f2_pack(__uint_as_float(oa[2 * c]), __uint_as_float(oa[2 * c + 1]));
+        uint64_t o2;
+        if constexpr (C::kSharedO) {
+          o2 = ptx::f2_mul(a2, sa2);  // one accumulator: m_a = m_b, so sa = 1 / l
+        } else {
+          o2 = ptx::f2_fma(a2, sa2,
+                           ptx::f2_mul(ptx::f2_pack(__uint_as_float(ob[2 * c]), __uint_as_float(ob[2 * c + 1])),
+                                       sb2));
+        }
         float o0, o1;
         ptx::f2_unpack(o2, o0, o1);
         h[c] = pack2<BF16>(o0, o1);
@@ -1190,6 +1270,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kPvWarp) {
     ptx::tmem_alloc(br.tmem_word(), C::kTmemCols);
     ptx::tmem_relinquish();
+  }
+  if constexpr (C::kSharedO) {
+    // max-exchange slots: both parities start with the tag bit set
+    if (threadIdx.x < kSoftmaxThreads) {
+      ptx::st_shared_volatile(smem + C::kOffMx + threadIdx.x * 4u, 1u);
+      ptx::st_shared_volatile(smem + C::kOffMx + (kSoftmaxThreads + threadIdx.x) * 4u, 1u);
+    }
   }
   ptx::tc_fence_before();
   __syncthreads();
