@@ -809,47 +809,30 @@ __device__ __forceinline__ float exp_half(const uint32_t (&s)[BH], uint64_t sc2,
 }
 
 // Shared O (D = 128): the two halves of a row agree on one running max at
-// every step.  Each thread publishes its half row's maximum in a shared-memory
-// word per (step parity, half, row) and reads its partner's (the other half,
-// same row).  The word's lowest bit carries bit 1 of the exchange count: a
-// slot holds either this exchange's value or the one two exchanges back (a
-// partner cannot get further ahead, since it needs this thread's next value
-// to pass its next exchange), and the two differ in that bit; the slots start
-// with the bit set, which no exchange 0 or 1 writes.  The value itself is the
-// maximum with its two lowest mantissa bits cleared (at most 3 ulp below it),
-// whatever the count: both halves take the maximum of the same two values, so
-// they agree bit for bit, and the result does not depend on how many
-// exchanges came before (the schedule of units over CTAs).  The lowered max
-// only shifts the offset of the exponentials, exact after the final division.
-// A half with no visible key publishes -FLT_MAX, read back as -inf.  The wait
-// for the partner is bounded like every other wait.
+// every step.  Each thread writes its half row's maximum into a shared-memory
+// word per (step parity, half, row); the two warps of a TMEM lane quadrant
+// (warp q and q + 4) meet at named barrier kXBar0 + q, and each reads its
+// partner's word.  Two parities: a word is rewritten two exchanges later, by
+// when the partner has passed the exchange in between (so it has read it).
+// Both halves take fmaxf of the same two values, so they agree bit for bit.
+// A named-barrier wait has no time limit, so a warp that leaves the softmax
+// early (a bounded wait elsewhere gave up, which raises the CTA's abort flag)
+// arrives once more at its quadrant's barrier on the way out: that releases
+// the one exchange its partner can be waiting in or reach next, and the
+// partner, reading the abort flag right after every exchange, leaves too.
+constexpr uint32_t kXBar0 = 1;  // named barriers 1-4 (0 is __syncthreads)
+
 template <class BarsT>
-__device__ __forceinline__ bool exchange_max(const BarsT& br, int* status, uint32_t mine0,
-                                             uint32_t other0, uint32_t& xs, float& mx) {
+__device__ __forceinline__ bool exchange_max(const BarsT& br, uint32_t mine0, uint32_t other0,
+                                             uint32_t quad, uint32_t& xs, float& mx) {
   const uint32_t off = (xs & 1u) * (2u * BM * 4u);
-  const uint32_t tag = (xs >> 1) & 1u;
   ++xs;
-  const uint32_t v = ((mx == -INFINITY) ? 0xFF7FFFFFu : __float_as_uint(mx)) & ~3u;
-  const uint32_t w = v | tag;
-  ptx::st_shared_volatile(mine0 + off, w);
-  uint32_t o = ptx::ld_shared_volatile(other0 + off);
-  if ((o & 1u) != tag) {
-    const uint64_t t0 = ptx::globaltimer_ns();
-    for (;;) {
-#pragma unroll 1
-      for (int i = 0; i < 16 && (o & 1u) != tag; ++i) o = ptx::ld_shared_volatile(other0 + off);
-      if ((o & 1u) == tag) break;
-      if (ptx::ld_shared_volatile(br.abort_word()) != 0u) return false;
-      if (ptx::globaltimer_ns() - t0 > ATTN_WAIT_LIMIT_NS) {
-        ptx::st_shared_volatile(br.abort_word(), 1u);
-        atomicOr(status, kStatusTimeout | kRoleSoftmax);
-        return false;
-      }
-    }
-  }
-  const float r = fmaxf(__uint_as_float(v), __uint_as_float(o & ~3u));
-  mx = (r < -1.0e38f) ? -INFINITY : r;
-  return true;
+  ptx::st_shared_f32(mine0 + off, mx);
+  ptx::named_barrier_sync(kXBar0 + quad, 64);
+  const float partner = ptx::ld_shared_f32(other0 + off);
+  const bool abort = ptx::ld_shared_volatile(br.abort_word()) != 0u;
+  mx = fmaxf(mx, partner);
+  return !abort;
 }
 
 // Two softmax warpgroups share every query tile: warps 0-3 (half a) own key
@@ -864,7 +847,7 @@ __device__ __forceinline__ bool exchange_max(const BarsT& br, int* status, uint3
 // At D = 128 (shared O) the halves exchange their maxima every step, so
 // m_a = m_b and the same formulas reduce to O / (l_a + l_b).
 template <int D, bool BF16, bool MASK>
-__device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t smem, uint32_t tmem) {
+__device__ bool softmax_role(const KParams& p, const Bars<D>& br, uint32_t smem, uint32_t tmem) {
   using C = Cfg<D>;
   constexpr int SB = C::kScoreBufs;
   const int lane_row = threadIdx.x & 127;           // row within the tile = TMEM lane
@@ -897,7 +880,7 @@ __device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t smem,
     const uint32_t slot = static_cast<uint32_t>(r) % kUnitSlots;
     if (!__all_sync(0xffffffffu, wait_bar(br, p.status, br.unit_full(slot),
                                           (static_cast<uint32_t>(r) / kUnitSlots) & 1u, kRoleSoftmax)))
-      return;
+      return false;
     uint32_t fmask;
     const Unit w = read_unit(smem + C::kOffRing + slot * (kUnitWords * 4), &fmask);
     ptx::mbar_arrive(br.unit_empty(slot));
@@ -998,7 +981,7 @@ __device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t smem,
       }
       // shared O: the row's max over both halves (the same value in both)
       if constexpr (C::kSharedO) {
-        if (!__all_sync(0xffffffffu, exchange_max(br, p.status, mx_mine, mx_other, xs, mx))) {
+        if (!__all_sync(0xffffffffu, exchange_max(br, mx_mine, mx_other, quad, xs, mx))) {
           ok = false;
           break;
         }
@@ -1057,20 +1040,21 @@ __device__ void softmax_role(const KParams& p, const Bars<D>& br, uint32_t smem,
       ptx::mbar_arrive(br.p_full(b));
     }
     g += cnt;
-    if (!ok) return;
+    if (!ok) return false;
     // Hand this half's row statistics to the epilogue warpgroup, which
     // combines the halves and writes O and the LSE once the unit's last P.V
     // has completed; meanwhile this warp goes on with the next unit.  The
     // slot is free once the epilogue has read the previous unit's values.
     if (epi > 0) {
       ok = wait_bar(br, p.status, br.ml_empty(), (epi - 1u) & 1u, kRoleSoftmax);
-      if (!__all_sync(0xffffffffu, ok)) return;
+      if (!__all_sync(0xffffffffu, ok)) return false;
     }
     ptx::st_shared_f32(xch, m);
     ptx::st_shared_f32(xch + 4u, l);
     ptx::mbar_arrive(br.ml_full());
     ++epi;
   }
+  return true;
 }
 
 // ------------------------------------------------------------------ epilogue
@@ -1271,13 +1255,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tmem_alloc(br.tmem_word(), C::kTmemCols);
     ptx::tmem_relinquish();
   }
-  if constexpr (C::kSharedO) {
-    // max-exchange slots: both parities start with the tag bit set
-    if (threadIdx.x < kSoftmaxThreads) {
-      ptx::st_shared_volatile(smem + C::kOffMx + threadIdx.x * 4u, 1u);
-      ptx::st_shared_volatile(smem + C::kOffMx + (kSoftmaxThreads + threadIdx.x) * 4u, 1u);
-    }
-  }
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
@@ -1301,7 +1278,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
-    softmax_role<D, BF16, MASK>(p, br, smem, tmem);  // warps 0-7
+    const bool done = softmax_role<D, BF16, MASK>(p, br, smem, tmem);  // warps 0-7
+    // shared O: a half that left early releases its partner's next exchange
+    if constexpr (C::kSharedO)
+      if (!done) ptx::named_barrier_arrive(kXBar0 + ((threadIdx.x >> 5) & 3u), 64);
   }
 
   ptx::tc_fence_before();

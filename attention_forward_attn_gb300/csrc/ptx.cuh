@@ -119,6 +119,11 @@ __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t count) 
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// Arrive at named barrier `id` (of `count` threads) without waiting.
+__device__ __forceinline__ void named_barrier_arrive(uint32_t id, uint32_t count) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // ------------------------------------------------------------------ TMA
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
