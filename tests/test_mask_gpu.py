@@ -12,6 +12,9 @@ causal and padding masks.
   implicit masks, also at full size (C3, C4).
 * A full-size block-sparse mask on the C4 shapes, compared with the oracle on
   sampled rows (tile-boundary rows of every head group).
+* At D = 128 (one accumulator shared by the two halves of each key tile):
+  rows that keep one half of every tile only, with the running max growing
+  through one half.
 """
 import math
 import zlib
@@ -100,6 +103,34 @@ def test_masks_full_compare(kind, D, dtype, causal):
 
 def _same(a, b):
     return torch.equal(a.contiguous().view(torch.int16), b.contiguous().view(torch.int16))
+
+
+@pytest.mark.parametrize("dtype", [wl.BF16, wl.F16])
+@pytest.mark.parametrize("causal", [False, True])
+def test_half_tile_masks_and_one_sided_max_growth(dtype, causal):
+    """D = 128, where the two softmax halves of a row (keys 0-63 and 64-127
+    of every 128-key tile) share one accumulator and agree on the running max
+    every step: rows that keep only the first half of every tile, only the
+    second, or both, with the scores of the second halves growing along the
+    keys (Q x 4, K rows of the second halves scaled by up to 3), so that the
+    running max moves, by more than the lazy-rescale threshold, through one
+    half only."""
+    B, Hq, Hkv, L, D = 2, 2, 1, 520, 128
+    q, k, v, _ = wl.make_inputs(B, Hq, Hkv, L, D, dtype, seed=44 + causal, q_scale=4.0)
+    j = torch.arange(L)
+    ramp = torch.where(j % 128 >= 64, 1.0 + 2.0 * j.float() / L, torch.ones(L))
+    k = (k.float() * ramp[None, None, :, None]).to(k.dtype)
+    i = np.arange(L)[:, None]
+    jj = np.arange(L)[None, :]
+    first = (jj % 128) < 64
+    mk = np.where(i % 3 == 0, first, np.where(i % 3 == 1, ~first, True))
+    mk = np.broadcast_to(mk, (B, L, L)).astype(np.uint8)
+    sm = 1.0 / math.sqrt(D)
+    o, lse = run(q, k, v, causal, None, sm, mk)
+    o_ref, lse_ref = oracle.attn_fwd_bits(wl.bits(q), wl.bits(k), wl.bits(v), wl.dtype_code(dtype),
+                                          sm, causal=causal, mask=mk)
+    check(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref,
+          "half-tile masks causal=%s" % causal)
 
 
 @pytest.mark.parametrize("name", ["C2", "C3", "C4"])
