@@ -124,7 +124,7 @@ def test_half_tile_masks_and_one_sided_max_growth(dtype, causal):
     jj = np.arange(L)[None, :]
     first = (jj % 128) < 64
     mk = np.where(i % 3 == 0, first, np.where(i % 3 == 1, ~first, True))
-    mk = np.broadcast_to(mk, (B, L, L)).astype(np.uint8)
+    mk = np.ascontiguousarray(np.broadcast_to(mk, (B, L, L))).astype(np.uint8)
     sm = 1.0 / math.sqrt(D)
     o, lse = run(q, k, v, causal, None, sm, mk)
     o_ref, lse_ref = oracle.attn_fwd_bits(wl.bits(q), wl.bits(k), wl.bits(v), wl.dtype_code(dtype),
