@@ -623,7 +623,7 @@ def run_gpu(args, w, world, rank, local):
         def call_y():
             y.call(attn, stream)
 
-        for _ in range(3):
+        for _ in range(10):  # warm-up calls
             flush.zero_()
             call_y()
         ms = time_calls(call_y, args.workload_calls, flush, stream)
@@ -645,7 +645,8 @@ def run_gpu(args, w, world, rank, local):
         torch.cuda.empty_cache()
     line["workloads"] = recs
     line["workloads_note"] = (
-        "per workload: %d calls (the headline: the timed steps' calls), L2 flushed before each, "
+        "per workload: 10 warm-up and %d timed calls (the headline: the timed steps' calls), L2 "
+        "flushed before each, "
         "CUDA events; fractions of the %s peaks (bf16_tflops burst, hbm_gbs) from algorithmic "
         "FLOPs and the minimum bytes Q+K+V+O+LSE; parity: the whole output against the float64 "
         "oracle run over the whole workload on %d host cores (cpu_oracle_s)" % (
@@ -1003,7 +1004,7 @@ def main(argv=None):
                     help="attn_fwd calls per timed step (0: enough for --step-ms)")
     ap.add_argument("--step-ms", type=float, default=120.0,
                     help="device time a timed step aims at when --calls-per-step is 0")
-    ap.add_argument("--workload-calls", type=int, default=30,
+    ap.add_argument("--workload-calls", type=int, default=50,
                     help="timed calls per workload of the per-workload record")
     ap.add_argument("--mask-workloads", action="store_true",
                     help="instead of the headline line, one line per explicit-mask workload")
