@@ -81,6 +81,15 @@ def test_small_shapes_full_compare(simt, D, dtype, causal):
     full_case(2, 4, 2, 700, D, dtype, causal, seed=100 + D, simt=simt)
 
 
+@pytest.mark.parametrize("D, dtype", [(128, wl.BF16), (64, wl.F16)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_long_ragged_sequences(D, dtype, causal):
+    # 3001 rows and keys: 24 key tiles, the last one key long; MQA, padding
+    # that ends inside the second half of a key tile in one batch and on a
+    # half-tile boundary in the other (every row compared)
+    full_case(2, 4, 1, 3001, D, dtype, causal, seed=3001 + D, valid_len=[2900, 2880])
+
+
 @pytest.mark.parametrize("simt", KERNELS)
 @pytest.mark.parametrize("L", [1, 2, 64, 127, 128, 129, 255, 256, 257, 383, 513])
 def test_sequence_lengths(simt, L):
