@@ -525,12 +525,13 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t q_desc, uint6
 }
 
 // O_h += P_h V_h for the two halves of a key tile (h = a: keys 0-63 into
-// O_a, h = b: keys 64-127 into O_b; with a shared O both into it).  A = P_h from TMEM (16-bit pairs, 8
-// columns per 16 keys, at the start of its half's 64 score columns), B = the
-// half's rows of the V tile as an MN-major 128-byte-swizzled operand (16 keys
-// = two 8-row groups).  fp16 V tile (fp16 inputs, or the exact fp16 copy of
-// a bf16 tile): fp16 P.  bf16 V tile (split): O_h += [P_hi | P_lo] [V_h; V_h]
-// with P_lo in the 32 columns after P_hi, the same V rows read twice.
+// O_a, h = b: keys 64-127 into O_b; with a shared O both into it).  A = P_h
+// from TMEM (16-bit pairs, 8 columns per 16 keys, at the start of its half's
+// 64 score columns), B = the half's rows of the V tile as an MN-major
+// 128-byte-swizzled operand (16 keys = two 8-row groups).  fp16 V tile (fp16
+// inputs, or the exact fp16 copy of a bf16 tile): fp16 P.  bf16 V tile
+// (split): O_h += [P_hi | P_lo] [V_h; V_h] with P_lo in the 32 columns after
+// P_hi, the same V rows read twice.
 template <int D>
 __device__ __forceinline__ void issue_pv(uint32_t o_a, uint32_t o_b, uint32_t p_tmem,
                                          uint64_t v_desc, bool accumulate, bool split) {
@@ -814,7 +815,8 @@ __device__ __forceinline__ float exp_half(const uint32_t (&s)[BH], uint64_t sc2,
 // (warp q and q + 4) meet at named barrier kXBar0 + q, and each reads its
 // partner's word.  Two parities: a word is rewritten two exchanges later, by
 // when the partner has passed the exchange in between (so it has read it).
-// Both halves take fmaxf of the same two values, so they agree bit for bit.
+// Both halves take fmaxf of the same two values, so they agree (up to the
+// sign of a zero maximum, which changes no exponential and no result).
 // A named-barrier wait has no time limit, so a warp that leaves the softmax
 // early (a bounded wait elsewhere gave up, which raises the CTA's abort flag)
 // arrives once more at its quadrant's barrier on the way out: that releases
