@@ -837,6 +837,42 @@ __device__ __forceinline__ bool exchange_max(const BarsT& br, uint32_t mine0, ui
   return !abort;
 }
 
+// O_h *= alpha over ncols columns of this thread's TMEM row, once PV(j-1)
+// (barrier `bar`, phase `parity`) has completed -- the rare rescale of the
+// softmax step, kept out of line so that the step's hot code stays compact.
+// The wait is bounded like wait_bar's; false: it gave up (recorded) or the
+// CTA is aborting.
+__device__ __noinline__ bool rescale_o(uint32_t bar, uint32_t parity, uint32_t abort_word,
+                                       int* status, uint32_t t_oh, int ncols, float alpha) {
+  bool done = ptx::mbar_try_wait(bar, parity);
+  if (!done) {
+    const uint64_t t0 = ptx::globaltimer_ns();
+    for (;;) {
+      if (ptx::mbar_try_wait(bar, parity)) {
+        done = true;
+        break;
+      }
+      if (ptx::ld_shared_volatile(abort_word) != 0u) break;
+      if (ptx::globaltimer_ns() - t0 > ATTN_WAIT_LIMIT_NS) {
+        ptx::st_shared_volatile(abort_word, 1u);
+        atomicOr(status, kStatusTimeout | kRoleSoftmax);
+        break;
+      }
+    }
+  }
+  if (!__all_sync(0xffffffffu, done)) return false;
+  ptx::tc_fence_after();
+#pragma unroll 1
+  for (int c0 = 0; c0 < ncols; c0 += 32) {
+    uint32_t o[32];
+    ptx::tmem_ld32(t_oh + c0, o);
+#pragma unroll
+    for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+    ptx::tmem_st32(t_oh + c0, o);
+  }
+  return true;
+}
+
 // Two softmax warpgroups share every query tile: warps 0-3 (half a) own key
 // columns 0-63 of each key tile and warps 4-7 (half b) columns 64-127, for
 // the same rows (warp w and w + 4 read the same TMEM lane quadrant).  At
@@ -902,144 +938,173 @@ __device__ bool softmax_role(const KParams& p, const Bars<D>& br, uint32_t smem,
     uint32_t cnt = 0;   // key tiles of this unit visited so far
     TileWalk<MASK> tw;
     tw.init(p, w);
-    for (int j = tw.next(0, w.last); j <= w.last; j = tw.next(j + 1, w.last), ++cnt) {
-      const uint32_t gg = g + cnt;
-      const uint32_t b = gg % SB;
-      const uint32_t t_s = tmem + lane_addr + C::col_s(b) + static_cast<uint32_t>(half * BH);
-      // P format of this key tile: fp16 P, or the bf16 pair (split)
-      if ((j >> 5) != fchunk) {
-        fchunk = j >> 5;
-        fmask = v_fp16_mask<BF16>(p, z_kv, j & ~31, w.n);
-      }
-      const bool split = BF16 && ((fmask >> (j & 31)) & 1u) == 0u;
-      // explicit mask: this row's 64 bits of the half tile when the tile is
-      // partial (loaded before the wait, to hide its latency)
-      const bool partial = tw.partial(j);
-      uint2 keep = make_uint2(0xFFFFFFFFu, 0xFFFFFFFFu);
-      if constexpr (MASK) {
-        if (partial && row_ok) {
-          const int64_t mrow = static_cast<int64_t>(p.mask_shared ? 0 : w.b) * p.Lq + row;
-          keep = __ldg(reinterpret_cast<const uint2*>(p.mbits + (mrow * p.n_kt + j) * 4 + half * 2));
+    // D = 64 without an explicit mask: the key tiles below j_plain are
+    // visible to every row of the unit in both halves (the causal and padding
+    // limits of the unit's first row lie beyond them), so they run in a first
+    // pass whose copy of the step has no masking code at all (C2 +2.4 %, C3
+    // +5.5 % against one loop carrying it); the rest -- the diagonal and the
+    // padding edge -- in a second pass with it.  D = 128 (measured no faster)
+    // and explicit masks: one pass.
+    constexpr bool kSplit = !MASK && !C::kSharedO;
+    const int j_plain = kSplit ? (p.causal ? min(w.kv_len, w.m0 + 1) : w.kv_len) / BN : 0;
+    int j = tw.next(0, w.last);
+#pragma unroll
+    for (int pass = 0; pass < 2; ++pass) {
+      const bool plain = kSplit && pass == 0;  // compile-time in each unrolled copy
+      if (!kSplit && pass == 0) continue;
+      const int j_end = plain ? min(j_plain, w.last + 1) : w.last + 1;
+      for (; j < j_end; j = tw.next(j + 1, w.last), ++cnt) {
+        const uint32_t gg = g + cnt;
+        const uint32_t b = gg % SB;
+        const uint32_t t_s = tmem + lane_addr + C::col_s(b) + static_cast<uint32_t>(half * BH);
+        // P format of this key tile: fp16 P, or the bf16 pair (split)
+        if ((j >> 5) != fchunk) {
+          fchunk = j >> 5;
+          fmask = v_fp16_mask<BF16>(p, z_kv, j & ~31, w.n);
         }
-      }
-      if (!s_ready) {
-        ok = wait_bar(br, p.status, br.s_full(b), (gg / SB) & 1u, kRoleSoftmax);
-        if (!__all_sync(0xffffffffu, ok)) {
-          ok = false;
-          break;
-        }
-      }
-      ptx::tc_fence_after();
-      // the half row's scores with their maximum, reduced by the load itself
-      uint32_t s[BH];
-      float mx = ptx::tmem_ld64_max(t_s, s);
-      const int n0 = j * BN + half * BH;  // key of column 0 of this half
-      const bool masked = partial || (n0 + BH > w.kv_len) || (p.causal && n0 + BH - 1 > w.m0);
-      const int c_lim = key_lim - n0;  // columns c < c_lim are visible
-      // Boundary and partially masked tiles only: invisible scores become
-      // -inf and the maximum is taken again over what is left, so the
-      // exponentials below are the same code for every tile (one copy of the
-      // unrolled loop keeps the hot code small); exp2(-inf * scale - m) = 0
-      // because the scale is > 0 (a zero sm_scale arrives as FLT_MIN).
-      if (masked) {
+        const bool split = BF16 && ((fmask >> (j & 31)) & 1u) == 0u;
+        // explicit mask: this row's 64 bits of the half tile when the tile is
+        // partial (loaded before the wait, to hide its latency)
+        const bool partial = tw.partial(j);
+        uint2 keep = make_uint2(0xFFFFFFFFu, 0xFFFFFFFFu);
         if constexpr (MASK) {
-          // columns >= c_lim leave the keep bits first; then per column one
-          // prmt replicates its bit (moved to a byte's sign) over a word and
-          // one logic op selects the score or -inf: about the cost of the
-          // implicit masks' compare-and-select (a per-column bit test
-          // measured ~30 % slower on every step, partial or not)
-          uint32_t kw[2] = {keep.x, keep.y};
-#pragma unroll
-          for (int wd = 0; wd < 2; ++wd) {
-            const int n = c_lim - 32 * wd;  // columns of this word below c_lim
-            kw[wd] &= n >= 32 ? 0xFFFFFFFFu : (n <= 0 ? 0u : (1u << n) - 1u);
+          if (partial && row_ok) {
+            const int64_t mrow = static_cast<int64_t>(p.mask_shared ? 0 : w.b) * p.Lq + row;
+            keep = __ldg(reinterpret_cast<const uint2*>(p.mbits + (mrow * p.n_kt + j) * 4 + half * 2));
           }
-#pragma unroll
-          for (int wd = 0; wd < 2; ++wd) {
-#pragma unroll
-            for (int c0 = 0; c0 < 8; ++c0) {
-              const uint32_t t = kw[wd] << (7 - c0);  // bit c0 + 8k -> sign of byte k
-#pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                const uint32_t m = ptx::prmt(t, 0u, 0x8888u + 0x1111u * k);
-                const int c = 32 * wd + 8 * k + c0;
-                s[c] = (s[c] & m) | (0xFF800000u & ~m);
-              }
-            }
+        }
+        if (!s_ready) {
+          ok = wait_bar(br, p.status, br.s_full(b), (gg / SB) & 1u, kRoleSoftmax);
+          if (!__all_sync(0xffffffffu, ok)) {
+            ok = false;
+            break;
           }
-        } else {
-#pragma unroll
-          for (int c = 0; c < BH; ++c) s[c] = (c < c_lim) ? s[c] : 0xFF800000u;
-        }
-        // max of the visible scores: 8 independent chains of 3-input maxima
-        float mxk[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) mxk[k] = -INFINITY;
-#pragma unroll
-        for (int i = 0; i < BH / 2; ++i)
-          mxk[i & 7] = ptx::max3(mxk[i & 7], __uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1]));
-        mx = ptx::max3(ptx::max3(mxk[0], mxk[1], mxk[2]), ptx::max3(mxk[3], mxk[4], mxk[5]),
-                       fmaxf(mxk[6], mxk[7]));
-      }
-      // shared O: the row's max over both halves (the same value in both)
-      if constexpr (C::kSharedO) {
-        if (!__all_sync(0xffffffffu, exchange_max(br, mx_mine, mx_other, quad, xs, mx))) {
-          ok = false;
-          break;
-        }
-      }
-      const float m_tile = (mx == -INFINITY) ? -INFINITY : mx * scale_log2;
-      const float m_new = fmaxf(m, m_tile);
-      float alpha = 1.f;
-      bool rescale = false;
-      if (m_new > m + kRescaleLog2) {  // also taken on the first visible key (m = -inf)
-        alpha = ptx::ex2_approx(m - m_new);
-        m = m_new;
-        rescale = true;
-      }
-      const float neg_m = (m == -INFINITY) ? 0.f : -m;
-      // look ahead (non-blocking): has S(gg+1) completed?  Its answer is used
-      // at the next step, so the test's latency hides behind the exponentials.
-      // S(gg+1) may be the next unit's first tile: g counts every tile.  With
-      // three score buffers the scores are normally ready (with two, at
-      // D = 128 before the shared O, it measured slower).
-      if constexpr (SB > 2)
-        s_ready = __all_sync(0xffffffffu, ptx::mbar_test_wait(br.s_full((gg + 1u) % SB), ((gg + 1u) / SB) & 1u));
-      const uint64_t sc2 = ptx::f2_pack(scale_log2, scale_log2);
-      const uint64_t nm2 = ptx::f2_pack(neg_m, neg_m);
-      // P over the half's S columns (every S value is already in registers)
-      float rowsum;
-      if (!split) {
-        rowsum = exp_half<false>(s, sc2, nm2, t_s);
-      } else if constexpr (BF16) {
-        rowsum = exp_half<true>(s, sc2, nm2, t_s);
-      } else {
-        rowsum = 0.f;
-      }
-      l = l * alpha + rowsum;
-      // O_h was accumulated against the old max: rescale it before PV(j)
-      // runs.  PV(j-SB) and earlier are complete (S(j) was issued after
-      // PV(j-SB) completed); PV(j-1) may still be running: wait for it (the
-      // tensor core completes them in order).
-      if (cnt > 0 && __any_sync(0xffffffffu, rescale)) {
-        ok = wait_bar(br, p.status, br.pv_done((gg - 1u) % SB), ((gg - 1u) / SB) & 1u, kRoleSoftmax);
-        if (!__all_sync(0xffffffffu, ok)) {
-          ok = false;
-          break;
         }
         ptx::tc_fence_after();
-#pragma unroll 1
-        for (int c0 = 0; c0 < kOCols; c0 += 32) {
-          uint32_t o[32];
-          ptx::tmem_ld32(t_oh + c0, o);
-#pragma unroll
-          for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-          ptx::tmem_st32(t_oh + c0, o);
+        // the half row's scores with their maximum, reduced by the load itself
+        uint32_t s[BH];
+        float mx = ptx::tmem_ld64_max(t_s, s);
+        const int n0 = j * BN + half * BH;  // key of column 0 of this half
+        const bool masked =
+            !plain && (partial || (n0 + BH > w.kv_len) || (p.causal && n0 + BH - 1 > w.m0));
+        const int c_lim = key_lim - n0;  // columns c < c_lim are visible
+        // Boundary and partially masked tiles only: invisible scores become
+        // -inf and the maximum is taken again over what is left, so the
+        // exponentials below are the same code for every tile (one copy of the
+        // unrolled loop keeps the hot code small); exp2(-inf * scale - m) = 0
+        // because the scale is > 0 (a zero sm_scale arrives as FLT_MIN).
+        if (masked) {
+          if constexpr (MASK) {
+            // columns >= c_lim leave the keep bits first; then per column one
+            // prmt replicates its bit (moved to a byte's sign) over a word and
+            // one logic op selects the score or -inf: about the cost of the
+            // implicit masks' compare-and-select (a per-column bit test
+            // measured ~30 % slower on every step, partial or not)
+            uint32_t kw[2] = {keep.x, keep.y};
+  #pragma unroll
+            for (int wd = 0; wd < 2; ++wd) {
+              const int n = c_lim - 32 * wd;  // columns of this word below c_lim
+              kw[wd] &= n >= 32 ? 0xFFFFFFFFu : (n <= 0 ? 0u : (1u << n) - 1u);
+            }
+  #pragma unroll
+            for (int wd = 0; wd < 2; ++wd) {
+  #pragma unroll
+              for (int c0 = 0; c0 < 8; ++c0) {
+                const uint32_t t = kw[wd] << (7 - c0);  // bit c0 + 8k -> sign of byte k
+  #pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                  const uint32_t m = ptx::prmt(t, 0u, 0x8888u + 0x1111u * k);
+                  const int c = 32 * wd + 8 * k + c0;
+                  s[c] = (s[c] & m) | (0xFF800000u & ~m);
+                }
+              }
+            }
+          } else {
+  #pragma unroll
+            for (int c = 0; c < BH; ++c) s[c] = (c < c_lim) ? s[c] : 0xFF800000u;
+          }
+          // max of the visible scores: 8 independent chains of 3-input maxima
+          float mxk[8];
+  #pragma unroll
+          for (int k = 0; k < 8; ++k) mxk[k] = -INFINITY;
+  #pragma unroll
+          for (int i = 0; i < BH / 2; ++i)
+            mxk[i & 7] = ptx::max3(mxk[i & 7], __uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1]));
+          mx = ptx::max3(ptx::max3(mxk[0], mxk[1], mxk[2]), ptx::max3(mxk[3], mxk[4], mxk[5]),
+                         fmaxf(mxk[6], mxk[7]));
         }
+        // shared O: the row's max over both halves (the same value in both)
+        if constexpr (C::kSharedO) {
+          if (!__all_sync(0xffffffffu, exchange_max(br, mx_mine, mx_other, quad, xs, mx))) {
+            ok = false;
+            break;
+          }
+        }
+        const float m_tile = (mx == -INFINITY) ? -INFINITY : mx * scale_log2;
+        const float m_new = fmaxf(m, m_tile);
+        float alpha = 1.f;
+        bool rescale = false;
+        if (m_new > m + kRescaleLog2) {  // also taken on the first visible key (m = -inf)
+          alpha = ptx::ex2_approx(m - m_new);
+          m = m_new;
+          rescale = true;
+        }
+        const float neg_m = (m == -INFINITY) ? 0.f : -m;
+        // look ahead (non-blocking): has S(gg+1) completed?  Its answer is used
+        // at the next step, so the test's latency hides behind the exponentials.
+        // S(gg+1) may be the next unit's first tile: g counts every tile.  With
+        // three score buffers the scores are normally ready (with two, at
+        // D = 128 before the shared O, it measured slower).
+        if constexpr (SB > 2)
+          s_ready = __all_sync(0xffffffffu, ptx::mbar_test_wait(br.s_full((gg + 1u) % SB), ((gg + 1u) / SB) & 1u));
+        const uint64_t sc2 = ptx::f2_pack(scale_log2, scale_log2);
+        const uint64_t nm2 = ptx::f2_pack(neg_m, neg_m);
+        // P over the half's S columns (every S value is already in registers)
+        float rowsum;
+        if (!split) {
+          rowsum = exp_half<false>(s, sc2, nm2, t_s);
+        } else if constexpr (BF16) {
+          rowsum = exp_half<true>(s, sc2, nm2, t_s);
+        } else {
+          rowsum = 0.f;
+        }
+        l = l * alpha + rowsum;
+        // O_h was accumulated against the old max: rescale it before PV(j)
+        // runs.  PV(j-SB) and earlier are complete (S(j) was issued after
+        // PV(j-SB) completed); PV(j-1) may still be running: wait for it (the
+        // tensor core completes them in order).
+        if (cnt > 0 && __any_sync(0xffffffffu, rescale)) {
+          const uint32_t done_bar = br.pv_done((gg - 1u) % SB);
+          const uint32_t done_par = ((gg - 1u) / SB) & 1u;
+          if constexpr (!C::kSharedO) {
+            // D = 64: out of line (C2 +2.4 %, C3 +1 %); at D = 128 that measured
+            // slower where rescales are frequent (C5, Q x 4)
+            if (!rescale_o(done_bar, done_par, br.abort_word(), p.status, t_oh, kOCols, alpha)) {
+              ok = false;
+              break;
+            }
+          } else {
+            ok = wait_bar(br, p.status, done_bar, done_par, kRoleSoftmax);
+            if (!__all_sync(0xffffffffu, ok)) {
+              ok = false;
+              break;
+            }
+            ptx::tc_fence_after();
+  #pragma unroll 1
+            for (int c0 = 0; c0 < kOCols; c0 += 32) {
+              uint32_t o[32];
+              ptx::tmem_ld32(t_oh + c0, o);
+  #pragma unroll
+              for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+              ptx::tmem_st32(t_oh + c0, o);
+            }
+          }
+        }
+        ptx::tmem_st_wait();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(br.p_full(b));
       }
-      ptx::tmem_st_wait();
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(br.p_full(b));
+      if (!ok) break;
     }
     g += cnt;
     if (!ok) return false;
